@@ -1,0 +1,552 @@
+"""Plain CPU oracle of the RDKV hot path (weights, allocation, TriZone pack, decode).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py``; never by the library.  It shares no code with
+the CUDA sources.
+
+Sources (the pages are summaries; every step they leave open follows the
+project's written reading, listed at the end of this header):
+
+* "RDKV - rate-distortion bit allocation for joint KV eviction and
+  quantisation" (gist.science/ko/paper/2605.08317):
+  section 2.1 (token weight w_t, channel weight w_c, the objective),
+  section 2.2 (discrete reverse water-filling over {0,2,4,8,16}; steps 1-3),
+  section 2.3 (TriZone layout: zone A packed 2/4/8-bit rows grouped by width,
+  zone B fp16 V rows of 16-bit tokens, zone C fp16 rows of new tokens).
+* "Matematika KV Cache Compression" (aistudio.id), section "Anatomi Krisis"
+  (the KV-size formula 2*L*H_kv*D*P*N) and section "Solusi 3" (asymmetric
+  min-max quantiser).
+
+Arithmetic: weights, spreads and attention in float64; breakpoints, gains and
+the quantiser in IEEE float32 / float16 exactly as the encoding fixes them, so
+that the packed bytes and the bit allocation are reproducible bit for bit.
+
+Parity pins (tests/test_oracle_pins.py): every function below is pinned by a
+closed form, an invariant, a library special case or brute force; none is
+"parity unpinned".  The end-to-end accuracy of the method on real tasks is not
+an oracle function and is out of scope (it needs datasets and trained models).
+
+Readings where the pages are silent (each is a project decision):
+ R1 GQA: w_t of KV head j sums over the G query heads of its group.
+ R2 The last W prompt tokens (the window) go to zone C in fp16 and are not
+    allocated; the allocatable prefix is tokens [0, N-W).
+ R3 sigma_u (undefined on the page) = population standard deviation of the
+    unit's values: a V row over its D elements; a K channel over the kept
+    prefix tokens.  The printed linear form g_u * 2**-b_u is kept.
+ R4 One water level per sequence, pooled over KV heads; budget
+    B = floor(avg_bits * units); slack left unused.
+ R5 At a breakpoint the cheaper width wins (strict >); g = 0 gives 0 bits.
+ R6 Quantiser groups: 32 consecutive channels of a V row; for K, one channel
+    over the real tokens of a 32-token tile.  fp16 scale and zero.
+ R7 16-bit K channels are stored raw in fp16 inside zone A; 0-bit K channels
+    are dropped and contribute nothing to the logits.
+ R8 Byte layout of the zones: see ``pack``.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+WIDTHS = np.array([0, 2, 4, 8, 16], dtype=np.uint8)
+STEP_BITS = np.diff(WIDTHS.astype(np.int64))            # bits gained by each upgrade: 2, 2, 4, 8
+V_CLASSES = (2, 4, 8, 16)                                # zone order of kept tokens
+K_CLASSES = (16, 8, 4, 2)                                # slot order of kept channels
+TILE = 32                                                # tokens per zone-A tile
+GROUP = 32                                               # channels per V quantiser group
+
+
+# ---------------------------------------------------------------------------
+# KV-size formula (aistudio.id, "Anatomi Krisis")
+# ---------------------------------------------------------------------------
+def kv_cache_bytes(n_layers, h_kv, head_dim, bytes_per_elem, n_tokens):
+    """Bytes of a full K+V cache: 2 * L * H_kv * D * P * N."""
+    return 2 * n_layers * h_kv * head_dim * bytes_per_elem * n_tokens
+
+
+# ---------------------------------------------------------------------------
+# Step 1: distortion weights (RDKV section 2.1; computed once after prefill,
+# section 2.2 step 1)
+# ---------------------------------------------------------------------------
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _masked_logits(q_rows, k_all, first_row, head_dim):
+    """Causal logits q_tau . k_t / sqrt(D) for rows tau = first_row.., -inf where t > tau."""
+    s = q_rows @ k_all.T / math.sqrt(head_dim)
+    taus = np.arange(first_row, first_row + q_rows.shape[0])[:, None]
+    s[np.arange(k_all.shape[0])[None, :] > taus] = -np.inf
+    return s
+
+
+def token_weights(q, k, first_row=0, row_block=512):
+    """V-token weight w_t = sum over query positions tau (and the G heads of the
+    group, R1) of the softmax attention a_{tau,t}.
+
+    q [N, H_q, D], k [N, H_kv, D] -> w [H_kv, N] float64.  Only query rows
+    tau >= first_row contribute, which is exact for every t >= first_row
+    (a_{tau,t} = 0 for tau < t).
+    """
+    q64, k64 = _f64(q), _f64(k)
+    N, Hq, D = q64.shape
+    Hkv = k64.shape[1]
+    G = Hq // Hkv
+    w = np.zeros((Hkv, N))
+    for h in range(Hq):
+        j = h // G
+        for r0 in range(first_row, N, row_block):
+            r1 = min(N, r0 + row_block)
+            s = _masked_logits(q64[r0:r1, h, :], k64[:, j, :], r0, D)
+            a = np.exp(s - s.max(axis=1, keepdims=True))
+            a /= a.sum(axis=1, keepdims=True)
+            w[j] += a.sum(axis=0)
+    return w
+
+
+def row_lse(q, k, h, rows):
+    """log sum_{t <= tau} exp(q_tau,h . k_t / sqrt(D)) for the listed query rows."""
+    q64, k64 = _f64(q), _f64(k)
+    N, Hq, D = q64.shape
+    j = h // (Hq // k64.shape[1])
+    out = np.empty(len(rows))
+    for i, tau in enumerate(rows):
+        s = q64[tau, h, :] @ k64[: tau + 1, j, :].T / math.sqrt(D)
+        m = s.max()
+        out[i] = m + math.log(np.exp(s - m).sum())
+    return out
+
+
+def channel_weights(q, k):
+    """K-channel weight w_c = ||Q_{:,c}|| * ||K_{:,c}|| / sqrt(d) per KV head.
+
+    Q_{:,c} stacks the G query heads of the group over all N positions (R1);
+    K_{:,c} runs over all N tokens.  Returns [H_kv, D] float64.
+    """
+    q64, k64 = _f64(q), _f64(k)
+    N, Hq, D = q64.shape
+    Hkv = k64.shape[1]
+    G = Hq // Hkv
+    qn = np.sqrt((q64 ** 2).reshape(N, Hkv, G, D).sum(axis=(0, 2)))
+    kn = np.sqrt((k64 ** 2).sum(axis=0))
+    return qn * kn / math.sqrt(D)
+
+
+def value_spread(v):
+    """sigma of each V row (R3): population std over its D elements.  [H_kv, N] float64."""
+    v64 = _f64(v)                                       # [N, H_kv, D]
+    mean = v64.mean(axis=2, keepdims=True)
+    return np.sqrt(((v64 - mean) ** 2).mean(axis=2)).T
+
+
+def token_gains(w_tok, sigma_tok, n_prefix):
+    """g_t = fl32(fl32(w_t) * fl32(sigma_t)) on the allocatable prefix."""
+    w32 = np.asarray(w_tok[:, :n_prefix], dtype=np.float32)
+    s32 = np.asarray(sigma_tok[:, :n_prefix], dtype=np.float32)
+    return w32 * s32
+
+
+def score(q, k, v, window):
+    """All step-1 outputs for one sequence, rounded to float32 as the library returns them."""
+    N = q.shape[0]
+    w_tok = token_weights(q, k)
+    sig = value_spread(v)
+    return dict(
+        w_tok=w_tok.astype(np.float32),
+        w_chan=channel_weights(q, k).astype(np.float32),
+        sigma_tok=sig.astype(np.float32),
+        g_tok=token_gains(w_tok, sig, N - window),
+    )
+
+
+# ---------------------------------------------------------------------------
+# Steps 2 and 3: discrete reverse water-filling (RDKV section 2.2)
+# ---------------------------------------------------------------------------
+# The distortion of a unit at width b is g * 2**-b (section 2.1 objective).
+# Moving from width b_k to b_{k+1} removes g * (2**-b_k - 2**-b_{k+1}) of
+# distortion for (b_{k+1} - b_k) bits: the slope per bit below, times g.
+SLOPES = np.array(
+    [(2.0 ** -int(b0) - 2.0 ** -int(b1)) / (int(b1) - int(b0)) for b0, b1 in zip(WIDTHS[:-1], WIDTHS[1:])],
+    dtype=np.float32)
+
+
+def breakpoints(g):
+    """beta_{u,k} = fl32(g_u * slope_k): the water levels at which unit u buys upgrade k."""
+    g = np.asarray(g, dtype=np.float32).reshape(-1)
+    return g[:, None] * SLOPES[None, :]
+
+
+def widths_at(beta, lam):
+    """Lagrangian choice at water level lam: every upgrade whose breakpoint is strictly above lam (R5)."""
+    return WIDTHS[(beta > np.float32(lam)).sum(axis=1)]
+
+
+def budget_bits(avg_bits, n_units):
+    """B = floor(avg_bits * units) (R4); avg_bits arrives as float32."""
+    return int(math.floor(float(np.float32(avg_bits)) * float(n_units)))
+
+
+def waterfill(g, avg_bits):
+    """Multiple-choice knapsack over {0,2,4,8,16} by Lagrangian relaxation.
+
+    Returns (bits uint8 [U], lambda float32): lambda is the smallest
+    non-negative float32 water level whose total width fits the budget
+    B = floor(avg_bits * U).  Found exactly: the bit total only changes at
+    breakpoints, so the candidates are 0 and the breakpoint values, sorted.
+    """
+    g = np.asarray(g, dtype=np.float32).reshape(-1)
+    assert np.all(np.isfinite(g)) and np.all(g >= 0), "gains must be finite and non-negative"
+    U = g.size
+    B = budget_bits(avg_bits, U)
+    beta = breakpoints(g)
+    vals, inv = np.unique(np.concatenate([beta.reshape(-1), np.zeros(1, np.float32)]), return_inverse=True)
+    weight = np.concatenate([np.tile(STEP_BITS, U), [0]])
+    per_val = np.bincount(inv.reshape(-1), weights=weight, minlength=vals.size).astype(np.int64)
+    above = int(per_val.sum()) - np.cumsum(per_val)      # bits bought strictly above each candidate
+    i = int(np.argmax(above <= B))                       # first (smallest) level that fits
+    lam = np.float32(vals[i]) + np.float32(0.0)          # canonical +0.0
+    return widths_at(beta, lam).astype(np.uint8), lam
+
+
+def kept_channel_spread(k, bits_tok):
+    """sigma_c (R3) of each K channel over the kept prefix tokens of its head; 0 if none kept."""
+    k64 = _f64(k)
+    Hkv, Np = bits_tok.shape
+    out = np.zeros((Hkv, k64.shape[2]))
+    for j in range(Hkv):
+        kept = np.nonzero(bits_tok[j] > 0)[0]
+        if kept.size:
+            x = k64[kept, j, :]
+            out[j] = np.sqrt(((x - x.mean(axis=0)) ** 2).mean(axis=0))
+    return out
+
+
+def allocate(g_tok, w_chan, k, avg_bits_v, avg_bits_k):
+    """Section 2.2 step 2 (V tokens) then step 3 (K channels over the kept tokens), one sequence."""
+    Hkv, Np = g_tok.shape
+    bits_tok, lam_v = waterfill(g_tok, avg_bits_v)
+    bits_tok = bits_tok.reshape(Hkv, Np)
+    sig_c = kept_channel_spread(k, bits_tok)
+    g_chan = np.asarray(w_chan, np.float32) * sig_c.astype(np.float32)
+    bits_chan, lam_k = waterfill(g_chan, avg_bits_k)
+    return dict(bits_tok=bits_tok, lam_v=lam_v, sigma_chan=sig_c.astype(np.float32),
+                g_chan=g_chan, bits_chan=bits_chan.reshape(g_chan.shape), lam_k=lam_k)
+
+
+# ---------------------------------------------------------------------------
+# TriZone plan and pack (RDKV section 2.3; layout R8)
+# ---------------------------------------------------------------------------
+def _ceil_div(a, b):
+    return -(-a // b)
+
+
+def head_plan(bits_tok_j, bits_chan_j, head_dim):
+    """Counts, sizes and orders of one (sequence, KV head)."""
+    D = head_dim
+    n_v = [int((bits_tok_j == b).sum()) for b in V_CLASSES]
+    tiles = [_ceil_div(n, TILE) for n in n_v]
+    n_k = [int((bits_chan_j == b).sum()) for b in K_CLASSES]
+    k_words = [_ceil_div(n * b, 32) for n, b in zip(n_k, K_CLASSES)]
+    row_words = sum(k_words)
+    k_slots = sum(w * (32 // b) for w, b in zip(k_words, K_CLASSES))
+    meta_slots = sum(w * (32 // b) for w, b in zip(k_words, K_CLASSES) if b < 16)
+    tile_bytes = [4 * TILE * row_words + 4 * meta_slots + ((TILE * D * b) // 8 + 4 * D if b < 16 else 0)
+                  for b in V_CLASSES]
+    slots = []
+    for (b, w) in zip(K_CLASSES, k_words):
+        ch = np.nonzero(bits_chan_j == b)[0].tolist()
+        slots += ch + [-1] * (w * (32 // b) - len(ch))
+    tokens = []
+    for b, nt in zip(V_CLASSES, tiles):
+        t = np.nonzero(bits_tok_j == b)[0].tolist()
+        tokens.append(np.array(t + [-1] * (nt * TILE - len(t)), dtype=np.int64))
+    return dict(n_v=n_v, tiles=tiles, n_k=n_k + [D - sum(n_k)], k_words=k_words, row_words=row_words,
+                k_slots=k_slots, meta_slots=meta_slots, tile_bytes=tile_bytes,
+                a_bytes=sum(nt * tb for nt, tb in zip(tiles, tile_bytes)),
+                slots=np.array(slots, dtype=np.int64), tokens=tokens)
+
+
+def make_plan(bits_tok, bits_chan, head_dim):
+    """Plan of a batch: bits_tok [B, H_kv, N_p], bits_chan [B, H_kv, D]; heads in (b, j) order."""
+    B, Hkv = bits_tok.shape[:2]
+    heads = []
+    a_off = b_row = slot_off = 0
+    for b in range(B):
+        for j in range(Hkv):
+            hp = head_plan(bits_tok[b, j], bits_chan[b, j], head_dim)
+            hp.update(a_off=a_off, b_row=b_row, slot_off=slot_off)
+            a_off += hp["a_bytes"]
+            b_row += TILE * hp["tiles"][3]
+            slot_off += TILE * sum(hp["tiles"])
+            heads.append(hp)
+    return dict(heads=heads, zone_a_bytes=a_off, zone_b_rows=b_row, index_slots=slot_off,
+                kept_tokens=int(sum(sum(h["n_v"]) for h in heads)),
+                max_tile_bytes=max([tb for h in heads for tb, nt in zip(h["tile_bytes"], h["tiles"]) if nt] or [0]))
+
+
+def quantize_groups(x, b):
+    """Asymmetric min-max quantiser ("Solusi 3"): q = round((x - min) / scale),
+    scale = (max - min) / (2**b - 1), along the last axis, with fp16 scale and
+    zero (R6).  All arithmetic IEEE float32; round half to even; scale 0 -> codes 0.
+    Returns codes uint32 (same shape), scale fp16 and zero fp16 (shape without the last axis).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    mn, mx = x.min(axis=-1), x.max(axis=-1)
+    zero = mn.astype(np.float16)
+    scale = ((mx - mn) / np.float32((1 << b) - 1)).astype(np.float32).astype(np.float16)
+    s32 = scale.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = (x - zero.astype(np.float32)[..., None]) / s32
+    codes = np.clip(np.rint(t), 0, (1 << b) - 1)
+    codes = np.where(s32 == 0, 0, codes).astype(np.uint32)
+    return codes, scale, zero
+
+
+def bit_offset(e, b):
+    """Bit position of element e (0-based inside its 32-bit word) at width b:
+    even elements fill the low half-word, odd elements the high half-word,
+    each half LSB-first."""
+    return 16 * (e % 2) + b * (e // 2)
+
+
+def _halves_bits(a):
+    return np.asarray(a, dtype=np.float16).view(np.uint16).astype(np.uint32)
+
+
+def _pack_words(codes, b, per_word, first_off_fn):
+    """Sum codes (uint64 [..., n]) shifted to their bit offsets into words [..., n // per_word]."""
+    n = codes.shape[-1]
+    shifts = np.array([first_off_fn(e) for e in range(n)], dtype=np.uint64)
+    return (codes.astype(np.uint64) << shifts).reshape(*codes.shape[:-1], n // per_word, per_word).sum(axis=-1)
+
+
+def _k_segments(hp):
+    """(width, first word, words, first meta slot, slot list) of each K segment, in row order."""
+    seg = []
+    w0 = m0 = s0 = 0
+    for b, nw in zip(K_CLASSES, hp["k_words"]):
+        ns = nw * (32 // b)
+        seg.append((b, w0, nw, m0, hp["slots"][s0:s0 + ns]))
+        w0 += nw
+        s0 += ns
+        if b < 16:
+            m0 += ns
+    return seg
+
+
+def pack_head(k_j, v_j, hp, head_dim):
+    """Zone-A bytes and zone-B rows of one (sequence, KV head).
+
+    k_j, v_j: [N, D] float32 values of that head.  Tile layout (little-endian):
+      K codes   32 rows x row_words uint32 (segments 16, 8, 4, 2 bits, each
+                padded to whole words; a 16-bit slot holds the raw fp16 value)
+      K meta    per slot pair of the 8/4/2-bit segments: scale(2i), scale(2i+1),
+                zero(2i), zero(2i+1) as fp16
+      V codes   (width b < 16 only) 16 token pairs x D*b/16 uint32; word w of
+                pair p holds channels [w*16/b, (w+1)*16/b): token 2p in the low
+                half, token 2p+1 in the high half, LSB-first
+      V meta    (b < 16 only) per token pair and 32-channel group: scale(2p),
+                scale(2p+1), zero(2p), zero(2p+1) as fp16
+    Pad tokens and pad slots hold code 0, scale 0 and zero 0.
+    """
+    D = head_dim
+    out, zone_b = [], []
+    seg = _k_segments(hp)
+    RW, QS = hp["row_words"], hp["meta_slots"]
+    for ci, bv in enumerate(V_CLASSES):
+        toks = hp["tokens"][ci]
+        for ti in range(hp["tiles"][ci]):
+            tt = toks[ti * TILE:(ti + 1) * TILE]
+            real = tt >= 0
+            rows = tt[real]
+            kw = np.zeros((TILE, RW), dtype=np.uint64)
+            ksc = np.zeros(QS, dtype=np.float16)
+            kze = np.zeros(QS, dtype=np.float16)
+            for b, wbase, nw, mbase, slots in seg:
+                if nw == 0:
+                    continue
+                per_word = 32 // b
+                sidx = np.nonzero(slots >= 0)[0]
+                X = k_j[np.ix_(rows, slots[sidx])]                     # [real tokens, channels]
+                codes = np.zeros((rows.size, slots.size), dtype=np.uint32)
+                if b == 16:
+                    codes[:, sidx] = _halves_bits(X)
+                else:
+                    c, sc, ze = quantize_groups(X.T, b)                 # one group per channel
+                    codes[:, sidx] = c.T
+                    ksc[mbase + sidx], kze[mbase + sidx] = sc, ze
+                kw[real, wbase:wbase + nw] = _pack_words(codes, b, per_word, lambda e: bit_offset(e % per_word, b))
+            kmeta = np.stack([ksc[0::2], ksc[1::2], kze[0::2], kze[1::2]], axis=1)
+            parts = [kw.astype(np.uint32).tobytes(), kmeta.astype(np.float16).tobytes()]
+            if bv < 16:
+                vals = np.zeros((TILE, D), dtype=np.float32)
+                vals[real] = v_j[rows]
+                codes, sc, ze = quantize_groups(vals.reshape(TILE, D // GROUP, GROUP), bv)
+                codes = codes.reshape(TILE, D)
+                codes[~real], sc[~real], ze[~real] = 0, 0, 0
+                per_word = 16 // bv                                    # channels per word
+                words = _pack_words(codes, bv, per_word, lambda c: bv * (c % per_word))
+                vw = words[0::2] + (words[1::2] << np.uint64(16))      # even token low, odd token high
+                vmeta = np.stack([sc[0::2], sc[1::2], ze[0::2], ze[1::2]], axis=2)   # [16, D/32, 4]
+                parts += [vw.astype(np.uint32).tobytes(), vmeta.astype(np.float16).tobytes()]
+            else:
+                rows16 = np.zeros((TILE, D), dtype=np.float16)
+                rows16[real] = v_j[rows].astype(np.float16)
+                zone_b.append(rows16)
+            tile = b"".join(parts)
+            assert len(tile) == hp["tile_bytes"][ci]
+            out.append(tile)
+    zb = np.concatenate(zone_b) if zone_b else np.zeros((0, D), np.float16)
+    return b"".join(out), zb
+
+
+def pack(k, v, bits_tok, bits_chan, window, cap_c=None):
+    """TriZone pack of a batch.  k, v [B, N, H_kv, D] (fp16 or fp32).
+
+    Returns dict(plan, zone_a uint8, zone_b fp16 [rows, D], zone_c_k / zone_c_v
+    fp16 [B, H_kv, cap_c, D] holding the window in rows [0, W), index int32
+    (original position per token slot, -1 for pads), len_c).
+    """
+    B, N, Hkv, D = k.shape
+    plan = make_plan(bits_tok, bits_chan, D)
+    cap_c = window if cap_c is None else cap_c
+    za, zb = [], []
+    index = np.full(plan["index_slots"], -1, dtype=np.int32)
+    for hi, hp in enumerate(plan["heads"]):
+        b, j = divmod(hi, Hkv)
+        a, rows = pack_head(np.asarray(k[b, :, j, :], np.float32), np.asarray(v[b, :, j, :], np.float32), hp, D)
+        za.append(a)
+        zb.append(rows)
+        toks = np.concatenate(hp["tokens"])
+        index[hp["slot_off"]:hp["slot_off"] + toks.size] = toks
+    zc_k = np.zeros((B, Hkv, cap_c, D), np.float16)
+    zc_v = np.zeros((B, Hkv, cap_c, D), np.float16)
+    zc_k[:, :, :window] = np.asarray(k[:, N - window:], np.float32).astype(np.float16).transpose(0, 2, 1, 3)
+    zc_v[:, :, :window] = np.asarray(v[:, N - window:], np.float32).astype(np.float16).transpose(0, 2, 1, 3)
+    return dict(plan=plan, zone_a=np.frombuffer(b"".join(za), dtype=np.uint8).copy(),
+                zone_b=np.concatenate(zb) if zb else np.zeros((0, D), np.float16),
+                zone_c_k=zc_k, zone_c_v=zc_v, index=index, len_c=window)
+
+
+def append(cache, k_new, v_new):
+    """Zone C receives the fp16 K and V rows of a new token (RDKV section 2.3)."""
+    r = cache["len_c"]
+    if r >= cache["zone_c_k"].shape[2]:
+        raise ValueError("zone C is full")
+    cache["zone_c_k"][:, :, r] = np.asarray(k_new, np.float32).astype(np.float16)
+    cache["zone_c_v"][:, :, r] = np.asarray(v_new, np.float32).astype(np.float16)
+    cache["len_c"] = r + 1
+
+
+# ---------------------------------------------------------------------------
+# Unpack and decode (RDKV section 2.3: attention over zones A, B and C)
+# ---------------------------------------------------------------------------
+def _field(words, off, b):
+    return (words >> np.uint32(off)) & np.uint32((1 << b) - 1)
+
+
+def unpack_head(zone_a, zone_b, hp, head_dim):
+    """Read one head's tiles back: (original positions, K-hat [n, D], V-hat [n, D]) in float64.
+    Dequantised value = zero + scale * code; dropped channels read as 0."""
+    D = head_dim
+    RW, QS = hp["row_words"], hp["meta_slots"]
+    seg = _k_segments(hp)
+    toks_all, K_all, V_all = [], [], []
+    off = hp["a_off"]
+    brow = hp["b_row"]
+    r = np.arange(TILE)[:, None]
+    c = np.arange(D)[None, :]
+    for ci, bv in enumerate(V_CLASSES):
+        for ti in range(hp["tiles"][ci]):
+            tt = hp["tokens"][ci][ti * TILE:(ti + 1) * TILE]
+            real = tt >= 0
+            kw = np.frombuffer(zone_a, np.uint32, TILE * RW, off).reshape(TILE, RW)
+            p = off + 4 * TILE * RW
+            km = np.frombuffer(zone_a, np.float16, 2 * QS, p).reshape(QS // 2, 4).astype(np.float64)
+            ksc, kze = np.empty(QS), np.empty(QS)
+            ksc[0::2], ksc[1::2], kze[0::2], kze[1::2] = km[:, 0], km[:, 1], km[:, 2], km[:, 3]
+            p += 4 * QS
+            Kt = np.zeros((TILE, D))
+            for b, wbase, nw, mbase, slots in seg:
+                per_word = 32 // b
+                for s in np.nonzero(slots >= 0)[0]:
+                    code = _field(kw[:, wbase + s // per_word], bit_offset(s % per_word, b), b)
+                    if b == 16:
+                        Kt[:, slots[s]] = code.astype(np.uint16).view(np.float16).astype(np.float64)
+                    else:
+                        Kt[:, slots[s]] = kze[mbase + s] + ksc[mbase + s] * code.astype(np.float64)
+            if bv < 16:
+                per_word = 16 // bv
+                vw = np.frombuffer(zone_a, np.uint32, (TILE // 2) * (D // per_word), p).reshape(TILE // 2, D // per_word)
+                p += 4 * vw.size
+                vm = np.frombuffer(zone_a, np.float16, (TILE // 2) * (D // GROUP) * 4, p)
+                vm = vm.reshape(TILE // 2, D // GROUP, 4).astype(np.float64)
+                p += 2 * vm.size
+                code = _field(vw[r // 2, c // per_word], 16 * (r % 2) + bv * (c % per_word), bv).astype(np.float64)
+                Vt = vm[r // 2, c // GROUP, 2 + r % 2] + vm[r // 2, c // GROUP, r % 2] * code
+            else:
+                Vt = zone_b[brow:brow + TILE].astype(np.float64)
+                brow += TILE
+            assert p - off == hp["tile_bytes"][ci]
+            off = p
+            toks_all.append(tt[real])
+            K_all.append(Kt[real])
+            V_all.append(Vt[real])
+    if not toks_all:
+        return np.zeros(0, np.int64), np.zeros((0, D)), np.zeros((0, D))
+    return np.concatenate(toks_all), np.concatenate(K_all), np.concatenate(V_all)
+
+
+def attention(q, K, V):
+    """Textbook softmax attention of one query over rows K, V (scale 1/sqrt(D)), float64.
+    With no rows the output is 0."""
+    q = _f64(q)
+    if K.shape[0] == 0:
+        return np.zeros(q.shape[-1])
+    s = _f64(K) @ q / math.sqrt(q.shape[-1])
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    return p @ _f64(V)
+
+
+def unpack(cache, head_dim):
+    """Per head: (positions, K-hat, V-hat) of zones A and B."""
+    return [unpack_head(cache["zone_a"].tobytes(), cache["zone_b"], hp, head_dim) for hp in cache["plan"]["heads"]]
+
+
+def decode(cache, q, unpacked=None):
+    """One decode step: out [B, H_q, D] float64 attending over zones A+B of the
+    plan and rows [0, len_c) of zone C, for queries q [B, H_q, D]."""
+    q64 = _f64(q)
+    B, Hq, D = q64.shape
+    Hkv = cache["zone_c_k"].shape[1]
+    G = Hq // Hkv
+    un = unpacked if unpacked is not None else unpack(cache, D)
+    L = cache["len_c"]
+    out = np.zeros((B, Hq, D))
+    for b in range(B):
+        for j in range(Hkv):
+            _, Ka, Va = un[b * Hkv + j]
+            K = np.concatenate([Ka, cache["zone_c_k"][b, j, :L].astype(np.float64)])
+            V = np.concatenate([Va, cache["zone_c_v"][b, j, :L].astype(np.float64)])
+            for h in range(j * G, (j + 1) * G):
+                out[b, h] = attention(q64[b, h], K, V)
+    return out
+
+
+def decode_bytes(plan, head_dim, h_q, h_kv, len_c, batch):
+    """Algorithmic bytes one decode step must read and write: zone-A payload and
+    metadata of real tokens and real channels, zone-B rows of real tokens,
+    zone-C rows, q (fp16) and out (fp32).  Padding is excluded."""
+    D = head_dim
+    total = 0
+    for hp in plan["heads"]:
+        n16k, n8k, n4k, n2k, _ = hp["n_k"]
+        kq = n8k + n4k + n2k
+        ntok = sum(hp["n_v"])
+        k_payload = ntok * (2 * n16k + (8 * n8k + 4 * n4k + 2 * n2k) / 8)
+        k_meta = 4 * kq * ntok / TILE
+        v_payload = sum(n * (D * b / 8 + (4 * D / GROUP if b < 16 else 0)) for n, b in zip(hp["n_v"], V_CLASSES))
+        total += k_payload + k_meta + v_payload + len_c * 4 * D
+    total += batch * h_q * D * (2 + 4)
+    return total

@@ -1,0 +1,207 @@
+/*
+ * rdkv.h — C ABI of the RDKV hot path on one GPU (sm_103a).
+ *
+ * RDKV ("RDKV - KV 캐시 공동 추방 및 양자화를 위한 왜곡-비트 할당",
+ * gist.science/ko/paper/2605.08317) compresses a KV cache after prefill by
+ *   section 2.1  distortion weights: w_t (attention mass a token receives) for
+ *                V tokens, w_c = |Q_:,c| |K_:,c| / sqrt(d) for K channels;
+ *   section 2.2  discrete reverse water-filling (Lagrangian relaxation of a
+ *                multiple-choice knapsack) over widths {0,2,4,8,16}: V tokens
+ *                first, then K channels of the kept tokens;
+ *   section 2.3  the TriZone layout: zone A packed 2/4/8-bit rows grouped by
+ *                width, zone B fp16 V rows of 16-bit tokens, zone C fp16 rows
+ *                of new tokens; decode attention dequantises inside the
+ *                products and reads the three zones in one pass.
+ * The quantiser is the asymmetric min-max formula of "Matematika KV Cache
+ * Compression" (aistudio.id), section "Solusi 3".
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory.  Scratch memory is passed in as `ws` with
+ *     the size the matching *_workspace_bytes() call returns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream unless stated otherwise.
+ *   - Tensors are dense, row-major, little-endian.  fp16 = IEEE binary16.
+ *   - Shapes: B = batch, N = prompt tokens, H_q, H_kv query/KV heads
+ *     (G = H_q / H_kv), D = head_dim (64 or 128), W = window,
+ *     N_p = N - W allocatable prefix tokens.
+ *   - Errors: a call that returns anything but RDKV_OK launched nothing
+ *     (argument errors) or hit a CUDA error (RDKV_ERR_CUDA); the message is
+ *     in rdkv_last_error_string() (thread-local).
+ */
+#ifndef RDKV_H
+#define RDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rdkv_status {
+  RDKV_OK = 0,
+  RDKV_ERR_INVALID_ARG = 1,   /* bad pointer, size, budget or (device-side) gain */
+  RDKV_ERR_UNSUPPORTED = 2,   /* dtype / head_dim / group size outside the supported set */
+  RDKV_ERR_CAPACITY = 3,      /* zone C is full (rdkv_append) */
+  RDKV_ERR_CUDA = 4,          /* a CUDA runtime error */
+  RDKV_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
+  RDKV_ERR_WORKSPACE = 6      /* ws too small */
+} rdkv_status;
+
+enum { RDKV_F16 = 0, RDKV_F32 = 1 };
+
+/* Problem shape.  Q, K, V of the prefill are [B][N][H][D] in `dtype`. */
+typedef struct rdkv_shape {
+  int32_t batch, n_tokens, h_q, h_kv, head_dim, window, dtype;
+} rdkv_shape;
+
+/* One (sequence, KV head) of the plan, written by rdkv_allocate (device memory).
+ * Token classes are V widths 2,4,8,16; K segments are widths 16,8,4,2. */
+typedef struct rdkv_head_plan {
+  int32_t n_v[4];        /* kept prefix tokens of each V width */
+  int32_t tiles[4];      /* 32-token tiles of each V width: ceil(n_v / 32) */
+  int32_t n_k[5];        /* channels of K width 16, 8, 4, 2, 0 */
+  int32_t k_words[4];    /* 32-bit words per K row in the 16/8/4/2-bit segments */
+  int32_t row_words;     /* sum of k_words */
+  int32_t k_slots;       /* channel slots of a K row (kept channels + pads) */
+  int32_t meta_slots;    /* slots of the 8/4/2-bit segments (those carry scale/zero) */
+  int32_t tile_bytes[4]; /* zone-A bytes of one tile of each V width */
+  int64_t a_off;         /* byte offset of this head's first tile in zone A */
+  int64_t a_bytes;       /* zone-A bytes of this head */
+  int64_t b_row;         /* first zone-B row of this head */
+  int64_t slot_off;      /* first index-map slot of this head */
+} rdkv_head_plan;        /* 128 bytes */
+
+/* Head of the device plan buffer.  The buffer continues with
+ *   rdkv_head_plan heads[n_heads]                 (heads in (b, j) order)
+ *   int16_t slot_channel[n_heads][slot_stride]    (channel of each K slot, -1 = pad)
+ *   float lambda_v[batch], lambda_k[batch]        (water levels found)
+ * at the offsets given by the fields below. */
+typedef struct rdkv_plan_header {
+  int32_t status;          /* RDKV_OK, or RDKV_ERR_INVALID_ARG if a gain was NaN/inf/negative */
+  int32_t n_heads;         /* batch * h_kv */
+  int32_t batch, h_kv, head_dim, slot_stride;
+  int64_t heads_off, slots_off, lambda_off;   /* byte offsets inside the plan buffer */
+  int64_t zone_a_bytes;    /* zone-A bytes of the whole batch */
+  int64_t zone_b_rows;     /* zone-B rows (each D fp16) */
+  int64_t index_slots;     /* index-map entries */
+  int64_t kept_tokens;     /* kept prefix tokens over all heads */
+  int64_t max_tile_bytes;  /* largest zone-A tile present */
+} rdkv_plan_header;
+
+/* Host copy of the totals, from rdkv_plan_sizes. */
+typedef struct rdkv_sizes {
+  int64_t zone_a_bytes, zone_b_rows, index_slots, kept_tokens, max_tile_bytes;
+  int32_t status, n_heads;
+} rdkv_sizes;
+
+/* A packed TriZone cache.  All pointers are caller-owned device memory.
+ * zone_c_k / zone_c_v are fp16 [batch][h_kv][cap_c][D].  len_c is the number
+ * of zone-C rows in use (same for every sequence): rdkv_pack sets it to the
+ * window W, rdkv_append advances it; the library keeps it on the host. */
+typedef struct rdkv_cache {
+  rdkv_shape shape;
+  const void* plan;
+  uint8_t* zone_a;
+  uint16_t* zone_b;
+  uint16_t* zone_c_k;
+  uint16_t* zone_c_v;
+  int32_t* index_map;
+  int32_t cap_c;
+  int32_t len_c;
+  rdkv_sizes sizes;
+} rdkv_cache;
+
+/* ---------------------------------------------------------------- misc */
+const char* rdkv_last_error_string(void);
+int32_t rdkv_version(void);
+
+/* ---------------------------------------------------------------- step 1: weights
+ * RDKV section 2.1 (and section 2.2 step 1: computed once after prefill on the
+ * full cache).  For each sequence b and KV head j (query heads h of group j):
+ *   w_tok[b][j][t]  = sum_{h in j} sum_{tau >= t} softmax_t(q_tau,h . k_t / sqrt(D))   (causal)
+ *   w_chan[b][j][c] = sqrt(sum_{tau, h in j} q_tau,h,c^2) * sqrt(sum_t k_t,j,c^2) / sqrt(D)
+ *   sigma_tok[b][j][t] = population std of v_t,j over its D elements
+ *   g_tok[b][j][t]  = fl32(w_tok * sigma_tok) for t < N_p
+ * q [B][N][H_q][D], k, v [B][N][H_kv][D] in shape->dtype.  Outputs fp32:
+ * w_tok, sigma_tok [B][H_kv][N], w_chan [B][H_kv][D], g_tok [B][H_kv][N_p].
+ * Supported: D in {64, 128}, 1 <= G <= 8.  fp16 inputs use tensor cores with
+ * fp32 accumulation; fp32 inputs use fp32 CUDA-core arithmetic. */
+size_t rdkv_score_workspace_bytes(const rdkv_shape* shape);
+rdkv_status rdkv_score(const rdkv_shape* shape, const void* q, const void* k, const void* v,
+                       float* w_tok, float* w_chan, float* sigma_tok, float* g_tok,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- step 2/3: allocation
+ * Discrete reverse water-filling (RDKV section 2.2) on n_inst independent
+ * instances of n_units gains each: g [n_inst][n_units] fp32 (finite, >= 0).
+ * Per instance, with B = floor((double)avg_bits * n_units):
+ *   beta_{u,k} = fl32(g_u * s_k), s = (0.375, 0.09375, 0.0146484375, 255/524288)
+ *   lambda*    = smallest float32 >= 0 with sum_u b_u(lambda*) <= B
+ *   b_u        = width after every upgrade k with beta_{u,k} > lambda*
+ * bits [n_inst][n_units] uint8 in {0,2,4,8,16}; lambda_out [n_inst] fp32 (may be NULL).
+ * lambda* is found by an 8-bit-per-level bisection of the float32 bit pattern.
+ * status_out (device int32, may be NULL) is set to RDKV_ERR_INVALID_ARG if a
+ * gain is NaN, infinite or negative (that unit gets 0 bits). */
+size_t rdkv_waterfill_workspace_bytes(int32_t n_inst, int64_t n_units);
+rdkv_status rdkv_waterfill(int32_t n_inst, int64_t n_units, const float* g, float avg_bits,
+                           uint8_t* bits, float* lambda_out, int32_t* status_out,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Full allocation of a batch (RDKV section 2.2 steps 2 and 3) and the TriZone plan:
+ *   V: water-filling of g_tok [B][H_kv][N_p] per sequence (pooled over heads)
+ *      with avg_bits_v -> bits_tok [B][H_kv][N_p];
+ *   K: sigma_chan [B][H_kv][D] = population std of K over the kept prefix
+ *      tokens of the head (0 if none); g_chan = fl32(w_chan * sigma_chan);
+ *      water-filling per sequence with avg_bits_k -> bits_chan [B][H_kv][D];
+ *   plan: counts, orders and zone offsets (layout above) in `plan`
+ *      (rdkv_plan_bytes(shape) bytes of device memory).
+ * k is the prefill K [B][N][H_kv][D]. */
+size_t rdkv_plan_bytes(const rdkv_shape* shape);
+size_t rdkv_allocate_workspace_bytes(const rdkv_shape* shape);
+rdkv_status rdkv_allocate(const rdkv_shape* shape, const float* g_tok, const float* w_chan,
+                          const void* k, float avg_bits_v, float avg_bits_k,
+                          uint8_t* bits_tok, float* sigma_chan, float* g_chan, uint8_t* bits_chan,
+                          void* plan, void* ws, size_t ws_bytes, void* stream);
+
+/* Copies the plan totals to the host.  SYNCHRONISES `stream`.  Returns the
+ * plan's device status (RDKV_ERR_INVALID_ARG if a gain was invalid). */
+rdkv_status rdkv_plan_sizes(const void* plan, rdkv_sizes* out, void* stream);
+
+/* ---------------------------------------------------------------- TriZone pack
+ * RDKV section 2.3.  Writes zone A (sizes.zone_a_bytes), zone B
+ * (sizes.zone_b_rows x D fp16), the index map (sizes.index_slots int32) and
+ * the window rows [0, W) of zone C from the prefill k, v [B][N][H_kv][D];
+ * sets cache->len_c = W.  cache->plan must be the plan bits_tok/bits_chan came
+ * with; cap_c >= W.  Bytes are bit-exact with the layout rules:
+ * asymmetric min-max codes (aistudio.id "Solusi 3") with fp16 scale/zero. */
+rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v,
+                      const uint8_t* bits_tok, const uint8_t* bits_chan, void* stream);
+
+/* ---------------------------------------------------------------- append
+ * RDKV section 2.3 zone C: writes the new token's k_new, v_new [B][H_kv][D]
+ * (shape->dtype) as fp16 rows at index len_c of zone C and advances len_c.
+ * Returns RDKV_ERR_CAPACITY (nothing written) when len_c == cap_c. */
+rdkv_status rdkv_append(rdkv_cache* cache, const void* k_new, const void* v_new, void* stream);
+
+/* ---------------------------------------------------------------- decode attention
+ * RDKV section 2.3: for every sequence b and query head h (KV head h / G),
+ *   out[b][h] = sum_t softmax_t(q[b][h] . k^_t / sqrt(D)) v^_t
+ * over the kept tokens of zones A (dequantised K and V) and B (fp16 V) and the
+ * len_c rows of zone C.  q [B][H_q][D] in shape->dtype (used as fp16 by the
+ * tensor cores), out [B][H_q][D] fp32.  Split-K over tiles with an fp32
+ * online softmax; the partial results live in ws. */
+size_t rdkv_decode_workspace_bytes(const rdkv_cache* cache);
+rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, float* out,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Reads the status word the last rdkv_decode_attn on this cache and ws left
+ * behind.  SYNCHRONISES `stream`.  RDKV_ERR_TIMEOUT means a bounded wait for a
+ * tile copy ran out (the output of that call is not valid). */
+rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RDKV_H */

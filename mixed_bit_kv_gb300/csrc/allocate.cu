@@ -1,0 +1,435 @@
+// Bit allocation of RDKV (gist.science/ko/paper/2605.08317, section 2.2):
+// discrete reverse water-filling over widths {0, 2, 4, 8, 16} by Lagrangian
+// relaxation, first for V tokens (step 2), then for K channels of the kept
+// tokens (step 3); and the TriZone plan (section 2.3) that the pack and the
+// decode read.
+//
+// Water level search.  The distortion of a unit at width b is g * 2^-b
+// (section 2.1 objective), so upgrade k (b_k -> b_{k+1}) is worth it while
+// g * s_k > lambda with s_k the distortion drop per bit.  The bits bought,
+// H(lambda) = sum over breakpoints beta = fl32(g * s_k) > lambda of the
+// upgrade's bits, only changes at breakpoints.  The smallest float32
+// lambda >= 0 with H(lambda) <= B is found by bisecting the float32 bit
+// pattern (monotone in value for non-negative floats) eight bits per level:
+// each level histograms the breakpoints that share the prefix fixed so far,
+// weighted by their bits, and keeps the smallest digit whose upper tail fits.
+// Four levels give the exact minimum; the counts are integers, so the result
+// does not depend on the order of the additions.
+#include <cmath>
+
+#include "common.cuh"
+
+namespace rdkv {
+
+// Distortion drop per bit of each upgrade 0->2, 2->4, 4->8, 8->16, exact in fp32.
+__constant__ float kSlope[4] = {0.375f, 0.09375f, 0.0146484375f, 255.0f / 524288.0f};
+__constant__ uint32_t kStepBits[4] = {2, 2, 4, 8};
+__constant__ uint8_t kWidth[5] = {0, 2, 4, 8, 16};
+
+struct WfState {
+  unsigned long long above;  // bits bought strictly above the fixed prefix range
+  uint32_t prefix;           // bit pattern fixed so far
+  int32_t pad;
+};
+
+static size_t wf_ws_bytes(int n_inst) {
+  return (size_t)align_up((int64_t)n_inst * (256 * 8 + (int64_t)sizeof(WfState)) + 16, 256);
+}
+
+__global__ void wf_init(WfState* st, unsigned long long* hist, int n_inst, int32_t* status) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_inst * 256; i += gridDim.x * blockDim.x) hist[i] = 0;
+  if (blockIdx.x == 0 && threadIdx.x < n_inst) st[threadIdx.x] = WfState{0ull, 0u, 0};
+  if (blockIdx.x == 0 && threadIdx.x == 0 && status) *status = RDKV_OK;
+}
+
+__device__ __forceinline__ bool gain_valid(float g) { return g >= 0.0f && g <= 3.402823466e38f; }
+
+__global__ void wf_hist(const float* __restrict__ g, int64_t n_units, int level, const WfState* __restrict__ st,
+                        unsigned long long* __restrict__ hist, int32_t* status) {
+  __shared__ uint32_t h[256];
+  const int inst = blockIdx.y;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  const uint32_t prefix = st[inst].prefix;
+  const int shift = 24 - 8 * level;
+  const float* gi = g + (int64_t)inst * n_units;
+  bool bad = false;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)gridDim.x * blockDim.x) {
+    const float gv = gi[u];
+    if (!gain_valid(gv)) {
+      bad = true;
+      continue;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t p = level_bits(gv * kSlope[k]);
+      if (level == 0 || (p >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&h[(p >> shift) & 255u], kStepBits[k]);
+    }
+  }
+  if (bad && level == 0 && status) atomicExch(status, (int32_t)RDKV_ERR_INVALID_ARG);
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    if (h[i]) atomicAdd(&hist[inst * 256 + i], (unsigned long long)h[i]);
+}
+
+// One block of 256 threads per instance: digit d is kept if the bits bought
+// above x_d = prefix | d << shift | (lower bits all ones) fit the budget.
+__global__ void wf_select(int level, long long budget, WfState* st, unsigned long long* hist) {
+  __shared__ unsigned long long s[256];
+  __shared__ int best;
+  const int inst = blockIdx.x, t = threadIdx.x;
+  const unsigned long long v = hist[inst * 256 + t];
+  s[255 - t] = v;  // reversed so that an inclusive scan gives sums over d' >= t
+  if (t == 0) best = 255;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    unsigned long long x = (255 - t >= off) ? s[255 - t - off] : 0ull;
+    __syncthreads();
+    s[255 - t] += x;
+    __syncthreads();
+  }
+  const unsigned long long tail = s[255 - t] - v;  // sum over d' > t
+  const unsigned long long above = st[inst].above;
+  if (above + tail <= (unsigned long long)budget) atomicMin(&best, t);
+  __syncthreads();
+  const int d = best;
+  if (t == d) {
+    st[inst].prefix |= (uint32_t)d << (24 - 8 * level);
+    st[inst].above = above + tail;
+  }
+  hist[inst * 256 + t] = 0;
+}
+
+__global__ void wf_assign(const float* __restrict__ g, int64_t n_units, const WfState* __restrict__ st,
+                          uint8_t* __restrict__ bits, float* __restrict__ lambda_out) {
+  const int inst = blockIdx.y;
+  const uint32_t lam = st[inst].prefix;
+  if (lambda_out && blockIdx.x == 0 && threadIdx.x == 0) lambda_out[inst] = __uint_as_float(lam);
+  const float* gi = g + (int64_t)inst * n_units;
+  uint8_t* bi = bits + (int64_t)inst * n_units;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)gridDim.x * blockDim.x) {
+    const float gv = gi[u];
+    int m = 0;
+    if (gain_valid(gv)) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m += level_bits(gv * kSlope[k]) > lam ? 1 : 0;
+    }
+    bi[u] = kWidth[m];
+  }
+}
+
+static rdkv_status launch_waterfill(int n_inst, int64_t n_units, const float* g, float avg_bits, uint8_t* bits,
+                                    float* lambda_out, int32_t* status_out, void* ws, cudaStream_t st) {
+  const long long budget = (long long)std::floor((double)avg_bits * (double)n_units);
+  auto* state = reinterpret_cast<WfState*>(ws);
+  auto* hist = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + align_up((int64_t)n_inst * sizeof(WfState), 16));
+  int32_t* status = status_out;
+  wf_init<<<4, 256, 0, st>>>(state, hist, n_inst, status);
+  RDKV_CHECK_LAUNCH("waterfill init");
+  const int per_inst = (int)std::min<int64_t>(std::max<int64_t>(ceil_div64(n_units, 256 * 16), 1), 512);
+  for (int level = 0; level < 4; ++level) {
+    wf_hist<<<dim3(per_inst, n_inst), 256, 0, st>>>(g, n_units, level, state, hist, status);
+    RDKV_CHECK_LAUNCH("waterfill histogram");
+    wf_select<<<n_inst, 256, 0, st>>>(level, budget, state, hist);
+    RDKV_CHECK_LAUNCH("waterfill select");
+  }
+  wf_assign<<<dim3(per_inst, n_inst), 256, 0, st>>>(g, n_units, state, bits, lambda_out);
+  RDKV_CHECK_LAUNCH("waterfill assign");
+  return RDKV_OK;
+}
+
+// ---------------------------------------------------------------- K channel spread over kept tokens
+// sigma_c (population std of K[kept tokens, j, c]) in two passes: chunk sums
+// in fp32, combined in fp64 in a fixed order; then sums of squared deviations.
+constexpr int kChanChunk = 256;
+
+__global__ void chan_pass(const void* __restrict__ k, const uint8_t* __restrict__ bits_tok, int dtype, int N, int h_kv,
+                          int D, int Np, const float* __restrict__ mean, float* __restrict__ part,
+                          int* __restrict__ part_cnt) {
+  const int head = blockIdx.y;  // b * h_kv + j
+  const int b = head / h_kv, j = head % h_kv;
+  const int chunk = blockIdx.x, nchunk = gridDim.x;
+  const int c = threadIdx.x;
+  const int t0 = chunk * kChanChunk, t1 = min(Np, t0 + kChanChunk);
+  const uint8_t* bt = bits_tok + (int64_t)head * Np;
+  const float m = mean ? mean[head * D + c] : 0.0f;
+  float acc = 0.0f;
+  int cnt = 0;
+  for (int t = t0; t < t1; ++t) {
+    if (bt[t] == 0) continue;
+    const float x = load_as_float(k, (((int64_t)b * N + t) * h_kv + j) * D + c, dtype);
+    const float d = x - m;
+    acc += mean ? d * d : x;
+    ++cnt;
+  }
+  part[((int64_t)head * nchunk + chunk) * D + c] = acc;
+  if (c == 0 && part_cnt) part_cnt[head * nchunk + chunk] = cnt;
+}
+
+__global__ void chan_finish(const float* __restrict__ part, const int* __restrict__ part_cnt, int nchunk, int D,
+                            float* __restrict__ mean_out, const float* __restrict__ w_chan,
+                            float* __restrict__ sigma_out, float* __restrict__ g_out) {
+  const int head = blockIdx.x, c = threadIdx.x;
+  double s = 0.0;
+  long long n = 0;
+  for (int i = 0; i < nchunk; ++i) {
+    s += (double)part[((int64_t)head * nchunk + i) * D + c];
+    n += part_cnt[head * nchunk + i];
+  }
+  if (mean_out) {
+    mean_out[head * D + c] = n ? (float)(s / (double)n) : 0.0f;
+  } else {
+    const float sig = n ? (float)sqrt(s / (double)n) : 0.0f;
+    sigma_out[head * D + c] = sig;
+    g_out[head * D + c] = w_chan[head * D + c] * sig;
+  }
+}
+
+// ---------------------------------------------------------------- plan
+__global__ void plan_heads_kernel(const uint8_t* __restrict__ bits_tok, const uint8_t* __restrict__ bits_chan, int Np,
+                                  int D, char* plan, int64_t heads_off, int64_t slots_off, int slot_stride) {
+  const int head = blockIdx.x;
+  __shared__ int nv[4], nk[5];
+  __shared__ int seg_base[4];
+  if (threadIdx.x < 4) nv[threadIdx.x] = 0;
+  if (threadIdx.x < 5) nk[threadIdx.x] = 0;
+  int16_t* slots = reinterpret_cast<int16_t*>(plan + slots_off) + (int64_t)head * slot_stride;
+  for (int i = threadIdx.x; i < slot_stride; i += blockDim.x) slots[i] = -1;
+  __syncthreads();
+  int cnt[4] = {0, 0, 0, 0};
+  const uint8_t* bt = bits_tok + (int64_t)head * Np;
+  for (int t = threadIdx.x; t < Np; t += blockDim.x) {
+    const int b = bt[t];
+    cnt[0] += b == 2;
+    cnt[1] += b == 4;
+    cnt[2] += b == 8;
+    cnt[3] += b == 16;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) atomicAdd(&nv[i], cnt[i]);
+  const uint8_t* bc = bits_chan + (int64_t)head * D;
+  auto kclass = [](int b) { return b == 16 ? 0 : b == 8 ? 1 : b == 4 ? 2 : b == 2 ? 3 : 4; };
+  for (int c = threadIdx.x; c < D; c += blockDim.x) atomicAdd(&nk[kclass(bc[c])], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    rdkv_head_plan hp;
+    int words_total = 0, slots_total = 0, meta = 0;
+    for (int i = 0; i < 4; ++i) {
+      const int b = 16 >> i;  // K segment widths 16, 8, 4, 2
+      hp.k_words[i] = ceil_div(nk[i] * b, 32);
+      seg_base[i] = slots_total;
+      words_total += hp.k_words[i];
+      slots_total += hp.k_words[i] * (32 / b);
+      if (b < 16) meta += hp.k_words[i] * (32 / b);
+    }
+    for (int i = 0; i < 5; ++i) hp.n_k[i] = nk[i];
+    hp.row_words = words_total;
+    hp.k_slots = slots_total;
+    hp.meta_slots = meta;
+    int64_t a = 0;
+    for (int i = 0; i < 4; ++i) {
+      hp.n_v[i] = nv[i];
+      hp.tiles[i] = ceil_div(nv[i], kTile);
+      hp.tile_bytes[i] = tile_bytes_of(words_total, meta, D, 2 << i);  // V widths 2, 4, 8, 16
+      a += (int64_t)hp.tiles[i] * hp.tile_bytes[i];
+    }
+    hp.a_bytes = a;
+    hp.a_off = hp.b_row = hp.slot_off = 0;
+    reinterpret_cast<rdkv_head_plan*>(plan + heads_off)[head] = hp;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    const int cls = kclass(bc[c]);
+    if (cls == 4) continue;
+    int rank = 0;
+    for (int c2 = 0; c2 < c; ++c2) rank += kclass(bc[c2]) == cls;
+    slots[seg_base[cls] + rank] = (int16_t)c;
+  }
+}
+
+__global__ void plan_offsets_kernel(char* plan, int batch, int h_kv, int D, int slot_stride, int64_t heads_off,
+                                    int64_t slots_off, int64_t lambda_off, const int32_t* status_v,
+                                    const int32_t* status_k) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  auto* hdr = reinterpret_cast<rdkv_plan_header*>(plan);
+  auto* heads = reinterpret_cast<rdkv_head_plan*>(plan + heads_off);
+  const int n_heads = batch * h_kv;
+  int64_t a = 0, brow = 0, slot = 0, kept = 0, maxt = 0;
+  for (int i = 0; i < n_heads; ++i) {
+    rdkv_head_plan& hp = heads[i];
+    hp.a_off = a;
+    hp.b_row = brow;
+    hp.slot_off = slot;
+    a += hp.a_bytes;
+    brow += (int64_t)kTile * hp.tiles[3];
+    int nt = 0;
+    for (int c = 0; c < 4; ++c) {
+      nt += hp.tiles[c];
+      kept += hp.n_v[c];
+      if (hp.tiles[c] && hp.tile_bytes[c] > maxt) maxt = hp.tile_bytes[c];
+    }
+    slot += (int64_t)kTile * nt;
+  }
+  int32_t s = RDKV_OK;
+  if (*status_v != RDKV_OK) s = *status_v;
+  if (*status_k != RDKV_OK) s = *status_k;
+  hdr->status = s;
+  hdr->n_heads = n_heads;
+  hdr->batch = batch;
+  hdr->h_kv = h_kv;
+  hdr->head_dim = D;
+  hdr->slot_stride = slot_stride;
+  hdr->heads_off = heads_off;
+  hdr->slots_off = slots_off;
+  hdr->lambda_off = lambda_off;
+  hdr->zone_a_bytes = a;
+  hdr->zone_b_rows = brow;
+  hdr->index_slots = slot;
+  hdr->kept_tokens = kept;
+  hdr->max_tile_bytes = maxt;
+}
+
+// ---------------------------------------------------------------- shape checks shared with the other calls
+rdkv_status check_shape(const rdkv_shape* s) {
+  RDKV_REQUIRE(s != nullptr, RDKV_ERR_INVALID_ARG, "shape is NULL");
+  RDKV_REQUIRE(s->batch >= 1 && s->n_tokens >= 1 && s->h_q >= 1 && s->h_kv >= 1, RDKV_ERR_INVALID_ARG,
+               "shape sizes must be positive (batch=%d n_tokens=%d h_q=%d h_kv=%d)", s->batch, s->n_tokens, s->h_q,
+               s->h_kv);
+  RDKV_REQUIRE(s->window >= 0 && s->window <= s->n_tokens, RDKV_ERR_INVALID_ARG, "window %d outside [0, n_tokens=%d]",
+               s->window, s->n_tokens);
+  RDKV_REQUIRE(s->h_q % s->h_kv == 0, RDKV_ERR_INVALID_ARG, "h_q=%d is not a multiple of h_kv=%d", s->h_q, s->h_kv);
+  RDKV_REQUIRE(s->h_q / s->h_kv <= 8, RDKV_ERR_UNSUPPORTED, "group size %d > 8", s->h_q / s->h_kv);
+  RDKV_REQUIRE(s->head_dim == 64 || s->head_dim == 128, RDKV_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}",
+               s->head_dim);
+  RDKV_REQUIRE(s->dtype == RDKV_F16 || s->dtype == RDKV_F32, RDKV_ERR_UNSUPPORTED, "dtype %d", s->dtype);
+  return RDKV_OK;
+}
+
+}  // namespace rdkv
+
+using namespace rdkv;
+
+extern "C" size_t rdkv_waterfill_workspace_bytes(int32_t n_inst, int64_t n_units) {
+  (void)n_units;
+  return n_inst > 0 ? wf_ws_bytes(n_inst) + 256 : 0;
+}
+
+extern "C" rdkv_status rdkv_waterfill(int32_t n_inst, int64_t n_units, const float* g, float avg_bits, uint8_t* bits,
+                                      float* lambda_out, int32_t* status_out, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  RDKV_REQUIRE(n_inst >= 1 && n_inst <= 65535 && n_units >= 0, RDKV_ERR_INVALID_ARG, "n_inst=%d n_units=%lld", n_inst,
+               (long long)n_units);
+  RDKV_REQUIRE(std::isfinite(avg_bits) && avg_bits >= 0.0f, RDKV_ERR_INVALID_ARG, "avg_bits %f", (double)avg_bits);
+  RDKV_REQUIRE(n_units == 0 || (g && bits), RDKV_ERR_INVALID_ARG, "g or bits is NULL");
+  RDKV_REQUIRE(ws && ws_bytes >= rdkv_waterfill_workspace_bytes(n_inst, n_units), RDKV_ERR_WORKSPACE,
+               "waterfill workspace too small (%zu < %zu)", ws_bytes, rdkv_waterfill_workspace_bytes(n_inst, n_units));
+  int32_t* status = status_out ? status_out
+                               : reinterpret_cast<int32_t*>(static_cast<char*>(ws) + wf_ws_bytes(n_inst));
+  if (n_units == 0) {
+    return RDKV_OK;
+  }
+  return launch_waterfill(n_inst, n_units, g, avg_bits, bits, lambda_out, status, ws, (cudaStream_t)stream);
+}
+
+extern "C" size_t rdkv_plan_bytes(const rdkv_shape* s) {
+  if (!s || s->batch < 1 || s->h_kv < 1) return 0;
+  return (size_t)plan_layout(s->batch, s->h_kv, s->head_dim).total;
+}
+
+static size_t alloc_ws_parts(const rdkv_shape* s, size_t* wf, size_t* part, size_t* cnt, size_t* mean) {
+  const int64_t n_heads = (int64_t)s->batch * s->h_kv;
+  const int Np = s->n_tokens - s->window;
+  const int nchunk = std::max(1, ceil_div(Np, kChanChunk));
+  *wf = align_up(wf_ws_bytes(s->batch), 256);
+  *part = align_up(n_heads * nchunk * s->head_dim * 4, 256);
+  *cnt = align_up(n_heads * nchunk * 4, 256);
+  *mean = align_up(n_heads * s->head_dim * 4, 256);
+  return *wf + *part + *cnt + *mean + 256;
+}
+
+extern "C" size_t rdkv_allocate_workspace_bytes(const rdkv_shape* s) {
+  if (check_shape(s) != RDKV_OK) return 0;
+  size_t a, b, c, d;
+  return alloc_ws_parts(s, &a, &b, &c, &d);
+}
+
+extern "C" rdkv_status rdkv_allocate(const rdkv_shape* s, const float* g_tok, const float* w_chan, const void* k,
+                                     float avg_bits_v, float avg_bits_k, uint8_t* bits_tok, float* sigma_chan,
+                                     float* g_chan, uint8_t* bits_chan, void* plan, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  rdkv_status st = check_shape(s);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(std::isfinite(avg_bits_v) && avg_bits_v >= 0 && std::isfinite(avg_bits_k) && avg_bits_k >= 0,
+               RDKV_ERR_INVALID_ARG, "budgets must be finite and >= 0 (v=%f k=%f)", (double)avg_bits_v,
+               (double)avg_bits_k);
+  const int Np = s->n_tokens - s->window;
+  RDKV_REQUIRE(w_chan && k && bits_chan && sigma_chan && g_chan && plan && (Np == 0 || (g_tok && bits_tok)),
+               RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  size_t wf_b, part_b, cnt_b, mean_b;
+  const size_t need = alloc_ws_parts(s, &wf_b, &part_b, &cnt_b, &mean_b);
+  RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "allocate workspace too small (%zu < %zu)", ws_bytes, need);
+  cudaStream_t cs = (cudaStream_t)stream;
+  char* w = static_cast<char*>(ws);
+  char* wf = w;
+  float* part = reinterpret_cast<float*>(w + wf_b);
+  int* pcnt = reinterpret_cast<int*>(w + wf_b + part_b);
+  float* mean = reinterpret_cast<float*>(w + wf_b + part_b + cnt_b);
+  int32_t* status = reinterpret_cast<int32_t*>(w + wf_b + part_b + cnt_b + mean_b);  // [2]
+  const PlanLayout L = plan_layout(s->batch, s->h_kv, s->head_dim);
+  char* pl = static_cast<char*>(plan);
+  float* lam = reinterpret_cast<float*>(pl + L.lambda_off);
+  const int D = s->head_dim;
+  const int n_heads = s->batch * s->h_kv;
+
+  // step 2: V tokens, one water level per sequence over all its heads
+  RDKV_TRY_CUDA(cudaMemsetAsync(status, 0, 8, cs), "status reset");
+  if (Np > 0) {
+    st = launch_waterfill(s->batch, (int64_t)s->h_kv * Np, g_tok, avg_bits_v, bits_tok, lam, status, wf, cs);
+    if (st != RDKV_OK) return st;
+  } else {
+    RDKV_TRY_CUDA(cudaMemsetAsync(lam, 0, 4 * s->batch, cs), "lambda reset");
+  }
+  // step 3: K channel spread over the kept tokens, gains, water level
+  const int nchunk = std::max(1, ceil_div(Np, kChanChunk));
+  if (Np > 0) {
+    chan_pass<<<dim3(nchunk, n_heads), D, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np, nullptr, part,
+                                                   pcnt);
+    RDKV_CHECK_LAUNCH("channel sums");
+    chan_finish<<<n_heads, D, 0, cs>>>(part, pcnt, nchunk, D, mean, nullptr, nullptr, nullptr);
+    RDKV_CHECK_LAUNCH("channel means");
+    chan_pass<<<dim3(nchunk, n_heads), D, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np, mean, part,
+                                                   nullptr);
+    RDKV_CHECK_LAUNCH("channel deviations");
+    chan_finish<<<n_heads, D, 0, cs>>>(part, pcnt, nchunk, D, nullptr, w_chan, sigma_chan, g_chan);
+    RDKV_CHECK_LAUNCH("channel spread");
+  } else {
+    RDKV_TRY_CUDA(cudaMemsetAsync(sigma_chan, 0, 4 * (size_t)n_heads * D, cs), "sigma reset");
+    RDKV_TRY_CUDA(cudaMemsetAsync(g_chan, 0, 4 * (size_t)n_heads * D, cs), "gain reset");
+  }
+  st = launch_waterfill(s->batch, (int64_t)s->h_kv * D, g_chan, avg_bits_k, bits_chan, lam + s->batch, status + 1,
+                        wf, cs);
+  if (st != RDKV_OK) return st;
+  // TriZone plan
+  plan_heads_kernel<<<n_heads, 256, 0, cs>>>(bits_tok, bits_chan, Np, D, pl, L.heads_off, L.slots_off, L.slot_stride);
+  RDKV_CHECK_LAUNCH("plan heads");
+  plan_offsets_kernel<<<1, 32, 0, cs>>>(pl, s->batch, s->h_kv, D, L.slot_stride, L.heads_off, L.slots_off,
+                                        L.lambda_off, status, status + 1);
+  RDKV_CHECK_LAUNCH("plan offsets");
+  return RDKV_OK;
+}
+
+extern "C" rdkv_status rdkv_plan_sizes(const void* plan, rdkv_sizes* out, void* stream) {
+  RDKV_REQUIRE(plan && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  rdkv_plan_header h;
+  RDKV_TRY_CUDA(cudaMemcpyAsync(&h, plan, sizeof(h), cudaMemcpyDeviceToHost, (cudaStream_t)stream), "plan read");
+  RDKV_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "plan read sync");
+  out->zone_a_bytes = h.zone_a_bytes;
+  out->zone_b_rows = h.zone_b_rows;
+  out->index_slots = h.index_slots;
+  out->kept_tokens = h.kept_tokens;
+  out->max_tile_bytes = h.max_tile_bytes;
+  out->status = h.status;
+  out->n_heads = h.n_heads;
+  if (h.status != RDKV_OK) set_error("plan status %d: a gain was NaN, infinite or negative", h.status);
+  return (rdkv_status)h.status;
+}

@@ -1,0 +1,384 @@
+// TriZone pack and append of RDKV (gist.science/ko/paper/2605.08317,
+// section 2.3): zone A holds the kept K rows and the 2/4/8-bit V rows, packed
+// and grouped by width; zone B holds the fp16 V rows of 16-bit tokens; zone C
+// holds fp16 K and V rows of the recent window and of every decoded token.
+//
+// The quantiser is the asymmetric min-max formula of "Matematika KV Cache
+// Compression" (aistudio.id, "Solusi 3") with fp16 scale and zero:
+//   zero = fp16(min), scale = fp16(fl32(max - min) / (2^b - 1)),
+//   code = clamp(rint((x - zero) / scale), 0, 2^b - 1)   (IEEE fp32, ties to even)
+// V groups are 32 consecutive channels of a token; K groups are one channel
+// over the real tokens of a 32-token tile.  Layout rules: include/rdkv.h.
+#include "common.cuh"
+
+namespace rdkv {
+
+__device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_float(float x) { return x; }
+
+// Quantiser parameters of one group; returns false when scale is 0 (all codes 0).
+struct QParams {
+  float zero, scale;
+  uint16_t zero_h, scale_h;
+};
+__device__ __forceinline__ QParams qparams(float mn, float mx, int bits) {
+  QParams p;
+  const __half zh = __float2half_rn(mn);
+  const __half sh = __float2half_rn(__fdiv_rn(mx - mn, (float)((1 << bits) - 1)));
+  p.zero_h = __half_as_ushort(zh);
+  p.scale_h = __half_as_ushort(sh);
+  p.zero = __half2float(zh);
+  p.scale = __half2float(sh);
+  return p;
+}
+__device__ __forceinline__ uint32_t qcode(float x, const QParams& p, int bits) {
+  if (p.scale == 0.0f) return 0u;
+  const float t = rintf(__fdiv_rn(x - p.zero, p.scale));
+  const float hi = (float)((1 << bits) - 1);
+  return (uint32_t)fminf(fmaxf(t, 0.0f), hi);
+}
+
+// Bit position of element e inside a word of b-bit elements: even elements in
+// the low half-word, odd ones in the high half-word, LSB-first.
+__device__ __forceinline__ int bit_off(int e, int b) { return 16 * (e & 1) + b * (e >> 1); }
+
+// ---------------------------------------------------------------- index map
+// One block per (sequence, KV head): the kept prefix tokens of each V width, in
+// position order, at the class's slot range; pads -1.
+__global__ void __launch_bounds__(1024) index_kernel(const uint8_t* __restrict__ bits_tok, int Np,
+                                                      const void* __restrict__ plan, int32_t* __restrict__ index_map) {
+  __shared__ int warp_tot[4][32];
+  const int head = blockIdx.x;
+  const rdkv_head_plan hp = plan_heads(plan)[head];
+  const uint8_t* bt = bits_tok + (int64_t)head * Np;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+  const int chunk = ceil_div(Np, blockDim.x);
+  const int t0 = min(Np, tid * chunk), t1 = min(Np, t0 + chunk);
+  auto cls = [](int b) { return b == 2 ? 0 : b == 4 ? 1 : b == 8 ? 2 : b == 16 ? 3 : -1; };
+  int cnt[4] = {0, 0, 0, 0};
+  for (int t = t0; t < t1; ++t) {
+    const int c = cls(bt[t]);
+    if (c >= 0) ++cnt[c];
+  }
+  int base[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    int x = cnt[c];
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[c][wid] = x;
+    base[c] = x - cnt[c];
+  }
+  __syncthreads();
+  if (wid == 0) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      int x = lane < nw ? warp_tot[c][lane] : 0;
+      const int own = x;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane < nw) warp_tot[c][lane] = x - own;
+    }
+  }
+  __syncthreads();
+  int start[4];
+  int acc = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    base[c] += warp_tot[c][wid];
+    start[c] = acc;
+    acc += kTile * hp.tiles[c];
+  }
+  int32_t* out = index_map + hp.slot_off;
+  for (int t = t0; t < t1; ++t) {
+    const int c = cls(bt[t]);
+    if (c >= 0) out[start[c] + base[c]++] = t;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    for (int r = hp.n_v[c] + tid; r < kTile * hp.tiles[c]; r += blockDim.x) out[start[c] + r] = -1;
+}
+
+// ---------------------------------------------------------------- tile pack
+// One block (128 threads) per zone-A tile.
+template <typename T>
+__global__ void __launch_bounds__(128) pack_tile_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                                                         const void* __restrict__ plan,
+                                                         const int32_t* __restrict__ index_map,
+                                                         uint8_t* __restrict__ zone_a, uint16_t* __restrict__ zone_b,
+                                                         int N, int h_kv, int D) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const rdkv_plan_header* hdr = plan_header(plan);
+  const rdkv_head_plan* heads = plan_heads(plan);
+  const int64_t slot0 = (int64_t)blockIdx.x * kTile;
+  // head whose slot range holds this tile
+  int lo = 0, hi = hdr->n_heads - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (heads[mid].slot_off <= slot0) lo = mid; else hi = mid - 1;
+  }
+  const int head = lo;
+  const rdkv_head_plan hp = heads[head];
+  const int b = head / h_kv, j = head % h_kv;
+  int ti = (int)((slot0 - hp.slot_off) / kTile), cls = 0;
+  int64_t tile_off = hp.a_off;
+  int64_t brow = hp.b_row;
+  while (ti >= hp.tiles[cls]) {
+    ti -= hp.tiles[cls];
+    tile_off += (int64_t)hp.tiles[cls] * hp.tile_bytes[cls];
+    ++cls;
+  }
+  tile_off += (int64_t)ti * hp.tile_bytes[cls];
+  brow += (int64_t)kTile * ti;
+  const int vbits = 2 << cls;
+  const int n_real = min(kTile, hp.n_v[cls] - ti * kTile);
+  const int RW = hp.row_words, KS = hp.k_slots;
+  const int16_t* slot_ch = plan_slots(plan) + (int64_t)head * hdr->slot_stride;
+
+  float* Kf = reinterpret_cast<float*>(smem_raw);            // [32][D]
+  float* Vf = Kf + kTile * D;                                // [32][D]
+  uint16_t* kc = reinterpret_cast<uint16_t*>(Vf + kTile * D);  // [32][KS]
+  uint8_t* vc = reinterpret_cast<uint8_t*>(kc + kTile * KS);   // [32][D]
+  __shared__ int tok[kTile];
+  const int tid = threadIdx.x;
+  if (tid < kTile) tok[tid] = index_map[slot0 + tid];
+  __syncthreads();
+  for (int i = tid; i < kTile * D; i += blockDim.x) {
+    const int r = i / D, c = i % D;
+    const int t = tok[r];
+    const int64_t src = (((int64_t)b * N + t) * h_kv + j) * D + c;
+    Kf[i] = t >= 0 ? to_float(k[src]) : 0.0f;
+    Vf[i] = t >= 0 ? to_float(v[src]) : 0.0f;
+  }
+  __syncthreads();
+
+  uint8_t* tile = zone_a + tile_off;
+  uint16_t* kmeta = reinterpret_cast<uint16_t*>(tile + 4 * kTile * RW);
+  // K codes per slot (segment widths 16, 8, 4, 2)
+  const int s16 = 2 * hp.k_words[0];
+  for (int s = tid; s < KS; s += blockDim.x) {
+    int seg = 0, sbase = 0;
+    while (seg < 3 && s >= sbase + hp.k_words[seg] * (32 >> (4 - seg))) {
+      sbase += hp.k_words[seg] * (32 >> (4 - seg));
+      ++seg;
+    }
+    const int kb = 16 >> seg;
+    const int c = slot_ch[s];
+    if (kb == 16) {
+      for (int r = 0; r < kTile; ++r)
+        kc[r * KS + s] = (c >= 0 && r < n_real) ? half_bits(Kf[r * D + c]) : (uint16_t)0;
+      continue;
+    }
+    const int m = s - s16;  // index among the quantised slots
+    uint16_t sc_h = 0, ze_h = 0;
+    if (c >= 0) {
+      float mn = Kf[c], mx = Kf[c];
+      for (int r = 1; r < n_real; ++r) {
+        mn = fminf(mn, Kf[r * D + c]);
+        mx = fmaxf(mx, Kf[r * D + c]);
+      }
+      const QParams p = qparams(mn, mx, kb);
+      sc_h = p.scale_h;
+      ze_h = p.zero_h;
+      for (int r = 0; r < kTile; ++r) kc[r * KS + s] = r < n_real ? (uint16_t)qcode(Kf[r * D + c], p, kb) : 0;
+    } else {
+      for (int r = 0; r < kTile; ++r) kc[r * KS + s] = 0;
+    }
+    kmeta[4 * (m >> 1) + (m & 1)] = sc_h;
+    kmeta[4 * (m >> 1) + 2 + (m & 1)] = ze_h;
+  }
+  // V codes per (token, 32-channel group)
+  const int ngrp = D / kVGroup;
+  uint8_t* vcode = tile + 4 * kTile * RW + 4 * hp.meta_slots;
+  uint16_t* vmeta = reinterpret_cast<uint16_t*>(vcode + kTile * D * vbits / 8);
+  if (vbits < 16) {
+    for (int i = tid; i < kTile * ngrp; i += blockDim.x) {
+      const int r = i / ngrp, g = i % ngrp;
+      const float* x = Vf + r * D + g * kVGroup;
+      uint16_t sc_h = 0, ze_h = 0;
+      if (r < n_real) {
+        float mn = x[0], mx = x[0];
+        for (int e = 1; e < kVGroup; ++e) {
+          mn = fminf(mn, x[e]);
+          mx = fmaxf(mx, x[e]);
+        }
+        const QParams p = qparams(mn, mx, vbits);
+        sc_h = p.scale_h;
+        ze_h = p.zero_h;
+        for (int e = 0; e < kVGroup; ++e) vc[r * D + g * kVGroup + e] = (uint8_t)qcode(x[e], p, vbits);
+      } else {
+        for (int e = 0; e < kVGroup; ++e) vc[r * D + g * kVGroup + e] = 0;
+      }
+      const int p = r >> 1, mm = r & 1;
+      vmeta[(p * ngrp + g) * 4 + mm] = sc_h;
+      vmeta[(p * ngrp + g) * 4 + 2 + mm] = ze_h;
+    }
+  } else {
+    for (int i = tid; i < kTile * D; i += blockDim.x) {
+      const int r = i / D;
+      zone_b[brow * D + i] = r < n_real ? half_bits(Vf[i]) : (uint16_t)0;
+    }
+  }
+  __syncthreads();
+  // K words
+  uint32_t* kw = reinterpret_cast<uint32_t*>(tile);
+  for (int i = tid; i < kTile * RW; i += blockDim.x) {
+    const int r = i / RW, w = i % RW;
+    int seg = 0, wbase = 0, sbase = 0;
+    while (seg < 3 && w >= wbase + hp.k_words[seg]) {
+      wbase += hp.k_words[seg];
+      sbase += hp.k_words[seg] * (32 >> (4 - seg));
+      ++seg;
+    }
+    const int kb = 16 >> seg, per = 32 / kb;
+    const int s0 = sbase + (w - wbase) * per;
+    uint32_t word = 0;
+    for (int e = 0; e < per; ++e) word |= (uint32_t)kc[r * KS + s0 + e] << bit_off(e, kb);
+    kw[i] = word;
+  }
+  // V words: pair p, word w holds channels [w*16/b, (w+1)*16/b) of tokens 2p (low half) and 2p+1 (high half)
+  if (vbits < 16) {
+    uint32_t* vw = reinterpret_cast<uint32_t*>(vcode);
+    const int wpp = D * vbits / 16, per = 16 / vbits;
+    for (int i = tid; i < (kTile / 2) * wpp; i += blockDim.x) {
+      const int p = i / wpp, w = i % wpp;
+      uint32_t word = 0;
+      for (int e = 0; e < per; ++e) {
+        const int c = w * per + e;
+        word |= (uint32_t)vc[(2 * p) * D + c] << (vbits * e);
+        word |= (uint32_t)vc[(2 * p + 1) * D + c] << (16 + vbits * e);
+      }
+      vw[i] = word;
+    }
+  }
+}
+
+template <typename T>
+__global__ void window_kernel(const T* __restrict__ x, int N, int W, int h_kv, int D, int cap, int batch,
+                              uint16_t* __restrict__ zc) {
+  const int64_t total = (int64_t)batch * h_kv * W * D;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % D);
+    int64_t rest = i / D;
+    const int r = (int)(rest % W);
+    rest /= W;
+    const int j = (int)(rest % h_kv);
+    const int b = (int)(rest / h_kv);
+    zc[(((int64_t)b * h_kv + j) * cap + r) * D + c] = half_bits(to_float(x[(((int64_t)b * N + (N - W) + r) * h_kv + j) * D + c]));
+  }
+}
+
+template <typename T>
+__global__ void append_kernel(const T* __restrict__ kn, const T* __restrict__ vn, int64_t n, int D, int cap, int row,
+                              uint16_t* __restrict__ zk, uint16_t* __restrict__ zv) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int64_t head = i / D;
+  const int c = (int)(i % D);
+  const int64_t dst = (head * cap + row) * D + c;
+  zk[dst] = half_bits(to_float(kn[i]));
+  zv[dst] = half_bits(to_float(vn[i]));
+}
+
+static size_t pack_smem_bytes(int D) {
+  const int max_slots = D + kSlotPad;
+  return (size_t)2 * kTile * D * 4 + (size_t)kTile * max_slots * 2 + (size_t)kTile * D;
+}
+
+static rdkv_status check_cache(const rdkv_cache* c) {
+  RDKV_REQUIRE(c != nullptr, RDKV_ERR_INVALID_ARG, "cache is NULL");
+  rdkv_status st = check_shape(&c->shape);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(c->plan && c->zone_c_k && c->zone_c_v, RDKV_ERR_INVALID_ARG, "cache plan or zone C is NULL");
+  RDKV_REQUIRE(c->sizes.zone_a_bytes == 0 || c->zone_a, RDKV_ERR_INVALID_ARG, "zone A is NULL");
+  RDKV_REQUIRE(c->sizes.zone_b_rows == 0 || c->zone_b, RDKV_ERR_INVALID_ARG, "zone B is NULL");
+  RDKV_REQUIRE(c->sizes.index_slots == 0 || c->index_map, RDKV_ERR_INVALID_ARG, "index map is NULL");
+  RDKV_REQUIRE(c->cap_c >= c->shape.window && c->cap_c >= 0, RDKV_ERR_INVALID_ARG, "cap_c %d < window %d", c->cap_c,
+               c->shape.window);
+  RDKV_REQUIRE(c->len_c >= 0 && c->len_c <= c->cap_c, RDKV_ERR_INVALID_ARG, "len_c %d outside [0, cap_c]", c->len_c);
+  RDKV_REQUIRE(c->sizes.n_heads == c->shape.batch * c->shape.h_kv, RDKV_ERR_INVALID_ARG,
+               "cache sizes do not belong to this shape (call rdkv_plan_sizes)");
+  return RDKV_OK;
+}
+
+rdkv_status check_cache_public(const rdkv_cache* c) { return check_cache(c); }
+
+}  // namespace rdkv
+
+using namespace rdkv;
+
+extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v, const uint8_t* bits_tok,
+                                 const uint8_t* bits_chan, void* stream) {
+  rdkv_status st = check_cache(cache);
+  if (st != RDKV_OK) return st;
+  const rdkv_shape& s = cache->shape;
+  const int N = s.n_tokens, D = s.head_dim, W = s.window, Np = N - W;
+  RDKV_REQUIRE(k && v && (Np == 0 || bits_tok) && bits_chan, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  (void)bits_chan;  // the channel widths reach the pack through the plan's slot table
+  cudaStream_t cs = (cudaStream_t)stream;
+  const int n_heads = s.batch * s.h_kv;
+  if (Np > 0 && cache->sizes.index_slots > 0) {
+    index_kernel<<<n_heads, 1024, 0, cs>>>(bits_tok, Np, cache->plan, cache->index_map);
+    RDKV_CHECK_LAUNCH("index map");
+    const int64_t n_tiles = cache->sizes.index_slots / kTile;
+    const size_t smem = pack_smem_bytes(D);
+    RDKV_REQUIRE(n_tiles <= 0x7fffffff, RDKV_ERR_UNSUPPORTED, "too many tiles");
+    if (s.dtype == RDKV_F16) {
+      RDKV_TRY_CUDA(cudaFuncSetAttribute(pack_tile_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                    "pack smem");
+      pack_tile_kernel<__half><<<(unsigned)n_tiles, 128, smem, cs>>>(
+          static_cast<const __half*>(k), static_cast<const __half*>(v), cache->plan, cache->index_map, cache->zone_a,
+          cache->zone_b, N, s.h_kv, D);
+    } else {
+      RDKV_TRY_CUDA(cudaFuncSetAttribute(pack_tile_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                    "pack smem");
+      pack_tile_kernel<float><<<(unsigned)n_tiles, 128, smem, cs>>>(
+          static_cast<const float*>(k), static_cast<const float*>(v), cache->plan, cache->index_map, cache->zone_a,
+          cache->zone_b, N, s.h_kv, D);
+    }
+    RDKV_CHECK_LAUNCH("tile pack");
+  }
+  if (W > 0) {
+    const int64_t total = (int64_t)s.batch * s.h_kv * W * D;
+    const unsigned grid = (unsigned)std::min<int64_t>(ceil_div64(total, 256), 4096);
+    if (s.dtype == RDKV_F16) {
+      window_kernel<__half><<<grid, 256, 0, cs>>>(static_cast<const __half*>(k), N, W, s.h_kv, D, cache->cap_c, s.batch,
+                                                  cache->zone_c_k);
+      window_kernel<__half><<<grid, 256, 0, cs>>>(static_cast<const __half*>(v), N, W, s.h_kv, D, cache->cap_c, s.batch,
+                                                  cache->zone_c_v);
+    } else {
+      window_kernel<float><<<grid, 256, 0, cs>>>(static_cast<const float*>(k), N, W, s.h_kv, D, cache->cap_c, s.batch,
+                                                 cache->zone_c_k);
+      window_kernel<float><<<grid, 256, 0, cs>>>(static_cast<const float*>(v), N, W, s.h_kv, D, cache->cap_c, s.batch,
+                                                 cache->zone_c_v);
+    }
+    RDKV_CHECK_LAUNCH("zone C window");
+  }
+  cache->len_c = W;
+  return RDKV_OK;
+}
+
+extern "C" rdkv_status rdkv_append(rdkv_cache* cache, const void* k_new, const void* v_new, void* stream) {
+  rdkv_status st = check_cache(cache);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(k_new && v_new, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  RDKV_REQUIRE(cache->len_c < cache->cap_c, RDKV_ERR_CAPACITY, "zone C is full (%d rows)", cache->cap_c);
+  const rdkv_shape& s = cache->shape;
+  const int64_t n = (int64_t)s.batch * s.h_kv * s.head_dim;
+  cudaStream_t cs = (cudaStream_t)stream;
+  if (s.dtype == RDKV_F16)
+    append_kernel<__half><<<(unsigned)ceil_div64(n, 256), 256, 0, cs>>>(
+        static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), n, s.head_dim, cache->cap_c,
+        cache->len_c, cache->zone_c_k, cache->zone_c_v);
+  else
+    append_kernel<float><<<(unsigned)ceil_div64(n, 256), 256, 0, cs>>>(
+        static_cast<const float*>(k_new), static_cast<const float*>(v_new), n, s.head_dim, cache->cap_c, cache->len_c,
+        cache->zone_c_k, cache->zone_c_v);
+  RDKV_CHECK_LAUNCH("append");
+  cache->len_c += 1;
+  return RDKV_OK;
+}

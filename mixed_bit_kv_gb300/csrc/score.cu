@@ -1,0 +1,255 @@
+// Distortion weights of RDKV (gist.science/ko/paper/2605.08317, section 2.1),
+// computed once after prefill on the full cache (section 2.2, step 1):
+//   w_t  = sum over query positions tau >= t and the G query heads of the
+//          group of the causal softmax a_{tau,h,t}        (V-cache weight)
+//   w_c  = |Q_:,c| |K_:,c| / sqrt(d)                      (K-cache weight)
+// plus the spread sigma_t of each V row and the gain g_t = w_t * sigma_t of
+// the objective's V units.
+//
+// w_t needs the normaliser of every softmax row before any column can be
+// summed, so the scorer runs two passes over the causal pairs: pass 1 keeps
+// one log-sum-exp per query row; pass 2 recomputes each logit, turns it into
+// a probability with that row's normaliser and sums the columns.  This file
+// holds the CUDA-core passes (exact fp32 logits) and the row/column
+// reductions.
+#include <cmath>
+
+#include "common.cuh"
+
+namespace rdkv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSTile = 32;      // query rows / keys per block in the CUDA-core passes
+constexpr int kColChunk = 256;  // rows per partial column sum
+
+// ---------------------------------------------------------------- sigma of V rows: one warp per row
+__global__ void value_spread_kernel(const void* __restrict__ v, int dtype, int64_t n_rows, int h_kv, int N, int D,
+                                    float* __restrict__ sigma) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // (b, t, j) flattened
+  if (row >= n_rows) return;
+  float x[4];
+  const int per = D / 32;
+  float s = 0.f;
+  for (int i = 0; i < per; ++i) {
+    x[i] = load_as_float(v, row * D + lane + 32 * i, dtype);
+    s += x[i];
+  }
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mean = s / (float)D;
+  float m2 = 0.f;
+  for (int i = 0; i < per; ++i) m2 += (x[i] - mean) * (x[i] - mean);
+  for (int o = 16; o; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+  if (lane == 0) {
+    const int j = (int)(row % h_kv);
+    const int64_t bt = row / h_kv;
+    const int t = (int)(bt % N);
+    const int64_t b = bt / N;
+    sigma[(b * h_kv + j) * N + t] = sqrtf(m2 / (float)D);
+  }
+}
+
+// ---------------------------------------------------------------- column sums of squares (for w_c)
+// part[b][chunk][col] = sum over the chunk's rows of x[b][row][col]^2, cols = H*D.
+__global__ void colsq_kernel(const void* __restrict__ x, int dtype, int N, int cols, float* __restrict__ part) {
+  const int b = blockIdx.z, chunk = blockIdx.y;
+  const int col = blockIdx.x * blockDim.x + threadIdx.x;
+  if (col >= cols) return;
+  const int r0 = chunk * kColChunk, r1 = min(N, r0 + kColChunk);
+  float acc = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const float v = load_as_float(x, ((int64_t)b * N + r) * cols + col, dtype);
+    acc += v * v;
+  }
+  part[((int64_t)b * gridDim.y + chunk) * cols + col] = acc;
+}
+
+__global__ void channel_weight_kernel(const float* __restrict__ qpart, const float* __restrict__ kpart, int nchunk,
+                                      int h_q, int h_kv, int D, float* __restrict__ w_chan) {
+  const int head = blockIdx.x;  // b * h_kv + j
+  const int b = head / h_kv, j = head % h_kv;
+  const int c = threadIdx.x;
+  const int G = h_q / h_kv;
+  double qs = 0.0, ks = 0.0;
+  for (int i = 0; i < nchunk; ++i) {
+    const float* qp = qpart + ((int64_t)b * nchunk + i) * h_q * D;
+    for (int h = j * G; h < (j + 1) * G; ++h) qs += (double)qp[h * D + c];
+    ks += (double)kpart[((int64_t)b * nchunk + i) * h_kv * D + j * D + c];
+  }
+  w_chan[head * D + c] = (float)(sqrt(qs) * sqrt(ks) / sqrt((double)D));
+}
+
+// ---------------------------------------------------------------- CUDA-core pass 1: row log-sum-exp (base 2)
+// Block: 32 query rows of one (b, h); 128 threads, 4 per row, each thread
+// takes 8 consecutive keys of every 32-key tile.
+__global__ void __launch_bounds__(128) lse_simt_kernel(const void* __restrict__ q, const void* __restrict__ k,
+                                                        int dtype, int N, int h_q, int h_kv, int D,
+                                                        float* __restrict__ lse2) {
+  extern __shared__ float sm[];
+  float* Qs = sm;                      // [32][D + 1]
+  float* Kt = sm + kSTile * (D + 1);   // [D][32 + 4] (keys contiguous)
+  const int b = blockIdx.z, h = blockIdx.y, r0 = blockIdx.x * kSTile;
+  const int j = h / (h_q / h_kv);
+  const int tid = threadIdx.x, row = tid >> 2, sub = tid & 3;
+  const float sc = kLog2e / sqrtf((float)D);
+  for (int i = tid; i < kSTile * D; i += blockDim.x) {
+    const int r = i / D, d = i % D;
+    Qs[r * (D + 1) + d] = (r0 + r < N) ? load_as_float(q, (((int64_t)b * N + r0 + r) * h_q + h) * D + d, dtype) : 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  const int tau = r0 + row;
+  const int n_tiles = ceil_div(min(N, r0 + kSTile), kSTile);
+  for (int kt = 0; kt < n_tiles; ++kt) {
+    __syncthreads();
+    for (int i = tid; i < kSTile * D; i += blockDim.x) {
+      const int key = i / D, d = i % D, t = kt * kSTile + key;
+      Kt[d * (kSTile + 4) + key] = (t < N) ? load_as_float(k, (((int64_t)b * N + t) * h_kv + j) * D + d, dtype) : 0.f;
+    }
+    __syncthreads();
+    float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int d = 0; d < D; ++d) {
+      const float qv = Qs[row * (D + 1) + d];
+      const float4 k0 = *reinterpret_cast<const float4*>(&Kt[d * (kSTile + 4) + 8 * sub]);
+      const float4 k1 = *reinterpret_cast<const float4*>(&Kt[d * (kSTile + 4) + 8 * sub + 4]);
+      s[0] += qv * k0.x; s[1] += qv * k0.y; s[2] += qv * k0.z; s[3] += qv * k0.w;
+      s[4] += qv * k1.x; s[5] += qv * k1.y; s[6] += qv * k1.z; s[7] += qv * k1.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = kt * kSTile + 8 * sub + i;
+      if (t <= tau && tau < N) {
+        const float x = s[i] * sc;
+        if (x > m) {
+          l = l * exp2f(m - x) + 1.f;
+          m = x;
+        } else {
+          l += exp2f(x - m);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < 4; o <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    const float mm = fmaxf(m, m2);
+    l = (m == -INFINITY ? 0.f : l * exp2f(m - mm)) + (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - mm));
+    m = mm;
+  }
+  if (sub == 0 && tau < N) lse2[((int64_t)b * h_q + h) * N + tau] = m + log2f(l);
+}
+
+// ---------------------------------------------------------------- CUDA-core pass 2: column sums
+// Block: 32 keys of one (b, j); sweeps the query rows tau >= key block start
+// for the G heads of the group.  4 threads per key, 8 rows each per tile.
+__global__ void __launch_bounds__(128) colsum_simt_kernel(const void* __restrict__ q, const void* __restrict__ k,
+                                                           int dtype, int N, int Np, int h_q, int h_kv, int D,
+                                                           const float* __restrict__ lse2,
+                                                           const float* __restrict__ sigma,
+                                                           float* __restrict__ w_tok, float* __restrict__ g_tok) {
+  extern __shared__ float sm[];
+  float* Ks = sm;                      // [32][D + 1]
+  float* Qt = sm + kSTile * (D + 1);   // [D][32 + 4] (rows contiguous)
+  float* L = Qt + D * (kSTile + 4);    // [32]
+  const int b = blockIdx.z, j = blockIdx.y, t0 = blockIdx.x * kSTile;
+  const int G = h_q / h_kv;
+  const int tid = threadIdx.x, key = tid >> 2, sub = tid & 3;
+  const float sc = kLog2e / sqrtf((float)D);
+  for (int i = tid; i < kSTile * D; i += blockDim.x) {
+    const int r = i / D, d = i % D;
+    Ks[r * (D + 1) + d] = (t0 + r < N) ? load_as_float(k, (((int64_t)b * N + t0 + r) * h_kv + j) * D + d, dtype) : 0.f;
+  }
+  const int t = t0 + key;
+  float acc = 0.f;
+  for (int h = j * G; h < (j + 1) * G; ++h) {
+    for (int r0 = t0; r0 < N; r0 += kSTile) {
+      __syncthreads();
+      for (int i = tid; i < kSTile * D; i += blockDim.x) {
+        const int r = i / D, d = i % D, tau = r0 + r;
+        Qt[d * (kSTile + 4) + r] = (tau < N) ? load_as_float(q, (((int64_t)b * N + tau) * h_q + h) * D + d, dtype) : 0.f;
+      }
+      if (tid < kSTile) L[tid] = (r0 + tid < N) ? lse2[((int64_t)b * h_q + h) * N + r0 + tid] : 0.f;
+      __syncthreads();
+      float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int d = 0; d < D; ++d) {
+        const float kv = Ks[key * (D + 1) + d];
+        const float4 q0 = *reinterpret_cast<const float4*>(&Qt[d * (kSTile + 4) + 8 * sub]);
+        const float4 q1 = *reinterpret_cast<const float4*>(&Qt[d * (kSTile + 4) + 8 * sub + 4]);
+        s[0] += kv * q0.x; s[1] += kv * q0.y; s[2] += kv * q0.z; s[3] += kv * q0.w;
+        s[4] += kv * q1.x; s[5] += kv * q1.y; s[6] += kv * q1.z; s[7] += kv * q1.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int tau = r0 + 8 * sub + i;
+        if (tau >= t && tau < N) acc += exp2f(s[i] * sc - L[8 * sub + i]);
+      }
+    }
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  if (sub == 0 && t < N) {
+    const int64_t o = ((int64_t)b * h_kv + j) * N + t;
+    w_tok[o] = acc;
+    if (t < Np) g_tok[((int64_t)b * h_kv + j) * Np + t] = acc * sigma[o];
+  }
+}
+
+static size_t score_ws_parts(const rdkv_shape* s, size_t* lse, size_t* qp, size_t* kp) {
+  const int nchunk = ceil_div(s->n_tokens, kColChunk);
+  *lse = align_up((int64_t)s->batch * s->h_q * s->n_tokens * 4, 256);
+  *qp = align_up((int64_t)s->batch * nchunk * s->h_q * s->head_dim * 4, 256);
+  *kp = align_up((int64_t)s->batch * nchunk * s->h_kv * s->head_dim * 4, 256);
+  return *lse + *qp + *kp;
+}
+
+}  // namespace rdkv
+
+using namespace rdkv;
+
+extern "C" size_t rdkv_score_workspace_bytes(const rdkv_shape* s) {
+  if (check_shape(s) != RDKV_OK) return 0;
+  size_t a, b, c;
+  return score_ws_parts(s, &a, &b, &c);
+}
+
+extern "C" rdkv_status rdkv_score(const rdkv_shape* s, const void* q, const void* k, const void* v, float* w_tok,
+                                  float* w_chan, float* sigma_tok, float* g_tok, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  rdkv_status st = check_shape(s);
+  if (st != RDKV_OK) return st;
+  const int N = s->n_tokens, D = s->head_dim, Np = N - s->window;
+  RDKV_REQUIRE(q && k && v && w_tok && w_chan && sigma_tok && (Np == 0 || g_tok), RDKV_ERR_INVALID_ARG,
+               "NULL pointer argument");
+  size_t lse_b, qp_b, kp_b;
+  const size_t need = score_ws_parts(s, &lse_b, &qp_b, &kp_b);
+  RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "score workspace too small (%zu < %zu)", ws_bytes, need);
+  cudaStream_t cs = (cudaStream_t)stream;
+  char* w = static_cast<char*>(ws);
+  float* lse2 = reinterpret_cast<float*>(w);
+  float* qpart = reinterpret_cast<float*>(w + lse_b);
+  float* kpart = reinterpret_cast<float*>(w + lse_b + qp_b);
+
+  // sigma of V rows
+  const int64_t rows = (int64_t)s->batch * N * s->h_kv;
+  value_spread_kernel<<<(unsigned)ceil_div64(rows * 32, 256), 256, 0, cs>>>(v, s->dtype, rows, s->h_kv, N, D,
+                                                                            sigma_tok);
+  RDKV_CHECK_LAUNCH("value spread");
+  // channel weights
+  const int nchunk = ceil_div(N, kColChunk);
+  colsq_kernel<<<dim3(ceil_div(s->h_q * D, 256), nchunk, s->batch), 256, 0, cs>>>(q, s->dtype, N, s->h_q * D, qpart);
+  RDKV_CHECK_LAUNCH("query column norms");
+  colsq_kernel<<<dim3(ceil_div(s->h_kv * D, 256), nchunk, s->batch), 256, 0, cs>>>(k, s->dtype, N, s->h_kv * D,
+                                                                                   kpart);
+  RDKV_CHECK_LAUNCH("key column norms");
+  channel_weight_kernel<<<s->batch * s->h_kv, D, 0, cs>>>(qpart, kpart, nchunk, s->h_q, s->h_kv, D, w_chan);
+  RDKV_CHECK_LAUNCH("channel weights");
+  // token weights
+  const size_t smem = (size_t)(kSTile * (D + 1) + D * (kSTile + 4) + kSTile) * 4;
+  lse_simt_kernel<<<dim3(ceil_div(N, kSTile), s->h_q, s->batch), 128, smem, cs>>>(q, k, s->dtype, N, s->h_q, s->h_kv,
+                                                                                    D, lse2);
+  RDKV_CHECK_LAUNCH("row log-sum-exp");
+  colsum_simt_kernel<<<dim3(ceil_div(N, kSTile), s->h_kv, s->batch), 128, smem, cs>>>(
+      q, k, s->dtype, N, Np, s->h_q, s->h_kv, D, lse2, sigma_tok, w_tok, g_tok);
+  RDKV_CHECK_LAUNCH("attention column sums");
+  return RDKV_OK;
+}

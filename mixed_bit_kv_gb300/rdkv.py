@@ -1,0 +1,248 @@
+"""Python binding of librdkv (include/rdkv.h): the same entry points, argument marshalling only.
+
+Torch supplies device memory and the current CUDA stream; every computation
+runs in the library's CUDA kernels.  Loading fails loudly when the library is
+missing: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librdkv.so")
+
+RDKV_OK, RDKV_ERR_INVALID_ARG, RDKV_ERR_UNSUPPORTED, RDKV_ERR_CAPACITY = 0, 1, 2, 3
+RDKV_ERR_CUDA, RDKV_ERR_TIMEOUT, RDKV_ERR_WORKSPACE = 4, 5, 6
+RDKV_F16, RDKV_F32 = 0, 1
+
+EXPORTED = (
+    "rdkv_last_error_string", "rdkv_version",
+    "rdkv_score_workspace_bytes", "rdkv_score",
+    "rdkv_waterfill_workspace_bytes", "rdkv_waterfill",
+    "rdkv_plan_bytes", "rdkv_allocate_workspace_bytes", "rdkv_allocate", "rdkv_plan_sizes",
+    "rdkv_pack", "rdkv_append",
+    "rdkv_decode_workspace_bytes", "rdkv_decode_attn", "rdkv_decode_status",
+)
+
+
+class RDKVError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"rdkv status {code}: {msg}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("batch", "n_tokens", "h_q", "h_kv", "head_dim", "window", "dtype")]
+
+
+class Sizes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("zone_a_bytes", "zone_b_rows", "index_slots", "kept_tokens",
+                                               "max_tile_bytes")] + [("status", ctypes.c_int32),
+                                                                     ("n_heads", ctypes.c_int32)]
+
+
+class CacheStruct(ctypes.Structure):
+    _fields_ = [("shape", Shape), ("plan", ctypes.c_void_p), ("zone_a", ctypes.c_void_p),
+                ("zone_b", ctypes.c_void_p), ("zone_c_k", ctypes.c_void_p), ("zone_c_v", ctypes.c_void_p),
+                ("index_map", ctypes.c_void_p), ("cap_c", ctypes.c_int32), ("len_c", ctypes.c_int32),
+                ("sizes", Sizes)]
+
+
+HEAD_PLAN_DTYPE = [("n_v", "<i4", 4), ("tiles", "<i4", 4), ("n_k", "<i4", 5), ("k_words", "<i4", 4),
+                   ("row_words", "<i4"), ("k_slots", "<i4"), ("meta_slots", "<i4"), ("tile_bytes", "<i4", 4),
+                   ("a_off", "<i8"), ("a_bytes", "<i8"), ("b_row", "<i8"), ("slot_off", "<i8")]
+PLAN_HEADER_DTYPE = [("status", "<i4"), ("n_heads", "<i4"), ("batch", "<i4"), ("h_kv", "<i4"),
+                     ("head_dim", "<i4"), ("slot_stride", "<i4"), ("heads_off", "<i8"), ("slots_off", "<i8"),
+                     ("lambda_off", "<i8"), ("zone_a_bytes", "<i8"), ("zone_b_rows", "<i8"),
+                     ("index_slots", "<i8"), ("kept_tokens", "<i8"), ("max_tile_bytes", "<i8")]
+
+_lib = None
+_P = ctypes.c_void_p
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RDKVError(-1, f"{LIB_PATH} is missing: build it with mixed_bit_kv_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        sp, szp, cp = ctypes.POINTER(Shape), ctypes.POINTER(Sizes), ctypes.POINTER(CacheStruct)
+        sig = {
+            "rdkv_last_error_string": (ctypes.c_char_p, []),
+            "rdkv_version": (ctypes.c_int32, []),
+            "rdkv_score_workspace_bytes": (ctypes.c_size_t, [sp]),
+            "rdkv_score": (ctypes.c_int, [sp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+            "rdkv_waterfill_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int64]),
+            "rdkv_waterfill": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int64, _P, ctypes.c_float, _P, _P, _P, _P,
+                                              ctypes.c_size_t, _P]),
+            "rdkv_plan_bytes": (ctypes.c_size_t, [sp]),
+            "rdkv_allocate_workspace_bytes": (ctypes.c_size_t, [sp]),
+            "rdkv_allocate": (ctypes.c_int, [sp, _P, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P, _P, _P, _P, _P,
+                                             ctypes.c_size_t, _P]),
+            "rdkv_plan_sizes": (ctypes.c_int, [_P, szp, _P]),
+            "rdkv_pack": (ctypes.c_int, [cp, _P, _P, _P, _P, _P]),
+            "rdkv_append": (ctypes.c_int, [cp, _P, _P, _P]),
+            "rdkv_decode_workspace_bytes": (ctypes.c_size_t, [cp]),
+            "rdkv_decode_attn": (ctypes.c_int, [cp, _P, _P, _P, ctypes.c_size_t, _P]),
+            "rdkv_decode_status": (ctypes.c_int, [cp, _P, _P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def _check(code):
+    if code != RDKV_OK:
+        raise RDKVError(code, lib().rdkv_last_error_string().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ws(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def make_shape(batch, n_tokens, h_q, h_kv, head_dim, window, dtype):
+    code = RDKV_F16 if dtype in (torch.float16, "f16") else RDKV_F32
+    return Shape(batch, n_tokens, h_q, h_kv, head_dim, window, code)
+
+
+def shape_of(q, k, window):
+    """Shape of prefill tensors q [B, N, H_q, D], k [B, N, H_kv, D]."""
+    B, N, Hq, D = q.shape
+    return make_shape(B, N, Hq, k.shape[2], D, window, q.dtype)
+
+
+# ---------------------------------------------------------------- step 1
+def rdkv_score(shape, q, k, v, stream=None):
+    dev = q.device
+    B, N, Hkv, D = shape.batch, shape.n_tokens, shape.h_kv, shape.head_dim
+    Np = N - shape.window
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(w_tok=torch.empty(B, Hkv, N, **f32), w_chan=torch.empty(B, Hkv, D, **f32),
+               sigma_tok=torch.empty(B, Hkv, N, **f32), g_tok=torch.empty(B, Hkv, max(Np, 0), **f32))
+    L = lib()
+    nb = L.rdkv_score_workspace_bytes(ctypes.byref(shape))
+    ws = _ws(nb, dev)
+    _check(L.rdkv_score(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out["w_tok"]), _ptr(out["w_chan"]),
+                        _ptr(out["sigma_tok"]), _ptr(out["g_tok"]), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- steps 2 and 3
+def rdkv_waterfill(g, avg_bits, stream=None):
+    """g [n_inst, n_units] fp32 on the GPU -> (bits uint8, lambda fp32 [n_inst], status int32 [1])."""
+    n_inst, n_units = g.shape
+    dev = g.device
+    bits = torch.empty(n_inst, n_units, dtype=torch.uint8, device=dev)
+    lam = torch.empty(n_inst, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    L = lib()
+    ws = _ws(L.rdkv_waterfill_workspace_bytes(n_inst, n_units), dev)
+    _check(L.rdkv_waterfill(n_inst, n_units, _ptr(g), float(avg_bits), _ptr(bits), _ptr(lam), _ptr(status),
+                            _ptr(ws), ws.numel(), _stream(stream)))
+    return bits, lam, status
+
+
+def rdkv_allocate(shape, g_tok, w_chan, k, avg_bits_v, avg_bits_k, stream=None):
+    dev = k.device
+    B, Hkv, D = shape.batch, shape.h_kv, shape.head_dim
+    Np = shape.n_tokens - shape.window
+    L = lib()
+    out = dict(bits_tok=torch.empty(B, Hkv, max(Np, 0), dtype=torch.uint8, device=dev),
+               sigma_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+               g_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+               bits_chan=torch.empty(B, Hkv, D, dtype=torch.uint8, device=dev),
+               plan=torch.zeros(L.rdkv_plan_bytes(ctypes.byref(shape)), dtype=torch.uint8, device=dev))
+    ws = _ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), dev)
+    _check(L.rdkv_allocate(ctypes.byref(shape), _ptr(g_tok), _ptr(w_chan), _ptr(k), float(avg_bits_v),
+                           float(avg_bits_k), _ptr(out["bits_tok"]), _ptr(out["sigma_chan"]), _ptr(out["g_chan"]),
+                           _ptr(out["bits_chan"]), _ptr(out["plan"]), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def rdkv_plan_sizes(plan, stream=None):
+    sz = Sizes()
+    _check(lib().rdkv_plan_sizes(_ptr(plan), ctypes.byref(sz), _stream(stream)))
+    return sz
+
+
+# ---------------------------------------------------------------- TriZone cache
+class Cache:
+    """Device buffers of one packed TriZone cache plus the C struct that points at them."""
+
+    def __init__(self, shape, plan, sizes, cap_c, device):
+        D = shape.head_dim
+        self.shape, self.plan, self.sizes = shape, plan, sizes
+        self.zone_a = torch.zeros(max(sizes.zone_a_bytes, 16), dtype=torch.uint8, device=device)
+        self.zone_b = torch.zeros(max(sizes.zone_b_rows, 1), D, dtype=torch.float16, device=device)
+        self.zone_c_k = torch.zeros(shape.batch, shape.h_kv, cap_c, D, dtype=torch.float16, device=device)
+        self.zone_c_v = torch.zeros_like(self.zone_c_k)
+        self.index_map = torch.zeros(max(sizes.index_slots, 1), dtype=torch.int32, device=device)
+        self.c = CacheStruct(shape, plan.data_ptr(), self.zone_a.data_ptr(), self.zone_b.data_ptr(),
+                             self.zone_c_k.data_ptr(), self.zone_c_v.data_ptr(), self.index_map.data_ptr(),
+                             cap_c, 0, sizes)
+        self._ws = None
+
+    @property
+    def len_c(self):
+        return self.c.len_c
+
+    def decode_workspace(self):
+        nb = lib().rdkv_decode_workspace_bytes(ctypes.byref(self.c))
+        if self._ws is None or self._ws.numel() < nb:
+            self._ws = _ws(nb, self.zone_a.device)
+        return self._ws
+
+
+def rdkv_pack(shape, plan, k, v, bits_tok, bits_chan, cap_c, stream=None, sizes=None):
+    sizes = sizes if sizes is not None else rdkv_plan_sizes(plan, stream)
+    cache = Cache(shape, plan, sizes, cap_c, k.device)
+    _check(lib().rdkv_pack(ctypes.byref(cache.c), _ptr(k), _ptr(v), _ptr(bits_tok), _ptr(bits_chan),
+                           _stream(stream)))
+    return cache
+
+
+def rdkv_append(cache, k_new, v_new, stream=None):
+    _check(lib().rdkv_append(ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new), _stream(stream)))
+
+
+def rdkv_decode_attn(cache, q, out=None, stream=None):
+    B, Hq, D = q.shape
+    out = out if out is not None else torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    ws = cache.decode_workspace()
+    _check(lib().rdkv_decode_attn(ctypes.byref(cache.c), _ptr(q), _ptr(out), _ptr(ws), ws.numel(),
+                                  _stream(stream)))
+    return out
+
+
+def rdkv_decode_status(cache, stream=None):
+    ws = cache.decode_workspace()
+    return lib().rdkv_decode_status(ctypes.byref(cache.c), _ptr(ws), _stream(stream))
+
+
+# ---------------------------------------------------------------- plan inspection (tests)
+def read_plan(plan):
+    """Host view of a device plan buffer: header dict, head records, slot table, lambdas."""
+    import numpy as np
+    raw = plan.cpu().numpy()
+    hdr = np.frombuffer(raw.tobytes(), dtype=np.dtype(PLAN_HEADER_DTYPE), count=1)[0]
+    n = int(hdr["n_heads"])
+    heads = np.frombuffer(raw.tobytes(), dtype=np.dtype(HEAD_PLAN_DTYPE), count=n, offset=int(hdr["heads_off"]))
+    slots = np.frombuffer(raw.tobytes(), dtype="<i2", count=n * int(hdr["slot_stride"]),
+                          offset=int(hdr["slots_off"])).reshape(n, int(hdr["slot_stride"]))
+    lam = np.frombuffer(raw.tobytes(), dtype="<f4", count=2 * int(hdr["batch"]), offset=int(hdr["lambda_off"]))
+    return hdr, heads, slots, lam

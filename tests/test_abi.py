@@ -1,0 +1,93 @@
+"""The C-ABI library loads without a GPU, exports every declared entry point,
+and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixed_bit_kv_gb300 import rdkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    return rdkv.lib()
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(rdkv_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = _declared()
+    assert len(declared) >= 15
+    for name in sorted(declared):
+        assert hasattr(L, name), name
+    assert set(rdkv.EXPORTED) <= declared
+
+
+def test_version_and_struct_sizes(L):
+    assert L.rdkv_version() >= 1
+    assert ctypes.sizeof(rdkv.Shape) == 28
+    assert ctypes.sizeof(rdkv.Sizes) == 48
+    import numpy as np
+    assert np.dtype(rdkv.HEAD_PLAN_DTYPE).itemsize == 128
+    assert np.dtype(rdkv.PLAN_HEADER_DTYPE).itemsize == 88
+
+
+def test_workspace_queries_are_host_only(L):
+    s = rdkv.make_shape(1, 32768, 24, 8, 128, 128, "f16")
+    assert L.rdkv_score_workspace_bytes(ctypes.byref(s)) > 0
+    assert L.rdkv_allocate_workspace_bytes(ctypes.byref(s)) > 0
+    assert L.rdkv_plan_bytes(ctypes.byref(s)) > 8 * 128
+    assert L.rdkv_waterfill_workspace_bytes(4, 1000) > 0
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 96, rdkv.RDKV_ERR_UNSUPPORTED),
+    ("h_q", 25, rdkv.RDKV_ERR_INVALID_ARG),
+    ("window", 40000, rdkv.RDKV_ERR_INVALID_ARG),
+    ("dtype", 7, rdkv.RDKV_ERR_UNSUPPORTED),
+    ("h_q", 80, rdkv.RDKV_ERR_UNSUPPORTED),
+])
+def test_bad_shapes_are_rejected_before_any_launch(L, field, value, code):
+    s = rdkv.make_shape(1, 32768, 24, 8, 128, 128, "f16")
+    setattr(s, field, value)
+    fake = ctypes.c_void_p(16)
+    r = L.rdkv_score(ctypes.byref(s), fake, fake, fake, fake, fake, fake, fake, fake, 1 << 40, None)
+    assert r == code
+    assert L.rdkv_last_error_string()
+
+
+def test_null_and_budget_errors(L):
+    s = rdkv.make_shape(1, 1024, 4, 1, 64, 32, "f32")
+    r = L.rdkv_score(ctypes.byref(s), None, None, None, None, None, None, None, None, 0, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(16)
+    r = L.rdkv_waterfill(1, 10, fake, ctypes.c_float(float("nan")), fake, None, None, fake, 1 << 20, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+    r = L.rdkv_waterfill(1, 10, fake, ctypes.c_float(-1.0), fake, None, None, fake, 1 << 20, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+    r = L.rdkv_waterfill(1, 10, fake, ctypes.c_float(2.0), fake, None, None, fake, 8, None)
+    assert r == rdkv.RDKV_ERR_WORKSPACE
+
+
+def test_append_capacity_is_checked_on_the_host(L):
+    s = rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16")
+    sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 1)
+    fake = ctypes.c_void_p(256)
+    c = rdkv.CacheStruct(s, 256, None, None, 256, 256, None, 8, 8, sizes)
+    r = L.rdkv_append(ctypes.byref(c), fake, fake, None)
+    assert r == rdkv.RDKV_ERR_CAPACITY
+    assert c.len_c == 8

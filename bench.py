@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Benchmark of the RDKV hot path (score -> allocate -> TriZone pack -> append + decode) on GB300.
+
+One step = compress every layer of a stack of independently generated layers
+of the chosen workload (default: the Llama-3.2-3B-shaped layer, N = 32768,
+28 layers like the model), then run the workload's decode steps over all
+layers (append the new token, attend).  Inputs are resident in HBM when the
+timed region starts; the decode phase is replayed from a captured CUDA graph.
+The working set (prefill inputs ~9 GB, packed caches ~0.7 GB) is larger than
+L2, and each decode call reads a cache last touched 27 calls earlier.
+
+Rank 0 prints one JSON line.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import resource
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TriZone decode attn HBM GB/s (scoring TFLOP/s, decode us/step alongside)"
+UNIT = "GB/s"
+
+
+# ---------------------------------------------------------------- environment
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    sm_max_mhz=float(d.get("sm_max_mhz", 2070.0)), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, sm_max_mhz=2070.0,
+                source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running (SM clock, max clock, throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- algorithmic work
+def decode_bytes_per_call(heads, D, h_q, batch, len_c):
+    """Bytes one decode call must move: zone-A payload and metadata of real tokens
+    and channels, zone-B rows of real tokens, len_c zone-C rows per head, q in and
+    out.  Padding excluded."""
+    total = 0.0
+    for hp in heads:
+        n16k, n8k, n4k, n2k, _ = (int(x) for x in hp["n_k"])
+        ntok = int(np.sum(hp["n_v"]))
+        kq = n8k + n4k + n2k
+        total += ntok * (2 * n16k + (8 * n8k + 4 * n4k + 2 * n2k) / 8) + 4 * kq * ntok / 32
+        for n, b in zip(hp["n_v"], (2, 4, 8, 16)):
+            total += int(n) * (D * b / 8 + (4 * D / 32 if b < 16 else 0))
+        total += len_c * 4 * D
+    return total + batch * h_q * D * (2 + 4)
+
+
+def scorer_flops(w):
+    """2 passes x 2*D flops per causal (query head, row, key) pair."""
+    return 2 * 2 * w.head_dim * w.h_q * w.batch * w.n_tokens * (w.n_tokens + 1) / 2
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, ws, rank, local):
+    from mixed_bit_kv_gb300 import rdkv, synth
+
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    L = args.layers
+    S = args.decode_steps if args.decode_steps is not None else w.decode_steps
+    avg = w.budgets[0] if args.budget is None else args.budget
+    first_seq = rank * w.batch
+    shape = rdkv.make_shape(w.batch, w.n_tokens, w.h_q, w.h_kv, w.head_dim, w.window, w.dtype)
+    cap_c = w.window + S
+
+    # inputs resident in HBM
+    pre = []
+    for layer in range(L):
+        qs, ks, vs = zip(*(synth.prefill(w, first_seq + b, layer, device=dev) for b in range(w.batch)))
+        pre.append(tuple(torch.stack(t).contiguous() for t in (qs, ks, vs)))
+    dq, dk, dv = synth.decode_stream(w, S, L, first_seq, device=dev)
+    outs = torch.empty(S, L, w.batch, w.h_q, w.head_dim, dtype=torch.float32, device=dev)
+
+    score_out = [None] * L
+    alloc_out = [None] * L
+    caches = [None] * L
+    lib = rdkv.lib()
+    stream = torch.cuda.current_stream()
+
+    def compress(timing):
+        for layer in range(L):
+            q, k, v = pre[layer]
+            if timing is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            score_out[layer] = rdkv.rdkv_score(shape, q, k, v, out=score_out[layer])
+            if timing is not None:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record()
+                timing.append((e0, e1))
+            sc = score_out[layer]
+            alloc_out[layer] = rdkv.rdkv_allocate(shape, sc["g_tok"], sc["w_chan"], k, avg, avg,
+                                                  out=alloc_out[layer])
+            al = alloc_out[layer]
+            caches[layer] = rdkv.rdkv_pack(shape, al["plan"], k, v, al["bits_tok"], al["bits_chan"], cap_c,
+                                           into=caches[layer])
+
+    def decode_phase():
+        for s in range(S):
+            for layer in range(L):
+                rdkv.rdkv_append(caches[layer], dk[s, layer], dv[s, layer])
+                rdkv.rdkv_decode_attn(caches[layer], dq[s, layer], out=outs[s, layer])
+
+    # warm-up: eager once (allocates every buffer), then capture the decode phase
+    compress(None)
+    for c in caches:
+        c.decode_workspace()
+    torch.cuda.synchronize()
+    n0 = lib.rdkv_launch_count()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        decode_phase()
+    decode_launches = lib.rdkv_launch_count() - n0
+    for _ in range(max(0, args.warmup - 1)):
+        compress(None)
+        g.replay()
+    torch.cuda.synchronize()
+    for c in caches:
+        st = rdkv.rdkv_decode_status(c)
+        if st != 0:
+            raise RuntimeError(f"decode status {st}")
+
+    # algorithmic decode bytes per step (all layers, all decode steps)
+    heads_per_layer = [rdkv.read_plan(alloc_out[layer]["plan"])[1] for layer in range(L)]
+    dec_bytes = sum(decode_bytes_per_call(h, w.head_dim, w.h_q, w.batch, w.window + s + 1)
+                    for h in heads_per_layer for s in range(S))
+    kept = sum(int(np.sum(h["n_v"])) for h in heads_per_layer) / (L * w.batch * w.h_kv * w.n_prefix)
+
+    # timed region
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = []
+    score_ev = []
+    launches0 = lib.rdkv_launch_count()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(torch.cuda.current_device())
+    with ClockSampler(gpu_id) as clk:
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            c = torch.cuda.Event(enable_timing=True)
+            a.record()
+            compress(score_ev)
+            b.record()
+            g.replay()
+            c.record()
+            ev.append((a, b, c))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if ws > 1:
+        torch.distributed.barrier()
+    compress_launches = lib.rdkv_launch_count() - launches0
+    gpu_launches = int(compress_launches + args.steps * decode_launches)
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
+    score_ms = sum(e0.elapsed_time(e1) for e0, e1 in score_ev) / args.steps
+    tot_ms, tot_dec, tot_score = sum(step_ms), sum(dec_ms), score_ms * args.steps
+    if ws > 1:
+        t = torch.tensor([tot_ms, tot_dec, tot_score], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot_ms, tot_dec, tot_score = t.tolist()
+
+    ms_per_step = tot_ms / args.steps
+    dec_ms_step = tot_dec / args.steps
+    value = ws * dec_bytes / (dec_ms_step * 1e-3) / 1e9
+    flops = scorer_flops(w) * L
+    score_tflops = ws * flops / (score_ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    clocks = clk.summary()
+
+    # roofline of the dominant kernel by time share in the step
+    dec_frac_time, score_frac_time = dec_ms_step / ms_per_step, score_ms / ms_per_step
+    decode_roof = {"bound": "hbm", "achieved": round(value / ws, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": round(value / ws / peaks["hbm_gbs"], 4), "traffic": None,
+                   "peak_source": peaks["source"], "time_share": round(dec_frac_time, 3)}
+    # the fp16 scorer currently runs fp32 FMA on CUDA cores: roofline against the FP32 ALU peak
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = sms * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+    score_roof = {"bound": "alu", "achieved": round(score_tflops / ws, 2), "peak": round(alu_peak, 1),
+                  "unit": "TFLOP/s", "frac": round(score_tflops / ws / alu_peak, 4), "traffic": None,
+                  "peak_source": "152 SMs x 128 FP32 lanes x 2 flops x max SM clock",
+                  "time_share": round(score_frac_time, 3)}
+    dominant = score_roof if score_frac_time >= dec_frac_time else decode_roof
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16" if w.dtype == "f16" else "f32",
+        "data": "synthetic (seeded generator, workload shapes and salience structure)",
+        "config": {"workload": w.name, "description": w.description, "layers": L, "decode_steps": S,
+                   "avg_bits": avg, "batch_per_gpu": w.batch, "kept_fraction": round(kept, 4),
+                   "parallelism": f"replicas x{ws} (independent sequences per rank)",
+                   "l2": "inputs larger than L2: 9 GB prefill, ~0.7 GB of packed caches rotated across layers"},
+        "decode_us_per_layer_step": round(dec_ms_step * 1e3 / (S * L), 3),
+        "decode_ms_per_model_step": round(dec_ms_step / S, 4),
+        "decode_bytes_per_step": int(dec_bytes),
+        "scorer_tflops": round(score_tflops, 2), "scorer_ms_per_layer": round(score_ms / L, 3),
+        "compress_ms_per_layer": round((ms_per_step - dec_ms_step) / L, 3),
+        "roofline": dominant, "rooflines": {"decode": decode_roof, "scorer": score_roof},
+        "gpu_launches": gpu_launches, "clocks": clocks, "wall_s": round(wall, 3),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    return line
+
+
+def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev):
+    """Same metric through the public API with pinned host inputs: every step copies the
+    prefill inputs and every decode step's inputs host->device and reads each output back."""
+    from mixed_bit_kv_gb300 import rdkv
+
+    h_pre = [tuple(t.cpu().pin_memory() for t in trip) for trip in pre]
+    h_dq, h_dk, h_dv = (t.cpu().pin_memory() for t in (dq, dk, dv))
+    h_out = torch.empty((S, L, w.batch, w.h_q, w.head_dim), dtype=torch.float32).pin_memory()
+    d_pre = [tuple(torch.empty_like(t) for t in trip) for trip in pre]
+    d_dq, d_dk, d_dv = (torch.empty_like(t[0]) for t in (dq, dk, dv))   # one decode step, all layers
+    d_out = torch.empty((L, w.batch, w.h_q, w.head_dim), dtype=torch.float32, device=dev)
+    score_out, alloc_out, caches = [None] * L, [None] * L, [None] * L
+
+    def step_compress():
+        for layer in range(L):
+            for dst, src in zip(d_pre[layer], h_pre[layer]):
+                dst.copy_(src, non_blocking=True)
+            q, k, v = d_pre[layer]
+            score_out[layer] = rdkv.rdkv_score(shape, q, k, v, out=score_out[layer])
+            sc = score_out[layer]
+            alloc_out[layer] = rdkv.rdkv_allocate(shape, sc["g_tok"], sc["w_chan"], k, avg, avg,
+                                                  out=alloc_out[layer])
+            al = alloc_out[layer]
+            caches[layer] = rdkv.rdkv_pack(shape, al["plan"], k, v, al["bits_tok"], al["bits_chan"], cap_c,
+                                           into=caches[layer])
+
+    def decode_phase():
+        for s in range(S):
+            d_dq.copy_(h_dq[s], non_blocking=True)
+            d_dk.copy_(h_dk[s], non_blocking=True)
+            d_dv.copy_(h_dv[s], non_blocking=True)
+            for layer in range(L):
+                rdkv.rdkv_append(caches[layer], d_dk[layer], d_dv[layer])
+                rdkv.rdkv_decode_attn(caches[layer], d_dq[layer], out=d_out[layer])
+            h_out[s].copy_(d_out, non_blocking=True)
+
+    step_compress()
+    for c in caches:
+        c.decode_workspace()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        decode_phase()
+    step_compress()
+    g.replay()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 2))
+    t_dec = 0.0
+    for _ in range(steps):
+        step_compress()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        g.replay()
+        torch.cuda.synchronize()
+        t_dec += time.perf_counter() - t0
+    h2d = sum(t.numel() * t.element_size() for trip in h_pre for t in trip) + \
+        sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv))
+    d2h = h_out.numel() * 4 + L * 88
+    return {"value": round(ws * dec_bytes / (t_dec / steps) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "note": "decode phase wall time incl. per-decode-step H2D of q/k/v and D2H of outputs; "
+                    "the prefill H2D copies run in the compress phase of the same step"}
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
+def oracle_sample(w, avg, n_tokens, layers_sample=1, decode_calls=2):
+    """Times the CPU oracle's decode (unpack + float64 attention) on a reduced-length
+    sample of the workload; returns (GB/s of algorithmic decode bytes, cores used, description)."""
+    import oracle as O
+    from mixed_bit_kv_gb300 import synth
+    ws_ = w.scaled(n_tokens=n_tokens, batch=1)
+    q, k, v = (t.numpy() for t in synth.prefill(ws_, 0, 0))
+    sc = O.score(q, k, v, ws_.window)
+    al = O.allocate(sc["g_tok"], sc["w_chan"], k, avg, avg)
+    cache = O.pack(k[None], v[None], al["bits_tok"][None], al["bits_chan"][None], ws_.window,
+                   cap_c=ws_.window + decode_calls)
+    qn, kn, vn = (t.numpy() for t in synth.decode_step(ws_, 0))
+    O.append(cache, kn, vn)
+    r0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for _ in range(decode_calls):
+        O.decode(cache, qn)
+        nbytes += O.decode_bytes(cache["plan"], ws_.head_dim, ws_.h_q, ws_.h_kv, cache["len_c"], 1)
+    dt = time.perf_counter() - t0
+    r1 = resource.getrusage(resource.RUSAGE_SELF)
+    cpu = (r1.ru_utime - r0.ru_utime) + (r1.ru_stime - r0.ru_stime)
+    cores = max(1, int(round(cpu / dt)))
+    desc = (f"oracle decode (unpack + float64 attention) of one {w.name}-shaped layer at N={n_tokens} "
+            f"(full workload N={w.n_tokens}), {decode_calls} calls, {dt:.1f} s")
+    return nbytes / dt / 1e9, cores, desc
+
+
+def run_reference(args):
+    from mixed_bit_kv_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    avg = w.budgets[0] if args.budget is None else args.budget
+    n = min(w.n_tokens, args.oracle_tokens)
+    vals, t_all = [], time.perf_counter()
+    for _ in range(args.warmup + args.steps):
+        gbs, cores, desc = oracle_sample(w, avg, n, decode_calls=1)
+        vals.append(gbs)
+    value = float(np.mean(vals[args.warmup:]))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round((time.perf_counter() - t_all) * 1e3 / (args.warmup + args.steps), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator)", "config": {"workload": w.name, "avg_bits": avg,
+                                                               "oracle_tokens": n},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3b")
+    ap.add_argument("--layers", type=int, default=28)
+    ap.add_argument("--decode-steps", type=int, default=None)
+    ap.add_argument("--budget", type=float, default=None)
+    ap.add_argument("--oracle-tokens", type=int, default=4096)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    line = run_ours(args, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            from mixed_bit_kv_gb300 import synth
+            w = synth.WORKLOADS[args.workload]
+            avg = w.budgets[0] if args.budget is None else args.budget
+            gbs, cores, desc = oracle_sample(w, avg, min(w.n_tokens, args.oracle_tokens))
+            line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -97,9 +97,13 @@ typedef struct rdkv_sizes {
 } rdkv_sizes;
 
 /* A packed TriZone cache.  All pointers are caller-owned device memory.
- * zone_c_k / zone_c_v are fp16 [batch][h_kv][cap_c][D].  len_c is the number
- * of zone-C rows in use (same for every sequence): rdkv_pack sets it to the
- * window W, rdkv_append advances it; the library keeps it on the host. */
+ * zone_c_k / zone_c_v are fp16 [batch][h_kv][cap_c][D].  The number of zone-C
+ * rows in use (same for every sequence) is kept twice: len_dev (one device
+ * int32) is what the kernels read and advance, so a captured CUDA graph of
+ * append + decode calls stays correct when replayed; len_c is the host mirror
+ * the host-side capacity check uses.  rdkv_pack sets both to the window W;
+ * rdkv_append advances both.  Replaying captured appends advances only
+ * len_dev; a device-side append past cap_c writes nothing. */
 typedef struct rdkv_cache {
   rdkv_shape shape;
   const void* plan;
@@ -108,6 +112,7 @@ typedef struct rdkv_cache {
   uint16_t* zone_c_k;
   uint16_t* zone_c_v;
   int32_t* index_map;
+  int32_t* len_dev;
   int32_t cap_c;
   int32_t len_c;
   rdkv_sizes sizes;
@@ -116,6 +121,9 @@ typedef struct rdkv_cache {
 /* ---------------------------------------------------------------- misc */
 const char* rdkv_last_error_string(void);
 int32_t rdkv_version(void);
+/* Number of CUDA kernels this library has launched (or recorded into a graph
+ * being captured) in this process, over all threads. */
+uint64_t rdkv_launch_count(void);
 
 /* ---------------------------------------------------------------- step 1: weights
  * RDKV section 2.1 (and section 2.2 step 1: computed once after prefill on the
@@ -181,15 +189,16 @@ rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v,
 
 /* ---------------------------------------------------------------- append
  * RDKV section 2.3 zone C: writes the new token's k_new, v_new [B][H_kv][D]
- * (shape->dtype) as fp16 rows at index len_c of zone C and advances len_c.
- * Returns RDKV_ERR_CAPACITY (nothing written) when len_c == cap_c. */
+ * (shape->dtype) as fp16 rows at row *len_dev of zone C and advances *len_dev
+ * and len_c.  Returns RDKV_ERR_CAPACITY (nothing launched) when the host
+ * mirror len_c == cap_c. */
 rdkv_status rdkv_append(rdkv_cache* cache, const void* k_new, const void* v_new, void* stream);
 
 /* ---------------------------------------------------------------- decode attention
  * RDKV section 2.3: for every sequence b and query head h (KV head h / G),
  *   out[b][h] = sum_t softmax_t(q[b][h] . k^_t / sqrt(D)) v^_t
  * over the kept tokens of zones A (dequantised K and V) and B (fp16 V) and the
- * len_c rows of zone C.  q [B][H_q][D] in shape->dtype (used as fp16 by the
+ * *len_dev rows of zone C.  q [B][H_q][D] in shape->dtype (used as fp16 by the
  * tensor cores), out [B][H_q][D] fp32.  Split-K over tiles with an fp32
  * online softmax; the partial results live in ws. */
 size_t rdkv_decode_workspace_bytes(const rdkv_cache* cache);

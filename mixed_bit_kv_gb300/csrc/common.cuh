@@ -72,6 +72,7 @@ void set_error(const char* fmt, ...);
 rdkv_status cuda_status(cudaError_t e, const char* what);
 rdkv_status check_shape(const rdkv_shape* s);
 int num_sms();
+void count_launch();
 
 }  // namespace rdkv
 
@@ -81,7 +82,11 @@ int num_sms();
     if (_e != cudaSuccess) return ::rdkv::cuda_status(_e, what);        \
   } while (0)
 
-#define RDKV_CHECK_LAUNCH(what) RDKV_TRY_CUDA(cudaGetLastError(), what)
+#define RDKV_CHECK_LAUNCH(what)                 \
+  do {                                          \
+    ::rdkv::count_launch();                     \
+    RDKV_TRY_CUDA(cudaGetLastError(), what);    \
+  } while (0)
 
 #define RDKV_REQUIRE(cond, code, ...)            \
   do {                                           \

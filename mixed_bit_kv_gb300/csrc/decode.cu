@@ -43,7 +43,7 @@ struct KBDesc {
 
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings).
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
-  return ((256 + (int64_t)(kMaxKB + D / 16) * 32 * 8 + kDecWarps * kMaxInflight * 12 +
+  return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + kDecWarps * kMaxInflight * 12 +
            (int64_t)kDecWarps * 8 * (D + 2) * 4) + 127) / 128 * 128;
 }
 
@@ -56,7 +56,8 @@ struct DecodeParams {
   const void* q;
   float* partial;   // [n_heads][splits][G][D + 2]
   int32_t* error;   // device status word
-  int dtype, h_q, h_kv, cap_c, len_c, ring_bytes;
+  const int32_t* len_dev;  // zone-C rows in use
+  int dtype, h_q, h_kv, cap_c, ring_bytes;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -136,9 +137,28 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t w, int shift, uint32_t
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// Two codes of a pair -> the same codes as exact fp16 values (no scale, no zero).
+__device__ __forceinline__ uint32_t exact_codes(uint32_t w, int shift, uint32_t mask2) {
+  const uint32_t x = ((w >> shift) & mask2) | 0x64006400u;
+  const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&x), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+  return *reinterpret_cast<const uint32_t*>(&c);
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// (x0, x1) and (x2, x3) as fp16 pairs: high parts {x, y}, remainders {z, w}; hi + lo keeps ~22 bits.
+__device__ __forceinline__ uint4 split_hi_lo(float x0, float x1, float x2, float x3) {
+  const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+  const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+  uint4 r;
+  r.x = *reinterpret_cast<const uint32_t*>(&h01);
+  r.y = *reinterpret_cast<const uint32_t*>(&h23);
+  r.z = pack_half2(x0 - f01.x, x1 - f01.y);
+  r.w = pack_half2(x2 - f23.x, x3 - f23.y);
+  return r;
 }
 
 // ---------------------------------------------------------------- per-warp state
@@ -191,52 +211,85 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
 }
 
 // K logits of a zone-A tile: S^T for token blocks 0 and 1.
+// A quantised K element is zero_c + scale_c * code, so per head g
+//   q_g . k^ = sum_c q_gc zero_c + sum_c code * (q_gc scale_c).
+// The codes are exact in fp16 and form the A operand; q_gc * scale_c (exact in
+// fp32) is split into an fp16 high part and an fp16 remainder, two B operands,
+// so the products keep ~22 bits; the zero term is summed in fp32.  Raw 16-bit
+// channels use the stored fp16 value against q directly.
 template <int D>
 __device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW, int nkb, const KBDesc* kbd,
-                                            const uint2* qfrag, int lane, float (&s)[2][4]) {
+                                            const float4* qv, int lane, float (&s)[2][4]) {
   const int g = lane >> 2, q = lane & 3;
+  float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) s[tb][0] = s[tb][1] = s[tb][2] = s[tb][3] = 0.f;
   for (int kb = 0; kb < nkb; ++kb) {
     const KBDesc d = kbd[kb];
-    const uint2 qf = qfrag[kb * 32 + lane];
+    const float4 qq = qv[kb * 32 + lane];  // q_g at slots 2q, 2q+1, 2q+8, 2q+9 (0 for pads)
     const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
-    uint32_t w0, w1;  // word offsets of pair 0 (slots 2q, 2q+1) and pair 1 (slots 2q+8, 2q+9)
-    int sh0, sh1;
-    uint32_t mask2 = 0xffffffffu, sc0 = 0, ze0 = 0, sc1 = 0, ze1 = 0;
     const int b = d.width;
     if (b == 16) {
-      w0 = d.word0 + q; w1 = d.word0 + q + 4; sh0 = sh1 = 0;
-    } else {
-      if (b == 8) {
-        w0 = d.word0 + (q >> 1); w1 = w0 + 2; sh0 = sh1 = 8 * (q & 1); mask2 = 0x00ff00ffu;
-      } else if (b == 4) {
-        w0 = d.word0; w1 = w0 + 1; sh0 = sh1 = 4 * q; mask2 = 0x000f000fu;
-      } else {
-        w0 = w1 = d.word0; sh0 = 2 * q; sh1 = 2 * q + 8; mask2 = 0x00030003u;
+      const uint4 qs = split_hi_lo(qq.x, qq.y, qq.z, qq.w);
+      const uint32_t w0 = d.word0 + q, w1 = d.word0 + q + 4;
+#pragma unroll
+      for (int tb = 0; tb < 2; ++tb) {
+        const uint32_t r0 = kw + 4u * ((16 * tb + g) * RW), r1 = r0 + 4u * (8 * RW);
+        const uint32_t a0 = v0 ? lds32(r0 + 4 * w0) : 0u, a1 = v0 ? lds32(r1 + 4 * w0) : 0u;
+        const uint32_t a2 = v1 ? lds32(r0 + 4 * w1) : 0u, a3 = v1 ? lds32(r1 + 4 * w1) : 0u;
+        mma16816(s[tb], a0, a1, a2, a3, qs.x, qs.y);
+        mma16816(s[tb], a0, a1, a2, a3, qs.z, qs.w);
       }
-      if (v0) { const uint2 m = lds64(kmeta + 8 * (d.meta0 + q)); sc0 = m.x; ze0 = m.y; }
-      if (v1) { const uint2 m = lds64(kmeta + 8 * (d.meta0 + q + 4)); sc1 = m.x; ze1 = m.y; }
+      continue;
     }
+    uint32_t w0, w1, mask2;
+    int sh0, sh1;
+    if (b == 8) {
+      w0 = d.word0 + (q >> 1); w1 = w0 + 2; sh0 = sh1 = 8 * (q & 1); mask2 = 0x00ff00ffu;
+    } else if (b == 4) {
+      w0 = d.word0; w1 = w0 + 1; sh0 = sh1 = 4 * q; mask2 = 0x000f000fu;
+    } else {
+      w0 = w1 = d.word0; sh0 = 2 * q; sh1 = 2 * q + 8; mask2 = 0x00030003u;
+    }
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, ze[4] = {0.f, 0.f, 0.f, 0.f};
+    if (v0) {
+      const uint2 m = lds64(kmeta + 8 * (d.meta0 + q));
+      const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&m.x));
+      const float2 z2 = __half22float2(*reinterpret_cast<const __half2*>(&m.y));
+      sc[0] = s2.x; sc[1] = s2.y; ze[0] = z2.x; ze[1] = z2.y;
+    }
+    if (v1) {
+      const uint2 m = lds64(kmeta + 8 * (d.meta0 + q + 4));
+      const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&m.x));
+      const float2 z2 = __half22float2(*reinterpret_cast<const __half2*>(&m.y));
+      sc[2] = s2.x; sc[3] = s2.y; ze[2] = z2.x; ze[3] = z2.y;
+    }
+    bias = fmaf(qq.x, ze[0], bias);
+    bias = fmaf(qq.y, ze[1], bias);
+    bias = fmaf(qq.z, ze[2], bias);
+    bias = fmaf(qq.w, ze[3], bias);
+    const uint4 qs = split_hi_lo(qq.x * sc[0], qq.y * sc[1], qq.z * sc[2], qq.w * sc[3]);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
       const uint32_t r0 = kw + 4u * ((16 * tb + g) * RW), r1 = r0 + 4u * (8 * RW);
-      uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-      if (b == 16) {
-        if (v0) { a0 = lds32(r0 + 4 * w0); a1 = lds32(r1 + 4 * w0); }
-        if (v1) { a2 = lds32(r0 + 4 * w1); a3 = lds32(r1 + 4 * w1); }
-      } else {
-        if (v0) {
-          a0 = dequant_pair(lds32(r0 + 4 * w0), sh0, mask2, sc0, ze0);
-          a1 = dequant_pair(lds32(r1 + 4 * w0), sh0, mask2, sc0, ze0);
-        }
-        if (v1) {
-          a2 = dequant_pair(lds32(r0 + 4 * w1), sh1, mask2, sc1, ze1);
-          a3 = dequant_pair(lds32(r1 + 4 * w1), sh1, mask2, sc1, ze1);
-        }
-      }
-      mma16816(s[tb], a0, a1, a2, a3, qf.x, qf.y);
+      const uint32_t a0 = v0 ? exact_codes(lds32(r0 + 4 * w0), sh0, mask2) : 0u;
+      const uint32_t a1 = v0 ? exact_codes(lds32(r1 + 4 * w0), sh0, mask2) : 0u;
+      const uint32_t a2 = v1 ? exact_codes(lds32(r0 + 4 * w1), sh1, mask2) : 0u;
+      const uint32_t a3 = v1 ? exact_codes(lds32(r1 + 4 * w1), sh1, mask2) : 0u;
+      mma16816(s[tb], a0, a1, a2, a3, qs.x, qs.y);
+      mma16816(s[tb], a0, a1, a2, a3, qs.z, qs.w);
     }
+  }
+  // zero-point term: lanes (g, 0..3) hold parts of head g; S^T lane (g', q') needs heads 2q', 2q'+1
+  bias += __shfl_xor_sync(0xffffffffu, bias, 1);
+  bias += __shfl_xor_sync(0xffffffffu, bias, 2);
+  const float be = __shfl_sync(0xffffffffu, bias, 8 * q), bo = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
+#pragma unroll
+  for (int tb = 0; tb < 2; ++tb) {
+    s[tb][0] += be;
+    s[tb][1] += bo;
+    s[tb][2] += be;
+    s[tb][3] += bo;
   }
 }
 
@@ -301,9 +354,9 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
 
   // shared memory map
   KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
-  uint2* qfrag = reinterpret_cast<uint2*>(smem + 256);                             // [kMaxKB][32]
-  uint2* qfragc = qfrag + kMaxKB * 32;                                             // [D/16][32]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qfragc + (D / 16) * 32);            // [warps][kMaxInflight]
+  float4* qv = reinterpret_cast<float4*>(smem + 256);                              // [kMaxKB][32]
+  uint4* qfragc = reinterpret_cast<uint4*>(qv + kMaxKB * 32);                      // [D/16][32] hi, lo
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qfragc + (D / 16) * 32);           // [warps][kMaxInflight]
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
   float* red = reinterpret_cast<float*>(ring_pos + kDecWarps * kMaxInflight);      // [warps][8][D + 2]
   unsigned char* ring = smem + decode_fixed_smem(D);
@@ -350,8 +403,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
         if (ch >= 0) v[e] = load_as_float(P.q, (int64_t)(qbase + g) * D + ch, P.dtype);
       }
     }
-    const uint2 f = make_uint2(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]));
-    if (kb < nkb) qfrag[kb * 32 + ln] = f; else qfragc[(kb - nkb) * 32 + ln] = f;
+    if (kb < nkb) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
+    else qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
   }
   if (lane == 0)
     for (int k = 0; k < kMaxInflight; ++k) mbar_init(&bars[warp * kMaxInflight + k], 1);
@@ -361,7 +414,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
   // items of this head and of this split
   int cls_tiles[4], n_tiles = 0;
   for (int c = 0; c < 4; ++c) { cls_tiles[c] = hp.tiles[c]; n_tiles += hp.tiles[c]; }
-  const int n_items = n_tiles + ceil_div(P.len_c, kCRows);
+  const int len_c = min(*P.len_dev, P.cap_c);
+  const int n_items = n_tiles + ceil_div(len_c, kCRows);
   const int i0 = (int)((int64_t)n_items * split / n_split), i1 = (int)((int64_t)n_items * (split + 1) / n_split);
   const int my_n = i1 - i0 > warp ? ceil_div(i1 - i0 - warp, kDecWarps) : 0;
 
@@ -422,7 +476,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
           bulk_copy(dst, P.zone_a + a_src, a_bytes, bar);
           if (zb) bulk_copy(dst + a_bytes, P.zone_b + (hp.b_row + (int64_t)kTile * ti) * D, zb, bar);
         } else {
-          const int rows = min(kCRows, P.len_c - c_row);
+          const int rows = min(kCRows, len_c - c_row);
           const uint32_t bytes = (uint32_t)rows * D * 2;
           const int64_t src = ((int64_t)head * P.cap_c + c_row) * D;
           mbar_arrive_expect_tx(bar, 2 * bytes);
@@ -450,7 +504,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
       const int n_real = min(kTile, hp.n_v[cls] - kTile * ti);
       const uint32_t kmeta = st + 4u * kTile * hp.row_words;
       float s[2][4];
-      tile_logits<D>(st, kmeta, hp.row_words, nkb, kbd, qfrag, lane, s);
+      tile_logits<D>(st, kmeta, hp.row_words, nkb, kbd, qv, lane, s);
       const int g = lane >> 2;
 #pragma unroll
       for (int tb = 0; tb < 2; ++tb) {
@@ -470,7 +524,7 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
         pv_fp16<D, 2>(acc, st + a_bytes, lane, pb);
       }
     } else {
-      const int rows = min(kCRows, P.len_c - c_row);
+      const int rows = min(kCRows, len_c - c_row);
       if (rows < kCRows) {  // clear the rows the copy did not fill (they meet p = 0 in the products)
         uint32_t* kz = reinterpret_cast<uint32_t*>(wring + wpos[slot]);
         for (int i = rows * D / 2 + lane; i < kCRows * D / 2; i += 32) {
@@ -486,8 +540,9 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
         uint32_t a0, a1, a2, a3;
         const int row = (mi & 1) * 8 + r, col = 16 * kb + (mi >> 1) * 8;
         ldsm_x4(st + 2u * (row * D + col), a0, a1, a2, a3);
-        const uint2 qf = qfragc[kb * 32 + lane];
+        const uint4 qf = qfragc[kb * 32 + lane];
         mma16816(s[0], a0, a1, a2, a3, qf.x, qf.y);
+        mma16816(s[0], a0, a1, a2, a3, qf.z, qf.w);
       }
       const int g = lane >> 2;
       const bool va = g < rows, vb = g + 8 < rows;
@@ -648,19 +703,25 @@ extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, 
   P.h_q = s.h_q;
   P.h_kv = s.h_kv;
   P.cap_c = cache->cap_c;
-  P.len_c = cache->len_c;
+  P.len_dev = cache->len_dev;
   P.ring_bytes = geo.ring_bytes;
   RDKV_TRY_CUDA(cudaMemsetAsync(P.error, 0, 4, cs), "decode status reset");
   const dim3 grid(geo.splits, s.batch * s.h_kv);
-  if (s.head_dim == 128) {
-    RDKV_TRY_CUDA(cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem),
+  // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is captured)
+  static size_t smem_set[2][64] = {};
+  int dev = 0;
+  RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
+  const int ki = s.head_dim == 128 ? 1 : 0;
+  if (dev < 64 && geo.smem > smem_set[ki][dev]) {
+    RDKV_TRY_CUDA(cudaFuncSetAttribute(ki ? (const void*)decode_kernel<128> : (const void*)decode_kernel<64>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmemLimit),
                   "decode smem");
-    decode_kernel<128><<<grid, kDecWarps * 32, geo.smem, cs>>>(P);
-  } else {
-    RDKV_TRY_CUDA(cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)geo.smem),
-                  "decode smem");
-    decode_kernel<64><<<grid, kDecWarps * 32, geo.smem, cs>>>(P);
+    smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
   }
+  if (ki)
+    decode_kernel<128><<<grid, kDecWarps * 32, geo.smem, cs>>>(P);
+  else
+    decode_kernel<64><<<grid, kDecWarps * 32, geo.smem, cs>>>(P);
   RDKV_CHECK_LAUNCH("decode");
   decode_merge_kernel<<<s.batch * s.h_q, s.head_dim, 0, cs>>>(P.partial, geo.splits, s.h_q, s.h_kv, s.head_dim, out);
   RDKV_CHECK_LAUNCH("decode merge");

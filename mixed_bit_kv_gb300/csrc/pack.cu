@@ -272,17 +272,24 @@ __global__ void window_kernel(const T* __restrict__ x, int N, int W, int h_kv, i
   }
 }
 
+// One block: every thread reads the row index before thread 0 advances it.
 template <typename T>
-__global__ void append_kernel(const T* __restrict__ kn, const T* __restrict__ vn, int64_t n, int D, int cap, int row,
-                              uint16_t* __restrict__ zk, uint16_t* __restrict__ zv) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const int64_t head = i / D;
-  const int c = (int)(i % D);
-  const int64_t dst = (head * cap + row) * D + c;
-  zk[dst] = half_bits(to_float(kn[i]));
-  zv[dst] = half_bits(to_float(vn[i]));
+__global__ void __launch_bounds__(1024) append_kernel(const T* __restrict__ kn, const T* __restrict__ vn, int64_t n,
+                                                      int D, int cap, int32_t* len_dev, uint16_t* __restrict__ zk,
+                                                      uint16_t* __restrict__ zv) {
+  const int row = *len_dev;
+  if (row < cap) {
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+      const int64_t dst = ((i / D) * cap + row) * D + (i % D);
+      zk[dst] = half_bits(to_float(kn[i]));
+      zv[dst] = half_bits(to_float(vn[i]));
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && row < cap) *len_dev = row + 1;
 }
+
+__global__ void set_len_kernel(int32_t* len_dev, int value) { *len_dev = value; }
 
 static size_t pack_smem_bytes(int D) {
   const int max_slots = D + kSlotPad;
@@ -293,7 +300,8 @@ static rdkv_status check_cache(const rdkv_cache* c) {
   RDKV_REQUIRE(c != nullptr, RDKV_ERR_INVALID_ARG, "cache is NULL");
   rdkv_status st = check_shape(&c->shape);
   if (st != RDKV_OK) return st;
-  RDKV_REQUIRE(c->plan && c->zone_c_k && c->zone_c_v, RDKV_ERR_INVALID_ARG, "cache plan or zone C is NULL");
+  RDKV_REQUIRE(c->plan && c->zone_c_k && c->zone_c_v && c->len_dev, RDKV_ERR_INVALID_ARG,
+               "cache plan, zone C or len_dev is NULL");
   RDKV_REQUIRE(c->sizes.zone_a_bytes == 0 || c->zone_a, RDKV_ERR_INVALID_ARG, "zone A is NULL");
   RDKV_REQUIRE(c->sizes.zone_b_rows == 0 || c->zone_b, RDKV_ERR_INVALID_ARG, "zone B is NULL");
   RDKV_REQUIRE(c->sizes.index_slots == 0 || c->index_map, RDKV_ERR_INVALID_ARG, "index map is NULL");
@@ -358,6 +366,8 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
     }
     RDKV_CHECK_LAUNCH("zone C window");
   }
+  set_len_kernel<<<1, 1, 0, cs>>>(cache->len_dev, W);
+  RDKV_CHECK_LAUNCH("zone C length");
   cache->len_c = W;
   return RDKV_OK;
 }
@@ -371,13 +381,13 @@ extern "C" rdkv_status rdkv_append(rdkv_cache* cache, const void* k_new, const v
   const int64_t n = (int64_t)s.batch * s.h_kv * s.head_dim;
   cudaStream_t cs = (cudaStream_t)stream;
   if (s.dtype == RDKV_F16)
-    append_kernel<__half><<<(unsigned)ceil_div64(n, 256), 256, 0, cs>>>(
-        static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), n, s.head_dim, cache->cap_c,
-        cache->len_c, cache->zone_c_k, cache->zone_c_v);
+    append_kernel<__half><<<1, 1024, 0, cs>>>(static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), n,
+                                               s.head_dim, cache->cap_c, cache->len_dev, cache->zone_c_k,
+                                               cache->zone_c_v);
   else
-    append_kernel<float><<<(unsigned)ceil_div64(n, 256), 256, 0, cs>>>(
-        static_cast<const float*>(k_new), static_cast<const float*>(v_new), n, s.head_dim, cache->cap_c, cache->len_c,
-        cache->zone_c_k, cache->zone_c_v);
+    append_kernel<float><<<1, 1024, 0, cs>>>(static_cast<const float*>(k_new), static_cast<const float*>(v_new), n,
+                                              s.head_dim, cache->cap_c, cache->len_dev, cache->zone_c_k,
+                                              cache->zone_c_v);
   RDKV_CHECK_LAUNCH("append");
   cache->len_c += 1;
   return RDKV_OK;

@@ -19,7 +19,7 @@ RDKV_ERR_CUDA, RDKV_ERR_TIMEOUT, RDKV_ERR_WORKSPACE = 4, 5, 6
 RDKV_F16, RDKV_F32 = 0, 1
 
 EXPORTED = (
-    "rdkv_last_error_string", "rdkv_version",
+    "rdkv_last_error_string", "rdkv_version", "rdkv_launch_count",
     "rdkv_score_workspace_bytes", "rdkv_score",
     "rdkv_waterfill_workspace_bytes", "rdkv_waterfill",
     "rdkv_plan_bytes", "rdkv_allocate_workspace_bytes", "rdkv_allocate", "rdkv_plan_sizes",
@@ -47,7 +47,8 @@ class Sizes(ctypes.Structure):
 class CacheStruct(ctypes.Structure):
     _fields_ = [("shape", Shape), ("plan", ctypes.c_void_p), ("zone_a", ctypes.c_void_p),
                 ("zone_b", ctypes.c_void_p), ("zone_c_k", ctypes.c_void_p), ("zone_c_v", ctypes.c_void_p),
-                ("index_map", ctypes.c_void_p), ("cap_c", ctypes.c_int32), ("len_c", ctypes.c_int32),
+                ("index_map", ctypes.c_void_p), ("len_dev", ctypes.c_void_p), ("cap_c", ctypes.c_int32),
+                ("len_c", ctypes.c_int32),
                 ("sizes", Sizes)]
 
 
@@ -74,6 +75,7 @@ def lib():
         sig = {
             "rdkv_last_error_string": (ctypes.c_char_p, []),
             "rdkv_version": (ctypes.c_int32, []),
+            "rdkv_launch_count": (ctypes.c_uint64, []),
             "rdkv_score_workspace_bytes": (ctypes.c_size_t, [sp]),
             "rdkv_score": (ctypes.c_int, [sp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_waterfill_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int64]),
@@ -127,16 +129,18 @@ def shape_of(q, k, window):
 
 
 # ---------------------------------------------------------------- step 1
-def rdkv_score(shape, q, k, v, stream=None):
+def rdkv_score(shape, q, k, v, stream=None, out=None, ws=None):
+    """Outputs are allocated unless `out` (a dict from an earlier call) is given."""
     dev = q.device
     B, N, Hkv, D = shape.batch, shape.n_tokens, shape.h_kv, shape.head_dim
     Np = N - shape.window
     f32 = dict(dtype=torch.float32, device=dev)
-    out = dict(w_tok=torch.empty(B, Hkv, N, **f32), w_chan=torch.empty(B, Hkv, D, **f32),
-               sigma_tok=torch.empty(B, Hkv, N, **f32), g_tok=torch.empty(B, Hkv, max(Np, 0), **f32))
+    if out is None:
+        out = dict(w_tok=torch.empty(B, Hkv, N, **f32), w_chan=torch.empty(B, Hkv, D, **f32),
+                   sigma_tok=torch.empty(B, Hkv, N, **f32), g_tok=torch.empty(B, Hkv, max(Np, 0), **f32))
     L = lib()
-    nb = L.rdkv_score_workspace_bytes(ctypes.byref(shape))
-    ws = _ws(nb, dev)
+    if ws is None:
+        ws = _ws(L.rdkv_score_workspace_bytes(ctypes.byref(shape)), dev)
     _check(L.rdkv_score(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out["w_tok"]), _ptr(out["w_chan"]),
                         _ptr(out["sigma_tok"]), _ptr(out["g_tok"]), _ptr(ws), ws.numel(), _stream(stream)))
     return out
@@ -157,17 +161,20 @@ def rdkv_waterfill(g, avg_bits, stream=None):
     return bits, lam, status
 
 
-def rdkv_allocate(shape, g_tok, w_chan, k, avg_bits_v, avg_bits_k, stream=None):
+def rdkv_allocate(shape, g_tok, w_chan, k, avg_bits_v, avg_bits_k, stream=None, out=None, ws=None):
+    """Outputs (widths, spreads, gains and the plan buffer) are allocated unless `out` is given."""
     dev = k.device
     B, Hkv, D = shape.batch, shape.h_kv, shape.head_dim
     Np = shape.n_tokens - shape.window
     L = lib()
-    out = dict(bits_tok=torch.empty(B, Hkv, max(Np, 0), dtype=torch.uint8, device=dev),
-               sigma_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
-               g_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
-               bits_chan=torch.empty(B, Hkv, D, dtype=torch.uint8, device=dev),
-               plan=torch.zeros(L.rdkv_plan_bytes(ctypes.byref(shape)), dtype=torch.uint8, device=dev))
-    ws = _ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), dev)
+    if out is None:
+        out = dict(bits_tok=torch.empty(B, Hkv, max(Np, 0), dtype=torch.uint8, device=dev),
+                   sigma_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+                   g_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+                   bits_chan=torch.empty(B, Hkv, D, dtype=torch.uint8, device=dev),
+                   plan=torch.zeros(L.rdkv_plan_bytes(ctypes.byref(shape)), dtype=torch.uint8, device=dev))
+    if ws is None:
+        ws = _ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), dev)
     _check(L.rdkv_allocate(ctypes.byref(shape), _ptr(g_tok), _ptr(w_chan), _ptr(k), float(avg_bits_v),
                            float(avg_bits_k), _ptr(out["bits_tok"]), _ptr(out["sigma_chan"]), _ptr(out["g_chan"]),
                            _ptr(out["bits_chan"]), _ptr(out["plan"]), _ptr(ws), ws.numel(), _stream(stream)))
@@ -192,9 +199,15 @@ class Cache:
         self.zone_c_k = torch.zeros(shape.batch, shape.h_kv, cap_c, D, dtype=torch.float16, device=device)
         self.zone_c_v = torch.zeros_like(self.zone_c_k)
         self.index_map = torch.zeros(max(sizes.index_slots, 1), dtype=torch.int32, device=device)
+        self.len_dev = torch.zeros(1, dtype=torch.int32, device=device)
         self.c = CacheStruct(shape, plan.data_ptr(), self.zone_a.data_ptr(), self.zone_b.data_ptr(),
                              self.zone_c_k.data_ptr(), self.zone_c_v.data_ptr(), self.index_map.data_ptr(),
-                             cap_c, 0, sizes)
+                             self.len_dev.data_ptr(), cap_c, 0, sizes)
+
+    def fits(self, sizes):
+        """True when a plan with these totals can be packed into this cache's buffers."""
+        return (sizes.zone_a_bytes <= self.zone_a.numel() and sizes.zone_b_rows <= self.zone_b.shape[0]
+                and sizes.index_slots <= self.index_map.numel())
         self._ws = None
 
     @property
@@ -208,9 +221,15 @@ class Cache:
         return self._ws
 
 
-def rdkv_pack(shape, plan, k, v, bits_tok, bits_chan, cap_c, stream=None, sizes=None):
+def rdkv_pack(shape, plan, k, v, bits_tok, bits_chan, cap_c, stream=None, sizes=None, into=None):
+    """Packs into a new Cache, or into the buffers of `into` when they are large enough."""
     sizes = sizes if sizes is not None else rdkv_plan_sizes(plan, stream)
-    cache = Cache(shape, plan, sizes, cap_c, k.device)
+    if into is not None and into.fits(sizes) and into.c.cap_c == cap_c:
+        cache = into
+        cache.plan, cache.sizes = plan, sizes
+        cache.c.plan, cache.c.sizes = plan.data_ptr(), sizes
+    else:
+        cache = Cache(shape, plan, sizes, cap_c, k.device)
     _check(lib().rdkv_pack(ctypes.byref(cache.c), _ptr(k), _ptr(v), _ptr(bits_tok), _ptr(bits_chan),
                            _stream(stream)))
     return cache

@@ -26,8 +26,9 @@ none of them):
 * decode steps draw fresh q (with the same u_j), k and v (with the same
   outlier channels) from a per-step seed.
 
-Seeds: prefill of (workload id c, sequence s, layer l) uses 1000*c + 10*s + l;
-decode step i uses that value + 100000*(i + 1).
+Seeds: prefill of (workload id c, sequence s, layer l) uses
+1_000_000*c + 1000*s + l; decode step i uses that value * 2**20 + i + 1, and the
+bulk decode stream of a (sequence, layer) uses that value * 2**20.
 """
 from __future__ import annotations
 
@@ -109,7 +110,7 @@ WORKLOADS = {
 
 
 def prefill_seed(w: Workload, seq: int = 0, layer: int = 0) -> int:
-    return 1000 * w.workload_id + 10 * seq + layer
+    return 1_000_000 * w.workload_id + 1000 * seq + layer
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -178,7 +179,7 @@ def decode_step(w: Workload, step: int, layer: int = 0, device="cpu"):
         g0 = _gen(base, device)
         u = _directions(g0, w, device)
         outl = _outlier_channels(g0, w, device)
-        g = _gen(base + 100000 * (step + 1), device)
+        g = _gen((base << 20) + step + 1, device)
         kv_of_q = torch.arange(w.h_q, device=device) // w.group
         q = torch.randn(w.h_q, w.head_dim, generator=g, device=device) + MU * u[kv_of_q]
         k = torch.randn(w.h_kv, w.head_dim, generator=g, device=device)
@@ -189,3 +190,30 @@ def decode_step(w: Workload, step: int, layer: int = 0, device="cpu"):
         qs.append(q); ks.append(k); vs.append(v)
     dt = w.torch_dtype
     return torch.stack(qs).to(dt), torch.stack(ks).to(dt), torch.stack(vs).to(dt)
+
+
+def decode_stream(w: Workload, steps: int, layers: int, first_seq: int = 0, device="cpu"):
+    """Decode inputs of `steps` steps for `layers` layers of sequences first_seq.. (batch w.batch):
+    q [steps, layers, B, H_q, D], k and v [steps, layers, B, H_kv, D], drawn per (sequence, layer)
+    with that prefill's query direction and outlier channels."""
+    B = w.batch
+    qs = torch.empty(steps, layers, B, w.h_q, w.head_dim, device=device)
+    ks = torch.empty(steps, layers, B, w.h_kv, w.head_dim, device=device)
+    vs = torch.empty(steps, layers, B, w.h_kv, w.head_dim, device=device)
+    kv_of_q = torch.arange(w.h_q, device=device) // w.group
+    for layer in range(layers):
+        for b in range(B):
+            base = prefill_seed(w, first_seq + b, layer)
+            g0 = _gen(base, device)
+            u = _directions(g0, w, device)
+            outl = _outlier_channels(g0, w, device)
+            g = _gen(base << 20, device)
+            qs[:, layer, b] = torch.randn(steps, w.h_q, w.head_dim, generator=g, device=device) + MU * u[kv_of_q]
+            k = torch.randn(steps, w.h_kv, w.head_dim, generator=g, device=device)
+            for j in range(w.h_kv):
+                if outl.shape[1]:
+                    k[:, j, outl[j]] *= w.outlier_scale
+            ks[:, layer, b] = k
+            vs[:, layer, b] = torch.randn(steps, w.h_kv, w.head_dim, generator=g, device=device)
+    dt = w.torch_dtype
+    return qs.to(dt), ks.to(dt), vs.to(dt)

@@ -87,7 +87,7 @@ def test_append_capacity_is_checked_on_the_host(L):
     s = rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16")
     sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 1)
     fake = ctypes.c_void_p(256)
-    c = rdkv.CacheStruct(s, 256, None, None, 256, 256, None, 8, 8, sizes)
+    c = rdkv.CacheStruct(s, 256, None, None, 256, 256, None, 256, 8, 8, sizes)
     r = L.rdkv_append(ctypes.byref(c), fake, fake, None)
     assert r == rdkv.RDKV_ERR_CAPACITY
     assert c.len_c == 8

@@ -636,7 +636,7 @@ __global__ void decode_merge_kernel(const float* __restrict__ partial, int n_spl
   out[(int64_t)bh * D + c] = l > 0.f ? o / l : 0.f;
 }
 
-constexpr int64_t kDecodeSmemLimit = 227 * 1024;
+constexpr int64_t kDecodeSmemLimit = 227 * 1024 - 1024;  // per-block limit less room for static shared memory
 
 struct DecodeGeom {
   int64_t max_item;

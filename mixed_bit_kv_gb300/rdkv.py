@@ -203,12 +203,12 @@ class Cache:
         self.c = CacheStruct(shape, plan.data_ptr(), self.zone_a.data_ptr(), self.zone_b.data_ptr(),
                              self.zone_c_k.data_ptr(), self.zone_c_v.data_ptr(), self.index_map.data_ptr(),
                              self.len_dev.data_ptr(), cap_c, 0, sizes)
+        self._ws = None
 
     def fits(self, sizes):
         """True when a plan with these totals can be packed into this cache's buffers."""
         return (sizes.zone_a_bytes <= self.zone_a.numel() and sizes.zone_b_rows <= self.zone_b.shape[0]
                 and sizes.index_slots <= self.index_map.numel())
-        self._ws = None
 
     @property
     def len_c(self):

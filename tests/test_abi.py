@@ -91,3 +91,17 @@ def test_append_capacity_is_checked_on_the_host(L):
     r = L.rdkv_append(ctypes.byref(c), fake, fake, None)
     assert r == rdkv.RDKV_ERR_CAPACITY
     assert c.len_c == 8
+
+
+def test_binding_cache_object_on_host_memory(L):
+    """The Python Cache wrapper builds its C struct and sizes its decode workspace without a GPU."""
+    import torch
+    s = rdkv.make_shape(2, 1000, 6, 2, 128, 40, "f16")
+    plan = torch.zeros(L.rdkv_plan_bytes(ctypes.byref(s)), dtype=torch.uint8)
+    sizes = rdkv.Sizes(4096, 64, 256, 200, 2048, 0, 4)
+    c = rdkv.Cache(s, plan, sizes, 48, "cpu")
+    assert c.c.len_dev == c.len_dev.data_ptr() and c.c.cap_c == 48 and c.len_c == 0
+    ws = c.decode_workspace()
+    assert ws.numel() >= L.rdkv_decode_workspace_bytes(ctypes.byref(c.c)) > 0
+    assert c.decode_workspace() is ws
+    assert c.fits(sizes) and not c.fits(rdkv.Sizes(1 << 30, 64, 256, 200, 2048, 0, 4))

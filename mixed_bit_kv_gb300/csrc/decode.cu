@@ -7,10 +7,12 @@
 //
 // Work: grid = (splits, sequence x KV head).  A head's work items are its
 // zone-A tiles (32 tokens, in class order) followed by zone-C blocks of 16
-// rows; split s takes a contiguous range of items and its 4 warps take the
-// items round-robin.  Every warp streams its items through its own ring of
-// shared memory, filled by bulk asynchronous copies that complete on
-// per-slot mbarriers (all waits are bounded and report RDKV_ERR_TIMEOUT).
+// rows; split s takes a contiguous range of items and its 8 warps take the
+// items round-robin.  Every warp streams its items through its own small ring
+// of shared memory, filled by bulk asynchronous copies that complete on
+// per-slot mbarriers (all waits are bounded and report RDKV_ERR_TIMEOUT), so
+// two blocks (16 warps) fit on an SM.  The last block of a head to finish
+// (an atomic ticket) merges the splits' partial softmax states into the output.
 //
 // Products: mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens on M:
 //   S^T[16 tok x 8 heads]  += K^[16 tok x 16 slots] * Q^T[16 slots x 8 heads]
@@ -27,8 +29,8 @@
 
 namespace rdkv {
 
-constexpr int kDecWarps = 4;
-constexpr int kMaxInflight = 8;
+constexpr int kDecWarps = 8;
+constexpr int kMaxInflight = 4;
 constexpr int kCRows = 16;        // zone-C rows per work item
 constexpr int kMaxKB = 16;        // k-blocks of a K row (D = 128: at most 13)
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at GB300 clocks
@@ -43,9 +45,11 @@ struct KBDesc {
 
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings).
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
-  return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + kDecWarps * kMaxInflight * 12 +
-           (int64_t)kDecWarps * 8 * (D + 2) * 4) + 127) / 128 * 128;
+  return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + kDecWarps * kMaxInflight * 12) + 127) /
+         128 * 128;
 }
+// The warps' partial results are combined in the ring area once every ring is drained.
+__host__ __device__ constexpr int64_t decode_reduce_bytes(int D) { return (int64_t)kDecWarps * 8 * (D + 2) * 4; }
 
 struct DecodeParams {
   const void* plan;
@@ -56,6 +60,8 @@ struct DecodeParams {
   const void* q;
   float* partial;   // [n_heads][splits][G][D + 2]
   int32_t* error;   // device status word
+  int32_t* tickets; // [n_heads] blocks finished per head (zeroed before the launch)
+  float* out;       // [batch][h_q][D]
   const int32_t* len_dev;  // zone-C rows in use
   int dtype, h_q, h_kv, cap_c, ring_bytes;
 };
@@ -210,77 +216,88 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
   }
 }
 
-// K logits of a zone-A tile: S^T for token blocks 0 and 1.
+// K logits of one width segment of a zone-A tile, k-blocks [kb0, kb1).
 // A quantised K element is zero_c + scale_c * code, so per head g
 //   q_g . k^ = sum_c q_gc zero_c + sum_c code * (q_gc scale_c).
 // The codes are exact in fp16 and form the A operand; q_gc * scale_c (exact in
 // fp32) is split into an fp16 high part and an fp16 remainder, two B operands,
 // so the products keep ~22 bits; the zero term is summed in fp32.  Raw 16-bit
-// channels use the stored fp16 value against q directly.
-template <int D>
-__device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW, int nkb, const KBDesc* kbd,
-                                            const float4* qv, int lane, float (&s)[2][4]) {
+// channels use the stored fp16 value against q (split the same way when q
+// carries more than fp16 precision).
+template <int W, bool QLO>
+__device__ __forceinline__ void k_segment(uint32_t kw, uint32_t kmeta, int RW, int kb0, int kb1, const KBDesc* kbd,
+                                          const float4* qv, int lane, float (&s)[2][4], float& bias) {
   const int g = lane >> 2, q = lane & 3;
-  float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
-#pragma unroll
-  for (int tb = 0; tb < 2; ++tb) s[tb][0] = s[tb][1] = s[tb][2] = s[tb][3] = 0.f;
-  for (int kb = 0; kb < nkb; ++kb) {
+  const uint32_t row0 = kw + 4u * (g * RW), rstep = 4u * (8 * RW);   // rows g, g+8, g+16, g+24
+  // word offsets (relative to the block's first word) and shifts of this lane's two slot pairs
+  constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
+  const int o0 = W == 16 ? q : W == 8 ? (q >> 1) : 0;
+  const int o1 = W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0;
+  const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
+  const int sh1 = W == 2 ? 2 * q + 8 : sh0;
+  for (int kb = kb0; kb < kb1; ++kb) {
     const KBDesc d = kbd[kb];
     const float4 qq = qv[kb * 32 + lane];  // q_g at slots 2q, 2q+1, 2q+8, 2q+9 (0 for pads)
     const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
-    const int b = d.width;
-    if (b == 16) {
-      const uint4 qs = split_hi_lo(qq.x, qq.y, qq.z, qq.w);
-      const uint32_t w0 = d.word0 + q, w1 = d.word0 + q + 4;
-#pragma unroll
-      for (int tb = 0; tb < 2; ++tb) {
-        const uint32_t r0 = kw + 4u * ((16 * tb + g) * RW), r1 = r0 + 4u * (8 * RW);
-        const uint32_t a0 = v0 ? lds32(r0 + 4 * w0) : 0u, a1 = v0 ? lds32(r1 + 4 * w0) : 0u;
-        const uint32_t a2 = v1 ? lds32(r0 + 4 * w1) : 0u, a3 = v1 ? lds32(r1 + 4 * w1) : 0u;
-        mma16816(s[tb], a0, a1, a2, a3, qs.x, qs.y);
-        mma16816(s[tb], a0, a1, a2, a3, qs.z, qs.w);
-      }
-      continue;
-    }
-    uint32_t w0, w1, mask2;
-    int sh0, sh1;
-    if (b == 8) {
-      w0 = d.word0 + (q >> 1); w1 = w0 + 2; sh0 = sh1 = 8 * (q & 1); mask2 = 0x00ff00ffu;
-    } else if (b == 4) {
-      w0 = d.word0; w1 = w0 + 1; sh0 = sh1 = 4 * q; mask2 = 0x000f000fu;
+    const uint32_t w0 = 4u * (d.word0 + o0), w1 = 4u * (d.word0 + o1);
+    uint4 bq;
+    if (W == 16) {
+      bq = split_hi_lo(qq.x, qq.y, qq.z, qq.w);
     } else {
-      w0 = w1 = d.word0; sh0 = 2 * q; sh1 = 2 * q + 8; mask2 = 0x00030003u;
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (v0) {
+        const uint2 m = lds64(kmeta + 8 * (d.meta0 + q));
+        const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&m.x));
+        const float2 z2 = __half22float2(*reinterpret_cast<const __half2*>(&m.y));
+        sc[0] = s2.x; sc[1] = s2.y;
+        bias = fmaf(qq.x, z2.x, fmaf(qq.y, z2.y, bias));
+      }
+      if (v1) {
+        const uint2 m = lds64(kmeta + 8 * (d.meta0 + q + 4));
+        const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&m.x));
+        const float2 z2 = __half22float2(*reinterpret_cast<const __half2*>(&m.y));
+        sc[2] = s2.x; sc[3] = s2.y;
+        bias = fmaf(qq.z, z2.x, fmaf(qq.w, z2.y, bias));
+      }
+      bq = split_hi_lo(qq.x * sc[0], qq.y * sc[1], qq.z * sc[2], qq.w * sc[3]);
     }
-    float sc[4] = {0.f, 0.f, 0.f, 0.f}, ze[4] = {0.f, 0.f, 0.f, 0.f};
-    if (v0) {
-      const uint2 m = lds64(kmeta + 8 * (d.meta0 + q));
-      const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&m.x));
-      const float2 z2 = __half22float2(*reinterpret_cast<const __half2*>(&m.y));
-      sc[0] = s2.x; sc[1] = s2.y; ze[0] = z2.x; ze[1] = z2.y;
-    }
-    if (v1) {
-      const uint2 m = lds64(kmeta + 8 * (d.meta0 + q + 4));
-      const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&m.x));
-      const float2 z2 = __half22float2(*reinterpret_cast<const __half2*>(&m.y));
-      sc[2] = s2.x; sc[3] = s2.y; ze[2] = z2.x; ze[3] = z2.y;
-    }
-    bias = fmaf(qq.x, ze[0], bias);
-    bias = fmaf(qq.y, ze[1], bias);
-    bias = fmaf(qq.z, ze[2], bias);
-    bias = fmaf(qq.w, ze[3], bias);
-    const uint4 qs = split_hi_lo(qq.x * sc[0], qq.y * sc[1], qq.z * sc[2], qq.w * sc[3]);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
-      const uint32_t r0 = kw + 4u * ((16 * tb + g) * RW), r1 = r0 + 4u * (8 * RW);
-      const uint32_t a0 = v0 ? exact_codes(lds32(r0 + 4 * w0), sh0, mask2) : 0u;
-      const uint32_t a1 = v0 ? exact_codes(lds32(r1 + 4 * w0), sh0, mask2) : 0u;
-      const uint32_t a2 = v1 ? exact_codes(lds32(r0 + 4 * w1), sh1, mask2) : 0u;
-      const uint32_t a3 = v1 ? exact_codes(lds32(r1 + 4 * w1), sh1, mask2) : 0u;
-      mma16816(s[tb], a0, a1, a2, a3, qs.x, qs.y);
-      mma16816(s[tb], a0, a1, a2, a3, qs.z, qs.w);
+      const uint32_t r0 = row0 + 2u * tb * rstep, r1 = r0 + rstep;
+      uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+      if (W == 16) {
+        if (v0) { a0 = lds32(r0 + w0); a1 = lds32(r1 + w0); }
+        if (v1) { a2 = lds32(r0 + w1); a3 = lds32(r1 + w1); }
+      } else {
+        if (v0) {
+          const uint32_t x0 = lds32(r0 + w0), x1 = lds32(r1 + w0);
+          a0 = exact_codes(x0, sh0, mask2);
+          a1 = exact_codes(x1, sh0, mask2);
+          if (W == 2 && v1) { a2 = exact_codes(x0, sh1, mask2); a3 = exact_codes(x1, sh1, mask2); }
+        }
+        if (W != 2 && v1) {
+          a2 = exact_codes(lds32(r0 + w1), sh1, mask2);
+          a3 = exact_codes(lds32(r1 + w1), sh1, mask2);
+        }
+      }
+      mma16816(s[tb], a0, a1, a2, a3, bq.x, bq.y);
+      if (W != 16 || QLO) mma16816(s[tb], a0, a1, a2, a3, bq.z, bq.w);
     }
   }
+}
+
+template <int D, bool QLO>
+__device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW, const int (&seg_kb)[5],
+                                            const KBDesc* kbd, const float4* qv, int lane, float (&s)[2][4]) {
+  float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
+#pragma unroll
+  for (int tb = 0; tb < 2; ++tb) s[tb][0] = s[tb][1] = s[tb][2] = s[tb][3] = 0.f;
+  if (seg_kb[1] > seg_kb[0]) k_segment<16, QLO>(kw, kmeta, RW, seg_kb[0], seg_kb[1], kbd, qv, lane, s, bias);
+  if (seg_kb[2] > seg_kb[1]) k_segment<8, QLO>(kw, kmeta, RW, seg_kb[1], seg_kb[2], kbd, qv, lane, s, bias);
+  if (seg_kb[3] > seg_kb[2]) k_segment<4, QLO>(kw, kmeta, RW, seg_kb[2], seg_kb[3], kbd, qv, lane, s, bias);
+  if (seg_kb[4] > seg_kb[3]) k_segment<2, QLO>(kw, kmeta, RW, seg_kb[3], seg_kb[4], kbd, qv, lane, s, bias);
   // zero-point term: lanes (g, 0..3) hold parts of head g; S^T lane (g', q') needs heads 2q', 2q'+1
+  const int q = lane & 3;
   bias += __shfl_xor_sync(0xffffffffu, bias, 1);
   bias += __shfl_xor_sync(0xffffffffu, bias, 2);
   const float be = __shfl_sync(0xffffffffu, bias, 8 * q), bo = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
@@ -293,17 +310,19 @@ __device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW,
   }
 }
 
-// PV of a zone-A tile with packed V (width vb).
-template <int D>
-__device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, uint32_t vcodes, uint32_t vmeta, int vb, int lane,
+// PV of a zone-A tile with packed V of width VB.
+template <int D, int VB>
+__device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, uint32_t vcodes, uint32_t vmeta, int lane,
                                                const uint32_t (&pb)[2][2]) {
   const int g = lane >> 2, q = lane & 3;
-  const int wpp = D * vb / 16;  // words per token pair
-  const int per = 16 / vb;      // channels per word
-  const uint32_t mask2 = vb == 8 ? 0x00ff00ffu : vb == 4 ? 0x000f000fu : 0x00030003u;
+  constexpr int wpp = D * VB / 16;  // words per token pair
+  constexpr int per = 16 / VB;      // channels per word
+  constexpr uint32_t mask2 = VB == 8 ? 0x00ff00ffu : VB == 4 ? 0x000f000fu : 0x00030003u;
+  const int sh0 = VB * (g % per), sh1 = VB * ((g + 8) % per);
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
     const int p0 = 8 * tb + q, p1 = p0 + 4;
+    const uint32_t base0 = vcodes + 4u * (p0 * wpp), base1 = vcodes + 4u * (p1 * wpp);
 #pragma unroll
     for (int grp = 0; grp < D / 32; ++grp) {
       const uint2 m0 = lds64(vmeta + 8 * (p0 * (D / 32) + grp));
@@ -312,13 +331,10 @@ __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, uint32_t vcodes,
       for (int half = 0; half < 2; ++half) {
         const int cm = 2 * grp + half;
         const int c0 = 16 * cm + g, c1 = c0 + 8;
-        const uint32_t wa = vcodes + 4u * (p0 * wpp + c0 / per), wb = vcodes + 4u * (p0 * wpp + c1 / per);
-        const uint32_t wc = vcodes + 4u * (p1 * wpp + c0 / per), wd = vcodes + 4u * (p1 * wpp + c1 / per);
-        const int sh0 = vb * (c0 % per), sh1 = vb * (c1 % per);
-        const uint32_t a0 = dequant_pair(lds32(wa), sh0, mask2, m0.x, m0.y);
-        const uint32_t a1 = dequant_pair(lds32(wb), sh1, mask2, m0.x, m0.y);
-        const uint32_t a2 = dequant_pair(lds32(wc), sh0, mask2, m1.x, m1.y);
-        const uint32_t a3 = dequant_pair(lds32(wd), sh1, mask2, m1.x, m1.y);
+        const uint32_t a0 = dequant_pair(lds32(base0 + 4 * (c0 / per)), sh0, mask2, m0.x, m0.y);
+        const uint32_t a1 = dequant_pair(lds32(base0 + 4 * (c1 / per)), sh1, mask2, m0.x, m0.y);
+        const uint32_t a2 = dequant_pair(lds32(base1 + 4 * (c0 / per)), sh0, mask2, m1.x, m1.y);
+        const uint32_t a3 = dequant_pair(lds32(base1 + 4 * (c1 / per)), sh1, mask2, m1.x, m1.y);
         mma16816(acc.o[cm], a0, a1, a2, a3, pb[tb][0], pb[tb][1]);
       }
     }
@@ -342,15 +358,21 @@ __device__ __forceinline__ void pv_fp16(WarpAcc<D>& acc, uint32_t vrows, int lan
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) {
+struct HeadItems {
+  int start[5];       // first item of each V class (tiles), start[4] = first zone-C item
+  int64_t off[4];     // byte offset of each class's first tile in zone A
+  int tbytes[4];
+  int nv[4];
+};
+
+template <int D, bool QLO>
+__global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int head = blockIdx.y, split = blockIdx.x, n_split = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.h_q / P.h_kv;
   const int b = head / P.h_kv, j = head % P.h_kv;
-  const rdkv_head_plan hp = plan_heads(P.plan)[head];
-  const int16_t* slot_ch = plan_slots(P.plan) + (int64_t)head * plan_header(P.plan)->slot_stride;
+  const rdkv_head_plan* hpp = plan_heads(P.plan) + head;
 
   // shared memory map
   KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
@@ -358,16 +380,97 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
   uint4* qfragc = reinterpret_cast<uint4*>(qv + kMaxKB * 32);                      // [D/16][32] hi, lo
   uint64_t* bars = reinterpret_cast<uint64_t*>(qfragc + (D / 16) * 32);           // [warps][kMaxInflight]
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
-  float* red = reinterpret_cast<float*>(ring_pos + kDecWarps * kMaxInflight);      // [warps][8][D + 2]
   unsigned char* ring = smem + decode_fixed_smem(D);
-  __shared__ int nkb_s;
+  float* red = reinterpret_cast<float*>(ring);                                     // [warps][8][D + 2], after the loop
+  __shared__ int seg_kb_s[5];
+  __shared__ int is_last;
+
+  // items of this head and of this split
+  HeadItems hi;
+  {
+    int t = 0;
+    int64_t off = hpp->a_off;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      hi.start[c] = t;
+      hi.off[c] = off;
+      hi.tbytes[c] = hpp->tile_bytes[c];
+      hi.nv[c] = hpp->n_v[c];
+      t += hpp->tiles[c];
+      off += (int64_t)hpp->tiles[c] * hi.tbytes[c];
+    }
+    hi.start[4] = t;
+  }
+  const int64_t b_row = hpp->b_row;
+  const int RW = hpp->row_words, meta_slots = hpp->meta_slots;
+  const int len_c = min(*P.len_dev, P.cap_c);
+  const int n_items = hi.start[4] + ceil_div(len_c, kCRows);
+  const int i0 = (int)((int64_t)n_items * split / n_split), i1 = (int)((int64_t)n_items * (split + 1) / n_split);
+  const int my_n = i1 - i0 > warp ? ceil_div(i1 - i0 - warp, kDecWarps) : 0;
+
+  auto item_cls = [&](int it) { return it < hi.start[1] ? 0 : it < hi.start[2] ? 1 : it < hi.start[3] ? 2 : it < hi.start[4] ? 3 : -1; };
+
+  // per-warp ring of shared memory filled by bulk copies (lane 0 issues)
+  unsigned char* wring = ring + (int64_t)warp * P.ring_bytes;
+  uint64_t* wbar = bars + warp * kMaxInflight;
+  int* wpos = ring_pos + warp * kMaxInflight;
+  uint32_t head_v = 0, tail_v = 0;     // virtual ring offsets (bytes)
+  uint32_t vend[kMaxInflight];         // lane 0 only
+  int issued = 0, done = 0;
+  auto issue = [&]() {
+    if (issued == done) head_v = tail_v = 0;  // empty ring: start at its beginning
+    while (issued < my_n && issued - done < kMaxInflight) {
+      const int it = i0 + warp + issued * kDecWarps;
+      const int cls = item_cls(it);
+      uint32_t sz, a_bytes = 0;
+      int c_row = 0;
+      if (cls >= 0) {
+        a_bytes = (uint32_t)hi.tbytes[cls];
+        sz = (uint32_t)align_up(a_bytes + (cls == 3 ? kTile * D * 2 : 0), 128);
+      } else {
+        c_row = (it - hi.start[4]) * kCRows;
+        sz = 2u * kCRows * D * 2;
+      }
+      uint32_t phys = head_v % (uint32_t)P.ring_bytes;
+      uint32_t need = sz;
+      if (phys + sz > (uint32_t)P.ring_bytes) { need += (uint32_t)P.ring_bytes - phys; phys = 0; }
+      if (head_v - tail_v + need > (uint32_t)P.ring_bytes) break;
+      head_v += need;
+      const int slot = issued % kMaxInflight;
+      vend[slot] = head_v;
+      wpos[slot] = (int)phys;
+      unsigned char* dst = wring + phys;
+      uint64_t* bar = &wbar[slot];
+      if (cls >= 0) {
+        const int ti = it - hi.start[cls];
+        const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
+        mbar_arrive_expect_tx(bar, a_bytes + zb);
+        bulk_copy(dst, P.zone_a + hi.off[cls] + (int64_t)ti * a_bytes, a_bytes, bar);
+        if (zb) bulk_copy(dst + a_bytes, P.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar);
+      } else {
+        const int rows = min(kCRows, len_c - c_row);
+        const uint32_t bytes = (uint32_t)rows * D * 2;
+        const int64_t src = ((int64_t)head * P.cap_c + c_row) * D;
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_copy(dst, P.zone_c_k + src, bytes, bar);
+        bulk_copy(dst + kCRows * D * 2, P.zone_c_v + src, bytes, bar);
+      }
+      ++issued;
+    }
+  };
+  if (lane == 0) {
+    for (int k = 0; k < kMaxInflight; ++k) mbar_init(&wbar[k], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    issue();  // the first copies fly while the query fragments are built
+  }
 
   // k-block descriptors of this head's K rows (each block inside one width segment)
   if (tid == 0) {
     int nkb = 0, wbase = 0, sbase = 0, meta = 0;
     for (int seg = 0; seg < 4; ++seg) {
       const int w = 16 >> seg, per = 32 / w;
-      const int nslot = hp.k_words[seg] * per;
+      const int nslot = hpp->k_words[seg] * per;
+      seg_kb_s[seg] = nkb;
       for (int s0 = 0; s0 < nslot; s0 += 16) {
         KBDesc d;
         d.width = (int16_t)w;
@@ -377,28 +480,33 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
         d.pad = sbase + s0;  // first slot of the block (for the query fragments)
         kbd[nkb++] = d;
       }
-      wbase += hp.k_words[seg];
+      wbase += hpp->k_words[seg];
       sbase += nslot;
       if (w < 16) meta += nslot;
     }
-    nkb_s = nkb;
+    seg_kb_s[4] = nkb;
   }
   __syncthreads();
-  const int nkb = nkb_s;
+  const int nkb = seg_kb_s[4];
+  int seg_kb[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) seg_kb[i] = seg_kb_s[i];
   // query fragments: B[k = slot pair][n = head g] in slot order (zone A) and channel order (zone C)
+  const int16_t* slot_ch = plan_slots(P.plan) + (int64_t)head * plan_header(P.plan)->slot_stride;
   const int qbase = b * P.h_q + j * G;
   for (int i = tid; i < (nkb + D / 16) * 32; i += blockDim.x) {
     const int kb = i >> 5, ln = i & 31, g = ln >> 2, qq = ln & 3;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
-    const int offs[4] = {2 * qq, 2 * qq + 1, 2 * qq + 8, 2 * qq + 9};
     if (g < G) {
+#pragma unroll
       for (int e = 0; e < 4; ++e) {
+        const int off = 2 * qq + (e & 1) + 8 * (e >> 1);
         int ch;
         if (kb < nkb) {
           const KBDesc d = kbd[kb];
-          ch = offs[e] < d.nrem ? slot_ch[d.pad + offs[e]] : -1;
+          ch = off < d.nrem ? slot_ch[d.pad + off] : -1;
         } else {
-          ch = 16 * (kb - nkb) + offs[e];
+          ch = 16 * (kb - nkb) + off;
         }
         if (ch >= 0) v[e] = load_as_float(P.q, (int64_t)(qbase + g) * D + ch, P.dtype);
       }
@@ -406,106 +514,35 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
     if (kb < nkb) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
     else qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
   }
-  if (lane == 0)
-    for (int k = 0; k < kMaxInflight; ++k) mbar_init(&bars[warp * kMaxInflight + k], 1);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
-
-  // items of this head and of this split
-  int cls_tiles[4], n_tiles = 0;
-  for (int c = 0; c < 4; ++c) { cls_tiles[c] = hp.tiles[c]; n_tiles += hp.tiles[c]; }
-  const int len_c = min(*P.len_dev, P.cap_c);
-  const int n_items = n_tiles + ceil_div(len_c, kCRows);
-  const int i0 = (int)((int64_t)n_items * split / n_split), i1 = (int)((int64_t)n_items * (split + 1) / n_split);
-  const int my_n = i1 - i0 > warp ? ceil_div(i1 - i0 - warp, kDecWarps) : 0;
 
   WarpAcc<D> acc;
 #pragma unroll
   for (int cm = 0; cm < D / 16; ++cm) acc.o[cm][0] = acc.o[cm][1] = acc.o[cm][2] = acc.o[cm][3] = 0.f;
   acc.m[0] = acc.m[1] = -INFINITY;
   acc.l[0] = acc.l[1] = 0.f;
-
   const float sl2 = 1.4426950408889634f / sqrtf((float)D);
-  unsigned char* wring = ring + (int64_t)warp * P.ring_bytes;
-  uint64_t* wbar = bars + warp * kMaxInflight;
-  int* wpos = ring_pos + warp * kMaxInflight;
-  uint32_t head_v = 0, tail_v = 0;     // virtual ring offsets (bytes)
-  uint32_t vend[kMaxInflight];         // lane 0 only
-  int issued = 0, done = 0;
+  const int g = lane >> 2, q = lane & 3;
   bool ok = true;
 
-  auto item_info = [&](int it, int& cls, int& ti, int64_t& a_src, uint32_t& a_bytes, int& c_row) {
-    if (it < n_tiles) {
-      int t = it, c = 0;
-      int64_t off = hp.a_off;
-      while (t >= cls_tiles[c]) { off += (int64_t)cls_tiles[c] * hp.tile_bytes[c]; t -= cls_tiles[c]; ++c; }
-      cls = c; ti = t; a_src = off + (int64_t)t * hp.tile_bytes[c]; a_bytes = hp.tile_bytes[c]; c_row = -1;
-    } else {
-      cls = -1; ti = 0; a_src = 0; a_bytes = 0; c_row = (it - n_tiles) * kCRows;
-    }
-  };
-  auto stage_bytes = [&](int cls, uint32_t a_bytes) -> uint32_t {
-    if (cls < 0) return 2u * kCRows * D * 2;
-    return (uint32_t)align_up(a_bytes + (cls == 3 ? kTile * D * 2 : 0), 128);
-  };
-
-  while (done < my_n && ok) {
-    // issue as many items as the ring and the slots allow (lane 0)
-    if (lane == 0) {
-      if (issued == done) head_v = tail_v = 0;  // empty ring: start at its beginning
-      while (issued < my_n && issued - done < kMaxInflight) {
-        const int it = i0 + warp + issued * kDecWarps;
-        int cls, ti, c_row;
-        int64_t a_src;
-        uint32_t a_bytes;
-        item_info(it, cls, ti, a_src, a_bytes, c_row);
-        const uint32_t sz = stage_bytes(cls, a_bytes);
-        uint32_t phys = head_v % (uint32_t)P.ring_bytes;
-        uint32_t need = sz;
-        if (phys + sz > (uint32_t)P.ring_bytes) { need += (uint32_t)P.ring_bytes - phys; phys = 0; }
-        if (head_v - tail_v + need > (uint32_t)P.ring_bytes) break;
-        head_v += need;
-        const int slot = issued % kMaxInflight;
-        vend[slot] = head_v;
-        wpos[slot] = (int)phys;
-        unsigned char* dst = wring + phys;
-        uint64_t* bar = &wbar[slot];
-        if (cls >= 0) {
-          const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
-          mbar_arrive_expect_tx(bar, a_bytes + zb);
-          bulk_copy(dst, P.zone_a + a_src, a_bytes, bar);
-          if (zb) bulk_copy(dst + a_bytes, P.zone_b + (hp.b_row + (int64_t)kTile * ti) * D, zb, bar);
-        } else {
-          const int rows = min(kCRows, len_c - c_row);
-          const uint32_t bytes = (uint32_t)rows * D * 2;
-          const int64_t src = ((int64_t)head * P.cap_c + c_row) * D;
-          mbar_arrive_expect_tx(bar, 2 * bytes);
-          bulk_copy(dst, P.zone_c_k + src, bytes, bar);
-          bulk_copy(dst + kCRows * D * 2, P.zone_c_v + src, bytes, bar);
-        }
-        ++issued;
-      }
-    }
+  while (done < my_n) {
+    if (lane == 0) issue();
     __syncwarp();
     const int slot = done % kMaxInflight;
-    const uint32_t parity = (uint32_t)(done / kMaxInflight) & 1u;
-    const bool arrived = mbar_wait(&wbar[slot], parity);
+    const bool arrived = mbar_wait(&wbar[slot], (uint32_t)(done / kMaxInflight) & 1u);
     if (__any_sync(0xffffffffu, !arrived)) {
       ok = false;
       break;
     }
     const uint32_t st = smem_u32(wring + wpos[slot]);
     const int it = i0 + warp + done * kDecWarps;
-    int cls, ti, c_row;
-    int64_t a_src;
-    uint32_t a_bytes;
-    item_info(it, cls, ti, a_src, a_bytes, c_row);
+    const int cls = item_cls(it);
     if (cls >= 0) {
-      const int n_real = min(kTile, hp.n_v[cls] - kTile * ti);
-      const uint32_t kmeta = st + 4u * kTile * hp.row_words;
+      const int ti = it - hi.start[cls];
+      const int n_real = min(kTile, hi.nv[cls] - kTile * ti);
+      const uint32_t kmeta = st + 4u * kTile * RW;
       float s[2][4];
-      tile_logits<D>(st, kmeta, hp.row_words, nkb, kbd, qv, lane, s);
-      const int g = lane >> 2;
+      tile_logits<D, QLO>(st, kmeta, RW, seg_kb, kbd, qv, lane, s);
 #pragma unroll
       for (int tb = 0; tb < 2; ++tb) {
         const bool va = 16 * tb + g < n_real, vb = 16 * tb + g + 8 < n_real;
@@ -516,14 +553,13 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
       }
       uint32_t pb[2][2];
       softmax_update<D, 2>(acc, s, pb);
-      const uint32_t vcodes = kmeta + 4u * hp.meta_slots;
-      if (cls < 3) {
-        const int vb = 2 << cls;
-        tile_pv_packed<D>(acc, vcodes, vcodes + (uint32_t)(kTile * D * vb / 8), vb, lane, pb);
-      } else {
-        pv_fp16<D, 2>(acc, st + a_bytes, lane, pb);
-      }
+      const uint32_t vcodes = kmeta + 4u * meta_slots;
+      if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 2 / 8), lane, pb);
+      else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 4 / 8), lane, pb);
+      else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 8 / 8), lane, pb);
+      else pv_fp16<D, 2>(acc, st + (uint32_t)hi.tbytes[3], lane, pb);
     } else {
+      const int c_row = (it - hi.start[4]) * kCRows;
       const int rows = min(kCRows, len_c - c_row);
       if (rows < kCRows) {  // clear the rows the copy did not fill (they meet p = 0 in the products)
         uint32_t* kz = reinterpret_cast<uint32_t*>(wring + wpos[slot]);
@@ -542,9 +578,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
         ldsm_x4(st + 2u * (row * D + col), a0, a1, a2, a3);
         const uint4 qf = qfragc[kb * 32 + lane];
         mma16816(s[0], a0, a1, a2, a3, qf.x, qf.y);
-        mma16816(s[0], a0, a1, a2, a3, qf.z, qf.w);
+        if (QLO) mma16816(s[0], a0, a1, a2, a3, qf.z, qf.w);
       }
-      const int g = lane >> 2;
       const bool va = g < rows, vb = g + 8 < rows;
       s[0][0] = va ? s[0][0] * sl2 : -INFINITY;
       s[0][1] = va ? s[0][1] * sl2 : -INFINITY;
@@ -561,16 +596,17 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
     ++done;
   }
   if (!ok) {
-    if (lane == 0) atomicExch(P.error, (int)RDKV_ERR_TIMEOUT);
-    // wait (bounded) for this warp's copies still in flight before leaving
-    if (lane == 0)
+    if (lane == 0) {
+      atomicExch(P.error, (int)RDKV_ERR_TIMEOUT);
+      // wait (bounded) for this warp's copies still in flight before the ring is reused
       for (int k = done; k < issued; ++k)
         if (!mbar_wait(&wbar[k % kMaxInflight], (uint32_t)(k / kMaxInflight) & 1u)) break;
+    }
     __syncwarp();
   }
+  __syncthreads();  // every ring drained: the ring area now holds the warps' results
 
   // warp result -> shared memory: m, l per head; O per head and channel
-  const int g = lane >> 2, q = lane & 3;
   float l0 = acc.l[0], l1 = acc.l[1];
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -592,51 +628,52 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams P) 
     rw[(2 * q + 1) * (D + 2) + D + 1] = l1;
   }
   __syncthreads();
-  // combine the warps; write this split's partial result for the G heads
-  float* out = P.partial + ((int64_t)head * n_split + split) * G * (D + 2);
+  // combine the warps; write this split's partial result (m, l, unnormalised o) for the G heads
+  float* part = P.partial + (int64_t)head * n_split * G * (D + 2);
+  float* mine = part + (int64_t)split * G * (D + 2);
   for (int i = tid; i < G * (D + 2); i += blockDim.x) {
     const int h = i / (D + 2), c = i % (D + 2);
     float M = -INFINITY;
     for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red[((int64_t)w * 8 + h) * (D + 2) + D]);
-    float val = 0.f;
-    if (c == D) {
-      val = M;
-    } else {
+    float val = M;
+    if (c != D) {
+      val = 0.f;
       for (int w = 0; w < kDecWarps; ++w) {
         const float mw = red[((int64_t)w * 8 + h) * (D + 2) + D];
         if (mw != -INFINITY) val += exp2f(mw - M) * red[((int64_t)w * 8 + h) * (D + 2) + c];
       }
     }
-    out[i] = val;
+    mine[i] = val;
   }
-}
-
-// out[b][h][c] = sum_s 2^(M_s - M) O_s[c] / sum_s 2^(M_s - M) L_s   (0 when no token)
-__global__ void decode_merge_kernel(const float* __restrict__ partial, int n_split, int h_q, int h_kv, int D,
-                                    float* __restrict__ out) {
-  const int bh = blockIdx.x;  // b * h_q + h
-  const int G = h_q / h_kv;
-  const int b = bh / h_q, h = bh % h_q;
-  const int head = b * h_kv + h / G, hl = h % G;
-  const int c = threadIdx.x;
-  const float* p = partial + (int64_t)head * n_split * G * (D + 2) + hl * (D + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < n_split; ++s) M = fmaxf(M, p[(int64_t)s * G * (D + 2) + D]);
-  float o = 0.f, l = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_split; ++s) {
-      const float* ps = p + (int64_t)s * G * (D + 2);
-      const float ms = ps[D];
-      if (ms == -INFINITY) continue;
-      const float f = exp2f(ms - M);
-      o += f * ps[c];
-      l += f * ps[D + 1];
+  // the last block of this head merges every split: out = sum 2^(M_s - M) O_s / sum 2^(M_s - M) L_s
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = atomicAdd(&P.tickets[head], 1) == n_split - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int i = tid; i < G * D; i += blockDim.x) {
+    const int h = i / D, c = i % D;
+    const float* ph = part + h * (D + 2);
+    float M = -INFINITY;
+    for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, __ldcg(ph + (int64_t)sp * G * (D + 2) + D));
+    float o = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+      for (int sp = 0; sp < n_split; ++sp) {
+        const float* ps = ph + (int64_t)sp * G * (D + 2);
+        const float ms = __ldcg(ps + D);
+        if (ms == -INFINITY) continue;
+        const float f = exp2f(ms - M);
+        o += f * __ldcg(ps + c);
+        l += f * __ldcg(ps + D + 1);
+      }
     }
+    P.out[((int64_t)b * P.h_q + j * G + h) * D + c] = l > 0.f ? o / l : 0.f;
   }
-  out[(int64_t)bh * D + c] = l > 0.f ? o / l : 0.f;
 }
 
 constexpr int64_t kDecodeSmemLimit = 227 * 1024 - 1024;  // per-block limit less room for static shared memory
+constexpr int64_t kTwoBlockSmem = 112 * 1024;             // two blocks per SM below this
 
 struct DecodeGeom {
   int64_t max_item;
@@ -644,6 +681,7 @@ struct DecodeGeom {
   int ring_bytes;
   size_t smem;
   size_t partial_bytes;
+  size_t ticket_off;   // tickets then the status word
 };
 
 static DecodeGeom decode_geom(const rdkv_cache* c) {
@@ -652,19 +690,30 @@ static DecodeGeom decode_geom(const rdkv_cache* c) {
   const int D = s.head_dim, G = s.h_q / s.h_kv;
   const int n_heads = s.batch * s.h_kv;
   const int sms = num_sms();
+  const int64_t fixed = decode_fixed_smem(D);
+  const int64_t max_item = std::max<int64_t>(align_up(c->sizes.max_tile_bytes + kTile * D * 2, 128), 2 * kCRows * D * 2);
+  g.max_item = max_item;
+  int64_t ring = ((kTwoBlockSmem - fixed) / kDecWarps) / 128 * 128;
+  int blocks_per_sm = 2;
+  if (ring < max_item) {
+    ring = std::min<int64_t>(align_up(2 * max_item, 128), ((kDecodeSmemLimit - fixed) / kDecWarps) / 128 * 128);
+    blocks_per_sm = 1;
+  }
+  ring = std::max<int64_t>(ring, align_up(decode_reduce_bytes(D), 128 * kDecWarps) / kDecWarps);
+  g.ring_bytes = (int)ring;
+  g.smem = (size_t)(fixed + (int64_t)kDecWarps * ring);
   const int64_t items = ceil_div64(c->sizes.index_slots, kTile) + (int64_t)n_heads * ceil_div(c->cap_c, kCRows);
   const int64_t per_head = std::max<int64_t>(1, items / std::max(1, n_heads));
-  int splits = ceil_div(2 * sms, n_heads);
-  splits = (int)std::max<int64_t>(1, std::min<int64_t>(splits, ceil_div64(per_head, 2 * kDecWarps)));
+  int splits = ceil_div(blocks_per_sm * sms, n_heads);
+  splits = (int)std::max<int64_t>(1, std::min<int64_t>(splits, ceil_div64(per_head, kDecWarps)));
   g.splits = std::min(splits, 1024);
-  const int64_t max_item = std::max<int64_t>(align_up(c->sizes.max_tile_bytes + kTile * D * 2, 128), 2 * kCRows * D * 2);
-  const int64_t fixed = decode_fixed_smem(D);
-  const int64_t ring_cap = ((kDecodeSmemLimit - fixed) / kDecWarps) / 128 * 128;
-  g.max_item = max_item;
-  g.ring_bytes = (int)std::min<int64_t>(std::max<int64_t>(align_up(2 * max_item, 128), 24 * 1024), ring_cap);
-  g.smem = (size_t)(fixed + (int64_t)kDecWarps * g.ring_bytes);
   g.partial_bytes = (size_t)align_up((int64_t)n_heads * g.splits * G * (D + 2) * 4, 256);
+  g.ticket_off = g.partial_bytes;
   return g;
+}
+
+static size_t decode_ws_bytes(const DecodeGeom& g, int n_heads) {
+  return g.ticket_off + (size_t)align_up(((int64_t)n_heads + 1) * 4, 256);
 }
 
 rdkv_status check_cache_public(const rdkv_cache* c);
@@ -675,7 +724,7 @@ using namespace rdkv;
 
 extern "C" size_t rdkv_decode_workspace_bytes(const rdkv_cache* cache) {
   if (check_cache_public(cache) != RDKV_OK) return 0;
-  return decode_geom(cache).partial_bytes + 256;
+  return decode_ws_bytes(decode_geom(cache), cache->shape.batch * cache->shape.h_kv);
 }
 
 extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, float* out, void* ws, size_t ws_bytes,
@@ -683,12 +732,13 @@ extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, 
   rdkv_status st = check_cache_public(cache);
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(q && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  const rdkv_shape& s = cache->shape;
+  const int n_heads = s.batch * s.h_kv;
   const DecodeGeom geo = decode_geom(cache);
-  RDKV_REQUIRE(ws && ws_bytes >= geo.partial_bytes + 256, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)",
-               ws_bytes, geo.partial_bytes + 256);
+  const size_t need = decode_ws_bytes(geo, n_heads);
+  RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
-  const rdkv_shape& s = cache->shape;
   cudaStream_t cs = (cudaStream_t)stream;
   DecodeParams P;
   P.plan = cache->plan;
@@ -697,34 +747,41 @@ extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, 
   P.zone_c_k = cache->zone_c_k;
   P.zone_c_v = cache->zone_c_v;
   P.q = q;
-  P.error = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + geo.partial_bytes);
   P.partial = static_cast<float*>(ws);
+  P.tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + geo.ticket_off);
+  P.error = P.tickets + n_heads;
+  P.out = out;
+  P.len_dev = cache->len_dev;
   P.dtype = s.dtype;
   P.h_q = s.h_q;
   P.h_kv = s.h_kv;
   P.cap_c = cache->cap_c;
-  P.len_dev = cache->len_dev;
   P.ring_bytes = geo.ring_bytes;
-  RDKV_TRY_CUDA(cudaMemsetAsync(P.error, 0, 4, cs), "decode status reset");
-  const dim3 grid(geo.splits, s.batch * s.h_kv);
+  // tickets and the status word start at zero for every launch
+  RDKV_TRY_CUDA(cudaMemsetAsync(P.tickets, 0, ((size_t)n_heads + 1) * 4, cs), "decode ticket reset");
   // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is captured)
-  static size_t smem_set[2][64] = {};
+  static size_t smem_set[4][64] = {};
   int dev = 0;
   RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
-  const int ki = s.head_dim == 128 ? 1 : 0;
+  const bool qlo = s.dtype == RDKV_F32;
+  const int ki = (s.head_dim == 128 ? 2 : 0) + (qlo ? 1 : 0);
+  const void* fn = ki == 3 ? (const void*)decode_kernel<128, true>
+                 : ki == 2 ? (const void*)decode_kernel<128, false>
+                 : ki == 1 ? (const void*)decode_kernel<64, true>
+                           : (const void*)decode_kernel<64, false>;
   if (dev < 64 && geo.smem > smem_set[ki][dev]) {
-    RDKV_TRY_CUDA(cudaFuncSetAttribute(ki ? (const void*)decode_kernel<128> : (const void*)decode_kernel<64>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmemLimit),
+    RDKV_TRY_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmemLimit),
                   "decode smem");
     smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
   }
-  if (ki)
-    decode_kernel<128><<<grid, kDecWarps * 32, geo.smem, cs>>>(P);
-  else
-    decode_kernel<64><<<grid, kDecWarps * 32, geo.smem, cs>>>(P);
+  const dim3 grid(geo.splits, n_heads);
+  switch (ki) {
+    case 3: decode_kernel<128, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    case 2: decode_kernel<128, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    case 1: decode_kernel<64, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    default: decode_kernel<64, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+  }
   RDKV_CHECK_LAUNCH("decode");
-  decode_merge_kernel<<<s.batch * s.h_q, s.head_dim, 0, cs>>>(P.partial, geo.splits, s.h_q, s.h_kv, s.head_dim, out);
-  RDKV_CHECK_LAUNCH("decode merge");
   return RDKV_OK;
 }
 
@@ -733,9 +790,10 @@ extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* w
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(ws, RDKV_ERR_INVALID_ARG, "NULL workspace");
   const DecodeGeom geo = decode_geom(cache);
+  const int n_heads = cache->shape.batch * cache->shape.h_kv;
   int32_t v = 0;
-  RDKV_TRY_CUDA(cudaMemcpyAsync(&v, static_cast<const char*>(ws) + geo.partial_bytes, 4, cudaMemcpyDeviceToHost,
-                                (cudaStream_t)stream),
+  RDKV_TRY_CUDA(cudaMemcpyAsync(&v, static_cast<const char*>(ws) + geo.ticket_off + 4 * (size_t)n_heads, 4,
+                                cudaMemcpyDeviceToHost, (cudaStream_t)stream),
                 "status read");
   RDKV_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status sync");
   if (v != RDKV_OK) set_error("decode reported status %d (a bounded wait ran out)", v);

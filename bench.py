@@ -342,7 +342,7 @@ def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, de
         t_dec += time.perf_counter() - t0
     h2d = sum(t.numel() * t.element_size() for trip in h_pre for t in trip) + \
         sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv))
-    d2h = h_out.numel() * 4 + L * 88
+    d2h = h_out.numel() * 4 + L * 96
     return {"value": round(ws * dec_bytes / (t_dec / steps) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "note": "decode phase wall time incl. per-decode-step H2D of q/k/v and D2H of outputs; "

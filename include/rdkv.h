@@ -88,11 +88,12 @@ typedef struct rdkv_plan_header {
   int64_t index_slots;     /* index-map entries */
   int64_t kept_tokens;     /* kept prefix tokens over all heads */
   int64_t max_tile_bytes;  /* largest zone-A tile present */
+  int64_t max_stage_bytes; /* largest tile plus the zone-B rows it carries (decode staging) */
 } rdkv_plan_header;
 
 /* Host copy of the totals, from rdkv_plan_sizes. */
 typedef struct rdkv_sizes {
-  int64_t zone_a_bytes, zone_b_rows, index_slots, kept_tokens, max_tile_bytes;
+  int64_t zone_a_bytes, zone_b_rows, index_slots, kept_tokens, max_tile_bytes, max_stage_bytes;
   int32_t status, n_heads;
 } rdkv_sizes;
 

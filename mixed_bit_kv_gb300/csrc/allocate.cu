@@ -254,7 +254,7 @@ __global__ void plan_offsets_kernel(char* plan, int batch, int h_kv, int D, int 
   auto* hdr = reinterpret_cast<rdkv_plan_header*>(plan);
   auto* heads = reinterpret_cast<rdkv_head_plan*>(plan + heads_off);
   const int n_heads = batch * h_kv;
-  int64_t a = 0, brow = 0, slot = 0, kept = 0, maxt = 0;
+  int64_t a = 0, brow = 0, slot = 0, kept = 0, maxt = 0, maxs = 0;
   for (int i = 0; i < n_heads; ++i) {
     rdkv_head_plan& hp = heads[i];
     hp.a_off = a;
@@ -267,6 +267,8 @@ __global__ void plan_offsets_kernel(char* plan, int batch, int h_kv, int D, int 
       nt += hp.tiles[c];
       kept += hp.n_v[c];
       if (hp.tiles[c] && hp.tile_bytes[c] > maxt) maxt = hp.tile_bytes[c];
+      const int64_t stage = hp.tile_bytes[c] + (c == 3 ? (int64_t)kTile * D * 2 : 0);
+      if (hp.tiles[c] && stage > maxs) maxs = stage;
     }
     slot += (int64_t)kTile * nt;
   }
@@ -287,6 +289,7 @@ __global__ void plan_offsets_kernel(char* plan, int batch, int h_kv, int D, int 
   hdr->index_slots = slot;
   hdr->kept_tokens = kept;
   hdr->max_tile_bytes = maxt;
+  hdr->max_stage_bytes = maxs;
 }
 
 // ---------------------------------------------------------------- shape checks shared with the other calls
@@ -428,6 +431,7 @@ extern "C" rdkv_status rdkv_plan_sizes(const void* plan, rdkv_sizes* out, void* 
   out->index_slots = h.index_slots;
   out->kept_tokens = h.kept_tokens;
   out->max_tile_bytes = h.max_tile_bytes;
+  out->max_stage_bytes = h.max_stage_bytes;
   out->status = h.status;
   out->n_heads = h.n_heads;
   if (h.status != RDKV_OK) set_error("plan status %d: a gain was NaN, infinite or negative", h.status);

@@ -45,7 +45,7 @@ struct KBDesc {
 
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings).
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
-  return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + kDecWarps * kMaxInflight * 12) + 127) /
+  return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + kDecWarps * kMaxInflight * 16) + 127) /
          128 * 128;
 }
 // The warps' partial results are combined in the ring area once every ring is drained.
@@ -225,63 +225,65 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
 // channels use the stored fp16 value against q (split the same way when q
 // carries more than fp16 precision).
 template <int W, bool QLO>
-__device__ __forceinline__ void k_segment(uint32_t kw, uint32_t kmeta, int RW, int kb0, int kb1, const KBDesc* kbd,
-                                          const float4* qv, int lane, float (&s)[2][4], float& bias) {
-  const int g = lane >> 2, q = lane & 3;
-  const uint32_t row0 = kw + 4u * (g * RW), rstep = 4u * (8 * RW);   // rows g, g+8, g+16, g+24
-  // word offsets (relative to the block's first word) and shifts of this lane's two slot pairs
+__device__ __forceinline__ void k_segment(const uint32_t (&rows)[4], uint32_t kmeta, int kb0, int kb1,
+                                          const KBDesc* kbd, const float4* qv, int lane, float (&s)[2][4],
+                                          float& bias) {
+  const int q = lane & 3;
+  // byte offsets (from the block's first word) and shifts of this lane's two slot pairs
   constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
-  const int o0 = W == 16 ? q : W == 8 ? (q >> 1) : 0;
-  const int o1 = W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0;
+  const uint32_t o0 = 4u * (W == 16 ? q : W == 8 ? (q >> 1) : 0);
+  const uint32_t o1 = 4u * (W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0);
   const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
   const int sh1 = W == 2 ? 2 * q + 8 : sh0;
   for (int kb = kb0; kb < kb1; ++kb) {
     const KBDesc d = kbd[kb];
-    const float4 qq = qv[kb * 32 + lane];  // q_g at slots 2q, 2q+1, 2q+8, 2q+9 (0 for pads)
-    const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
-    const uint32_t w0 = 4u * (d.word0 + o0), w1 = 4u * (d.word0 + o1);
-    uint4 bq;
+    const float4 qq = qv[kb * 32 + lane];  // q_g at slots 2q, 2q+1, 2q+8, 2q+9 (0 for pads and missing slots)
+    const uint32_t wb = 4u * (uint32_t)d.word0;
+    uint32_t bh0, bh1, bl0 = 0, bl1 = 0;
     if (W == 16) {
-      bq = split_hi_lo(qq.x, qq.y, qq.z, qq.w);
+      if (QLO) {
+        const uint4 t = split_hi_lo(qq.x, qq.y, qq.z, qq.w);
+        bh0 = t.x; bh1 = t.y; bl0 = t.z; bl1 = t.w;
+      } else {
+        bh0 = pack_half2(qq.x, qq.y);
+        bh1 = pack_half2(qq.z, qq.w);
+      }
     } else {
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (v0) {
-        const uint2 m = lds64(kmeta + 8 * (d.meta0 + q));
-        const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&m.x));
-        const float2 z2 = __half22float2(*reinterpret_cast<const __half2*>(&m.y));
-        sc[0] = s2.x; sc[1] = s2.y;
-        bias = fmaf(qq.x, z2.x, fmaf(qq.y, z2.y, bias));
-      }
-      if (v1) {
-        const uint2 m = lds64(kmeta + 8 * (d.meta0 + q + 4));
-        const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&m.x));
-        const float2 z2 = __half22float2(*reinterpret_cast<const __half2*>(&m.y));
-        sc[2] = s2.x; sc[3] = s2.y;
-        bias = fmaf(qq.z, z2.x, fmaf(qq.w, z2.y, bias));
-      }
-      bq = split_hi_lo(qq.x * sc[0], qq.y * sc[1], qq.z * sc[2], qq.w * sc[3]);
+      // a pair past the segment end reads the block's first (valid) pair: its q entries are 0
+      const int p0 = d.meta0 + (2 * q < d.nrem ? q : 0), p1 = d.meta0 + (2 * q + 8 < d.nrem ? q + 4 : 0);
+      const uint2 m0 = lds64(kmeta + 8u * p0), m1 = lds64(kmeta + 8u * p1);
+      const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&m0.x));
+      const float2 z0 = __half22float2(*reinterpret_cast<const __half2*>(&m0.y));
+      const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&m1.x));
+      const float2 z1 = __half22float2(*reinterpret_cast<const __half2*>(&m1.y));
+      bias = fmaf(qq.x, z0.x, fmaf(qq.y, z0.y, fmaf(qq.z, z1.x, fmaf(qq.w, z1.y, bias))));
+      const uint4 t = split_hi_lo(qq.x * s0.x, qq.y * s0.y, qq.z * s1.x, qq.w * s1.y);
+      bh0 = t.x; bh1 = t.y; bl0 = t.z; bl1 = t.w;
     }
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
-      const uint32_t r0 = row0 + 2u * tb * rstep, r1 = r0 + rstep;
-      uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+      const uint32_t r0 = rows[2 * tb] + wb, r1 = rows[2 * tb + 1] + wb;
+      uint32_t a0, a1, a2, a3;
       if (W == 16) {
-        if (v0) { a0 = lds32(r0 + w0); a1 = lds32(r1 + w0); }
-        if (v1) { a2 = lds32(r0 + w1); a3 = lds32(r1 + w1); }
+        // raw fp16 words past the segment end may hold anything: zero them
+        const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
+        const uint32_t x0 = lds32(r0 + o0), x1 = lds32(r1 + o0), x2 = lds32(r0 + o1), x3 = lds32(r1 + o1);
+        a0 = v0 ? x0 : 0u; a1 = v0 ? x1 : 0u; a2 = v1 ? x2 : 0u; a3 = v1 ? x3 : 0u;
       } else {
-        if (v0) {
-          const uint32_t x0 = lds32(r0 + w0), x1 = lds32(r1 + w0);
-          a0 = exact_codes(x0, sh0, mask2);
-          a1 = exact_codes(x1, sh0, mask2);
-          if (W == 2 && v1) { a2 = exact_codes(x0, sh1, mask2); a3 = exact_codes(x1, sh1, mask2); }
-        }
-        if (W != 2 && v1) {
-          a2 = exact_codes(lds32(r0 + w1), sh1, mask2);
-          a3 = exact_codes(lds32(r1 + w1), sh1, mask2);
+        // codes past the segment end are small integers met by zero query entries
+        const uint32_t x0 = lds32(r0 + o0), x1 = lds32(r1 + o0);
+        a0 = exact_codes(x0, sh0, mask2);
+        a1 = exact_codes(x1, sh0, mask2);
+        if (W == 2) {
+          a2 = exact_codes(x0, sh1, mask2);
+          a3 = exact_codes(x1, sh1, mask2);
+        } else {
+          a2 = exact_codes(lds32(r0 + o1), sh1, mask2);
+          a3 = exact_codes(lds32(r1 + o1), sh1, mask2);
         }
       }
-      mma16816(s[tb], a0, a1, a2, a3, bq.x, bq.y);
-      if (W != 16 || QLO) mma16816(s[tb], a0, a1, a2, a3, bq.z, bq.w);
+      mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
+      if (W != 16 || QLO) mma16816(s[tb], a0, a1, a2, a3, bl0, bl1);
     }
   }
 }
@@ -290,12 +292,15 @@ template <int D, bool QLO>
 __device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW, const int (&seg_kb)[5],
                                             const KBDesc* kbd, const float4* qv, int lane, float (&s)[2][4]) {
   float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
+  const int g = lane >> 2;
+  const uint32_t rows[4] = {kw + 4u * (g * RW), kw + 4u * ((g + 8) * RW), kw + 4u * ((g + 16) * RW),
+                            kw + 4u * ((g + 24) * RW)};
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) s[tb][0] = s[tb][1] = s[tb][2] = s[tb][3] = 0.f;
-  if (seg_kb[1] > seg_kb[0]) k_segment<16, QLO>(kw, kmeta, RW, seg_kb[0], seg_kb[1], kbd, qv, lane, s, bias);
-  if (seg_kb[2] > seg_kb[1]) k_segment<8, QLO>(kw, kmeta, RW, seg_kb[1], seg_kb[2], kbd, qv, lane, s, bias);
-  if (seg_kb[3] > seg_kb[2]) k_segment<4, QLO>(kw, kmeta, RW, seg_kb[2], seg_kb[3], kbd, qv, lane, s, bias);
-  if (seg_kb[4] > seg_kb[3]) k_segment<2, QLO>(kw, kmeta, RW, seg_kb[3], seg_kb[4], kbd, qv, lane, s, bias);
+  k_segment<16, QLO>(rows, kmeta, seg_kb[0], seg_kb[1], kbd, qv, lane, s, bias);
+  k_segment<8, QLO>(rows, kmeta, seg_kb[1], seg_kb[2], kbd, qv, lane, s, bias);
+  k_segment<4, QLO>(rows, kmeta, seg_kb[2], seg_kb[3], kbd, qv, lane, s, bias);
+  k_segment<2, QLO>(rows, kmeta, seg_kb[3], seg_kb[4], kbd, qv, lane, s, bias);
   // zero-point term: lanes (g, 0..3) hold parts of head g; S^T lane (g', q') needs heads 2q', 2q'+1
   const int q = lane & 3;
   bias += __shfl_xor_sync(0xffffffffu, bias, 1);
@@ -358,11 +363,10 @@ __device__ __forceinline__ void pv_fp16(WarpAcc<D>& acc, uint32_t vrows, int lan
   }
 }
 
-struct HeadItems {
-  int start[5];       // first item of each V class (tiles), start[4] = first zone-C item
-  int64_t off[4];     // byte offset of each class's first tile in zone A
-  int tbytes[4];
-  int nv[4];
+// Per-class values of a head, read with a class index without dynamic array indexing.
+struct ClassVals {
+  int64_t v[4];
+  __device__ __forceinline__ int64_t operator()(int c) const { return c == 0 ? v[0] : c == 1 ? v[1] : c == 2 ? v[2] : v[3]; }
 };
 
 template <int D, bool QLO>
@@ -380,72 +384,93 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   uint4* qfragc = reinterpret_cast<uint4*>(qv + kMaxKB * 32);                      // [D/16][32] hi, lo
   uint64_t* bars = reinterpret_cast<uint64_t*>(qfragc + (D / 16) * 32);           // [warps][kMaxInflight]
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
+  int* ring_item = ring_pos + kDecWarps * kMaxInflight;                            // [warps][kMaxInflight]
   unsigned char* ring = smem + decode_fixed_smem(D);
   float* red = reinterpret_cast<float*>(ring);                                     // [warps][8][D + 2], after the loop
+  // staging for the query fragments, in the ring area before any copy is issued into it
+  float* q_s = reinterpret_cast<float*>(ring);                                     // [8][D]
+  int16_t* slot_s = reinterpret_cast<int16_t*>(q_s + 8 * D);                       // [k_slots]
   __shared__ int seg_kb_s[5];
   __shared__ int is_last;
+  __shared__ int next_item;
 
   // items of this head and of this split
-  HeadItems hi;
+  ClassVals cstart, coff, ctb, cnv;  // first item, first byte in zone A, tile bytes, kept tokens per class
+  int zc_start;
   {
     int t = 0;
     int64_t off = hpp->a_off;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      hi.start[c] = t;
-      hi.off[c] = off;
-      hi.tbytes[c] = hpp->tile_bytes[c];
-      hi.nv[c] = hpp->n_v[c];
+      cstart.v[c] = t;
+      coff.v[c] = off;
+      ctb.v[c] = hpp->tile_bytes[c];
+      cnv.v[c] = hpp->n_v[c];
       t += hpp->tiles[c];
-      off += (int64_t)hpp->tiles[c] * hi.tbytes[c];
+      off += (int64_t)hpp->tiles[c] * hpp->tile_bytes[c];
     }
-    hi.start[4] = t;
+    zc_start = t;
   }
   const int64_t b_row = hpp->b_row;
   const int RW = hpp->row_words, meta_slots = hpp->meta_slots;
   const int len_c = min(*P.len_dev, P.cap_c);
-  const int n_items = hi.start[4] + ceil_div(len_c, kCRows);
+  const int n_items = zc_start + ceil_div(len_c, kCRows);
   const int i0 = (int)((int64_t)n_items * split / n_split), i1 = (int)((int64_t)n_items * (split + 1) / n_split);
-  const int my_n = i1 - i0 > warp ? ceil_div(i1 - i0 - warp, kDecWarps) : 0;
+  if (tid == 0) next_item = i0;
 
-  auto item_cls = [&](int it) { return it < hi.start[1] ? 0 : it < hi.start[2] ? 1 : it < hi.start[3] ? 2 : it < hi.start[4] ? 3 : -1; };
+  auto item_cls = [&](int it) {
+    return it < (int)cstart.v[1] ? 0 : it < (int)cstart.v[2] ? 1 : it < (int)cstart.v[3] ? 2 : it < zc_start ? 3 : -1;
+  };
 
   // per-warp ring of shared memory filled by bulk copies (lane 0 issues)
   unsigned char* wring = ring + (int64_t)warp * P.ring_bytes;
   uint64_t* wbar = bars + warp * kMaxInflight;
   int* wpos = ring_pos + warp * kMaxInflight;
   uint32_t head_v = 0, tail_v = 0;     // virtual ring offsets (bytes)
+  int* witem = ring_item + warp * kMaxInflight;
   uint32_t vend[kMaxInflight];         // lane 0 only
   int issued = 0, done = 0;
+  bool drained = false;                // lane 0: no item left for this block
+  int pending = -1;                    // lane 0: item taken but not yet issued (ring full)
   auto issue = [&]() {
     if (issued == done) head_v = tail_v = 0;  // empty ring: start at its beginning
-    while (issued < my_n && issued - done < kMaxInflight) {
-      const int it = i0 + warp + issued * kDecWarps;
+    while (!drained && issued - done < kMaxInflight) {
+      int it = pending;
+      if (it < 0) it = atomicAdd(&next_item, 1);  // items are taken in order of need: no warp idles early
+      if (it >= i1) {
+        drained = true;
+        break;
+      }
       const int cls = item_cls(it);
       uint32_t sz, a_bytes = 0;
       int c_row = 0;
       if (cls >= 0) {
-        a_bytes = (uint32_t)hi.tbytes[cls];
+        a_bytes = (uint32_t)ctb(cls);
         sz = (uint32_t)align_up(a_bytes + (cls == 3 ? kTile * D * 2 : 0), 128);
       } else {
-        c_row = (it - hi.start[4]) * kCRows;
+        c_row = (it - zc_start) * kCRows;
         sz = 2u * kCRows * D * 2;
       }
       uint32_t phys = head_v % (uint32_t)P.ring_bytes;
       uint32_t need = sz;
       if (phys + sz > (uint32_t)P.ring_bytes) { need += (uint32_t)P.ring_bytes - phys; phys = 0; }
-      if (head_v - tail_v + need > (uint32_t)P.ring_bytes) break;
+      if (head_v - tail_v + need > (uint32_t)P.ring_bytes) {
+        pending = it;
+        break;
+      }
+      pending = -1;
       head_v += need;
       const int slot = issued % kMaxInflight;
       vend[slot] = head_v;
       wpos[slot] = (int)phys;
+      witem[slot] = it;
       unsigned char* dst = wring + phys;
       uint64_t* bar = &wbar[slot];
       if (cls >= 0) {
-        const int ti = it - hi.start[cls];
+        const int ti = it - (int)cstart(cls);
         const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
         mbar_arrive_expect_tx(bar, a_bytes + zb);
-        bulk_copy(dst, P.zone_a + hi.off[cls] + (int64_t)ti * a_bytes, a_bytes, bar);
+        bulk_copy(dst, P.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar);
         if (zb) bulk_copy(dst + a_bytes, P.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar);
       } else {
         const int rows = min(kCRows, len_c - c_row);
@@ -461,8 +486,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   if (lane == 0) {
     for (int k = 0; k < kMaxInflight; ++k) mbar_init(&wbar[k], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    issue();  // the first copies fly while the query fragments are built
   }
+  // stage the query rows of the group and this head's slot table (one coalesced round trip each)
+  const int16_t* slot_ch = plan_slots(P.plan) + (int64_t)head * plan_header(P.plan)->slot_stride;
+  const int qbase = b * P.h_q + j * G;
+  const int k_slots = hpp->k_slots;
+  for (int i = tid; i < G * D; i += blockDim.x) q_s[i] = load_as_float(P.q, (int64_t)qbase * D + i, P.dtype);
+  for (int i = tid; i < k_slots; i += blockDim.x) slot_s[i] = slot_ch[i];
 
   // k-block descriptors of this head's K rows (each block inside one width segment)
   if (tid == 0) {
@@ -492,8 +522,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
 #pragma unroll
   for (int i = 0; i < 5; ++i) seg_kb[i] = seg_kb_s[i];
   // query fragments: B[k = slot pair][n = head g] in slot order (zone A) and channel order (zone C)
-  const int16_t* slot_ch = plan_slots(P.plan) + (int64_t)head * plan_header(P.plan)->slot_stride;
-  const int qbase = b * P.h_q + j * G;
   for (int i = tid; i < (nkb + D / 16) * 32; i += blockDim.x) {
     const int kb = i >> 5, ln = i & 31, g = ln >> 2, qq = ln & 3;
     float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -504,17 +532,18 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
         int ch;
         if (kb < nkb) {
           const KBDesc d = kbd[kb];
-          ch = off < d.nrem ? slot_ch[d.pad + off] : -1;
+          ch = off < d.nrem ? slot_s[d.pad + off] : -1;
         } else {
           ch = 16 * (kb - nkb) + off;
         }
-        if (ch >= 0) v[e] = load_as_float(P.q, (int64_t)(qbase + g) * D + ch, P.dtype);
+        if (ch >= 0) v[e] = q_s[g * D + ch];
       }
     }
     if (kb < nkb) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
     else qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
   }
-  __syncthreads();
+  __syncthreads();  // the staging area is free again: the rings may fill it
+  if (lane == 0) issue();
 
   WarpAcc<D> acc;
 #pragma unroll
@@ -525,9 +554,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   const int g = lane >> 2, q = lane & 3;
   bool ok = true;
 
-  while (done < my_n) {
+  while (true) {
     if (lane == 0) issue();
     __syncwarp();
+    if (__shfl_sync(0xffffffffu, issued, 0) == done) break;  // nothing in flight and nothing left
     const int slot = done % kMaxInflight;
     const bool arrived = mbar_wait(&wbar[slot], (uint32_t)(done / kMaxInflight) & 1u);
     if (__any_sync(0xffffffffu, !arrived)) {
@@ -535,11 +565,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       break;
     }
     const uint32_t st = smem_u32(wring + wpos[slot]);
-    const int it = i0 + warp + done * kDecWarps;
+    const int it = witem[slot];
     const int cls = item_cls(it);
     if (cls >= 0) {
-      const int ti = it - hi.start[cls];
-      const int n_real = min(kTile, hi.nv[cls] - kTile * ti);
+      const int ti = it - (int)cstart(cls);
+      const int n_real = min(kTile, (int)cnv(cls) - kTile * ti);
       const uint32_t kmeta = st + 4u * kTile * RW;
       float s[2][4];
       tile_logits<D, QLO>(st, kmeta, RW, seg_kb, kbd, qv, lane, s);
@@ -557,9 +587,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 2 / 8), lane, pb);
       else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 4 / 8), lane, pb);
       else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 8 / 8), lane, pb);
-      else pv_fp16<D, 2>(acc, st + (uint32_t)hi.tbytes[3], lane, pb);
+      else pv_fp16<D, 2>(acc, st + (uint32_t)ctb.v[3], lane, pb);
     } else {
-      const int c_row = (it - hi.start[4]) * kCRows;
+      const int c_row = (it - zc_start) * kCRows;
       const int rows = min(kCRows, len_c - c_row);
       if (rows < kCRows) {  // clear the rows the copy did not fill (they meet p = 0 in the products)
         uint32_t* kz = reinterpret_cast<uint32_t*>(wring + wpos[slot]);
@@ -691,7 +721,7 @@ static DecodeGeom decode_geom(const rdkv_cache* c) {
   const int n_heads = s.batch * s.h_kv;
   const int sms = num_sms();
   const int64_t fixed = decode_fixed_smem(D);
-  const int64_t max_item = std::max<int64_t>(align_up(c->sizes.max_tile_bytes + kTile * D * 2, 128), 2 * kCRows * D * 2);
+  const int64_t max_item = std::max<int64_t>(align_up(c->sizes.max_stage_bytes, 128), 2 * kCRows * D * 2);
   g.max_item = max_item;
   int64_t ring = ((kTwoBlockSmem - fixed) / kDecWarps) / 128 * 128;
   int blocks_per_sm = 2;

@@ -40,8 +40,8 @@ class Shape(ctypes.Structure):
 
 class Sizes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("zone_a_bytes", "zone_b_rows", "index_slots", "kept_tokens",
-                                               "max_tile_bytes")] + [("status", ctypes.c_int32),
-                                                                     ("n_heads", ctypes.c_int32)]
+                                               "max_tile_bytes", "max_stage_bytes")] + [
+        ("status", ctypes.c_int32), ("n_heads", ctypes.c_int32)]
 
 
 class CacheStruct(ctypes.Structure):
@@ -58,7 +58,8 @@ HEAD_PLAN_DTYPE = [("n_v", "<i4", 4), ("tiles", "<i4", 4), ("n_k", "<i4", 5), ("
 PLAN_HEADER_DTYPE = [("status", "<i4"), ("n_heads", "<i4"), ("batch", "<i4"), ("h_kv", "<i4"),
                      ("head_dim", "<i4"), ("slot_stride", "<i4"), ("heads_off", "<i8"), ("slots_off", "<i8"),
                      ("lambda_off", "<i8"), ("zone_a_bytes", "<i8"), ("zone_b_rows", "<i8"),
-                     ("index_slots", "<i8"), ("kept_tokens", "<i8"), ("max_tile_bytes", "<i8")]
+                     ("index_slots", "<i8"), ("kept_tokens", "<i8"), ("max_tile_bytes", "<i8"),
+                     ("max_stage_bytes", "<i8")]
 
 _lib = None
 _P = ctypes.c_void_p

@@ -279,9 +279,11 @@ def make_plan(bits_tok, bits_chan, head_dim):
             b_row += TILE * hp["tiles"][3]
             slot_off += TILE * sum(hp["tiles"])
             heads.append(hp)
+    present = [(tb, b) for h in heads for tb, nt, b in zip(h["tile_bytes"], h["tiles"], V_CLASSES) if nt]
     return dict(heads=heads, zone_a_bytes=a_off, zone_b_rows=b_row, index_slots=slot_off,
                 kept_tokens=int(sum(sum(h["n_v"]) for h in heads)),
-                max_tile_bytes=max([tb for h in heads for tb, nt in zip(h["tile_bytes"], h["tiles"]) if nt] or [0]))
+                max_tile_bytes=max([tb for tb, b in present] or [0]),
+                max_stage_bytes=max([tb + (TILE * head_dim * 2 if b == 16 else 0) for tb, b in present] or [0]))
 
 
 def quantize_groups(x, b):

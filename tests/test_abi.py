@@ -40,10 +40,10 @@ def test_every_declared_symbol_is_exported(L):
 def test_version_and_struct_sizes(L):
     assert L.rdkv_version() >= 1
     assert ctypes.sizeof(rdkv.Shape) == 28
-    assert ctypes.sizeof(rdkv.Sizes) == 48
+    assert ctypes.sizeof(rdkv.Sizes) == 56
     import numpy as np
     assert np.dtype(rdkv.HEAD_PLAN_DTYPE).itemsize == 128
-    assert np.dtype(rdkv.PLAN_HEADER_DTYPE).itemsize == 88
+    assert np.dtype(rdkv.PLAN_HEADER_DTYPE).itemsize == 96
 
 
 def test_workspace_queries_are_host_only(L):
@@ -85,7 +85,7 @@ def test_null_and_budget_errors(L):
 
 def test_append_capacity_is_checked_on_the_host(L):
     s = rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16")
-    sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 1)
+    sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 0, 1)
     fake = ctypes.c_void_p(256)
     c = rdkv.CacheStruct(s, 256, None, None, 256, 256, None, 256, 8, 8, sizes)
     r = L.rdkv_append(ctypes.byref(c), fake, fake, None)
@@ -98,10 +98,10 @@ def test_binding_cache_object_on_host_memory(L):
     import torch
     s = rdkv.make_shape(2, 1000, 6, 2, 128, 40, "f16")
     plan = torch.zeros(L.rdkv_plan_bytes(ctypes.byref(s)), dtype=torch.uint8)
-    sizes = rdkv.Sizes(4096, 64, 256, 200, 2048, 0, 4)
+    sizes = rdkv.Sizes(4096, 64, 256, 200, 2048, 2048, 0, 4)
     c = rdkv.Cache(s, plan, sizes, 48, "cpu")
     assert c.c.len_dev == c.len_dev.data_ptr() and c.c.cap_c == 48 and c.len_c == 0
     ws = c.decode_workspace()
     assert ws.numel() >= L.rdkv_decode_workspace_bytes(ctypes.byref(c.c)) > 0
     assert c.decode_workspace() is ws
-    assert c.fits(sizes) and not c.fits(rdkv.Sizes(1 << 30, 64, 256, 200, 2048, 0, 4))
+    assert c.fits(sizes) and not c.fits(rdkv.Sizes(1 << 30, 64, 256, 200, 2048, 2048, 0, 4))

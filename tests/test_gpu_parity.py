@@ -120,7 +120,7 @@ def test_allocate_and_plan_match_oracle(case):
         assert float(lam[w.batch + b]) == float(rl)
     plan = O.make_plan(bits_tok, bits_chan, w.head_dim)
     assert int(hdr["status"]) == 0 and sizes.status == 0
-    for key in ("zone_a_bytes", "zone_b_rows", "index_slots", "kept_tokens", "max_tile_bytes"):
+    for key in ("zone_a_bytes", "zone_b_rows", "index_slots", "kept_tokens", "max_tile_bytes", "max_stage_bytes"):
         assert int(hdr[key]) == plan[key] == getattr(sizes, key), key
     for i, hp in enumerate(plan["heads"]):
         for key in ("n_v", "tiles", "n_k", "k_words", "tile_bytes"):

@@ -211,6 +211,27 @@ rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, float* out,
  * tile copy ran out (the output of that call is not valid). */
 rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream);
 
+/* ---------------------------------------------------------------- decode without a workspace
+ * No counterpart in the paper: a deployment variant of rdkv_decode_attn.
+ * Some callers cannot allocate device memory themselves: a plugin hosted by
+ * an engine that owns every device allocation, or code that must not call the
+ * allocator on its serving path.  This entry point computes the same output as
+ * rdkv_decode_attn, but keeps its scratch (split partials, per-head tickets and
+ * the status word) in a fixed 4 MiB array built into the library, which every
+ * GPU that loads the library holds until the process exits; it allocates
+ * nothing.
+ *   - Returns RDKV_ERR_WORKSPACE (nothing launched) when the cache needs more
+ *     than 4 MiB of scratch (rdkv_decode_workspace_bytes tells how much).
+ *   - The first call on a device looks up the array's device address (and
+ *     raises the kernel's shared-memory limit); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array and each clears the counters it needs, so
+ *     calls that overlap on the GPU (other streams, other threads) race and
+ *     must be serialised by the caller.
+ *   - The status word of a call lives in that shared array and is not exposed;
+ *     callers that need the timeout report use rdkv_decode_attn. */
+rdkv_status rdkv_decode_attn_noalloc(const rdkv_cache* cache, const void* q, float* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -829,3 +829,89 @@ extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* w
   if (v != RDKV_OK) set_error("decode reported status %d (a bounded wait ran out)", v);
   return (rdkv_status)v;
 }
+
+// ---------------------------------------------------------------- decode without a caller workspace
+// Scratch of rdkv_decode_attn_noalloc: split partials, tickets and the status
+// word.  Every GPU that loads this library holds it until the process exits.
+namespace rdkv {
+constexpr size_t kNoAllocScratchBytes = 4u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array for the current device, looked up once per
+// device.  The array's name is only a host-side stand-in in host code.
+static rdkv_status noalloc_scratch(void** out) {
+  static void* addr[64] = {};
+  int dev = 0;
+  RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
+  RDKV_REQUIRE(dev >= 0 && dev < 64, RDKV_ERR_UNSUPPORTED, "device index %d", dev);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    RDKV_TRY_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch), "scratch address");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return RDKV_OK;
+}
+}  // namespace rdkv
+
+extern "C" rdkv_status rdkv_decode_attn_noalloc(const rdkv_cache* cache, const void* q, float* out, void* stream) {
+  rdkv_status st = check_cache_public(cache);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(q && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  const rdkv_shape& s = cache->shape;
+  const int n_heads = s.batch * s.h_kv;
+  const DecodeGeom geo = decode_geom(cache);
+  const size_t need = decode_ws_bytes(geo, n_heads);
+  RDKV_REQUIRE(need <= kNoAllocScratchBytes, RDKV_ERR_WORKSPACE,
+               "this cache needs %zu bytes of decode scratch; the built-in scratch holds %zu "
+               "(use rdkv_decode_attn with a workspace)",
+               need, kNoAllocScratchBytes);
+  RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
+               (long long)geo.max_item);
+  void* ws = nullptr;
+  st = noalloc_scratch(&ws);
+  if (st != RDKV_OK) return st;
+  cudaStream_t cs = (cudaStream_t)stream;
+  DecodeParams P;
+  P.plan = cache->plan;
+  P.zone_a = cache->zone_a;
+  P.zone_b = cache->zone_b;
+  P.zone_c_k = cache->zone_c_k;
+  P.zone_c_v = cache->zone_c_v;
+  P.q = q;
+  P.partial = static_cast<float*>(ws);
+  P.tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + geo.ticket_off);
+  P.error = P.tickets + n_heads;
+  P.out = out;
+  P.len_dev = cache->len_dev;
+  P.dtype = s.dtype;
+  P.h_q = s.h_q;
+  P.h_kv = s.h_kv;
+  P.cap_c = cache->cap_c;
+  P.ring_bytes = geo.ring_bytes;
+  // the previous call's tickets and status word are still in the scratch: clear them
+  RDKV_TRY_CUDA(cudaMemsetAsync(P.tickets, 0, ((size_t)n_heads + 1) * 4, cs), "decode ticket reset");
+  static size_t smem_set[4][64] = {};
+  int dev = 0;
+  RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
+  const bool qlo = s.dtype == RDKV_F32;
+  const int ki = (s.head_dim == 128 ? 2 : 0) + (qlo ? 1 : 0);
+  const void* fn = ki == 3 ? (const void*)decode_kernel<128, true>
+                 : ki == 2 ? (const void*)decode_kernel<128, false>
+                 : ki == 1 ? (const void*)decode_kernel<64, true>
+                           : (const void*)decode_kernel<64, false>;
+  if (dev < 64 && geo.smem > smem_set[ki][dev]) {
+    RDKV_TRY_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmemLimit),
+                  "decode smem");
+    smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
+  }
+  const dim3 grid(geo.splits, n_heads);
+  switch (ki) {
+    case 3: decode_kernel<128, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    case 2: decode_kernel<128, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    case 1: decode_kernel<64, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    default: decode_kernel<64, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+  }
+  RDKV_CHECK_LAUNCH("decode");
+  return RDKV_OK;
+}

@@ -24,7 +24,7 @@ EXPORTED = (
     "rdkv_waterfill_workspace_bytes", "rdkv_waterfill",
     "rdkv_plan_bytes", "rdkv_allocate_workspace_bytes", "rdkv_allocate", "rdkv_plan_sizes",
     "rdkv_pack", "rdkv_append",
-    "rdkv_decode_workspace_bytes", "rdkv_decode_attn", "rdkv_decode_status",
+    "rdkv_decode_workspace_bytes", "rdkv_decode_attn", "rdkv_decode_status", "rdkv_decode_attn_noalloc",
 )
 
 
@@ -92,6 +92,7 @@ def lib():
             "rdkv_decode_workspace_bytes": (ctypes.c_size_t, [cp]),
             "rdkv_decode_attn": (ctypes.c_int, [cp, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_status": (ctypes.c_int, [cp, _P, _P]),
+            "rdkv_decode_attn_noalloc": (ctypes.c_int, [cp, _P, _P, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -246,6 +247,12 @@ def rdkv_decode_attn(cache, q, out=None, stream=None):
     ws = cache.decode_workspace()
     _check(lib().rdkv_decode_attn(ctypes.byref(cache.c), _ptr(q), _ptr(out), _ptr(ws), ws.numel(),
                                   _stream(stream)))
+    return out
+
+
+def rdkv_decode_attn_noalloc(cache, q, out, stream=None):
+    """Decode with the library's built-in scratch; `out` must be given (this path allocates nothing)."""
+    _check(lib().rdkv_decode_attn_noalloc(ctypes.byref(cache.c), _ptr(q), _ptr(out), _stream(stream)))
     return out
 
 

@@ -10,8 +10,9 @@
 // summed, so the scorer runs two passes over the causal pairs: pass 1 keeps
 // one log-sum-exp per query row; pass 2 recomputes each logit, turns it into
 // a probability with that row's normaliser and sums the columns.  This file
-// holds the CUDA-core passes (exact fp32 logits) and the row/column
-// reductions.
+// holds the CUDA-core passes (exact fp32 logits, used for fp32 inputs) and
+// the row/column reductions; the fp16 passes run on the tensor cores
+// (score_tc.cu).
 #include <cmath>
 
 #include "common.cuh"
@@ -194,9 +195,14 @@ __global__ void __launch_bounds__(128) colsum_simt_kernel(const void* __restrict
   }
 }
 
+// The fp16 tensor-core passes live in score_tc.cu.
+rdkv_status launch_score_tc(const rdkv_shape* s, const void* q, const void* k, const float* sigma, float* lse2,
+                            float* w_tok, float* g_tok, cudaStream_t st);
+int score_tc_lse_stride(int n_tokens);
+
 static size_t score_ws_parts(const rdkv_shape* s, size_t* lse, size_t* qp, size_t* kp) {
   const int nchunk = ceil_div(s->n_tokens, kColChunk);
-  *lse = align_up((int64_t)s->batch * s->h_q * s->n_tokens * 4, 256);
+  *lse = align_up((int64_t)s->batch * s->h_q * score_tc_lse_stride(s->n_tokens) * 4, 256);
   *qp = align_up((int64_t)s->batch * nchunk * s->h_q * s->head_dim * 4, 256);
   *kp = align_up((int64_t)s->batch * nchunk * s->h_kv * s->head_dim * 4, 256);
   return *lse + *qp + *kp;
@@ -244,6 +250,7 @@ extern "C" rdkv_status rdkv_score(const rdkv_shape* s, const void* q, const void
   channel_weight_kernel<<<s->batch * s->h_kv, D, 0, cs>>>(qpart, kpart, nchunk, s->h_q, s->h_kv, D, w_chan);
   RDKV_CHECK_LAUNCH("channel weights");
   // token weights
+  if (s->dtype == RDKV_F16) return launch_score_tc(s, q, k, sigma_tok, lse2, w_tok, g_tok, cs);
   const size_t smem = (size_t)(kSTile * (D + 1) + D * (kSTile + 4) + kSTile) * 4;
   lse_simt_kernel<<<dim3(ceil_div(N, kSTile), s->h_q, s->batch), 128, smem, cs>>>(q, k, s->dtype, N, s->h_q, s->h_kv,
                                                                                     D, lse2);

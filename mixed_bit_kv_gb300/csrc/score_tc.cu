@@ -1,0 +1,387 @@
+// Tensor-core passes of the RDKV token weights (gist.science/ko/paper/2605.08317,
+// section 2.1: w_t = sum over query positions of the attention a_{tau,t}) for
+// fp16 inputs, on the 5th-generation tensor cores.
+//
+// Both passes multiply a stationary block of 128 rows (operand A) by a stream
+// of 128-row tiles (operand B), tile = A . B^T into a 128 x 128 fp32 tensor
+// memory accumulator:
+//   pass 1  A = 128 query rows of head h, B = key tiles t <= tau.  The epilogue
+//           keeps, per query row, the running max and sum of 2^(s*c) and writes
+//           lse2 = log2 sum_t 2^(s_t * c), c = log2(e)/sqrt(D).
+//   pass 2  A = 128 keys of KV head j, B = query tiles tau >= t of the G heads
+//           of the group.  The epilogue adds 2^(s*c - lse2[tau]) per key:
+//           the column sums of the attention, i.e. w_t; then g_t = w_t * sigma_t.
+// Roles (320 threads): warp 0 loads tiles with TMA into a 4-stage ring; warp 1
+// issues tcgen05.mma (one thread) into two TMEM accumulators; warps 2..9 read
+// the accumulators back (two warps per TMEM lane quarter, one per column
+// half) and run the softmax arithmetic.  Every wait is bounded: a wait that
+// runs out writes NaN into the affected outputs, which the allocation reports
+// as invalid gains.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace rdkv {
+
+namespace tc {
+
+constexpr int kRows = 128;       // rows of A, rows of a streamed tile
+constexpr int kStages = 4;       // TMA ring depth
+constexpr int kThreads = 320;    // producer, MMA, 8 epilogue warps
+constexpr long long kWait = 4000000000ll;
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t c) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(c) : "memory");
+}
+__device__ __forceinline__ void mbar_expect(uint64_t* b, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(tx) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > kWait) return false;
+  }
+}
+__device__ __forceinline__ void tma4(void* dst, const CUtensorMap* m, int c0, int c1, int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(su32(dst)),
+      "l"((uint64_t)m), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   su32(dst)),
+               "l"(src), "r"(bytes), "r"(su32(bar))
+               : "memory");
+}
+// Shared-memory matrix descriptor: K-major operand written by TMA with the
+// 128-byte swizzle (8-row x 128-byte atoms, 1024 bytes apart).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)2 << 61);
+}
+// Instruction descriptor: fp32 accumulate, fp16 A and B, both K-major, M = N = 128.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kRows >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t ta, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct Params {
+  int N, n_blk, h_q, h_kv, G, Np, lse_stride;
+  float c;             // log2(e) / sqrt(D)
+  float* lse2;         // [B][H_q][lse_stride]
+  const float* sigma;  // [B][H_kv][N]
+  float* w_tok;        // [B][H_kv][N]
+  float* g_tok;        // [B][H_kv][Np]
+};
+
+template <int D, int PASS>
+__global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                             const __grid_constant__ CUtensorMap tmB, Params P) {
+  constexpr int kHalves = D / 64;                 // 64-element (128-byte) column halves of a row
+  constexpr uint32_t kTileBytes = kRows * D * 2;  // one 128-row tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* As = sm;
+  uint8_t* Bs = sm + kTileBytes;                           // [kStages][tile]
+  float* lse_s = reinterpret_cast<float*>(Bs + kStages * kTileBytes);  // [2][128] (pass 2)
+  __shared__ uint64_t bar_a, full[kStages], empty[kStages], tfull[2], tempty[2], lfull[2], lempty[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int failed;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z;
+  // pass 1: A = queries of head h = blockIdx.y, block qb; pass 2: A = keys of KV head j = blockIdx.y, block kb
+  const int blk = PASS == 1 ? P.n_blk - 1 - (int)blockIdx.x : (int)blockIdx.x;  // heaviest blocks first
+  const int row0 = blk * kRows;
+  const int n_tiles = PASS == 1 ? blk + 1 : P.G * (P.n_blk - blk);
+  auto tile_of = [&](int i, int& head, int& t0) {
+    if (PASS == 1) {
+      head = blockIdx.y / P.G;   // KV head of query head blockIdx.y
+      t0 = i * kRows;
+    } else {
+      head = blockIdx.y * P.G + i / (P.n_blk - blk);
+      t0 = (blk + i % (P.n_blk - blk)) * kRows;
+    }
+  };
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(su32(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 32) {
+    mbar_init(&bar_a, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&tfull[t], 1);
+      mbar_init(&tempty[t], 8);
+      mbar_init(&lfull[t], 1);
+      mbar_init(&lempty[t], 8);
+    }
+    failed = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const int a_head = blockIdx.y;
+      mbar_expect(&bar_a, kTileBytes);
+      for (int hh = 0; hh < kHalves; ++hh) tma4(As + hh * kRows * 128, &tmA, 64 * hh, a_head, row0, b, &bar_a);
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1)) { failed = 1; break; }
+        int head, t0;
+        tile_of(i, head, t0);
+        mbar_expect(&full[s], kTileBytes);
+        for (int hh = 0; hh < kHalves; ++hh)
+          tma4(Bs + s * kTileBytes + hh * kRows * 128, &tmB, 64 * hh, head, t0, b, &full[s]);
+        if (PASS == 2) {
+          const int t = i & 1;
+          if (!mbar_wait(&lempty[t], ((i >> 1) & 1) ^ 1)) { failed = 1; break; }
+          mbar_expect(&lfull[t], kRows * 4);
+          bulk_g2s(lse_s + t * kRows, P.lse2 + ((int64_t)b * P.h_q + head) * P.lse_stride + t0, kRows * 4, &lfull[t]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      if (!mbar_wait(&bar_a, 0)) failed = 1;
+      for (int i = 0; i < n_tiles && !failed; ++i) {
+        const int s = i % kStages, t = i & 1;
+        if (!mbar_wait(&full[s], (i / kStages) & 1)) { failed = 1; break; }
+        if (!mbar_wait(&tempty[t], ((i >> 1) & 1) ^ 1)) { failed = 1; break; }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t a0 = su32(As), b0 = su32(Bs + s * kTileBytes);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (uint32_t)((k >> 2) * kRows * 128 + (k & 3) * 32);
+          const uint64_t ad = sdesc(a0 + off), bd = sdesc(b0 + off);
+          asm volatile(
+              "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::
+                  "r"(tmem + (uint32_t)(t * kRows)),
+              "l"(ad), "l"(bd), "r"(kIdesc), "r"(k > 0 ? 1u : 0u));
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         su32(&empty[s]))
+                     : "memory");
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         su32(&tfull[t]))
+                     : "memory");
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int colh = (warp - 2) >> 2;        // column half: 0 for warps 2..5, 1 for warps 6..9
+    const int r = quarter * 32 + lane;       // accumulator row = A row
+    const int row = row0 + r;                // query (pass 1) or key (pass 2)
+    float m = -INFINITY, l = 0.f;            // pass 1: running max and sum (base 2, scaled logits)
+    float acc = 0.f;                         // pass 2: column sum of the attention
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int t = i & 1;
+      if (!mbar_wait(&tfull[t], (i >> 1) & 1)) { ok = false; break; }
+      if (PASS == 2 && !mbar_wait(&lfull[t], (i >> 1) & 1)) { ok = false; break; }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      int head, t0;
+      tile_of(i, head, t0);
+      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t * kRows + colh * 64);
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        float v[32];
+        tmem_ld32(ta + 32 * ch, v);
+        const int c0 = t0 + colh * 64 + ch * 32;  // first key (pass 1) or query (pass 2) of the chunk
+        if (PASS == 1) {
+          // valid keys: c <= row (and c < N, implied when row < N)
+          float mx = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            v[e] = (c0 + e <= row) ? v[e] * P.c : -INFINITY;
+            mx = fmaxf(mx, v[e]);
+          }
+          const float mn = fmaxf(m, mx);
+          if (mn != -INFINITY) {
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sum += ex2(v[e] - mn);
+            l = l * ex2(m - mn) + sum;
+            m = mn;
+          }
+        } else {
+          const float* ls = lse_s + t * kRows + colh * 64 + ch * 32;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float p = ex2(fmaf(v[e], P.c, -ls[e]));
+            acc += (c0 + e >= row && c0 + e < P.N) ? p : 0.f;
+          }
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tempty[t]);
+        if (PASS == 2) mbar_arrive(&lempty[t]);
+      }
+    }
+    if (!ok) failed = 1;
+    // combine the two column halves of each row through shared memory (the A tile is free now)
+    float* comb = reinterpret_cast<float*>(As);  // [2][128] partial values
+    __syncwarp();
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // every epilogue warp is past its last TMEM read
+    const bool bad = failed != 0;
+    if (PASS == 1) {
+      if (colh == 1) {
+        comb[r] = m;
+        comb[kRows + r] = l;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (colh == 0 && row < P.N) {
+        const float m2 = comb[r], l2 = comb[kRows + r];
+        const float mm = fmaxf(m, m2);
+        const float ll = (m == -INFINITY ? 0.f : l * ex2(m - mm)) + (m2 == -INFINITY ? 0.f : l2 * ex2(m2 - mm));
+        P.lse2[((int64_t)b * P.h_q + blockIdx.y) * P.lse_stride + row] = bad ? __int_as_float(0x7fc00000) : mm + __log2f(ll);
+      }
+    } else {
+      if (colh == 1) comb[r] = acc;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (colh == 0 && row < P.N) {
+        const float w = bad ? __int_as_float(0x7fc00000) : acc + comb[r];
+        const int64_t o = ((int64_t)b * P.h_kv + blockIdx.y) * P.N + row;
+        P.w_tok[o] = w;
+        if (row < P.Np) P.g_tok[((int64_t)b * P.h_kv + blockIdx.y) * P.Np + row] = w * P.sigma[o];
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+// [B][N][H][D] fp16 tensor, 128-row x 64-column boxes with the 128-byte swizzle.
+static rdkv_status make_map(CUtensorMap* m, const void* base, int B, int N, int H, int D) {
+  EncodeTiledFn enc = encode_fn();
+  RDKV_REQUIRE(enc != nullptr, RDKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)N * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kRows, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  RDKV_REQUIRE(r == CUDA_SUCCESS, RDKV_ERR_CUDA, "tensor map encoding failed (%d)", (int)r);
+  return RDKV_OK;
+}
+
+template <int D>
+static size_t smem_bytes() {
+  return 1024 + (size_t)(1 + kStages) * kRows * D * 2 + 2 * kRows * 4;
+}
+
+template <int D>
+static rdkv_status launch(const rdkv_shape* s, const void* q, const void* k, const float* sigma, float* lse2,
+                          int lse_stride, float* w_tok, float* g_tok, cudaStream_t st) {
+  CUtensorMap mq, mk;
+  rdkv_status e = make_map(&mq, q, s->batch, s->n_tokens, s->h_q, D);
+  if (e != RDKV_OK) return e;
+  e = make_map(&mk, k, s->batch, s->n_tokens, s->h_kv, D);
+  if (e != RDKV_OK) return e;
+  Params P;
+  P.N = s->n_tokens;
+  P.n_blk = ceil_div(s->n_tokens, kRows);
+  P.h_q = s->h_q;
+  P.h_kv = s->h_kv;
+  P.G = s->h_q / s->h_kv;
+  P.Np = s->n_tokens - s->window;
+  P.lse_stride = lse_stride;
+  P.c = 1.4426950408889634f / sqrtf((float)D);
+  P.lse2 = lse2;
+  P.sigma = sigma;
+  P.w_tok = w_tok;
+  P.g_tok = g_tok;
+  const size_t smem = smem_bytes<D>();
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[0]) {
+    RDKV_TRY_CUDA(cudaFuncSetAttribute(score_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                  "score smem");
+    RDKV_TRY_CUDA(cudaFuncSetAttribute(score_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                  "score smem");
+    attr_set[0] = attr_set[1] = true;
+  }
+  score_kernel<D, 1><<<dim3(P.n_blk, s->h_q, s->batch), kThreads, smem, st>>>(mq, mk, P);
+  RDKV_CHECK_LAUNCH("row log-sum-exp (tensor cores)");
+  score_kernel<D, 2><<<dim3(P.n_blk, s->h_kv, s->batch), kThreads, smem, st>>>(mk, mq, P);
+  RDKV_CHECK_LAUNCH("attention column sums (tensor cores)");
+  return RDKV_OK;
+}
+
+}  // namespace tc
+
+// Row stride of the lse workspace: the last tile of a row may read up to 128 values past N.
+int score_tc_lse_stride(int n_tokens) { return ceil_div(n_tokens, tc::kRows) * tc::kRows; }
+
+rdkv_status launch_score_tc(const rdkv_shape* s, const void* q, const void* k, const float* sigma, float* lse2,
+                            float* w_tok, float* g_tok, cudaStream_t st) {
+  RDKV_REQUIRE(((uintptr_t)q % 16) == 0 && ((uintptr_t)k % 16) == 0, RDKV_ERR_INVALID_ARG,
+               "q and k must be 16-byte aligned for the tensor-core scorer");
+  const int ls = score_tc_lse_stride(s->n_tokens);
+  if (s->head_dim == 128) return tc::launch<128>(s, q, k, sigma, lse2, ls, w_tok, g_tok, st);
+  return tc::launch<64>(s, q, k, sigma, lse2, ls, w_tok, g_tok, st);
+}
+
+}  // namespace rdkv

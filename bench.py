@@ -101,6 +101,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def captured_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu record, or None when the kernel's
+    source has changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(p))[kernel]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    except (OSError, KeyError, ValueError):
+        return None
+    if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_16"]:
+        return None
+    return rec["bytes_per_launch"]
+
+
 # ---------------------------------------------------------------- algorithmic work
 def decode_bytes_per_call(heads, D, h_q, batch, len_c):
     """Bytes one decode call must move: zone-A payload and metadata of real tokens
@@ -248,15 +263,18 @@ def run_ours(args, ws, rank, local):
     # roofline of the dominant kernel by time share in the step
     dec_frac_time, score_frac_time = dec_ms_step / ms_per_step, score_ms / ms_per_step
     decode_roof = {"bound": "hbm", "achieved": round(value / ws, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                   "frac": round(value / ws / peaks["hbm_gbs"], 4), "traffic": None,
+                   "frac": round(value / ws / peaks["hbm_gbs"], 4), "traffic": captured_traffic("decode_kernel"),
+                   "algorithmic_bytes_per_launch": int(dec_bytes / (S * L)),
                    "peak_source": peaks["source"], "time_share": round(dec_frac_time, 3)}
     # fp16 scorer on the tensor cores: measured dense bf16 peak (fp16 has the same nominal dense rate);
     # the sustained figure, since the scorer runs back to back over every layer inside the step.
     # fp32 inputs run on CUDA cores: roofline against the FP32 FMA peak instead.
     if w.dtype == "f16":
+        t1, t2 = captured_traffic("score_kernel_pass1"), captured_traffic("score_kernel_pass2")
         score_roof = {"bound": "tensor", "achieved": round(score_tflops / ws, 2),
                       "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                      "frac": round(score_tflops / ws / peaks["bf16_tflops_sustained"], 4), "traffic": None,
+                      "frac": round(score_tflops / ws / peaks["bf16_tflops_sustained"], 4),
+                      "traffic": (t1 + t2) if (t1 and t2) else None, "flops_per_launch_pair": scorer_flops(w),
                       "peak_source": f"{peaks['source']} bf16 dense sustained (fp16 nominal rate equal)",
                       "time_share": round(score_frac_time, 3)}
     else:

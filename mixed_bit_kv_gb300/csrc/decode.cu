@@ -288,6 +288,67 @@ __device__ __forceinline__ void k_segment(const uint32_t (&rows)[4], uint32_t km
   }
 }
 
+// The same for fp16 queries (q exact in fp16).  hi = fp16(q * scale) by one
+// half2 multiply (the exact product rounded once) and lo = q * scale - hi by
+// one half2 FMA, which is exact because that remainder fits fp16; the
+// zero-point term sum_c q_c zero_c runs on the tensor core as a one-row A
+// operand (row 0 = the zeros) against B = q, accumulated in zacc.
+template <int W>
+__device__ __forceinline__ void k_segment_h(const uint32_t (&rows)[4], uint32_t kmeta, int kb0, int kb1,
+                                            const KBDesc* kbd, const uint2* qh, int lane, float (&s)[2][4],
+                                            float (&zacc)[4]) {
+  const int g = lane >> 2, q = lane & 3;
+  constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
+  const uint32_t o0 = 4u * (W == 16 ? q : W == 8 ? (q >> 1) : 0);
+  const uint32_t o1 = 4u * (W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0);
+  const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
+  const int sh1 = W == 2 ? 2 * q + 8 : sh0;
+  for (int kb = kb0; kb < kb1; ++kb) {
+    const KBDesc d = kbd[kb];
+    const uint2 qq = qh[kb * 32 + lane];  // q_g (fp16 pairs) at slots (2q, 2q+1), (2q+8, 2q+9); 0 for pads
+    const uint32_t wb = 4u * (uint32_t)d.word0;
+    uint32_t bh0 = qq.x, bh1 = qq.y, bl0 = 0, bl1 = 0;
+    if (W != 16) {
+      const int p0 = d.meta0 + (2 * q < d.nrem ? q : 0), p1 = d.meta0 + (2 * q + 8 < d.nrem ? q + 4 : 0);
+      const uint2 m0 = lds64(kmeta + 8u * p0), m1 = lds64(kmeta + 8u * p1);
+      const __half2 q0 = *reinterpret_cast<const __half2*>(&qq.x), q1 = *reinterpret_cast<const __half2*>(&qq.y);
+      const __half2 s0 = *reinterpret_cast<const __half2*>(&m0.x), s1 = *reinterpret_cast<const __half2*>(&m1.x);
+      const __half2 h0 = __hmul2(q0, s0), h1 = __hmul2(q1, s1);
+      const __half2 l0 = __hfma2(q0, s0, __hneg2(h0)), l1 = __hfma2(q1, s1, __hneg2(h1));
+      bh0 = *reinterpret_cast<const uint32_t*>(&h0);
+      bh1 = *reinterpret_cast<const uint32_t*>(&h1);
+      bl0 = *reinterpret_cast<const uint32_t*>(&l0);
+      bl1 = *reinterpret_cast<const uint32_t*>(&l1);
+      // zero row: lanes of group 0 hold (zero_2q, zero_2q+1) and (zero_2q+8, zero_2q+9)
+      mma16816(zacc, g == 0 ? m0.y : 0u, 0u, g == 0 ? m1.y : 0u, 0u, qq.x, qq.y);
+    }
+#pragma unroll
+    for (int tb = 0; tb < 2; ++tb) {
+      const uint32_t r0 = rows[2 * tb] + wb, r1 = rows[2 * tb + 1] + wb;
+      uint32_t a0, a1, a2, a3;
+      if (W == 16) {
+        const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
+        const uint32_t x0 = lds32(r0 + o0), x1 = lds32(r1 + o0), x2 = lds32(r0 + o1), x3 = lds32(r1 + o1);
+        a0 = v0 ? x0 : 0u; a1 = v0 ? x1 : 0u; a2 = v1 ? x2 : 0u; a3 = v1 ? x3 : 0u;
+        mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
+      } else {
+        const uint32_t x0 = lds32(r0 + o0), x1 = lds32(r1 + o0);
+        a0 = exact_codes(x0, sh0, mask2);
+        a1 = exact_codes(x1, sh0, mask2);
+        if (W == 2) {
+          a2 = exact_codes(x0, sh1, mask2);
+          a3 = exact_codes(x1, sh1, mask2);
+        } else {
+          a2 = exact_codes(lds32(r0 + o1), sh1, mask2);
+          a3 = exact_codes(lds32(r1 + o1), sh1, mask2);
+        }
+        mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
+        mma16816(s[tb], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+  }
+}
+
 template <int D, bool QLO>
 __device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW, const int (&seg_kb)[5],
                                             const KBDesc* kbd, const float4* qv, int lane, float (&s)[2][4]) {
@@ -297,15 +358,28 @@ __device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW,
                             kw + 4u * ((g + 24) * RW)};
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) s[tb][0] = s[tb][1] = s[tb][2] = s[tb][3] = 0.f;
-  k_segment<16, QLO>(rows, kmeta, seg_kb[0], seg_kb[1], kbd, qv, lane, s, bias);
-  k_segment<8, QLO>(rows, kmeta, seg_kb[1], seg_kb[2], kbd, qv, lane, s, bias);
-  k_segment<4, QLO>(rows, kmeta, seg_kb[2], seg_kb[3], kbd, qv, lane, s, bias);
-  k_segment<2, QLO>(rows, kmeta, seg_kb[3], seg_kb[4], kbd, qv, lane, s, bias);
-  // zero-point term: lanes (g, 0..3) hold parts of head g; S^T lane (g', q') needs heads 2q', 2q'+1
   const int q = lane & 3;
-  bias += __shfl_xor_sync(0xffffffffu, bias, 1);
-  bias += __shfl_xor_sync(0xffffffffu, bias, 2);
-  const float be = __shfl_sync(0xffffffffu, bias, 8 * q), bo = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
+  float be, bo;
+  if (QLO) {
+    k_segment<16, QLO>(rows, kmeta, seg_kb[0], seg_kb[1], kbd, qv, lane, s, bias);
+    k_segment<8, QLO>(rows, kmeta, seg_kb[1], seg_kb[2], kbd, qv, lane, s, bias);
+    k_segment<4, QLO>(rows, kmeta, seg_kb[2], seg_kb[3], kbd, qv, lane, s, bias);
+    k_segment<2, QLO>(rows, kmeta, seg_kb[3], seg_kb[4], kbd, qv, lane, s, bias);
+    // zero-point term: lanes (g, 0..3) hold parts of head g; S^T lane (g', q') needs heads 2q', 2q'+1
+    bias += __shfl_xor_sync(0xffffffffu, bias, 1);
+    bias += __shfl_xor_sync(0xffffffffu, bias, 2);
+    be = __shfl_sync(0xffffffffu, bias, 8 * q);
+    bo = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
+  } else {
+    const uint2* qh = reinterpret_cast<const uint2*>(qv);
+    float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // row 0 (lanes of group 0): zero-point term of heads 2q, 2q+1
+    k_segment_h<16>(rows, kmeta, seg_kb[0], seg_kb[1], kbd, qh, lane, s, zacc);
+    k_segment_h<8>(rows, kmeta, seg_kb[1], seg_kb[2], kbd, qh, lane, s, zacc);
+    k_segment_h<4>(rows, kmeta, seg_kb[2], seg_kb[3], kbd, qh, lane, s, zacc);
+    k_segment_h<2>(rows, kmeta, seg_kb[3], seg_kb[4], kbd, qh, lane, s, zacc);
+    be = __shfl_sync(0xffffffffu, zacc[0], q);
+    bo = __shfl_sync(0xffffffffu, zacc[1], q);
+  }
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
     s[tb][0] += be;
@@ -539,8 +613,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
         if (ch >= 0) v[e] = q_s[g * D + ch];
       }
     }
-    if (kb < nkb) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
-    else qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
+    if (kb >= nkb) qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
+    else if (QLO) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
+    else reinterpret_cast<uint2*>(qv)[kb * 32 + ln] = make_uint2(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]));
   }
   __syncthreads();  // the staging area is free again: the rings may fill it
   if (lane == 0) issue();

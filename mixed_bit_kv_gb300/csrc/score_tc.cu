@@ -232,28 +232,56 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         tmem_ld32(ta + 32 * ch, v);
         const int c0 = t0 + colh * 64 + ch * 32;  // first key (pass 1) or query (pass 2) of the chunk
         if (PASS == 1) {
-          // valid keys: c <= row (and c < N, implied when row < N)
+          // valid keys: c <= row (c < N follows for rows < N); only the diagonal tile needs the mask.
+          // The max is taken on raw logits (c > 0) and the scale folded into one FMA per element.
           float mx = -INFINITY;
+          if (t0 + kRows <= row0) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            v[e] = (c0 + e <= row) ? v[e] * P.c : -INFINITY;
-            mx = fmaxf(mx, v[e]);
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, v[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              v[e] = (c0 + e <= row) ? v[e] : -INFINITY;
+              mx = fmaxf(mx, v[e]);
+            }
           }
-          const float mn = fmaxf(m, mx);
+          const float mn = fmaxf(m, mx * P.c);
           if (mn != -INFINITY) {
-            float sum = 0.f;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sum += ex2(v[e] - mn);
-            l = l * ex2(m - mn) + sum;
+            for (int e = 0; e < 32; e += 2) {
+              s0 += ex2(fmaf(v[e], P.c, -mn));
+              s1 += ex2(fmaf(v[e + 1], P.c, -mn));
+            }
+            l = l * ex2(m - mn) + (s0 + s1);
             m = mn;
           }
         } else {
-          const float* ls = lse_s + t * kRows + colh * 64 + ch * 32;
+          const float4* ls4 = reinterpret_cast<const float4*>(lse_s + t * kRows + colh * 64 + ch * 32);
+          float a0 = 0.f, a1 = 0.f;
+          if (t0 != row0 && t0 + kRows <= P.N) {  // no causal edge and no tail in this tile
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float p = ex2(fmaf(v[e], P.c, -ls[e]));
-            acc += (c0 + e >= row && c0 + e < P.N) ? p : 0.f;
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 L = ls4[e4];
+              a0 += ex2(fmaf(v[4 * e4 + 0], P.c, -L.x));
+              a1 += ex2(fmaf(v[4 * e4 + 1], P.c, -L.y));
+              a0 += ex2(fmaf(v[4 * e4 + 2], P.c, -L.z));
+              a1 += ex2(fmaf(v[4 * e4 + 3], P.c, -L.w));
+            }
+          } else {
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 L = ls4[e4];
+              const float lv[4] = {L.x, L.y, L.z, L.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int c = c0 + 4 * e4 + u;
+                const float p = ex2(fmaf(v[4 * e4 + u], P.c, -lv[u]));
+                a0 += (c >= row && c < P.N) ? p : 0.f;
+              }
+            }
           }
+          acc += a0 + a1;
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

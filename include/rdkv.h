@@ -199,16 +199,19 @@ rdkv_status rdkv_append(rdkv_cache* cache, const void* k_new, const void* v_new,
  * RDKV section 2.3: for every sequence b and query head h (KV head h / G),
  *   out[b][h] = sum_t softmax_t(q[b][h] . k^_t / sqrt(D)) v^_t
  * over the kept tokens of zones A (dequantised K and V) and B (fp16 V) and the
- * *len_dev rows of zone C.  q [B][H_q][D] in shape->dtype (used as fp16 by the
- * tensor cores), out [B][H_q][D] fp32.  Split-K over tiles with an fp32
- * online softmax; the partial results live in ws. */
+ * *len_dev rows of zone C.  q [B][H_q][D] in shape->dtype, out [B][H_q][D]
+ * fp32.  Split-K over tiles with an fp32 online softmax; the partial results
+ * and per-head tickets live in ws, which must be ZERO-FILLED before its first
+ * use: every call leaves the tickets at zero again, so the same ws serves any
+ * number of calls (and CUDA-graph replays) without a reset. */
 size_t rdkv_decode_workspace_bytes(const rdkv_cache* cache);
 rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, float* out,
                              void* ws, size_t ws_bytes, void* stream);
 
-/* Reads the status word the last rdkv_decode_attn on this cache and ws left
- * behind.  SYNCHRONISES `stream`.  RDKV_ERR_TIMEOUT means a bounded wait for a
- * tile copy ran out (the output of that call is not valid). */
+/* Reads the status word the rdkv_decode_attn calls on this cache and ws left
+ * behind since the last read, and clears it.  SYNCHRONISES `stream`.
+ * RDKV_ERR_TIMEOUT means a bounded wait for a tile copy ran out in one of
+ * those calls (its output is not valid). */
 rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream);
 
 /* ---------------------------------------------------------------- decode without a workspace

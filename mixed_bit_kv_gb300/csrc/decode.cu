@@ -45,9 +45,13 @@ struct KBDesc {
 
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings).
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
-  return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + kDecWarps * kMaxInflight * 16) + 127) /
+  return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + (int64_t)kMaxKB * 32 * 8 +
+           (int64_t)8 * D * 4 + (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 16) + 127) /
          128 * 128;
 }
+// Floats of one block's partial result (m, l, o for G heads), rounded up to a multiple of 4.
+__host__ __device__ constexpr int partial_stride(int G, int D) { return (G * (D + 2) + 3) / 4 * 4; }
+
 // The warps' partial results are combined in the ring area once every ring is drained.
 __host__ __device__ constexpr int64_t decode_reduce_bytes(int D) { return (int64_t)kDecWarps * 8 * (D + 2) * 4; }
 
@@ -63,7 +67,7 @@ struct DecodeParams {
   int32_t* tickets; // [n_heads] blocks finished per head (zeroed before the launch)
   float* out;       // [batch][h_q][D]
   const int32_t* len_dev;  // zone-C rows in use
-  int dtype, h_q, h_kv, cap_c, ring_bytes;
+  int dtype, h_q, h_kv, cap_c, ring_bytes, ctas;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -102,35 +106,34 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
 }
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
 }
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
+// Shared-memory loads through typed pointers into the block's shared window, so
+// the compiler folds constant offsets into the address ([reg + imm]).
+__device__ __forceinline__ uint32_t lds32(const unsigned char* base, uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(base + off);
 }
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
+__device__ __forceinline__ uint2 lds64(const unsigned char* base, uint32_t off) {
+  return *reinterpret_cast<const uint2*>(base + off);
 }
 
 // Two codes of a pair (already shifted to bit 0 and bit 16) -> exact fp16 codes
@@ -225,7 +228,7 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
 // channels use the stored fp16 value against q (split the same way when q
 // carries more than fp16 precision).
 template <int W, bool QLO>
-__device__ __forceinline__ void k_segment(const uint32_t (&rows)[4], uint32_t kmeta, int kb0, int kb1,
+__device__ __forceinline__ void k_segment(const unsigned char* const (&rows)[4], const unsigned char* kmeta, int kb0, int kb1,
                                           const KBDesc* kbd, const float4* qv, int lane, float (&s)[2][4],
                                           float& bias) {
   const int q = lane & 3;
@@ -251,7 +254,7 @@ __device__ __forceinline__ void k_segment(const uint32_t (&rows)[4], uint32_t km
     } else {
       // a pair past the segment end reads the block's first (valid) pair: its q entries are 0
       const int p0 = d.meta0 + (2 * q < d.nrem ? q : 0), p1 = d.meta0 + (2 * q + 8 < d.nrem ? q + 4 : 0);
-      const uint2 m0 = lds64(kmeta + 8u * p0), m1 = lds64(kmeta + 8u * p1);
+      const uint2 m0 = lds64(kmeta, 8u * p0), m1 = lds64(kmeta, 8u * p1);
       const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&m0.x));
       const float2 z0 = __half22float2(*reinterpret_cast<const __half2*>(&m0.y));
       const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&m1.x));
@@ -262,24 +265,25 @@ __device__ __forceinline__ void k_segment(const uint32_t (&rows)[4], uint32_t km
     }
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
-      const uint32_t r0 = rows[2 * tb] + wb, r1 = rows[2 * tb + 1] + wb;
+      const unsigned char* r0 = rows[2 * tb] + wb;
+      const unsigned char* r1 = rows[2 * tb + 1] + wb;
       uint32_t a0, a1, a2, a3;
       if (W == 16) {
         // raw fp16 words past the segment end may hold anything: zero them
         const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
-        const uint32_t x0 = lds32(r0 + o0), x1 = lds32(r1 + o0), x2 = lds32(r0 + o1), x3 = lds32(r1 + o1);
+        const uint32_t x0 = lds32(r0, o0), x1 = lds32(r1, o0), x2 = lds32(r0, o1), x3 = lds32(r1, o1);
         a0 = v0 ? x0 : 0u; a1 = v0 ? x1 : 0u; a2 = v1 ? x2 : 0u; a3 = v1 ? x3 : 0u;
       } else {
         // codes past the segment end are small integers met by zero query entries
-        const uint32_t x0 = lds32(r0 + o0), x1 = lds32(r1 + o0);
+        const uint32_t x0 = lds32(r0, o0), x1 = lds32(r1, o0);
         a0 = exact_codes(x0, sh0, mask2);
         a1 = exact_codes(x1, sh0, mask2);
         if (W == 2) {
           a2 = exact_codes(x0, sh1, mask2);
           a3 = exact_codes(x1, sh1, mask2);
         } else {
-          a2 = exact_codes(lds32(r0 + o1), sh1, mask2);
-          a3 = exact_codes(lds32(r1 + o1), sh1, mask2);
+          a2 = exact_codes(lds32(r0, o1), sh1, mask2);
+          a3 = exact_codes(lds32(r1, o1), sh1, mask2);
         }
       }
       mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
@@ -294,23 +298,23 @@ __device__ __forceinline__ void k_segment(const uint32_t (&rows)[4], uint32_t km
 // zero-point term sum_c q_c zero_c runs on the tensor core as a one-row A
 // operand (row 0 = the zeros) against B = q, accumulated in zacc.
 template <int W>
-__device__ __forceinline__ void k_segment_h(const uint32_t (&rows)[4], uint32_t kmeta, int kb0, int kb1,
-                                            const KBDesc* kbd, const uint2* qh, int lane, float (&s)[2][4],
-                                            float (&zacc)[4]) {
+__device__ __forceinline__ void k_segment_h(const unsigned char* const (&rows)[4], const unsigned char* kmeta, int kb0, int kb1,
+                                            const uint2* koff, const uint2* qh, int lane, float (&s)[2][4],
+                                            float (&slo)[2][4], float (&zacc)[4]) {
   const int g = lane >> 2, q = lane & 3;
   constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
-  const uint32_t o0 = 4u * (W == 16 ? q : W == 8 ? (q >> 1) : 0);
-  const uint32_t o1 = 4u * (W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0);
   const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
   const int sh1 = W == 2 ? 2 * q + 8 : sh0;
+#pragma unroll 2
   for (int kb = kb0; kb < kb1; ++kb) {
-    const KBDesc d = kbd[kb];
+    // this lane's byte offsets, 16 bits each: words of its two slot pairs in a row (bit 15 marks a
+    // pair past the segment end: only raw 16-bit words need zeroing then) and their metadata
+    const uint2 off = koff[kb * 32 + lane];
     const uint2 qq = qh[kb * 32 + lane];  // q_g (fp16 pairs) at slots (2q, 2q+1), (2q+8, 2q+9); 0 for pads
-    const uint32_t wb = 4u * (uint32_t)d.word0;
+    const uint32_t w0 = off.x & 0x7fffu, w1 = (off.x >> 16) & 0x7fffu;
     uint32_t bh0 = qq.x, bh1 = qq.y, bl0 = 0, bl1 = 0;
     if (W != 16) {
-      const int p0 = d.meta0 + (2 * q < d.nrem ? q : 0), p1 = d.meta0 + (2 * q + 8 < d.nrem ? q + 4 : 0);
-      const uint2 m0 = lds64(kmeta + 8u * p0), m1 = lds64(kmeta + 8u * p1);
+      const uint2 m0 = lds64(kmeta, off.y & 0xffffu), m1 = lds64(kmeta, off.y >> 16);
       const __half2 q0 = *reinterpret_cast<const __half2*>(&qq.x), q1 = *reinterpret_cast<const __half2*>(&qq.y);
       const __half2 s0 = *reinterpret_cast<const __half2*>(&m0.x), s1 = *reinterpret_cast<const __half2*>(&m1.x);
       const __half2 h0 = __hmul2(q0, s0), h1 = __hmul2(q1, s1);
@@ -324,38 +328,40 @@ __device__ __forceinline__ void k_segment_h(const uint32_t (&rows)[4], uint32_t 
     }
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
-      const uint32_t r0 = rows[2 * tb] + wb, r1 = rows[2 * tb + 1] + wb;
+      const unsigned char* r0 = rows[2 * tb];
+      const unsigned char* r1 = rows[2 * tb + 1];
       uint32_t a0, a1, a2, a3;
       if (W == 16) {
-        const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
-        const uint32_t x0 = lds32(r0 + o0), x1 = lds32(r1 + o0), x2 = lds32(r0 + o1), x3 = lds32(r1 + o1);
+        const uint32_t x0 = lds32(r0, w0), x1 = lds32(r1, w0), x2 = lds32(r0, w1), x3 = lds32(r1, w1);
+        const bool v0 = (off.x & 0x8000u) == 0, v1 = (off.x & 0x80000000u) == 0;
         a0 = v0 ? x0 : 0u; a1 = v0 ? x1 : 0u; a2 = v1 ? x2 : 0u; a3 = v1 ? x3 : 0u;
         mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
       } else {
-        const uint32_t x0 = lds32(r0 + o0), x1 = lds32(r1 + o0);
+        const uint32_t x0 = lds32(r0, w0), x1 = lds32(r1, w0);
         a0 = exact_codes(x0, sh0, mask2);
         a1 = exact_codes(x1, sh0, mask2);
         if (W == 2) {
           a2 = exact_codes(x0, sh1, mask2);
           a3 = exact_codes(x1, sh1, mask2);
         } else {
-          a2 = exact_codes(lds32(r0 + o1), sh1, mask2);
-          a3 = exact_codes(lds32(r1 + o1), sh1, mask2);
+          a2 = exact_codes(lds32(r0, w1), sh1, mask2);
+          a3 = exact_codes(lds32(r1, w1), sh1, mask2);
         }
         mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
-        mma16816(s[tb], a0, a1, a2, a3, bl0, bl1);
+        mma16816(slo[tb], a0, a1, a2, a3, bl0, bl1);
       }
     }
   }
 }
 
 template <int D, bool QLO>
-__device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW, const int (&seg_kb)[5],
-                                            const KBDesc* kbd, const float4* qv, int lane, float (&s)[2][4]) {
+__device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsigned char* kmeta, int RW, const int (&seg_kb)[5],
+                                            const KBDesc* kbd, const float4* qv, const uint2* koff, int lane,
+                                            float (&s)[2][4]) {
   float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
   const int g = lane >> 2;
-  const uint32_t rows[4] = {kw + 4u * (g * RW), kw + 4u * ((g + 8) * RW), kw + 4u * ((g + 16) * RW),
-                            kw + 4u * ((g + 24) * RW)};
+  const unsigned char* const rows[4] = {kw + 4 * (g * RW), kw + 4 * ((g + 8) * RW), kw + 4 * ((g + 16) * RW),
+                                        kw + 4 * ((g + 24) * RW)};
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) s[tb][0] = s[tb][1] = s[tb][2] = s[tb][3] = 0.f;
   const int q = lane & 3;
@@ -373,10 +379,15 @@ __device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW,
   } else {
     const uint2* qh = reinterpret_cast<const uint2*>(qv);
     float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // row 0 (lanes of group 0): zero-point term of heads 2q, 2q+1
-    k_segment_h<16>(rows, kmeta, seg_kb[0], seg_kb[1], kbd, qh, lane, s, zacc);
-    k_segment_h<8>(rows, kmeta, seg_kb[1], seg_kb[2], kbd, qh, lane, s, zacc);
-    k_segment_h<4>(rows, kmeta, seg_kb[2], seg_kb[3], kbd, qh, lane, s, zacc);
-    k_segment_h<2>(rows, kmeta, seg_kb[3], seg_kb[4], kbd, qh, lane, s, zacc);
+    float slo[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // remainder products, a separate chain
+    k_segment_h<16>(rows, kmeta, seg_kb[0], seg_kb[1], koff, qh, lane, s, slo, zacc);
+    k_segment_h<8>(rows, kmeta, seg_kb[1], seg_kb[2], koff, qh, lane, s, slo, zacc);
+    k_segment_h<4>(rows, kmeta, seg_kb[2], seg_kb[3], koff, qh, lane, s, slo, zacc);
+    k_segment_h<2>(rows, kmeta, seg_kb[3], seg_kb[4], koff, qh, lane, s, slo, zacc);
+#pragma unroll
+    for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[tb][e] += slo[tb][e];
     be = __shfl_sync(0xffffffffu, zacc[0], q);
     bo = __shfl_sync(0xffffffffu, zacc[1], q);
   }
@@ -391,7 +402,7 @@ __device__ __forceinline__ void tile_logits(uint32_t kw, uint32_t kmeta, int RW,
 
 // PV of a zone-A tile with packed V of width VB.
 template <int D, int VB>
-__device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, uint32_t vcodes, uint32_t vmeta, int lane,
+__device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned char* vcodes, const unsigned char* vmeta, int lane,
                                                const uint32_t (&pb)[2][2]) {
   const int g = lane >> 2, q = lane & 3;
   constexpr int wpp = D * VB / 16;  // words per token pair
@@ -401,19 +412,20 @@ __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, uint32_t vcodes,
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
     const int p0 = 8 * tb + q, p1 = p0 + 4;
-    const uint32_t base0 = vcodes + 4u * (p0 * wpp), base1 = vcodes + 4u * (p1 * wpp);
+    const unsigned char* base0 = vcodes + 4 * (p0 * wpp);
+    const unsigned char* base1 = vcodes + 4 * (p1 * wpp);
 #pragma unroll
     for (int grp = 0; grp < D / 32; ++grp) {
-      const uint2 m0 = lds64(vmeta + 8 * (p0 * (D / 32) + grp));
-      const uint2 m1 = lds64(vmeta + 8 * (p1 * (D / 32) + grp));
+      const uint2 m0 = lds64(vmeta, 8 * (p0 * (D / 32) + grp));
+      const uint2 m1 = lds64(vmeta, 8 * (p1 * (D / 32) + grp));
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int cm = 2 * grp + half;
         const int c0 = 16 * cm + g, c1 = c0 + 8;
-        const uint32_t a0 = dequant_pair(lds32(base0 + 4 * (c0 / per)), sh0, mask2, m0.x, m0.y);
-        const uint32_t a1 = dequant_pair(lds32(base0 + 4 * (c1 / per)), sh1, mask2, m0.x, m0.y);
-        const uint32_t a2 = dequant_pair(lds32(base1 + 4 * (c0 / per)), sh0, mask2, m1.x, m1.y);
-        const uint32_t a3 = dequant_pair(lds32(base1 + 4 * (c1 / per)), sh1, mask2, m1.x, m1.y);
+        const uint32_t a0 = dequant_pair(lds32(base0, 4 * (c0 / per)), sh0, mask2, m0.x, m0.y);
+        const uint32_t a1 = dequant_pair(lds32(base0, 4 * (c1 / per)), sh1, mask2, m0.x, m0.y);
+        const uint32_t a2 = dequant_pair(lds32(base1, 4 * (c0 / per)), sh0, mask2, m1.x, m1.y);
+        const uint32_t a3 = dequant_pair(lds32(base1, 4 * (c1 / per)), sh1, mask2, m1.x, m1.y);
         mma16816(acc.o[cm], a0, a1, a2, a3, pb[tb][0], pb[tb][1]);
       }
     }
@@ -446,9 +458,42 @@ struct ClassVals {
 template <int D, bool QLO>
 __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const int head = blockIdx.y, split = blockIdx.x, n_split = gridDim.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.h_q / P.h_kv;
+  __shared__ int asg[3];  // head, first block of the head, blocks of the head
+  {
+    // Blocks are dealt to heads in proportion to their items (tiles plus zone-C blocks), at least
+    // one per head, over a nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the
+    // blocks past the last head's range leave at once.
+    const int n_heads = plan_header(P.plan)->n_heads;
+    const rdkv_head_plan* heads = plan_heads(P.plan);
+    const int len = min(*P.len_dev, P.cap_c);
+    int* items = reinterpret_cast<int*>(smem + decode_fixed_smem(D));  // scratch in the ring area
+    for (int h = tid; h < n_heads; h += blockDim.x) {
+      const rdkv_head_plan& hp = heads[h];
+      items[h] = hp.tiles[0] + hp.tiles[1] + hp.tiles[2] + hp.tiles[3] + ceil_div(len, kCRows);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int64_t total = 0;
+      for (int h = 0; h < n_heads; ++h) total += items[h];
+      int start = 0;
+      asg[0] = -1;
+      for (int h = 0; h < n_heads; ++h) {
+        const int c = max(1, (int)(total > 0 ? (int64_t)items[h] * P.ctas / total : 0));
+        if ((int)blockIdx.x >= start && (int)blockIdx.x < start + c) {
+          asg[0] = h;
+          asg[1] = start;
+          asg[2] = c;
+          break;
+        }
+        start += c;
+      }
+    }
+    __syncthreads();
+  }
+  if (asg[0] < 0) return;
+  const int head = asg[0], split = (int)blockIdx.x - asg[1], n_split = asg[2], first_block = asg[1];
   const int b = head / P.h_kv, j = head % P.h_kv;
   const rdkv_head_plan* hpp = plan_heads(P.plan) + head;
 
@@ -456,14 +501,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
   float4* qv = reinterpret_cast<float4*>(smem + 256);                              // [kMaxKB][32]
   uint4* qfragc = reinterpret_cast<uint4*>(qv + kMaxKB * 32);                      // [D/16][32] hi, lo
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qfragc + (D / 16) * 32);           // [warps][kMaxInflight]
+  uint2* koff = reinterpret_cast<uint2*>(qfragc + (D / 16) * 32);                  // [kMaxKB][32]
+  float* q_s = reinterpret_cast<float*>(koff + kMaxKB * 32);                       // [8][D] query rows of the group
+  int16_t* slot_s = reinterpret_cast<int16_t*>(q_s + 8 * D);                       // [D + kSlotPad] slot table
+  uint64_t* bars = reinterpret_cast<uint64_t*>(slot_s + D + kSlotPad);             // [warps][kMaxInflight]
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
   int* ring_item = ring_pos + kDecWarps * kMaxInflight;                            // [warps][kMaxInflight]
   unsigned char* ring = smem + decode_fixed_smem(D);
   float* red = reinterpret_cast<float*>(ring);                                     // [warps][8][D + 2], after the loop
-  // staging for the query fragments, in the ring area before any copy is issued into it
-  float* q_s = reinterpret_cast<float*>(ring);                                     // [8][D]
-  int16_t* slot_s = reinterpret_cast<int16_t*>(q_s + 8 * D);                       // [k_slots]
   __shared__ int seg_kb_s[5];
   __shared__ int is_last;
   __shared__ int next_item;
@@ -561,6 +606,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     for (int k = 0; k < kMaxInflight; ++k) mbar_init(&wbar[k], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  __syncthreads();  // next_item is set
+  if (lane == 0) issue();  // the first copies fly while the query fragments are built
   // stage the query rows of the group and this head's slot table (one coalesced round trip each)
   const int16_t* slot_ch = plan_slots(P.plan) + (int64_t)head * plan_header(P.plan)->slot_stride;
   const int qbase = b * P.h_q + j * G;
@@ -613,12 +660,24 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
         if (ch >= 0) v[e] = q_s[g * D + ch];
       }
     }
+    if (kb < nkb) {
+      // byte offsets of this lane's two slot pairs (words within a row; metadata), see k_segment_h
+      const KBDesc d = kbd[kb];
+      const int w = d.width;
+      const int o0 = w == 16 ? qq : w == 8 ? (qq >> 1) : 0;
+      const int o1 = w == 16 ? qq + 4 : w == 8 ? (qq >> 1) + 2 : w == 4 ? 1 : 0;
+      const bool v0 = 2 * qq < d.nrem, v1 = 2 * qq + 8 < d.nrem;
+      const uint32_t w0 = 4u * (uint32_t)(d.word0 + o0) | (v0 ? 0u : 0x8000u);
+      const uint32_t w1 = 4u * (uint32_t)(d.word0 + o1) | (v1 ? 0u : 0x8000u);
+      const uint32_t m0 = 8u * (uint32_t)(d.meta0 + (v0 ? qq : 0));  // a pair past the end reads the block's first pair
+      const uint32_t m1 = 8u * (uint32_t)(d.meta0 + (v1 ? qq + 4 : 0));
+      koff[kb * 32 + ln] = make_uint2(w0 | (w1 << 16), m0 | (m1 << 16));
+    }
     if (kb >= nkb) qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
     else if (QLO) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
     else reinterpret_cast<uint2*>(qv)[kb * 32 + ln] = make_uint2(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]));
   }
-  __syncthreads();  // the staging area is free again: the rings may fill it
-  if (lane == 0) issue();
+  __syncthreads();
 
   WarpAcc<D> acc;
 #pragma unroll
@@ -645,9 +704,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     if (cls >= 0) {
       const int ti = it - (int)cstart(cls);
       const int n_real = min(kTile, (int)cnv(cls) - kTile * ti);
-      const uint32_t kmeta = st + 4u * kTile * RW;
+      const unsigned char* stp = wring + wpos[slot];
+      const unsigned char* kmeta = stp + 4 * kTile * RW;
       float s[2][4];
-      tile_logits<D, QLO>(st, kmeta, RW, seg_kb, kbd, qv, lane, s);
+      tile_logits<D, QLO>(stp, kmeta, RW, seg_kb, kbd, qv, koff, lane, s);
 #pragma unroll
       for (int tb = 0; tb < 2; ++tb) {
         const bool va = 16 * tb + g < n_real, vb = 16 * tb + g + 8 < n_real;
@@ -658,10 +718,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       }
       uint32_t pb[2][2];
       softmax_update<D, 2>(acc, s, pb);
-      const uint32_t vcodes = kmeta + 4u * meta_slots;
-      if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 2 / 8), lane, pb);
-      else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 4 / 8), lane, pb);
-      else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + (uint32_t)(kTile * D * 8 / 8), lane, pb);
+      const unsigned char* vcodes = kmeta + 4 * meta_slots;
+      if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + kTile * D * 2 / 8, lane, pb);
+      else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + kTile * D * 4 / 8, lane, pb);
+      else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + kTile * D * 8 / 8, lane, pb);
       else pv_fp16<D, 2>(acc, st + (uint32_t)ctb.v[3], lane, pb);
     } else {
       const int c_row = (it - zc_start) * kCRows;
@@ -733,9 +793,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     rw[(2 * q + 1) * (D + 2) + D + 1] = l1;
   }
   __syncthreads();
-  // combine the warps; write this split's partial result (m, l, unnormalised o) for the G heads
-  float* part = P.partial + (int64_t)head * n_split * G * (D + 2);
-  float* mine = part + (int64_t)split * G * (D + 2);
+  // combine the warps; write this block's partial result (m, l, unnormalised o) for the G heads;
+  // one block's partial takes pstride floats (a multiple of 4: the merge copies it as float4)
+  const int pstride = partial_stride(G, D);
+  float* part = P.partial + (int64_t)first_block * pstride;
+  float* mine = part + (int64_t)split * pstride;
   for (int i = tid; i < G * (D + 2); i += blockDim.x) {
     const int h = i / (D + 2), c = i % (D + 2);
     float M = -INFINITY;
@@ -757,23 +819,63 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  for (int i = tid; i < G * D; i += blockDim.x) {
-    const int h = i / D, c = i % D;
-    const float* ph = part + h * (D + 2);
-    float M = -INFINITY;
-    for (int sp = 0; sp < n_split; ++sp) M = fmaxf(M, __ldcg(ph + (int64_t)sp * G * (D + 2) + D));
-    float o = 0.f, l = 0.f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < n_split; ++sp) {
-        const float* ps = ph + (int64_t)sp * G * (D + 2);
-        const float ms = __ldcg(ps + D);
-        if (ms == -INFINITY) continue;
-        const float f = exp2f(ms - M);
-        o += f * __ldcg(ps + c);
-        l += f * __ldcg(ps + D + 1);
+  if (tid == 0) P.tickets[head] = 0;  // every block of this head has counted: ready for the next call
+  // Merge: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per query head.  The splits' partial
+  // blocks are copied into shared memory (the ring area is free) in chunks with coalesced loads.
+  __shared__ float Mh[8], Lh[8], Sh[8];  // running max, running sum, rescale of the previous chunks
+  float* buf = reinterpret_cast<float*>(ring);
+  const int per = pstride;                                       // floats of one split's partial
+  const int chunk = max(1, (int)((int64_t)kDecWarps * P.ring_bytes / 4 / per));
+  if (tid < G) {
+    Mh[tid] = -INFINITY;
+    Lh[tid] = 0.f;
+  }
+  float o[4] = {0.f, 0.f, 0.f, 0.f};  // outputs i = tid + k * blockDim.x, k < 4 (G * D <= 1024)
+  for (int s0 = 0; s0 < n_split; s0 += chunk) {
+    const int ns = min(chunk, n_split - s0);
+    const float4* src = reinterpret_cast<const float4*>(part + (int64_t)s0 * per);
+    float4* dst = reinterpret_cast<float4*>(buf);
+    __syncthreads();  // the previous chunk is consumed
+    for (int i = tid; i < ns * per / 4; i += blockDim.x) dst[i] = __ldcg(src + i);
+    __syncthreads();
+    if (tid < G) {
+      float mc = -INFINITY;
+      for (int sp = 0; sp < ns; ++sp) mc = fmaxf(mc, buf[sp * per + tid * (D + 2) + D]);
+      const float Mo = Mh[tid], Mn = fmaxf(Mo, mc);
+      const float so = (Mo == -INFINITY) ? 0.f : exp2f(Mo - Mn);
+      float L = Lh[tid] * so;
+      for (int sp = 0; sp < ns; ++sp) {
+        const float ms = buf[sp * per + tid * (D + 2) + D];
+        if (ms != -INFINITY) L += exp2f(ms - Mn) * buf[sp * per + tid * (D + 2) + D + 1];
+      }
+      Mh[tid] = Mn;
+      Lh[tid] = L;
+      Sh[tid] = so;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = tid + k * blockDim.x;
+      if (i < G * D) {
+        const int h = i / D, c = i % D;
+        const float Mn = Mh[h];
+        float acc = o[k] * Sh[h];
+        for (int sp = 0; sp < ns; ++sp) {
+          const float ms = buf[sp * per + h * (D + 2) + D];
+          if (ms != -INFINITY) acc = fmaf(exp2f(ms - Mn), buf[sp * per + h * (D + 2) + c], acc);
+        }
+        o[k] = acc;
       }
     }
-    P.out[((int64_t)b * P.h_q + j * G + h) * D + c] = l > 0.f ? o / l : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = tid + k * blockDim.x;
+    if (i < G * D) {
+      const int h = i / D, c = i % D;
+      const float L = Lh[h];
+      P.out[((int64_t)b * P.h_q + j * G + h) * D + c] = L > 0.f ? o[k] / L : 0.f;
+    }
   }
 }
 
@@ -782,7 +884,8 @@ constexpr int64_t kTwoBlockSmem = 112 * 1024;             // two blocks per SM b
 
 struct DecodeGeom {
   int64_t max_item;
-  int splits;
+  int ctas;     // nominal number of blocks dealt to heads
+  int splits;   // grid size: ctas + one spare block per head
   int ring_bytes;
   size_t smem;
   size_t partial_bytes;
@@ -807,12 +910,12 @@ static DecodeGeom decode_geom(const rdkv_cache* c) {
   ring = std::max<int64_t>(ring, align_up(decode_reduce_bytes(D), 128 * kDecWarps) / kDecWarps);
   g.ring_bytes = (int)ring;
   g.smem = (size_t)(fixed + (int64_t)kDecWarps * ring);
+  // blocks dealt to heads in proportion to their work: a nominal count that fills every SM once,
+  // fewer when there is little work (at least kDecWarps items per block on average)
   const int64_t items = ceil_div64(c->sizes.index_slots, kTile) + (int64_t)n_heads * ceil_div(c->cap_c, kCRows);
-  const int64_t per_head = std::max<int64_t>(1, items / std::max(1, n_heads));
-  int splits = ceil_div(blocks_per_sm * sms, n_heads);
-  splits = (int)std::max<int64_t>(1, std::min<int64_t>(splits, ceil_div64(per_head, kDecWarps)));
-  g.splits = std::min(splits, 1024);
-  g.partial_bytes = (size_t)align_up((int64_t)n_heads * g.splits * G * (D + 2) * 4, 256);
+  g.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)blocks_per_sm * sms, ceil_div64(items, kDecWarps)));
+  g.splits = g.ctas + n_heads;  // grid size
+  g.partial_bytes = (size_t)align_up((int64_t)g.splits * partial_stride(G, D) * 4, 256);
   g.ticket_off = g.partial_bytes;
   return g;
 }
@@ -862,8 +965,7 @@ extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, 
   P.h_kv = s.h_kv;
   P.cap_c = cache->cap_c;
   P.ring_bytes = geo.ring_bytes;
-  // tickets and the status word start at zero for every launch
-  RDKV_TRY_CUDA(cudaMemsetAsync(P.tickets, 0, ((size_t)n_heads + 1) * 4, cs), "decode ticket reset");
+  // the tickets are zero here: the workspace starts zero-filled and every call leaves them at zero
   // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is captured)
   static size_t smem_set[4][64] = {};
   int dev = 0;
@@ -879,7 +981,8 @@ extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, 
                   "decode smem");
     smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
   }
-  const dim3 grid(geo.splits, n_heads);
+  P.ctas = geo.ctas;
+  const dim3 grid(geo.splits);
   switch (ki) {
     case 3: decode_kernel<128, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
     case 2: decode_kernel<128, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
@@ -901,7 +1004,13 @@ extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* w
                                 cudaMemcpyDeviceToHost, (cudaStream_t)stream),
                 "status read");
   RDKV_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status sync");
-  if (v != RDKV_OK) set_error("decode reported status %d (a bounded wait ran out)", v);
+  if (v != RDKV_OK) {
+    set_error("decode reported status %d (a bounded wait ran out)", v);
+    RDKV_TRY_CUDA(cudaMemsetAsync(static_cast<char*>(const_cast<void*>(ws)) + geo.ticket_off + 4 * (size_t)n_heads, 0, 4,
+                                  (cudaStream_t)stream),
+                  "status clear");
+    RDKV_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status clear sync");
+  }
   return (rdkv_status)v;
 }
 
@@ -980,7 +1089,8 @@ extern "C" rdkv_status rdkv_decode_attn_noalloc(const rdkv_cache* cache, const v
                   "decode smem");
     smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
   }
-  const dim3 grid(geo.splits, n_heads);
+  P.ctas = geo.ctas;
+  const dim3 grid(geo.splits);
   switch (ki) {
     case 3: decode_kernel<128, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
     case 2: decode_kernel<128, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;

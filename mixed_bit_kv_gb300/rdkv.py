@@ -217,9 +217,10 @@ class Cache:
         return self.c.len_c
 
     def decode_workspace(self):
+        """Zero-filled once; the decode leaves it ready for the next call."""
         nb = lib().rdkv_decode_workspace_bytes(ctypes.byref(self.c))
         if self._ws is None or self._ws.numel() < nb:
-            self._ws = _ws(nb, self.zone_a.device)
+            self._ws = torch.zeros(max(int(nb), 256), dtype=torch.uint8, device=self.zone_a.device)
         return self._ws
 
 

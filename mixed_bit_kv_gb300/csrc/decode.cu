@@ -46,7 +46,7 @@ struct KBDesc {
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings).
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
   return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + (int64_t)kMaxKB * 32 * 8 +
-           (int64_t)8 * D * 4 + (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 16) + 127) /
+           (int64_t)8 * D * 4 + (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 20) + 127) /
          128 * 128;
 }
 // Floats of one block's partial result (m, l, o for G heads), rounded up to a multiple of 4.
@@ -67,7 +67,9 @@ struct DecodeParams {
   int32_t* tickets; // [n_heads] blocks finished per head (zeroed before the launch)
   float* out;       // [batch][h_q][D]
   const int32_t* len_dev;  // zone-C rows in use
-  int dtype, h_q, h_kv, cap_c, ring_bytes, ctas;
+  const rdkv_head_plan* heads;  // the plan's head records (offset fixed by the shape)
+  const int16_t* slots;         // the plan's slot tables, slot_stride entries per head
+  int dtype, h_q, h_kv, cap_c, ring_bytes, ctas, n_heads, slot_stride;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -460,26 +462,26 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.h_q / P.h_kv;
-  __shared__ int asg[3];  // head, first block of the head, blocks of the head
+  __shared__ int asg[4];  // head, first block of the head, blocks of the head, zone-C rows
   {
     // Blocks are dealt to heads in proportion to their items (tiles plus zone-C blocks), at least
     // one per head, over a nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the
-    // blocks past the last head's range leave at once.
-    const int n_heads = plan_header(P.plan)->n_heads;
-    const rdkv_head_plan* heads = plan_heads(P.plan);
+    // blocks past the last head's range leave at once.  One round trip: the tile counts of every
+    // head and the zone-C length are loaded together.
     const int len = min(*P.len_dev, P.cap_c);
     int* items = reinterpret_cast<int*>(smem + decode_fixed_smem(D));  // scratch in the ring area
-    for (int h = tid; h < n_heads; h += blockDim.x) {
-      const rdkv_head_plan& hp = heads[h];
-      items[h] = hp.tiles[0] + hp.tiles[1] + hp.tiles[2] + hp.tiles[3] + ceil_div(len, kCRows);
+    for (int h = tid; h < P.n_heads; h += blockDim.x) {
+      const int4 t = *reinterpret_cast<const int4*>(P.heads[h].tiles);
+      items[h] = t.x + t.y + t.z + t.w + ceil_div(len, kCRows);
     }
     __syncthreads();
     if (tid == 0) {
       int64_t total = 0;
-      for (int h = 0; h < n_heads; ++h) total += items[h];
+      for (int h = 0; h < P.n_heads; ++h) total += items[h];
       int start = 0;
       asg[0] = -1;
-      for (int h = 0; h < n_heads; ++h) {
+      asg[3] = len;
+      for (int h = 0; h < P.n_heads; ++h) {
         const int c = max(1, (int)(total > 0 ? (int64_t)items[h] * P.ctas / total : 0));
         if ((int)blockIdx.x >= start && (int)blockIdx.x < start + c) {
           asg[0] = h;
@@ -494,8 +496,22 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   }
   if (asg[0] < 0) return;
   const int head = asg[0], split = (int)blockIdx.x - asg[1], n_split = asg[2], first_block = asg[1];
+  const int len_c = asg[3];
   const int b = head / P.h_kv, j = head % P.h_kv;
-  const rdkv_head_plan* hpp = plan_heads(P.plan) + head;
+  const rdkv_head_plan* hpp = P.heads + head;
+
+  // the query rows of the group and the slot table go into registers now; they land while the
+  // rings are set up and the first tiles are requested
+  const int qbase = b * P.h_q + j * G;
+  const int16_t* slot_ch = P.slots + (int64_t)head * P.slot_stride;
+  float qr[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = tid + k * kDecWarps * 32;
+    qr[k] = i < G * D ? load_as_float(P.q, (int64_t)qbase * D + i, P.dtype) : 0.f;
+  }
+  const int k_slots = hpp->k_slots;  // <= D + kSlotPad <= the block's threads
+  const int16_t sr = tid < k_slots ? slot_ch[tid] : (int16_t)-1;
 
   // shared memory map
   KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
@@ -507,13 +523,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   uint64_t* bars = reinterpret_cast<uint64_t*>(slot_s + D + kSlotPad);             // [warps][kMaxInflight]
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
   int* ring_item = ring_pos + kDecWarps * kMaxInflight;                            // [warps][kMaxInflight]
+  uint32_t* ring_vend = reinterpret_cast<uint32_t*>(ring_item + kDecWarps * kMaxInflight);  // [warps][kMaxInflight]
   unsigned char* ring = smem + decode_fixed_smem(D);
   float* red = reinterpret_cast<float*>(ring);                                     // [warps][8][D + 2], after the loop
   __shared__ int seg_kb_s[5];
   __shared__ int is_last;
-  __shared__ int next_item;
+  __shared__ int next_k;
 
-  // items of this head and of this split
+  // items of this head: its tiles in class order, then its zone-C blocks
   ClassVals cstart, coff, ctb, cnv;  // first item, first byte in zone A, tile bytes, kept tokens per class
   int zc_start;
   {
@@ -532,10 +549,45 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   }
   const int64_t b_row = hpp->b_row;
   const int RW = hpp->row_words, meta_slots = hpp->meta_slots;
-  const int len_c = min(*P.len_dev, P.cap_c);
+  // split s of n takes items s, s + n, s + 2n, ...: every split gets its share of each class
   const int n_items = zc_start + ceil_div(len_c, kCRows);
-  const int i0 = (int)((int64_t)n_items * split / n_split), i1 = (int)((int64_t)n_items * (split + 1) / n_split);
-  if (tid == 0) next_item = i0;
+  if (tid == 0) next_k = 0;
+
+  // k-block descriptors of this head's K rows (each block inside one width segment), one per thread
+  if (warp == 1 && lane < kMaxKB) {
+    int nb[4], wb[4], sb[4], mb[4], ns[4];
+    int nkb = 0, wsum = 0, ssum = 0, msum = 0;
+#pragma unroll
+    for (int seg = 0; seg < 4; ++seg) {
+      const int w = 16 >> seg, per = 32 / w;
+      const int nslot = hpp->k_words[seg] * per;
+      ns[seg] = nslot;
+      nb[seg] = nkb;
+      wb[seg] = wsum;
+      sb[seg] = ssum;
+      mb[seg] = msum;
+      nkb += ceil_div(nslot, 16);
+      wsum += hpp->k_words[seg];
+      ssum += nslot;
+      if (w < 16) msum += nslot;
+    }
+    auto pick = [](const int (&a)[4], int i) { return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : a[3]; };
+    if (lane < 4) seg_kb_s[lane] = pick(nb, lane);
+    if (lane == 4) seg_kb_s[4] = nkb;
+    if (lane < nkb) {
+      const int seg = (lane >= nb[1]) + (lane >= nb[2]) + (lane >= nb[3]);
+      const int w = 16 >> seg, per = 32 / w;
+      const int nslot = pick(ns, seg);
+      const int s0 = 16 * (lane - pick(nb, seg));
+      KBDesc d;
+      d.width = (int16_t)w;
+      d.nrem = (int16_t)min(16, nslot - s0);
+      d.word0 = pick(wb, seg) + s0 / per;
+      d.meta0 = (w < 16 ? pick(mb, seg) + s0 : 0) / 2;
+      d.pad = pick(sb, seg) + s0;  // first slot of the block (for the query fragments)
+      kbd[lane] = d;
+    }
+  }
 
   auto item_cls = [&](int it) {
     return it < (int)cstart.v[1] ? 0 : it < (int)cstart.v[2] ? 1 : it < (int)cstart.v[3] ? 2 : it < zc_start ? 3 : -1;
@@ -547,7 +599,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   int* wpos = ring_pos + warp * kMaxInflight;
   uint32_t head_v = 0, tail_v = 0;     // virtual ring offsets (bytes)
   int* witem = ring_item + warp * kMaxInflight;
-  uint32_t vend[kMaxInflight];         // lane 0 only
+  uint32_t* vend = ring_vend + warp * kMaxInflight;  // ring end after each slot's copy (lane 0)
   int issued = 0, done = 0;
   bool drained = false;                // lane 0: no item left for this block
   int pending = -1;                    // lane 0: item taken but not yet issued (ring full)
@@ -555,8 +607,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     if (issued == done) head_v = tail_v = 0;  // empty ring: start at its beginning
     while (!drained && issued - done < kMaxInflight) {
       int it = pending;
-      if (it < 0) it = atomicAdd(&next_item, 1);  // items are taken in order of need: no warp idles early
-      if (it >= i1) {
+      if (it < 0) it = split + n_split * atomicAdd(&next_k, 1);  // taken in order of need: no warp idles early
+      if (it >= n_items) {
         drained = true;
         break;
       }
@@ -606,37 +658,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     for (int k = 0; k < kMaxInflight; ++k) mbar_init(&wbar[k], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();  // next_item is set
+  __syncthreads();  // next_k, the barriers and the k-block descriptors are set
   if (lane == 0) issue();  // the first copies fly while the query fragments are built
-  // stage the query rows of the group and this head's slot table (one coalesced round trip each)
-  const int16_t* slot_ch = plan_slots(P.plan) + (int64_t)head * plan_header(P.plan)->slot_stride;
-  const int qbase = b * P.h_q + j * G;
-  const int k_slots = hpp->k_slots;
-  for (int i = tid; i < G * D; i += blockDim.x) q_s[i] = load_as_float(P.q, (int64_t)qbase * D + i, P.dtype);
-  for (int i = tid; i < k_slots; i += blockDim.x) slot_s[i] = slot_ch[i];
-
-  // k-block descriptors of this head's K rows (each block inside one width segment)
-  if (tid == 0) {
-    int nkb = 0, wbase = 0, sbase = 0, meta = 0;
-    for (int seg = 0; seg < 4; ++seg) {
-      const int w = 16 >> seg, per = 32 / w;
-      const int nslot = hpp->k_words[seg] * per;
-      seg_kb_s[seg] = nkb;
-      for (int s0 = 0; s0 < nslot; s0 += 16) {
-        KBDesc d;
-        d.width = (int16_t)w;
-        d.nrem = (int16_t)min(16, nslot - s0);
-        d.word0 = wbase + s0 / per;
-        d.meta0 = (w < 16 ? meta + s0 : 0) / 2;
-        d.pad = sbase + s0;  // first slot of the block (for the query fragments)
-        kbd[nkb++] = d;
-      }
-      wbase += hpp->k_words[seg];
-      sbase += nslot;
-      if (w < 16) meta += nslot;
-    }
-    seg_kb_s[4] = nkb;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = tid + k * kDecWarps * 32;
+    if (i < G * D) q_s[i] = qr[k];
   }
+  if (tid < k_slots) slot_s[tid] = sr;
   __syncthreads();
   const int nkb = seg_kb_s[4];
   int seg_kb[5];
@@ -820,12 +849,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   if (!is_last) return;
   __threadfence();
   if (tid == 0) P.tickets[head] = 0;  // every block of this head has counted: ready for the next call
-  // Merge: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per query head.  The splits' partial
-  // blocks are copied into shared memory (the ring area is free) in chunks with coalesced loads.
+  // Merge: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per query head.  The splits'
+  // partials (contiguous) are copied into shared memory (the ring area is free) by 16-byte
+  // asynchronous copies, all in flight at once, in chunks that fit; each split's weight
+  // 2^(m_s - M) is computed once per head.
   __shared__ float Mh[8], Lh[8], Sh[8];  // running max, running sum, rescale of the previous chunks
+  const int per = pstride;               // floats of one split's partial
+  const int chunk = max(1, (int)((int64_t)kDecWarps * P.ring_bytes / (4 * (per + 8))));
   float* buf = reinterpret_cast<float*>(ring);
-  const int per = pstride;                                       // floats of one split's partial
-  const int chunk = max(1, (int)((int64_t)kDecWarps * P.ring_bytes / 4 / per));
+  float* wts = buf + (int64_t)chunk * per;  // [8][chunk]
   if (tid < G) {
     Mh[tid] = -INFINITY;
     Lh[tid] = 0.f;
@@ -833,20 +865,24 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   float o[4] = {0.f, 0.f, 0.f, 0.f};  // outputs i = tid + k * blockDim.x, k < 4 (G * D <= 1024)
   for (int s0 = 0; s0 < n_split; s0 += chunk) {
     const int ns = min(chunk, n_split - s0);
-    const float4* src = reinterpret_cast<const float4*>(part + (int64_t)s0 * per);
-    float4* dst = reinterpret_cast<float4*>(buf);
+    const float* src = part + (int64_t)s0 * per;
     __syncthreads();  // the previous chunk is consumed
-    for (int i = tid; i < ns * per / 4; i += blockDim.x) dst[i] = __ldcg(src + i);
+    for (int i = tid; i < ns * per / 4; i += blockDim.x)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + 4 * i)), "l"(src + 4 * i)
+                   : "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if (tid < G) {
-      float mc = -INFINITY;
-      for (int sp = 0; sp < ns; ++sp) mc = fmaxf(mc, buf[sp * per + tid * (D + 2) + D]);
-      const float Mo = Mh[tid], Mn = fmaxf(Mo, mc);
+      const float Mo = Mh[tid];
+      float Mn = Mo;
+      for (int sp = 0; sp < ns; ++sp) Mn = fmaxf(Mn, buf[sp * per + tid * (D + 2) + D]);
       const float so = (Mo == -INFINITY) ? 0.f : exp2f(Mo - Mn);
       float L = Lh[tid] * so;
       for (int sp = 0; sp < ns; ++sp) {
         const float ms = buf[sp * per + tid * (D + 2) + D];
-        if (ms != -INFINITY) L += exp2f(ms - Mn) * buf[sp * per + tid * (D + 2) + D + 1];
+        const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - Mn);
+        wts[tid * chunk + sp] = wgt;
+        L = fmaf(wgt, buf[sp * per + tid * (D + 2) + D + 1], L);
       }
       Mh[tid] = Mn;
       Lh[tid] = L;
@@ -858,13 +894,16 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       const int i = tid + k * blockDim.x;
       if (i < G * D) {
         const int h = i / D, c = i % D;
-        const float Mn = Mh[h];
-        float acc = o[k] * Sh[h];
-        for (int sp = 0; sp < ns; ++sp) {
-          const float ms = buf[sp * per + h * (D + 2) + D];
-          if (ms != -INFINITY) acc = fmaf(exp2f(ms - Mn), buf[sp * per + h * (D + 2) + c], acc);
+        const float* wh = wts + h * chunk;
+        const float* bh = buf + h * (D + 2) + c;
+        float a0 = o[k] * Sh[h], a1 = 0.f;
+        int sp = 0;
+        for (; sp + 1 < ns; sp += 2) {
+          a0 = fmaf(wh[sp], bh[sp * per], a0);
+          a1 = fmaf(wh[sp + 1], bh[(sp + 1) * per], a1);
         }
-        o[k] = acc;
+        if (sp < ns) a0 = fmaf(wh[sp], bh[sp * per], a0);
+        o[k] = a0 + a1;
       }
     }
   }
@@ -926,6 +965,63 @@ static size_t decode_ws_bytes(const DecodeGeom& g, int n_heads) {
 
 rdkv_status check_cache_public(const rdkv_cache* c);
 
+// Kernel arguments of one decode call; ws holds the partials, then the tickets and the status word.
+static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo, const void* q, float* out, void* ws) {
+  const rdkv_shape& s = cache->shape;
+  const int n_heads = s.batch * s.h_kv;
+  const PlanLayout L = plan_layout(s.batch, s.h_kv, s.head_dim);
+  DecodeParams P;
+  P.plan = cache->plan;
+  P.zone_a = cache->zone_a;
+  P.zone_b = cache->zone_b;
+  P.zone_c_k = cache->zone_c_k;
+  P.zone_c_v = cache->zone_c_v;
+  P.q = q;
+  P.partial = static_cast<float*>(ws);
+  P.tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + geo.ticket_off);
+  P.error = P.tickets + n_heads;
+  P.out = out;
+  P.len_dev = cache->len_dev;
+  P.heads = reinterpret_cast<const rdkv_head_plan*>(static_cast<const char*>(cache->plan) + L.heads_off);
+  P.slots = reinterpret_cast<const int16_t*>(static_cast<const char*>(cache->plan) + L.slots_off);
+  P.slot_stride = L.slot_stride;
+  P.n_heads = n_heads;
+  P.dtype = s.dtype;
+  P.h_q = s.h_q;
+  P.h_kv = s.h_kv;
+  P.cap_c = cache->cap_c;
+  P.ring_bytes = geo.ring_bytes;
+  P.ctas = geo.ctas;
+  return P;
+}
+
+static rdkv_status launch_decode(const DecodeParams& P, const DecodeGeom& geo, const rdkv_shape& s, cudaStream_t cs) {
+  // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is captured)
+  static size_t smem_set[4][64] = {};
+  int dev = 0;
+  RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
+  const bool qlo = s.dtype == RDKV_F32;
+  const int ki = (s.head_dim == 128 ? 2 : 0) + (qlo ? 1 : 0);
+  const void* fn = ki == 3 ? (const void*)decode_kernel<128, true>
+                 : ki == 2 ? (const void*)decode_kernel<128, false>
+                 : ki == 1 ? (const void*)decode_kernel<64, true>
+                           : (const void*)decode_kernel<64, false>;
+  if (dev < 64 && geo.smem > smem_set[ki][dev]) {
+    RDKV_TRY_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmemLimit),
+                  "decode smem");
+    smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
+  }
+  const dim3 grid(geo.splits);
+  switch (ki) {
+    case 3: decode_kernel<128, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    case 2: decode_kernel<128, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    case 1: decode_kernel<64, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+    default: decode_kernel<64, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
+  }
+  RDKV_CHECK_LAUNCH("decode");
+  return RDKV_OK;
+}
+
 }  // namespace rdkv
 
 using namespace rdkv;
@@ -947,50 +1043,8 @@ extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, 
   RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
-  cudaStream_t cs = (cudaStream_t)stream;
-  DecodeParams P;
-  P.plan = cache->plan;
-  P.zone_a = cache->zone_a;
-  P.zone_b = cache->zone_b;
-  P.zone_c_k = cache->zone_c_k;
-  P.zone_c_v = cache->zone_c_v;
-  P.q = q;
-  P.partial = static_cast<float*>(ws);
-  P.tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + geo.ticket_off);
-  P.error = P.tickets + n_heads;
-  P.out = out;
-  P.len_dev = cache->len_dev;
-  P.dtype = s.dtype;
-  P.h_q = s.h_q;
-  P.h_kv = s.h_kv;
-  P.cap_c = cache->cap_c;
-  P.ring_bytes = geo.ring_bytes;
   // the tickets are zero here: the workspace starts zero-filled and every call leaves them at zero
-  // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is captured)
-  static size_t smem_set[4][64] = {};
-  int dev = 0;
-  RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
-  const bool qlo = s.dtype == RDKV_F32;
-  const int ki = (s.head_dim == 128 ? 2 : 0) + (qlo ? 1 : 0);
-  const void* fn = ki == 3 ? (const void*)decode_kernel<128, true>
-                 : ki == 2 ? (const void*)decode_kernel<128, false>
-                 : ki == 1 ? (const void*)decode_kernel<64, true>
-                           : (const void*)decode_kernel<64, false>;
-  if (dev < 64 && geo.smem > smem_set[ki][dev]) {
-    RDKV_TRY_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmemLimit),
-                  "decode smem");
-    smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
-  }
-  P.ctas = geo.ctas;
-  const dim3 grid(geo.splits);
-  switch (ki) {
-    case 3: decode_kernel<128, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    case 2: decode_kernel<128, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    case 1: decode_kernel<64, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    default: decode_kernel<64, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-  }
-  RDKV_CHECK_LAUNCH("decode");
-  return RDKV_OK;
+  return launch_decode(decode_params(cache, geo, q, out, ws), geo, s, (cudaStream_t)stream);
 }
 
 extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream) {
@@ -1055,48 +1109,8 @@ extern "C" rdkv_status rdkv_decode_attn_noalloc(const rdkv_cache* cache, const v
   void* ws = nullptr;
   st = noalloc_scratch(&ws);
   if (st != RDKV_OK) return st;
-  cudaStream_t cs = (cudaStream_t)stream;
-  DecodeParams P;
-  P.plan = cache->plan;
-  P.zone_a = cache->zone_a;
-  P.zone_b = cache->zone_b;
-  P.zone_c_k = cache->zone_c_k;
-  P.zone_c_v = cache->zone_c_v;
-  P.q = q;
-  P.partial = static_cast<float*>(ws);
-  P.tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + geo.ticket_off);
-  P.error = P.tickets + n_heads;
-  P.out = out;
-  P.len_dev = cache->len_dev;
-  P.dtype = s.dtype;
-  P.h_q = s.h_q;
-  P.h_kv = s.h_kv;
-  P.cap_c = cache->cap_c;
-  P.ring_bytes = geo.ring_bytes;
+  const DecodeParams P = decode_params(cache, geo, q, out, ws);
   // the previous call's tickets and status word are still in the scratch: clear them
-  RDKV_TRY_CUDA(cudaMemsetAsync(P.tickets, 0, ((size_t)n_heads + 1) * 4, cs), "decode ticket reset");
-  static size_t smem_set[4][64] = {};
-  int dev = 0;
-  RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
-  const bool qlo = s.dtype == RDKV_F32;
-  const int ki = (s.head_dim == 128 ? 2 : 0) + (qlo ? 1 : 0);
-  const void* fn = ki == 3 ? (const void*)decode_kernel<128, true>
-                 : ki == 2 ? (const void*)decode_kernel<128, false>
-                 : ki == 1 ? (const void*)decode_kernel<64, true>
-                           : (const void*)decode_kernel<64, false>;
-  if (dev < 64 && geo.smem > smem_set[ki][dev]) {
-    RDKV_TRY_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmemLimit),
-                  "decode smem");
-    smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
-  }
-  P.ctas = geo.ctas;
-  const dim3 grid(geo.splits);
-  switch (ki) {
-    case 3: decode_kernel<128, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    case 2: decode_kernel<128, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    case 1: decode_kernel<64, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    default: decode_kernel<64, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-  }
-  RDKV_CHECK_LAUNCH("decode");
-  return RDKV_OK;
+  RDKV_TRY_CUDA(cudaMemsetAsync(P.tickets, 0, ((size_t)n_heads + 1) * 4, (cudaStream_t)stream), "decode ticket reset");
+  return launch_decode(P, geo, s, (cudaStream_t)stream);
 }

@@ -43,9 +43,11 @@ struct KBDesc {
   int32_t pad;
 };
 
-// Bytes of the fixed part of the decode kernel's shared memory (before the rings).
-__host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
-  return ((256 + (int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + (int64_t)kMaxKB * 32 * 8 +
+// Bytes of the fixed part of the decode kernel's shared memory (before the rings): k-block
+// descriptors, query fragments (float4 per lane for fp32 queries, two fp16 pairs otherwise),
+// zone-C query fragments, per-lane offsets, query rows, slot table, ring bookkeeping.
+__host__ __device__ constexpr int64_t decode_fixed_smem(int D, bool qlo) {
+  return ((256 + (int64_t)kMaxKB * 32 * (qlo ? 16 : 8) + (int64_t)(D / 16) * 32 * 16 + (int64_t)kMaxKB * 32 * 16 +
            (int64_t)8 * D * 4 + (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 20) + 127) /
          128 * 128;
 }
@@ -296,27 +298,28 @@ __device__ __forceinline__ void k_segment(const unsigned char* const (&rows)[4],
 
 // The same for fp16 queries (q exact in fp16).  hi = fp16(q * scale) by one
 // half2 multiply (the exact product rounded once) and lo = q * scale - hi by
-// one half2 FMA, which is exact because that remainder fits fp16; the
-// zero-point term sum_c q_c zero_c runs on the tensor core as a one-row A
-// operand (row 0 = the zeros) against B = q, accumulated in zacc.
+// one half2 FMA, which is exact because that remainder fits fp16.  The codes
+// enter the tensor core as fp16 subnormals: the bit pattern of a code c placed
+// at bit 0 of a half-word is the value c * 2^-24 exactly, so one shift and one
+// mask make the A operand and the products land in sq scaled by 2^-24 (undone
+// once per tile).  Raw 16-bit channels go to sr at scale 1, and the zero-point
+// term sum_c q_c zero_c runs as an MMA whose A rows all hold the zeros, so
+// every row of zacc carries it for heads (2q, 2q+1).
 template <int W>
 __device__ __forceinline__ void k_segment_h(const unsigned char* const (&rows)[4], const unsigned char* kmeta, int kb0, int kb1,
-                                            const uint2* koff, const uint2* qh, int lane, float (&s)[2][4],
-                                            float (&slo)[2][4], float (&zacc)[4]) {
-  const int g = lane >> 2, q = lane & 3;
+                                            const uint4* koff, const uint2* qh, int lane, float (&sq)[2][4],
+                                            float (&sr)[2][4], float (&zacc)[4]) {
+  const int q = lane & 3;
   constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
   const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
   const int sh1 = W == 2 ? 2 * q + 8 : sh0;
-#pragma unroll 2
+#pragma unroll 1
   for (int kb = kb0; kb < kb1; ++kb) {
-    // this lane's byte offsets, 16 bits each: words of its two slot pairs in a row (bit 15 marks a
-    // pair past the segment end: only raw 16-bit words need zeroing then) and their metadata
-    const uint2 off = koff[kb * 32 + lane];
+    const uint4 off = koff[kb * 32 + lane];
     const uint2 qq = qh[kb * 32 + lane];  // q_g (fp16 pairs) at slots (2q, 2q+1), (2q+8, 2q+9); 0 for pads
-    const uint32_t w0 = off.x & 0x7fffu, w1 = (off.x >> 16) & 0x7fffu;
     uint32_t bh0 = qq.x, bh1 = qq.y, bl0 = 0, bl1 = 0;
     if (W != 16) {
-      const uint2 m0 = lds64(kmeta, off.y & 0xffffu), m1 = lds64(kmeta, off.y >> 16);
+      const uint2 m0 = lds64(kmeta, off.z), m1 = lds64(kmeta, off.w);
       const __half2 q0 = *reinterpret_cast<const __half2*>(&qq.x), q1 = *reinterpret_cast<const __half2*>(&qq.y);
       const __half2 s0 = *reinterpret_cast<const __half2*>(&m0.x), s1 = *reinterpret_cast<const __half2*>(&m1.x);
       const __half2 h0 = __hmul2(q0, s0), h1 = __hmul2(q1, s1);
@@ -325,32 +328,23 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* const (&rows)[4
       bh1 = *reinterpret_cast<const uint32_t*>(&h1);
       bl0 = *reinterpret_cast<const uint32_t*>(&l0);
       bl1 = *reinterpret_cast<const uint32_t*>(&l1);
-      // zero row: lanes of group 0 hold (zero_2q, zero_2q+1) and (zero_2q+8, zero_2q+9)
-      mma16816(zacc, g == 0 ? m0.y : 0u, 0u, g == 0 ? m1.y : 0u, 0u, qq.x, qq.y);
+      mma16816(zacc, m0.y, m0.y, m1.y, m1.y, qq.x, qq.y);
     }
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
       const unsigned char* r0 = rows[2 * tb];
       const unsigned char* r1 = rows[2 * tb + 1];
-      uint32_t a0, a1, a2, a3;
       if (W == 16) {
-        const uint32_t x0 = lds32(r0, w0), x1 = lds32(r1, w0), x2 = lds32(r0, w1), x3 = lds32(r1, w1);
-        const bool v0 = (off.x & 0x8000u) == 0, v1 = (off.x & 0x80000000u) == 0;
-        a0 = v0 ? x0 : 0u; a1 = v0 ? x1 : 0u; a2 = v1 ? x2 : 0u; a3 = v1 ? x3 : 0u;
-        mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
+        const uint32_t a0 = lds32(r0, off.x) & off.z, a1 = lds32(r1, off.x) & off.z;
+        const uint32_t a2 = lds32(r0, off.y) & off.w, a3 = lds32(r1, off.y) & off.w;
+        mma16816(sr[tb], a0, a1, a2, a3, bh0, bh1);
       } else {
-        const uint32_t x0 = lds32(r0, w0), x1 = lds32(r1, w0);
-        a0 = exact_codes(x0, sh0, mask2);
-        a1 = exact_codes(x1, sh0, mask2);
-        if (W == 2) {
-          a2 = exact_codes(x0, sh1, mask2);
-          a3 = exact_codes(x1, sh1, mask2);
-        } else {
-          a2 = exact_codes(lds32(r0, w1), sh1, mask2);
-          a3 = exact_codes(lds32(r1, w1), sh1, mask2);
-        }
-        mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
-        mma16816(slo[tb], a0, a1, a2, a3, bl0, bl1);
+        const uint32_t x0 = lds32(r0, off.x), x1 = lds32(r1, off.x);
+        const uint32_t x2 = W == 2 ? x0 : lds32(r0, off.y), x3 = W == 2 ? x1 : lds32(r1, off.y);
+        const uint32_t a0 = (x0 >> sh0) & mask2, a1 = (x1 >> sh0) & mask2;
+        const uint32_t a2 = (x2 >> sh1) & mask2, a3 = (x3 >> sh1) & mask2;
+        mma16816(sq[tb], a0, a1, a2, a3, bh0, bh1);
+        mma16816(sq[tb], a0, a1, a2, a3, bl0, bl1);
       }
     }
   }
@@ -358,7 +352,7 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* const (&rows)[4
 
 template <int D, bool QLO>
 __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsigned char* kmeta, int RW, const int (&seg_kb)[5],
-                                            const KBDesc* kbd, const float4* qv, const uint2* koff, int lane,
+                                            const KBDesc* kbd, const float4* qv, const uint4* koff, int lane,
                                             float (&s)[2][4]) {
   float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
   const int g = lane >> 2;
@@ -380,18 +374,19 @@ __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsig
     bo = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
   } else {
     const uint2* qh = reinterpret_cast<const uint2*>(qv);
-    float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // row 0 (lanes of group 0): zero-point term of heads 2q, 2q+1
-    float slo[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // remainder products, a separate chain
-    k_segment_h<16>(rows, kmeta, seg_kb[0], seg_kb[1], koff, qh, lane, s, slo, zacc);
-    k_segment_h<8>(rows, kmeta, seg_kb[1], seg_kb[2], koff, qh, lane, s, slo, zacc);
-    k_segment_h<4>(rows, kmeta, seg_kb[2], seg_kb[3], koff, qh, lane, s, slo, zacc);
-    k_segment_h<2>(rows, kmeta, seg_kb[3], seg_kb[4], koff, qh, lane, s, slo, zacc);
+    float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // zero-point term of heads 2q, 2q+1 (every row)
+    float sr[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // raw 16-bit channels, scale 1
+    k_segment_h<16>(rows, kmeta, seg_kb[0], seg_kb[1], koff, qh, lane, s, sr, zacc);
+    k_segment_h<8>(rows, kmeta, seg_kb[1], seg_kb[2], koff, qh, lane, s, sr, zacc);
+    k_segment_h<4>(rows, kmeta, seg_kb[2], seg_kb[3], koff, qh, lane, s, sr, zacc);
+    k_segment_h<2>(rows, kmeta, seg_kb[3], seg_kb[4], koff, qh, lane, s, sr, zacc);
+    // s holds the code products at 2^-24
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[tb][e] += slo[tb][e];
-    be = __shfl_sync(0xffffffffu, zacc[0], q);
-    bo = __shfl_sync(0xffffffffu, zacc[1], q);
+      for (int e = 0; e < 4; ++e) s[tb][e] = fmaf(s[tb][e], 16777216.f, sr[tb][e]);
+    be = zacc[0];
+    bo = zacc[1];
   }
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
@@ -469,7 +464,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     // blocks past the last head's range leave at once.  One round trip: the tile counts of every
     // head and the zone-C length are loaded together.
     const int len = min(*P.len_dev, P.cap_c);
-    int* items = reinterpret_cast<int*>(smem + decode_fixed_smem(D));  // scratch in the ring area
+    int* items = reinterpret_cast<int*>(smem + decode_fixed_smem(D, QLO));  // scratch in the ring area
     for (int h = tid; h < P.n_heads; h += blockDim.x) {
       const int4 t = *reinterpret_cast<const int4*>(P.heads[h].tiles);
       items[h] = t.x + t.y + t.z + t.w + ceil_div(len, kCRows);
@@ -515,16 +510,16 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
 
   // shared memory map
   KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
-  float4* qv = reinterpret_cast<float4*>(smem + 256);                              // [kMaxKB][32]
-  uint4* qfragc = reinterpret_cast<uint4*>(qv + kMaxKB * 32);                      // [D/16][32] hi, lo
-  uint2* koff = reinterpret_cast<uint2*>(qfragc + (D / 16) * 32);                  // [kMaxKB][32]
+  float4* qv = reinterpret_cast<float4*>(smem + 256);                              // [kMaxKB][32] (uint2 if !QLO)
+  uint4* qfragc = reinterpret_cast<uint4*>(smem + 256 + kMaxKB * 32 * (QLO ? 16 : 8));  // [D/16][32] hi, lo
+  uint4* koff = qfragc + (D / 16) * 32;                                            // [kMaxKB][32]
   float* q_s = reinterpret_cast<float*>(koff + kMaxKB * 32);                       // [8][D] query rows of the group
   int16_t* slot_s = reinterpret_cast<int16_t*>(q_s + 8 * D);                       // [D + kSlotPad] slot table
   uint64_t* bars = reinterpret_cast<uint64_t*>(slot_s + D + kSlotPad);             // [warps][kMaxInflight]
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
   int* ring_item = ring_pos + kDecWarps * kMaxInflight;                            // [warps][kMaxInflight]
   uint32_t* ring_vend = reinterpret_cast<uint32_t*>(ring_item + kDecWarps * kMaxInflight);  // [warps][kMaxInflight]
-  unsigned char* ring = smem + decode_fixed_smem(D);
+  unsigned char* ring = smem + decode_fixed_smem(D, QLO);
   float* red = reinterpret_cast<float*>(ring);                                     // [warps][8][D + 2], after the loop
   __shared__ int seg_kb_s[5];
   __shared__ int is_last;
@@ -690,17 +685,25 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       }
     }
     if (kb < nkb) {
-      // byte offsets of this lane's two slot pairs (words within a row; metadata), see k_segment_h
+      // this lane's byte offsets in a K row of the words holding its two slot pairs, and either the
+      // metadata offsets of those pairs (quantised widths; a pair past the segment end reads the
+      // block's first pair) or masks that zero raw 16-bit words past the segment end
       const KBDesc d = kbd[kb];
       const int w = d.width;
       const int o0 = w == 16 ? qq : w == 8 ? (qq >> 1) : 0;
       const int o1 = w == 16 ? qq + 4 : w == 8 ? (qq >> 1) + 2 : w == 4 ? 1 : 0;
       const bool v0 = 2 * qq < d.nrem, v1 = 2 * qq + 8 < d.nrem;
-      const uint32_t w0 = 4u * (uint32_t)(d.word0 + o0) | (v0 ? 0u : 0x8000u);
-      const uint32_t w1 = 4u * (uint32_t)(d.word0 + o1) | (v1 ? 0u : 0x8000u);
-      const uint32_t m0 = 8u * (uint32_t)(d.meta0 + (v0 ? qq : 0));  // a pair past the end reads the block's first pair
-      const uint32_t m1 = 8u * (uint32_t)(d.meta0 + (v1 ? qq + 4 : 0));
-      koff[kb * 32 + ln] = make_uint2(w0 | (w1 << 16), m0 | (m1 << 16));
+      uint4 e;
+      e.x = 4u * (uint32_t)(d.word0 + o0);
+      e.y = 4u * (uint32_t)(d.word0 + o1);
+      if (w == 16) {
+        e.z = v0 ? ~0u : 0u;
+        e.w = v1 ? ~0u : 0u;
+      } else {
+        e.z = 8u * (uint32_t)(d.meta0 + (v0 ? qq : 0));
+        e.w = 8u * (uint32_t)(d.meta0 + (v1 ? qq + 4 : 0));
+      }
+      koff[kb * 32 + ln] = e;
     }
     if (kb >= nkb) qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
     else if (QLO) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
@@ -937,7 +940,7 @@ static DecodeGeom decode_geom(const rdkv_cache* c) {
   const int D = s.head_dim, G = s.h_q / s.h_kv;
   const int n_heads = s.batch * s.h_kv;
   const int sms = num_sms();
-  const int64_t fixed = decode_fixed_smem(D);
+  const int64_t fixed = decode_fixed_smem(D, s.dtype == RDKV_F32);
   const int64_t max_item = std::max<int64_t>(align_up(c->sizes.max_stage_bytes, 128), 2 * kCRows * D * 2);
   g.max_item = max_item;
   int64_t ring = ((kTwoBlockSmem - fixed) / kDecWarps) / 128 * 128;

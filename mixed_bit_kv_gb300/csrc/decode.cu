@@ -178,6 +178,7 @@ __device__ __forceinline__ uint4 split_hi_lo(float x0, float x1, float x2, float
 template <int D>
 struct WarpAcc {
   float o[D / 16][4];   // O^T fragments: (ch 16cm+g, heads 2q, 2q+1), (ch 16cm+g+8, ...)
+  float z[4];           // zero-point products of packed V: row g = channel group g, heads 2q, 2q+1
   float m[2];           // running max (base 2) of heads 2q, 2q+1
   float l[2];           // this lane's share of the running sum
 };
@@ -214,6 +215,8 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
   }
   acc.l[0] = acc.l[0] * al0 + ps0;
   acc.l[1] = acc.l[1] * al1 + ps1;
+  acc.z[0] *= al0;
+  acc.z[1] *= al1;
 #pragma unroll
   for (int cm = 0; cm < D / 16; ++cm) {
     acc.o[cm][0] *= al0;
@@ -397,35 +400,80 @@ __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsig
   }
 }
 
-// PV of a zone-A tile with packed V of width VB.
+// PV of a zone-A tile with packed V of width VB.  A dequantised V element is
+// zero + scale * code per (token, 32-channel group), so per head h and channel c
+//   O[h][c] += sum_t (p_ht scale_t) code_tc + sum_t p_ht zero_t.
+// The codes enter the tensor core as fp16 subnormals (code * 2^-24, one shift
+// and one mask) against B = p * scale of the group (one half2 multiply per
+// fragment), so the products land in acc.o scaled by 2^-24 (the caller keeps
+// track of that scale); the zero-point sums go to acc.z through one MMA per
+// 16 tokens whose A row g holds the zeros of channel group g.
 template <int D, int VB>
 __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned char* vcodes, const unsigned char* vmeta, int lane,
                                                const uint32_t (&pb)[2][2]) {
   const int g = lane >> 2, q = lane & 3;
   constexpr int wpp = D * VB / 16;  // words per token pair
-  constexpr int per = 16 / VB;      // channels per word
+  constexpr int per = 16 / VB;      // channels per half-word
+  constexpr int NG = D / 32;        // channel groups
   constexpr uint32_t mask2 = VB == 8 ? 0x00ff00ffu : VB == 4 ? 0x000f000fu : 0x00030003u;
   const int sh0 = VB * (g % per), sh1 = VB * ((g + 8) % per);
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
     const int p0 = 8 * tb + q, p1 = p0 + 4;
-    const unsigned char* base0 = vcodes + 4 * (p0 * wpp);
-    const unsigned char* base1 = vcodes + 4 * (p1 * wpp);
+    // words of channel c = 16 cm + g (+8): (16 cm)/per + g/per (+8/per)
+    const unsigned char* base0 = vcodes + 4 * (p0 * wpp + g / per);
+    const unsigned char* base1 = vcodes + 4 * (p1 * wpp + g / per);
+    uint32_t za0 = 0u, za2 = 0u;
+    if (g < NG) {
+      za0 = lds32(vmeta, 8 * (p0 * NG + g) + 4);
+      za2 = lds32(vmeta, 8 * (p1 * NG + g) + 4);
+    }
+    mma16816(acc.z, za0, 0u, za2, 0u, pb[tb][0], pb[tb][1]);
 #pragma unroll
-    for (int grp = 0; grp < D / 32; ++grp) {
-      const uint2 m0 = lds64(vmeta, 8 * (p0 * (D / 32) + grp));
-      const uint2 m1 = lds64(vmeta, 8 * (p1 * (D / 32) + grp));
+    for (int grp = 0; grp < NG; ++grp) {
+      const uint32_t s0 = lds32(vmeta, 8 * (p0 * NG + grp)), s1 = lds32(vmeta, 8 * (p1 * NG + grp));
+      const __half2 b0h = __hmul2(*reinterpret_cast<const __half2*>(&pb[tb][0]), *reinterpret_cast<const __half2*>(&s0));
+      const __half2 b1h = __hmul2(*reinterpret_cast<const __half2*>(&pb[tb][1]), *reinterpret_cast<const __half2*>(&s1));
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&b0h), b1 = *reinterpret_cast<const uint32_t*>(&b1h);
+      uint32_t w0[4], w1[4];  // words of (cm, c0), (cm, c1) for cm = 2 grp, 2 grp + 1
+      if (VB == 2) {
+        // the pair's words 4 grp .. 4 grp + 3 are exactly these (g / per = 0)
+        const uint4 v0 = *reinterpret_cast<const uint4*>(vcodes + 4 * (p0 * wpp) + 16 * grp);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(vcodes + 4 * (p1 * wpp) + 16 * grp);
+        w0[0] = v0.x; w0[1] = v0.y; w0[2] = v0.z; w0[3] = v0.w;
+        w1[0] = v1.x; w1[1] = v1.y; w1[2] = v1.z; w1[3] = v1.w;
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int cm = 2 * grp + half;
+          w0[2 * half] = lds32(base0, 4 * ((16 * cm) / per));
+          w0[2 * half + 1] = lds32(base0, 4 * ((16 * cm + 8) / per));
+          w1[2 * half] = lds32(base1, 4 * ((16 * cm) / per));
+          w1[2 * half + 1] = lds32(base1, 4 * ((16 * cm + 8) / per));
+        }
+      }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int cm = 2 * grp + half;
-        const int c0 = 16 * cm + g, c1 = c0 + 8;
-        const uint32_t a0 = dequant_pair(lds32(base0, 4 * (c0 / per)), sh0, mask2, m0.x, m0.y);
-        const uint32_t a1 = dequant_pair(lds32(base0, 4 * (c1 / per)), sh1, mask2, m0.x, m0.y);
-        const uint32_t a2 = dequant_pair(lds32(base1, 4 * (c0 / per)), sh0, mask2, m1.x, m1.y);
-        const uint32_t a3 = dequant_pair(lds32(base1, 4 * (c1 / per)), sh1, mask2, m1.x, m1.y);
-        mma16816(acc.o[cm], a0, a1, a2, a3, pb[tb][0], pb[tb][1]);
+        const uint32_t a0 = (w0[2 * half] >> sh0) & mask2;
+        const uint32_t a1 = (w0[2 * half + 1] >> sh1) & mask2;
+        const uint32_t a2 = (w1[2 * half] >> sh0) & mask2;
+        const uint32_t a3 = (w1[2 * half + 1] >> sh1) & mask2;
+        mma16816(acc.o[cm], a0, a1, a2, a3, b0, b1);
       }
     }
+  }
+}
+
+// Multiplies the O^T accumulators by f (a power of two: exact).
+template <int D>
+__device__ __forceinline__ void scale_o(WarpAcc<D>& acc, float f) {
+#pragma unroll
+  for (int cm = 0; cm < D / 16; ++cm) {
+    acc.o[cm][0] *= f;
+    acc.o[cm][1] *= f;
+    acc.o[cm][2] *= f;
+    acc.o[cm][3] *= f;
   }
 }
 
@@ -714,6 +762,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   WarpAcc<D> acc;
 #pragma unroll
   for (int cm = 0; cm < D / 16; ++cm) acc.o[cm][0] = acc.o[cm][1] = acc.o[cm][2] = acc.o[cm][3] = 0.f;
+  acc.z[0] = acc.z[1] = acc.z[2] = acc.z[3] = 0.f;
+  // acc.o holds packed-V products at 2^-24 while this is set; a warp meets the classes in
+  // increasing order (items ascend), so it switches at most once, at its first 16-bit tile or
+  // zone-C block
+  bool o_sub = true;
   acc.m[0] = acc.m[1] = -INFINITY;
   acc.l[0] = acc.l[1] = 0.f;
   const float sl2 = 1.4426950408889634f / sqrtf((float)D);
@@ -751,11 +804,22 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       uint32_t pb[2][2];
       softmax_update<D, 2>(acc, s, pb);
       const unsigned char* vcodes = kmeta + 4 * meta_slots;
+      if (cls < 3 && !o_sub) {
+        scale_o(acc, 5.9604644775390625e-8f);
+        o_sub = true;
+      } else if (cls == 3 && o_sub) {
+        scale_o(acc, 16777216.f);
+        o_sub = false;
+      }
       if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + kTile * D * 2 / 8, lane, pb);
       else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + kTile * D * 4 / 8, lane, pb);
       else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + kTile * D * 8 / 8, lane, pb);
       else pv_fp16<D, 2>(acc, st + (uint32_t)ctb.v[3], lane, pb);
     } else {
+      if (o_sub) {
+        scale_o(acc, 16777216.f);
+        o_sub = false;
+      }
       const int c_row = (it - zc_start) * kCRows;
       const int rows = min(kCRows, len_c - c_row);
       if (rows < kCRows) {  // clear the rows the copy did not fill (they meet p = 0 in the products)
@@ -802,6 +866,17 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     __syncwarp();
   }
   __syncthreads();  // every ring drained: the ring area now holds the warps' results
+  if (o_sub) scale_o(acc, 16777216.f);
+  // zero-point sums of packed V: channel 16 cm + g (+8) is in group cm / 2, held by lane (cm / 2, q)
+#pragma unroll
+  for (int cm = 0; cm < D / 16; ++cm) {
+    const float z0 = __shfl_sync(0xffffffffu, acc.z[0], (cm / 2) * 4 + q);
+    const float z1 = __shfl_sync(0xffffffffu, acc.z[1], (cm / 2) * 4 + q);
+    acc.o[cm][0] += z0;
+    acc.o[cm][1] += z1;
+    acc.o[cm][2] += z0;
+    acc.o[cm][3] += z1;
+  }
 
   // warp result -> shared memory: m, l per head; O per head and channel
   float l0 = acc.l[0], l1 = acc.l[1];

@@ -494,6 +494,18 @@ __device__ __forceinline__ void pv_fp16(WarpAcc<D>& acc, uint32_t vrows, int lan
   }
 }
 
+// Estimated decode cost of a head (instruction units per warp) from its plan record: every tile
+// pays a base (softmax, staging) plus its K k-blocks (quantised blocks cost about twice a raw
+// 16-bit one) plus its V class; every zone-C block of 16 rows pays a flat amount.  Only the ratios
+// between heads matter: they decide how many blocks each head gets.
+__device__ __forceinline__ int64_t head_cost(const rdkv_head_plan& hp, int zc_blocks) {
+  const int nkb16 = ceil_div(hp.k_words[0] * 2, 16);
+  const int nkbq = ceil_div(hp.k_words[1] * 4, 16) + ceil_div(hp.k_words[2] * 8, 16) + ceil_div(hp.k_words[3] * 16, 16);
+  const int64_t per_tile = 250 + 20 * nkb16 + 40 * nkbq;
+  return (int64_t)hp.tiles[0] * (per_tile + 200) + (int64_t)hp.tiles[1] * (per_tile + 215) +
+         (int64_t)hp.tiles[2] * (per_tile + 250) + (int64_t)hp.tiles[3] * (per_tile + 60) + (int64_t)zc_blocks * 300;
+}
+
 // Per-class values of a head, read with a class index without dynamic array indexing.
 struct ClassVals {
   int64_t v[4];
@@ -506,42 +518,53 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.h_q / P.h_kv;
   __shared__ int asg[4];  // head, first block of the head, blocks of the head, zone-C rows
-  {
-    // Blocks are dealt to heads in proportion to their items (tiles plus zone-C blocks), at least
-    // one per head, over a nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the
-    // blocks past the last head's range leave at once.  One round trip: the tile counts of every
-    // head and the zone-C length are loaded together.
+  __shared__ __align__(16) rdkv_head_plan hp_s;  // this block's head record
+  if (warp == 0) {
+    // Blocks are dealt to heads in proportion to their estimated cost, at least one per head, over a
+    // nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the blocks past the last head's
+    // range leave at once.  Warp 0: one lane per head, one round trip for the plan records and the
+    // zone-C length, then a scan.
     const int len = min(*P.len_dev, P.cap_c);
-    int* items = reinterpret_cast<int*>(smem + decode_fixed_smem(D, QLO));  // scratch in the ring area
-    for (int h = tid; h < P.n_heads; h += blockDim.x) {
-      const int4 t = *reinterpret_cast<const int4*>(P.heads[h].tiles);
-      items[h] = t.x + t.y + t.z + t.w + ceil_div(len, kCRows);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int64_t total = 0;
-      for (int h = 0; h < P.n_heads; ++h) total += items[h];
-      int start = 0;
-      asg[0] = -1;
-      asg[3] = len;
-      for (int h = 0; h < P.n_heads; ++h) {
-        const int c = max(1, (int)(total > 0 ? (int64_t)items[h] * P.ctas / total : 0));
-        if ((int)blockIdx.x >= start && (int)blockIdx.x < start + c) {
-          asg[0] = h;
-          asg[1] = start;
-          asg[2] = c;
-          break;
-        }
-        start += c;
+    const int zc = ceil_div(len, kCRows);
+    int64_t total = 0;
+    for (int h = lane; h < P.n_heads; h += 32) total += head_cost(P.heads[h], zc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    int start = 0, found = -1;
+    for (int h0 = 0; h0 < P.n_heads; h0 += 32) {
+      const int h = h0 + lane;
+      const int64_t w = h < P.n_heads ? head_cost(P.heads[h], zc) : 0;
+      const int c = h < P.n_heads ? max(1, (int)(total > 0 ? w * P.ctas / total : 0)) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
+      const int first = start + incl - c;
+      if (c > 0 && (int)blockIdx.x >= first && (int)blockIdx.x < first + c) {
+        asg[0] = h;
+        asg[1] = first;
+        asg[2] = c;
+        found = h;
+      }
+      start += __shfl_sync(0xffffffffu, incl, 31);
     }
-    __syncthreads();
+    const unsigned any = __ballot_sync(0xffffffffu, found >= 0);
+    const int head_found = any ? __shfl_sync(0xffffffffu, found, __ffs(any) - 1) : -1;
+    if (lane == 0) {
+      if (!any) asg[0] = -1;
+      asg[3] = len;
+    }
+    if (head_found >= 0)  // the head record into shared memory, one word per lane
+      reinterpret_cast<int32_t*>(&hp_s)[lane] = reinterpret_cast<const int32_t*>(P.heads + head_found)[lane];
   }
+  __syncthreads();
   if (asg[0] < 0) return;
   const int head = asg[0], split = (int)blockIdx.x - asg[1], n_split = asg[2], first_block = asg[1];
   const int len_c = asg[3];
   const int b = head / P.h_kv, j = head % P.h_kv;
-  const rdkv_head_plan* hpp = P.heads + head;
+  const rdkv_head_plan* hpp = &hp_s;
 
   // the query rows of the group and the slot table go into registers now; they land while the
   // rings are set up and the first tiles are requested
@@ -905,17 +928,28 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   const int pstride = partial_stride(G, D);
   float* part = P.partial + (int64_t)first_block * pstride;
   float* mine = part + (int64_t)split * pstride;
+  // the warps' weights 2^(m_w - M) per head, once: thread (h, w) of the first 8 G threads
+  __shared__ float wred[8][kDecWarps], mred[8];
+  static_assert(kDecWarps == 8, "one group of 8 lanes per head");
+  if (tid < 64) {  // whole warps 0 and 1 take part in the shuffles (8 G <= 64)
+    const int h = tid / kDecWarps, w = tid % kDecWarps;
+    const float mw = h < G ? red[((int64_t)w * 8 + h) * (D + 2) + D] : -INFINITY;
+    float M = mw;
+#pragma unroll
+    for (int o = 1; o < kDecWarps; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (h < G) {
+      wred[h][w] = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      if (w == 0) mred[h] = M;
+    }
+  }
+  __syncthreads();
   for (int i = tid; i < G * (D + 2); i += blockDim.x) {
     const int h = i / (D + 2), c = i % (D + 2);
-    float M = -INFINITY;
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red[((int64_t)w * 8 + h) * (D + 2) + D]);
-    float val = M;
+    float val = mred[h];
     if (c != D) {
       val = 0.f;
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float mw = red[((int64_t)w * 8 + h) * (D + 2) + D];
-        if (mw != -INFINITY) val += exp2f(mw - M) * red[((int64_t)w * 8 + h) * (D + 2) + c];
-      }
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) val = fmaf(wred[h][w], red[((int64_t)w * 8 + h) * (D + 2) + c], val);
     }
     mine[i] = val;
   }
@@ -950,21 +984,29 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
                    : "memory");
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if (tid < G) {
-      const float Mo = Mh[tid];
-      float Mn = Mo;
-      for (int sp = 0; sp < ns; ++sp) Mn = fmaxf(Mn, buf[sp * per + tid * (D + 2) + D]);
+    if (warp < G) {  // warp h: the weights of head h, its lanes over the splits
+      const int h = warp;
+      const float Mo = Mh[h];
+      float mc = -INFINITY;
+      for (int sp = lane; sp < ns; sp += 32) mc = fmaxf(mc, buf[sp * per + h * (D + 2) + D]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+      const float Mn = fmaxf(Mo, mc);
       const float so = (Mo == -INFINITY) ? 0.f : exp2f(Mo - Mn);
-      float L = Lh[tid] * so;
-      for (int sp = 0; sp < ns; ++sp) {
-        const float ms = buf[sp * per + tid * (D + 2) + D];
+      float L = 0.f;
+      for (int sp = lane; sp < ns; sp += 32) {
+        const float ms = buf[sp * per + h * (D + 2) + D];
         const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - Mn);
-        wts[tid * chunk + sp] = wgt;
-        L = fmaf(wgt, buf[sp * per + tid * (D + 2) + D + 1], L);
+        wts[h * chunk + sp] = wgt;
+        L = fmaf(wgt, buf[sp * per + h * (D + 2) + D + 1], L);
       }
-      Mh[tid] = Mn;
-      Lh[tid] = L;
-      Sh[tid] = so;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (lane == 0) {
+        Mh[h] = Mn;
+        Lh[h] = Lh[h] * so + L;
+        Sh[h] = so;
+      }
     }
     __syncthreads();
 #pragma unroll

@@ -186,8 +186,8 @@ def run_ours(args, ws, rank, local):
     def decode_phase():
         for s in range(S):
             for layer in range(L):
-                rdkv.rdkv_append(caches[layer], dk[s, layer], dv[s, layer])
-                rdkv.rdkv_decode_attn(caches[layer], dq[s, layer], out=outs[s, layer])
+                # append the new token and attend, one launch per layer
+                rdkv.rdkv_decode_step(caches[layer], dq[s, layer], dk[s, layer], dv[s, layer], out=outs[s, layer])
 
     # warm-up: eager once (allocates every buffer), then capture the decode phase
     compress(None)
@@ -344,8 +344,7 @@ def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, de
             d_dk.copy_(h_dk[s], non_blocking=True)
             d_dv.copy_(h_dv[s], non_blocking=True)
             for layer in range(L):
-                rdkv.rdkv_append(caches[layer], d_dk[layer], d_dv[layer])
-                rdkv.rdkv_decode_attn(caches[layer], d_dq[layer], out=d_out[layer])
+                rdkv.rdkv_decode_step(caches[layer], d_dq[layer], d_dk[layer], d_dv[layer], out=d_out[layer])
             h_out[s].copy_(d_out, non_blocking=True)
 
     step_compress()

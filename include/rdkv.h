@@ -208,10 +208,33 @@ size_t rdkv_decode_workspace_bytes(const rdkv_cache* cache);
 rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, float* out,
                              void* ws, size_t ws_bytes, void* stream);
 
-/* Reads the status word the rdkv_decode_attn calls on this cache and ws left
- * behind since the last read, and clears it.  SYNCHRONISES `stream`.
- * RDKV_ERR_TIMEOUT means a bounded wait for a tile copy ran out in one of
- * those calls (its output is not valid). */
+/* Launch order (rdkv_decode_attn and rdkv_decode_step): the kernel is launched
+ * as a programmatic dependent of the kernel before it on `stream`.  Before it
+ * waits for that kernel it reads only the plan and zone A (dealing the work,
+ * staging tile copies); the query, the new token, zone C and *len_dev are read
+ * after the wait.  So the plan and zone A must not be written by the kernel
+ * launched immediately before a decode call on the same stream (rdkv_pack ends
+ * with a kernel that writes neither); anything else may be. */
+
+/* ---------------------------------------------------------------- decode step
+ * RDKV section 2.3, one decode step in one launch: rdkv_append(k_new, v_new)
+ * followed by rdkv_decode_attn(q), computed together.  The new token's row
+ * enters the attention straight from k_new/v_new; once every block of a head
+ * has read zone C, that head's row is stored at row *len_dev, and the last
+ * head to finish advances *len_dev (and the call advances the host mirror
+ * len_c).  Same q/out layout and workspace (same size, same zero-filled
+ * contract) as rdkv_decode_attn.  Returns RDKV_ERR_CAPACITY (nothing
+ * launched) when the host mirror len_c == cap_c; a replayed step that finds
+ * *len_dev == cap_c attends with the new token but stores nothing and leaves
+ * RDKV_ERR_CAPACITY in the status word. */
+rdkv_status rdkv_decode_step(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new,
+                             float* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Reads the status word the rdkv_decode_attn / rdkv_decode_step calls on this
+ * cache and ws left behind since the last read, and clears it.  SYNCHRONISES
+ * `stream`.  RDKV_ERR_TIMEOUT means a bounded wait for a tile copy ran out in
+ * one of those calls (its output is not valid); RDKV_ERR_CAPACITY means a
+ * step found zone C full and did not store its token. */
 rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream);
 
 /* ---------------------------------------------------------------- decode without a workspace

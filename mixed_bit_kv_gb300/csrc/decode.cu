@@ -48,7 +48,7 @@ struct KBDesc {
 // zone-C query fragments, per-lane offsets, query rows, slot table, ring bookkeeping.
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D, bool qlo) {
   return ((256 + (int64_t)kMaxKB * 32 * (qlo ? 16 : 8) + (int64_t)(D / 16) * 32 * 16 + (int64_t)kMaxKB * 32 * 16 +
-           (int64_t)8 * D * 4 + (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 20) + 127) /
+           (int64_t)8 * D * 4 + (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 20 + (int64_t)2 * D * 2) + 127) /
          128 * 128;
 }
 // Floats of one block's partial result (m, l, o for G heads), rounded up to a multiple of 4.
@@ -68,7 +68,10 @@ struct DecodeParams {
   int32_t* error;   // device status word
   int32_t* tickets; // [n_heads] blocks finished per head (zeroed before the launch)
   float* out;       // [batch][h_q][D]
-  const int32_t* len_dev;  // zone-C rows in use
+  int32_t* len_dev;        // zone-C rows in use (advanced by the fused step)
+  const void* k_new;       // fused step: the new token's K and V [batch][h_kv][D] (dtype), else NULL
+  const void* v_new;
+  int32_t* gticket;        // fused step: heads merged so far (zero between launches)
   const rdkv_head_plan* heads;  // the plan's head records (offset fixed by the shape)
   const int16_t* slots;         // the plan's slot tables, slot_stride entries per head
   int dtype, h_q, h_kv, cap_c, ring_bytes, ctas, n_heads, slot_stride;
@@ -517,15 +520,18 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.h_q / P.h_kv;
-  __shared__ int asg[4];  // head, first block of the head, blocks of the head, zone-C rows
+  // the next kernel on the stream may start its own static setup once every block of this one runs
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ int asg[3];  // head, first block of the head, blocks of the head
   __shared__ __align__(16) rdkv_head_plan hp_s;  // this block's head record
   if (warp == 0) {
     // Blocks are dealt to heads in proportion to their estimated cost, at least one per head, over a
     // nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the blocks past the last head's
     // range leave at once.  Warp 0: one lane per head, one round trip for the plan records and the
     // zone-C length, then a scan.
-    const int len = min(*P.len_dev, P.cap_c);
-    const int zc = ceil_div(len, kCRows);
+    // static inputs only (plan and capacity): the dealing is the same in every launch, also before
+    // the previous kernel on the stream has finished
+    const int zc = ceil_div(P.cap_c, kCRows);
     int64_t total = 0;
     for (int h = lane; h < P.n_heads; h += 32) total += head_cost(P.heads[h], zc);
 #pragma unroll
@@ -552,30 +558,20 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     }
     const unsigned any = __ballot_sync(0xffffffffu, found >= 0);
     const int head_found = any ? __shfl_sync(0xffffffffu, found, __ffs(any) - 1) : -1;
-    if (lane == 0) {
-      if (!any) asg[0] = -1;
-      asg[3] = len;
-    }
+    if (lane == 0 && !any) asg[0] = -1;
     if (head_found >= 0)  // the head record into shared memory, one word per lane
       reinterpret_cast<int32_t*>(&hp_s)[lane] = reinterpret_cast<const int32_t*>(P.heads + head_found)[lane];
   }
   __syncthreads();
   if (asg[0] < 0) return;
   const int head = asg[0], split = (int)blockIdx.x - asg[1], n_split = asg[2], first_block = asg[1];
-  const int len_c = asg[3];
   const int b = head / P.h_kv, j = head % P.h_kv;
   const rdkv_head_plan* hpp = &hp_s;
+  const bool fused = P.k_new != nullptr;
 
-  // the query rows of the group and the slot table go into registers now; they land while the
-  // rings are set up and the first tiles are requested
+  // the slot table goes into registers now (static data)
   const int qbase = b * P.h_q + j * G;
   const int16_t* slot_ch = P.slots + (int64_t)head * P.slot_stride;
-  float qr[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = tid + k * kDecWarps * 32;
-    qr[k] = i < G * D ? load_as_float(P.q, (int64_t)qbase * D + i, P.dtype) : 0.f;
-  }
   const int k_slots = hpp->k_slots;  // <= D + kSlotPad <= the block's threads
   const int16_t sr = tid < k_slots ? slot_ch[tid] : (int16_t)-1;
 
@@ -590,6 +586,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
   int* ring_item = ring_pos + kDecWarps * kMaxInflight;                            // [warps][kMaxInflight]
   uint32_t* ring_vend = reinterpret_cast<uint32_t*>(ring_item + kDecWarps * kMaxInflight);  // [warps][kMaxInflight]
+  uint16_t* newrow = reinterpret_cast<uint16_t*>(ring_vend + kDecWarps * kMaxInflight);     // [2][D] fused step: k, v
   unsigned char* ring = smem + decode_fixed_smem(D, QLO);
   float* red = reinterpret_cast<float*>(ring);                                     // [warps][8][D + 2], after the loop
   __shared__ int seg_kb_s[5];
@@ -615,8 +612,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   }
   const int64_t b_row = hpp->b_row;
   const int RW = hpp->row_words, meta_slots = hpp->meta_slots;
-  // split s of n takes items s, s + n, s + 2n, ...: every split gets its share of each class
-  const int n_items = zc_start + ceil_div(len_c, kCRows);
+  // split s of n takes items s, s + n, s + 2n, ...: every split gets its share of each class.  The
+  // zone-C length is known only after the wait for the previous kernel: until then only zone-A
+  // items are issued (an item past them stays pending)
+  int n_items = zc_start, len_c = 0, n_rows = 0;
+  bool items_final = false;
   if (tid == 0) next_k = 0;
 
   // k-block descriptors of this head's K rows (each block inside one width segment), one per thread
@@ -675,7 +675,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       int it = pending;
       if (it < 0) it = split + n_split * atomicAdd(&next_k, 1);  // taken in order of need: no warp idles early
       if (it >= n_items) {
-        drained = true;
+        if (items_final) drained = true;
+        else pending = it;
         break;
       }
       const int cls = item_cls(it);
@@ -710,12 +711,15 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
         bulk_copy(dst, P.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar);
         if (zb) bulk_copy(dst + a_bytes, P.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar);
       } else {
-        const int rows = min(kCRows, len_c - c_row);
+        // rows of zone C (the fused step's new row, past them, is written by the consumer)
+        const int rows = max(0, min(kCRows, len_c - c_row));
         const uint32_t bytes = (uint32_t)rows * D * 2;
         const int64_t src = ((int64_t)head * P.cap_c + c_row) * D;
         mbar_arrive_expect_tx(bar, 2 * bytes);
-        bulk_copy(dst, P.zone_c_k + src, bytes, bar);
-        bulk_copy(dst + kCRows * D * 2, P.zone_c_v + src, bytes, bar);
+        if (bytes) {
+          bulk_copy(dst, P.zone_c_k + src, bytes, bar);
+          bulk_copy(dst + kCRows * D * 2, P.zone_c_v + src, bytes, bar);
+        }
       }
       ++issued;
     }
@@ -725,7 +729,25 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();  // next_k, the barriers and the k-block descriptors are set
-  if (lane == 0) issue();  // the first copies fly while the query fragments are built
+  if (lane == 0) issue();  // the first zone-A copies fly while the query fragments are built
+  // Everything so far read only the plan and zone A, which the kernel launched just before this one
+  // on the stream does not write.  The query, the new token and the zone-C length may come from
+  // it: wait for it here (a no-op without programmatic dependent launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  len_c = min(*P.len_dev, P.cap_c);
+  n_rows = len_c + (fused ? 1 : 0);
+  n_items = zc_start + ceil_div(n_rows, kCRows);
+  items_final = true;
+  float qr[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = tid + k * kDecWarps * 32;
+    qr[k] = i < G * D ? load_as_float(P.q, (int64_t)qbase * D + i, P.dtype) : 0.f;
+  }
+  if (fused && tid < 2 * D) {
+    const int64_t src = (int64_t)head * D + (tid % D);
+    newrow[tid] = half_bits(load_as_float(tid < D ? P.k_new : P.v_new, src, P.dtype));
+  }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int i = tid + k * kDecWarps * 32;
@@ -844,12 +866,21 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
         o_sub = false;
       }
       const int c_row = (it - zc_start) * kCRows;
-      const int rows = min(kCRows, len_c - c_row);
-      if (rows < kCRows) {  // clear the rows the copy did not fill (they meet p = 0 in the products)
+      const int rows = min(kCRows, n_rows - c_row);  // rows attended (the fused step's new row last)
+      const int copied = max(0, min(kCRows, len_c - c_row));
+      if (rows < kCRows || copied < rows) {
         uint32_t* kz = reinterpret_cast<uint32_t*>(wring + wpos[slot]);
+        // clear the rows past the attended ones (they meet p = 0 in the products)
         for (int i = rows * D / 2 + lane; i < kCRows * D / 2; i += 32) {
           kz[i] = 0u;
           kz[kCRows * D / 2 + i] = 0u;
+        }
+        if (copied < rows) {  // the new row, from the staged copy of the caller's k_new, v_new
+          const uint32_t* nr = reinterpret_cast<const uint32_t*>(newrow);
+          for (int i = lane; i < D / 2; i += 32) {
+            kz[copied * D / 2 + i] = nr[i];
+            kz[kCRows * D / 2 + copied * D / 2 + i] = nr[D / 2 + i];
+          }
         }
         __syncwarp();
       }
@@ -961,6 +992,23 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   if (!is_last) return;
   __threadfence();
   if (tid == 0) P.tickets[head] = 0;  // every block of this head has counted: ready for the next call
+  if (fused) {
+    // every block of this head has read zone C: store the new row of this head; the last head to
+    // get here advances the length (every block of every head has read it by then)
+    if (len_c < P.cap_c) {
+      const int64_t dst = ((int64_t)head * P.cap_c + len_c) * D;
+      for (int i = tid; i < D; i += blockDim.x) {
+        const_cast<uint16_t*>(P.zone_c_k)[dst + i] = newrow[i];
+        const_cast<uint16_t*>(P.zone_c_v)[dst + i] = newrow[D + i];
+      }
+    } else if (tid == 0) {
+      atomicExch(P.error, (int)RDKV_ERR_CAPACITY);
+    }
+    if (tid == 0 && atomicAdd(P.gticket, 1) == P.n_heads - 1) {
+      *P.gticket = 0;
+      if (len_c < P.cap_c) *P.len_dev = len_c + 1;
+    }
+  }
   // Merge: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per query head.  The splits'
   // partials (contiguous) are copied into shared memory (the ring area is free) by 16-byte
   // asynchronous copies, all in flight at once, in chunks that fit; each split's weight
@@ -1079,14 +1127,16 @@ static DecodeGeom decode_geom(const rdkv_cache* c) {
   return g;
 }
 
+// ws: partials, then per-head tickets, the status word and the fused step's head counter
 static size_t decode_ws_bytes(const DecodeGeom& g, int n_heads) {
-  return g.ticket_off + (size_t)align_up(((int64_t)n_heads + 1) * 4, 256);
+  return g.ticket_off + (size_t)align_up(((int64_t)n_heads + 2) * 4, 256);
 }
 
 rdkv_status check_cache_public(const rdkv_cache* c);
 
 // Kernel arguments of one decode call; ws holds the partials, then the tickets and the status word.
-static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo, const void* q, float* out, void* ws) {
+static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo, const void* q, float* out, void* ws,
+                                  const void* k_new = nullptr, const void* v_new = nullptr) {
   const rdkv_shape& s = cache->shape;
   const int n_heads = s.batch * s.h_kv;
   const PlanLayout L = plan_layout(s.batch, s.h_kv, s.head_dim);
@@ -1100,8 +1150,11 @@ static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo
   P.partial = static_cast<float*>(ws);
   P.tickets = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + geo.ticket_off);
   P.error = P.tickets + n_heads;
+  P.gticket = P.tickets + n_heads + 1;
   P.out = out;
   P.len_dev = cache->len_dev;
+  P.k_new = k_new;
+  P.v_new = v_new;
   P.heads = reinterpret_cast<const rdkv_head_plan*>(static_cast<const char*>(cache->plan) + L.heads_off);
   P.slots = reinterpret_cast<const int16_t*>(static_cast<const char*>(cache->plan) + L.slots_off);
   P.slot_stride = L.slot_stride;
@@ -1115,29 +1168,38 @@ static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo
   return P;
 }
 
-static rdkv_status launch_decode(const DecodeParams& P, const DecodeGeom& geo, const rdkv_shape& s, cudaStream_t cs) {
+// pdl: programmatic dependent launch; the kernel's static setup (plan, zone A) may then overlap
+// the tail of the kernel launched before it on the stream, and it waits for that kernel before
+// it reads the query, the new token or zone C.
+static rdkv_status launch_decode(const DecodeParams& P, const DecodeGeom& geo, const rdkv_shape& s, cudaStream_t cs,
+                                 bool pdl) {
   // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is captured)
   static size_t smem_set[4][64] = {};
   int dev = 0;
   RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
   const bool qlo = s.dtype == RDKV_F32;
   const int ki = (s.head_dim == 128 ? 2 : 0) + (qlo ? 1 : 0);
-  const void* fn = ki == 3 ? (const void*)decode_kernel<128, true>
-                 : ki == 2 ? (const void*)decode_kernel<128, false>
-                 : ki == 1 ? (const void*)decode_kernel<64, true>
-                           : (const void*)decode_kernel<64, false>;
+  void (*const fn)(DecodeParams) = ki == 3 ? decode_kernel<128, true>
+                                 : ki == 2 ? decode_kernel<128, false>
+                                 : ki == 1 ? decode_kernel<64, true>
+                                           : decode_kernel<64, false>;
   if (dev < 64 && geo.smem > smem_set[ki][dev]) {
-    RDKV_TRY_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecodeSmemLimit),
+    RDKV_TRY_CUDA(cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kDecodeSmemLimit),
                   "decode smem");
     smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
   }
-  const dim3 grid(geo.splits);
-  switch (ki) {
-    case 3: decode_kernel<128, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    case 2: decode_kernel<128, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    case 1: decode_kernel<64, true><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-    default: decode_kernel<64, false><<<grid, kDecWarps * 32, geo.smem, cs>>>(P); break;
-  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(geo.splits);
+  cfg.blockDim = dim3(kDecWarps * 32);
+  cfg.dynamicSmemBytes = geo.smem;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  RDKV_TRY_CUDA(cudaLaunchKernelEx(&cfg, fn, P), "decode launch");
   RDKV_CHECK_LAUNCH("decode");
   return RDKV_OK;
 }
@@ -1164,7 +1226,25 @@ extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, 
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
   // the tickets are zero here: the workspace starts zero-filled and every call leaves them at zero
-  return launch_decode(decode_params(cache, geo, q, out, ws), geo, s, (cudaStream_t)stream);
+  return launch_decode(decode_params(cache, geo, q, out, ws), geo, s, (cudaStream_t)stream, true);
+}
+
+extern "C" rdkv_status rdkv_decode_step(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new,
+                                        float* out, void* ws, size_t ws_bytes, void* stream) {
+  rdkv_status st = check_cache_public(cache);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(q && out && k_new && v_new, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  RDKV_REQUIRE(cache->len_c < cache->cap_c, RDKV_ERR_CAPACITY, "zone C is full (%d rows)", cache->cap_c);
+  const rdkv_shape& s = cache->shape;
+  const int n_heads = s.batch * s.h_kv;
+  const DecodeGeom geo = decode_geom(cache);
+  const size_t need = decode_ws_bytes(geo, n_heads);
+  RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
+  RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
+               (long long)geo.max_item);
+  st = launch_decode(decode_params(cache, geo, q, out, ws, k_new, v_new), geo, s, (cudaStream_t)stream, true);
+  if (st == RDKV_OK) cache->len_c += 1;
+  return st;
 }
 
 extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream) {
@@ -1179,7 +1259,9 @@ extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* w
                 "status read");
   RDKV_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status sync");
   if (v != RDKV_OK) {
-    set_error("decode reported status %d (a bounded wait ran out)", v);
+    if (v == RDKV_ERR_TIMEOUT) set_error("decode: a bounded wait for a tile copy ran out");
+    else if (v == RDKV_ERR_CAPACITY) set_error("decode step: zone C was full, the new token was not stored");
+    else set_error("decode reported status %d", v);
     RDKV_TRY_CUDA(cudaMemsetAsync(static_cast<char*>(const_cast<void*>(ws)) + geo.ticket_off + 4 * (size_t)n_heads, 0, 4,
                                   (cudaStream_t)stream),
                   "status clear");
@@ -1231,6 +1313,6 @@ extern "C" rdkv_status rdkv_decode_attn_noalloc(const rdkv_cache* cache, const v
   if (st != RDKV_OK) return st;
   const DecodeParams P = decode_params(cache, geo, q, out, ws);
   // the previous call's tickets and status word are still in the scratch: clear them
-  RDKV_TRY_CUDA(cudaMemsetAsync(P.tickets, 0, ((size_t)n_heads + 1) * 4, (cudaStream_t)stream), "decode ticket reset");
-  return launch_decode(P, geo, s, (cudaStream_t)stream);
+  RDKV_TRY_CUDA(cudaMemsetAsync(P.tickets, 0, ((size_t)n_heads + 2) * 4, (cudaStream_t)stream), "decode ticket reset");
+  return launch_decode(P, geo, s, (cudaStream_t)stream, false);
 }

@@ -24,7 +24,8 @@ EXPORTED = (
     "rdkv_waterfill_workspace_bytes", "rdkv_waterfill",
     "rdkv_plan_bytes", "rdkv_allocate_workspace_bytes", "rdkv_allocate", "rdkv_plan_sizes",
     "rdkv_pack", "rdkv_append",
-    "rdkv_decode_workspace_bytes", "rdkv_decode_attn", "rdkv_decode_status", "rdkv_decode_attn_noalloc",
+    "rdkv_decode_workspace_bytes", "rdkv_decode_attn", "rdkv_decode_step", "rdkv_decode_status",
+    "rdkv_decode_attn_noalloc",
 )
 
 
@@ -91,6 +92,7 @@ def lib():
             "rdkv_append": (ctypes.c_int, [cp, _P, _P, _P]),
             "rdkv_decode_workspace_bytes": (ctypes.c_size_t, [cp]),
             "rdkv_decode_attn": (ctypes.c_int, [cp, _P, _P, _P, ctypes.c_size_t, _P]),
+            "rdkv_decode_step": (ctypes.c_int, [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_status": (ctypes.c_int, [cp, _P, _P]),
             "rdkv_decode_attn_noalloc": (ctypes.c_int, [cp, _P, _P, _P]),
         }
@@ -248,6 +250,16 @@ def rdkv_decode_attn(cache, q, out=None, stream=None):
     ws = cache.decode_workspace()
     _check(lib().rdkv_decode_attn(ctypes.byref(cache.c), _ptr(q), _ptr(out), _ptr(ws), ws.numel(),
                                   _stream(stream)))
+    return out
+
+
+def rdkv_decode_step(cache, q, k_new, v_new, out=None, stream=None):
+    """One decode step in one launch: append (k_new, v_new) to zone C and attend with q over the cache."""
+    B, Hq, D = q.shape
+    out = out if out is not None else torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    ws = cache.decode_workspace()
+    _check(lib().rdkv_decode_step(ctypes.byref(cache.c), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), _ptr(ws),
+                                  ws.numel(), _stream(stream)))
     return out
 
 

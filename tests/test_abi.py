@@ -93,6 +93,18 @@ def test_append_capacity_is_checked_on_the_host(L):
     assert c.len_c == 8
 
 
+def test_decode_step_capacity_is_checked_on_the_host(L):
+    s = rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16")
+    sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 0, 1)
+    fake = ctypes.c_void_p(256)
+    c = rdkv.CacheStruct(s, 256, None, None, 256, 256, None, 256, 8, 8, sizes)
+    r = L.rdkv_decode_step(ctypes.byref(c), fake, fake, fake, fake, fake, 1 << 20, None)
+    assert r == rdkv.RDKV_ERR_CAPACITY
+    assert c.len_c == 8
+    r = L.rdkv_decode_step(ctypes.byref(c), fake, None, fake, fake, fake, 1 << 20, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+
+
 def test_binding_cache_object_on_host_memory(L):
     """The Python Cache wrapper builds its C struct and sizes its decode workspace without a GPU."""
     import torch

@@ -197,3 +197,101 @@ def test_append_capacity():
     with pytest.raises(rdkv.RDKVError) as e:
         rdkv.rdkv_append(cache, kn.to(DEV), vn.to(DEV))
     assert e.value.code == rdkv.RDKV_ERR_CAPACITY
+
+
+# ---------------------------------------------------------------- fused decode step
+@pytest.mark.parametrize("case", list(CASES))
+@pytest.mark.parametrize("budget", ["page", "full"])
+def test_decode_step_matches_oracle(case, budget):
+    """append + attend in one launch: the output against the oracle, the stored rows bit-exact."""
+    w = CASES[case]
+    avg = {"page": w.budgets[0], "full": 16.0}[budget]
+    steps = 20  # crosses a 16-row zone-C block boundary for every window size
+    (q, k, v), _, shape, sc, al, sizes, cache = _compress(w, avg, avg, cap_extra=steps)
+    ref = O.pack(k.numpy(), v.numpy(), al["bits_tok"].cpu().numpy(), al["bits_chan"].cpu().numpy(), w.window,
+                 cap_c=w.window + steps)
+    un = O.unpack(ref, w.head_dim)
+    for step in range(steps):
+        qn, kn, vn = synth.decode_step(w, step)
+        out = rdkv.rdkv_decode_step(cache, qn.to(DEV), kn.to(DEV), vn.to(DEV)).cpu().numpy()
+        O.append(ref, kn.numpy(), vn.numpy())
+        exp = O.decode(ref, qn.numpy(), unpacked=un)
+        err = np.abs(out - exp).max()
+        assert err <= 2e-3, (case, budget, step, err)
+    assert rdkv.rdkv_decode_status(cache) == 0
+    assert cache.len_c == w.window + steps and int(cache.len_dev.item()) == w.window + steps
+    n = w.window + steps
+    assert np.array_equal(cache.zone_c_k.cpu().numpy()[:, :, :n].view(np.uint16), ref["zone_c_k"][:, :, :n].view(np.uint16))
+    assert np.array_equal(cache.zone_c_v.cpu().numpy()[:, :, :n].view(np.uint16), ref["zone_c_v"][:, :, :n].view(np.uint16))
+
+
+def test_decode_step_agrees_with_append_then_attend():
+    w = CASES["small_f16"]
+    steps = 6
+    (q, k, v), (qd, kd, vd), shape, sc, al, sizes, c1 = _compress(w, w.budgets[0], w.budgets[0], cap_extra=steps)
+    c2 = rdkv.rdkv_pack(shape, al["plan"], kd, vd, al["bits_tok"], al["bits_chan"], w.window + steps, sizes=sizes)
+    for step in range(steps):
+        qn, kn, vn = (t.to(DEV) for t in synth.decode_step(w, step))
+        a = rdkv.rdkv_decode_step(c1, qn, kn, vn)
+        rdkv.rdkv_append(c2, kn, vn)
+        b = rdkv.rdkv_decode_attn(c2, qn)
+        # the same values in the same blocks; only the order of the warps' fp32 sums may differ
+        torch.testing.assert_close(a, b, atol=2e-5, rtol=0)
+
+
+def test_decode_step_in_a_replayed_graph():
+    """A captured step replayed: every replay appends one row and attends over all of them."""
+    w = CASES["small_f16"]
+    steps = 5
+    (q, k, v), _, shape, sc, al, sizes, cache = _compress(w, w.budgets[0], w.budgets[0], cap_extra=steps + 1)
+    ref = O.pack(k.numpy(), v.numpy(), al["bits_tok"].cpu().numpy(), al["bits_chan"].cpu().numpy(), w.window,
+                 cap_c=w.window + steps + 1)
+    un = O.unpack(ref, w.head_dim)
+    q0, k0, v0 = (t.to(DEV) for t in synth.decode_step(w, 0))
+    qb, kb, vb = q0.clone(), k0.clone(), v0.clone()
+    out = torch.empty(w.batch, w.h_q, w.head_dim, dtype=torch.float32, device=DEV)
+    cache.decode_workspace()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        saved = int(cache.len_dev.item())
+        with torch.cuda.graph(g, stream=s):
+            rdkv.rdkv_decode_step(cache, qb, kb, vb, out=out, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert int(cache.len_dev.item()) == saved  # capture launches nothing
+    for step in range(steps):
+        qn, kn, vn = synth.decode_step(w, step)
+        qb.copy_(qn.to(DEV)); kb.copy_(kn.to(DEV)); vb.copy_(vn.to(DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        O.append(ref, kn.numpy(), vn.numpy())
+        exp = O.decode(ref, qn.numpy(), unpacked=un)
+        assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3, step
+    assert int(cache.len_dev.item()) == w.window + steps
+    assert rdkv.rdkv_decode_status(cache) == 0
+
+
+def test_decode_step_past_capacity_on_the_device():
+    """A step that finds zone C full attends with its token, stores nothing and reports it."""
+    w = CASES["tiny_f32"]
+    (q, k, v), _, shape, sc, al, sizes, cache = _compress(w, 3.0, 3.0, cap_extra=1)
+    ref = O.pack(k.numpy(), v.numpy(), al["bits_tok"].cpu().numpy(), al["bits_chan"].cpu().numpy(), w.window,
+                 cap_c=w.window + 2)
+    un = O.unpack(ref, w.head_dim)
+    qn, kn, vn = synth.decode_step(w, 0)
+    rdkv.rdkv_decode_step(cache, qn.to(DEV), kn.to(DEV), vn.to(DEV))
+    O.append(ref, kn.numpy(), vn.numpy())
+    assert int(cache.len_dev.item()) == cache.c.cap_c
+    before = cache.zone_c_k.clone()
+    cache.c.len_c -= 1  # make the host mirror lag, as a replayed graph would
+    qn, kn, vn = synth.decode_step(w, 1)
+    out = rdkv.rdkv_decode_step(cache, qn.to(DEV), kn.to(DEV), vn.to(DEV)).cpu().numpy()
+    O.append(ref, kn.numpy(), vn.numpy())  # the oracle's zone C has room for it: same attention
+    exp = O.decode(ref, qn.numpy(), unpacked=un)
+    assert np.abs(out - exp).max() <= 2e-3
+    assert int(cache.len_dev.item()) == cache.c.cap_c
+    assert torch.equal(cache.zone_c_k, before)
+    assert rdkv.rdkv_decode_status(cache) == rdkv.RDKV_ERR_CAPACITY
+    assert rdkv.rdkv_decode_status(cache) == 0  # read and cleared

@@ -186,7 +186,11 @@ struct WarpAcc {
   float l[2];           // this lane's share of the running sum
 };
 
-// Softmax update for NTB token blocks of S^T accumulators; returns P^T B-fragments.
+// Softmax update for NTB token blocks of S^T accumulators; returns P^T B-fragments.  The
+// reference max m of a head is raised only when a tile's max exceeds it by more than kLazy
+// (base 2), and then for every head of the warp at once (a warp-uniform branch), so most tiles
+// skip the rescale of the accumulators; p = 2^(s - m) <= 2^kLazy stays well inside fp16.
+constexpr float kLazy = 8.f;
 template <int D, int NTB>
 __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][4], uint32_t (&pb)[NTB][2]) {
   float mt0 = -INFINITY, mt1 = -INFINITY;
@@ -195,17 +199,34 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
     mt0 = fmaxf(mt0, fmaxf(s[tb][0], s[tb][2]));
     mt1 = fmaxf(mt1, fmaxf(s[tb][1], s[tb][3]));
   }
+  // a rescale is due when some head's tile max passes its reference by kLazy (a -inf reference:
+  // no token seen yet, passes as soon as a finite logit comes)
+  const bool due = mt0 > acc.m[0] + kLazy || mt1 > acc.m[1] + kLazy;
+  if (__any_sync(0xffffffffu, due)) {
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
-    mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
+    for (int o = 4; o < 32; o <<= 1) {
+      mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, o));
+      mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
+    }
+    const float mn0 = fmaxf(acc.m[0], mt0), mn1 = fmaxf(acc.m[1], mt1);
+    const float al0 = acc.m[0] == -INFINITY ? 0.f : exp2f(acc.m[0] - mn0);
+    const float al1 = acc.m[1] == -INFINITY ? 0.f : exp2f(acc.m[1] - mn1);
+    acc.m[0] = mn0;
+    acc.m[1] = mn1;
+    acc.l[0] *= al0;
+    acc.l[1] *= al1;
+    acc.z[0] *= al0;
+    acc.z[1] *= al1;
+#pragma unroll
+    for (int cm = 0; cm < D / 16; ++cm) {
+      acc.o[cm][0] *= al0;
+      acc.o[cm][1] *= al1;
+      acc.o[cm][2] *= al0;
+      acc.o[cm][3] *= al1;
+    }
   }
-  const float mn0 = fmaxf(acc.m[0], mt0), mn1 = fmaxf(acc.m[1], mt1);
   // all tokens so far masked: keep everything at zero
-  const float ref0 = mn0 == -INFINITY ? 0.f : mn0, ref1 = mn1 == -INFINITY ? 0.f : mn1;
-  const float al0 = exp2f(acc.m[0] - ref0), al1 = exp2f(acc.m[1] - ref1);
-  acc.m[0] = mn0;
-  acc.m[1] = mn1;
+  const float ref0 = acc.m[0] == -INFINITY ? 0.f : acc.m[0], ref1 = acc.m[1] == -INFINITY ? 0.f : acc.m[1];
   float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
   for (int tb = 0; tb < NTB; ++tb) {
@@ -216,17 +237,8 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
     pb[tb][0] = movmatrix_trans(pack_half2(p0, p1));
     pb[tb][1] = movmatrix_trans(pack_half2(p2, p3));
   }
-  acc.l[0] = acc.l[0] * al0 + ps0;
-  acc.l[1] = acc.l[1] * al1 + ps1;
-  acc.z[0] *= al0;
-  acc.z[1] *= al1;
-#pragma unroll
-  for (int cm = 0; cm < D / 16; ++cm) {
-    acc.o[cm][0] *= al0;
-    acc.o[cm][1] *= al1;
-    acc.o[cm][2] *= al0;
-    acc.o[cm][3] *= al1;
-  }
+  acc.l[0] += ps0;
+  acc.l[1] += ps1;
 }
 
 // K logits of one width segment of a zone-A tile, k-blocks [kb0, kb1).
@@ -839,12 +851,18 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       float s[2][4];
       tile_logits<D, QLO>(stp, kmeta, RW, seg_kb, kbd, qv, koff, lane, s);
 #pragma unroll
-      for (int tb = 0; tb < 2; ++tb) {
-        const bool va = 16 * tb + g < n_real, vb = 16 * tb + g + 8 < n_real;
-        s[tb][0] = va ? s[tb][0] * sl2 : -INFINITY;
-        s[tb][1] = va ? s[tb][1] * sl2 : -INFINITY;
-        s[tb][2] = vb ? s[tb][2] * sl2 : -INFINITY;
-        s[tb][3] = vb ? s[tb][3] * sl2 : -INFINITY;
+      for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[tb][e] *= sl2;
+      if (n_real < kTile) {  // the last tile of a class: tokens past the kept ones
+#pragma unroll
+        for (int tb = 0; tb < 2; ++tb) {
+          const bool va = 16 * tb + g < n_real, vb = 16 * tb + g + 8 < n_real;
+          s[tb][0] = va ? s[tb][0] : -INFINITY;
+          s[tb][1] = va ? s[tb][1] : -INFINITY;
+          s[tb][2] = vb ? s[tb][2] : -INFINITY;
+          s[tb][3] = vb ? s[tb][3] : -INFINITY;
+        }
       }
       uint32_t pb[2][2];
       softmax_update<D, 2>(acc, s, pb);

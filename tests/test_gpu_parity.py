@@ -235,8 +235,10 @@ def test_decode_step_agrees_with_append_then_attend():
         a = rdkv.rdkv_decode_step(c1, qn, kn, vn)
         rdkv.rdkv_append(c2, kn, vn)
         b = rdkv.rdkv_decode_attn(c2, qn)
-        # the same values in the same blocks; only the order of the warps' fp32 sums may differ
-        torch.testing.assert_close(a, b, atol=2e-5, rtol=0)
+        # the same values in the same blocks; which warp meets which tile first may differ, and with
+        # it the reference max that p = 2^(s - m) is rounded to fp16 against (p rounds to 2^-11
+        # relative either way; against the oracle both stay within 2e-3)
+        torch.testing.assert_close(a, b, atol=5e-4, rtol=0)
 
 
 def test_decode_step_in_a_replayed_graph():

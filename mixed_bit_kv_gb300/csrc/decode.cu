@@ -142,6 +142,10 @@ __device__ __forceinline__ uint32_t lds32(const unsigned char* base, uint32_t of
 __device__ __forceinline__ uint2 lds64(const unsigned char* base, uint32_t off) {
   return *reinterpret_cast<const uint2*>(base + off);
 }
+__device__ __forceinline__ uint4 lds128(const unsigned char* base, uint32_t off) {
+  return *reinterpret_cast<const uint4*>(base + off);
+}
+__device__ __forceinline__ uint32_t pick4(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 
 // Two codes of a pair (already shifted to bit 0 and bit 16) -> exact fp16 codes
 // -> scale * code + zero, one rounding.
@@ -250,20 +254,19 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
 // channels use the stored fp16 value against q (split the same way when q
 // carries more than fp16 precision).
 template <int W, bool QLO>
-__device__ __forceinline__ void k_segment(const unsigned char* const (&rows)[4], const unsigned char* kmeta, int kb0, int kb1,
+__device__ __forceinline__ void k_segment(const unsigned char* kw, const unsigned char* kmeta, int kb0, int kb1,
                                           const KBDesc* kbd, const float4* qv, int lane, float (&s)[2][4],
                                           float& bias) {
-  const int q = lane & 3;
-  // byte offsets (from the block's first word) and shifts of this lane's two slot pairs
+  const int g = lane >> 2, q = lane & 3;
+  // word offsets (inside the block's first word) and shifts of this lane's two slot pairs
   constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
-  const uint32_t o0 = 4u * (W == 16 ? q : W == 8 ? (q >> 1) : 0);
-  const uint32_t o1 = 4u * (W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0);
+  const int o0 = W == 16 ? q : W == 8 ? (q >> 1) : 0;
+  const int o1 = W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0;
   const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
   const int sh1 = W == 2 ? 2 * q + 8 : sh0;
   for (int kb = kb0; kb < kb1; ++kb) {
     const KBDesc d = kbd[kb];
     const float4 qq = qv[kb * 32 + lane];  // q_g at slots 2q, 2q+1, 2q+8, 2q+9 (0 for pads and missing slots)
-    const uint32_t wb = 4u * (uint32_t)d.word0;
     uint32_t bh0, bh1, bl0 = 0, bl1 = 0;
     if (W == 16) {
       if (QLO) {
@@ -285,28 +288,23 @@ __device__ __forceinline__ void k_segment(const unsigned char* const (&rows)[4],
       const uint4 t = split_hi_lo(qq.x * s0.x, qq.y * s0.y, qq.z * s1.x, qq.w * s1.y);
       bh0 = t.x; bh1 = t.y; bl0 = t.z; bl1 = t.w;
     }
+    // tokens g, g+8, g+16, g+24 of the lane's two words
+    const uint4 x0 = lds128(kw, 4u * (32u * (uint32_t)(d.word0 + o0) + 4u * g));
+    const uint4 x1 = W == 2 ? x0 : lds128(kw, 4u * (32u * (uint32_t)(d.word0 + o1) + 4u * g));
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
-      const unsigned char* r0 = rows[2 * tb] + wb;
-      const unsigned char* r1 = rows[2 * tb + 1] + wb;
       uint32_t a0, a1, a2, a3;
       if (W == 16) {
         // raw fp16 words past the segment end may hold anything: zero them
         const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
-        const uint32_t x0 = lds32(r0, o0), x1 = lds32(r1, o0), x2 = lds32(r0, o1), x3 = lds32(r1, o1);
-        a0 = v0 ? x0 : 0u; a1 = v0 ? x1 : 0u; a2 = v1 ? x2 : 0u; a3 = v1 ? x3 : 0u;
+        a0 = v0 ? pick4(x0, 2 * tb) : 0u; a1 = v0 ? pick4(x0, 2 * tb + 1) : 0u;
+        a2 = v1 ? pick4(x1, 2 * tb) : 0u; a3 = v1 ? pick4(x1, 2 * tb + 1) : 0u;
       } else {
         // codes past the segment end are small integers met by zero query entries
-        const uint32_t x0 = lds32(r0, o0), x1 = lds32(r1, o0);
-        a0 = exact_codes(x0, sh0, mask2);
-        a1 = exact_codes(x1, sh0, mask2);
-        if (W == 2) {
-          a2 = exact_codes(x0, sh1, mask2);
-          a3 = exact_codes(x1, sh1, mask2);
-        } else {
-          a2 = exact_codes(lds32(r0, o1), sh1, mask2);
-          a3 = exact_codes(lds32(r1, o1), sh1, mask2);
-        }
+        a0 = exact_codes(pick4(x0, 2 * tb), sh0, mask2);
+        a1 = exact_codes(pick4(x0, 2 * tb + 1), sh0, mask2);
+        a2 = exact_codes(pick4(x1, 2 * tb), sh1, mask2);
+        a3 = exact_codes(pick4(x1, 2 * tb + 1), sh1, mask2);
       }
       mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
       if (W != 16 || QLO) mma16816(s[tb], a0, a1, a2, a3, bl0, bl1);
@@ -324,7 +322,7 @@ __device__ __forceinline__ void k_segment(const unsigned char* const (&rows)[4],
 // term sum_c q_c zero_c runs as an MMA whose A rows all hold the zeros, so
 // every row of zacc carries it for heads (2q, 2q+1).
 template <int W>
-__device__ __forceinline__ void k_segment_h(const unsigned char* const (&rows)[4], const unsigned char* kmeta, int kb0, int kb1,
+__device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsigned char* kmeta, int kb0, int kb1,
                                             const uint4* koff, const uint2* qh, int lane, float (&sq)[2][4],
                                             float (&sr)[2][4], float (&zacc)[4]) {
   const int q = lane & 3;
@@ -348,17 +346,16 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* const (&rows)[4
       bl1 = *reinterpret_cast<const uint32_t*>(&l1);
       mma16816(zacc, m0.y, m0.y, m1.y, m1.y, qq.x, qq.y);
     }
+    // tokens g, g+8, g+16, g+24 of the lane's two words (one word for 2-bit codes)
+    const uint4 y0 = lds128(kw, off.x);
+    const uint4 y1 = W == 2 ? y0 : lds128(kw, off.y);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
-      const unsigned char* r0 = rows[2 * tb];
-      const unsigned char* r1 = rows[2 * tb + 1];
+      const uint32_t x0 = pick4(y0, 2 * tb), x1 = pick4(y0, 2 * tb + 1);
+      const uint32_t x2 = pick4(y1, 2 * tb), x3 = pick4(y1, 2 * tb + 1);
       if (W == 16) {
-        const uint32_t a0 = lds32(r0, off.x) & off.z, a1 = lds32(r1, off.x) & off.z;
-        const uint32_t a2 = lds32(r0, off.y) & off.w, a3 = lds32(r1, off.y) & off.w;
-        mma16816(sr[tb], a0, a1, a2, a3, bh0, bh1);
+        mma16816(sr[tb], x0 & off.z, x1 & off.z, x2 & off.w, x3 & off.w, bh0, bh1);
       } else {
-        const uint32_t x0 = lds32(r0, off.x), x1 = lds32(r1, off.x);
-        const uint32_t x2 = W == 2 ? x0 : lds32(r0, off.y), x3 = W == 2 ? x1 : lds32(r1, off.y);
         const uint32_t a0 = (x0 >> sh0) & mask2, a1 = (x1 >> sh0) & mask2;
         const uint32_t a2 = (x2 >> sh1) & mask2, a3 = (x3 >> sh1) & mask2;
         mma16816(sq[tb], a0, a1, a2, a3, bh0, bh1);
@@ -369,22 +366,19 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* const (&rows)[4
 }
 
 template <int D, bool QLO>
-__device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsigned char* kmeta, int RW, const int (&seg_kb)[5],
+__device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsigned char* kmeta, const int (&seg_kb)[5],
                                             const KBDesc* kbd, const float4* qv, const uint4* koff, int lane,
                                             float (&s)[2][4]) {
   float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
-  const int g = lane >> 2;
-  const unsigned char* const rows[4] = {kw + 4 * (g * RW), kw + 4 * ((g + 8) * RW), kw + 4 * ((g + 16) * RW),
-                                        kw + 4 * ((g + 24) * RW)};
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) s[tb][0] = s[tb][1] = s[tb][2] = s[tb][3] = 0.f;
   const int q = lane & 3;
   float be, bo;
   if (QLO) {
-    k_segment<16, QLO>(rows, kmeta, seg_kb[0], seg_kb[1], kbd, qv, lane, s, bias);
-    k_segment<8, QLO>(rows, kmeta, seg_kb[1], seg_kb[2], kbd, qv, lane, s, bias);
-    k_segment<4, QLO>(rows, kmeta, seg_kb[2], seg_kb[3], kbd, qv, lane, s, bias);
-    k_segment<2, QLO>(rows, kmeta, seg_kb[3], seg_kb[4], kbd, qv, lane, s, bias);
+    k_segment<16, QLO>(kw, kmeta, seg_kb[0], seg_kb[1], kbd, qv, lane, s, bias);
+    k_segment<8, QLO>(kw, kmeta, seg_kb[1], seg_kb[2], kbd, qv, lane, s, bias);
+    k_segment<4, QLO>(kw, kmeta, seg_kb[2], seg_kb[3], kbd, qv, lane, s, bias);
+    k_segment<2, QLO>(kw, kmeta, seg_kb[3], seg_kb[4], kbd, qv, lane, s, bias);
     // zero-point term: lanes (g, 0..3) hold parts of head g; S^T lane (g', q') needs heads 2q', 2q'+1
     bias += __shfl_xor_sync(0xffffffffu, bias, 1);
     bias += __shfl_xor_sync(0xffffffffu, bias, 2);
@@ -394,10 +388,10 @@ __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsig
     const uint2* qh = reinterpret_cast<const uint2*>(qv);
     float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // zero-point term of heads 2q, 2q+1 (every row)
     float sr[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // raw 16-bit channels, scale 1
-    k_segment_h<16>(rows, kmeta, seg_kb[0], seg_kb[1], koff, qh, lane, s, sr, zacc);
-    k_segment_h<8>(rows, kmeta, seg_kb[1], seg_kb[2], koff, qh, lane, s, sr, zacc);
-    k_segment_h<4>(rows, kmeta, seg_kb[2], seg_kb[3], koff, qh, lane, s, sr, zacc);
-    k_segment_h<2>(rows, kmeta, seg_kb[3], seg_kb[4], koff, qh, lane, s, sr, zacc);
+    k_segment_h<16>(kw, kmeta, seg_kb[0], seg_kb[1], koff, qh, lane, s, sr, zacc);
+    k_segment_h<8>(kw, kmeta, seg_kb[1], seg_kb[2], koff, qh, lane, s, sr, zacc);
+    k_segment_h<4>(kw, kmeta, seg_kb[2], seg_kb[3], koff, qh, lane, s, sr, zacc);
+    k_segment_h<2>(kw, kmeta, seg_kb[3], seg_kb[4], koff, qh, lane, s, sr, zacc);
     // s holds the code products at 2^-24
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb)
@@ -431,13 +425,15 @@ __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned c
   constexpr int per = 16 / VB;      // channels per half-word
   constexpr int NG = D / 32;        // channel groups
   constexpr uint32_t mask2 = VB == 8 ? 0x00ff00ffu : VB == 4 ? 0x000f000fu : 0x00030003u;
+  constexpr int R = VB / 2;         // word groups inside a pair (words w = r mod R together)
   const int sh0 = VB * (g % per), sh1 = VB * ((g + 8) % per);
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
     const int p0 = 8 * tb + q, p1 = p0 + 4;
-    // words of channel c = 16 cm + g (+8): (16 cm)/per + g/per (+8/per)
-    const unsigned char* base0 = vcodes + 4 * (p0 * wpp + g / per);
-    const unsigned char* base1 = vcodes + 4 * (p1 * wpp + g / per);
+    // this lane's channels c = g + 8 i (i = 0 .. D/8-1) live in the words w = 2 i / ... of group
+    // g / per, stored adjacently in order of i: word i of the group holds channel g + 8 i
+    const unsigned char* base0 = vcodes + 4 * (p0 * wpp + (g / per) * (wpp / R));
+    const unsigned char* base1 = vcodes + 4 * (p1 * wpp + (g / per) * (wpp / R));
     uint32_t za0 = 0u, za2 = 0u;
     if (g < NG) {
       za0 = lds32(vmeta, 8 * (p0 * NG + g) + 4);
@@ -450,23 +446,10 @@ __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned c
       const __half2 b0h = __hmul2(*reinterpret_cast<const __half2*>(&pb[tb][0]), *reinterpret_cast<const __half2*>(&s0));
       const __half2 b1h = __hmul2(*reinterpret_cast<const __half2*>(&pb[tb][1]), *reinterpret_cast<const __half2*>(&s1));
       const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&b0h), b1 = *reinterpret_cast<const uint32_t*>(&b1h);
-      uint32_t w0[4], w1[4];  // words of (cm, c0), (cm, c1) for cm = 2 grp, 2 grp + 1
-      if (VB == 2) {
-        // the pair's words 4 grp .. 4 grp + 3 are exactly these (g / per = 0)
-        const uint4 v0 = *reinterpret_cast<const uint4*>(vcodes + 4 * (p0 * wpp) + 16 * grp);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(vcodes + 4 * (p1 * wpp) + 16 * grp);
-        w0[0] = v0.x; w0[1] = v0.y; w0[2] = v0.z; w0[3] = v0.w;
-        w1[0] = v1.x; w1[1] = v1.y; w1[2] = v1.z; w1[3] = v1.w;
-      } else {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int cm = 2 * grp + half;
-          w0[2 * half] = lds32(base0, 4 * ((16 * cm) / per));
-          w0[2 * half + 1] = lds32(base0, 4 * ((16 * cm + 8) / per));
-          w1[2 * half] = lds32(base1, 4 * ((16 * cm) / per));
-          w1[2 * half + 1] = lds32(base1, 4 * ((16 * cm + 8) / per));
-        }
-      }
+      // words i = 4 grp .. 4 grp + 3 of the lane's group: channels of (cm, c0), (cm, c1) for
+      // cm = 2 grp, 2 grp + 1
+      const uint4 v0 = lds128(base0, 16 * grp), v1 = lds128(base1, 16 * grp);
+      const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int cm = 2 * grp + half;
@@ -798,9 +781,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       const int o0 = w == 16 ? qq : w == 8 ? (qq >> 1) : 0;
       const int o1 = w == 16 ? qq + 4 : w == 8 ? (qq >> 1) + 2 : w == 4 ? 1 : 0;
       const bool v0 = 2 * qq < d.nrem, v1 = 2 * qq + 8 < d.nrem;
-      uint4 e;
-      e.x = 4u * (uint32_t)(d.word0 + o0);
-      e.y = 4u * (uint32_t)(d.word0 + o1);
+      uint4 e;  // word-major tile: word w of tokens g, g+8, g+16, g+24 at 4 (32 w + 4 g)
+      e.x = 4u * (32u * (uint32_t)(d.word0 + o0) + 4u * (uint32_t)g);
+      e.y = 4u * (32u * (uint32_t)(d.word0 + o1) + 4u * (uint32_t)g);
       if (w == 16) {
         e.z = v0 ? ~0u : 0u;
         e.w = v1 ? ~0u : 0u;
@@ -849,7 +832,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       const unsigned char* stp = wring + wpos[slot];
       const unsigned char* kmeta = stp + 4 * kTile * RW;
       float s[2][4];
-      tile_logits<D, QLO>(stp, kmeta, RW, seg_kb, kbd, qv, koff, lane, s);
+      tile_logits<D, QLO>(stp, kmeta, seg_kb, kbd, qv, koff, lane, s);
 #pragma unroll
       for (int tb = 0; tb < 2; ++tb)
 #pragma unroll

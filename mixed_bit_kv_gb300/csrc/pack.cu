@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(128) pack_tile_kernel(const T* __restrict__ k,
     }
   }
   __syncthreads();
-  // K words
+  // K words: word w of token r at 32 w + 4 (r mod 8) + r / 8 (word-major; tokens r, r+8, r+16, r+24
+  // of one word index side by side, so one 16-byte load gives a decode lane its four token rows)
   uint32_t* kw = reinterpret_cast<uint32_t*>(tile);
   for (int i = tid; i < kTile * RW; i += blockDim.x) {
     const int r = i / RW, w = i % RW;
@@ -238,12 +239,14 @@ __global__ void __launch_bounds__(128) pack_tile_kernel(const T* __restrict__ k,
     const int s0 = sbase + (w - wbase) * per;
     uint32_t word = 0;
     for (int e = 0; e < per; ++e) word |= (uint32_t)kc[r * KS + s0 + e] << bit_off(e, kb);
-    kw[i] = word;
+    kw[32 * w + 4 * (r % 8) + r / 8] = word;
   }
-  // V words: pair p, word w holds channels [w*16/b, (w+1)*16/b) of tokens 2p (low half) and 2p+1 (high half)
+  // V words: pair p, word w holds channels [w*16/b, (w+1)*16/b) of tokens 2p (low half) and 2p+1 (high
+  // half); inside a pair, word w sits at (w mod R) wpp/R + w/R with R = b/2, so the words a decode lane
+  // needs (channels congruent to its own mod 8) are adjacent
   if (vbits < 16) {
     uint32_t* vw = reinterpret_cast<uint32_t*>(vcode);
-    const int wpp = D * vbits / 16, per = 16 / vbits;
+    const int wpp = D * vbits / 16, per = 16 / vbits, R = vbits / 2;
     for (int i = tid; i < (kTile / 2) * wpp; i += blockDim.x) {
       const int p = i / wpp, w = i % wpp;
       uint32_t word = 0;
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(128) pack_tile_kernel(const T* __restrict__ k,
         word |= (uint32_t)vc[(2 * p) * D + c] << (vbits * e);
         word |= (uint32_t)vc[(2 * p + 1) * D + c] << (16 + vbits * e);
       }
-      vw[i] = word;
+      vw[p * wpp + (w % R) * (wpp / R) + w / R] = word;
     }
   }
 }

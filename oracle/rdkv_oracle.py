@@ -311,6 +311,36 @@ def bit_offset(e, b):
     return 16 * (e % 2) + b * (e // 2)
 
 
+def k_word_position(t, w):
+    """Index, inside a tile's K words, of word w of token t (0 <= t < 32): the
+    words are stored word-major, and inside one word index the tokens sit in
+    the order t = 0, 8, 16, 24, 1, 9, 17, 25, ... (position 4 * (t mod 8) + t div 8),
+    so tokens t, t+8, t+16, t+24 of one word index are adjacent.  (Project
+    layout; the page fixes no byte order.)"""
+    return 32 * w + 4 * (t % 8) + t // 8
+
+
+def v_word_position(w, b, head_dim):
+    """Index, among the D*b/16 V words of one token pair, of the word that holds
+    channels [w*16/b, (w+1)*16/b): with R = b/2 the words are grouped by w mod R
+    (group r first holds words r, r+R, r+2R, ...), so the words whose channels
+    are congruent mod 8 to one value are adjacent.  R = 1 (b = 2) keeps the
+    natural order.  (Project layout.)"""
+    wpp = head_dim * b // 16
+    R = b // 2
+    return (w % R) * (wpp // R) + w // R
+
+
+def _k_positions(row_words):
+    t = np.arange(TILE)[:, None]
+    w = np.arange(row_words)[None, :]
+    return k_word_position(t, w)                   # [32, row_words]
+
+
+def _v_positions(b, head_dim):
+    return np.array([v_word_position(w, b, head_dim) for w in range(head_dim * b // 16)], dtype=np.int64)
+
+
 def _halves_bits(a):
     return np.asarray(a, dtype=np.float16).view(np.uint16).astype(np.uint32)
 
@@ -341,12 +371,14 @@ def pack_head(k_j, v_j, hp, head_dim):
 
     k_j, v_j: [N, D] float32 values of that head.  Tile layout (little-endian):
       K codes   32 rows x row_words uint32 (segments 16, 8, 4, 2 bits, each
-                padded to whole words; a 16-bit slot holds the raw fp16 value)
+                padded to whole words; a 16-bit slot holds the raw fp16 value),
+                word (t, w) stored at k_word_position(t, w)
       K meta    per slot pair of the 8/4/2-bit segments: scale(2i), scale(2i+1),
                 zero(2i), zero(2i+1) as fp16
       V codes   (width b < 16 only) 16 token pairs x D*b/16 uint32; word w of
                 pair p holds channels [w*16/b, (w+1)*16/b): token 2p in the low
-                half, token 2p+1 in the high half, LSB-first
+                half, token 2p+1 in the high half, LSB-first; stored pair by pair,
+                word w of a pair at v_word_position(w, b, D)
       V meta    (b < 16 only) per token pair and 32-channel group: scale(2p),
                 scale(2p+1), zero(2p), zero(2p+1) as fp16
     Pad tokens and pad slots hold code 0, scale 0 and zero 0.
@@ -379,7 +411,9 @@ def pack_head(k_j, v_j, hp, head_dim):
                     ksc[mbase + sidx], kze[mbase + sidx] = sc, ze
                 kw[real, wbase:wbase + nw] = _pack_words(codes, b, per_word, lambda e: bit_offset(e % per_word, b))
             kmeta = np.stack([ksc[0::2], ksc[1::2], kze[0::2], kze[1::2]], axis=1)
-            parts = [kw.astype(np.uint32).tobytes(), kmeta.astype(np.float16).tobytes()]
+            kflat = np.zeros(TILE * RW, dtype=np.uint32)
+            kflat[_k_positions(RW)] = kw.astype(np.uint32)
+            parts = [kflat.tobytes(), kmeta.astype(np.float16).tobytes()]
             if bv < 16:
                 vals = np.zeros((TILE, D), dtype=np.float32)
                 vals[real] = v_j[rows]
@@ -389,8 +423,10 @@ def pack_head(k_j, v_j, hp, head_dim):
                 per_word = 16 // bv                                    # channels per word
                 words = _pack_words(codes, bv, per_word, lambda c: bv * (c % per_word))
                 vw = words[0::2] + (words[1::2] << np.uint64(16))      # even token low, odd token high
+                vstore = np.zeros(vw.shape, dtype=np.uint32)
+                vstore[:, _v_positions(bv, D)] = vw.astype(np.uint32)
                 vmeta = np.stack([sc[0::2], sc[1::2], ze[0::2], ze[1::2]], axis=2)   # [16, D/32, 4]
-                parts += [vw.astype(np.uint32).tobytes(), vmeta.astype(np.float16).tobytes()]
+                parts += [vstore.tobytes(), vmeta.astype(np.float16).tobytes()]
             else:
                 rows16 = np.zeros((TILE, D), dtype=np.float16)
                 rows16[real] = v_j[rows].astype(np.float16)
@@ -462,7 +498,7 @@ def unpack_head(zone_a, zone_b, hp, head_dim):
         for ti in range(hp["tiles"][ci]):
             tt = hp["tokens"][ci][ti * TILE:(ti + 1) * TILE]
             real = tt >= 0
-            kw = np.frombuffer(zone_a, np.uint32, TILE * RW, off).reshape(TILE, RW)
+            kw = np.frombuffer(zone_a, np.uint32, TILE * RW, off)[_k_positions(RW)]   # [32, RW]
             p = off + 4 * TILE * RW
             km = np.frombuffer(zone_a, np.float16, 2 * QS, p).reshape(QS // 2, 4).astype(np.float64)
             ksc, kze = np.empty(QS), np.empty(QS)
@@ -481,6 +517,7 @@ def unpack_head(zone_a, zone_b, hp, head_dim):
                 per_word = 16 // bv
                 vw = np.frombuffer(zone_a, np.uint32, (TILE // 2) * (D // per_word), p).reshape(TILE // 2, D // per_word)
                 p += 4 * vw.size
+                vw = vw[:, _v_positions(bv, D)]
                 vm = np.frombuffer(zone_a, np.float16, (TILE // 2) * (D // GROUP) * 4, p)
                 vm = vm.reshape(TILE // 2, D // GROUP, 4).astype(np.float64)
                 p += 2 * vm.size

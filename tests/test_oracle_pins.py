@@ -238,6 +238,52 @@ def test_word_layout_golden():
         assert word == c["word"], c
 
 
+def test_tile_layout_golden():
+    g = json.load(open(os.path.join(GOLDEN, "tile_layout.json")))
+    for c in g["k_positions"]:
+        assert O.k_word_position(c["t"], c["w"]) == c["pos"], c
+    for c in g["v_positions"]:
+        assert O.v_word_position(c["w"], c["b"], c["D"]) == c["pos"], c
+    # both rules are permutations of the words they place
+    for rw in (1, 3, 11):
+        pos = sorted(O.k_word_position(t, w) for t in range(32) for w in range(rw))
+        assert pos == list(range(32 * rw))
+    for b in (2, 4, 8):
+        for D in (64, 128):
+            assert sorted(O.v_word_position(w, b, D) for w in range(D * b // 16)) == list(range(D * b // 16))
+
+
+def test_packed_words_sit_where_the_layout_puts_them():
+    """A word of the packed tile, rebuilt from the quantiser's codes, is found at its layout position."""
+    w, q, k, v, al, cache = _tiny_cache(3.0, 3.0)
+    hp = cache["plan"]["heads"][0]
+    za = cache["zone_a"].view(np.uint32)
+    # first tile of the first non-empty 2/4/8-bit class: its first quantised K segment, word 0 of token 9
+    ci = next(i for i in range(3) if hp["tiles"][i] > 0)
+    off_words = hp["a_off"] // 4 + sum(hp["tiles"][i] * hp["tile_bytes"][i] for i in range(ci)) // 4
+    tt = hp["tokens"][ci][:32]
+    # K segments in row order: widths 16, 8, 4, 2, each k_words[i] words of 32 / width slots
+    wbase = sbase = 0
+    for b, nw in zip((16, 8, 4, 2), hp["k_words"]):
+        if b < 16 and nw > 0:
+            break
+        wbase += nw
+        sbase += nw * (32 // b)
+    per = 32 // b
+    slots = hp["slots"][sbase:sbase + per]
+    t = 9 if tt[9] >= 0 else 0
+    rows = tt[tt >= 0]
+    word = 0
+    for e in range(per):
+        ch = slots[e]
+        if ch < 0:
+            continue
+        codes, _, _ = O.quantize_groups(k[rows, 0, ch].astype(np.float32)[None], b)
+        code = int(codes[0][np.nonzero(rows == tt[t])[0][0]])
+        word |= code << O.bit_offset(e, b)
+    assert int(za[off_words + O.k_word_position(t, wbase)]) == word
+
+
 def _tiny_cache(avg_v, avg_k, cap_extra=4, seed_w="tiny"):
     w = synth.WORKLOADS[seed_w]
     q, k, v = (t.numpy() for t in synth.prefill(w))

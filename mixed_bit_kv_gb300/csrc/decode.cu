@@ -5,14 +5,15 @@
 // tokens) and C (fp16 K and V rows of the window and of decoded tokens) in one
 // pass.
 //
-// Work: grid = (splits, sequence x KV head).  A head's work items are its
-// zone-A tiles (32 tokens, in class order) followed by zone-C blocks of 16
-// rows; split s takes a contiguous range of items and its 8 warps take the
-// items round-robin.  Every warp streams its items through its own small ring
-// of shared memory, filled by bulk asynchronous copies that complete on
-// per-slot mbarriers (all waits are bounded and report RDKV_ERR_TIMEOUT), so
-// two blocks (16 warps) fit on an SM.  The last block of a head to finish
-// (an atomic ticket) merges the splits' partial softmax states into the output.
+// Work: one block of 16 warps per SM, dealt to the (sequence, KV head) pairs
+// in proportion to their estimated cost.  A head's work items are its zone-A
+// tiles (32 tokens, in class order) followed by zone-C blocks of 16 rows;
+// split s of n takes items s, s + n, s + 2n, ... and its warps take them in
+// order of need.  Every warp streams its items through its own ring of shared
+// memory, filled by bulk asynchronous copies that complete on per-slot
+// mbarriers (all waits are bounded and report RDKV_ERR_TIMEOUT).  The last
+// block of a head to finish (an atomic ticket) merges the splits' partial
+// softmax states into the output.
 //
 // Products: mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens on M:
 //   S^T[16 tok x 8 heads]  += K^[16 tok x 16 slots] * Q^T[16 slots x 8 heads]
@@ -29,7 +30,7 @@
 
 namespace rdkv {
 
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 16;  // one block per SM
 constexpr int kMaxInflight = 4;
 constexpr int kCRows = 16;        // zone-C rows per work item
 constexpr int kMaxKB = 16;        // k-blocks of a K row (D = 128: at most 13)
@@ -74,7 +75,7 @@ struct DecodeParams {
   int32_t* gticket;        // fused step: heads merged so far (zero between launches)
   const rdkv_head_plan* heads;  // the plan's head records (offset fixed by the shape)
   const int16_t* slots;         // the plan's slot tables, slot_stride entries per head
-  int dtype, h_q, h_kv, cap_c, ring_bytes, ctas, n_heads, slot_stride;
+  int dtype, h_q, h_kv, cap_c, ring_bytes, ring_warps, ctas, n_heads, slot_stride;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -511,7 +512,7 @@ struct ClassVals {
 };
 
 template <int D, bool QLO>
-__global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams P) {
+__global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.h_q / P.h_kv;
@@ -662,7 +663,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   int* witem = ring_item + warp * kMaxInflight;
   uint32_t* vend = ring_vend + warp * kMaxInflight;  // ring end after each slot's copy (lane 0)
   int issued = 0, done = 0;
-  bool drained = false;                // lane 0: no item left for this block
+  bool drained = warp >= P.ring_warps;  // lane 0: no item left for this warp (warps without a ring take none)
   int pending = -1;                    // lane 0: item taken but not yet issued (ring full)
   auto issue = [&]() {
     if (issued == done) head_v = tail_v = 0;  // empty ring: start at its beginning
@@ -962,8 +963,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   float* mine = part + (int64_t)split * pstride;
   // the warps' weights 2^(m_w - M) per head, once: thread (h, w) of the first 8 G threads
   __shared__ float wred[8][kDecWarps], mred[8];
-  static_assert(kDecWarps == 8, "one group of 8 lanes per head");
-  if (tid < 64) {  // whole warps 0 and 1 take part in the shuffles (8 G <= 64)
+  static_assert(kDecWarps == 16, "one group of 16 lanes per head");
+  if (tid < 8 * kDecWarps) {  // whole warps 0-3 take part in the shuffles (16 G <= 128)
     const int h = tid / kDecWarps, w = tid % kDecWarps;
     const float mw = h < G ? red[((int64_t)w * 8 + h) * (D + 2) + D] : -INFINITY;
     float M = mw;
@@ -1016,7 +1017,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   // 2^(m_s - M) is computed once per head.
   __shared__ float Mh[8], Lh[8], Sh[8];  // running max, running sum, rescale of the previous chunks
   const int per = pstride;               // floats of one split's partial
-  const int chunk = max(1, (int)((int64_t)kDecWarps * P.ring_bytes / (4 * (per + 8))));
+  const int chunk = max(1, (int)((int64_t)P.ring_warps * P.ring_bytes / (4 * (per + 8))));
   float* buf = reinterpret_cast<float*>(ring);
   float* wts = buf + (int64_t)chunk * per;  // [8][chunk]
   if (tid < G) {
@@ -1088,13 +1089,13 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
 }
 
 constexpr int64_t kDecodeSmemLimit = 227 * 1024 - 1024;  // per-block limit less room for static shared memory
-constexpr int64_t kTwoBlockSmem = 112 * 1024;             // two blocks per SM below this
 
 struct DecodeGeom {
   int64_t max_item;
   int ctas;     // nominal number of blocks dealt to heads
   int splits;   // grid size: ctas + one spare block per head
   int ring_bytes;
+  int ring_warps;  // warps with a ring (all, or fewer with larger rings when tiles are large)
   size_t smem;
   size_t partial_bytes;
   size_t ticket_off;   // tickets then the status word
@@ -1109,15 +1110,19 @@ static DecodeGeom decode_geom(const rdkv_cache* c) {
   const int64_t fixed = decode_fixed_smem(D, s.dtype == RDKV_F32);
   const int64_t max_item = std::max<int64_t>(align_up(c->sizes.max_stage_bytes, 128), 2 * kCRows * D * 2);
   g.max_item = max_item;
-  int64_t ring = ((kTwoBlockSmem - fixed) / kDecWarps) / 128 * 128;
-  int blocks_per_sm = 2;
-  if (ring < max_item) {
-    ring = std::min<int64_t>(align_up(2 * max_item, 128), ((kDecodeSmemLimit - fixed) / kDecWarps) / 128 * 128);
-    blocks_per_sm = 1;
+  // one block of kDecWarps warps per SM; the warps with a ring share what is left equally: all of
+  // them, or half (a quarter) with twice (four times) the ring when the largest staged tile needs it
+  int ring_warps = kDecWarps;
+  int64_t ring = ((kDecodeSmemLimit - fixed) / ring_warps) / 128 * 128;
+  while (ring < max_item && ring_warps > kDecWarps / 4) {
+    ring_warps /= 2;
+    ring = ((kDecodeSmemLimit - fixed) / ring_warps) / 128 * 128;
   }
-  ring = std::max<int64_t>(ring, align_up(decode_reduce_bytes(D), 128 * kDecWarps) / kDecWarps);
+  const int blocks_per_sm = 1;
+  if ((int64_t)ring_warps * ring < decode_reduce_bytes(D)) ring = 0;  // the warps' results reuse the rings
   g.ring_bytes = (int)ring;
-  g.smem = (size_t)(fixed + (int64_t)kDecWarps * ring);
+  g.ring_warps = ring_warps;
+  g.smem = (size_t)(fixed + (int64_t)ring_warps * ring);
   // blocks dealt to heads in proportion to their work: a nominal count that fills every SM once,
   // fewer when there is little work (at least kDecWarps items per block on average)
   const int64_t items = ceil_div64(c->sizes.index_slots, kTile) + (int64_t)n_heads * ceil_div(c->cap_c, kCRows);
@@ -1165,6 +1170,7 @@ static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo
   P.h_kv = s.h_kv;
   P.cap_c = cache->cap_c;
   P.ring_bytes = geo.ring_bytes;
+  P.ring_warps = geo.ring_warps;
   P.ctas = geo.ctas;
   return P;
 }

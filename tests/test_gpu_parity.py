@@ -237,8 +237,11 @@ def test_decode_step_agrees_with_append_then_attend():
         b = rdkv.rdkv_decode_attn(c2, qn)
         # the same values in the same blocks; which warp meets which tile first may differ, and with
         # it the reference max that p = 2^(s - m) is rounded to fp16 against (p rounds to 2^-11
-        # relative either way; against the oracle both stay within 2e-3)
-        torch.testing.assert_close(a, b, atol=5e-4, rtol=0)
+        # relative either way), so single elements may differ by up to the parity bar; a structural
+        # difference (a token missed or counted twice) moves every element of a head
+        d = (a - b).abs()
+        assert float(d.max()) <= 2e-3, float(d.max())
+        assert float(d.mean()) <= 5e-5, float(d.mean())
 
 
 def test_decode_step_in_a_replayed_graph():

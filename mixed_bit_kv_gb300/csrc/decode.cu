@@ -36,19 +36,20 @@ constexpr int kCRows = 16;        // zone-C rows per work item
 constexpr int kMaxKB = 16;        // k-blocks of a K row (D = 128: at most 13)
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at GB300 clocks
 
+// One k-block of a head's K rows (16 slots inside one width segment).  The same for every lane:
+// each lane adds its own constant offsets.
 struct KBDesc {
-  int16_t width;    // 16, 8, 4, 2
-  int16_t nrem;     // slots of the segment from the block start (>= 1)
-  int32_t word0;    // word of the block's first slot inside a K row
-  int32_t meta0;    // index of the block's first slot pair among the quantised pairs
-  int32_t pad;
+  int32_t wbyte;    // byte offset in a tile of the block's first word: 128 * word (word-major layout)
+  int32_t mbyte;    // byte offset of the block's first slot pair in the K metadata: 8 * pair
+  int32_t nrem;     // slots of the segment from the block start (>= 1)
+  int32_t slot0;    // first slot of the block (for the query fragments)
 };
 
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings): k-block
 // descriptors, query fragments (float4 per lane for fp32 queries, two fp16 pairs otherwise),
-// zone-C query fragments, per-lane offsets, query rows, slot table, ring bookkeeping.
+// zone-C query fragments, query rows, slot table, ring bookkeeping, the fused step's new row.
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D, bool qlo) {
-  return ((256 + (int64_t)kMaxKB * 32 * (qlo ? 16 : 8) + (int64_t)(D / 16) * 32 * 16 + (int64_t)kMaxKB * 32 * 16 +
+  return ((256 + (int64_t)kMaxKB * 32 * (qlo ? 16 : 8) + (int64_t)(D / 16) * 32 * 16 +
            (int64_t)8 * D * 4 + (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 20 + (int64_t)2 * D * 2) + 127) /
          128 * 128;
 }
@@ -279,8 +280,8 @@ __device__ __forceinline__ void k_segment(const unsigned char* kw, const unsigne
       }
     } else {
       // a pair past the segment end reads the block's first (valid) pair: its q entries are 0
-      const int p0 = d.meta0 + (2 * q < d.nrem ? q : 0), p1 = d.meta0 + (2 * q + 8 < d.nrem ? q + 4 : 0);
-      const uint2 m0 = lds64(kmeta, 8u * p0), m1 = lds64(kmeta, 8u * p1);
+      const uint32_t p0 = d.mbyte + (2 * q < d.nrem ? 8 * q : 0), p1 = d.mbyte + (2 * q + 8 < d.nrem ? 8 * (q + 4) : 0);
+      const uint2 m0 = lds64(kmeta, p0), m1 = lds64(kmeta, p1);
       const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&m0.x));
       const float2 z0 = __half22float2(*reinterpret_cast<const __half2*>(&m0.y));
       const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&m1.x));
@@ -290,8 +291,8 @@ __device__ __forceinline__ void k_segment(const unsigned char* kw, const unsigne
       bh0 = t.x; bh1 = t.y; bl0 = t.z; bl1 = t.w;
     }
     // tokens g, g+8, g+16, g+24 of the lane's two words
-    const uint4 x0 = lds128(kw, 4u * (32u * (uint32_t)(d.word0 + o0) + 4u * g));
-    const uint4 x1 = W == 2 ? x0 : lds128(kw, 4u * (32u * (uint32_t)(d.word0 + o1) + 4u * g));
+    const uint4 x0 = lds128(kw, (uint32_t)d.wbyte + 128u * o0 + 16u * g);
+    const uint4 x1 = W == 2 ? x0 : lds128(kw, (uint32_t)d.wbyte + 128u * o1 + 16u * g);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
       uint32_t a0, a1, a2, a3;
@@ -320,23 +321,29 @@ __device__ __forceinline__ void k_segment(const unsigned char* kw, const unsigne
 // at bit 0 of a half-word is the value c * 2^-24 exactly, so one shift and one
 // mask make the A operand and the products land in sq scaled by 2^-24 (undone
 // once per tile).  Raw 16-bit channels go to sr at scale 1, and the zero-point
-// term sum_c q_c zero_c runs as an MMA whose A rows all hold the zeros, so
-// every row of zacc carries it for heads (2q, 2q+1).
+// term sum_c q_c zero_c runs as an MMA whose A rows g + 8 hold the zeros, so
+// zacc[2], zacc[3] carry it for heads (2q, 2q+1).
 template <int W>
 __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsigned char* kmeta, int kb0, int kb1,
-                                            const uint4* koff, const uint2* qh, int lane, float (&sq)[2][4],
+                                            const KBDesc* kbd, const uint2* qh, int lane, float (&sq)[2][4],
                                             float (&sr)[2][4], float (&zacc)[4]) {
-  const int q = lane & 3;
+  const int g = lane >> 2, q = lane & 3;
   constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
   const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
   const int sh1 = W == 2 ? 2 * q + 8 : sh0;
+  // this lane's offsets from a block's first word: words o0, o1 of its two slot pairs, tokens g ..
+  const uint32_t c0 = 128u * (W == 16 ? q : W == 8 ? (q >> 1) : 0) + 16u * g;
+  const uint32_t c1 = 128u * (W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0) + 16u * g;
 #pragma unroll 1
   for (int kb = kb0; kb < kb1; ++kb) {
-    const uint4 off = koff[kb * 32 + lane];
+    const KBDesc d = kbd[kb];  // the same address in every lane: one broadcast
     const uint2 qq = qh[kb * 32 + lane];  // q_g (fp16 pairs) at slots (2q, 2q+1), (2q+8, 2q+9); 0 for pads
+    const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
     uint32_t bh0 = qq.x, bh1 = qq.y, bl0 = 0, bl1 = 0;
     if (W != 16) {
-      const uint2 m0 = lds64(kmeta, off.z), m1 = lds64(kmeta, off.w);
+      // a pair past the segment end reads the block's first pair (its q entries are 0)
+      const uint2 m0 = lds64(kmeta, (uint32_t)d.mbyte + (v0 ? 8u * q : 0u));
+      const uint2 m1 = lds64(kmeta, (uint32_t)d.mbyte + (v1 ? 8u * (q + 4) : 0u));
       const __half2 q0 = *reinterpret_cast<const __half2*>(&qq.x), q1 = *reinterpret_cast<const __half2*>(&qq.y);
       const __half2 s0 = *reinterpret_cast<const __half2*>(&m0.x), s1 = *reinterpret_cast<const __half2*>(&m1.x);
       const __half2 h0 = __hmul2(q0, s0), h1 = __hmul2(q1, s1);
@@ -345,17 +352,20 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsig
       bh1 = *reinterpret_cast<const uint32_t*>(&h1);
       bl0 = *reinterpret_cast<const uint32_t*>(&l0);
       bl1 = *reinterpret_cast<const uint32_t*>(&l1);
-      mma16816(zacc, m0.y, m0.y, m1.y, m1.y, qq.x, qq.y);
+      // A = the metadata as loaded, {scales, zeros} of the two pairs: rows g get sum scale * q
+      // (unused) and rows g + 8 the zero-point term sum zero * q, with no register shuffling
+      mma16816(zacc, m0.x, m0.y, m1.x, m1.y, qq.x, qq.y);
     }
     // tokens g, g+8, g+16, g+24 of the lane's two words (one word for 2-bit codes)
-    const uint4 y0 = lds128(kw, off.x);
-    const uint4 y1 = W == 2 ? y0 : lds128(kw, off.y);
+    const uint4 y0 = lds128(kw, (uint32_t)d.wbyte + c0);
+    const uint4 y1 = W == 2 ? y0 : lds128(kw, (uint32_t)d.wbyte + c1);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
       const uint32_t x0 = pick4(y0, 2 * tb), x1 = pick4(y0, 2 * tb + 1);
       const uint32_t x2 = pick4(y1, 2 * tb), x3 = pick4(y1, 2 * tb + 1);
-      if (W == 16) {
-        mma16816(sr[tb], x0 & off.z, x1 & off.z, x2 & off.w, x3 & off.w, bh0, bh1);
+      if (W == 16) {  // raw fp16 words past the segment end may hold anything: zero them
+        const uint32_t k0 = v0 ? ~0u : 0u, k1 = v1 ? ~0u : 0u;
+        mma16816(sr[tb], x0 & k0, x1 & k0, x2 & k1, x3 & k1, bh0, bh1);
       } else {
         const uint32_t a0 = (x0 >> sh0) & mask2, a1 = (x1 >> sh0) & mask2;
         const uint32_t a2 = (x2 >> sh1) & mask2, a3 = (x3 >> sh1) & mask2;
@@ -368,7 +378,7 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsig
 
 template <int D, bool QLO>
 __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsigned char* kmeta, const int (&seg_kb)[5],
-                                            const KBDesc* kbd, const float4* qv, const uint4* koff, int lane,
+                                            const KBDesc* kbd, const float4* qv, int lane,
                                             float (&s)[2][4]) {
   float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
 #pragma unroll
@@ -387,19 +397,19 @@ __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsig
     bo = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
   } else {
     const uint2* qh = reinterpret_cast<const uint2*>(qv);
-    float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // zero-point term of heads 2q, 2q+1 (every row)
+    float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // [2], [3]: zero-point term of heads 2q, 2q+1
     float sr[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // raw 16-bit channels, scale 1
-    k_segment_h<16>(kw, kmeta, seg_kb[0], seg_kb[1], koff, qh, lane, s, sr, zacc);
-    k_segment_h<8>(kw, kmeta, seg_kb[1], seg_kb[2], koff, qh, lane, s, sr, zacc);
-    k_segment_h<4>(kw, kmeta, seg_kb[2], seg_kb[3], koff, qh, lane, s, sr, zacc);
-    k_segment_h<2>(kw, kmeta, seg_kb[3], seg_kb[4], koff, qh, lane, s, sr, zacc);
+    k_segment_h<16>(kw, kmeta, seg_kb[0], seg_kb[1], kbd, qh, lane, s, sr, zacc);
+    k_segment_h<8>(kw, kmeta, seg_kb[1], seg_kb[2], kbd, qh, lane, s, sr, zacc);
+    k_segment_h<4>(kw, kmeta, seg_kb[2], seg_kb[3], kbd, qh, lane, s, sr, zacc);
+    k_segment_h<2>(kw, kmeta, seg_kb[3], seg_kb[4], kbd, qh, lane, s, sr, zacc);
     // s holds the code products at 2^-24
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[tb][e] = fmaf(s[tb][e], 16777216.f, sr[tb][e]);
-    be = zacc[0];
-    bo = zacc[1];
+    be = zacc[2];
+    bo = zacc[3];
   }
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
@@ -575,8 +585,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
   KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
   float4* qv = reinterpret_cast<float4*>(smem + 256);                              // [kMaxKB][32] (uint2 if !QLO)
   uint4* qfragc = reinterpret_cast<uint4*>(smem + 256 + kMaxKB * 32 * (QLO ? 16 : 8));  // [D/16][32] hi, lo
-  uint4* koff = qfragc + (D / 16) * 32;                                            // [kMaxKB][32]
-  float* q_s = reinterpret_cast<float*>(koff + kMaxKB * 32);                       // [8][D] query rows of the group
+  float* q_s = reinterpret_cast<float*>(qfragc + (D / 16) * 32);                   // [8][D] query rows of the group
   int16_t* slot_s = reinterpret_cast<int16_t*>(q_s + 8 * D);                       // [D + kSlotPad] slot table
   uint64_t* bars = reinterpret_cast<uint64_t*>(slot_s + D + kSlotPad);             // [warps][kMaxInflight]
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
@@ -642,11 +651,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
       const int nslot = pick(ns, seg);
       const int s0 = 16 * (lane - pick(nb, seg));
       KBDesc d;
-      d.width = (int16_t)w;
-      d.nrem = (int16_t)min(16, nslot - s0);
-      d.word0 = pick(wb, seg) + s0 / per;
-      d.meta0 = (w < 16 ? pick(mb, seg) + s0 : 0) / 2;
-      d.pad = pick(sb, seg) + s0;  // first slot of the block (for the query fragments)
+      d.wbyte = 128 * (pick(wb, seg) + s0 / per);
+      d.mbyte = 8 * ((w < 16 ? pick(mb, seg) + s0 : 0) / 2);
+      d.nrem = min(16, nslot - s0);
+      d.slot0 = pick(sb, seg) + s0;
       kbd[lane] = d;
     }
   }
@@ -766,33 +774,12 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
         int ch;
         if (kb < nkb) {
           const KBDesc d = kbd[kb];
-          ch = off < d.nrem ? slot_s[d.pad + off] : -1;
+          ch = off < d.nrem ? slot_s[d.slot0 + off] : -1;
         } else {
           ch = 16 * (kb - nkb) + off;
         }
         if (ch >= 0) v[e] = q_s[g * D + ch];
       }
-    }
-    if (kb < nkb) {
-      // this lane's byte offsets in a K row of the words holding its two slot pairs, and either the
-      // metadata offsets of those pairs (quantised widths; a pair past the segment end reads the
-      // block's first pair) or masks that zero raw 16-bit words past the segment end
-      const KBDesc d = kbd[kb];
-      const int w = d.width;
-      const int o0 = w == 16 ? qq : w == 8 ? (qq >> 1) : 0;
-      const int o1 = w == 16 ? qq + 4 : w == 8 ? (qq >> 1) + 2 : w == 4 ? 1 : 0;
-      const bool v0 = 2 * qq < d.nrem, v1 = 2 * qq + 8 < d.nrem;
-      uint4 e;  // word-major tile: word w of tokens g, g+8, g+16, g+24 at 4 (32 w + 4 g)
-      e.x = 4u * (32u * (uint32_t)(d.word0 + o0) + 4u * (uint32_t)g);
-      e.y = 4u * (32u * (uint32_t)(d.word0 + o1) + 4u * (uint32_t)g);
-      if (w == 16) {
-        e.z = v0 ? ~0u : 0u;
-        e.w = v1 ? ~0u : 0u;
-      } else {
-        e.z = 8u * (uint32_t)(d.meta0 + (v0 ? qq : 0));
-        e.w = 8u * (uint32_t)(d.meta0 + (v1 ? qq + 4 : 0));
-      }
-      koff[kb * 32 + ln] = e;
     }
     if (kb >= nkb) qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
     else if (QLO) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
@@ -833,7 +820,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
       const unsigned char* stp = wring + wpos[slot];
       const unsigned char* kmeta = stp + 4 * kTile * RW;
       float s[2][4];
-      tile_logits<D, QLO>(stp, kmeta, seg_kb, kbd, qv, koff, lane, s);
+      tile_logits<D, QLO>(stp, kmeta, seg_kb, kbd, qv, lane, s);
 #pragma unroll
       for (int tb = 0; tb < 2; ++tb)
 #pragma unroll

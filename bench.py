@@ -41,6 +41,26 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_sequences(rank, batch):
+    """First and one-past-last sequence of this rank: every rank compresses and decodes its own
+    `batch` sequences (weak scaling, no data-path exchange)."""
+    return rank * batch, (rank + 1) * batch
+
+
+def max_over_ranks(values, ws, device):
+    """Element-wise maximum over ranks of per-rank totals: the slowest rank sets the step time."""
+    if ws <= 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(ws, units_per_rank, seconds):
+    """Units all ranks processed per second (each rank processes the same amount)."""
+    return ws * units_per_rank / seconds
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -147,7 +167,7 @@ def run_ours(args, ws, rank, local):
     L = args.layers
     S = args.decode_steps if args.decode_steps is not None else w.decode_steps
     avg = w.budgets[0] if args.budget is None else args.budget
-    first_seq = rank * w.batch
+    first_seq, _ = rank_sequences(rank, w.batch)
     shape = rdkv.make_shape(w.batch, w.n_tokens, w.h_q, w.h_kv, w.head_dim, w.window, w.dtype)
     cap_c = w.window + S
 
@@ -247,16 +267,14 @@ def run_ours(args, ws, rank, local):
     dec_ms = [b.elapsed_time(c) for a, b, c in ev]
     score_ms = sum(e0.elapsed_time(e1) for e0, e1 in score_ev) / args.steps
     tot_ms, tot_dec, tot_score = sum(step_ms), sum(dec_ms), score_ms * args.steps
-    if ws > 1:
-        t = torch.tensor([tot_ms, tot_dec, tot_score], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot_ms, tot_dec, tot_score = t.tolist()
+    tot_ms, tot_dec, tot_score = max_over_ranks([tot_ms, tot_dec, tot_score], ws, dev)
+    score_ms = tot_score / args.steps
 
     ms_per_step = tot_ms / args.steps
     dec_ms_step = tot_dec / args.steps
-    value = ws * dec_bytes / (dec_ms_step * 1e-3) / 1e9
+    value = whole_job_rate(ws, dec_bytes, dec_ms_step * 1e-3) / 1e9
     flops = scorer_flops(w) * L
-    score_tflops = ws * flops / (score_ms * 1e-3) / 1e12
+    score_tflops = whole_job_rate(ws, flops, score_ms * 1e-3) / 1e12
     peaks = measured_peaks()
     clocks = clk.summary()
 
@@ -289,6 +307,10 @@ def run_ours(args, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev)
+    comparator = None
+    if not args.no_comparator:
+        comparator = run_fp16_comparator(w, L, pre, dq, dev)
+        comparator["trizone_speedup"] = round(comparator["us_per_layer_step"] / (dec_ms_step * 1e3 / (S * L)), 2)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -309,7 +331,51 @@ def run_ours(args, ws, rank, local):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if comparator is not None:
+        line["comparator"] = comparator
     return line
+
+
+def run_fp16_comparator(w, L, pre, dq, dev, steps=16):
+    """Context number: decode over the full fp16 cache of the same layers (all N prompt tokens, no
+    compression) with torch's scaled_dot_product_attention (a library call), per layer step, replayed
+    from a CUDA graph like the TriZone decode.  The caches of all layers are rotated (inputs larger
+    than L2)."""
+    steps = min(steps, dq.shape[0])
+    caches = [tuple(t.permute(0, 2, 1, 3).contiguous() for t in (pre[layer][1], pre[layer][2])) for layer in range(L)]
+    qs = dq[:steps]  # [steps, L, B, H_q, D]
+    out = torch.empty(w.batch, w.h_q, 1, w.head_dim, dtype=qs.dtype, device=dev)
+
+    def run():
+        for s in range(steps):
+            for layer in range(L):
+                k, v = caches[layer]
+                out.copy_(torch.nn.functional.scaled_dot_product_attention(
+                    qs[s, layer].unsqueeze(2), k, v, enable_gqa=True))
+
+    run()
+    torch.cuda.synchronize()
+    mode = "graph"
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        replay = g.replay
+    except Exception:
+        mode = "eager"
+        replay = run
+    replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (steps * L)
+    nbytes = 2 * w.batch * w.n_tokens * w.h_kv * w.head_dim * 2
+    del caches
+    return {"kind": "fp16 full cache (all N prompt tokens), torch scaled_dot_product_attention, " + mode,
+            "us_per_layer_step": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
 
 
 def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev):
@@ -437,6 +503,7 @@ def main():
     ap.add_argument("--oracle-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-comparator", action="store_true", help="skip the fp16 full-cache SDPA context number")
     args = ap.parse_args()
     ws, rank, local = dist_env()
 

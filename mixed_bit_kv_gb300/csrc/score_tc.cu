@@ -11,10 +11,11 @@
 //   pass 2  A = 128 keys of KV head j, B = query tiles tau >= t of the G heads
 //           of the group.  The epilogue adds 2^(s*c - lse2[tau]) per key:
 //           the column sums of the attention, i.e. w_t; then g_t = w_t * sigma_t.
-// Roles (320 threads): warp 0 loads tiles with TMA into a 4-stage ring; warp 1
-// issues tcgen05.mma (one thread) into two TMEM accumulators; warps 2..9 read
-// the accumulators back (two warps per TMEM lane quarter, one per column
-// half) and run the softmax arithmetic.  Every wait is bounded: a wait that
+// Roles (576 threads): warp 0 loads tiles with TMA into a 4-stage ring; warp 1
+// issues tcgen05.mma (one thread) into two TMEM accumulators; warps 2..17 read
+// the accumulators back (four warps per TMEM lane quarter, one per 32-column
+// slice, so every SM sub-partition interleaves four of them) and run the
+// softmax arithmetic.  Every wait is bounded: a wait that
 // runs out writes NaN into the affected outputs, which the allocation reports
 // as invalid gains.
 #include <cuda.h>
@@ -27,7 +28,10 @@ namespace tc {
 
 constexpr int kRows = 128;       // rows of A, rows of a streamed tile
 constexpr int kStages = 4;       // TMA ring depth
-constexpr int kThreads = 320;    // producer, MMA, 8 epilogue warps
+constexpr int kEpiWarps = 16;                 // epilogue warps: 4 per TMEM lane quarter
+constexpr int kSlices = kEpiWarps / 4;        // column slices of the accumulator
+constexpr int kSliceCols = 128 / kSlices;     // columns per epilogue warp (multiple of 32)
+constexpr int kThreads = 64 + 32 * kEpiWarps; // producer, MMA, epilogue warps
 constexpr long long kWait = 4000000000ll;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -148,9 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&tfull[t], 1);
-      mbar_init(&tempty[t], 8);
+      mbar_init(&tempty[t], kEpiWarps);
       mbar_init(&lfull[t], 1);
-      mbar_init(&lempty[t], 8);
+      mbar_init(&lempty[t], kEpiWarps);
     }
     failed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   } else {
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int colh = (warp - 2) >> 2;        // column half: 0 for warps 2..5, 1 for warps 6..9
+    const int colh = (warp - 2) >> 2;        // column slice: warps 2..5 take slice 0, 6..9 slice 1, ...
     const int r = quarter * 32 + lane;       // accumulator row = A row
     const int row = row0 + r;                // query (pass 1) or key (pass 2)
     float m = -INFINITY, l = 0.f;            // pass 1: running max and sum (base 2, scaled logits)
@@ -225,12 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       int head, t0;
       tile_of(i, head, t0);
-      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t * kRows + colh * 64);
+      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t * kRows + colh * kSliceCols);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
+      for (int ch = 0; ch < kSliceCols / 32; ++ch) {
         float v[32];
         tmem_ld32(ta + 32 * ch, v);
-        const int c0 = t0 + colh * 64 + ch * 32;  // first key (pass 1) or query (pass 2) of the chunk
+        const int c0 = t0 + colh * kSliceCols + ch * 32;  // first key (pass 1) or query (pass 2) of the chunk
         if (PASS == 1) {
           // valid keys: c <= row (c < N follows for rows < N); only the diagonal tile needs the mask.
           // The max is taken on raw logits (c > 0) and the scale folded into one FMA per element.
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
             m = mn;
           }
         } else {
-          const float4* ls4 = reinterpret_cast<const float4*>(lse_s + t * kRows + colh * 64 + ch * 32);
+          const float4* ls4 = reinterpret_cast<const float4*>(lse_s + t * kRows + colh * kSliceCols + ch * 32);
           float a0 = 0.f, a1 = 0.f;
           if (t0 != row0 && t0 + kRows <= P.N) {  // no causal edge and no tail in this tile
 #pragma unroll
@@ -292,28 +296,35 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       }
     }
     if (!ok) failed = 1;
-    // combine the two column halves of each row through shared memory (the A tile is free now)
-    float* comb = reinterpret_cast<float*>(As);  // [2][128] partial values
+    // combine the column slices of each row through shared memory (the A tile is free now)
+    float* comb = reinterpret_cast<float*>(As);  // [2][kSlices][128] partial values
     __syncwarp();
-    asm volatile("bar.sync 1, 256;" ::: "memory");  // every epilogue warp is past its last TMEM read
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");  // every epilogue warp is past its last TMEM read
     const bool bad = failed != 0;
     if (PASS == 1) {
-      if (colh == 1) {
-        comb[r] = m;
-        comb[kRows + r] = l;
-      }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      comb[colh * kRows + r] = m;
+      comb[(kSlices + colh) * kRows + r] = l;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
       if (colh == 0 && row < P.N) {
-        const float m2 = comb[r], l2 = comb[kRows + r];
-        const float mm = fmaxf(m, m2);
-        const float ll = (m == -INFINITY ? 0.f : l * ex2(m - mm)) + (m2 == -INFINITY ? 0.f : l2 * ex2(m2 - mm));
+        float mm = -INFINITY;
+#pragma unroll
+        for (int sl = 0; sl < kSlices; ++sl) mm = fmaxf(mm, comb[sl * kRows + r]);
+        float ll = 0.f;
+#pragma unroll
+        for (int sl = 0; sl < kSlices; ++sl) {
+          const float ms = comb[sl * kRows + r];
+          if (ms != -INFINITY) ll += comb[(kSlices + sl) * kRows + r] * ex2(ms - mm);
+        }
         P.lse2[((int64_t)b * P.h_q + blockIdx.y) * P.lse_stride + row] = bad ? __int_as_float(0x7fc00000) : mm + __log2f(ll);
       }
     } else {
-      if (colh == 1) comb[r] = acc;
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      comb[colh * kRows + r] = acc;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
       if (colh == 0 && row < P.N) {
-        const float w = bad ? __int_as_float(0x7fc00000) : acc + comb[r];
+        float w = 0.f;
+#pragma unroll
+        for (int sl = 0; sl < kSlices; ++sl) w += comb[sl * kRows + r];
+        w = bad ? __int_as_float(0x7fc00000) : w;
         const int64_t o = ((int64_t)b * P.h_kv + blockIdx.y) * P.N + row;
         P.w_tok[o] = w;
         if (row < P.Np) P.g_tok[((int64_t)b * P.h_kv + blockIdx.y) * P.Np + row] = w * P.sigma[o];

@@ -12,7 +12,7 @@
 //           of the group.  The epilogue adds 2^(s*c - lse2[tau]) per key:
 //           the column sums of the attention, i.e. w_t; then g_t = w_t * sigma_t.
 // Roles (576 threads): warp 0 loads tiles with TMA into a 4-stage ring; warp 1
-// issues tcgen05.mma (one thread) into two TMEM accumulators; warps 2..17 read
+// issues tcgen05.mma (one thread) into four TMEM accumulators; warps 2..17 read
 // the accumulators back (four warps per TMEM lane quarter, one per 32-column
 // slice, so every SM sub-partition interleaves four of them) and run the
 // softmax arithmetic.  Every wait is bounded: a wait that
@@ -28,6 +28,7 @@ namespace tc {
 
 constexpr int kRows = 128;       // rows of A, rows of a streamed tile
 constexpr int kStages = 4;       // TMA ring depth
+constexpr int kAcc = 4;          // TMEM accumulators (4 x 128 columns: all of tensor memory)
 constexpr int kEpiWarps = 16;                 // epilogue warps: 4 per TMEM lane quarter
 constexpr int kSlices = kEpiWarps / 4;        // column slices of the accumulator
 constexpr int kSliceCols = 128 / kSlices;     // columns per epilogue warp (multiple of 32)
@@ -44,14 +45,17 @@ __device__ __forceinline__ void mbar_expect(uint64_t* b, uint32_t tx) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
 }
+// A waiting thread sleeps inside try_wait (woken when the phase completes) for up to this long
+// per attempt, instead of spinning on the issue slots the epilogue needs.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
   const long long t0 = clock64();
   while (true) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(su32(b)), "r"(parity)
+        : "r"(su32(b)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     if (ok) return true;
     if (clock64() - t0 > kWait) return false;
@@ -119,8 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* As = sm;
   uint8_t* Bs = sm + kTileBytes;                           // [kStages][tile]
-  float* lse_s = reinterpret_cast<float*>(Bs + kStages * kTileBytes);  // [2][128] (pass 2)
-  __shared__ uint64_t bar_a, full[kStages], empty[kStages], tfull[2], tempty[2], lfull[2], lempty[2];
+  float* lse_s = reinterpret_cast<float*>(Bs + kStages * kTileBytes);  // [kAcc][128] (pass 2)
+  __shared__ uint64_t bar_a, full[kStages], empty[kStages], tfull[kAcc], tempty[kAcc], lfull[kAcc], lempty[kAcc];
   __shared__ uint32_t tmem_base;
   __shared__ int failed;
 
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   };
 
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(su32(&tmem_base)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)), "n"(kAcc * kRows));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 32) {
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < kAcc; ++t) {
       mbar_init(&tfull[t], 1);
       mbar_init(&tempty[t], kEpiWarps);
       mbar_init(&lfull[t], 1);
@@ -179,8 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         for (int hh = 0; hh < kHalves; ++hh)
           tma4(Bs + s * kTileBytes + hh * kRows * 128, &tmB, 64 * hh, head, t0, b, &full[s]);
         if (PASS == 2) {
-          const int t = i & 1;
-          if (!mbar_wait(&lempty[t], ((i >> 1) & 1) ^ 1)) { failed = 1; break; }
+          const int t = i % kAcc;
+          if (!mbar_wait(&lempty[t], ((i / kAcc) & 1) ^ 1)) { failed = 1; break; }
           mbar_expect(&lfull[t], kRows * 4);
           bulk_g2s(lse_s + t * kRows, P.lse2 + ((int64_t)b * P.h_q + head) * P.lse_stride + t0, kRows * 4, &lfull[t]);
         }
@@ -191,9 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     if (lane == 0) {
       if (!mbar_wait(&bar_a, 0)) failed = 1;
       for (int i = 0; i < n_tiles && !failed; ++i) {
-        const int s = i % kStages, t = i & 1;
+        const int s = i % kStages, t = i % kAcc;
         if (!mbar_wait(&full[s], (i / kStages) & 1)) { failed = 1; break; }
-        if (!mbar_wait(&tempty[t], ((i >> 1) & 1) ^ 1)) { failed = 1; break; }
+        if (!mbar_wait(&tempty[t], ((i / kAcc) & 1) ^ 1)) { failed = 1; break; }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t a0 = su32(As), b0 = su32(Bs + s * kTileBytes);
 #pragma unroll
@@ -223,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     float acc = 0.f;                         // pass 2: column sum of the attention
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
-      const int t = i & 1;
-      if (!mbar_wait(&tfull[t], (i >> 1) & 1)) { ok = false; break; }
-      if (PASS == 2 && !mbar_wait(&lfull[t], (i >> 1) & 1)) { ok = false; break; }
+      const int t = i % kAcc;
+      if (!mbar_wait(&tfull[t], (i / kAcc) & 1)) { ok = false; break; }
+      if (PASS == 2 && !mbar_wait(&lfull[t], (i / kAcc) & 1)) { ok = false; break; }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       int head, t0;
       tile_of(i, head, t0);
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kAcc * kRows));
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -369,7 +373,7 @@ static rdkv_status make_map(CUtensorMap* m, const void* base, int B, int N, int 
 
 template <int D>
 static size_t smem_bytes() {
-  return 1024 + (size_t)(1 + kStages) * kRows * D * 2 + 2 * kRows * 4;
+  return 1024 + (size_t)(1 + kStages) * kRows * D * 2 + kAcc * kRows * 4;
 }
 
 template <int D>

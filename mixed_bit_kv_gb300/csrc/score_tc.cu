@@ -7,7 +7,7 @@
 // memory accumulator:
 //   pass 1  A = 128 query rows of head h, B = key tiles t <= tau.  The epilogue
 //           keeps, per query row, the running max and sum of 2^(s*c) and writes
-//           lse2 = log2 sum_t 2^(s_t * c), c = log2(e)/sqrt(D).
+//           -lse2, lse2 = log2 sum_t 2^(s_t * c), c = log2(e)/sqrt(D).
 //   pass 2  A = 128 keys of KV head j, B = query tiles tau >= t of the G heads
 //           of the group.  The epilogue adds 2^(s*c - lse2[tau]) per key:
 //           the column sums of the attention, i.e. w_t; then g_t = w_t * sigma_t.
@@ -90,6 +90,24 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // 32 consecutive accumulator columns of this thread's TMEM lane.
+// Paired fp32 arithmetic (two lanes of work per instruction): a * b + c and a + b, elementwise.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n .reg .b64 pa, pb, pc, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n mov.b64 pc, {%6, %7};\n"
+      " fma.rn.f32x2 pd, pa, pb, pc;\n mov.b64 {%0, %1}, pd;\n}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n add.rn.f32x2 pd, pa, pb;\n"
+      " mov.b64 {%0, %1}, pd;\n}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t ta, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -108,7 +126,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, float (&v)[32]) {
 struct Params {
   int N, n_blk, h_q, h_kv, G, Np, lse_stride;
   float c;             // log2(e) / sqrt(D)
-  float* lse2;         // [B][H_q][lse_stride]
+  float* lse2;         // [B][H_q][lse_stride]: -log2 sum_t 2^(s c) per query row (negated)
   const float* sigma;  // [B][H_kv][N]
   float* w_tok;        // [B][H_kv][N]
   float* g_tok;        // [B][H_kv][Np]
@@ -255,27 +273,38 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           }
           const float mn = fmaxf(m, mx * P.c);
           if (mn != -INFINITY) {
-            float s0 = 0.f, s1 = 0.f;
+            // 2^(v c - mn) with the scale-and-shift and the sums on paired fp32 instructions
+            const float2 cc = make_float2(P.c, P.c), sh = make_float2(-mn, -mn);
+            float2 s0 = make_float2(0.f, 0.f), s1 = s0;
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              s0 += ex2(fmaf(v[e], P.c, -mn));
-              s1 += ex2(fmaf(v[e + 1], P.c, -mn));
+            for (int e = 0; e < 32; e += 4) {
+              const float2 x0 = ffma2(make_float2(v[e], v[e + 1]), cc, sh);
+              const float2 x1 = ffma2(make_float2(v[e + 2], v[e + 3]), cc, sh);
+              s0 = fadd2(s0, make_float2(ex2(x0.x), ex2(x0.y)));
+              s1 = fadd2(s1, make_float2(ex2(x1.x), ex2(x1.y)));
             }
-            l = l * ex2(m - mn) + (s0 + s1);
+            const float2 st = fadd2(s0, s1);
+            l = l * ex2(m - mn) + (st.x + st.y);
             m = mn;
           }
         } else {
           const float4* ls4 = reinterpret_cast<const float4*>(lse_s + t * kRows + colh * kSliceCols + ch * 32);
           float a0 = 0.f, a1 = 0.f;
           if (t0 != row0 && t0 + kRows <= P.N) {  // no causal edge and no tail in this tile
+            // the staged values are -lse2: 2^(v c - lse2) = 2^(fma(v, c, -lse2)), paired
+            const float2 cc = make_float2(P.c, P.c);
+            float2 p0 = make_float2(0.f, 0.f), p1 = p0;
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const float4 L = ls4[e4];
-              a0 += ex2(fmaf(v[4 * e4 + 0], P.c, -L.x));
-              a1 += ex2(fmaf(v[4 * e4 + 1], P.c, -L.y));
-              a0 += ex2(fmaf(v[4 * e4 + 2], P.c, -L.z));
-              a1 += ex2(fmaf(v[4 * e4 + 3], P.c, -L.w));
+              const float2 x0 = ffma2(make_float2(v[4 * e4 + 0], v[4 * e4 + 1]), cc, make_float2(L.x, L.y));
+              const float2 x1 = ffma2(make_float2(v[4 * e4 + 2], v[4 * e4 + 3]), cc, make_float2(L.z, L.w));
+              p0 = fadd2(p0, make_float2(ex2(x0.x), ex2(x0.y)));
+              p1 = fadd2(p1, make_float2(ex2(x1.x), ex2(x1.y)));
             }
+            const float2 pt = fadd2(p0, p1);
+            a0 = pt.x;
+            a1 = pt.y;
           } else {
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
@@ -284,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const int c = c0 + 4 * e4 + u;
-                const float p = ex2(fmaf(v[4 * e4 + u], P.c, -lv[u]));
+                const float p = ex2(fmaf(v[4 * e4 + u], P.c, lv[u]));
                 a0 += (c >= row && c < P.N) ? p : 0.f;
               }
             }
@@ -319,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           const float ms = comb[sl * kRows + r];
           if (ms != -INFINITY) ll += comb[(kSlices + sl) * kRows + r] * ex2(ms - mm);
         }
-        P.lse2[((int64_t)b * P.h_q + blockIdx.y) * P.lse_stride + row] = bad ? __int_as_float(0x7fc00000) : mm + __log2f(ll);
+        // stored negated: pass 2 adds it in the same FMA that scales the logit
+        P.lse2[((int64_t)b * P.h_q + blockIdx.y) * P.lse_stride + row] = bad ? __int_as_float(0x7fc00000) : -(mm + __log2f(ll));
       }
     } else {
       comb[colh * kRows + r] = acc;

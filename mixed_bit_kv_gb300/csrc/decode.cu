@@ -112,6 +112,12 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
                : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// atomic add of 1 with acquire-release semantics at GPU scope; returns the old value
+__device__ __forceinline__ int ticket_acq_rel(int32_t* p) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
@@ -973,13 +979,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
     }
     mine[i] = val;
   }
-  // the last block of this head merges every split: out = sum 2^(M_s - M) O_s / sum 2^(M_s - M) L_s
-  __threadfence();
+  // the last block of this head merges every split: out = sum 2^(M_s - M) O_s / sum 2^(M_s - M) L_s.
+  // One acquire-release ticket by thread 0 after the block barrier: the release covers every
+  // thread's partial writes (ordered before it by the barrier), the acquire makes the other
+  // blocks' released partials visible to the merging block (ordered after it by the next barrier).
   __syncthreads();
-  if (tid == 0) is_last = atomicAdd(&P.tickets[head], 1) == n_split - 1;
+  if (tid == 0) is_last = ticket_acq_rel(&P.tickets[head]) == n_split - 1;
   __syncthreads();
   if (!is_last) return;
-  __threadfence();
   if (tid == 0) P.tickets[head] = 0;  // every block of this head has counted: ready for the next call
   if (fused) {
     // every block of this head has read zone C: store the new row of this head; the last head to

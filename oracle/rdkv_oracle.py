@@ -234,6 +234,50 @@ def allocate(g_tok, w_chan, k, avg_bits_v, avg_bits_k):
 
 
 # ---------------------------------------------------------------------------
+# Allocation variants (the next rows beside the method: a reading with one
+# water level per KV head, and two eviction-only baselines on the same zones)
+# ---------------------------------------------------------------------------
+def allocate_per_head(g_tok, w_chan, k, avg_bits_v, avg_bits_k):
+    """Steps 2 and 3 with one water level per KV head instead of one per sequence:
+    each head's V tokens share a budget floor(avg_bits_v * N_p), each head's K channels
+    floor(avg_bits_k * D)."""
+    Hkv, Np = g_tok.shape
+    bits_tok = np.zeros((Hkv, Np), np.uint8)
+    lam_v = np.zeros(Hkv, np.float32)
+    for j in range(Hkv):
+        bits_tok[j], lam_v[j] = waterfill(g_tok[j], avg_bits_v)
+    sig_c = kept_channel_spread(k, bits_tok)
+    g_chan = np.asarray(w_chan, np.float32) * sig_c.astype(np.float32)
+    bits_chan = np.zeros(g_chan.shape, np.uint8)
+    lam_k = np.zeros(Hkv, np.float32)
+    for j in range(Hkv):
+        bits_chan[j], lam_k[j] = waterfill(g_chan[j], avg_bits_k)
+    return dict(bits_tok=bits_tok, lam_v=lam_v, sigma_chan=sig_c.astype(np.float32), g_chan=g_chan,
+                bits_chan=bits_chan, lam_k=lam_k)
+
+
+def topk_keep(w, avg_bits):
+    """Heavy-hitter eviction (H2O-style): with k = floor(B / 16) tokens affordable at 16 bits
+    (B = floor(avg_bits * U)), keep every token whose weight is larger than lambda, the
+    smallest non-negative float32 that at most k weights exceed; the others are dropped.
+    Written from that definition: sorted descending, lambda is the (k+1)-th value (0 when
+    fewer than k+1 weights are positive); equal weights at lambda are all dropped."""
+    w = np.asarray(w, dtype=np.float32).reshape(-1)
+    assert np.all(np.isfinite(w)) and np.all(w >= 0), "weights must be finite and non-negative"
+    kk = budget_bits(avg_bits, w.size) // 16
+    srt = np.sort(w)[::-1]
+    lam = np.float32(srt[kk]) if kk < w.size and srt[kk] > 0 else np.float32(0.0)
+    lam = lam + np.float32(0.0)
+    return np.where(w > lam, 16, 0).astype(np.uint8), lam
+
+
+def threshold_keep(w, tau):
+    """Threshold eviction (KVzap-style): keep the tokens whose weight exceeds tau at 16 bits."""
+    w = np.asarray(w, dtype=np.float32).reshape(-1)
+    return np.where(w > np.float32(tau), 16, 0).astype(np.uint8)
+
+
+# ---------------------------------------------------------------------------
 # TriZone plan and pack (RDKV section 2.3; layout R8)
 # ---------------------------------------------------------------------------
 def _ceil_div(a, b):

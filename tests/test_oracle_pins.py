@@ -386,3 +386,62 @@ def test_decode_bytes_all_16_matches_kv_formula():
     got = O.decode_bytes(cache["plan"], w.head_dim, w.h_q, w.h_kv, len_c=w.window, batch=1)
     expect = O.kv_cache_bytes(1, w.h_kv, w.head_dim, 2, w.n_tokens) + w.h_q * w.head_dim * 6
     assert got == expect
+
+
+# ---------------------------------------------------------------- allocation variants
+def test_topk_keep_brute_force_and_argsort():
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        U = int(rng.integers(1, 9))
+        w = rng.choice([0.0, 0.5, 1.0, 2.0, 3.5, 7.0], size=U).astype(np.float32) if trial % 2 else \
+            rng.lognormal(0, 1, U).astype(np.float32)
+        avg = float(rng.choice([0.0, 1.0, 3.0, 5.5, 8.0, 16.0]))
+        bits, lam = O.topk_keep(w, avg)
+        k = int(np.floor(np.float32(avg) * U)) // 16
+        # brute force: the smallest candidate level >= 0 that at most k weights exceed
+        cands = sorted(set([0.0] + [float(x) for x in w]))
+        best = next(c for c in cands if np.sum(w > np.float32(c)) <= k)
+        assert float(lam) == best, (w, avg, lam, best)
+        assert np.array_equal(bits, np.where(w > lam, 16, 0))
+        assert int(np.sum(bits)) // 16 <= k
+        if len(set(w.tolist())) == U and np.all(w > 0):   # distinct weights: exactly the k largest
+            top = set(np.argsort(-w)[:k].tolist())
+            assert set(np.nonzero(bits)[0].tolist()) == top
+
+
+def test_topk_keep_ties_and_extremes():
+    w = np.full(10, 2.0, np.float32)
+    bits, lam = O.topk_keep(w, 3.2)                         # k = 2 of 10 equal weights: none strictly above
+    assert float(lam) == 2.0 and not bits.any()
+    bits, lam = O.topk_keep(w, 16.0)                        # k = U: all kept, lambda 0
+    assert float(lam) == 0.0 and np.all(bits == 16)
+    bits, lam = O.topk_keep(np.array([0, 0, 5], np.float32), 16.0)
+    assert list(bits) == [0, 0, 16]                         # zero weights never kept
+
+
+def test_threshold_keep_closed_form():
+    w = np.array([0.0, 0.1, 0.5, 0.5, 2.0], np.float32)
+    assert list(O.threshold_keep(w, 0.5)) == [0, 0, 0, 0, 16]
+    assert list(O.threshold_keep(w, 0.0)) == [0, 16, 16, 16, 16]
+
+
+def test_allocate_per_head_reduces_to_pooled_for_one_head_and_keeps_budgets():
+    w, q, k, v, al, cache = _tiny_cache(3.0, 3.0)
+    sc = O.score(q, k, v, w.window)
+    one = O.allocate_per_head(sc["g_tok"], sc["w_chan"], k, 3.0, 3.0)
+    pooled = O.allocate(sc["g_tok"], sc["w_chan"], k, 3.0, 3.0)
+    for key in ("bits_tok", "bits_chan", "sigma_chan", "g_chan"):
+        assert np.array_equal(one[key], pooled[key]), key
+    assert float(one["lam_v"][0]) == float(pooled["lam_v"]) and float(one["lam_k"][0]) == float(pooled["lam_k"])
+    # two heads: every head spends at most its own budget, and its level is the smallest that fits
+    rng = np.random.default_rng(5)
+    g = rng.lognormal(0, 2, (2, 300)).astype(np.float32)
+    wc = rng.lognormal(0, 1, (2, 64)).astype(np.float32)
+    kk = rng.standard_normal((300 + 10, 2, 64)).astype(np.float32)
+    r = O.allocate_per_head(g, wc, kk, 2.5, 2.0)
+    for j in range(2):
+        assert int(r["bits_tok"][j].astype(np.int64).sum()) <= int(np.floor(np.float32(2.5) * 300))
+        assert int(r["bits_chan"][j].astype(np.int64).sum()) <= int(np.floor(np.float32(2.0) * 64))
+        lower = np.nextafter(r["lam_v"][j], np.float32(-1))
+        if r["lam_v"][j] > 0:
+            assert int(O.widths_at(O.breakpoints(g[j]), lower).astype(np.int64).sum()) > int(np.floor(np.float32(2.5) * 300))

@@ -76,7 +76,7 @@ typedef struct rdkv_head_plan {
 /* Head of the device plan buffer.  The buffer continues with
  *   rdkv_head_plan heads[n_heads]                 (heads in (b, j) order)
  *   int16_t slot_channel[n_heads][slot_stride]    (channel of each K slot, -1 = pad)
- *   float lambda_v[batch], lambda_k[batch]        (water levels found)
+ *   float levels[2][batch * h_kv]                 (water levels found; see rdkv_allocate_mode)
  * at the offsets given by the fields below. */
 typedef struct rdkv_plan_header {
   int32_t status;          /* RDKV_OK, or RDKV_ERR_INVALID_ARG if a gain was NaN/inf/negative */
@@ -173,6 +173,42 @@ rdkv_status rdkv_allocate(const rdkv_shape* shape, const float* g_tok, const flo
                           const void* k, float avg_bits_v, float avg_bits_k,
                           uint8_t* bits_tok, float* sigma_chan, float* g_chan, uint8_t* bits_chan,
                           void* plan, void* ws, size_t ws_bytes, void* stream);
+
+/* Allocation variants on the same plan, pack and decode (the RDKV page's
+ * section 2.2 is the method; the others are a different reading of its scope
+ * and two eviction-only baselines the pages compare against).
+ *   RDKV_ALLOC_POOLED    the method, as rdkv_allocate (one water level per
+ *                        sequence for V and one for K);
+ *   RDKV_ALLOC_PER_HEAD  one water level per (sequence, KV head) for V (budget
+ *                        floor(avg_bits_v * N_p) per head) and for K (budget
+ *                        floor(avg_bits_k * D) per head);
+ *   RDKV_ALLOC_TOPK      heavy-hitter eviction (H2O-style): per (sequence, KV
+ *                        head), k = floor(floor(avg_bits_v * N_p) / 16) tokens
+ *                        are affordable at 16 bits; every prefix token whose
+ *                        w_t exceeds lambda, the smallest non-negative level
+ *                        at most k weights exceed, is kept at 16 bits (equal
+ *                        weights at lambda are all dropped); every K channel
+ *                        16 bits;
+ *   RDKV_ALLOC_THRESHOLD eviction by a threshold on the weight (KVzap-style):
+ *                        prefix tokens with w_t > param kept at 16 bits; every
+ *                        K channel 16 bits.
+ * w_tok [B][H_kv][N] (rdkv_score's output; used by TOPK and THRESHOLD),
+ * g_tok [B][H_kv][N_p] (used by POOLED and PER_HEAD); the other arguments as
+ * rdkv_allocate (sigma_chan, g_chan are computed over the kept tokens in every
+ * mode).  Levels in the plan: POOLED: V [B] then K [B]; the other modes:
+ * V [B*H_kv] then K [B*H_kv] (0 for the K stage of TOPK and THRESHOLD, param
+ * for the V stage of THRESHOLD). */
+typedef enum rdkv_alloc_mode {
+  RDKV_ALLOC_POOLED = 0,
+  RDKV_ALLOC_PER_HEAD = 1,
+  RDKV_ALLOC_TOPK = 2,
+  RDKV_ALLOC_THRESHOLD = 3
+} rdkv_alloc_mode;
+rdkv_status rdkv_allocate_mode(const rdkv_shape* shape, int mode, float param, const float* w_tok,
+                               const float* g_tok, const float* w_chan, const void* k,
+                               float avg_bits_v, float avg_bits_k, uint8_t* bits_tok,
+                               float* sigma_chan, float* g_chan, uint8_t* bits_chan,
+                               void* plan, void* ws, size_t ws_bytes, void* stream);
 
 /* Copies the plan totals to the host.  SYNCHRONISES `stream`.  Returns the
  * plan's device status (RDKV_ERR_INVALID_ARG if a gain was invalid). */

@@ -22,7 +22,15 @@
 namespace rdkv {
 
 // Distortion drop per bit of each upgrade 0->2, 2->4, 4->8, 8->16, exact in fp32.
-__constant__ float kSlope[4] = {0.375f, 0.09375f, 0.0146484375f, 255.0f / 524288.0f};
+constexpr float kRdkvSlopes[4] = {0.375f, 0.09375f, 0.0146484375f, 255.0f / 524288.0f};
+// All four breakpoints at the gain itself: a unit goes from 0 straight to 16 bits once its gain
+// passes the level (the keep-or-drop selection of the eviction baselines).
+constexpr float kKeepSlopes[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+
+struct Slopes {
+  float s[4];
+};
+static Slopes slopes_of(const float (&a)[4]) { return Slopes{{a[0], a[1], a[2], a[3]}}; }
 __constant__ uint32_t kStepBits[4] = {2, 2, 4, 8};
 __constant__ uint8_t kWidth[5] = {0, 2, 4, 8, 16};
 
@@ -44,15 +52,16 @@ __global__ void wf_init(WfState* st, unsigned long long* hist, int n_inst, int32
 
 __device__ __forceinline__ bool gain_valid(float g) { return g >= 0.0f && g <= 3.402823466e38f; }
 
-__global__ void wf_hist(const float* __restrict__ g, int64_t n_units, int level, const WfState* __restrict__ st,
-                        unsigned long long* __restrict__ hist, int32_t* status) {
+// g of instance i starts at g + i * in_stride (units contiguous).
+__global__ void wf_hist(const float* __restrict__ g, int64_t n_units, int64_t in_stride, Slopes sl, int level,
+                        const WfState* __restrict__ st, unsigned long long* __restrict__ hist, int32_t* status) {
   __shared__ uint32_t h[256];
   const int inst = blockIdx.y;
   for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const uint32_t prefix = st[inst].prefix;
   const int shift = 24 - 8 * level;
-  const float* gi = g + (int64_t)inst * n_units;
+  const float* gi = g + (int64_t)inst * in_stride;
   bool bad = false;
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)gridDim.x * blockDim.x) {
     const float gv = gi[u];
@@ -62,7 +71,7 @@ __global__ void wf_hist(const float* __restrict__ g, int64_t n_units, int level,
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t p = level_bits(gv * kSlope[k]);
+      const uint32_t p = level_bits(gv * sl.s[k]);
       if (level == 0 || (p >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&h[(p >> shift) & 255u], kStepBits[k]);
     }
   }
@@ -100,26 +109,30 @@ __global__ void wf_select(int level, long long budget, WfState* st, unsigned lon
   hist[inst * 256 + t] = 0;
 }
 
-__global__ void wf_assign(const float* __restrict__ g, int64_t n_units, const WfState* __restrict__ st,
-                          uint8_t* __restrict__ bits, float* __restrict__ lambda_out) {
+__global__ void wf_assign(const float* __restrict__ g, int64_t n_units, int64_t in_stride, Slopes sl,
+                          const WfState* __restrict__ st, uint8_t* __restrict__ bits, float* __restrict__ lambda_out) {
   const int inst = blockIdx.y;
   const uint32_t lam = st[inst].prefix;
   if (lambda_out && blockIdx.x == 0 && threadIdx.x == 0) lambda_out[inst] = __uint_as_float(lam);
-  const float* gi = g + (int64_t)inst * n_units;
+  const float* gi = g + (int64_t)inst * in_stride;
   uint8_t* bi = bits + (int64_t)inst * n_units;
   for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)gridDim.x * blockDim.x) {
     const float gv = gi[u];
     int m = 0;
     if (gain_valid(gv)) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) m += level_bits(gv * kSlope[k]) > lam ? 1 : 0;
+      for (int k = 0; k < 4; ++k) m += level_bits(gv * sl.s[k]) > lam ? 1 : 0;
     }
     bi[u] = kWidth[m];
   }
 }
 
+// One level per instance; instance i's n_units gains start at g + i * in_stride (in_stride = n_units
+// when they are packed), its widths at bits + i * n_units.
 static rdkv_status launch_waterfill(int n_inst, int64_t n_units, const float* g, float avg_bits, uint8_t* bits,
-                                    float* lambda_out, int32_t* status_out, void* ws, cudaStream_t st) {
+                                    float* lambda_out, int32_t* status_out, void* ws, cudaStream_t st,
+                                    int64_t in_stride = -1, Slopes sl = slopes_of(kRdkvSlopes)) {
+  if (in_stride < 0) in_stride = n_units;
   const long long budget = (long long)std::floor((double)avg_bits * (double)n_units);
   auto* state = reinterpret_cast<WfState*>(ws);
   auto* hist = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + align_up((int64_t)n_inst * sizeof(WfState), 16));
@@ -128,14 +141,35 @@ static rdkv_status launch_waterfill(int n_inst, int64_t n_units, const float* g,
   RDKV_CHECK_LAUNCH("waterfill init");
   const int per_inst = (int)std::min<int64_t>(std::max<int64_t>(ceil_div64(n_units, 256 * 16), 1), 512);
   for (int level = 0; level < 4; ++level) {
-    wf_hist<<<dim3(per_inst, n_inst), 256, 0, st>>>(g, n_units, level, state, hist, status);
+    wf_hist<<<dim3(per_inst, n_inst), 256, 0, st>>>(g, n_units, in_stride, sl, level, state, hist, status);
     RDKV_CHECK_LAUNCH("waterfill histogram");
     wf_select<<<n_inst, 256, 0, st>>>(level, budget, state, hist);
     RDKV_CHECK_LAUNCH("waterfill select");
   }
-  wf_assign<<<dim3(per_inst, n_inst), 256, 0, st>>>(g, n_units, state, bits, lambda_out);
+  wf_assign<<<dim3(per_inst, n_inst), 256, 0, st>>>(g, n_units, in_stride, sl, state, bits, lambda_out);
   RDKV_CHECK_LAUNCH("waterfill assign");
   return RDKV_OK;
+}
+
+// Keep-or-drop at a given level: 16 bits for units whose weight exceeds tau, else 0 (invalid
+// weights are flagged and dropped).
+__global__ void keep_above_kernel(const float* __restrict__ w, int64_t n_units, int64_t in_stride, float tau,
+                                  uint8_t* __restrict__ bits, float* __restrict__ lambda_out, int32_t* status) {
+  const int inst = blockIdx.y;
+  if (lambda_out && blockIdx.x == 0 && threadIdx.x == 0) lambda_out[inst] = tau;
+  const float* wi = w + (int64_t)inst * in_stride;
+  uint8_t* bi = bits + (int64_t)inst * n_units;
+  bool bad = false;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)gridDim.x * blockDim.x) {
+    const float x = wi[u];
+    if (!gain_valid(x)) bad = true;
+    bi[u] = (gain_valid(x) && x > tau) ? 16 : 0;
+  }
+  if (bad && status) atomicExch(status, (int32_t)RDKV_ERR_INVALID_ARG);
+}
+
+__global__ void fill_u8_kernel(uint8_t* __restrict__ p, int64_t n, uint8_t v) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) p[i] = v;
 }
 
 // ---------------------------------------------------------------- K channel spread over kept tokens
@@ -343,7 +377,7 @@ static size_t alloc_ws_parts(const rdkv_shape* s, size_t* wf, size_t* part, size
   const int64_t n_heads = (int64_t)s->batch * s->h_kv;
   const int Np = s->n_tokens - s->window;
   const int nchunk = std::max(1, ceil_div(Np, kChanChunk));
-  *wf = align_up(wf_ws_bytes(s->batch), 256);
+  *wf = align_up(wf_ws_bytes(s->batch * s->h_kv), 256);  // up to one instance per (sequence, KV head)
   *part = align_up(n_heads * nchunk * s->head_dim * 4, 256);
   *cnt = align_up(n_heads * nchunk * 4, 256);
   *mean = align_up(n_heads * s->head_dim * 4, 256);
@@ -356,17 +390,23 @@ extern "C" size_t rdkv_allocate_workspace_bytes(const rdkv_shape* s) {
   return alloc_ws_parts(s, &a, &b, &c, &d);
 }
 
-extern "C" rdkv_status rdkv_allocate(const rdkv_shape* s, const float* g_tok, const float* w_chan, const void* k,
-                                     float avg_bits_v, float avg_bits_k, uint8_t* bits_tok, float* sigma_chan,
-                                     float* g_chan, uint8_t* bits_chan, void* plan, void* ws, size_t ws_bytes,
-                                     void* stream) {
+static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, const float* w_tok, const float* g_tok,
+                                 const float* w_chan, const void* k, float avg_bits_v, float avg_bits_k,
+                                 uint8_t* bits_tok, float* sigma_chan, float* g_chan, uint8_t* bits_chan, void* plan,
+                                 void* ws, size_t ws_bytes, void* stream) {
   rdkv_status st = check_shape(s);
   if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(mode >= RDKV_ALLOC_POOLED && mode <= RDKV_ALLOC_THRESHOLD, RDKV_ERR_INVALID_ARG, "unknown allocation mode %d",
+               mode);
   RDKV_REQUIRE(std::isfinite(avg_bits_v) && avg_bits_v >= 0 && std::isfinite(avg_bits_k) && avg_bits_k >= 0,
                RDKV_ERR_INVALID_ARG, "budgets must be finite and >= 0 (v=%f k=%f)", (double)avg_bits_v,
                (double)avg_bits_k);
+  RDKV_REQUIRE(mode != RDKV_ALLOC_THRESHOLD || (std::isfinite(param) && param >= 0), RDKV_ERR_INVALID_ARG,
+               "threshold must be finite and >= 0 (%f)", (double)param);
   const int Np = s->n_tokens - s->window;
-  RDKV_REQUIRE(w_chan && k && bits_chan && sigma_chan && g_chan && plan && (Np == 0 || (g_tok && bits_tok)),
+  const bool by_weight = mode == RDKV_ALLOC_TOPK || mode == RDKV_ALLOC_THRESHOLD;
+  RDKV_REQUIRE(w_chan && k && bits_chan && sigma_chan && g_chan && plan && (Np == 0 || bits_tok) &&
+                   (Np == 0 || (by_weight ? w_tok != nullptr : g_tok != nullptr)),
                RDKV_ERR_INVALID_ARG, "NULL pointer argument");
   size_t wf_b, part_b, cnt_b, mean_b;
   const size_t need = alloc_ws_parts(s, &wf_b, &part_b, &cnt_b, &mean_b);
@@ -383,16 +423,29 @@ extern "C" rdkv_status rdkv_allocate(const rdkv_shape* s, const float* g_tok, co
   float* lam = reinterpret_cast<float*>(pl + L.lambda_off);
   const int D = s->head_dim;
   const int n_heads = s->batch * s->h_kv;
+  // levels: pooled: V [batch] then K [batch]; the other modes: V [n_heads] then K [n_heads]
+  const int n_lev = mode == RDKV_ALLOC_POOLED ? s->batch : n_heads;
 
-  // step 2: V tokens, one water level per sequence over all its heads
+  // step 2: V tokens
   RDKV_TRY_CUDA(cudaMemsetAsync(status, 0, 8, cs), "status reset");
   if (Np > 0) {
-    st = launch_waterfill(s->batch, (int64_t)s->h_kv * Np, g_tok, avg_bits_v, bits_tok, lam, status, wf, cs);
+    if (mode == RDKV_ALLOC_POOLED) {  // one water level per sequence over all its heads
+      st = launch_waterfill(s->batch, (int64_t)s->h_kv * Np, g_tok, avg_bits_v, bits_tok, lam, status, wf, cs);
+    } else if (mode == RDKV_ALLOC_PER_HEAD) {  // one water level per (sequence, KV head)
+      st = launch_waterfill(n_heads, Np, g_tok, avg_bits_v, bits_tok, lam, status, wf, cs);
+    } else if (mode == RDKV_ALLOC_TOPK) {  // keep-or-drop on w_t, at most floor(B / 16) kept per head
+      st = launch_waterfill(n_heads, Np, w_tok, avg_bits_v, bits_tok, lam, status, wf, cs, s->n_tokens,
+                            slopes_of(kKeepSlopes));
+    } else {  // keep w_t > threshold
+      const int per = (int)std::min<int64_t>(std::max<int64_t>(ceil_div64(Np, 256 * 16), 1), 512);
+      keep_above_kernel<<<dim3(per, n_heads), 256, 0, cs>>>(w_tok, Np, s->n_tokens, param, bits_tok, lam, status);
+      RDKV_CHECK_LAUNCH("keep above threshold");
+    }
     if (st != RDKV_OK) return st;
   } else {
-    RDKV_TRY_CUDA(cudaMemsetAsync(lam, 0, 4 * s->batch, cs), "lambda reset");
+    RDKV_TRY_CUDA(cudaMemsetAsync(lam, 0, 4 * (size_t)n_lev, cs), "lambda reset");
   }
-  // step 3: K channel spread over the kept tokens, gains, water level
+  // step 3: K channel spread over the kept tokens, gains, widths
   const int nchunk = std::max(1, ceil_div(Np, kChanChunk));
   if (Np > 0) {
     chan_pass<<<dim3(nchunk, n_heads), D, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np, nullptr, part,
@@ -409,8 +462,16 @@ extern "C" rdkv_status rdkv_allocate(const rdkv_shape* s, const float* g_tok, co
     RDKV_TRY_CUDA(cudaMemsetAsync(sigma_chan, 0, 4 * (size_t)n_heads * D, cs), "sigma reset");
     RDKV_TRY_CUDA(cudaMemsetAsync(g_chan, 0, 4 * (size_t)n_heads * D, cs), "gain reset");
   }
-  st = launch_waterfill(s->batch, (int64_t)s->h_kv * D, g_chan, avg_bits_k, bits_chan, lam + s->batch, status + 1,
-                        wf, cs);
+  if (mode == RDKV_ALLOC_POOLED) {
+    st = launch_waterfill(s->batch, (int64_t)s->h_kv * D, g_chan, avg_bits_k, bits_chan, lam + n_lev, status + 1,
+                          wf, cs);
+  } else if (mode == RDKV_ALLOC_PER_HEAD) {
+    st = launch_waterfill(n_heads, D, g_chan, avg_bits_k, bits_chan, lam + n_lev, status + 1, wf, cs);
+  } else {  // eviction baselines keep every K channel of the kept tokens at 16 bits
+    fill_u8_kernel<<<ceil_div(n_heads * D, 256), 256, 0, cs>>>(bits_chan, (int64_t)n_heads * D, 16);
+    RDKV_CHECK_LAUNCH("all channels 16 bits");
+    RDKV_TRY_CUDA(cudaMemsetAsync(lam + n_lev, 0, 4 * (size_t)n_lev, cs), "lambda reset");
+  }
   if (st != RDKV_OK) return st;
   // TriZone plan
   plan_heads_kernel<<<n_heads, 256, 0, cs>>>(bits_tok, bits_chan, Np, D, pl, L.heads_off, L.slots_off, L.slot_stride);
@@ -419,6 +480,22 @@ extern "C" rdkv_status rdkv_allocate(const rdkv_shape* s, const float* g_tok, co
                                         L.lambda_off, status, status + 1);
   RDKV_CHECK_LAUNCH("plan offsets");
   return RDKV_OK;
+}
+
+extern "C" rdkv_status rdkv_allocate(const rdkv_shape* s, const float* g_tok, const float* w_chan, const void* k,
+                                     float avg_bits_v, float avg_bits_k, uint8_t* bits_tok, float* sigma_chan,
+                                     float* g_chan, uint8_t* bits_chan, void* plan, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  return allocate_impl(s, RDKV_ALLOC_POOLED, 0.f, nullptr, g_tok, w_chan, k, avg_bits_v, avg_bits_k, bits_tok,
+                       sigma_chan, g_chan, bits_chan, plan, ws, ws_bytes, stream);
+}
+
+extern "C" rdkv_status rdkv_allocate_mode(const rdkv_shape* s, int mode, float param, const float* w_tok,
+                                          const float* g_tok, const float* w_chan, const void* k, float avg_bits_v,
+                                          float avg_bits_k, uint8_t* bits_tok, float* sigma_chan, float* g_chan,
+                                          uint8_t* bits_chan, void* plan, void* ws, size_t ws_bytes, void* stream) {
+  return allocate_impl(s, mode, param, w_tok, g_tok, w_chan, k, avg_bits_v, avg_bits_k, bits_tok, sigma_chan, g_chan,
+                       bits_chan, plan, ws, ws_bytes, stream);
 }
 
 extern "C" rdkv_status rdkv_plan_sizes(const void* plan, rdkv_sizes* out, void* stream) {

@@ -35,7 +35,7 @@ __host__ __device__ inline PlanLayout plan_layout(int batch, int h_kv, int head_
   L.heads_off = align_up(sizeof(rdkv_plan_header), 128);
   L.slots_off = align_up(L.heads_off + n_heads * (int64_t)sizeof(rdkv_head_plan), 128);
   L.lambda_off = align_up(L.slots_off + n_heads * L.slot_stride * 2, 128);
-  L.total = align_up(L.lambda_off + 2 * (int64_t)batch * 4, 256);
+  L.total = align_up(L.lambda_off + 2 * n_heads * 4, 256);  // room for one level per (sequence, KV head)
   return L;
 }
 

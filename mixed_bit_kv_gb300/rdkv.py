@@ -17,12 +17,13 @@ LIB_PATH = os.path.join(_HERE, "librdkv.so")
 RDKV_OK, RDKV_ERR_INVALID_ARG, RDKV_ERR_UNSUPPORTED, RDKV_ERR_CAPACITY = 0, 1, 2, 3
 RDKV_ERR_CUDA, RDKV_ERR_TIMEOUT, RDKV_ERR_WORKSPACE = 4, 5, 6
 RDKV_F16, RDKV_F32 = 0, 1
+RDKV_ALLOC_POOLED, RDKV_ALLOC_PER_HEAD, RDKV_ALLOC_TOPK, RDKV_ALLOC_THRESHOLD = 0, 1, 2, 3
 
 EXPORTED = (
     "rdkv_last_error_string", "rdkv_version", "rdkv_launch_count",
     "rdkv_score_workspace_bytes", "rdkv_score",
     "rdkv_waterfill_workspace_bytes", "rdkv_waterfill",
-    "rdkv_plan_bytes", "rdkv_allocate_workspace_bytes", "rdkv_allocate", "rdkv_plan_sizes",
+    "rdkv_plan_bytes", "rdkv_allocate_workspace_bytes", "rdkv_allocate", "rdkv_allocate_mode", "rdkv_plan_sizes",
     "rdkv_pack", "rdkv_append",
     "rdkv_decode_workspace_bytes", "rdkv_decode_attn", "rdkv_decode_step", "rdkv_decode_status",
     "rdkv_decode_attn_noalloc",
@@ -87,6 +88,8 @@ def lib():
             "rdkv_allocate_workspace_bytes": (ctypes.c_size_t, [sp]),
             "rdkv_allocate": (ctypes.c_int, [sp, _P, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P, _P, _P, _P, _P,
                                              ctypes.c_size_t, _P]),
+            "rdkv_allocate_mode": (ctypes.c_int, [sp, ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, ctypes.c_float,
+                                                  ctypes.c_float, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_plan_sizes": (ctypes.c_int, [_P, szp, _P]),
             "rdkv_pack": (ctypes.c_int, [cp, _P, _P, _P, _P, _P]),
             "rdkv_append": (ctypes.c_int, [cp, _P, _P, _P]),
@@ -182,6 +185,25 @@ def rdkv_allocate(shape, g_tok, w_chan, k, avg_bits_v, avg_bits_k, stream=None, 
     _check(L.rdkv_allocate(ctypes.byref(shape), _ptr(g_tok), _ptr(w_chan), _ptr(k), float(avg_bits_v),
                            float(avg_bits_k), _ptr(out["bits_tok"]), _ptr(out["sigma_chan"]), _ptr(out["g_chan"]),
                            _ptr(out["bits_chan"]), _ptr(out["plan"]), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def rdkv_allocate_mode(shape, mode, w_tok, g_tok, w_chan, k, avg_bits_v, avg_bits_k, param=0.0, stream=None):
+    """Allocation variant `mode` (RDKV_ALLOC_*): outputs as rdkv_allocate."""
+    dev = k.device
+    B, Hkv, D = shape.batch, shape.h_kv, shape.head_dim
+    Np = shape.n_tokens - shape.window
+    L = lib()
+    out = dict(bits_tok=torch.empty(B, Hkv, max(Np, 0), dtype=torch.uint8, device=dev),
+               sigma_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+               g_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+               bits_chan=torch.empty(B, Hkv, D, dtype=torch.uint8, device=dev),
+               plan=torch.zeros(L.rdkv_plan_bytes(ctypes.byref(shape)), dtype=torch.uint8, device=dev))
+    ws = _ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), dev)
+    _check(L.rdkv_allocate_mode(ctypes.byref(shape), int(mode), float(param), _ptr(w_tok), _ptr(g_tok), _ptr(w_chan),
+                                _ptr(k), float(avg_bits_v), float(avg_bits_k), _ptr(out["bits_tok"]),
+                                _ptr(out["sigma_chan"]), _ptr(out["g_chan"]), _ptr(out["bits_chan"]), _ptr(out["plan"]),
+                                _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 
@@ -284,5 +306,6 @@ def read_plan(plan):
     heads = np.frombuffer(raw.tobytes(), dtype=np.dtype(HEAD_PLAN_DTYPE), count=n, offset=int(hdr["heads_off"]))
     slots = np.frombuffer(raw.tobytes(), dtype="<i2", count=n * int(hdr["slot_stride"]),
                           offset=int(hdr["slots_off"])).reshape(n, int(hdr["slot_stride"]))
-    lam = np.frombuffer(raw.tobytes(), dtype="<f4", count=2 * int(hdr["batch"]), offset=int(hdr["lambda_off"]))
+    lam = np.frombuffer(raw.tobytes(), dtype="<f4", count=2 * int(hdr["batch"]) * int(hdr["h_kv"]),
+                        offset=int(hdr["lambda_off"]))
     return hdr, heads, slots, lam

@@ -117,3 +117,18 @@ def test_binding_cache_object_on_host_memory(L):
     assert ws.numel() >= L.rdkv_decode_workspace_bytes(ctypes.byref(c.c)) > 0
     assert c.decode_workspace() is ws
     assert c.fits(sizes) and not c.fits(rdkv.Sizes(1 << 30, 64, 256, 200, 2048, 2048, 0, 4))
+
+
+def test_allocate_mode_argument_checks(L):
+    s = rdkv.make_shape(1, 1024, 4, 1, 64, 32, "f32")
+    fake = ctypes.c_void_p(256)
+    f = ctypes.c_float
+    r = L.rdkv_allocate_mode(ctypes.byref(s), 7, f(0), fake, fake, fake, fake, f(2), f(2), fake, fake, fake, fake,
+                             fake, fake, 1 << 30, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG and b"mode" in L.rdkv_last_error_string()
+    r = L.rdkv_allocate_mode(ctypes.byref(s), rdkv.RDKV_ALLOC_TOPK, f(0), None, fake, fake, fake, f(2), f(2), fake,
+                             fake, fake, fake, fake, fake, 1 << 30, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+    r = L.rdkv_allocate_mode(ctypes.byref(s), rdkv.RDKV_ALLOC_THRESHOLD, f(float("nan")), fake, fake, fake, fake, f(2),
+                             f(2), fake, fake, fake, fake, fake, fake, 1 << 30, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG

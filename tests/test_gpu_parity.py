@@ -300,3 +300,72 @@ def test_decode_step_past_capacity_on_the_device():
     assert torch.equal(cache.zone_c_k, before)
     assert rdkv.rdkv_decode_status(cache) == rdkv.RDKV_ERR_CAPACITY
     assert rdkv.rdkv_decode_status(cache) == 0  # read and cleared
+
+
+# ---------------------------------------------------------------- allocation variants
+@pytest.mark.parametrize("case", ["small_f16", "zipf_f16", "tiny_f32"])
+@pytest.mark.parametrize("mode", ["per_head", "topk", "threshold"])
+def test_allocation_modes_match_oracle(case, mode):
+    """Variants on the same plan, pack and decode: widths and levels bit-exact given the same
+    weights, then the packed bytes and the decode against the oracle."""
+    w = CASES[case]
+    avg = w.budgets[0]
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    shape = rdkv.shape_of(qd, kd, w.window)
+    sc = rdkv.rdkv_score(shape, qd, kd, vd)
+    Np = w.n_tokens - w.window
+    w_tok = sc["w_tok"].cpu().numpy()
+    tau = float(np.float32(np.median(w_tok[:, :, :Np])))
+    code = {"per_head": rdkv.RDKV_ALLOC_PER_HEAD, "topk": rdkv.RDKV_ALLOC_TOPK,
+            "threshold": rdkv.RDKV_ALLOC_THRESHOLD}[mode]
+    al = rdkv.rdkv_allocate_mode(shape, code, sc["w_tok"], sc["g_tok"], sc["w_chan"], kd, avg, avg, param=tau)
+    hdr, heads, slots, lam = rdkv.read_plan(al["plan"])
+    bits_tok = al["bits_tok"].cpu().numpy()
+    bits_chan = al["bits_chan"].cpu().numpy()
+    H = w.h_kv
+    for b in range(w.batch):
+        if mode == "per_head":
+            r = O.allocate_per_head(sc["g_tok"][b].cpu().numpy(), sc["w_chan"][b].cpu().numpy(), k[b].numpy(), avg, avg)
+            # identical V widths -> identical kept sets -> spreads within float rounding; K widths
+            # are compared given the library's own channel gains
+            assert np.array_equal(bits_tok[b], r["bits_tok"])
+            assert np.array_equal(lam[b * H:(b + 1) * H], r["lam_v"])
+            for j in range(H):
+                rb, rl = O.waterfill(al["g_chan"][b, j].cpu().numpy(), avg)
+                assert np.array_equal(bits_chan[b, j], rb) and float(lam[w.batch * H + b * H + j]) == float(rl)
+        else:
+            for j in range(H):
+                wj = w_tok[b, j, :Np]
+                if mode == "topk":
+                    rb, rl = O.topk_keep(wj, avg)
+                else:
+                    rb, rl = O.threshold_keep(wj, tau), np.float32(tau)
+                assert np.array_equal(bits_tok[b, j], rb), (b, j)
+                assert float(lam[b * H + j]) == float(rl)
+            assert np.all(bits_chan[b] == 16)
+    plan = O.make_plan(bits_tok, bits_chan, w.head_dim)
+    for key in ("zone_a_bytes", "zone_b_rows", "index_slots", "kept_tokens"):
+        assert int(hdr[key]) == plan[key], key
+    sizes = rdkv.rdkv_plan_sizes(al["plan"])
+    steps = 3
+    cache = rdkv.rdkv_pack(shape, al["plan"], kd, vd, al["bits_tok"], al["bits_chan"], w.window + steps, sizes=sizes)
+    ref = O.pack(k.numpy(), v.numpy(), bits_tok, bits_chan, w.window, cap_c=w.window + steps)
+    torch.cuda.synchronize()
+    assert np.array_equal(cache.zone_a.cpu().numpy()[: ref["zone_a"].size], ref["zone_a"])
+    un = O.unpack(ref, w.head_dim)
+    for step in range(steps):
+        qn, kn, vn = synth.decode_step(w, step)
+        out = rdkv.rdkv_decode_step(cache, qn.to(DEV), kn.to(DEV), vn.to(DEV)).cpu().numpy()
+        O.append(ref, kn.numpy(), vn.numpy())
+        assert np.abs(out - O.decode(ref, qn.numpy(), unpacked=un)).max() <= 2e-3, (mode, step)
+
+
+def test_pooled_mode_equals_rdkv_allocate():
+    w = CASES["small_f16"]
+    (q, k, v), (qd, kd, vd) = _inputs(w)
+    shape = rdkv.shape_of(qd, kd, w.window)
+    sc = rdkv.rdkv_score(shape, qd, kd, vd)
+    a = rdkv.rdkv_allocate(shape, sc["g_tok"], sc["w_chan"], kd, 2.5, 2.0)
+    b = rdkv.rdkv_allocate_mode(shape, rdkv.RDKV_ALLOC_POOLED, None, sc["g_tok"], sc["w_chan"], kd, 2.5, 2.0)
+    for key in ("bits_tok", "bits_chan", "plan"):
+        assert torch.equal(a[key], b[key]), key

@@ -26,12 +26,13 @@ namespace rdkv {
 
 namespace tc {
 
-constexpr int kRows = 128;       // rows of A, rows of a streamed tile
-constexpr int kStages = 4;       // TMA ring depth
-constexpr int kAcc = 4;          // TMEM accumulators (4 x 128 columns: all of tensor memory)
+constexpr int kRows = 128;       // rows of A (the stationary block)
+constexpr int kCols = 256;       // rows of a streamed B tile = columns of a tile product (MMA N)
+constexpr int kStages = 2;       // TMA ring depth (2 x 64 KB of B tiles)
+constexpr int kAcc = 2;          // TMEM accumulators (2 x 256 columns: all of tensor memory)
 constexpr int kEpiWarps = 16;                 // epilogue warps: 4 per TMEM lane quarter
 constexpr int kSlices = kEpiWarps / 4;        // column slices of the accumulator
-constexpr int kSliceCols = 128 / kSlices;     // columns per epilogue warp (multiple of 32)
+constexpr int kSliceCols = kCols / kSlices;   // columns per epilogue warp (multiple of 32)
 constexpr int kThreads = 64 + 32 * kEpiWarps; // producer, MMA, epilogue warps
 constexpr long long kWait = 4000000000ll;
 
@@ -81,7 +82,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
          ((uint64_t)2 << 61);
 }
 // Instruction descriptor: fp32 accumulate, fp16 A and B, both K-major, M = N = 128.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kRows >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kCols >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -136,12 +137,13 @@ template <int D, int PASS>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB, Params P) {
   constexpr int kHalves = D / 64;                 // 64-element (128-byte) column halves of a row
-  constexpr uint32_t kTileBytes = kRows * D * 2;  // one 128-row tile
+  constexpr uint32_t kTileBytes = kRows * D * 2;   // the A block (128 rows)
+  constexpr uint32_t kBTileBytes = kCols * D * 2;  // one streamed B tile (256 rows)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* As = sm;
-  uint8_t* Bs = sm + kTileBytes;                           // [kStages][tile]
-  float* lse_s = reinterpret_cast<float*>(Bs + kStages * kTileBytes);  // [kAcc][128] (pass 2)
+  uint8_t* Bs = sm + kTileBytes;                           // [kStages][B tile]
+  float* lse_s = reinterpret_cast<float*>(Bs + kStages * kBTileBytes);  // [kAcc][kCols] (pass 2)
   __shared__ uint64_t bar_a, full[kStages], empty[kStages], tfull[kAcc], tempty[kAcc], lfull[kAcc], lempty[kAcc];
   __shared__ uint32_t tmem_base;
   __shared__ int failed;
@@ -151,19 +153,22 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   // pass 1: A = queries of head h = blockIdx.y, block qb; pass 2: A = keys of KV head j = blockIdx.y, block kb
   const int blk = PASS == 1 ? P.n_blk - 1 - (int)blockIdx.x : (int)blockIdx.x;  // heaviest blocks first
   const int row0 = blk * kRows;
-  const int n_tiles = PASS == 1 ? blk + 1 : P.G * (P.n_blk - blk);
+  // pass 1: key tiles [i kCols, (i+1) kCols) up to the block's last row; pass 2: per head of the
+  // group, query tiles from the block's first key on
+  const int nt2 = ceil_div(P.N - row0, kCols);
+  const int n_tiles = PASS == 1 ? ceil_div(row0 + kRows, kCols) : P.G * nt2;
   auto tile_of = [&](int i, int& head, int& t0) {
     if (PASS == 1) {
       head = blockIdx.y / P.G;   // KV head of query head blockIdx.y
-      t0 = i * kRows;
+      t0 = i * kCols;
     } else {
-      head = blockIdx.y * P.G + i / (P.n_blk - blk);
-      t0 = (blk + i % (P.n_blk - blk)) * kRows;
+      head = blockIdx.y * P.G + i / nt2;
+      t0 = row0 + (i % nt2) * kCols;
     }
   };
 
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)), "n"(kAcc * kRows));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)), "n"(kAcc * kCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 32) {
@@ -197,14 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         if (!mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1)) { failed = 1; break; }
         int head, t0;
         tile_of(i, head, t0);
-        mbar_expect(&full[s], kTileBytes);
+        mbar_expect(&full[s], kBTileBytes);
         for (int hh = 0; hh < kHalves; ++hh)
-          tma4(Bs + s * kTileBytes + hh * kRows * 128, &tmB, 64 * hh, head, t0, b, &full[s]);
+          tma4(Bs + s * kBTileBytes + hh * kCols * 128, &tmB, 64 * hh, head, t0, b, &full[s]);
         if (PASS == 2) {
           const int t = i % kAcc;
           if (!mbar_wait(&lempty[t], ((i / kAcc) & 1) ^ 1)) { failed = 1; break; }
-          mbar_expect(&lfull[t], kRows * 4);
-          bulk_g2s(lse_s + t * kRows, P.lse2 + ((int64_t)b * P.h_q + head) * P.lse_stride + t0, kRows * 4, &lfull[t]);
+          mbar_expect(&lfull[t], kCols * 4);
+          bulk_g2s(lse_s + t * kCols, P.lse2 + ((int64_t)b * P.h_q + head) * P.lse_stride + t0, kCols * 4, &lfull[t]);
         }
       }
     }
@@ -217,14 +222,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         if (!mbar_wait(&full[s], (i / kStages) & 1)) { failed = 1; break; }
         if (!mbar_wait(&tempty[t], ((i / kAcc) & 1) ^ 1)) { failed = 1; break; }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a0 = su32(As), b0 = su32(Bs + s * kTileBytes);
+        const uint32_t a0 = su32(As), b0 = su32(Bs + s * kBTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (uint32_t)((k >> 2) * kRows * 128 + (k & 3) * 32);
-          const uint64_t ad = sdesc(a0 + off), bd = sdesc(b0 + off);
+          // 64-column halves of a row are separate swizzled blocks: +16 KB (A) / +32 KB (B) per half
+          const uint32_t ka = (uint32_t)((k >> 2) * kRows * 128 + (k & 3) * 32);
+          const uint32_t kb = (uint32_t)((k >> 2) * kCols * 128 + (k & 3) * 32);
+          const uint64_t ad = sdesc(a0 + ka), bd = sdesc(b0 + kb);
           asm volatile(
               "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::
-                  "r"(tmem + (uint32_t)(t * kRows)),
+                  "r"(tmem + (uint32_t)(t * kCols)),
               "l"(ad), "l"(bd), "r"(kIdesc), "r"(k > 0 ? 1u : 0u));
         }
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       int head, t0;
       tile_of(i, head, t0);
-      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t * kRows + colh * kSliceCols);
+      const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(t * kCols + colh * kSliceCols);
 #pragma unroll
       for (int ch = 0; ch < kSliceCols / 32; ++ch) {
         float v[32];
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           // valid keys: c <= row (c < N follows for rows < N); only the diagonal tile needs the mask.
           // The max is taken on raw logits (c > 0) and the scale folded into one FMA per element.
           float mx = -INFINITY;
-          if (t0 + kRows <= row0) {
+          if (t0 + kCols <= row0) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) mx = fmaxf(mx, v[e]);
           } else {
@@ -288,9 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
             m = mn;
           }
         } else {
-          const float4* ls4 = reinterpret_cast<const float4*>(lse_s + t * kRows + colh * kSliceCols + ch * 32);
+          const float4* ls4 = reinterpret_cast<const float4*>(lse_s + t * kCols + colh * kSliceCols + ch * 32);
           float a0 = 0.f, a1 = 0.f;
-          if (t0 != row0 && t0 + kRows <= P.N) {  // no causal edge and no tail in this tile
+          if (t0 != row0 && t0 + kCols <= P.N) {  // no causal edge and no tail in this tile
             // the staged values are -lse2: 2^(v c - lse2) = 2^(fma(v, c, -lse2)), paired
             const float2 cc = make_float2(P.c, P.c);
             float2 p0 = make_float2(0.f, 0.f), p1 = p0;
@@ -367,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kAcc * kRows));
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kAcc * kCols));
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -386,13 +393,13 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [B][N][H][D] fp16 tensor, 128-row x 64-column boxes with the 128-byte swizzle.
-static rdkv_status make_map(CUtensorMap* m, const void* base, int B, int N, int H, int D) {
+// [B][N][H][D] fp16 tensor, `rows`-row x 64-column boxes with the 128-byte swizzle.
+static rdkv_status make_map(CUtensorMap* m, const void* base, int B, int N, int H, int D, int rows) {
   EncodeTiledFn enc = encode_fn();
   RDKV_REQUIRE(enc != nullptr, RDKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)N * H * D * 2};
-  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kRows, 1};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -403,16 +410,17 @@ static rdkv_status make_map(CUtensorMap* m, const void* base, int B, int N, int 
 
 template <int D>
 static size_t smem_bytes() {
-  return 1024 + (size_t)(1 + kStages) * kRows * D * 2 + kAcc * kRows * 4;
+  return 1024 + (size_t)kRows * D * 2 + (size_t)kStages * kCols * D * 2 + kAcc * kCols * 4;
 }
 
 template <int D>
 static rdkv_status launch(const rdkv_shape* s, const void* q, const void* k, const float* sigma, float* lse2,
                           int lse_stride, float* w_tok, float* g_tok, cudaStream_t st) {
-  CUtensorMap mq, mk;
-  rdkv_status e = make_map(&mq, q, s->batch, s->n_tokens, s->h_q, D);
-  if (e != RDKV_OK) return e;
-  e = make_map(&mk, k, s->batch, s->n_tokens, s->h_kv, D);
+  CUtensorMap mqa, mqb, mka, mkb;  // 128-row boxes (stationary A) and 256-row boxes (streamed B)
+  rdkv_status e = make_map(&mqa, q, s->batch, s->n_tokens, s->h_q, D, kRows);
+  if (e == RDKV_OK) e = make_map(&mqb, q, s->batch, s->n_tokens, s->h_q, D, kCols);
+  if (e == RDKV_OK) e = make_map(&mka, k, s->batch, s->n_tokens, s->h_kv, D, kRows);
+  if (e == RDKV_OK) e = make_map(&mkb, k, s->batch, s->n_tokens, s->h_kv, D, kCols);
   if (e != RDKV_OK) return e;
   Params P;
   P.N = s->n_tokens;
@@ -436,17 +444,18 @@ static rdkv_status launch(const rdkv_shape* s, const void* q, const void* k, con
                   "score smem");
     attr_set[0] = attr_set[1] = true;
   }
-  score_kernel<D, 1><<<dim3(P.n_blk, s->h_q, s->batch), kThreads, smem, st>>>(mq, mk, P);
+  score_kernel<D, 1><<<dim3(P.n_blk, s->h_q, s->batch), kThreads, smem, st>>>(mqa, mkb, P);
   RDKV_CHECK_LAUNCH("row log-sum-exp (tensor cores)");
-  score_kernel<D, 2><<<dim3(P.n_blk, s->h_kv, s->batch), kThreads, smem, st>>>(mk, mq, P);
+  score_kernel<D, 2><<<dim3(P.n_blk, s->h_kv, s->batch), kThreads, smem, st>>>(mka, mqb, P);
   RDKV_CHECK_LAUNCH("attention column sums (tensor cores)");
   return RDKV_OK;
 }
 
 }  // namespace tc
 
-// Row stride of the lse workspace: the last tile of a row may read up to 128 values past N.
-int score_tc_lse_stride(int n_tokens) { return ceil_div(n_tokens, tc::kRows) * tc::kRows; }
+// Row stride of the lse workspace: a streamed tile starts at a multiple of 128 below N and stages
+// kCols values, up to 128 past the rounded-up length.
+int score_tc_lse_stride(int n_tokens) { return ceil_div(n_tokens, tc::kRows) * tc::kRows + (tc::kCols - tc::kRows); }
 
 rdkv_status launch_score_tc(const rdkv_shape* s, const void* q, const void* k, const float* sigma, float* lse2,
                             float* w_tok, float* g_tok, cudaStream_t st) {

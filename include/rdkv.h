@@ -136,7 +136,8 @@ uint64_t rdkv_launch_count(void);
  * q [B][N][H_q][D], k, v [B][N][H_kv][D] in shape->dtype.  Outputs fp32:
  * w_tok, sigma_tok [B][H_kv][N], w_chan [B][H_kv][D], g_tok [B][H_kv][N_p].
  * Supported: D in {64, 128}, 1 <= G <= 8.  fp16 inputs use tensor cores with
- * fp32 accumulation; fp32 inputs use fp32 CUDA-core arithmetic. */
+ * fp32 accumulation; fp32 inputs use fp32 CUDA-core arithmetic.  q, k, v must
+ * be 16-byte aligned (RDKV_ERR_INVALID_ARG otherwise). */
 size_t rdkv_score_workspace_bytes(const rdkv_shape* shape);
 rdkv_status rdkv_score(const rdkv_shape* shape, const void* q, const void* k, const void* v,
                        float* w_tok, float* w_chan, float* sigma_tok, float* g_tok,

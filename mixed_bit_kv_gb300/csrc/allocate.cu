@@ -189,9 +189,29 @@ __global__ void chan_pass(const void* __restrict__ k, const uint8_t* __restrict_
   const float m = mean ? mean[head * D + c] : 0.0f;
   float acc = 0.0f;
   int cnt = 0;
-  for (int t = t0; t < t1; ++t) {
+  // branch-free, eight tokens per step so that their loads are in flight together; the tokens are
+  // taken in order, so the sum is the same as one token at a time
+  const int64_t row = (int64_t)h_kv * D;
+  const int64_t base = (((int64_t)b * N) * h_kv + j) * D + c;
+  int t = t0;
+  for (; t + 8 <= t1; t += 8) {
+    float x[8];
+    bool keep[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      keep[u] = bt[t + u] != 0;
+      x[u] = load_as_float(k, base + (int64_t)(t + u) * row, dtype);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float d = x[u] - m;
+      acc += keep[u] ? (mean ? d * d : x[u]) : 0.0f;
+      cnt += keep[u] ? 1 : 0;
+    }
+  }
+  for (; t < t1; ++t) {
     if (bt[t] == 0) continue;
-    const float x = load_as_float(k, (((int64_t)b * N + t) * h_kv + j) * D + c, dtype);
+    const float x = load_as_float(k, base + (int64_t)t * row, dtype);
     const float d = x - m;
     acc += mean ? d * d : x;
     ++cnt;
@@ -203,12 +223,24 @@ __global__ void chan_pass(const void* __restrict__ k, const uint8_t* __restrict_
 __global__ void chan_finish(const float* __restrict__ part, const int* __restrict__ part_cnt, int nchunk, int D,
                             float* __restrict__ mean_out, const float* __restrict__ w_chan,
                             float* __restrict__ sigma_out, float* __restrict__ g_out) {
-  const int head = blockIdx.x, c = threadIdx.x;
+  // thread (r, c) sums the chunks r, r + R, r + 2R, ... of channel c; the R sums are combined in a
+  // fixed order (deterministic)
+  __shared__ double ssum[1024];
+  __shared__ long long scnt[1024];
+  const int head = blockIdx.x, c = threadIdx.x % D, r = threadIdx.x / D, R = blockDim.x / D;
   double s = 0.0;
   long long n = 0;
-  for (int i = 0; i < nchunk; ++i) {
+  for (int i = r; i < nchunk; i += R) {
     s += (double)part[((int64_t)head * nchunk + i) * D + c];
     n += part_cnt[head * nchunk + i];
+  }
+  ssum[threadIdx.x] = s;
+  scnt[threadIdx.x] = n;
+  __syncthreads();
+  if (r != 0) return;
+  for (int rr = 1; rr < R; ++rr) {
+    s += ssum[rr * D + c];
+    n += scnt[rr * D + c];
   }
   if (mean_out) {
     mean_out[head * D + c] = n ? (float)(s / (double)n) : 0.0f;
@@ -451,12 +483,12 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
     chan_pass<<<dim3(nchunk, n_heads), D, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np, nullptr, part,
                                                    pcnt);
     RDKV_CHECK_LAUNCH("channel sums");
-    chan_finish<<<n_heads, D, 0, cs>>>(part, pcnt, nchunk, D, mean, nullptr, nullptr, nullptr);
+    chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, mean, nullptr, nullptr, nullptr);
     RDKV_CHECK_LAUNCH("channel means");
     chan_pass<<<dim3(nchunk, n_heads), D, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np, mean, part,
                                                    nullptr);
     RDKV_CHECK_LAUNCH("channel deviations");
-    chan_finish<<<n_heads, D, 0, cs>>>(part, pcnt, nchunk, D, nullptr, w_chan, sigma_chan, g_chan);
+    chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, nullptr, w_chan, sigma_chan, g_chan);
     RDKV_CHECK_LAUNCH("channel spread");
   } else {
     RDKV_TRY_CUDA(cudaMemsetAsync(sigma_chan, 0, 4 * (size_t)n_heads * D, cs), "sigma reset");

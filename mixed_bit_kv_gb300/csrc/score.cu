@@ -24,29 +24,64 @@ constexpr int kSTile = 32;      // query rows / keys per block in the CUDA-core 
 constexpr int kColChunk = 256;  // rows per partial column sum
 
 // ---------------------------------------------------------------- sigma of V rows: one warp per row
-__global__ void value_spread_kernel(const void* __restrict__ v, int dtype, int64_t n_rows, int h_kv, int N, int D,
-                                    float* __restrict__ sigma) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // (b, t, j) flattened
-  if (row >= n_rows) return;
-  float x[4];
-  const int per = D / 32;
-  float s = 0.f;
-  for (int i = 0; i < per; ++i) {
-    x[i] = load_as_float(v, row * D + lane + 32 * i, dtype);
-    s += x[i];
+// sigma of V rows: a warp takes kSpreadRows rows; lane l holds the D/32 consecutive elements
+// [l D/32, (l+1) D/32) of a row, loaded as one vector, so every row is one load per lane and a
+// warp keeps kSpreadRows loads in flight.
+constexpr int kSpreadRows = 8;
+template <typename T, int PER>
+__device__ __forceinline__ void load_row_part(const T* __restrict__ p, float (&x)[PER]) {
+  if constexpr (sizeof(T) == 2) {
+    if constexpr (PER == 4) {
+      const uint2 r = *reinterpret_cast<const uint2*>(p);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+      x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    } else {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
+      x[0] = a.x; x[1] = a.y;
+    }
+  } else {
+    if constexpr (PER == 4) {
+      const float4 r = *reinterpret_cast<const float4*>(p);
+      x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
+    } else {
+      const float2 r = *reinterpret_cast<const float2*>(p);
+      x[0] = r.x; x[1] = r.y;
+    }
   }
-  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  const float mean = s / (float)D;
-  float m2 = 0.f;
-  for (int i = 0; i < per; ++i) m2 += (x[i] - mean) * (x[i] - mean);
-  for (int o = 16; o; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
-  if (lane == 0) {
-    const int j = (int)(row % h_kv);
-    const int64_t bt = row / h_kv;
-    const int t = (int)(bt % N);
-    const int64_t b = bt / N;
-    sigma[(b * h_kv + j) * N + t] = sqrtf(m2 / (float)D);
+}
+template <typename T, int PER>
+__global__ void value_spread_kernel(const T* __restrict__ v, int64_t n_rows, int h_kv, int N, float* __restrict__ sigma) {
+  constexpr int D = 32 * PER;
+  const int lane = threadIdx.x & 31;
+  const int64_t row0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kSpreadRows;  // (b, t, j) flattened
+  float x[kSpreadRows][PER];
+#pragma unroll
+  for (int r = 0; r < kSpreadRows; ++r) {
+    if (row0 + r < n_rows) load_row_part<T, PER>(v + (row0 + r) * D + lane * PER, x[r]);
+    else
+#pragma unroll
+      for (int e = 0; e < PER; ++e) x[r][e] = 0.f;
+  }
+#pragma unroll
+  for (int r = 0; r < kSpreadRows; ++r) {
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) s += x[r][e];
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float mean = s / (float)D;
+    float m2 = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) m2 += (x[r][e] - mean) * (x[r][e] - mean);
+    for (int o = 16; o; o >>= 1) m2 += __shfl_xor_sync(0xffffffffu, m2, o);
+    const int64_t row = row0 + r;
+    if (lane == 0 && row < n_rows) {
+      const int j = (int)(row % h_kv);
+      const int64_t bt = row / h_kv;
+      const int t = (int)(bt % N);
+      const int64_t b = bt / N;
+      sigma[(b * h_kv + j) * N + t] = sqrtf(m2 / (float)D);
+    }
   }
 }
 
@@ -67,15 +102,25 @@ __global__ void colsq_kernel(const void* __restrict__ x, int dtype, int N, int c
 
 __global__ void channel_weight_kernel(const float* __restrict__ qpart, const float* __restrict__ kpart, int nchunk,
                                       int h_q, int h_kv, int D, float* __restrict__ w_chan) {
+  // thread (r, c) sums the chunks r, r + R, ... of channel c; the R sums combine in a fixed order
+  __shared__ double sq[1024], sk[1024];
   const int head = blockIdx.x;  // b * h_kv + j
   const int b = head / h_kv, j = head % h_kv;
-  const int c = threadIdx.x;
+  const int c = threadIdx.x % D, r = threadIdx.x / D, R = blockDim.x / D;
   const int G = h_q / h_kv;
   double qs = 0.0, ks = 0.0;
-  for (int i = 0; i < nchunk; ++i) {
+  for (int i = r; i < nchunk; i += R) {
     const float* qp = qpart + ((int64_t)b * nchunk + i) * h_q * D;
     for (int h = j * G; h < (j + 1) * G; ++h) qs += (double)qp[h * D + c];
     ks += (double)kpart[((int64_t)b * nchunk + i) * h_kv * D + j * D + c];
+  }
+  sq[threadIdx.x] = qs;
+  sk[threadIdx.x] = ks;
+  __syncthreads();
+  if (r != 0) return;
+  for (int rr = 1; rr < R; ++rr) {
+    qs += sq[rr * D + c];
+    ks += sk[rr * D + c];
   }
   w_chan[head * D + c] = (float)(sqrt(qs) * sqrt(ks) / sqrt((double)D));
 }
@@ -226,6 +271,8 @@ extern "C" rdkv_status rdkv_score(const rdkv_shape* s, const void* q, const void
   const int N = s->n_tokens, D = s->head_dim, Np = N - s->window;
   RDKV_REQUIRE(q && k && v && w_tok && w_chan && sigma_tok && (Np == 0 || g_tok), RDKV_ERR_INVALID_ARG,
                "NULL pointer argument");
+  RDKV_REQUIRE(((uintptr_t)q | (uintptr_t)k | (uintptr_t)v) % 16 == 0, RDKV_ERR_INVALID_ARG,
+               "q, k and v must be 16-byte aligned");
   size_t lse_b, qp_b, kp_b;
   const size_t need = score_ws_parts(s, &lse_b, &qp_b, &kp_b);
   RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "score workspace too small (%zu < %zu)", ws_bytes, need);
@@ -237,8 +284,16 @@ extern "C" rdkv_status rdkv_score(const rdkv_shape* s, const void* q, const void
 
   // sigma of V rows
   const int64_t rows = (int64_t)s->batch * N * s->h_kv;
-  value_spread_kernel<<<(unsigned)ceil_div64(rows * 32, 256), 256, 0, cs>>>(v, s->dtype, rows, s->h_kv, N, D,
-                                                                            sigma_tok);
+  {
+    const unsigned blocks = (unsigned)ceil_div64(ceil_div64(rows, kSpreadRows) * 32, 256);
+    if (s->dtype == RDKV_F16) {
+      if (D == 128) value_spread_kernel<__half, 4><<<blocks, 256, 0, cs>>>(static_cast<const __half*>(v), rows, s->h_kv, N, sigma_tok);
+      else value_spread_kernel<__half, 2><<<blocks, 256, 0, cs>>>(static_cast<const __half*>(v), rows, s->h_kv, N, sigma_tok);
+    } else {
+      if (D == 128) value_spread_kernel<float, 4><<<blocks, 256, 0, cs>>>(static_cast<const float*>(v), rows, s->h_kv, N, sigma_tok);
+      else value_spread_kernel<float, 2><<<blocks, 256, 0, cs>>>(static_cast<const float*>(v), rows, s->h_kv, N, sigma_tok);
+    }
+  }
   RDKV_CHECK_LAUNCH("value spread");
   // channel weights
   const int nchunk = ceil_div(N, kColChunk);
@@ -247,7 +302,8 @@ extern "C" rdkv_status rdkv_score(const rdkv_shape* s, const void* q, const void
   colsq_kernel<<<dim3(ceil_div(s->h_kv * D, 256), nchunk, s->batch), 256, 0, cs>>>(k, s->dtype, N, s->h_kv * D,
                                                                                    kpart);
   RDKV_CHECK_LAUNCH("key column norms");
-  channel_weight_kernel<<<s->batch * s->h_kv, D, 0, cs>>>(qpart, kpart, nchunk, s->h_q, s->h_kv, D, w_chan);
+  channel_weight_kernel<<<s->batch * s->h_kv, std::min(1024, 8 * D), 0, cs>>>(qpart, kpart, nchunk, s->h_q, s->h_kv,
+                                                                                D, w_chan);
   RDKV_CHECK_LAUNCH("channel weights");
   // token weights
   if (s->dtype == RDKV_F16) return launch_score_tc(s, q, k, sigma_tok, lse2, w_tok, g_tok, cs);

@@ -137,6 +137,17 @@ def captured_traffic(kernel):
 
 
 # ---------------------------------------------------------------- algorithmic work
+def pack_bytes_per_layer(w, sizes):
+    """Bytes the pack must move for one layer (from the plan's totals): K and V rows of the kept
+    prefix tokens and of the window read, zones A and B, the index map and the window rows of zone
+    C written."""
+    P = 2 if w.dtype == "f16" else 4
+    win = 2 * w.batch * w.h_kv * w.window * w.head_dim
+    read = 2 * int(sizes.kept_tokens) * w.head_dim * P + win * P
+    written = int(sizes.zone_a_bytes) + int(sizes.zone_b_rows) * w.head_dim * 2 + int(sizes.index_slots) * 4 + win * 2
+    return read + written
+
+
 def decode_bytes_per_call(heads, D, h_q, batch, len_c):
     """Bytes one decode call must move: zone-A payload and metadata of real tokens
     and channels, zone-B rows of real tokens, len_c zone-C rows per head, q in and
@@ -188,20 +199,27 @@ def run_ours(args, ws, rank, local):
     def compress(timing):
         for layer in range(L):
             q, k, v = pre[layer]
-            if timing is not None:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e0.record()
+            ev4 = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timing is not None else None
+            if ev4:
+                ev4[0].record()
             score_out[layer] = rdkv.rdkv_score(shape, q, k, v, out=score_out[layer])
-            if timing is not None:
-                e1 = torch.cuda.Event(enable_timing=True)
-                e1.record()
-                timing.append((e0, e1))
+            if ev4:
+                ev4[1].record()
             sc = score_out[layer]
             alloc_out[layer] = rdkv.rdkv_allocate(shape, sc["g_tok"], sc["w_chan"], k, avg, avg,
                                                   out=alloc_out[layer])
             al = alloc_out[layer]
+            if ev4:
+                ev4[2].record()
+            sizes = rdkv.rdkv_plan_sizes(al["plan"])  # zone sizes for the buffers (synchronises)
+            if ev4:
+                ev4[2] = torch.cuda.Event(enable_timing=True)  # the pack interval starts after the sizes
+                ev4[2].record()
             caches[layer] = rdkv.rdkv_pack(shape, al["plan"], k, v, al["bits_tok"], al["bits_chan"], cap_c,
-                                           into=caches[layer])
+                                           into=caches[layer], sizes=sizes)
+            if ev4:
+                ev4[3].record()
+                timing.append(ev4)
 
     def decode_phase():
         for s in range(S):
@@ -265,7 +283,9 @@ def run_ours(args, ws, rank, local):
     gpu_launches = int(compress_launches + args.steps * decode_launches)
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     dec_ms = [b.elapsed_time(c) for a, b, c in ev]
-    score_ms = sum(e0.elapsed_time(e1) for e0, e1 in score_ev) / args.steps
+    score_ms = sum(e[0].elapsed_time(e[1]) for e in score_ev) / args.steps
+    alloc_ms = sum(e[1].elapsed_time(e[2]) for e in score_ev) / args.steps  # incl. the sizes read-back
+    pack_ms = sum(e[2].elapsed_time(e[3]) for e in score_ev) / args.steps
     tot_ms, tot_dec, tot_score = sum(step_ms), sum(dec_ms), score_ms * args.steps
     tot_ms, tot_dec, tot_score = max_over_ranks([tot_ms, tot_dec, tot_score], ws, dev)
     score_ms = tot_score / args.steps
@@ -326,6 +346,11 @@ def run_ours(args, ws, rank, local):
         "decode_bytes_per_step": int(dec_bytes),
         "scorer_tflops": round(score_tflops, 2), "scorer_ms_per_layer": round(score_ms / L, 3),
         "compress_ms_per_layer": round((ms_per_step - dec_ms_step) / L, 3),
+        "compress_breakdown_ms_per_layer": {
+            "score (weights: tensor-core passes, channel norms, V spreads)": round(score_ms / L, 3),
+            "allocate (water-filling V and K, channel spreads, plan; sizes read back)": round(alloc_ms / L, 3),
+            "pack (index map, tiles, zone B, window)": round(pack_ms / L, 3)},
+        "pack_gbs": round(sum(pack_bytes_per_layer(w, c.c.sizes) for c in caches) / (pack_ms * 1e-3) / 1e9, 1),
         "roofline": dominant, "rooflines": {"decode": decode_roof, "scorer": score_roof},
         "gpu_launches": gpu_launches, "clocks": clocks, "wall_s": round(wall, 3),
     }

@@ -38,6 +38,17 @@ __device__ __forceinline__ uint32_t qcode(float x, const QParams& p, int bits) {
   return (uint32_t)fminf(fmaxf(t, 0.0f), hi);
 }
 
+// The same code with the division replaced by a multiply with r = fp32(1/scale): |d r - d/scale|
+// stays below 2^-15 for the |d/scale| < 256 of a group's own values, so rint agrees with the IEEE
+// quotient's unless d r is within 2^-12 of a half-integer; there the quotient is computed exactly.
+__device__ __forceinline__ uint32_t qcode_rcp(float x, float zero, float scale, float rscale, float hi) {
+  if (scale == 0.0f) return 0u;
+  const float d = x - zero;
+  float t = d * rscale;
+  if (fabsf(t - floorf(t) - 0.5f) < 0.000244140625f) t = __fdiv_rn(d, scale);
+  return (uint32_t)fminf(fmaxf(rintf(t), 0.0f), hi);
+}
+
 // Bit position of element e inside a word of b-bit elements: even elements in
 // the low half-word, odd ones in the high half-word, LSB-first.
 __device__ __forceinline__ int bit_off(int e, int b) { return 16 * (e & 1) + b * (e >> 1); }
@@ -104,13 +115,16 @@ __global__ void __launch_bounds__(1024) index_kernel(const uint8_t* __restrict__
 }
 
 // ---------------------------------------------------------------- tile pack
-// One block (128 threads) per zone-A tile.
+// One block (256 threads) per zone-A tile: stage the tile's K and V rows as floats, then the
+// quantiser statistics of every K slot and V group, then the codes (one element per thread step,
+// lanes along slots/channels, warps along tokens), then the words.
+constexpr int kPackThreads = 256;
 template <typename T>
-__global__ void __launch_bounds__(128) pack_tile_kernel(const T* __restrict__ k, const T* __restrict__ v,
-                                                         const void* __restrict__ plan,
-                                                         const int32_t* __restrict__ index_map,
-                                                         uint8_t* __restrict__ zone_a, uint16_t* __restrict__ zone_b,
-                                                         int N, int h_kv, int D) {
+__global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                                                                  const void* __restrict__ plan,
+                                                                  const int32_t* __restrict__ index_map,
+                                                                  uint8_t* __restrict__ zone_a,
+                                                                  uint16_t* __restrict__ zone_b, int N, int h_kv, int D) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const rdkv_plan_header* hdr = plan_header(plan);
   const rdkv_head_plan* heads = plan_heads(plan);
@@ -138,14 +152,19 @@ __global__ void __launch_bounds__(128) pack_tile_kernel(const T* __restrict__ k,
   const int n_real = min(kTile, hp.n_v[cls] - ti * kTile);
   const int RW = hp.row_words, KS = hp.k_slots;
   const int16_t* slot_ch = plan_slots(plan) + (int64_t)head * hdr->slot_stride;
+  const int ngrp = D / kVGroup;
 
   float* Kf = reinterpret_cast<float*>(smem_raw);            // [32][D]
   float* Vf = Kf + kTile * D;                                // [32][D]
   uint16_t* kc = reinterpret_cast<uint16_t*>(Vf + kTile * D);  // [32][KS]
   uint8_t* vc = reinterpret_cast<uint8_t*>(kc + kTile * KS);   // [32][D]
+  float* kq = reinterpret_cast<float*>(vc + kTile * D);        // [KS][3] zero, scale, 1/scale
+  float* vq = kq + 3 * KS;                                     // [32][ngrp][3]
+  int16_t* sch = reinterpret_cast<int16_t*>(vq + 3 * kTile * ngrp);  // [KS] slot channels
   __shared__ int tok[kTile];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
   if (tid < kTile) tok[tid] = index_map[slot0 + tid];
+  for (int s = tid; s < KS; s += blockDim.x) sch[s] = slot_ch[s];
   __syncthreads();
   for (int i = tid; i < kTile * D; i += blockDim.x) {
     const int r = i / D, c = i % D;
@@ -158,48 +177,47 @@ __global__ void __launch_bounds__(128) pack_tile_kernel(const T* __restrict__ k,
 
   uint8_t* tile = zone_a + tile_off;
   uint16_t* kmeta = reinterpret_cast<uint16_t*>(tile + 4 * kTile * RW);
-  // K codes per slot (segment widths 16, 8, 4, 2)
-  const int s16 = 2 * hp.k_words[0];
-  for (int s = tid; s < KS; s += blockDim.x) {
-    int seg = 0, sbase = 0;
-    while (seg < 3 && s >= sbase + hp.k_words[seg] * (32 >> (4 - seg))) {
-      sbase += hp.k_words[seg] * (32 >> (4 - seg));
-      ++seg;
-    }
-    const int kb = 16 >> seg;
-    const int c = slot_ch[s];
-    if (kb == 16) {
-      for (int r = 0; r < kTile; ++r)
-        kc[r * KS + s] = (c >= 0 && r < n_real) ? half_bits(Kf[r * D + c]) : (uint16_t)0;
-      continue;
-    }
-    const int m = s - s16;  // index among the quantised slots
-    uint16_t sc_h = 0, ze_h = 0;
-    if (c >= 0) {
-      float mn = Kf[c], mx = Kf[c];
-      for (int r = 1; r < n_real; ++r) {
-        mn = fminf(mn, Kf[r * D + c]);
-        mx = fmaxf(mx, Kf[r * D + c]);
-      }
-      const QParams p = qparams(mn, mx, kb);
-      sc_h = p.scale_h;
-      ze_h = p.zero_h;
-      for (int r = 0; r < kTile; ++r) kc[r * KS + s] = r < n_real ? (uint16_t)qcode(Kf[r * D + c], p, kb) : 0;
-    } else {
-      for (int r = 0; r < kTile; ++r) kc[r * KS + s] = 0;
-    }
-    kmeta[4 * (m >> 1) + (m & 1)] = sc_h;
-    kmeta[4 * (m >> 1) + 2 + (m & 1)] = ze_h;
-  }
-  // V codes per (token, 32-channel group)
-  const int ngrp = D / kVGroup;
   uint8_t* vcode = tile + 4 * kTile * RW + 4 * hp.meta_slots;
   uint16_t* vmeta = reinterpret_cast<uint16_t*>(vcode + kTile * D * vbits / 8);
-  if (vbits < 16) {
-    for (int i = tid; i < kTile * ngrp; i += blockDim.x) {
-      const int r = i / ngrp, g = i % ngrp;
+  const int s16 = 2 * hp.k_words[0];  // raw 16-bit slots come first
+  // statistics: K slot s (quantised slots only), then V group (r, g)
+  for (int i = tid; i < KS + (vbits < 16 ? kTile * ngrp : 0); i += blockDim.x) {
+    if (i < KS) {
+      const int s = i;
+      if (s < s16) continue;
+      int seg = 1, sbase = s16;
+      while (seg < 3 && s >= sbase + hp.k_words[seg] * (32 >> (4 - seg))) {
+        sbase += hp.k_words[seg] * (32 >> (4 - seg));
+        ++seg;
+      }
+      const int kb = 16 >> seg;
+      const int c = sch[s];
+      const int m = s - s16;  // index among the quantised slots
+      uint16_t sc_h = 0, ze_h = 0;
+      float z = 0.f, sc = 0.f, rs = 0.f;
+      if (c >= 0 && n_real > 0) {
+        float mn = Kf[c], mx = Kf[c];
+        for (int r = 1; r < n_real; ++r) {
+          mn = fminf(mn, Kf[r * D + c]);
+          mx = fmaxf(mx, Kf[r * D + c]);
+        }
+        const QParams p = qparams(mn, mx, kb);
+        sc_h = p.scale_h;
+        ze_h = p.zero_h;
+        z = p.zero;
+        sc = p.scale;
+        rs = sc != 0.f ? __frcp_rn(sc) : 0.f;
+      }
+      kq[3 * s] = z;
+      kq[3 * s + 1] = sc;
+      kq[3 * s + 2] = rs;
+      kmeta[4 * (m >> 1) + (m & 1)] = sc_h;
+      kmeta[4 * (m >> 1) + 2 + (m & 1)] = ze_h;
+    } else {
+      const int vi = i - KS, r = vi / ngrp, g = vi % ngrp;
       const float* x = Vf + r * D + g * kVGroup;
       uint16_t sc_h = 0, ze_h = 0;
+      float z = 0.f, sc = 0.f, rs = 0.f;
       if (r < n_real) {
         float mn = x[0], mx = x[0];
         for (int e = 1; e < kVGroup; ++e) {
@@ -209,18 +227,47 @@ __global__ void __launch_bounds__(128) pack_tile_kernel(const T* __restrict__ k,
         const QParams p = qparams(mn, mx, vbits);
         sc_h = p.scale_h;
         ze_h = p.zero_h;
-        for (int e = 0; e < kVGroup; ++e) vc[r * D + g * kVGroup + e] = (uint8_t)qcode(x[e], p, vbits);
-      } else {
-        for (int e = 0; e < kVGroup; ++e) vc[r * D + g * kVGroup + e] = 0;
+        z = p.zero;
+        sc = p.scale;
+        rs = sc != 0.f ? __frcp_rn(sc) : 0.f;
       }
-      const int p = r >> 1, mm = r & 1;
-      vmeta[(p * ngrp + g) * 4 + mm] = sc_h;
-      vmeta[(p * ngrp + g) * 4 + 2 + mm] = ze_h;
+      vq[3 * vi] = z;
+      vq[3 * vi + 1] = sc;
+      vq[3 * vi + 2] = rs;
+      const int pp = r >> 1, mm = r & 1;
+      vmeta[(pp * ngrp + g) * 4 + mm] = sc_h;
+      vmeta[(pp * ngrp + g) * 4 + 2 + mm] = ze_h;
     }
-  } else {
+  }
+  if (vbits == 16) {
     for (int i = tid; i < kTile * D; i += blockDim.x) {
       const int r = i / D;
       zone_b[brow * D + i] = r < n_real ? half_bits(Vf[i]) : (uint16_t)0;
+    }
+  }
+  __syncthreads();
+  // codes: lanes along slots (K) or channels (V), warps along tokens
+  for (int r = ty; r < kTile; r += blockDim.x >> 5) {
+    for (int s = tx; s < KS; s += 32) {
+      const int c = sch[s];
+      uint16_t code = 0;
+      if (c >= 0 && r < n_real) {
+        if (s < s16) {
+          code = half_bits(Kf[r * D + c]);
+        } else {
+          const int kb = s < s16 + hp.k_words[1] * 4 ? 8 : s < s16 + hp.k_words[1] * 4 + hp.k_words[2] * 8 ? 4 : 2;
+          code = (uint16_t)qcode_rcp(Kf[r * D + c], kq[3 * s], kq[3 * s + 1], kq[3 * s + 2], (float)((1 << kb) - 1));
+        }
+      }
+      kc[r * KS + s] = code;
+    }
+    if (vbits < 16) {
+      for (int c = tx; c < D; c += 32) {
+        const int vi = r * ngrp + c / kVGroup;
+        vc[r * D + c] = r < n_real ? (uint8_t)qcode_rcp(Vf[r * D + c], vq[3 * vi], vq[3 * vi + 1], vq[3 * vi + 2],
+                                                          (float)((1 << vbits) - 1))
+                                   : (uint8_t)0;
+      }
     }
   }
   __syncthreads();
@@ -296,7 +343,8 @@ __global__ void set_len_kernel(int32_t* len_dev, int value) { *len_dev = value; 
 
 static size_t pack_smem_bytes(int D) {
   const int max_slots = D + kSlotPad;
-  return (size_t)2 * kTile * D * 4 + (size_t)kTile * max_slots * 2 + (size_t)kTile * D;
+  return (size_t)2 * kTile * D * 4 + (size_t)kTile * max_slots * 2 + (size_t)kTile * D + (size_t)max_slots * 12 +
+         (size_t)kTile * (D / kVGroup) * 12 + (size_t)max_slots * 2 + 16;
 }
 
 static rdkv_status check_cache(const rdkv_cache* c) {
@@ -341,13 +389,13 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
     if (s.dtype == RDKV_F16) {
       RDKV_TRY_CUDA(cudaFuncSetAttribute(pack_tile_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
                     "pack smem");
-      pack_tile_kernel<__half><<<(unsigned)n_tiles, 128, smem, cs>>>(
+      pack_tile_kernel<__half><<<(unsigned)n_tiles, kPackThreads, smem, cs>>>(
           static_cast<const __half*>(k), static_cast<const __half*>(v), cache->plan, cache->index_map, cache->zone_a,
           cache->zone_b, N, s.h_kv, D);
     } else {
       RDKV_TRY_CUDA(cudaFuncSetAttribute(pack_tile_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
                     "pack smem");
-      pack_tile_kernel<float><<<(unsigned)n_tiles, 128, smem, cs>>>(
+      pack_tile_kernel<float><<<(unsigned)n_tiles, kPackThreads, smem, cs>>>(
           static_cast<const float*>(k), static_cast<const float*>(v), cache->plan, cache->index_map, cache->zone_a,
           cache->zone_b, N, s.h_kv, D);
     }

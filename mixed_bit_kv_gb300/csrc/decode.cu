@@ -47,10 +47,10 @@ struct KBDesc {
 
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings): k-block
 // descriptors, query fragments (float4 per lane for fp32 queries, two fp16 pairs otherwise),
-// zone-C query fragments, query rows, slot table, ring bookkeeping, the fused step's new row.
+// zone-C query fragments, slot table, ring bookkeeping, the fused step's new row.
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D, bool qlo) {
   return ((256 + (int64_t)kMaxKB * 32 * (qlo ? 16 : 8) + (int64_t)(D / 16) * 32 * 16 +
-           (int64_t)8 * D * 4 + (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 20 + (int64_t)2 * D * 2) + 127) /
+           (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 20 + (int64_t)2 * D * 2) + 127) /
          128 * 128;
 }
 // Floats of one block's partial result (m, l, o for G heads), rounded up to a multiple of 4.
@@ -155,6 +155,11 @@ __device__ __forceinline__ uint4 lds128(const unsigned char* base, uint32_t off)
 }
 __device__ __forceinline__ uint32_t pick4(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 
+// Byte-permute selector that moves bytes (0, 2) (odd = 0) or (1, 3) (odd = 1) of a word to the
+// low bytes of its two half-words and zeroes the high bytes: the two 8-bit codes of a pair at
+// bit 0 and bit 16, the same as a shift by 0 or 8 and a mask, in one instruction.
+__device__ __forceinline__ uint32_t byte_pair_sel(int odd) { return odd ? 0x4341u : 0x4240u; }
+
 // Two codes of a pair (already shifted to bit 0 and bit 16) -> exact fp16 codes
 // -> scale * code + zero, one rounding.
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t w, int shift, uint32_t mask2, uint32_t scale2,
@@ -189,6 +194,14 @@ __device__ __forceinline__ uint4 split_hi_lo(float x0, float x1, float x2, float
   return r;
 }
 
+// 2^x by the SFU's approximate base-2 exponential (relative error about 2^-22; results below
+// the normal range flush to zero, which the softmax weights can afford)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- per-warp state
 template <int D>
 struct WarpAcc {
@@ -221,8 +234,8 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
       mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, o));
     }
     const float mn0 = fmaxf(acc.m[0], mt0), mn1 = fmaxf(acc.m[1], mt1);
-    const float al0 = acc.m[0] == -INFINITY ? 0.f : exp2f(acc.m[0] - mn0);
-    const float al1 = acc.m[1] == -INFINITY ? 0.f : exp2f(acc.m[1] - mn1);
+    const float al0 = acc.m[0] == -INFINITY ? 0.f : ex2(acc.m[0] - mn0);
+    const float al1 = acc.m[1] == -INFINITY ? 0.f : ex2(acc.m[1] - mn1);
     acc.m[0] = mn0;
     acc.m[1] = mn1;
     acc.l[0] *= al0;
@@ -242,8 +255,8 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
   float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
   for (int tb = 0; tb < NTB; ++tb) {
-    const float p0 = exp2f(s[tb][0] - ref0), p1 = exp2f(s[tb][1] - ref1);
-    const float p2 = exp2f(s[tb][2] - ref0), p3 = exp2f(s[tb][3] - ref1);
+    const float p0 = ex2(s[tb][0] - ref0), p1 = ex2(s[tb][1] - ref1);
+    const float p2 = ex2(s[tb][2] - ref0), p3 = ex2(s[tb][3] - ref1);
     ps0 += p0 + p2;
     ps1 += p1 + p3;
     pb[tb][0] = movmatrix_trans(pack_half2(p0, p1));
@@ -337,6 +350,7 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsig
   constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
   const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
   const int sh1 = W == 2 ? 2 * q + 8 : sh0;
+  const uint32_t bsel = byte_pair_sel(q & 1);  // 8-bit codes: bytes (0, 2) or (1, 3) of a word
   // this lane's offsets from a block's first word: words o0, o1 of its two slot pairs, tokens g ..
   const uint32_t c0 = 128u * (W == 16 ? q : W == 8 ? (q >> 1) : 0) + 16u * g;
   const uint32_t c1 = 128u * (W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0) + 16u * g;
@@ -373,8 +387,10 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsig
         const uint32_t k0 = v0 ? ~0u : 0u, k1 = v1 ? ~0u : 0u;
         mma16816(sr[tb], x0 & k0, x1 & k0, x2 & k1, x3 & k1, bh0, bh1);
       } else {
-        const uint32_t a0 = (x0 >> sh0) & mask2, a1 = (x1 >> sh0) & mask2;
-        const uint32_t a2 = (x2 >> sh1) & mask2, a3 = (x3 >> sh1) & mask2;
+        const uint32_t a0 = W == 8 ? __byte_perm(x0, 0u, bsel) : (x0 >> sh0) & mask2;
+        const uint32_t a1 = W == 8 ? __byte_perm(x1, 0u, bsel) : (x1 >> sh0) & mask2;
+        const uint32_t a2 = W == 8 ? __byte_perm(x2, 0u, bsel) : (x2 >> sh1) & mask2;
+        const uint32_t a3 = W == 8 ? __byte_perm(x3, 0u, bsel) : (x3 >> sh1) & mask2;
         mma16816(sq[tb], a0, a1, a2, a3, bh0, bh1);
         mma16816(sq[tb], a0, a1, a2, a3, bl0, bl1);
       }
@@ -444,6 +460,7 @@ __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned c
   constexpr uint32_t mask2 = VB == 8 ? 0x00ff00ffu : VB == 4 ? 0x000f000fu : 0x00030003u;
   constexpr int R = VB / 2;         // word groups inside a pair (words w = r mod R together)
   const int sh0 = VB * (g % per), sh1 = VB * ((g + 8) % per);
+  const uint32_t bsel = byte_pair_sel(g & 1);  // 8-bit codes: bytes (0, 2) or (1, 3) of a word
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
     const int p0 = 8 * tb + q, p1 = p0 + 4;
@@ -470,10 +487,10 @@ __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned c
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int cm = 2 * grp + half;
-        const uint32_t a0 = (w0[2 * half] >> sh0) & mask2;
-        const uint32_t a1 = (w0[2 * half + 1] >> sh1) & mask2;
-        const uint32_t a2 = (w1[2 * half] >> sh0) & mask2;
-        const uint32_t a3 = (w1[2 * half + 1] >> sh1) & mask2;
+        const uint32_t a0 = VB == 8 ? __byte_perm(w0[2 * half], 0u, bsel) : (w0[2 * half] >> sh0) & mask2;
+        const uint32_t a1 = VB == 8 ? __byte_perm(w0[2 * half + 1], 0u, bsel) : (w0[2 * half + 1] >> sh1) & mask2;
+        const uint32_t a2 = VB == 8 ? __byte_perm(w1[2 * half], 0u, bsel) : (w1[2 * half] >> sh0) & mask2;
+        const uint32_t a3 = VB == 8 ? __byte_perm(w1[2 * half + 1], 0u, bsel) : (w1[2 * half + 1] >> sh1) & mask2;
         mma16816(acc.o[cm], a0, a1, a2, a3, b0, b1);
       }
     }
@@ -591,13 +608,12 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
   KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
   float4* qv = reinterpret_cast<float4*>(smem + 256);                              // [kMaxKB][32] (uint2 if !QLO)
   uint4* qfragc = reinterpret_cast<uint4*>(smem + 256 + kMaxKB * 32 * (QLO ? 16 : 8));  // [D/16][32] hi, lo
-  float* q_s = reinterpret_cast<float*>(qfragc + (D / 16) * 32);                   // [8][D] query rows of the group
-  int16_t* slot_s = reinterpret_cast<int16_t*>(q_s + 8 * D);                       // [D + kSlotPad] slot table
+  int16_t* slot_s = reinterpret_cast<int16_t*>(qfragc + (D / 16) * 32);            // [D + kSlotPad] slot table
   uint64_t* bars = reinterpret_cast<uint64_t*>(slot_s + D + kSlotPad);             // [warps][kMaxInflight]
   int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
   int* ring_item = ring_pos + kDecWarps * kMaxInflight;                            // [warps][kMaxInflight]
-  uint32_t* ring_vend = reinterpret_cast<uint32_t*>(ring_item + kDecWarps * kMaxInflight);  // [warps][kMaxInflight]
-  uint16_t* newrow = reinterpret_cast<uint16_t*>(ring_vend + kDecWarps * kMaxInflight);     // [2][D] fused step: k, v
+  uint32_t* ring_need = reinterpret_cast<uint32_t*>(ring_item + kDecWarps * kMaxInflight);  // [warps][kMaxInflight]
+  uint16_t* newrow = reinterpret_cast<uint16_t*>(ring_need + kDecWarps * kMaxInflight);     // [2][D] fused step: k, v
   unsigned char* ring = smem + decode_fixed_smem(D, QLO);
   float* red = reinterpret_cast<float*>(ring);                                     // [warps][8][D + 2], after the loop
   __shared__ int seg_kb_s[5];
@@ -673,14 +689,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
   unsigned char* wring = ring + (int64_t)warp * P.ring_bytes;
   uint64_t* wbar = bars + warp * kMaxInflight;
   int* wpos = ring_pos + warp * kMaxInflight;
-  uint32_t head_v = 0, tail_v = 0;     // virtual ring offsets (bytes)
-  int* witem = ring_item + warp * kMaxInflight;
-  uint32_t* vend = ring_vend + warp * kMaxInflight;  // ring end after each slot's copy (lane 0)
+  uint32_t head_p = 0, used = 0;       // lane 0: next write offset; bytes held, wrap waste included
+  int* witem = ring_item + warp * kMaxInflight;  // per slot: (class + 1) << 24 | index within the class
+  uint32_t* wneed = ring_need + warp * kMaxInflight;  // bytes each slot holds, wrap waste included
   int issued = 0, done = 0;
   bool drained = warp >= P.ring_warps;  // lane 0: no item left for this warp (warps without a ring take none)
   int pending = -1;                    // lane 0: item taken but not yet issued (ring full)
   auto issue = [&]() {
-    if (issued == done) head_v = tail_v = 0;  // empty ring: start at its beginning
+    if (issued == done) head_p = used = 0;  // empty ring: start at its beginning
     while (!drained && issued - done < kMaxInflight) {
       int it = pending;
       if (it < 0) it = split + n_split * atomicAdd(&next_k, 1);  // taken in order of need: no warp idles early
@@ -699,19 +715,21 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
         c_row = (it - zc_start) * kCRows;
         sz = 2u * kCRows * D * 2;
       }
-      uint32_t phys = head_v % (uint32_t)P.ring_bytes;
-      uint32_t need = sz;
+      // the held bytes end at head_p (circularly); a copy that does not fit before the end of the
+      // ring starts at its beginning and also holds the skipped tail until it is released
+      uint32_t phys = head_p, need = sz;
       if (phys + sz > (uint32_t)P.ring_bytes) { need += (uint32_t)P.ring_bytes - phys; phys = 0; }
-      if (head_v - tail_v + need > (uint32_t)P.ring_bytes) {
+      if (used + need > (uint32_t)P.ring_bytes) {
         pending = it;
         break;
       }
       pending = -1;
-      head_v += need;
+      head_p = phys + sz;
+      used += need;
       const int slot = issued % kMaxInflight;
-      vend[slot] = head_v;
+      wneed[slot] = need;
       wpos[slot] = (int)phys;
-      witem[slot] = it;
+      witem[slot] = ((cls + 1) << 24) | (cls >= 0 ? it - (int)cstart(cls) : it - zc_start);
       unsigned char* dst = wring + phys;
       uint64_t* bar = &wbar[slot];
       if (cls >= 0) {
@@ -738,8 +756,37 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
     for (int k = 0; k < kMaxInflight; ++k) mbar_init(&wbar[k], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();  // next_k, the barriers and the k-block descriptors are set
+  if (tid < k_slots) slot_s[tid] = sr;
+  __syncthreads();  // next_k, the barriers, the k-block descriptors and the slot table are set
   if (lane == 0) issue();  // the first zone-A copies fly while the query fragments are built
+  const int nkb = seg_kb_s[4];
+  int seg_kb[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) seg_kb[i] = seg_kb_s[i];
+  // Query fragments: B[k = slot pair][n = head g] in slot order (zone A) and channel order (zone C),
+  // at most two per thread.  Which query element each entry takes is static: look it up now.
+  static_assert((kMaxKB + 128 / 16) * 32 <= 2 * kDecWarps * 32, "two query fragments per thread");
+  const int n_frag = (nkb + D / 16) * 32;
+  int fq[2][4];  // element of the group's query rows [G][D] per fragment entry, or -1
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = tid + r * kDecWarps * 32;
+    const int kb = i >> 5, ln = i & 31, g = ln >> 2, qq = ln & 3;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int off = 2 * qq + (e & 1) + 8 * (e >> 1);
+      int ch = -1;
+      if (i < n_frag && g < G) {
+        if (kb < nkb) {
+          const KBDesc d = kbd[kb];
+          ch = off < d.nrem ? slot_s[d.slot0 + off] : -1;
+        } else {
+          ch = 16 * (kb - nkb) + off;
+        }
+      }
+      fq[r][e] = ch >= 0 ? g * D + ch : -1;
+    }
+  }
   // Everything so far read only the plan and zone A, which the kernel launched just before this one
   // on the stream does not write.  The query, the new token and the zone-C length may come from
   // it: wait for it here (a no-op without programmatic dependent launch).
@@ -748,48 +795,26 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
   n_rows = len_c + (fused ? 1 : 0);
   n_items = zc_start + ceil_div(n_rows, kCRows);
   items_final = true;
-  float qr[4];
+  float qf[2][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = tid + k * kDecWarps * 32;
-    qr[k] = i < G * D ? load_as_float(P.q, (int64_t)qbase * D + i, P.dtype) : 0.f;
-  }
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      qf[r][e] = fq[r][e] >= 0 ? load_as_float(P.q, (int64_t)qbase * D + fq[r][e], P.dtype) : 0.f;
   if (fused && tid < 2 * D) {
     const int64_t src = (int64_t)head * D + (tid % D);
     newrow[tid] = half_bits(load_as_float(tid < D ? P.k_new : P.v_new, src, P.dtype));
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = tid + k * kDecWarps * 32;
-    if (i < G * D) q_s[i] = qr[k];
-  }
-  if (tid < k_slots) slot_s[tid] = sr;
-  __syncthreads();
-  const int nkb = seg_kb_s[4];
-  int seg_kb[5];
-#pragma unroll
-  for (int i = 0; i < 5; ++i) seg_kb[i] = seg_kb_s[i];
-  // query fragments: B[k = slot pair][n = head g] in slot order (zone A) and channel order (zone C)
-  for (int i = tid; i < (nkb + D / 16) * 32; i += blockDim.x) {
-    const int kb = i >> 5, ln = i & 31, g = ln >> 2, qq = ln & 3;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (g < G) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int off = 2 * qq + (e & 1) + 8 * (e >> 1);
-        int ch;
-        if (kb < nkb) {
-          const KBDesc d = kbd[kb];
-          ch = off < d.nrem ? slot_s[d.slot0 + off] : -1;
-        } else {
-          ch = 16 * (kb - nkb) + off;
-        }
-        if (ch >= 0) v[e] = q_s[g * D + ch];
-      }
+  for (int r = 0; r < 2; ++r) {
+    const int i = tid + r * kDecWarps * 32;
+    if (i < n_frag) {
+      const int kb = i >> 5, ln = i & 31;
+      const float* v = qf[r];
+      if (kb >= nkb) qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
+      else if (QLO) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
+      else reinterpret_cast<uint2*>(qv)[kb * 32 + ln] = make_uint2(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]));
     }
-    if (kb >= nkb) qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
-    else if (QLO) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
-    else reinterpret_cast<uint2*>(qv)[kb * 32 + ln] = make_uint2(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]));
   }
   __syncthreads();
 
@@ -818,10 +843,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
       break;
     }
     const uint32_t st = smem_u32(wring + wpos[slot]);
-    const int it = witem[slot];
-    const int cls = item_cls(it);
+    const int rec = witem[slot];
+    const int cls = (rec >> 24) - 1, ti = rec & 0xffffff;  // ti: tile of the class, or zone-C block
     if (cls >= 0) {
-      const int ti = it - (int)cstart(cls);
       const int n_real = min(kTile, (int)cnv(cls) - kTile * ti);
       const unsigned char* stp = wring + wpos[slot];
       const unsigned char* kmeta = stp + 4 * kTile * RW;
@@ -860,7 +884,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
         scale_o(acc, 16777216.f);
         o_sub = false;
       }
-      const int c_row = (it - zc_start) * kCRows;
+      const int c_row = ti * kCRows;
       const int rows = min(kCRows, n_rows - c_row);  // rows attended (the fused step's new row last)
       const int copied = max(0, min(kCRows, len_c - c_row));
       if (rows < kCRows || copied < rows) {
@@ -902,7 +926,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
     // release the stage: order this warp's reads before later bulk writes into it
     fence_proxy_async();
     __syncwarp();
-    if (lane == 0) tail_v = vend[slot];
+    if (lane == 0) used -= wneed[slot];
     ++done;
   }
   if (!ok) {

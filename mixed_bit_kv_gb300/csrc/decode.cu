@@ -338,14 +338,18 @@ __device__ __forceinline__ void k_segment(const unsigned char* kw, const unsigne
 // one half2 FMA, which is exact because that remainder fits fp16.  The codes
 // enter the tensor core as fp16 subnormals: the bit pattern of a code c placed
 // at bit 0 of a half-word is the value c * 2^-24 exactly, so one shift and one
-// mask make the A operand and the products land in sq scaled by 2^-24 (undone
-// once per tile).  Raw 16-bit channels go to sr at scale 1, and the zero-point
-// term sum_c q_c zero_c runs as an MMA whose A rows g + 8 hold the zeros, so
-// zacc[2], zacc[3] carry it for heads (2q, 2q+1).
+// mask make the A operand and the products land at 2^-24: the hi products in
+// shi, the lo products in slo (two accumulators, two independent chains).  Raw
+// 16-bit channels use the stored fp16 value against q, at scale 1, into shi.
+// The zero-point term sum_c q_c zero_c runs as an MMA whose A rows g + 8 hold
+// the zeros, so zacc[2], zacc[3] carry it for heads (2q, 2q+1).  A segment's
+// k-blocks are consecutive: 64 W bytes of words and 64 bytes of metadata
+// apart, and only the last one may be partial.
 template <int W>
 __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsigned char* kmeta, int kb0, int kb1,
-                                            const KBDesc* kbd, const uint2* qh, int lane, float (&sq)[2][4],
-                                            float (&sr)[2][4], float (&zacc)[4]) {
+                                            const KBDesc* kbd, const uint2* qh, int lane, float (&shi)[2][4],
+                                            float (&slo)[2][4], float (&zacc)[4]) {
+  if (kb0 >= kb1) return;
   const int g = lane >> 2, q = lane & 3;
   constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
   const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
@@ -354,16 +358,23 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsig
   // this lane's offsets from a block's first word: words o0, o1 of its two slot pairs, tokens g ..
   const uint32_t c0 = 128u * (W == 16 ? q : W == 8 ? (q >> 1) : 0) + 16u * g;
   const uint32_t c1 = 128u * (W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0) + 16u * g;
+  const KBDesc d0 = kbd[kb0];
+  const int last_nrem = kbd[kb1 - 1].nrem;
+  uint32_t wb = (uint32_t)d0.wbyte, mb = (uint32_t)d0.mbyte;
+  const uint2* qp = qh + kb0 * 32 + lane;
 #pragma unroll 1
-  for (int kb = kb0; kb < kb1; ++kb) {
-    const KBDesc d = kbd[kb];  // the same address in every lane: one broadcast
-    const uint2 qq = qh[kb * 32 + lane];  // q_g (fp16 pairs) at slots (2q, 2q+1), (2q+8, 2q+9); 0 for pads
-    const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
+  for (int kb = kb0; kb < kb1; ++kb, wb += 64u * W, mb += 64u, qp += 32) {
+    const int nrem = kb == kb1 - 1 ? last_nrem : 16;
+    const uint2 qq = *qp;  // q_g (fp16 pairs) at slots (2q, 2q+1), (2q+8, 2q+9); 0 for pads
+    const bool v0 = 2 * q < nrem, v1 = 2 * q + 8 < nrem;
+    // tokens g, g+8, g+16, g+24 of the lane's two words (one word for 2-bit codes)
+    const uint4 y0 = lds128(kw, wb + c0);
+    const uint4 y1 = W == 2 ? y0 : lds128(kw, wb + c1);
     uint32_t bh0 = qq.x, bh1 = qq.y, bl0 = 0, bl1 = 0;
     if (W != 16) {
       // a pair past the segment end reads the block's first pair (its q entries are 0)
-      const uint2 m0 = lds64(kmeta, (uint32_t)d.mbyte + (v0 ? 8u * q : 0u));
-      const uint2 m1 = lds64(kmeta, (uint32_t)d.mbyte + (v1 ? 8u * (q + 4) : 0u));
+      const uint2 m0 = lds64(kmeta, mb + (v0 ? 8u * q : 0u));
+      const uint2 m1 = lds64(kmeta, mb + (v1 ? 8u * (q + 4) : 0u));
       const __half2 q0 = *reinterpret_cast<const __half2*>(&qq.x), q1 = *reinterpret_cast<const __half2*>(&qq.y);
       const __half2 s0 = *reinterpret_cast<const __half2*>(&m0.x), s1 = *reinterpret_cast<const __half2*>(&m1.x);
       const __half2 h0 = __hmul2(q0, s0), h1 = __hmul2(q1, s1);
@@ -376,23 +387,20 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsig
       // (unused) and rows g + 8 the zero-point term sum zero * q, with no register shuffling
       mma16816(zacc, m0.x, m0.y, m1.x, m1.y, qq.x, qq.y);
     }
-    // tokens g, g+8, g+16, g+24 of the lane's two words (one word for 2-bit codes)
-    const uint4 y0 = lds128(kw, (uint32_t)d.wbyte + c0);
-    const uint4 y1 = W == 2 ? y0 : lds128(kw, (uint32_t)d.wbyte + c1);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
       const uint32_t x0 = pick4(y0, 2 * tb), x1 = pick4(y0, 2 * tb + 1);
       const uint32_t x2 = pick4(y1, 2 * tb), x3 = pick4(y1, 2 * tb + 1);
       if (W == 16) {  // raw fp16 words past the segment end may hold anything: zero them
         const uint32_t k0 = v0 ? ~0u : 0u, k1 = v1 ? ~0u : 0u;
-        mma16816(sr[tb], x0 & k0, x1 & k0, x2 & k1, x3 & k1, bh0, bh1);
+        mma16816(shi[tb], x0 & k0, x1 & k0, x2 & k1, x3 & k1, bh0, bh1);
       } else {
         const uint32_t a0 = W == 8 ? __byte_perm(x0, 0u, bsel) : (x0 >> sh0) & mask2;
         const uint32_t a1 = W == 8 ? __byte_perm(x1, 0u, bsel) : (x1 >> sh0) & mask2;
         const uint32_t a2 = W == 8 ? __byte_perm(x2, 0u, bsel) : (x2 >> sh1) & mask2;
         const uint32_t a3 = W == 8 ? __byte_perm(x3, 0u, bsel) : (x3 >> sh1) & mask2;
-        mma16816(sq[tb], a0, a1, a2, a3, bh0, bh1);
-        mma16816(sq[tb], a0, a1, a2, a3, bl0, bl1);
+        mma16816(shi[tb], a0, a1, a2, a3, bh0, bh1);
+        mma16816(slo[tb], a0, a1, a2, a3, bl0, bl1);
       }
     }
   }
@@ -420,16 +428,21 @@ __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsig
   } else {
     const uint2* qh = reinterpret_cast<const uint2*>(qv);
     float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // [2], [3]: zero-point term of heads 2q, 2q+1
-    float sr[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // raw 16-bit channels, scale 1
-    k_segment_h<16>(kw, kmeta, seg_kb[0], seg_kb[1], kbd, qh, lane, s, sr, zacc);
-    k_segment_h<8>(kw, kmeta, seg_kb[1], seg_kb[2], kbd, qh, lane, s, sr, zacc);
-    k_segment_h<4>(kw, kmeta, seg_kb[2], seg_kb[3], kbd, qh, lane, s, sr, zacc);
-    k_segment_h<2>(kw, kmeta, seg_kb[3], seg_kb[4], kbd, qh, lane, s, sr, zacc);
-    // s holds the code products at 2^-24
+    // raw 16-bit channels first, at scale 1 in s; then s moves to 2^-24 and takes the hi products
+    float slo[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    k_segment_h<16>(kw, kmeta, seg_kb[0], seg_kb[1], kbd, qh, lane, s, slo, zacc);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[tb][e] = fmaf(s[tb][e], 16777216.f, sr[tb][e]);
+      for (int e = 0; e < 4; ++e) s[tb][e] *= 5.9604644775390625e-8f;
+    k_segment_h<8>(kw, kmeta, seg_kb[1], seg_kb[2], kbd, qh, lane, s, slo, zacc);
+    k_segment_h<4>(kw, kmeta, seg_kb[2], seg_kb[3], kbd, qh, lane, s, slo, zacc);
+    k_segment_h<2>(kw, kmeta, seg_kb[3], seg_kb[4], kbd, qh, lane, s, slo, zacc);
+    // back to scale 1
+#pragma unroll
+    for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[tb][e] = (s[tb][e] + slo[tb][e]) * 16777216.f;
     be = zacc[2];
     bo = zacc[3];
   }
@@ -1029,80 +1042,42 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
       if (len_c < P.cap_c) *P.len_dev = len_c + 1;
     }
   }
-  // Merge: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per query head.  The splits'
-  // partials (contiguous) are copied into shared memory (the ring area is free) by 16-byte
-  // asynchronous copies, all in flight at once, in chunks that fit; each split's weight
-  // 2^(m_s - M) is computed once per head.
-  __shared__ float Mh[8], Lh[8], Sh[8];  // running max, running sum, rescale of the previous chunks
-  const int per = pstride;               // floats of one split's partial
-  const int chunk = max(1, (int)((int64_t)P.ring_warps * P.ring_bytes / (4 * (per + 8))));
-  float* buf = reinterpret_cast<float*>(ring);
-  float* wts = buf + (int64_t)chunk * per;  // [8][chunk]
-  if (tid < G) {
-    Mh[tid] = -INFINITY;
-    Lh[tid] = 0.f;
-  }
-  float o[4] = {0.f, 0.f, 0.f, 0.f};  // outputs i = tid + k * blockDim.x, k < 4 (G * D <= 1024)
-  for (int s0 = 0; s0 < n_split; s0 += chunk) {
-    const int ns = min(chunk, n_split - s0);
-    const float* src = part + (int64_t)s0 * per;
-    __syncthreads();  // the previous chunk is consumed
-    for (int i = tid; i < ns * per / 4; i += blockDim.x)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(buf + 4 * i)), "l"(src + 4 * i)
-                   : "memory");
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    if (warp < G) {  // warp h: the weights of head h, its lanes over the splits
-      const int h = warp;
-      const float Mo = Mh[h];
-      float mc = -INFINITY;
-      for (int sp = lane; sp < ns; sp += 32) mc = fmaxf(mc, buf[sp * per + h * (D + 2) + D]);
+  // Merge: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per query head and channel.  One
+  // thread per output element loads what it needs straight from the splits' partials (L2; the
+  // acquire above made them visible), kMergeBatch splits at a time with every load of a batch in
+  // flight together, and folds each batch into its running (M, L, O).
+  constexpr int kMergeBatch = 24;
+  for (int i = tid; i < G * D; i += blockDim.x) {
+    const int h = i / D, c = i % D;
+    const float* ph = part + h * (D + 2);
+    float M = -INFINITY, L = 0.f, O = 0.f;
+    for (int s0 = 0; s0 < n_split; s0 += kMergeBatch) {
+      float mv[kMergeBatch], lv[kMergeBatch], ov[kMergeBatch];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
-      const float Mn = fmaxf(Mo, mc);
-      const float so = (Mo == -INFINITY) ? 0.f : exp2f(Mo - Mn);
-      float L = 0.f;
-      for (int sp = lane; sp < ns; sp += 32) {
-        const float ms = buf[sp * per + h * (D + 2) + D];
-        const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - Mn);
-        wts[h * chunk + sp] = wgt;
-        L = fmaf(wgt, buf[sp * per + h * (D + 2) + D + 1], L);
+      for (int k = 0; k < kMergeBatch; ++k) {
+        const bool in = s0 + k < n_split;
+        const float* ps = ph + (int64_t)(s0 + k) * pstride;
+        mv[k] = in ? __ldcg(ps + D) : -INFINITY;
+        lv[k] = in ? __ldcg(ps + D + 1) : 0.f;
+        ov[k] = in ? __ldcg(ps + c) : 0.f;
       }
+      float Mn = M;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      if (lane == 0) {
-        Mh[h] = Mn;
-        Lh[h] = Lh[h] * so + L;
-        Sh[h] = so;
+      for (int k = 0; k < kMergeBatch; ++k) Mn = fmaxf(Mn, mv[k]);
+      if (Mn == -INFINITY) continue;  // no token seen so far
+      const float so = M == -INFINITY ? 0.f : ex2(M - Mn);
+      float l1 = 0.f, o1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMergeBatch; ++k) {
+        const float w = ex2(mv[k] - Mn);  // 0 for a split without tokens (m = -inf)
+        l1 = fmaf(w, lv[k], l1);
+        o1 = fmaf(w, ov[k], o1);
       }
+      L = fmaf(L, so, l1);
+      O = fmaf(O, so, o1);
+      M = Mn;
     }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = tid + k * blockDim.x;
-      if (i < G * D) {
-        const int h = i / D, c = i % D;
-        const float* wh = wts + h * chunk;
-        const float* bh = buf + h * (D + 2) + c;
-        float a0 = o[k] * Sh[h], a1 = 0.f;
-        int sp = 0;
-        for (; sp + 1 < ns; sp += 2) {
-          a0 = fmaf(wh[sp], bh[sp * per], a0);
-          a1 = fmaf(wh[sp + 1], bh[(sp + 1) * per], a1);
-        }
-        if (sp < ns) a0 = fmaf(wh[sp], bh[sp * per], a0);
-        o[k] = a0 + a1;
-      }
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int i = tid + k * blockDim.x;
-    if (i < G * D) {
-      const int h = i / D, c = i % D;
-      const float L = Lh[h];
-      P.out[((int64_t)b * P.h_q + j * G + h) * D + c] = L > 0.f ? o[k] / L : 0.f;
-    }
+    P.out[((int64_t)b * P.h_q + j * G + h) * D + c] = L > 0.f ? O / L : 0.f;
   }
 }
 

@@ -91,10 +91,20 @@ typedef struct rdkv_plan_header {
   int64_t max_stage_bytes; /* largest tile plus the zone-B rows it carries (decode staging) */
 } rdkv_plan_header;
 
-/* Host copy of the totals, from rdkv_plan_sizes. */
+/* Heads whose decode work rdkv_plan_sizes estimates for the host (see rdkv_sizes). */
+#define RDKV_COST_HEADS 64
+
+/* Host copy of the totals, from rdkv_plan_sizes.  head_cost[h], for the first
+ * min(n_heads, RDKV_COST_HEADS) (sequence, KV head) pairs in plan order, is an
+ * estimate (> 0, arbitrary units) of the zone-A decode work of that head; the
+ * decode calls deal their blocks to the heads in proportion to it on the host.
+ * When it is not filled (zeros: more than RDKV_COST_HEADS heads, or a record
+ * built by hand) the decode kernel deals the blocks itself from the plan.  Only
+ * the speed of the decode depends on these numbers, never its result. */
 typedef struct rdkv_sizes {
   int64_t zone_a_bytes, zone_b_rows, index_slots, kept_tokens, max_tile_bytes, max_stage_bytes;
   int32_t status, n_heads;
+  int32_t head_cost[RDKV_COST_HEADS];
 } rdkv_sizes;
 
 /* A packed TriZone cache.  All pointers are caller-owned device memory.

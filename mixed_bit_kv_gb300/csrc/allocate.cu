@@ -15,6 +15,7 @@
 // weighted by their bits, and keeps the smallest digit whose upper tail fits.
 // Four levels give the exact minimum; the counts are integers, so the result
 // does not depend on the order of the additions.
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -543,6 +544,17 @@ extern "C" rdkv_status rdkv_plan_sizes(const void* plan, rdkv_sizes* out, void* 
   out->max_stage_bytes = h.max_stage_bytes;
   out->status = h.status;
   out->n_heads = h.n_heads;
+  for (int i = 0; i < RDKV_COST_HEADS; ++i) out->head_cost[i] = 0;
+  if (h.status == RDKV_OK && h.n_heads > 0 && h.n_heads <= RDKV_COST_HEADS) {
+    // the head records, for the decode's estimate of each head's work
+    rdkv_head_plan hp[RDKV_COST_HEADS];
+    RDKV_TRY_CUDA(cudaMemcpyAsync(hp, static_cast<const char*>(plan) + h.heads_off, sizeof(rdkv_head_plan) * h.n_heads,
+                                  cudaMemcpyDeviceToHost, (cudaStream_t)stream),
+                  "plan heads read");
+    RDKV_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "plan heads read sync");
+    for (int i = 0; i < h.n_heads; ++i)
+      out->head_cost[i] = (int32_t)std::min<int64_t>(std::max<int64_t>(1, head_cost_a(hp[i])), 0x7fffffff);
+  }
   if (h.status != RDKV_OK) set_error("plan status %d: a gain was NaN, infinite or negative", h.status);
   return (rdkv_status)h.status;
 }

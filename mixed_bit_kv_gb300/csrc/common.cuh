@@ -39,6 +39,20 @@ __host__ __device__ inline PlanLayout plan_layout(int batch, int h_kv, int head_
   return L;
 }
 
+// Estimated zone-A decode cost of a head (instruction units per warp) from its plan record: every
+// tile pays a base (softmax, staging) plus its K k-blocks (quantised blocks cost about twice a raw
+// 16-bit one) plus its V class.  Only the ratios between heads matter: they decide how many
+// blocks each head gets.
+__host__ __device__ inline int64_t head_cost_a(const rdkv_head_plan& hp) {
+  const int nkb16 = ceil_div(hp.k_words[0] * 2, 16);
+  const int nkbq = ceil_div(hp.k_words[1] * 4, 16) + ceil_div(hp.k_words[2] * 8, 16) + ceil_div(hp.k_words[3] * 16, 16);
+  const int64_t per_tile = 250 + 20 * nkb16 + 40 * nkbq;
+  return (int64_t)hp.tiles[0] * (per_tile + 200) + (int64_t)hp.tiles[1] * (per_tile + 215) +
+         (int64_t)hp.tiles[2] * (per_tile + 250) + (int64_t)hp.tiles[3] * (per_tile + 60);
+}
+// ... and of one zone-C block of 16 rows
+constexpr int kZoneCBlockCost = 300;
+
 __device__ __forceinline__ const rdkv_plan_header* plan_header(const void* plan) {
   return reinterpret_cast<const rdkv_plan_header*>(plan);
 }

@@ -32,6 +32,9 @@ namespace rdkv {
 
 constexpr int kDecWarps = 16;  // one block per SM
 constexpr int kMaxInflight = 4;
+constexpr int kPrologueItems = 2;
+constexpr int kMaxDealtBlocks = 256;  // grids up to this size may be dealt to heads on the host
+constexpr uint8_t kNoHead = 0xff;  // copies a warp issues before the wait for the previous kernel
 constexpr int kCRows = 16;        // zone-C rows per work item
 constexpr int kMaxKB = 16;        // k-blocks of a K row (D = 128: at most 13)
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at GB300 clocks
@@ -77,6 +80,9 @@ struct DecodeParams {
   const rdkv_head_plan* heads;  // the plan's head records (offset fixed by the shape)
   const int16_t* slots;         // the plan's slot tables, slot_stride entries per head
   int dtype, h_q, h_kv, cap_c, ring_bytes, ring_warps, ctas, n_heads, slot_stride;
+  int dealt;                    // 1: blocks dealt to heads on the host (below); 0: by the kernel
+  uint8_t block_head[kMaxDealtBlocks];       // head of each block, kNoHead for a block without work
+  int16_t head_first[RDKV_COST_HEADS + 1];   // first block of each head; [n_heads] = end
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -539,16 +545,9 @@ __device__ __forceinline__ void pv_fp16(WarpAcc<D>& acc, uint32_t vrows, int lan
   }
 }
 
-// Estimated decode cost of a head (instruction units per warp) from its plan record: every tile
-// pays a base (softmax, staging) plus its K k-blocks (quantised blocks cost about twice a raw
-// 16-bit one) plus its V class; every zone-C block of 16 rows pays a flat amount.  Only the ratios
-// between heads matter: they decide how many blocks each head gets.
-__device__ __forceinline__ int64_t head_cost(const rdkv_head_plan& hp, int zc_blocks) {
-  const int nkb16 = ceil_div(hp.k_words[0] * 2, 16);
-  const int nkbq = ceil_div(hp.k_words[1] * 4, 16) + ceil_div(hp.k_words[2] * 8, 16) + ceil_div(hp.k_words[3] * 16, 16);
-  const int64_t per_tile = 250 + 20 * nkb16 + 40 * nkbq;
-  return (int64_t)hp.tiles[0] * (per_tile + 200) + (int64_t)hp.tiles[1] * (per_tile + 215) +
-         (int64_t)hp.tiles[2] * (per_tile + 250) + (int64_t)hp.tiles[3] * (per_tile + 60) + (int64_t)zc_blocks * 300;
+// Estimated decode cost of a head: its zone-A tiles and its zone-C blocks.
+__host__ __device__ __forceinline__ int64_t head_cost(const rdkv_head_plan& hp, int zc_blocks) {
+  return head_cost_a(hp) + (int64_t)zc_blocks * kZoneCBlockCost;
 }
 
 // Per-class values of a head, read with a class index without dynamic array indexing.
@@ -558,7 +557,7 @@ struct ClassVals {
 };
 
 template <int D, bool QLO>
-__global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams P) {
+__global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.h_q / P.h_kv;
@@ -566,7 +565,21 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int asg[3];  // head, first block of the head, blocks of the head
   __shared__ __align__(16) rdkv_head_plan hp_s;  // this block's head record
-  if (warp == 0) {
+  int16_t slot_pre = -1;  // dealt on the host: this thread's slot-table entry, loaded with the record
+  if (P.dealt) {
+    // dealt on the host: this block's head and split range are kernel arguments
+    const int hb = P.block_head[blockIdx.x];
+    if (hb != kNoHead && tid < P.slot_stride) slot_pre = P.slots[(int64_t)hb * P.slot_stride + tid];
+    if (warp == 0) {
+      if (lane == 0) {
+        asg[0] = hb == kNoHead ? -1 : hb;
+        asg[1] = hb == kNoHead ? 0 : P.head_first[hb];
+        asg[2] = hb == kNoHead ? 0 : P.head_first[hb + 1] - P.head_first[hb];
+      }
+      if (hb != kNoHead)  // the head record into shared memory, one word per lane
+        reinterpret_cast<int32_t*>(&hp_s)[lane] = reinterpret_cast<const int32_t*>(P.heads + hb)[lane];
+    }
+  } else if (warp == 0) {
     // Blocks are dealt to heads in proportion to their estimated cost, at least one per head, over a
     // nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the blocks past the last head's
     // range leave at once.  Warp 0: one lane per head, one round trip for the plan records and the
@@ -615,7 +628,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
   const int qbase = b * P.h_q + j * G;
   const int16_t* slot_ch = P.slots + (int64_t)head * P.slot_stride;
   const int k_slots = hpp->k_slots;  // <= D + kSlotPad <= the block's threads
-  const int16_t sr = tid < k_slots ? slot_ch[tid] : (int16_t)-1;
+  const int16_t sr = tid < k_slots ? (P.dealt ? slot_pre : slot_ch[tid]) : (int16_t)-1;
 
   // shared memory map
   KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
@@ -708,9 +721,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
   int issued = 0, done = 0;
   bool drained = warp >= P.ring_warps;  // lane 0: no item left for this warp (warps without a ring take none)
   int pending = -1;                    // lane 0: item taken but not yet issued (ring full)
+  int cap = kPrologueItems;  // items in flight per warp: fewer before the loop starts
   auto issue = [&]() {
     if (issued == done) head_p = used = 0;  // empty ring: start at its beginning
-    while (!drained && issued - done < kMaxInflight) {
+    while (!drained && issued - done < cap) {
       int it = pending;
       if (it < 0) it = split + n_split * atomicAdd(&next_k, 1);  // taken in order of need: no warp idles early
       if (it >= n_items) {
@@ -831,6 +845,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(DecodeParams 
   }
   __syncthreads();
 
+  cap = kMaxInflight;
   WarpAcc<D> acc;
 #pragma unroll
   for (int cm = 0; cm < D / 16; ++cm) acc.o[cm][0] = acc.o[cm][1] = acc.o[cm][2] = acc.o[cm][3] = 0.f;
@@ -1119,7 +1134,12 @@ static DecodeGeom decode_geom(const rdkv_cache* c) {
   // blocks dealt to heads in proportion to their work: a nominal count that fills every SM once,
   // fewer when there is little work (at least kDecWarps items per block on average)
   const int64_t items = ceil_div64(c->sizes.index_slots, kTile) + (int64_t)n_heads * ceil_div(c->cap_c, kCRows);
-  g.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)blocks_per_sm * sms, ceil_div64(items, kDecWarps)));
+  // With few heads, leave one SM per head free: the last block of each head merges after the
+  // others have left, and on those SMs the next call's blocks would otherwise start only after
+  // the merge, with their whole set-up still ahead of them.
+  const int free_sms = n_heads <= sms / 16 ? n_heads : 0;
+  g.ctas = (int)std::max<int64_t>(
+      1, std::min<int64_t>((int64_t)blocks_per_sm * (sms - free_sms), ceil_div64(items, kDecWarps)));
   g.splits = g.ctas + n_heads;  // grid size
   g.partial_bytes = (size_t)align_up((int64_t)g.splits * partial_stride(G, D) * 4, 256);
   g.ticket_off = g.partial_bytes;
@@ -1165,6 +1185,28 @@ static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo
   P.ring_bytes = geo.ring_bytes;
   P.ring_warps = geo.ring_warps;
   P.ctas = geo.ctas;
+  // Deal the blocks to the heads here when the plan's cost estimates reached the host: the kernel
+  // then knows its head at once instead of reading every head record first.  The rule is the
+  // kernel's own (at least one block per head, the rest in proportion to the cost).
+  P.dealt = 0;
+  bool known = n_heads <= RDKV_COST_HEADS && geo.splits <= kMaxDealtBlocks && cache->sizes.n_heads == n_heads;
+  for (int h = 0; known && h < n_heads; ++h) known = cache->sizes.head_cost[h] > 0;
+  if (known) {
+    const int zc = ceil_div(cache->cap_c, kCRows);
+    int64_t total = 0;
+    for (int h = 0; h < n_heads; ++h) total += cache->sizes.head_cost[h] + (int64_t)zc * kZoneCBlockCost;
+    int start = 0;
+    for (int h = 0; h < n_heads; ++h) {
+      const int64_t w = cache->sizes.head_cost[h] + (int64_t)zc * kZoneCBlockCost;
+      const int c = std::max(1, (int)(w * geo.ctas / total));
+      P.head_first[h] = (int16_t)start;
+      for (int k = 0; k < c; ++k) P.block_head[start + k] = (uint8_t)h;
+      start += c;
+    }
+    P.head_first[n_heads] = (int16_t)start;
+    for (int k = start; k < geo.splits; ++k) P.block_head[k] = kNoHead;
+    P.dealt = 1;
+  }
   return P;
 }
 

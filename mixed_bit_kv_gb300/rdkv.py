@@ -40,10 +40,13 @@ class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("batch", "n_tokens", "h_q", "h_kv", "head_dim", "window", "dtype")]
 
 
+COST_HEADS = 64  # RDKV_COST_HEADS
+
+
 class Sizes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("zone_a_bytes", "zone_b_rows", "index_slots", "kept_tokens",
                                                "max_tile_bytes", "max_stage_bytes")] + [
-        ("status", ctypes.c_int32), ("n_heads", ctypes.c_int32)]
+        ("status", ctypes.c_int32), ("n_heads", ctypes.c_int32), ("head_cost", ctypes.c_int32 * COST_HEADS)]
 
 
 class CacheStruct(ctypes.Structure):

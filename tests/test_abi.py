@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(L):
 def test_version_and_struct_sizes(L):
     assert L.rdkv_version() >= 1
     assert ctypes.sizeof(rdkv.Shape) == 28
-    assert ctypes.sizeof(rdkv.Sizes) == 56
+    assert ctypes.sizeof(rdkv.Sizes) == 56 + 4 * rdkv.COST_HEADS
     import numpy as np
     assert np.dtype(rdkv.HEAD_PLAN_DTYPE).itemsize == 128
     assert np.dtype(rdkv.PLAN_HEADER_DTYPE).itemsize == 96

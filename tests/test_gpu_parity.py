@@ -176,6 +176,37 @@ def test_decode_matches_oracle(case, budget):
     assert rdkv.rdkv_decode_status(cache) == 0
 
 
+@pytest.mark.parametrize("case", ["small_f16", "zipf_f16"])
+def test_decode_block_dealing_host_and_kernel(case):
+    """The blocks are dealt to the heads on the host from the plan's cost estimates (filled by
+    rdkv_plan_sizes), or by the kernel itself when they are missing; any estimate gives the
+    same attention (only the split of the work changes)."""
+    w = CASES[case]
+    (q, k, v), _, shape, sc, al, sizes, cache = _compress(w, w.budgets[0], w.budgets[0], cap_extra=2)
+    n_heads = w.batch * w.h_kv
+    costs = list(sizes.head_cost)
+    assert all(c > 0 for c in costs[:n_heads]) and all(c == 0 for c in costs[n_heads:])
+    ref = O.pack(k.numpy(), v.numpy(), al["bits_tok"].cpu().numpy(), al["bits_chan"].cpu().numpy(), w.window,
+                 cap_c=w.window + 2)
+    qn, kn, vn = synth.decode_step(w, 0)
+    rdkv.rdkv_append(cache, kn.to(DEV), vn.to(DEV))
+    O.append(ref, kn.numpy(), vn.numpy())
+    exp = O.decode(ref, qn.numpy())
+    outs = []
+    for variant in ("host", "kernel", "skewed"):
+        for h in range(rdkv.COST_HEADS):
+            cache.c.sizes.head_cost[h] = {"host": costs[h], "kernel": 0,
+                                          "skewed": (1 if h % 2 else 1000000) if h < n_heads else 0}[variant]
+        out = rdkv.rdkv_decode_attn(cache, qn.to(DEV)).cpu().numpy()
+        assert np.abs(out - exp).max() <= 2e-3, variant
+        outs.append(out)
+    assert rdkv.rdkv_decode_status(cache) == 0
+    # a different split of the tokens moves the softmax's running reference and with it the
+    # fp16 rounding of the probabilities: the outputs agree to that rounding
+    d = np.abs(outs[0] - outs[1])
+    assert d.max() <= 2e-3 and d.mean() <= 5e-5, (d.max(), d.mean())
+
+
 def test_decode_without_window_and_empty_zone_c():
     """W = 0: before any append the cache may be empty for a zero budget (output 0)."""
     w = CASES["small_f16"].scaled(window=0)

@@ -1002,32 +1002,28 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   }
   __syncthreads();
   // combine the warps; write this block's partial result (m, l, unnormalised o) for the G heads;
-  // one block's partial takes pstride floats (a multiple of 4: the merge copies it as float4)
+  // one block's partial takes pstride floats
   const int pstride = partial_stride(G, D);
   float* part = P.partial + (int64_t)first_block * pstride;
   float* mine = part + (int64_t)split * pstride;
-  // the warps' weights 2^(m_w - M) per head, once: thread (h, w) of the first 8 G threads
-  __shared__ float wred[8][kDecWarps], mred[8];
-  static_assert(kDecWarps == 16, "one group of 16 lanes per head");
-  if (tid < 8 * kDecWarps) {  // whole warps 0-3 take part in the shuffles (16 G <= 128)
-    const int h = tid / kDecWarps, w = tid % kDecWarps;
-    const float mw = h < G ? red[((int64_t)w * 8 + h) * (D + 2) + D] : -INFINITY;
-    float M = mw;
-#pragma unroll
-    for (int o = 1; o < kDecWarps; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (h < G) {
-      wred[h][w] = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      if (w == 0) mred[h] = M;
-    }
-  }
-  __syncthreads();
+  // each element: the block's running max M of its head over the warps, then the warps' results
+  // weighted by 2^(m_w - M) (the m (c = D) entry holds M)
   for (int i = tid; i < G * (D + 2); i += blockDim.x) {
     const int h = i / (D + 2), c = i % (D + 2);
-    float val = mred[h];
+    float mw[kDecWarps];
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      mw[w] = red[((int64_t)w * 8 + h) * (D + 2) + D];
+      M = fmaxf(M, mw[w]);
+    }
+    float val = M;
     if (c != D) {
       val = 0.f;
+      if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) val = fmaf(wred[h][w], red[((int64_t)w * 8 + h) * (D + 2) + c], val);
+        for (int w = 0; w < kDecWarps; ++w) val = fmaf(ex2(mw[w] - M), red[((int64_t)w * 8 + h) * (D + 2) + c], val);
+      }
     }
     mine[i] = val;
   }

@@ -351,12 +351,19 @@ __device__ __forceinline__ void k_segment(const unsigned char* kw, const unsigne
 // the zeros, so zacc[2], zacc[3] carry it for heads (2q, 2q+1).  A segment's
 // k-blocks are consecutive: 64 W bytes of words and 64 bytes of metadata
 // apart, and only the last one may be partial.
-template <int W>
+// PK (at most 4 heads): the hi and lo operands share one MMA.  B columns 0-3
+// take hi of heads 0-3 and columns 4-7 lo of the same heads (lanes g >= 4 of
+// the query fragments hold head g - 4), so one product gives both and shi
+// holds hi in its columns (2q, 2q+1) for q < 2 and lo for q >= 2; slo is unused.
+template <int W, bool PK>
 __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsigned char* kmeta, int kb0, int kb1,
                                             const KBDesc* kbd, const uint2* qh, int lane, float (&shi)[2][4],
                                             float (&slo)[2][4], float (&zacc)[4]) {
   if (kb0 >= kb1) return;
   const int g = lane >> 2, q = lane & 3;
+  // PK: lo lanes take q * scale - fp16(q * scale), hi lanes fp16(q * scale); raw channels only hi
+  const bool lo_lane = PK && g >= 4;
+  const __half2 lo_sel = lo_lane ? __half2(__float2half(-1.f), __float2half(-1.f)) : __half2(__float2half(0.f), __float2half(0.f));
   constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
   const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
   const int sh1 = W == 2 ? 2 * q + 8 : sh0;
@@ -376,8 +383,19 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsig
     // tokens g, g+8, g+16, g+24 of the lane's two words (one word for 2-bit codes)
     const uint4 y0 = lds128(kw, wb + c0);
     const uint4 y1 = W == 2 ? y0 : lds128(kw, wb + c1);
-    uint32_t bh0 = qq.x, bh1 = qq.y, bl0 = 0, bl1 = 0;
-    if (W != 16) {
+    uint32_t bh0 = lo_lane ? 0u : qq.x, bh1 = lo_lane ? 0u : qq.y, bl0 = 0, bl1 = 0;
+    if (W != 16 && PK) {
+      const uint2 m0 = lds64(kmeta, mb + (v0 ? 8u * q : 0u));
+      const uint2 m1 = lds64(kmeta, mb + (v1 ? 8u * (q + 4) : 0u));
+      const __half2 q0 = *reinterpret_cast<const __half2*>(&qq.x), q1 = *reinterpret_cast<const __half2*>(&qq.y);
+      const __half2 s0 = *reinterpret_cast<const __half2*>(&m0.x), s1 = *reinterpret_cast<const __half2*>(&m1.x);
+      // hi: q * scale + 0 rounded once; lo: q * scale - hi, exact
+      const __half2 h0 = __hmul2(q0, s0), h1 = __hmul2(q1, s1);
+      const __half2 b0 = __hfma2(q0, s0, __hmul2(h0, lo_sel)), b1 = __hfma2(q1, s1, __hmul2(h1, lo_sel));
+      bh0 = *reinterpret_cast<const uint32_t*>(&b0);
+      bh1 = *reinterpret_cast<const uint32_t*>(&b1);
+      mma16816(zacc, m0.x, m0.y, m1.x, m1.y, qq.x, qq.y);
+    } else if (W != 16) {
       // a pair past the segment end reads the block's first pair (its q entries are 0)
       const uint2 m0 = lds64(kmeta, mb + (v0 ? 8u * q : 0u));
       const uint2 m1 = lds64(kmeta, mb + (v1 ? 8u * (q + 4) : 0u));
@@ -406,13 +424,13 @@ __device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsig
         const uint32_t a2 = W == 8 ? __byte_perm(x2, 0u, bsel) : (x2 >> sh1) & mask2;
         const uint32_t a3 = W == 8 ? __byte_perm(x3, 0u, bsel) : (x3 >> sh1) & mask2;
         mma16816(shi[tb], a0, a1, a2, a3, bh0, bh1);
-        mma16816(slo[tb], a0, a1, a2, a3, bl0, bl1);
+        if (!PK) mma16816(slo[tb], a0, a1, a2, a3, bl0, bl1);
       }
     }
   }
 }
 
-template <int D, bool QLO>
+template <int D, bool QLO, bool PK>
 __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsigned char* kmeta, const int (&seg_kb)[5],
                                             const KBDesc* kbd, const float4* qv, int lane,
                                             float (&s)[2][4]) {
@@ -436,19 +454,20 @@ __device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsig
     float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // [2], [3]: zero-point term of heads 2q, 2q+1
     // raw 16-bit channels first, at scale 1 in s; then s moves to 2^-24 and takes the hi products
     float slo[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    k_segment_h<16>(kw, kmeta, seg_kb[0], seg_kb[1], kbd, qh, lane, s, slo, zacc);
+    k_segment_h<16, PK>(kw, kmeta, seg_kb[0], seg_kb[1], kbd, qh, lane, s, slo, zacc);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[tb][e] *= 5.9604644775390625e-8f;
-    k_segment_h<8>(kw, kmeta, seg_kb[1], seg_kb[2], kbd, qh, lane, s, slo, zacc);
-    k_segment_h<4>(kw, kmeta, seg_kb[2], seg_kb[3], kbd, qh, lane, s, slo, zacc);
-    k_segment_h<2>(kw, kmeta, seg_kb[3], seg_kb[4], kbd, qh, lane, s, slo, zacc);
-    // back to scale 1
+    k_segment_h<8, PK>(kw, kmeta, seg_kb[1], seg_kb[2], kbd, qh, lane, s, slo, zacc);
+    k_segment_h<4, PK>(kw, kmeta, seg_kb[2], seg_kb[3], kbd, qh, lane, s, slo, zacc);
+    k_segment_h<2, PK>(kw, kmeta, seg_kb[3], seg_kb[4], kbd, qh, lane, s, slo, zacc);
+    // back to scale 1; PK: the lo columns (2q + 4, 2q + 5) are held by lane q ^ 2
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[tb][e] = (s[tb][e] + slo[tb][e]) * 16777216.f;
+      for (int e = 0; e < 4; ++e)
+        s[tb][e] = (s[tb][e] + (PK ? __shfl_xor_sync(0xffffffffu, s[tb][e], 2) : slo[tb][e])) * 16777216.f;
     be = zacc[2];
     bo = zacc[3];
   }
@@ -556,7 +575,7 @@ struct ClassVals {
   __device__ __forceinline__ int64_t operator()(int c) const { return c == 0 ? v[0] : c == 1 ? v[1] : c == 2 ? v[2] : v[3]; }
 };
 
-template <int D, bool QLO>
+template <int D, bool QLO, bool PK>
 __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -798,7 +817,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int i = tid + r * kDecWarps * 32;
-    const int kb = i >> 5, ln = i & 31, g = ln >> 2, qq = ln & 3;
+    const int kb = i >> 5, ln = i & 31, qq = ln & 3;
+    // the head of column g: zone-A fragments with PK hold heads 0-3 twice (hi and lo columns)
+    const int g = (PK && kb < nkb) ? (ln >> 2) & 3 : ln >> 2;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int off = 2 * qq + (e & 1) + 8 * (e >> 1);
@@ -878,7 +899,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       const unsigned char* stp = wring + wpos[slot];
       const unsigned char* kmeta = stp + 4 * kTile * RW;
       float s[2][4];
-      tile_logits<D, QLO>(stp, kmeta, seg_kb, kbd, qv, lane, s);
+      tile_logits<D, QLO, PK>(stp, kmeta, seg_kb, kbd, qv, lane, s);
 #pragma unroll
       for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
@@ -1212,15 +1233,19 @@ static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo
 static rdkv_status launch_decode(const DecodeParams& P, const DecodeGeom& geo, const rdkv_shape& s, cudaStream_t cs,
                                  bool pdl) {
   // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is captured)
-  static size_t smem_set[4][64] = {};
+  static size_t smem_set[6][64] = {};
   int dev = 0;
   RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
   const bool qlo = s.dtype == RDKV_F32;
-  const int ki = (s.head_dim == 128 ? 2 : 0) + (qlo ? 1 : 0);
-  void (*const fn)(DecodeParams) = ki == 3 ? decode_kernel<128, true>
-                                 : ki == 2 ? decode_kernel<128, false>
-                                 : ki == 1 ? decode_kernel<64, true>
-                                           : decode_kernel<64, false>;
+  // fp16 queries and at most 4 heads per KV head: hi and lo share one MMA per K block
+  const bool pk = !qlo && s.h_q / s.h_kv <= 4;
+  const int ki = (s.head_dim == 128 ? 3 : 0) + (qlo ? 1 : pk ? 2 : 0);
+  void (*const fn)(DecodeParams) = ki == 4 ? decode_kernel<128, true, false>
+                                 : ki == 5 ? decode_kernel<128, false, true>
+                                 : ki == 3 ? decode_kernel<128, false, false>
+                                 : ki == 1 ? decode_kernel<64, true, false>
+                                 : ki == 2 ? decode_kernel<64, false, true>
+                                           : decode_kernel<64, false, false>;
   if (dev < 64 && geo.smem > smem_set[ki][dev]) {
     RDKV_TRY_CUDA(cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kDecodeSmemLimit),

@@ -3,7 +3,7 @@
 // fp16 inputs, on the 5th-generation tensor cores.
 //
 // Both passes multiply a stationary block of 128 rows (operand A) by a stream
-// of 128-row tiles (operand B), tile = A . B^T into a 128 x 128 fp32 tensor
+// of 256-row tiles (operand B), tile = A . B^T into a 128 x 256 fp32 tensor
 // memory accumulator:
 //   pass 1  A = 128 query rows of head h, B = key tiles t <= tau.  The epilogue
 //           keeps, per query row, the running max and sum of 2^(s*c) and writes
@@ -11,11 +11,11 @@
 //   pass 2  A = 128 keys of KV head j, B = query tiles tau >= t of the G heads
 //           of the group.  The epilogue adds 2^(s*c - lse2[tau]) per key:
 //           the column sums of the attention, i.e. w_t; then g_t = w_t * sigma_t.
-// Roles (576 threads): warp 0 loads tiles with TMA into a 4-stage ring; warp 1
-// issues tcgen05.mma (one thread) into four TMEM accumulators; warps 2..17 read
-// the accumulators back (four warps per TMEM lane quarter, one per 32-column
-// slice, so every SM sub-partition interleaves four of them) and run the
-// softmax arithmetic.  Every wait is bounded: a wait that
+// Roles (576 threads): warp 0 loads tiles with TMA into a 2-stage ring of 64 KB
+// stages; warp 1 issues tcgen05.mma (one thread) into two 256-column TMEM
+// accumulators; warps 2..17 read the accumulators back (four warps per TMEM
+// lane quarter, one per 64-column slice, so every SM sub-partition interleaves
+// four of them) and run the softmax arithmetic.  Every wait is bounded: a wait that
 // runs out writes NaN into the affected outputs, which the allocation reports
 // as invalid gains.
 #include <cuda.h>

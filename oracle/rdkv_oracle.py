@@ -41,6 +41,8 @@ Readings where the pages are silent (each is a project decision):
  R7 16-bit K channels are stored raw in fp16 inside zone A; 0-bit K channels
     are dropped and contribute nothing to the logits.
  R8 Byte layout of the zones: see ``pack``.
+ R9 Zone-C re-compression (new tokens joining zones A and B): see the last
+    section, above ``attention_lse``.
 """
 from __future__ import annotations
 
@@ -633,3 +635,118 @@ def decode_bytes(plan, head_dim, h_q, h_kv, len_c, batch):
         total += k_payload + k_meta + v_payload + len_c * 4 * D
     total += batch * h_q * D * (2 + 4)
     return total
+
+
+# ---------------------------------------------------------------------------
+# Zone-C re-compression (next row beside the method).  New tokens start in
+# zone C at fp16 (RDKV section 2.3); the pages do not say how they later join
+# zones A and B.  Reading R9 (a project decision):
+#  * the oldest rows of zone C (all but a recent tail) move into a new segment,
+#    a TriZone cache of their own with no window;
+#  * their token weights are the attention the recent decode queries gave
+#    them: w_t = sum over recent queries tau and the G heads of the group of
+#    exp(q.k_t / sqrt(D) - lse_tau,h), lse the log-sum-exp of that decode;
+#    sigma_t and g_t as in step 1;
+#  * the allocation is incremental: the instance keeps its water levels
+#    lambda_V, lambda_K of the prefill and the moved units take the Lagrangian
+#    choice at those levels (section 2.2), K channels over the moved kept
+#    tokens with the prefill's channel weights w_c;
+#  * the attention over several segments and the live zone C is the softmax
+#    over the union of their keys, merged from each part's output and
+#    log-sum-exp.
+# ---------------------------------------------------------------------------
+def attention_lse(q, K, V):
+    """attention(q, K, V) and its log-sum-exp ln sum_t exp(q . k_t / sqrt(D)); -inf with no rows."""
+    q = _f64(q)
+    if K.shape[0] == 0:
+        return np.zeros(q.shape[-1]), -np.inf
+    s = _f64(K) @ q / math.sqrt(q.shape[-1])
+    m = s.max()
+    e = np.exp(s - m)
+    return (e @ _f64(V)) / e.sum(), m + math.log(e.sum())
+
+
+def decode_lse(cache, q, unpacked=None):
+    """decode() and the log-sum-exp of every query head: (out [B, H_q, D], lse [B, H_q]) float64."""
+    q64 = _f64(q)
+    B, Hq, D = q64.shape
+    Hkv = cache["zone_c_k"].shape[1]
+    G = Hq // Hkv
+    un = unpacked if unpacked is not None else unpack(cache, D)
+    L = cache["len_c"]
+    out, lse = np.zeros((B, Hq, D)), np.full((B, Hq), -np.inf)
+    for b in range(B):
+        for j in range(Hkv):
+            _, Ka, Va = un[b * Hkv + j]
+            K = np.concatenate([Ka, cache["zone_c_k"][b, j, :L].astype(np.float64)])
+            V = np.concatenate([Va, cache["zone_c_v"][b, j, :L].astype(np.float64)])
+            for h in range(j * G, (j + 1) * G):
+                out[b, h], lse[b, h] = attention_lse(q64[b, h], K, V)
+    return out, lse
+
+
+def merge_attention(outs, lses):
+    """Attention over the union of disjoint key sets from each part's output and log-sum-exp:
+    out = sum_i e^(lse_i) out_i / sum_i e^(lse_i), lse = ln sum_i e^(lse_i).
+    outs [P, ..., D], lses [P, ...]; parts without keys (lse = -inf) weigh 0; no keys at all: 0, -inf."""
+    outs, lses = _f64(outs), _f64(lses)
+    m = lses.max(axis=0)
+    safe = np.where(np.isfinite(m), m, 0.0)
+    wts = np.where(np.isfinite(lses), np.exp(lses - safe[None]), 0.0)
+    tot = wts.sum(axis=0)
+    out = np.where(tot[..., None] > 0, (wts[..., None] * outs).sum(axis=0) / np.where(tot > 0, tot, 1.0)[..., None],
+                   0.0)
+    lse = np.where(tot > 0, safe + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+    return out, lse
+
+
+def take_zone_c(cache, n_move):
+    """Removes rows [0, n_move) of zone C: returns them as k, v [B, n_move, H_kv, D] (fp16 values)
+    and moves rows [n_move, len_c) to the front."""
+    L = cache["len_c"]
+    if not 0 < n_move <= L:
+        raise ValueError("n_move outside (0, len_c]")
+    k = cache["zone_c_k"][:, :, :n_move].transpose(0, 2, 1, 3).copy()
+    v = cache["zone_c_v"][:, :, :n_move].transpose(0, 2, 1, 3).copy()
+    rest = L - n_move
+    cache["zone_c_k"][:, :, :rest] = cache["zone_c_k"][:, :, n_move:L].copy()
+    cache["zone_c_v"][:, :, :rest] = cache["zone_c_v"][:, :, n_move:L].copy()
+    cache["len_c"] = rest
+    return k, v
+
+
+def recent_token_weights(k_seg, q_recent, lse_recent):
+    """R9 token weights of moved tokens.  k_seg [n, H_kv, D], q_recent [R, H_q, D], lse_recent
+    [R, H_q] (natural log) -> w [H_kv, n] float64: sum over the R queries and the G heads of the
+    group of exp(q . k_t / sqrt(D) - lse)."""
+    k64, q64, l64 = _f64(k_seg), _f64(q_recent), _f64(lse_recent)
+    n, Hkv, D = k64.shape
+    R, Hq, _ = q64.shape
+    G = Hq // Hkv
+    w = np.zeros((Hkv, n))
+    for h in range(Hq):
+        j = h // G
+        s = q64[:, h, :] @ k64[:, j, :].T / math.sqrt(D)       # [R, n]
+        w[j] += np.exp(s - l64[:, h][:, None]).sum(axis=0)
+    return w
+
+
+def recompress_gains(k_seg, v_seg, q_recent, lse_recent):
+    """R9 step 1 for the moved tokens of one sequence: w_tok, sigma_tok (float32) and g_tok."""
+    w = recent_token_weights(k_seg, q_recent, lse_recent)
+    sig = value_spread(v_seg)
+    n = k_seg.shape[0]
+    return dict(w_tok=w.astype(np.float32), sigma_tok=sig.astype(np.float32), g_tok=token_gains(w, sig, n))
+
+
+def allocate_at_levels(g_tok, w_chan, k, lam_v, lam_k):
+    """R9 incremental allocation of one sequence: V widths at water level lam_v, then sigma_c over
+    the kept moved tokens, g_c = fl32(w_c * sigma_c) and K widths at lam_k (section 2.2 steps 2-3
+    with the levels given instead of found)."""
+    g_tok = np.asarray(g_tok, np.float32)
+    Hkv, n = g_tok.shape
+    bits_tok = widths_at(breakpoints(g_tok), lam_v).astype(np.uint8).reshape(Hkv, n)
+    sig_c = kept_channel_spread(k, bits_tok)
+    g_chan = np.asarray(w_chan, np.float32) * sig_c.astype(np.float32)
+    bits_chan = widths_at(breakpoints(g_chan), lam_k).astype(np.uint8).reshape(g_chan.shape)
+    return dict(bits_tok=bits_tok, sigma_chan=sig_c.astype(np.float32), g_chan=g_chan, bits_chan=bits_chan)

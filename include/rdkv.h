@@ -305,6 +305,72 @@ rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* st
  *     callers that need the timeout report use rdkv_decode_attn. */
 rdkv_status rdkv_decode_attn_noalloc(const rdkv_cache* cache, const void* q, float* out, void* stream);
 
+/* ---------------------------------------------------------------- zone-C re-compression
+ * New tokens start in zone C (RDKV section 2.3); the pages do not say how
+ * they later join zones A and B.  These calls move the oldest zone-C rows into
+ * a new SEGMENT: a TriZone cache of their own (window 0) packed by rdkv_pack,
+ * with token weights from the attention the recent decode queries gave them
+ * and widths at the prefill's water levels (section 2.2, the levels kept
+ * instead of found again).  The attention over the segments and the live
+ * cache is merged from each part's output and log-sum-exp. */
+
+/* rdkv_decode_attn / rdkv_decode_step that also write lse [B][H_q] fp32: the
+ * natural log of the softmax denominator, ln sum_t exp(q . k^_t / sqrt(D)),
+ * over the same keys (-inf when there are none; out is then 0).  lse is
+ * caller-owned device memory; everything else as in the calls without it. */
+rdkv_status rdkv_decode_attn_lse(const rdkv_cache* cache, const void* q, float* out, float* lse,
+                                 void* ws, size_t ws_bytes, void* stream);
+rdkv_status rdkv_decode_step_lse(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new,
+                                 float* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Attention over the union of disjoint key sets from its parts:
+ *   out = sum_i e^(lse_i) out_i / sum_i e^(lse_i),  lse = ln sum_i e^(lse_i)
+ * per row.  outs [n_parts][rows][head_dim], lses [n_parts][rows] fp32 device
+ * (rows = B * H_q for decode outputs); out [rows][head_dim] and lse_out
+ * [rows] (may be NULL) fp32 device.  Parts with lse = -inf weigh 0; a row with
+ * no keys in any part gets out 0, lse -inf.  out may alias outs[0]. */
+rdkv_status rdkv_merge_attn(int32_t n_parts, const float* outs, const float* lses, int64_t rows,
+                            int32_t head_dim, float* out, float* lse_out, void* stream);
+
+/* Takes rows [0, n_move) of every head's zone C out of the cache: copies them
+ * to k_out, v_out [B][n_move][H_kv][D] fp16 (the prefill layout, ready for
+ * rdkv_recompress_score, rdkv_allocate_at_levels and rdkv_pack with a shape
+ * of n_move tokens and window 0), moves rows [n_move, len_c) to the front and
+ * lowers len_c and *len_dev by n_move.  Requires 0 < n_move <= len_c and
+ * len_c - n_move <= n_move (the rows that stay fit in the rows that leave, so
+ * the move never overlaps itself), else RDKV_ERR_INVALID_ARG with nothing
+ * launched.  Uses the host mirror len_c: do not call it while captured
+ * decode steps are pending replay. */
+rdkv_status rdkv_zone_c_take(rdkv_cache* cache, int32_t n_move, void* k_out, void* v_out, void* stream);
+
+/* Token weights and gains of moved tokens (reading of section 2.1 for tokens
+ * that entered after the prefill): for sequence b, KV head j and moved token t
+ *   w_tok[b][j][t] = sum over r < n_recent and the G query heads h of group j
+ *                    of exp(q_recent[b][r][h] . k[b][t][j] / sqrt(D) - lse_recent[b][r][h])
+ * i.e. the attention the recent decode steps gave the token (their lse from
+ * rdkv_decode_*_lse), sigma_tok = population std of the token's V row and
+ * g_tok = fl32(w_tok * sigma_tok).  seg: the segment's shape (n_tokens =
+ * moved rows, window 0, dtype of k, v); k, v [B][n][H_kv][D]; q_recent
+ * [B][n_recent][H_q][D] in q_dtype; lse_recent [B][n_recent][H_q] fp32;
+ * outputs [B][H_kv][n] fp32.  All device memory; 1 <= n_recent. */
+rdkv_status rdkv_recompress_score(const rdkv_shape* seg, const void* k, const void* v, const void* q_recent,
+                                  int32_t q_dtype, const float* lse_recent, int32_t n_recent,
+                                  float* w_tok, float* sigma_tok, float* g_tok, void* stream);
+
+/* Section 2.2 steps 2 and 3 at given water levels: V widths are the
+ * Lagrangian choice at lam_v, then sigma_c of each K channel over the kept
+ * moved tokens, g_chan = fl32(w_chan * sigma_c) and K widths at lam_k; then
+ * the plan, as rdkv_allocate.  levels [2][n_inst] fp32 device: lam_v of every
+ * instance, then lam_k; an instance is a sequence (per_head = 0, the pooled
+ * levels of rdkv_allocate) or a (sequence, KV head) pair (per_head = 1).  The
+ * plan's own levels are set to these.  w_chan is the prefill's [B][H_kv][D];
+ * other arguments, outputs and the workspace as rdkv_allocate for the
+ * segment's shape. */
+rdkv_status rdkv_allocate_at_levels(const rdkv_shape* seg, int32_t per_head, const float* levels,
+                                    const float* g_tok, const float* w_chan, const void* k, uint8_t* bits_tok,
+                                    float* sigma_chan, float* g_chan, uint8_t* bits_chan, void* plan, void* ws,
+                                    size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -169,6 +169,36 @@ __global__ void keep_above_kernel(const float* __restrict__ w, int64_t n_units, 
   if (bad && status) atomicExch(status, (int32_t)RDKV_ERR_INVALID_ARG);
 }
 
+// Widths at given water levels (one per instance): the Lagrangian choice of wf_assign with the
+// level read from levels[inst] instead of found by the bisection; invalid gains are flagged.
+__global__ void assign_at_level_kernel(const float* __restrict__ g, int64_t n_units, int64_t in_stride, Slopes sl,
+                                       const float* __restrict__ levels, uint8_t* __restrict__ bits,
+                                       float* __restrict__ lambda_out, int32_t* status) {
+  const int inst = blockIdx.y;
+  const float lv = levels[inst];
+  const uint32_t lam = level_bits(lv);
+  if (lambda_out && blockIdx.x == 0 && threadIdx.x == 0) lambda_out[inst] = lv;
+  const float* gi = g + (int64_t)inst * in_stride;
+  uint8_t* bi = bits + (int64_t)inst * n_units;
+  bool bad = false;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)gridDim.x * blockDim.x) {
+    const float gv = gi[u];
+    int m = 0;
+    if (gain_valid(gv)) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) m += level_bits(gv * sl.s[k]) > lam ? 1 : 0;
+    } else {
+      bad = true;
+    }
+    bi[u] = kWidth[m];
+  }
+  if (bad && status) atomicExch(status, (int32_t)RDKV_ERR_INVALID_ARG);
+}
+
+// Allocation modes beyond the public ones: widths at given levels, pooled or per head.
+constexpr int kAllocLevelsPooled = 100;
+constexpr int kAllocLevelsPerHead = 101;
+
 __global__ void fill_u8_kernel(uint8_t* __restrict__ p, int64_t n, uint8_t v) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) p[i] = v;
 }
@@ -426,11 +456,13 @@ extern "C" size_t rdkv_allocate_workspace_bytes(const rdkv_shape* s) {
 static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, const float* w_tok, const float* g_tok,
                                  const float* w_chan, const void* k, float avg_bits_v, float avg_bits_k,
                                  uint8_t* bits_tok, float* sigma_chan, float* g_chan, uint8_t* bits_chan, void* plan,
-                                 void* ws, size_t ws_bytes, void* stream) {
+                                 void* ws, size_t ws_bytes, void* stream, const float* levels = nullptr) {
   rdkv_status st = check_shape(s);
   if (st != RDKV_OK) return st;
-  RDKV_REQUIRE(mode >= RDKV_ALLOC_POOLED && mode <= RDKV_ALLOC_THRESHOLD, RDKV_ERR_INVALID_ARG, "unknown allocation mode %d",
-               mode);
+  const bool at_levels = mode == kAllocLevelsPooled || mode == kAllocLevelsPerHead;
+  RDKV_REQUIRE((mode >= RDKV_ALLOC_POOLED && mode <= RDKV_ALLOC_THRESHOLD) || at_levels, RDKV_ERR_INVALID_ARG,
+               "unknown allocation mode %d", mode);
+  RDKV_REQUIRE(!at_levels || levels != nullptr, RDKV_ERR_INVALID_ARG, "NULL levels");
   RDKV_REQUIRE(std::isfinite(avg_bits_v) && avg_bits_v >= 0 && std::isfinite(avg_bits_k) && avg_bits_k >= 0,
                RDKV_ERR_INVALID_ARG, "budgets must be finite and >= 0 (v=%f k=%f)", (double)avg_bits_v,
                (double)avg_bits_k);
@@ -457,7 +489,8 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
   const int D = s->head_dim;
   const int n_heads = s->batch * s->h_kv;
   // levels: pooled: V [batch] then K [batch]; the other modes: V [n_heads] then K [n_heads]
-  const int n_lev = mode == RDKV_ALLOC_POOLED ? s->batch : n_heads;
+  const int n_lev = (mode == RDKV_ALLOC_POOLED || mode == kAllocLevelsPooled) ? s->batch : n_heads;
+  const int per_units = (int)std::min<int64_t>(std::max<int64_t>(ceil_div64((int64_t)s->h_kv * std::max(Np, D), 256 * 16), 1), 512);
 
   // step 2: V tokens
   RDKV_TRY_CUDA(cudaMemsetAsync(status, 0, 8, cs), "status reset");
@@ -466,6 +499,11 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
       st = launch_waterfill(s->batch, (int64_t)s->h_kv * Np, g_tok, avg_bits_v, bits_tok, lam, status, wf, cs);
     } else if (mode == RDKV_ALLOC_PER_HEAD) {  // one water level per (sequence, KV head)
       st = launch_waterfill(n_heads, Np, g_tok, avg_bits_v, bits_tok, lam, status, wf, cs);
+    } else if (at_levels) {  // the given levels: one per sequence or per (sequence, KV head)
+      const int64_t units = mode == kAllocLevelsPooled ? (int64_t)s->h_kv * Np : Np;
+      assign_at_level_kernel<<<dim3(per_units, n_lev), 256, 0, cs>>>(g_tok, units, units, slopes_of(kRdkvSlopes), levels,
+                                                                    bits_tok, lam, status);
+      RDKV_CHECK_LAUNCH("widths at level (V)");
     } else if (mode == RDKV_ALLOC_TOPK) {  // keep-or-drop on w_t, at most floor(B / 16) kept per head
       st = launch_waterfill(n_heads, Np, w_tok, avg_bits_v, bits_tok, lam, status, wf, cs, s->n_tokens,
                             slopes_of(kKeepSlopes));
@@ -500,6 +538,11 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
                           wf, cs);
   } else if (mode == RDKV_ALLOC_PER_HEAD) {
     st = launch_waterfill(n_heads, D, g_chan, avg_bits_k, bits_chan, lam + n_lev, status + 1, wf, cs);
+  } else if (at_levels) {
+    const int64_t units = mode == kAllocLevelsPooled ? (int64_t)s->h_kv * D : D;
+    assign_at_level_kernel<<<dim3(per_units, n_lev), 256, 0, cs>>>(g_chan, units, units, slopes_of(kRdkvSlopes),
+                                                                  levels + n_lev, bits_chan, lam + n_lev, status + 1);
+    RDKV_CHECK_LAUNCH("widths at level (K)");
   } else {  // eviction baselines keep every K channel of the kept tokens at 16 bits
     fill_u8_kernel<<<ceil_div(n_heads * D, 256), 256, 0, cs>>>(bits_chan, (int64_t)n_heads * D, 16);
     RDKV_CHECK_LAUNCH("all channels 16 bits");
@@ -527,8 +570,20 @@ extern "C" rdkv_status rdkv_allocate_mode(const rdkv_shape* s, int mode, float p
                                           const float* g_tok, const float* w_chan, const void* k, float avg_bits_v,
                                           float avg_bits_k, uint8_t* bits_tok, float* sigma_chan, float* g_chan,
                                           uint8_t* bits_chan, void* plan, void* ws, size_t ws_bytes, void* stream) {
+  RDKV_REQUIRE(mode >= RDKV_ALLOC_POOLED && mode <= RDKV_ALLOC_THRESHOLD, RDKV_ERR_INVALID_ARG,
+               "unknown allocation mode %d", mode);
   return allocate_impl(s, mode, param, w_tok, g_tok, w_chan, k, avg_bits_v, avg_bits_k, bits_tok, sigma_chan, g_chan,
                        bits_chan, plan, ws, ws_bytes, stream);
+}
+
+extern "C" rdkv_status rdkv_allocate_at_levels(const rdkv_shape* s, int32_t per_head, const float* levels,
+                                               const float* g_tok, const float* w_chan, const void* k,
+                                               uint8_t* bits_tok, float* sigma_chan, float* g_chan,
+                                               uint8_t* bits_chan, void* plan, void* ws, size_t ws_bytes,
+                                               void* stream) {
+  RDKV_REQUIRE(per_head == 0 || per_head == 1, RDKV_ERR_INVALID_ARG, "per_head must be 0 or 1 (%d)", per_head);
+  return allocate_impl(s, per_head ? kAllocLevelsPerHead : kAllocLevelsPooled, 0.f, nullptr, g_tok, w_chan, k, 0.f,
+                       0.f, bits_tok, sigma_chan, g_chan, bits_chan, plan, ws, ws_bytes, stream, levels);
 }
 
 extern "C" rdkv_status rdkv_plan_sizes(const void* plan, rdkv_sizes* out, void* stream) {

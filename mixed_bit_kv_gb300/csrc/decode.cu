@@ -73,6 +73,7 @@ struct DecodeParams {
   int32_t* error;   // device status word
   int32_t* tickets; // [n_heads] blocks finished per head (zeroed before the launch)
   float* out;       // [batch][h_q][D]
+  float* lse;       // [batch][h_q] natural-log softmax denominators, or NULL
   int32_t* len_dev;        // zone-C rows in use (advanced by the fused step)
   const void* k_new;       // fused step: the new token's K and V [batch][h_kv][D] (dtype), else NULL
   const void* v_new;
@@ -1110,6 +1111,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       M = Mn;
     }
     P.out[((int64_t)b * P.h_q + j * G + h) * D + c] = L > 0.f ? O / L : 0.f;
+    // ln of the denominator: the running sums are of 2^(s log2(e) / sqrt(D) - M)
+    if (P.lse != nullptr && c == 0)
+      P.lse[(int64_t)b * P.h_q + j * G + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
 }
 
@@ -1172,7 +1176,7 @@ rdkv_status check_cache_public(const rdkv_cache* c);
 
 // Kernel arguments of one decode call; ws holds the partials, then the tickets and the status word.
 static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo, const void* q, float* out, void* ws,
-                                  const void* k_new = nullptr, const void* v_new = nullptr) {
+                                  const void* k_new = nullptr, const void* v_new = nullptr, float* lse = nullptr) {
   const rdkv_shape& s = cache->shape;
   const int n_heads = s.batch * s.h_kv;
   const PlanLayout L = plan_layout(s.batch, s.h_kv, s.head_dim);
@@ -1188,6 +1192,7 @@ static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo
   P.error = P.tickets + n_heads;
   P.gticket = P.tickets + n_heads + 1;
   P.out = out;
+  P.lse = lse;
   P.len_dev = cache->len_dev;
   P.k_new = k_new;
   P.v_new = v_new;
@@ -1276,8 +1281,8 @@ extern "C" size_t rdkv_decode_workspace_bytes(const rdkv_cache* cache) {
   return decode_ws_bytes(decode_geom(cache), cache->shape.batch * cache->shape.h_kv);
 }
 
-extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, float* out, void* ws, size_t ws_bytes,
-                                        void* stream) {
+static rdkv_status decode_attn_impl(const rdkv_cache* cache, const void* q, float* out, float* lse, void* ws,
+                                    size_t ws_bytes, void* stream) {
   rdkv_status st = check_cache_public(cache);
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(q && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
@@ -1289,11 +1294,12 @@ extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, 
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
   // the tickets are zero here: the workspace starts zero-filled and every call leaves them at zero
-  return launch_decode(decode_params(cache, geo, q, out, ws), geo, s, (cudaStream_t)stream, true);
+  return launch_decode(decode_params(cache, geo, q, out, ws, nullptr, nullptr, lse), geo, s, (cudaStream_t)stream,
+                       true);
 }
 
-extern "C" rdkv_status rdkv_decode_step(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new,
-                                        float* out, void* ws, size_t ws_bytes, void* stream) {
+static rdkv_status decode_step_impl(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new, float* out,
+                                    float* lse, void* ws, size_t ws_bytes, void* stream) {
   rdkv_status st = check_cache_public(cache);
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(q && out && k_new && v_new, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
@@ -1305,9 +1311,31 @@ extern "C" rdkv_status rdkv_decode_step(rdkv_cache* cache, const void* q, const 
   RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
-  st = launch_decode(decode_params(cache, geo, q, out, ws, k_new, v_new), geo, s, (cudaStream_t)stream, true);
+  st = launch_decode(decode_params(cache, geo, q, out, ws, k_new, v_new, lse), geo, s, (cudaStream_t)stream, true);
   if (st == RDKV_OK) cache->len_c += 1;
   return st;
+}
+
+extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, float* out, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  return decode_attn_impl(cache, q, out, nullptr, ws, ws_bytes, stream);
+}
+
+extern "C" rdkv_status rdkv_decode_attn_lse(const rdkv_cache* cache, const void* q, float* out, float* lse, void* ws,
+                                            size_t ws_bytes, void* stream) {
+  RDKV_REQUIRE(lse, RDKV_ERR_INVALID_ARG, "NULL lse");
+  return decode_attn_impl(cache, q, out, lse, ws, ws_bytes, stream);
+}
+
+extern "C" rdkv_status rdkv_decode_step(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new,
+                                        float* out, void* ws, size_t ws_bytes, void* stream) {
+  return decode_step_impl(cache, q, k_new, v_new, out, nullptr, ws, ws_bytes, stream);
+}
+
+extern "C" rdkv_status rdkv_decode_step_lse(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new,
+                                            float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  RDKV_REQUIRE(lse, RDKV_ERR_INVALID_ARG, "NULL lse");
+  return decode_step_impl(cache, q, k_new, v_new, out, lse, ws, ws_bytes, stream);
 }
 
 extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream) {

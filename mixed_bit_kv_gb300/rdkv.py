@@ -27,6 +27,8 @@ EXPORTED = (
     "rdkv_pack", "rdkv_append",
     "rdkv_decode_workspace_bytes", "rdkv_decode_attn", "rdkv_decode_step", "rdkv_decode_status",
     "rdkv_decode_attn_noalloc",
+    "rdkv_decode_attn_lse", "rdkv_decode_step_lse", "rdkv_merge_attn", "rdkv_zone_c_take", "rdkv_recompress_score",
+    "rdkv_allocate_at_levels",
 )
 
 
@@ -101,6 +103,14 @@ def lib():
             "rdkv_decode_step": (ctypes.c_int, [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_status": (ctypes.c_int, [cp, _P, _P]),
             "rdkv_decode_attn_noalloc": (ctypes.c_int, [cp, _P, _P, _P]),
+            "rdkv_decode_attn_lse": (ctypes.c_int, [cp, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+            "rdkv_decode_step_lse": (ctypes.c_int, [cp, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+            "rdkv_merge_attn": (ctypes.c_int, [ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
+            "rdkv_zone_c_take": (ctypes.c_int, [cp, ctypes.c_int32, _P, _P, _P]),
+            "rdkv_recompress_score": (ctypes.c_int, [sp, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P, _P, _P,
+                                                     _P]),
+            "rdkv_allocate_at_levels": (ctypes.c_int, [sp, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                       ctypes.c_size_t, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -225,7 +235,7 @@ class Cache:
         self.shape, self.plan, self.sizes = shape, plan, sizes
         self.zone_a = torch.zeros(max(sizes.zone_a_bytes, 16), dtype=torch.uint8, device=device)
         self.zone_b = torch.zeros(max(sizes.zone_b_rows, 1), D, dtype=torch.float16, device=device)
-        self.zone_c_k = torch.zeros(shape.batch, shape.h_kv, cap_c, D, dtype=torch.float16, device=device)
+        self.zone_c_k = torch.zeros(shape.batch, shape.h_kv, max(cap_c, 1), D, dtype=torch.float16, device=device)
         self.zone_c_v = torch.zeros_like(self.zone_c_k)
         self.index_map = torch.zeros(max(sizes.index_slots, 1), dtype=torch.int32, device=device)
         self.len_dev = torch.zeros(1, dtype=torch.int32, device=device)
@@ -312,3 +322,113 @@ def read_plan(plan):
     lam = np.frombuffer(raw.tobytes(), dtype="<f4", count=2 * int(hdr["batch"]) * int(hdr["h_kv"]),
                         offset=int(hdr["lambda_off"]))
     return hdr, heads, slots, lam
+
+
+# ---------------------------------------------------------------- zone-C re-compression
+def rdkv_decode_attn_lse(cache, q, out=None, lse=None, stream=None):
+    """rdkv_decode_attn plus the natural-log softmax denominator lse [B, H_q] of every query head."""
+    B, Hq, D = q.shape
+    out = out if out is not None else torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    lse = lse if lse is not None else torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    ws = cache.decode_workspace()
+    _check(lib().rdkv_decode_attn_lse(ctypes.byref(cache.c), _ptr(q), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                      _stream(stream)))
+    return out, lse
+
+
+def rdkv_decode_step_lse(cache, q, k_new, v_new, out=None, lse=None, stream=None):
+    """rdkv_decode_step plus lse [B, H_q]."""
+    B, Hq, D = q.shape
+    out = out if out is not None else torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    lse = lse if lse is not None else torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    ws = cache.decode_workspace()
+    _check(lib().rdkv_decode_step_lse(ctypes.byref(cache.c), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), _ptr(lse),
+                                      _ptr(ws), ws.numel(), _stream(stream)))
+    return out, lse
+
+
+def rdkv_merge_attn(outs, lses, out=None, lse=None, stream=None):
+    """Attention over the union of disjoint key sets: outs [P, ..., D], lses [P, ...] fp32 (contiguous)."""
+    P, D = outs.shape[0], outs.shape[-1]
+    rows = lses[0].numel()
+    out = out if out is not None else torch.empty(outs.shape[1:], dtype=torch.float32, device=outs.device)
+    lse = lse if lse is not None else torch.empty(lses.shape[1:], dtype=torch.float32, device=outs.device)
+    _check(lib().rdkv_merge_attn(P, _ptr(outs), _ptr(lses), rows, D, _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def rdkv_zone_c_take(cache, n_move, stream=None):
+    """Rows [0, n_move) of zone C out of the cache as k, v [B, n_move, H_kv, D] fp16; the rest move to the front."""
+    s = cache.shape
+    k = torch.empty(s.batch, n_move, s.h_kv, s.head_dim, dtype=torch.float16, device=cache.zone_c_k.device)
+    v = torch.empty_like(k)
+    _check(lib().rdkv_zone_c_take(ctypes.byref(cache.c), int(n_move), _ptr(k), _ptr(v), _stream(stream)))
+    return k, v
+
+
+def rdkv_recompress_score(seg_shape, k, v, q_recent, lse_recent, stream=None):
+    """Token weights, V spreads and gains [B, H_kv, n] of moved tokens from recent queries
+    q_recent [B, R, H_q, D] and their decode lse [B, R, H_q]."""
+    B, n, Hkv = seg_shape.batch, seg_shape.n_tokens, seg_shape.h_kv
+    dev = k.device
+    out = {name: torch.empty(B, Hkv, n, dtype=torch.float32, device=dev) for name in ("w_tok", "sigma_tok", "g_tok")}
+    qd = RDKV_F16 if q_recent.dtype == torch.float16 else RDKV_F32
+    _check(lib().rdkv_recompress_score(ctypes.byref(seg_shape), _ptr(k), _ptr(v), _ptr(q_recent), qd, _ptr(lse_recent),
+                                       int(q_recent.shape[1]), _ptr(out["w_tok"]), _ptr(out["sigma_tok"]),
+                                       _ptr(out["g_tok"]), _stream(stream)))
+    return out
+
+
+def plan_levels(plan):
+    """Device view of a plan's water levels: float32 [2, n_inst] (V levels, then K levels)."""
+    import numpy as np
+    raw = plan[:256].cpu().numpy()
+    hdr = np.frombuffer(raw.tobytes(), dtype=np.dtype(PLAN_HEADER_DTYPE), count=1)[0]
+    n = 2 * int(hdr["batch"]) * int(hdr["h_kv"])
+    off = int(hdr["lambda_off"])
+    return plan[off:off + 4 * n].view(torch.float32)
+
+
+def rdkv_allocate_at_levels(seg_shape, levels, g_tok, w_chan, k, per_head=False, stream=None):
+    """Widths of a segment at given water levels [2, n_inst] (n_inst = batch, or batch * h_kv per head);
+    outputs as rdkv_allocate."""
+    dev = k.device
+    B, Hkv, D, n = seg_shape.batch, seg_shape.h_kv, seg_shape.head_dim, seg_shape.n_tokens
+    L = lib()
+    out = dict(bits_tok=torch.empty(B, Hkv, n, dtype=torch.uint8, device=dev),
+               sigma_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+               g_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+               bits_chan=torch.empty(B, Hkv, D, dtype=torch.uint8, device=dev),
+               plan=torch.zeros(L.rdkv_plan_bytes(ctypes.byref(seg_shape)), dtype=torch.uint8, device=dev))
+    ws = _ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(seg_shape)), dev)
+    _check(L.rdkv_allocate_at_levels(ctypes.byref(seg_shape), int(bool(per_head)), _ptr(levels), _ptr(g_tok),
+                                     _ptr(w_chan), _ptr(k), _ptr(out["bits_tok"]), _ptr(out["sigma_chan"]),
+                                     _ptr(out["g_chan"]), _ptr(out["bits_chan"]), _ptr(out["plan"]), _ptr(ws), ws.numel(),
+                                     _stream(stream)))
+    return out
+
+
+def recompress(live, prefill_plan, w_chan, q_recent, lse_recent, n_move, per_head=False, stream=None):
+    """Moves the oldest n_move zone-C rows of `live` into a new segment (a Cache with window 0):
+    weights from the recent queries and their decode lse, widths at the water levels of
+    `prefill_plan` (the plan the prefill allocation wrote), the prefill's channel weights w_chan."""
+    s = live.shape
+    k, v = rdkv_zone_c_take(live, n_move, stream)
+    seg = Shape(s.batch, int(n_move), s.h_q, s.h_kv, s.head_dim, 0, RDKV_F16)
+    sc = rdkv_recompress_score(seg, k, v, q_recent, lse_recent, stream)
+    al = rdkv_allocate_at_levels(seg, plan_levels(prefill_plan), sc["g_tok"], w_chan, k, per_head, stream)
+    cache = rdkv_pack(seg, al["plan"], k, v, al["bits_tok"], al["bits_chan"], 0, stream)
+    cache._keep = (sc, al)
+    return cache
+
+
+def decode_segments(segments, live, q, stream=None):
+    """Attention of q [B, H_q, D] over the segments' zones A and B and the live cache (its zones and
+    zone C), merged: (out [B, H_q, D], lse [B, H_q])."""
+    parts = list(segments) + [live]
+    B, Hq, D = q.shape
+    outs = torch.empty(len(parts), B, Hq, D, dtype=torch.float32, device=q.device)
+    lses = torch.empty(len(parts), B, Hq, dtype=torch.float32, device=q.device)
+    for i, c in enumerate(parts):
+        rdkv_decode_attn_lse(c, q, out=outs[i], lse=lses[i], stream=stream)
+    return rdkv_merge_attn(outs, lses, stream=stream)

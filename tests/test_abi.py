@@ -132,3 +132,28 @@ def test_allocate_mode_argument_checks(L):
     r = L.rdkv_allocate_mode(ctypes.byref(s), rdkv.RDKV_ALLOC_THRESHOLD, f(float("nan")), fake, fake, fake, fake, f(2),
                              f(2), fake, fake, fake, fake, fake, fake, 1 << 30, None)
     assert r == rdkv.RDKV_ERR_INVALID_ARG
+
+
+def test_recompress_argument_checks(L):
+    """The zone-C re-compression calls reject bad arguments on the host, before any launch."""
+    fake = ctypes.c_void_p(256)
+    assert L.rdkv_merge_attn(0, fake, fake, 4, 64, fake, None, None) == rdkv.RDKV_ERR_INVALID_ARG
+    assert L.rdkv_merge_attn(2, None, fake, 4, 64, fake, None, None) == rdkv.RDKV_ERR_INVALID_ARG
+    s = rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16")
+    sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 0, 1)
+    c = rdkv.CacheStruct(s, 256, None, None, 256, 256, None, 256, 32, 20, sizes)
+    for n_move in (0, 21, 9):  # nothing, more than held, fewer than the rows that would stay
+        assert L.rdkv_zone_c_take(ctypes.byref(c), n_move, fake, fake, None) == rdkv.RDKV_ERR_INVALID_ARG
+    assert c.len_c == 20
+    seg = rdkv.make_shape(1, 40, 4, 1, 64, 8, "f16")  # a segment has no window
+    r = L.rdkv_recompress_score(ctypes.byref(seg), fake, fake, fake, rdkv.RDKV_F16, fake, 4, fake, fake, fake, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG and b"window" in L.rdkv_last_error_string()
+    seg = rdkv.make_shape(1, 40, 4, 1, 64, 0, "f16")
+    r = L.rdkv_recompress_score(ctypes.byref(seg), fake, fake, fake, rdkv.RDKV_F16, fake, 0, fake, fake, fake, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+    r = L.rdkv_allocate_at_levels(ctypes.byref(seg), 2, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                  1 << 30, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+    r = L.rdkv_allocate_at_levels(ctypes.byref(seg), 0, None, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                  1 << 30, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG and b"levels" in L.rdkv_last_error_string()

@@ -333,9 +333,11 @@ rdkv_status rdkv_merge_attn(int32_t n_parts, const float* outs, const float* lse
                             int32_t head_dim, float* out, float* lse_out, void* stream);
 
 /* Takes rows [0, n_move) of every head's zone C out of the cache: copies them
- * to k_out, v_out [B][n_move][H_kv][D] fp16 (the prefill layout, ready for
+ * to k_out, v_out [B][n_move][H_kv][D] in the cache's dtype (the fp16 values
+ * of zone C, widened for fp32 caches; the prefill layout, ready for
  * rdkv_recompress_score, rdkv_allocate_at_levels and rdkv_pack with a shape
- * of n_move tokens and window 0), moves rows [n_move, len_c) to the front and
+ * of n_move tokens, window 0 and the cache's dtype, whose queries are then
+ * the model's), moves rows [n_move, len_c) to the front and
  * lowers len_c and *len_dev by n_move.  Requires 0 < n_move <= len_c and
  * len_c - n_move <= n_move (the rows that stay fit in the rows that leave, so
  * the move never overlaps itself), else RDKV_ERR_INVALID_ARG with nothing

@@ -39,16 +39,23 @@ __global__ void merge_attn_kernel(int n_parts, const float* outs, const float* _
 }
 
 // ---------------------------------------------------------------- taking zone-C rows
-// Rows [0, n_move) of head (b, j) -> dst [b][t][j][D]; one block per (head, row).
+// Rows [0, n_move) of head (b, j) -> dst [b][t][j][D] in the cache's dtype (fp16 bits, or the fp16
+// values widened to fp32); one block per (head, row).
+template <typename T>
 __global__ void take_rows_kernel(const uint16_t* __restrict__ zk, const uint16_t* __restrict__ zv, int h_kv, int cap,
-                                 int D, int n_move, uint16_t* __restrict__ k_out, uint16_t* __restrict__ v_out) {
+                                 int D, int n_move, T* __restrict__ k_out, T* __restrict__ v_out) {
   const int head = blockIdx.y, t = blockIdx.x;
   const int b = head / h_kv, j = head % h_kv;
   const int64_t src = ((int64_t)head * cap + t) * D;
   const int64_t dst = (((int64_t)b * n_move + t) * h_kv + j) * D;
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    k_out[dst + c] = zk[src + c];
-    v_out[dst + c] = zv[src + c];
+    if constexpr (sizeof(T) == 2) {
+      k_out[dst + c] = zk[src + c];
+      v_out[dst + c] = zv[src + c];
+    } else {
+      k_out[dst + c] = __half2float(__ushort_as_half(zk[src + c]));
+      v_out[dst + c] = __half2float(__ushort_as_half(zv[src + c]));
+    }
   }
 }
 
@@ -176,9 +183,14 @@ extern "C" rdkv_status rdkv_zone_c_take(rdkv_cache* cache, int32_t n_move, void*
   const rdkv_shape& s = cache->shape;
   const int n_heads = s.batch * s.h_kv, D = s.head_dim;
   cudaStream_t cs = (cudaStream_t)stream;
-  take_rows_kernel<<<dim3(n_move, n_heads), std::min(D, 256), 0, cs>>>(
-      cache->zone_c_k, cache->zone_c_v, s.h_kv, cache->cap_c, D, n_move, static_cast<uint16_t*>(k_out),
-      static_cast<uint16_t*>(v_out));
+  if (s.dtype == RDKV_F16)
+    take_rows_kernel<uint16_t><<<dim3(n_move, n_heads), std::min(D, 256), 0, cs>>>(
+        cache->zone_c_k, cache->zone_c_v, s.h_kv, cache->cap_c, D, n_move, static_cast<uint16_t*>(k_out),
+        static_cast<uint16_t*>(v_out));
+  else
+    take_rows_kernel<float><<<dim3(n_move, n_heads), std::min(D, 256), 0, cs>>>(
+        cache->zone_c_k, cache->zone_c_v, s.h_kv, cache->cap_c, D, n_move, static_cast<float*>(k_out),
+        static_cast<float*>(v_out));
   RDKV_CHECK_LAUNCH("zone C rows out");
   if (L - n_move > 0) {
     shift_rows_kernel<<<dim3(L - n_move, n_heads), std::min(D, 256), 0, cs>>>(cache->zone_c_k, cache->zone_c_v,

@@ -358,9 +358,11 @@ def rdkv_merge_attn(outs, lses, out=None, lse=None, stream=None):
 
 
 def rdkv_zone_c_take(cache, n_move, stream=None):
-    """Rows [0, n_move) of zone C out of the cache as k, v [B, n_move, H_kv, D] fp16; the rest move to the front."""
+    """Rows [0, n_move) of zone C out of the cache as k, v [B, n_move, H_kv, D] in the cache's dtype;
+    the rest move to the front."""
     s = cache.shape
-    k = torch.empty(s.batch, n_move, s.h_kv, s.head_dim, dtype=torch.float16, device=cache.zone_c_k.device)
+    dt = torch.float16 if s.dtype == RDKV_F16 else torch.float32
+    k = torch.empty(s.batch, n_move, s.h_kv, s.head_dim, dtype=dt, device=cache.zone_c_k.device)
     v = torch.empty_like(k)
     _check(lib().rdkv_zone_c_take(ctypes.byref(cache.c), int(n_move), _ptr(k), _ptr(v), _stream(stream)))
     return k, v
@@ -414,7 +416,7 @@ def recompress(live, prefill_plan, w_chan, q_recent, lse_recent, n_move, per_hea
     `prefill_plan` (the plan the prefill allocation wrote), the prefill's channel weights w_chan."""
     s = live.shape
     k, v = rdkv_zone_c_take(live, n_move, stream)
-    seg = Shape(s.batch, int(n_move), s.h_q, s.h_kv, s.head_dim, 0, RDKV_F16)
+    seg = Shape(s.batch, int(n_move), s.h_q, s.h_kv, s.head_dim, 0, s.dtype)
     sc = rdkv_recompress_score(seg, k, v, q_recent, lse_recent, stream)
     al = rdkv_allocate_at_levels(seg, plan_levels(prefill_plan), sc["g_tok"], w_chan, k, per_head, stream)
     cache = rdkv_pack(seg, al["plan"], k, v, al["bits_tok"], al["bits_chan"], 0, stream)

@@ -75,8 +75,9 @@ def test_decode_attn_lse_matches_oracle(case):
     exp, exp_lse = O.decode_lse(ref, qn.numpy())
     assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3
     assert np.abs(lse.cpu().numpy() - exp_lse).max() <= 2e-3
-    # the plain call computes the same output
-    assert torch.equal(rdkv.rdkv_decode_attn(cache, qn.to(DEV)), out)
+    # the plain call computes the same output (up to the order in which warps take tiles)
+    d = (rdkv.rdkv_decode_attn(cache, qn.to(DEV)) - out).abs()
+    assert d.max().item() <= 2e-3 and d.mean().item() <= 5e-5
 
 
 def test_merge_matches_oracle():
@@ -111,13 +112,14 @@ def test_recompress_matches_oracle_step_by_step(case):
     # rows out of zone C
     k_seg, v_seg = rdkv.rdkv_zone_c_take(cache, n_move)
     rk, rv = O.take_zone_c(ref, n_move)
-    assert np.array_equal(k_seg.cpu().numpy(), rk) and np.array_equal(v_seg.cpu().numpy(), rv)
+    assert np.array_equal(k_seg.float().cpu().numpy(), rk.astype(np.float32))
+    assert np.array_equal(v_seg.float().cpu().numpy(), rv.astype(np.float32))
     assert cache.len_c == w.window == ref["len_c"] and int(cache.len_dev.item()) == w.window
     zk = cache.zone_c_k.cpu().numpy()
     assert np.array_equal(zk[:, :, :w.window], ref["zone_c_k"][:, :, :w.window])
     assert np.array_equal(zk[:, :, :w.window], zk_before[:, :, n_move:n_move + w.window])
     # weights of the moved tokens from the recent queries
-    seg = rdkv.Shape(w.batch, n_move, w.h_q, w.h_kv, w.head_dim, 0, rdkv.RDKV_F16)
+    seg = rdkv.Shape(w.batch, n_move, w.h_q, w.h_kv, w.head_dim, 0, cache.shape.dtype)
     gs = rdkv.rdkv_recompress_score(seg, k_seg, v_seg, q_rec, lse_rec)
     for b in range(w.batch):
         eg = O.recompress_gains(rk[b], rv[b], q_rec[b].cpu().numpy(), lse_rec[b].cpu().numpy())

@@ -41,7 +41,8 @@ Readings where the pages are silent (each is a project decision):
  R7 16-bit K channels are stored raw in fp16 inside zone A; 0-bit K channels
     are dropped and contribute nothing to the logits.
  R8 Byte layout of the zones: see ``pack``.
- R9 Zone-C re-compression (new tokens joining zones A and B): see the last
+ R9 Decode: see ``decode`` (scale 1/sqrt(D), every token of zones A, B, C).
+ R10 Zone-C re-compression (new tokens joining zones A and B): see the last
     section, above ``attention_lse``.
 """
 from __future__ import annotations
@@ -640,7 +641,7 @@ def decode_bytes(plan, head_dim, h_q, h_kv, len_c, batch):
 # ---------------------------------------------------------------------------
 # Zone-C re-compression (next row beside the method).  New tokens start in
 # zone C at fp16 (RDKV section 2.3); the pages do not say how they later join
-# zones A and B.  Reading R9 (a project decision):
+# zones A and B.  Reading R10 (a project decision):
 #  * the oldest rows of zone C (all but a recent tail) move into a new segment,
 #    a TriZone cache of their own with no window;
 #  * their token weights are the attention the recent decode queries gave
@@ -716,7 +717,7 @@ def take_zone_c(cache, n_move):
 
 
 def recent_token_weights(k_seg, q_recent, lse_recent):
-    """R9 token weights of moved tokens.  k_seg [n, H_kv, D], q_recent [R, H_q, D], lse_recent
+    """R10 token weights of moved tokens.  k_seg [n, H_kv, D], q_recent [R, H_q, D], lse_recent
     [R, H_q] (natural log) -> w [H_kv, n] float64: sum over the R queries and the G heads of the
     group of exp(q . k_t / sqrt(D) - lse)."""
     k64, q64, l64 = _f64(k_seg), _f64(q_recent), _f64(lse_recent)
@@ -732,7 +733,7 @@ def recent_token_weights(k_seg, q_recent, lse_recent):
 
 
 def recompress_gains(k_seg, v_seg, q_recent, lse_recent):
-    """R9 step 1 for the moved tokens of one sequence: w_tok, sigma_tok (float32) and g_tok."""
+    """R10 step 1 for the moved tokens of one sequence: w_tok, sigma_tok (float32) and g_tok."""
     w = recent_token_weights(k_seg, q_recent, lse_recent)
     sig = value_spread(v_seg)
     n = k_seg.shape[0]
@@ -740,7 +741,7 @@ def recompress_gains(k_seg, v_seg, q_recent, lse_recent):
 
 
 def allocate_at_levels(g_tok, w_chan, k, lam_v, lam_k):
-    """R9 incremental allocation of one sequence: V widths at water level lam_v, then sigma_c over
+    """R10 incremental allocation of one sequence: V widths at water level lam_v, then sigma_c over
     the kept moved tokens, g_c = fl32(w_c * sigma_c) and K widths at lam_k (section 2.2 steps 2-3
     with the levels given instead of found)."""
     g_tok = np.asarray(g_tok, np.float32)

@@ -1,4 +1,4 @@
-"""GPU parity of zone-C re-compression (reading R9) through the C ABI against the CPU oracle.
+"""GPU parity of zone-C re-compression (reading R10) through the C ABI against the CPU oracle.
 
 Bars: log-sum-exp and attention outputs max abs 2e-3 (the decode's bar); merge of parts 1e-5;
 rows taken from zone C, widths at the prefill's levels and the segment's packed bytes bit-exact

@@ -1,4 +1,4 @@
-"""Pins of the oracle's zone-C re-compression (reading R9) against facts it does not compute itself:
+"""Pins of the oracle's zone-C re-compression (reading R10) against facts it does not compute itself:
 closed forms, invariants, library routines on special cases and brute force on tiny inputs.
 CPU only."""
 import math

@@ -331,6 +331,9 @@ def run_ours(args, ws, rank, local):
     if not args.no_comparator:
         comparator = run_fp16_comparator(w, L, pre, dq, dev)
         comparator["trizone_speedup"] = round(comparator["us_per_layer_step"] / (dec_ms_step * 1e3 / (S * L)), 2)
+    recompress = None
+    if not args.no_recompress and rank == 0:
+        recompress = run_recompress(w, caches[L - 1], alloc_out[L - 1]["plan"], score_out[L - 1]["w_chan"], dq, dev)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -358,6 +361,8 @@ def run_ours(args, ws, rank, local):
         line["e2e"] = e2e
     if comparator is not None:
         line["comparator"] = comparator
+    if recompress is not None:
+        line["recompress"] = recompress
     return line
 
 
@@ -401,6 +406,56 @@ def run_fp16_comparator(w, L, pre, dq, dev, steps=16):
     del caches
     return {"kind": "fp16 full cache (all N prompt tokens), torch scaled_dot_product_attention, " + mode,
             "us_per_layer_step": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+
+
+def run_recompress(w, cache, prefill_plan, w_chan, dq, dev, recent=32, reps=20):
+    """The zone-C re-compression row, measured beside the path on the last layer's cache as the
+    timed steps left it (window + decode rows in zone C): the rows beyond the window move into a
+    segment (weights from the last `recent` decode queries and their log-sum-exps); reported with
+    the decode of the cache before (one launch) and after (segment and live cache: two launches and
+    a merge)."""
+    from mixed_bit_kv_gb300 import rdkv
+    S, layer = dq.shape[0], dq.shape[1] - 1
+    R = min(recent, S)
+    lses = torch.empty(w.batch, R, w.h_q, dtype=torch.float32, device=dev)
+    for r in range(R):
+        lses[:, r].copy_(rdkv.rdkv_decode_attn_lse(cache, dq[S - R + r, layer])[1])
+    q_rec = dq[S - R:, layer].transpose(0, 1).contiguous()
+    q = dq[S - 1, layer]
+    out = torch.empty(w.batch, w.h_q, w.head_dim, dtype=torch.float32, device=dev)
+
+    def per_call_us(fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    us_plain = per_call_us(lambda: rdkv.rdkv_decode_attn(cache, q, out=out))
+    n_move = cache.len_c - w.window
+    if n_move < w.window:
+        return {"skipped": f"{n_move} rows beyond the window; a move needs at least as many rows as stay"}
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    seg = rdkv.recompress(cache, prefill_plan, w_chan, q_rec, lses, n_move)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    us_seg = per_call_us(lambda: rdkv.decode_segments([seg], cache, q))
+    st = seg.c.sizes
+    seg_bytes = int(st.zone_a_bytes) + int(st.zone_b_rows) * w.head_dim * 2
+    fp16_bytes = 2 * w.batch * n_move * w.h_kv * w.head_dim * 2
+    return {"rows_moved": int(n_move), "recent_queries": int(R), "ms_per_layer": round(ms, 3),
+            "segment_kept_fraction": round(int(st.kept_tokens) / (w.batch * w.h_kv * n_move), 4),
+            "segment_bytes": seg_bytes, "fp16_bytes_of_the_rows": fp16_bytes,
+            "decode_us_one_cache": round(us_plain, 3), "decode_us_segment_and_cache": round(us_seg, 3),
+            "note": "take rows + weights from recent queries + widths at the prefill's levels + plan "
+                    "(sizes read back) + pack, CUDA events; decodes eager, per call"}
 
 
 def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev):
@@ -529,6 +584,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-comparator", action="store_true", help="skip the fp16 full-cache SDPA context number")
+    ap.add_argument("--no-recompress", action="store_true", help="skip the zone-C re-compression measurement")
     args = ap.parse_args()
     ws, rank, local = dist_env()
 

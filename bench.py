@@ -417,6 +417,7 @@ def run_recompress(w, cache, prefill_plan, w_chan, dq, dev, recent=32, reps=20):
     from mixed_bit_kv_gb300 import rdkv
     S, layer = dq.shape[0], dq.shape[1] - 1
     R = min(recent, S)
+    cache.c.len_c = int(cache.len_dev.item())  # graph replays advanced only the device length
     lses = torch.empty(w.batch, R, w.h_q, dtype=torch.float32, device=dev)
     for r in range(R):
         lses[:, r].copy_(rdkv.rdkv_decode_attn_lse(cache, dq[S - R + r, layer])[1])

@@ -347,16 +347,19 @@ rdkv_status rdkv_zone_c_take(rdkv_cache* cache, int32_t n_move, void* k_out, voi
 
 /* Token weights and gains of moved tokens (reading of section 2.1 for tokens
  * that entered after the prefill): for sequence b, KV head j and moved token t
- *   w_tok[b][j][t] = sum over r < n_recent and the G query heads h of group j
- *                    of exp(q_recent[b][r][h] . k[b][t][j] / sqrt(D) - lse_recent[b][r][h])
+ *   w_tok[b][j][t] = weight_scale * sum over r < n_recent and the G query heads
+ *                    h of group j of
+ *                    exp(q_recent[b][r][h] . k[b][t][j] / sqrt(D) - lse_recent[b][r][h])
  * i.e. the attention the recent decode steps gave the token (their lse from
- * rdkv_decode_*_lse), sigma_tok = population std of the token's V row and
- * g_tok = fl32(w_tok * sigma_tok).  seg: the segment's shape (n_tokens =
+ * rdkv_decode_*_lse), scaled: a prefill weight sums the attention of up to N
+ * query rows, so weight_scale = N / n_recent puts the moved tokens on the scale
+ * the prefill's water levels were found for.  sigma_tok = population std of
+ * the token's V row and g_tok = fl32(w_tok * sigma_tok).  seg: the segment's shape (n_tokens =
  * moved rows, window 0, dtype of k, v); k, v [B][n][H_kv][D]; q_recent
  * [B][n_recent][H_q][D] in q_dtype; lse_recent [B][n_recent][H_q] fp32;
  * outputs [B][H_kv][n] fp32.  All device memory; 1 <= n_recent. */
 rdkv_status rdkv_recompress_score(const rdkv_shape* seg, const void* k, const void* v, const void* q_recent,
-                                  int32_t q_dtype, const float* lse_recent, int32_t n_recent,
+                                  int32_t q_dtype, const float* lse_recent, int32_t n_recent, float weight_scale,
                                   float* w_tok, float* sigma_tok, float* g_tok, void* stream);
 
 /* Section 2.2 steps 2 and 3 at given water levels: V widths are the

@@ -11,6 +11,8 @@
 //     bytes from rdkv_pack;
 //   * rdkv_merge_attn combines the decode outputs of the segments and the live
 //     cache into the attention over the union of their keys.
+#include <cmath>
+
 #include "common.cuh"
 
 namespace rdkv {
@@ -86,7 +88,7 @@ constexpr int kScoreQ = 8;         // recent queries staged per round
 // 2^(q . k log2(e) / sqrt(D) - lse log2(e)) over its share of the (query, head) pairs.
 __global__ void __launch_bounds__(kScoreThreads) recent_weights_kernel(
     const void* __restrict__ k, const void* __restrict__ v, int dtype, const void* __restrict__ q, int q_dtype,
-    const float* __restrict__ lse, int R, int n, int h_q, int h_kv, int D, float* __restrict__ w_tok,
+    const float* __restrict__ lse, int R, float wscale, int n, int h_q, int h_kv, int D, float* __restrict__ w_tok,
     float* __restrict__ sigma_tok, float* __restrict__ g_tok) {
   extern __shared__ float sm[];
   const int G = h_q / h_kv;
@@ -132,6 +134,7 @@ __global__ void __launch_bounds__(kScoreThreads) recent_weights_kernel(
   if (tid < kScoreTok && t0 + tid < n) {
     float w = 0.f;
     for (int g = 0; g < ngrp; ++g) w += red[g * kScoreTok + tid];
+    w *= wscale;
     // population std of the V row, two passes
     const float* vr = vs + tid * (D + 1);
     float mean = 0.f;
@@ -207,12 +210,15 @@ extern "C" rdkv_status rdkv_zone_c_take(rdkv_cache* cache, int32_t n_move, void*
 
 extern "C" rdkv_status rdkv_recompress_score(const rdkv_shape* seg, const void* k, const void* v, const void* q_recent,
                                              int32_t q_dtype, const float* lse_recent, int32_t n_recent,
-                                             float* w_tok, float* sigma_tok, float* g_tok, void* stream) {
+                                             float weight_scale, float* w_tok, float* sigma_tok, float* g_tok,
+                                             void* stream) {
   rdkv_status st = check_shape(seg);
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(seg->window == 0, RDKV_ERR_INVALID_ARG, "a segment has no window (window %d)", seg->window);
   RDKV_REQUIRE(q_dtype == RDKV_F16 || q_dtype == RDKV_F32, RDKV_ERR_UNSUPPORTED, "query dtype %d", q_dtype);
   RDKV_REQUIRE(n_recent >= 1, RDKV_ERR_INVALID_ARG, "n_recent %d < 1", n_recent);
+  RDKV_REQUIRE(std::isfinite(weight_scale) && weight_scale > 0.f, RDKV_ERR_INVALID_ARG, "weight_scale %f",
+               (double)weight_scale);
   RDKV_REQUIRE(k && v && q_recent && lse_recent && w_tok && sigma_tok && g_tok, RDKV_ERR_INVALID_ARG,
                "NULL pointer argument");
   const int D = seg->head_dim, G = seg->h_q / seg->h_kv, n = seg->n_tokens;
@@ -222,7 +228,8 @@ extern "C" rdkv_status rdkv_recompress_score(const rdkv_shape* seg, const void* 
                 "recompress smem");
   const dim3 grid(ceil_div(n, kScoreTok), seg->h_kv, seg->batch);
   recent_weights_kernel<<<grid, kScoreThreads, smem, (cudaStream_t)stream>>>(
-      k, v, seg->dtype, q_recent, q_dtype, lse_recent, n_recent, n, seg->h_q, seg->h_kv, D, w_tok, sigma_tok, g_tok);
+      k, v, seg->dtype, q_recent, q_dtype, lse_recent, n_recent, weight_scale, n, seg->h_q, seg->h_kv, D, w_tok,
+      sigma_tok, g_tok);
   RDKV_CHECK_LAUNCH("recent token weights");
   return RDKV_OK;
 }

@@ -107,8 +107,8 @@ def lib():
             "rdkv_decode_step_lse": (ctypes.c_int, [cp, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_merge_attn": (ctypes.c_int, [ctypes.c_int32, _P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
             "rdkv_zone_c_take": (ctypes.c_int, [cp, ctypes.c_int32, _P, _P, _P]),
-            "rdkv_recompress_score": (ctypes.c_int, [sp, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P, _P, _P,
-                                                     _P]),
+            "rdkv_recompress_score": (ctypes.c_int, [sp, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32,
+                                                     ctypes.c_float, _P, _P, _P, _P]),
             "rdkv_allocate_at_levels": (ctypes.c_int, [sp, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                        ctypes.c_size_t, _P]),
         }
@@ -368,15 +368,16 @@ def rdkv_zone_c_take(cache, n_move, stream=None):
     return k, v
 
 
-def rdkv_recompress_score(seg_shape, k, v, q_recent, lse_recent, stream=None):
+def rdkv_recompress_score(seg_shape, k, v, q_recent, lse_recent, weight_scale=1.0, stream=None):
     """Token weights, V spreads and gains [B, H_kv, n] of moved tokens from recent queries
-    q_recent [B, R, H_q, D] and their decode lse [B, R, H_q]."""
+    q_recent [B, R, H_q, D] and their decode lse [B, R, H_q], weights times weight_scale."""
     B, n, Hkv = seg_shape.batch, seg_shape.n_tokens, seg_shape.h_kv
     dev = k.device
     out = {name: torch.empty(B, Hkv, n, dtype=torch.float32, device=dev) for name in ("w_tok", "sigma_tok", "g_tok")}
     qd = RDKV_F16 if q_recent.dtype == torch.float16 else RDKV_F32
     _check(lib().rdkv_recompress_score(ctypes.byref(seg_shape), _ptr(k), _ptr(v), _ptr(q_recent), qd, _ptr(lse_recent),
-                                       int(q_recent.shape[1]), _ptr(out["w_tok"]), _ptr(out["sigma_tok"]),
+                                       int(q_recent.shape[1]), ctypes.c_float(weight_scale), _ptr(out["w_tok"]),
+                                       _ptr(out["sigma_tok"]),
                                        _ptr(out["g_tok"]), _stream(stream)))
     return out
 
@@ -417,7 +418,8 @@ def recompress(live, prefill_plan, w_chan, q_recent, lse_recent, n_move, per_hea
     s = live.shape
     k, v = rdkv_zone_c_take(live, n_move, stream)
     seg = Shape(s.batch, int(n_move), s.h_q, s.h_kv, s.head_dim, 0, s.dtype)
-    sc = rdkv_recompress_score(seg, k, v, q_recent, lse_recent, stream)
+    # a prefill weight sums the attention of up to N query rows: the recent sums are scaled by N / R
+    sc = rdkv_recompress_score(seg, k, v, q_recent, lse_recent, s.n_tokens / q_recent.shape[1], stream)
     al = rdkv_allocate_at_levels(seg, plan_levels(prefill_plan), sc["g_tok"], w_chan, k, per_head, stream)
     cache = rdkv_pack(seg, al["plan"], k, v, al["bits_tok"], al["bits_chan"], 0, stream)
     cache._keep = (sc, al)

@@ -645,9 +645,11 @@ def decode_bytes(plan, head_dim, h_q, h_kv, len_c, batch):
 #  * the oldest rows of zone C (all but a recent tail) move into a new segment,
 #    a TriZone cache of their own with no window;
 #  * their token weights are the attention the recent decode queries gave
-#    them: w_t = sum over recent queries tau and the G heads of the group of
-#    exp(q.k_t / sqrt(D) - lse_tau,h), lse the log-sum-exp of that decode;
-#    sigma_t and g_t as in step 1;
+#    them: w_t = (N / R) * sum over the R recent queries tau and the G heads
+#    of the group of exp(q.k_t / sqrt(D) - lse_tau,h), lse the log-sum-exp of
+#    that decode; a prefill weight sums the attention of up to N query rows,
+#    and the factor puts the moved tokens on that scale; sigma_t and g_t as in
+#    step 1;
 #  * the allocation is incremental: the instance keeps its water levels
 #    lambda_V, lambda_K of the prefill and the moved units take the Lagrangian
 #    choice at those levels (section 2.2), K channels over the moved kept
@@ -716,10 +718,11 @@ def take_zone_c(cache, n_move):
     return k, v
 
 
-def recent_token_weights(k_seg, q_recent, lse_recent):
+def recent_token_weights(k_seg, q_recent, lse_recent, scale=1.0):
     """R10 token weights of moved tokens.  k_seg [n, H_kv, D], q_recent [R, H_q, D], lse_recent
     [R, H_q] (natural log) -> w [H_kv, n] float64: sum over the R queries and the G heads of the
-    group of exp(q . k_t / sqrt(D) - lse)."""
+    group of exp(q . k_t / sqrt(D) - lse), times `scale` (N / R: the prefill's weights sum over up to
+    N query rows)."""
     k64, q64, l64 = _f64(k_seg), _f64(q_recent), _f64(lse_recent)
     n, Hkv, D = k64.shape
     R, Hq, _ = q64.shape
@@ -729,12 +732,12 @@ def recent_token_weights(k_seg, q_recent, lse_recent):
         j = h // G
         s = q64[:, h, :] @ k64[:, j, :].T / math.sqrt(D)       # [R, n]
         w[j] += np.exp(s - l64[:, h][:, None]).sum(axis=0)
-    return w
+    return w * scale
 
 
-def recompress_gains(k_seg, v_seg, q_recent, lse_recent):
+def recompress_gains(k_seg, v_seg, q_recent, lse_recent, scale=1.0):
     """R10 step 1 for the moved tokens of one sequence: w_tok, sigma_tok (float32) and g_tok."""
-    w = recent_token_weights(k_seg, q_recent, lse_recent)
+    w = recent_token_weights(k_seg, q_recent, lse_recent, scale)
     sig = value_spread(v_seg)
     n = k_seg.shape[0]
     return dict(w_tok=w.astype(np.float32), sigma_tok=sig.astype(np.float32), g_tok=token_gains(w, sig, n))

@@ -146,11 +146,17 @@ def test_recompress_argument_checks(L):
         assert L.rdkv_zone_c_take(ctypes.byref(c), n_move, fake, fake, None) == rdkv.RDKV_ERR_INVALID_ARG
     assert c.len_c == 20
     seg = rdkv.make_shape(1, 40, 4, 1, 64, 8, "f16")  # a segment has no window
-    r = L.rdkv_recompress_score(ctypes.byref(seg), fake, fake, fake, rdkv.RDKV_F16, fake, 4, fake, fake, fake, None)
+    f = ctypes.c_float
+    r = L.rdkv_recompress_score(ctypes.byref(seg), fake, fake, fake, rdkv.RDKV_F16, fake, 4, f(1), fake, fake, fake,
+                                None)
     assert r == rdkv.RDKV_ERR_INVALID_ARG and b"window" in L.rdkv_last_error_string()
     seg = rdkv.make_shape(1, 40, 4, 1, 64, 0, "f16")
-    r = L.rdkv_recompress_score(ctypes.byref(seg), fake, fake, fake, rdkv.RDKV_F16, fake, 0, fake, fake, fake, None)
+    r = L.rdkv_recompress_score(ctypes.byref(seg), fake, fake, fake, rdkv.RDKV_F16, fake, 0, f(1), fake, fake, fake,
+                                None)
     assert r == rdkv.RDKV_ERR_INVALID_ARG
+    r = L.rdkv_recompress_score(ctypes.byref(seg), fake, fake, fake, rdkv.RDKV_F16, fake, 4, f(0), fake, fake, fake,
+                                None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG and b"weight_scale" in L.rdkv_last_error_string()
     r = L.rdkv_allocate_at_levels(ctypes.byref(seg), 2, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
                                   1 << 30, None)
     assert r == rdkv.RDKV_ERR_INVALID_ARG

@@ -120,9 +120,10 @@ def test_recompress_matches_oracle_step_by_step(case):
     assert np.array_equal(zk[:, :, :w.window], zk_before[:, :, n_move:n_move + w.window])
     # weights of the moved tokens from the recent queries
     seg = rdkv.Shape(w.batch, n_move, w.h_q, w.h_kv, w.head_dim, 0, cache.shape.dtype)
-    gs = rdkv.rdkv_recompress_score(seg, k_seg, v_seg, q_rec, lse_rec)
+    scale = w.n_tokens / steps
+    gs = rdkv.rdkv_recompress_score(seg, k_seg, v_seg, q_rec, lse_rec, scale)
     for b in range(w.batch):
-        eg = O.recompress_gains(rk[b], rv[b], q_rec[b].cpu().numpy(), lse_rec[b].cpu().numpy())
+        eg = O.recompress_gains(rk[b], rv[b], q_rec[b].cpu().numpy(), lse_rec[b].cpu().numpy(), scale)
         for name in ("w_tok", "sigma_tok"):
             got = gs[name][b].cpu().numpy().astype(np.float64)
             exp = eg[name].astype(np.float64)

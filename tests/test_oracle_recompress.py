@@ -68,6 +68,8 @@ def test_recent_weights_sum_to_queries_times_group():
     lse = np.array([[logsumexp(k[:, h // G, :] @ q[r, h] / math.sqrt(D)) for h in range(Hq)] for r in range(R)])
     w = O.recent_token_weights(k, q, lse)
     np.testing.assert_allclose(w.sum(axis=1), R * G, rtol=1e-12)
+    # the scale multiplies every weight
+    np.testing.assert_allclose(O.recent_token_weights(k, q, lse, 2.5), 2.5 * w, rtol=1e-15)
 
 
 def test_recent_weights_brute_force():

@@ -328,7 +328,8 @@ rdkv_status rdkv_decode_step_lse(rdkv_cache* cache, const void* q, const void* k
  * per row.  outs [n_parts][rows][head_dim], lses [n_parts][rows] fp32 device
  * (rows = B * H_q for decode outputs); out [rows][head_dim] and lse_out
  * [rows] (may be NULL) fp32 device.  Parts with lse = -inf weigh 0; a row with
- * no keys in any part gets out 0, lse -inf.  out may alias outs[0]. */
+ * no keys in any part gets out 0, lse -inf.  out may alias outs[0]; lse_out
+ * must not alias lses. */
 rdkv_status rdkv_merge_attn(int32_t n_parts, const float* outs, const float* lses, int64_t rows,
                             int32_t head_dim, float* out, float* lse_out, void* stream);
 

@@ -463,6 +463,8 @@ def run_recompress(w, cache, prefill_plan, w_chan, dq, dev, recent=32, reps=20):
         rdkv.rdkv_merge_attn(outs, lse2, out=out, lse=lse_m)
 
     us_seg = per_call_us(segmented)
+    md = rdkv.MultiDecode([seg, cache])
+    us_multi = per_call_us(lambda: md.attn(q, out=out, lse=lse_m))
     st = seg.c.sizes
     seg_bytes = int(st.zone_a_bytes) + int(st.zone_b_rows) * w.head_dim * 2
     fp16_bytes = 2 * w.batch * n_move * w.h_kv * w.head_dim * 2
@@ -470,9 +472,10 @@ def run_recompress(w, cache, prefill_plan, w_chan, dq, dev, recent=32, reps=20):
             "segment_kept_fraction": round(int(st.kept_tokens) / (w.batch * w.h_kv * n_move), 4),
             "segment_bytes": seg_bytes, "fp16_bytes_of_the_rows": fp16_bytes,
             "decode_us_one_cache": round(us_plain, 3), "decode_us_segment_and_cache": round(us_seg, 3),
+            "decode_us_segment_and_cache_one_launch": round(us_multi, 3),
             "note": "take rows + weights from recent queries + widths at the prefill's levels + plan "
                     "(sizes read back) + pack, CUDA events; decodes per call from CUDA graphs: one launch for the "
-                    "cache, two launches and a merge for segment and cache"}
+                    "cache; segment and cache as two launches and a merge, or as one launch over both"}
 
 
 def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev):

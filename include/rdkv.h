@@ -333,6 +333,23 @@ rdkv_status rdkv_decode_step_lse(rdkv_cache* cache, const void* q, const void* k
 rdkv_status rdkv_merge_attn(int32_t n_parts, const float* outs, const float* lses, int64_t rows,
                             int32_t head_dim, float* out, float* lse_out, void* stream);
 
+/* One launch over several caches sharing the query: the softmax over the union
+ * of their keys (zones A and B of each, and each one's zone-C rows), the same
+ * output rdkv_merge_attn gives from one call per cache, without the extra
+ * launches.  parts[0 .. n_parts) (1 <= n_parts <= 8) must share batch, h_q,
+ * h_kv, head_dim and dtype; typically the segments moved out of zone C and
+ * then the live cache.  q, out, lse (may be NULL) and the workspace contract
+ * as rdkv_decode_attn_lse, the workspace sized by
+ * rdkv_decode_multi_workspace_bytes for the same list (0 if the list is
+ * invalid).  With more than one cache, every cache's sizes must carry its
+ * plan costs (rdkv_plan_sizes) and the batch at most RDKV_COST_HEADS heads,
+ * else RDKV_ERR_UNSUPPORTED.  rdkv_decode_multi_status reads and clears the
+ * status word as rdkv_decode_status does. */
+size_t rdkv_decode_multi_workspace_bytes(const rdkv_cache* const* parts, int32_t n_parts);
+rdkv_status rdkv_decode_attn_multi(const rdkv_cache* const* parts, int32_t n_parts, const void* q, float* out,
+                                   float* lse, void* ws, size_t ws_bytes, void* stream);
+rdkv_status rdkv_decode_multi_status(const rdkv_cache* const* parts, int32_t n_parts, const void* ws, void* stream);
+
 /* Takes rows [0, n_move) of every head's zone C out of the cache: copies them
  * to k_out, v_out [B][n_move][H_kv][D] in the cache's dtype (the fp16 values
  * of zone C, widened for fp32 caches; the prefill layout, ready for

@@ -34,7 +34,8 @@ constexpr int kDecWarps = 16;  // one block per SM
 constexpr int kMaxInflight = 4;
 constexpr int kPrologueItems = 2;
 constexpr int kMaxDealtBlocks = 256;  // grids up to this size may be dealt to heads on the host
-constexpr uint8_t kNoHead = 0xff;  // copies a warp issues before the wait for the previous kernel
+constexpr uint8_t kNoHead = 0xff;
+constexpr int kMaxParts = 8;          // caches one launch may attend  // copies a warp issues before the wait for the previous kernel
 constexpr int kCRows = 16;        // zone-C rows per work item
 constexpr int kMaxKB = 16;        // k-blocks of a K row (D = 128: at most 13)
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at GB300 clocks
@@ -62,6 +63,20 @@ __host__ __device__ constexpr int partial_stride(int G, int D) { return (G * (D 
 // The warps' partial results are combined in the ring area once every ring is drained.
 __host__ __device__ constexpr int64_t decode_reduce_bytes(int D) { return (int64_t)kDecWarps * 8 * (D + 2) * 4; }
 
+// One cache attended by a launch: its zones, its zone-C length and capacity and its plan's head
+// records and slot tables.  A launch attends one cache, or several sharing the query (segments
+// moved out of zone C and the live cache): the softmax then runs over the union of their keys.
+struct DecodePart {
+  const uint8_t* zone_a;
+  const uint16_t* zone_b;
+  const uint16_t* zone_c_k;
+  const uint16_t* zone_c_v;
+  int32_t* len_dev;
+  const rdkv_head_plan* heads;
+  const int16_t* slots;
+  int cap_c;
+};
+
 struct DecodeParams {
   const void* plan;
   const uint8_t* zone_a;
@@ -84,6 +99,11 @@ struct DecodeParams {
   int dealt;                    // 1: blocks dealt to heads on the host (below); 0: by the kernel
   uint8_t block_head[kMaxDealtBlocks];       // head of each block, kNoHead for a block without work
   int16_t head_first[RDKV_COST_HEADS + 1];   // first block of each head; [n_heads] = end
+  // host dealing over several caches: each block reads one cache (block_part) and takes items
+  // block_split, block_split + block_nsplit, ... of that cache's head; the blocks of a head over all
+  // caches share its partials, ticket and merge.  One cache: part 0, the block's split of the head.
+  uint8_t block_part[kMaxDealtBlocks], block_split[kMaxDealtBlocks], block_nsplit[kMaxDealtBlocks];
+  DecodePart parts[kMaxParts];  // parts[0] is the cache of the fields above
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -586,10 +606,12 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   __shared__ int asg[3];  // head, first block of the head, blocks of the head
   __shared__ __align__(16) rdkv_head_plan hp_s;  // this block's head record
   int16_t slot_pre = -1;  // dealt on the host: this thread's slot-table entry, loaded with the record
+  // the cache this block reads (part 0 unless the host dealt blocks over several caches)
+  const DecodePart& PP = P.parts[P.dealt ? P.block_part[blockIdx.x] : 0];
   if (P.dealt) {
     // dealt on the host: this block's head and split range are kernel arguments
     const int hb = P.block_head[blockIdx.x];
-    if (hb != kNoHead && tid < P.slot_stride) slot_pre = P.slots[(int64_t)hb * P.slot_stride + tid];
+    if (hb != kNoHead && tid < P.slot_stride) slot_pre = PP.slots[(int64_t)hb * P.slot_stride + tid];
     if (warp == 0) {
       if (lane == 0) {
         asg[0] = hb == kNoHead ? -1 : hb;
@@ -597,7 +619,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         asg[2] = hb == kNoHead ? 0 : P.head_first[hb + 1] - P.head_first[hb];
       }
       if (hb != kNoHead)  // the head record into shared memory, one word per lane
-        reinterpret_cast<int32_t*>(&hp_s)[lane] = reinterpret_cast<const int32_t*>(P.heads + hb)[lane];
+        reinterpret_cast<int32_t*>(&hp_s)[lane] = reinterpret_cast<const int32_t*>(PP.heads + hb)[lane];
     }
   } else if (warp == 0) {
     // Blocks are dealt to heads in proportion to their estimated cost, at least one per head, over a
@@ -640,13 +662,16 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   __syncthreads();
   if (asg[0] < 0) return;
   const int head = asg[0], split = (int)blockIdx.x - asg[1], n_split = asg[2], first_block = asg[1];
+  // items of this block's cache: isplit, isplit + in_split, ...
+  const int isplit = P.dealt ? (int)P.block_split[blockIdx.x] : split;
+  const int in_split = P.dealt ? (int)P.block_nsplit[blockIdx.x] : n_split;
   const int b = head / P.h_kv, j = head % P.h_kv;
   const rdkv_head_plan* hpp = &hp_s;
   const bool fused = P.k_new != nullptr;
 
   // the slot table goes into registers now (static data)
   const int qbase = b * P.h_q + j * G;
-  const int16_t* slot_ch = P.slots + (int64_t)head * P.slot_stride;
+  const int16_t* slot_ch = PP.slots + (int64_t)head * P.slot_stride;
   const int k_slots = hpp->k_slots;  // <= D + kSlotPad <= the block's threads
   const int16_t sr = tid < k_slots ? (P.dealt ? slot_pre : slot_ch[tid]) : (int16_t)-1;
 
@@ -746,7 +771,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     if (issued == done) head_p = used = 0;  // empty ring: start at its beginning
     while (!drained && issued - done < cap) {
       int it = pending;
-      if (it < 0) it = split + n_split * atomicAdd(&next_k, 1);  // taken in order of need: no warp idles early
+      if (it < 0) it = isplit + in_split * atomicAdd(&next_k, 1);  // taken in order of need: no warp idles early
       if (it >= n_items) {
         if (items_final) drained = true;
         else pending = it;
@@ -783,17 +808,17 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         const int ti = it - (int)cstart(cls);
         const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
         mbar_arrive_expect_tx(bar, a_bytes + zb);
-        bulk_copy(dst, P.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar);
-        if (zb) bulk_copy(dst + a_bytes, P.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar);
+        bulk_copy(dst, PP.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar);
+        if (zb) bulk_copy(dst + a_bytes, PP.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar);
       } else {
         // rows of zone C (the fused step's new row, past them, is written by the consumer)
         const int rows = max(0, min(kCRows, len_c - c_row));
         const uint32_t bytes = (uint32_t)rows * D * 2;
-        const int64_t src = ((int64_t)head * P.cap_c + c_row) * D;
+        const int64_t src = ((int64_t)head * PP.cap_c + c_row) * D;
         mbar_arrive_expect_tx(bar, 2 * bytes);
         if (bytes) {
-          bulk_copy(dst, P.zone_c_k + src, bytes, bar);
-          bulk_copy(dst + kCRows * D * 2, P.zone_c_v + src, bytes, bar);
+          bulk_copy(dst, PP.zone_c_k + src, bytes, bar);
+          bulk_copy(dst + kCRows * D * 2, PP.zone_c_v + src, bytes, bar);
         }
       }
       ++issued;
@@ -840,7 +865,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   // on the stream does not write.  The query, the new token and the zone-C length may come from
   // it: wait for it here (a no-op without programmatic dependent launch).
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  len_c = min(*P.len_dev, P.cap_c);
+  len_c = min(*PP.len_dev, PP.cap_c);
   n_rows = len_c + (fused ? 1 : 0);
   n_items = zc_start + ceil_div(n_rows, kCRows);
   items_final = true;
@@ -1130,14 +1155,19 @@ struct DecodeGeom {
   size_t ticket_off;   // tickets then the status word
 };
 
-static DecodeGeom decode_geom(const rdkv_cache* c) {
+// Geometry of a launch over the caches parts[0 .. n) (one, or segments and the live cache).
+static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n) {
   DecodeGeom g;
-  const rdkv_shape& s = c->shape;
+  const rdkv_shape& s = parts[0]->shape;
   const int D = s.head_dim, G = s.h_q / s.h_kv;
   const int n_heads = s.batch * s.h_kv;
   const int sms = num_sms();
   const int64_t fixed = decode_fixed_smem(D, s.dtype == RDKV_F32);
-  const int64_t max_item = std::max<int64_t>(align_up(c->sizes.max_stage_bytes, 128), 2 * kCRows * D * 2);
+  int64_t max_item = 2 * kCRows * D * 2, items = 0;
+  for (int p = 0; p < n; ++p) {
+    max_item = std::max<int64_t>(max_item, align_up(parts[p]->sizes.max_stage_bytes, 128));
+    items += ceil_div64(parts[p]->sizes.index_slots, kTile) + (int64_t)n_heads * ceil_div(parts[p]->cap_c, kCRows);
+  }
   g.max_item = max_item;
   // one block of kDecWarps warps per SM; the warps with a ring share what is left equally: all of
   // them, or half (a quarter) with twice (four times) the ring when the largest staged tile needs it
@@ -1153,19 +1183,19 @@ static DecodeGeom decode_geom(const rdkv_cache* c) {
   g.ring_warps = ring_warps;
   g.smem = (size_t)(fixed + (int64_t)ring_warps * ring);
   // blocks dealt to heads in proportion to their work: a nominal count that fills every SM once,
-  // fewer when there is little work (at least kDecWarps items per block on average)
-  const int64_t items = ceil_div64(c->sizes.index_slots, kTile) + (int64_t)n_heads * ceil_div(c->cap_c, kCRows);
+  // fewer when there is little work (at least kDecWarps items per block on average).
   // With few heads, leave one SM per head free: the last block of each head merges after the
   // others have left, and on those SMs the next call's blocks would otherwise start only after
   // the merge, with their whole set-up still ahead of them.
   const int free_sms = n_heads <= sms / 16 ? n_heads : 0;
   g.ctas = (int)std::max<int64_t>(
       1, std::min<int64_t>((int64_t)blocks_per_sm * (sms - free_sms), ceil_div64(items, kDecWarps)));
-  g.splits = g.ctas + n_heads;  // grid size
+  g.splits = g.ctas + n_heads * n;  // grid size: room for at least one block per (cache, head)
   g.partial_bytes = (size_t)align_up((int64_t)g.splits * partial_stride(G, D) * 4, 256);
   g.ticket_off = g.partial_bytes;
   return g;
 }
+static DecodeGeom decode_geom(const rdkv_cache* c) { return decode_geom(&c, 1); }
 
 // ws: partials, then per-head tickets, the status word and the fused step's head counter
 static size_t decode_ws_bytes(const DecodeGeom& g, int n_heads) {
@@ -1174,9 +1204,13 @@ static size_t decode_ws_bytes(const DecodeGeom& g, int n_heads) {
 
 rdkv_status check_cache_public(const rdkv_cache* c);
 
-// Kernel arguments of one decode call; ws holds the partials, then the tickets and the status word.
-static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo, const void* q, float* out, void* ws,
-                                  const void* k_new = nullptr, const void* v_new = nullptr, float* lse = nullptr) {
+// Kernel arguments of one decode call over parts[0 .. n); ws holds the partials, then the tickets and
+// the status word.  The blocks are dealt on the host when every cache's plan costs reached it
+// (rdkv_plan_sizes), else (one cache only) by the kernel.
+static DecodeParams decode_params(const rdkv_cache* const* parts, int n, const DecodeGeom& geo, const void* q,
+                                  float* out, void* ws, const void* k_new = nullptr, const void* v_new = nullptr,
+                                  float* lse = nullptr) {
+  const rdkv_cache* cache = parts[0];
   const rdkv_shape& s = cache->shape;
   const int n_heads = s.batch * s.h_kv;
   const PlanLayout L = plan_layout(s.batch, s.h_kv, s.head_dim);
@@ -1207,29 +1241,61 @@ static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo
   P.ring_bytes = geo.ring_bytes;
   P.ring_warps = geo.ring_warps;
   P.ctas = geo.ctas;
-  // Deal the blocks to the heads here when the plan's cost estimates reached the host: the kernel
+  for (int p = 0; p < kMaxParts; ++p) {
+    const rdkv_cache* c = parts[p < n ? p : 0];
+    DecodePart& d = P.parts[p];
+    d.zone_a = c->zone_a;
+    d.zone_b = c->zone_b;
+    d.zone_c_k = c->zone_c_k;
+    d.zone_c_v = c->zone_c_v;
+    d.len_dev = c->len_dev;
+    d.heads = reinterpret_cast<const rdkv_head_plan*>(static_cast<const char*>(c->plan) + L.heads_off);
+    d.slots = reinterpret_cast<const int16_t*>(static_cast<const char*>(c->plan) + L.slots_off);
+    d.cap_c = c->cap_c;
+  }
+  // Deal the blocks to the heads here when the plans' cost estimates reached the host: the kernel
   // then knows its head at once instead of reading every head record first.  The rule is the
-  // kernel's own (at least one block per head, the rest in proportion to the cost).
+  // kernel's own (at least one block per head and cache, the rest in proportion to the cost).
   P.dealt = 0;
-  bool known = n_heads <= RDKV_COST_HEADS && geo.splits <= kMaxDealtBlocks && cache->sizes.n_heads == n_heads;
-  for (int h = 0; known && h < n_heads; ++h) known = cache->sizes.head_cost[h] > 0;
+  bool known = n_heads <= RDKV_COST_HEADS && geo.splits <= kMaxDealtBlocks;
+  for (int p = 0; known && p < n; ++p) {
+    known = parts[p]->sizes.n_heads == n_heads;
+    for (int h = 0; known && h < n_heads; ++h) known = parts[p]->sizes.head_cost[h] > 0;
+  }
   if (known) {
-    const int zc = ceil_div(cache->cap_c, kCRows);
+    auto cost = [&](int p, int h) {
+      return parts[p]->sizes.head_cost[h] + (int64_t)ceil_div(parts[p]->cap_c, kCRows) * kZoneCBlockCost;
+    };
     int64_t total = 0;
-    for (int h = 0; h < n_heads; ++h) total += cache->sizes.head_cost[h] + (int64_t)zc * kZoneCBlockCost;
+    for (int p = 0; p < n; ++p)
+      for (int h = 0; h < n_heads; ++h) total += cost(p, h);
     int start = 0;
     for (int h = 0; h < n_heads; ++h) {
-      const int64_t w = cache->sizes.head_cost[h] + (int64_t)zc * kZoneCBlockCost;
-      const int c = std::max(1, (int)(w * geo.ctas / total));
       P.head_first[h] = (int16_t)start;
-      for (int k = 0; k < c; ++k) P.block_head[start + k] = (uint8_t)h;
-      start += c;
+      for (int p = 0; p < n; ++p) {
+        const int c = std::max(1, (int)(cost(p, h) * geo.ctas / total));
+        for (int k = 0; k < c; ++k) {
+          P.block_head[start + k] = (uint8_t)h;
+          P.block_part[start + k] = (uint8_t)p;
+          P.block_split[start + k] = (uint8_t)k;
+          P.block_nsplit[start + k] = (uint8_t)c;
+        }
+        start += c;
+      }
     }
     P.head_first[n_heads] = (int16_t)start;
-    for (int k = start; k < geo.splits; ++k) P.block_head[k] = kNoHead;
+    for (int k = start; k < geo.splits; ++k) {
+      P.block_head[k] = kNoHead;
+      P.block_part[k] = P.block_split[k] = 0;
+      P.block_nsplit[k] = 1;
+    }
     P.dealt = 1;
   }
   return P;
+}
+static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo, const void* q, float* out, void* ws,
+                                  const void* k_new = nullptr, const void* v_new = nullptr, float* lse = nullptr) {
+  return decode_params(&cache, 1, geo, q, out, ws, k_new, v_new, lse);
 }
 
 // pdl: programmatic dependent launch; the kernel's static setup (plan, zone A) may then overlap
@@ -1338,27 +1404,78 @@ extern "C" rdkv_status rdkv_decode_step_lse(rdkv_cache* cache, const void* q, co
   return decode_step_impl(cache, q, k_new, v_new, out, lse, ws, ws_bytes, stream);
 }
 
-extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream) {
-  rdkv_status st = check_cache_public(cache);
-  if (st != RDKV_OK) return st;
-  RDKV_REQUIRE(ws, RDKV_ERR_INVALID_ARG, "NULL workspace");
-  const DecodeGeom geo = decode_geom(cache);
-  const int n_heads = cache->shape.batch * cache->shape.h_kv;
+static rdkv_status decode_status_at(const void* ws, size_t status_off, void* stream) {
   int32_t v = 0;
-  RDKV_TRY_CUDA(cudaMemcpyAsync(&v, static_cast<const char*>(ws) + geo.ticket_off + 4 * (size_t)n_heads, 4,
-                                cudaMemcpyDeviceToHost, (cudaStream_t)stream),
+  RDKV_TRY_CUDA(cudaMemcpyAsync(&v, static_cast<const char*>(ws) + status_off, 4, cudaMemcpyDeviceToHost,
+                                (cudaStream_t)stream),
                 "status read");
   RDKV_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status sync");
   if (v != RDKV_OK) {
     if (v == RDKV_ERR_TIMEOUT) set_error("decode: a bounded wait for a tile copy ran out");
     else if (v == RDKV_ERR_CAPACITY) set_error("decode step: zone C was full, the new token was not stored");
     else set_error("decode reported status %d", v);
-    RDKV_TRY_CUDA(cudaMemsetAsync(static_cast<char*>(const_cast<void*>(ws)) + geo.ticket_off + 4 * (size_t)n_heads, 0, 4,
-                                  (cudaStream_t)stream),
+    RDKV_TRY_CUDA(cudaMemsetAsync(static_cast<char*>(const_cast<void*>(ws)) + status_off, 0, 4, (cudaStream_t)stream),
                   "status clear");
     RDKV_TRY_CUDA(cudaStreamSynchronize((cudaStream_t)stream), "status clear sync");
   }
   return (rdkv_status)v;
+}
+
+extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream) {
+  rdkv_status st = check_cache_public(cache);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(ws, RDKV_ERR_INVALID_ARG, "NULL workspace");
+  const DecodeGeom geo = decode_geom(cache);
+  const int n_heads = cache->shape.batch * cache->shape.h_kv;
+  return decode_status_at(ws, geo.ticket_off + 4 * (size_t)n_heads, stream);
+}
+
+// ---------------------------------------------------------------- one launch over several caches
+static rdkv_status check_parts(const rdkv_cache* const* parts, int32_t n_parts) {
+  RDKV_REQUIRE(parts && n_parts >= 1 && n_parts <= kMaxParts, RDKV_ERR_INVALID_ARG, "n_parts %d outside [1, %d]",
+               n_parts, kMaxParts);
+  for (int p = 0; p < n_parts; ++p) {
+    rdkv_status st = check_cache_public(parts[p]);
+    if (st != RDKV_OK) return st;
+    const rdkv_shape &a = parts[0]->shape, &b = parts[p]->shape;
+    RDKV_REQUIRE(a.batch == b.batch && a.h_q == b.h_q && a.h_kv == b.h_kv && a.head_dim == b.head_dim &&
+                     a.dtype == b.dtype,
+                 RDKV_ERR_INVALID_ARG, "cache %d does not share the shape of cache 0 (batch, heads, D, dtype)", p);
+  }
+  return RDKV_OK;
+}
+
+extern "C" size_t rdkv_decode_multi_workspace_bytes(const rdkv_cache* const* parts, int32_t n_parts) {
+  if (check_parts(parts, n_parts) != RDKV_OK) return 0;
+  return decode_ws_bytes(decode_geom(parts, n_parts), parts[0]->shape.batch * parts[0]->shape.h_kv);
+}
+
+extern "C" rdkv_status rdkv_decode_attn_multi(const rdkv_cache* const* parts, int32_t n_parts, const void* q,
+                                              float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  rdkv_status st = check_parts(parts, n_parts);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(q && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  const rdkv_shape& s = parts[0]->shape;
+  const int n_heads = s.batch * s.h_kv;
+  const DecodeGeom geo = decode_geom(parts, n_parts);
+  const size_t need = decode_ws_bytes(geo, n_heads);
+  RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
+  RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
+               (long long)geo.max_item);
+  const DecodeParams P = decode_params(parts, n_parts, geo, q, out, ws, nullptr, nullptr, lse);
+  RDKV_REQUIRE(P.dealt || n_parts == 1, RDKV_ERR_UNSUPPORTED,
+               "several caches need their plan costs on the host (rdkv_plan_sizes), at most %d heads and %d blocks",
+               RDKV_COST_HEADS, kMaxDealtBlocks);
+  return launch_decode(P, geo, s, (cudaStream_t)stream, true);
+}
+
+extern "C" rdkv_status rdkv_decode_multi_status(const rdkv_cache* const* parts, int32_t n_parts, const void* ws,
+                                                void* stream) {
+  rdkv_status st = check_parts(parts, n_parts);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(ws, RDKV_ERR_INVALID_ARG, "NULL workspace");
+  const DecodeGeom geo = decode_geom(parts, n_parts);
+  return decode_status_at(ws, geo.ticket_off + 4 * (size_t)(parts[0]->shape.batch * parts[0]->shape.h_kv), stream);
 }
 
 // ---------------------------------------------------------------- decode without a caller workspace

@@ -28,7 +28,8 @@ EXPORTED = (
     "rdkv_decode_workspace_bytes", "rdkv_decode_attn", "rdkv_decode_step", "rdkv_decode_status",
     "rdkv_decode_attn_noalloc",
     "rdkv_decode_attn_lse", "rdkv_decode_step_lse", "rdkv_merge_attn", "rdkv_zone_c_take", "rdkv_recompress_score",
-    "rdkv_allocate_at_levels",
+    "rdkv_allocate_at_levels", "rdkv_decode_multi_workspace_bytes", "rdkv_decode_attn_multi",
+    "rdkv_decode_multi_status",
 )
 
 
@@ -109,6 +110,9 @@ def lib():
             "rdkv_zone_c_take": (ctypes.c_int, [cp, ctypes.c_int32, _P, _P, _P]),
             "rdkv_recompress_score": (ctypes.c_int, [sp, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32,
                                                      ctypes.c_float, _P, _P, _P, _P]),
+            "rdkv_decode_multi_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32]),
+            "rdkv_decode_attn_multi": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+            "rdkv_decode_multi_status": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P]),
             "rdkv_allocate_at_levels": (ctypes.c_int, [sp, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                        ctypes.c_size_t, _P]),
         }
@@ -436,3 +440,34 @@ def decode_segments(segments, live, q, stream=None):
     for i, c in enumerate(parts):
         rdkv_decode_attn_lse(c, q, out=outs[i], lse=lses[i], stream=stream)
     return rdkv_merge_attn(outs, lses, stream=stream)
+
+
+class MultiDecode:
+    """One launch over several caches (segments, then the live cache): keeps the array of their C
+    structs and the zero-filled workspace the list needs."""
+
+    def __init__(self, parts):
+        self.parts = list(parts)
+        self._arr = (ctypes.POINTER(CacheStruct) * len(self.parts))(*[ctypes.pointer(c.c) for c in self.parts])
+        self._ws = None
+
+    def workspace(self):
+        nb = lib().rdkv_decode_multi_workspace_bytes(ctypes.cast(self._arr, _P), len(self.parts))
+        if nb == 0:
+            _check(RDKV_ERR_INVALID_ARG)
+        if self._ws is None or self._ws.numel() < nb:
+            self._ws = torch.zeros(max(int(nb), 256), dtype=torch.uint8, device=self.parts[0].zone_a.device)
+        return self._ws
+
+    def attn(self, q, out=None, lse=None, stream=None):
+        B, Hq, D = q.shape
+        out = out if out is not None else torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+        lse = lse if lse is not None else torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+        ws = self.workspace()
+        _check(lib().rdkv_decode_attn_multi(ctypes.cast(self._arr, _P), len(self.parts), _ptr(q), _ptr(out), _ptr(lse),
+                                            _ptr(ws), ws.numel(), _stream(stream)))
+        return out, lse
+
+    def status(self, stream=None):
+        return lib().rdkv_decode_multi_status(ctypes.cast(self._arr, _P), len(self.parts), _ptr(self.workspace()),
+                                              _stream(stream))

@@ -163,3 +163,24 @@ def test_recompress_argument_checks(L):
     r = L.rdkv_allocate_at_levels(ctypes.byref(seg), 0, None, fake, fake, fake, fake, fake, fake, fake, fake, fake,
                                   1 << 30, None)
     assert r == rdkv.RDKV_ERR_INVALID_ARG and b"levels" in L.rdkv_last_error_string()
+
+
+def test_multi_decode_argument_checks(L):
+    """The several-cache decode checks the list and the shared shape on the host."""
+    sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 0, 1)
+    a = rdkv.CacheStruct(rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16"), 256, None, None, 256, 256, None, 256, 16, 8, sizes)
+    b = rdkv.CacheStruct(rdkv.make_shape(1, 64, 4, 1, 128, 8, "f16"), 256, None, None, 256, 256, None, 256, 16, 8,
+                         sizes)
+    arr = (ctypes.POINTER(rdkv.CacheStruct) * 9)(*([ctypes.pointer(a)] * 9))
+    fake = ctypes.c_void_p(256)
+    assert L.rdkv_decode_multi_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), 9) == 0
+    assert L.rdkv_decode_multi_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), 2) > 0
+    r = L.rdkv_decode_attn_multi(ctypes.cast(arr, ctypes.c_void_p), 0, fake, fake, None, fake, 1 << 30, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+    arr[1] = ctypes.pointer(b)
+    r = L.rdkv_decode_attn_multi(ctypes.cast(arr, ctypes.c_void_p), 2, fake, fake, None, fake, 1 << 30, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG and b"shape" in L.rdkv_last_error_string()
+    # without plan costs on the host, several caches cannot be dealt
+    arr[1] = ctypes.pointer(a)
+    r = L.rdkv_decode_attn_multi(ctypes.cast(arr, ctypes.c_void_p), 2, fake, fake, None, fake, 1 << 30, None)
+    assert r == rdkv.RDKV_ERR_UNSUPPORTED

@@ -162,6 +162,15 @@ def test_recompress_matches_oracle_step_by_step(case):
     exp, exp_lse = O.merge_attention(np.stack([o1, o2]), np.stack([l1, l2]))
     assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3
     assert np.abs(lse.cpu().numpy() - exp_lse).max() <= 2e-3
+    # one launch over both caches
+    md = rdkv.MultiDecode([seg_cache, cache])
+    out, lse = md.attn(qn.to(DEV))
+    assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3
+    assert np.abs(lse.cpu().numpy() - exp_lse).max() <= 2e-3
+    assert md.status() == 0
+    # one cache through the several-cache call: the plain decode's result
+    one, one_lse = rdkv.MultiDecode([cache]).attn(qn.to(DEV))
+    assert np.abs(one.cpu().numpy() - o2).max() <= 2e-3 and np.abs(one_lse.cpu().numpy() - l2).max() <= 2e-3
 
 
 def test_recompress_helper_and_a_second_segment():
@@ -196,5 +205,8 @@ def test_recompress_helper_and_a_second_segment():
     out, lse = rdkv.decode_segments(segs, cache, qn.to(DEV))
     parts = [O.decode_lse(r, qn.numpy()) for r in seg_refs + [ref]]
     exp, exp_lse = O.merge_attention(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3
+    assert np.abs(lse.cpu().numpy() - exp_lse).max() <= 2e-3
+    out, lse = rdkv.MultiDecode(segs + [cache]).attn(qn.to(DEV))  # three caches, one launch
     assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3
     assert np.abs(lse.cpu().numpy() - exp_lse).max() <= 2e-3

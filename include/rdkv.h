@@ -107,8 +107,17 @@ typedef struct rdkv_sizes {
   int32_t head_cost[RDKV_COST_HEADS];
 } rdkv_sizes;
 
+/* Rows of one zone-C page when zone C is paged (see rdkv_cache). */
+#define RDKV_ZONE_C_PAGE_ROWS 16
+
 /* A packed TriZone cache.  All pointers are caller-owned device memory.
- * zone_c_k / zone_c_v are fp16 [batch][h_kv][cap_c][D].  The number of zone-C
+ * zone_c_k / zone_c_v are fp16 [batch][h_kv][cap_c][D], or, when
+ * zone_c_pages is not NULL, pools of pages [n_pages][RDKV_ZONE_C_PAGE_ROWS][D]
+ * (PagedAttention-style block table): row r of head h = b * h_kv + j is row
+ * r % 16 of page zone_c_pages[h * zone_c_page_stride + r / 16].  The table
+ * (int32, device) must name a distinct page for every 16-row block a head may
+ * use (up to cap_c rows, so zone_c_page_stride >= ceil(cap_c / 16)); the
+ * kernels read it when they touch zone C.  The number of zone-C
  * rows in use (same for every sequence) is kept twice: len_dev (one device
  * int32) is what the kernels read and advance, so a captured CUDA graph of
  * append + decode calls stays correct when replayed; len_c is the host mirror
@@ -127,6 +136,8 @@ typedef struct rdkv_cache {
   int32_t cap_c;
   int32_t len_c;
   rdkv_sizes sizes;
+  const int32_t* zone_c_pages;  /* NULL: contiguous zone C; else its page table */
+  int32_t zone_c_page_stride;   /* table entries per head */
 } rdkv_cache;
 
 /* ---------------------------------------------------------------- misc */

@@ -70,6 +70,14 @@ __host__ __device__ inline int tile_bytes_of(int row_words, int meta_slots, int 
   return b;
 }
 
+// Element offset of row `row` of head `head` in zone C: contiguous [heads][cap][D], or, with a page
+// table, row row % 16 of page pages[head * stride + row / 16] of a pool [pages][16][D].
+constexpr int kZoneCPageRows = RDKV_ZONE_C_PAGE_ROWS;
+__host__ __device__ inline int64_t zone_c_offset(const int32_t* pages, int stride, int cap, int head, int row, int D) {
+  return pages ? ((int64_t)pages[(int64_t)head * stride + row / kZoneCPageRows] * kZoneCPageRows + row % kZoneCPageRows) * D
+               : ((int64_t)head * cap + row) * D;
+}
+
 // ---------------------------------------------------------------- numerics
 __device__ __forceinline__ float load_as_float(const void* p, int64_t i, int dtype) {
   return dtype == RDKV_F16 ? __half2float(static_cast<const __half*>(p)[i]) : static_cast<const float*>(p)[i];

@@ -74,6 +74,8 @@ struct DecodePart {
   int32_t* len_dev;
   const rdkv_head_plan* heads;
   const int16_t* slots;
+  const int32_t* zc_pages;  // zone-C page table, or NULL (contiguous)
+  int zc_page_stride;
   int cap_c;
 };
 
@@ -814,7 +816,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         // rows of zone C (the fused step's new row, past them, is written by the consumer)
         const int rows = max(0, min(kCRows, len_c - c_row));
         const uint32_t bytes = (uint32_t)rows * D * 2;
-        const int64_t src = ((int64_t)head * PP.cap_c + c_row) * D;
+        // a zone-C item is 16 rows: one page when zone C is paged
+        const int64_t src = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, head, c_row, D);
         mbar_arrive_expect_tx(bar, 2 * bytes);
         if (bytes) {
           bulk_copy(dst, PP.zone_c_k + src, bytes, bar);
@@ -1087,10 +1090,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     // every block of this head has read zone C: store the new row of this head; the last head to
     // get here advances the length (every block of every head has read it by then)
     if (len_c < P.cap_c) {
-      const int64_t dst = ((int64_t)head * P.cap_c + len_c) * D;
+      const int64_t dst = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, head, len_c, D);
       for (int i = tid; i < D; i += blockDim.x) {
-        const_cast<uint16_t*>(P.zone_c_k)[dst + i] = newrow[i];
-        const_cast<uint16_t*>(P.zone_c_v)[dst + i] = newrow[D + i];
+        const_cast<uint16_t*>(PP.zone_c_k)[dst + i] = newrow[i];
+        const_cast<uint16_t*>(PP.zone_c_v)[dst + i] = newrow[D + i];
       }
     } else if (tid == 0) {
       atomicExch(P.error, (int)RDKV_ERR_CAPACITY);
@@ -1251,6 +1254,8 @@ static DecodeParams decode_params(const rdkv_cache* const* parts, int n, const D
     d.len_dev = c->len_dev;
     d.heads = reinterpret_cast<const rdkv_head_plan*>(static_cast<const char*>(c->plan) + L.heads_off);
     d.slots = reinterpret_cast<const int16_t*>(static_cast<const char*>(c->plan) + L.slots_off);
+    d.zc_pages = c->zone_c_pages;
+    d.zc_page_stride = c->zone_c_page_stride;
     d.cap_c = c->cap_c;
   }
   // Deal the blocks to the heads here when the plans' cost estimates reached the host: the kernel

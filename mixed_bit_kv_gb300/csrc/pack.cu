@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
 
 template <typename T>
 __global__ void window_kernel(const T* __restrict__ x, int N, int W, int h_kv, int D, int cap, int batch,
-                              uint16_t* __restrict__ zc) {
+                              uint16_t* __restrict__ zc, const int32_t* __restrict__ pages, int stride) {
   const int64_t total = (int64_t)batch * h_kv * W * D;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int c = (int)(i % D);
@@ -318,7 +318,8 @@ __global__ void window_kernel(const T* __restrict__ x, int N, int W, int h_kv, i
     rest /= W;
     const int j = (int)(rest % h_kv);
     const int b = (int)(rest / h_kv);
-    zc[(((int64_t)b * h_kv + j) * cap + r) * D + c] = half_bits(to_float(x[(((int64_t)b * N + (N - W) + r) * h_kv + j) * D + c]));
+    zc[zone_c_offset(pages, stride, cap, b * h_kv + j, r, D) + c] =
+        half_bits(to_float(x[(((int64_t)b * N + (N - W) + r) * h_kv + j) * D + c]));
   }
 }
 
@@ -326,11 +327,12 @@ __global__ void window_kernel(const T* __restrict__ x, int N, int W, int h_kv, i
 template <typename T>
 __global__ void __launch_bounds__(1024) append_kernel(const T* __restrict__ kn, const T* __restrict__ vn, int64_t n,
                                                       int D, int cap, int32_t* len_dev, uint16_t* __restrict__ zk,
-                                                      uint16_t* __restrict__ zv) {
+                                                      uint16_t* __restrict__ zv, const int32_t* __restrict__ pages,
+                                                      int stride) {
   const int row = *len_dev;
   if (row < cap) {
     for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-      const int64_t dst = ((i / D) * cap + row) * D + (i % D);
+      const int64_t dst = zone_c_offset(pages, stride, cap, (int)(i / D), row, D) + (i % D);
       zk[dst] = half_bits(to_float(kn[i]));
       zv[dst] = half_bits(to_float(vn[i]));
     }
@@ -359,6 +361,8 @@ static rdkv_status check_cache(const rdkv_cache* c) {
   RDKV_REQUIRE(c->cap_c >= c->shape.window && c->cap_c >= 0, RDKV_ERR_INVALID_ARG, "cap_c %d < window %d", c->cap_c,
                c->shape.window);
   RDKV_REQUIRE(c->len_c >= 0 && c->len_c <= c->cap_c, RDKV_ERR_INVALID_ARG, "len_c %d outside [0, cap_c]", c->len_c);
+  RDKV_REQUIRE(c->zone_c_pages == nullptr || (int64_t)c->zone_c_page_stride * kZoneCPageRows >= c->cap_c,
+               RDKV_ERR_INVALID_ARG, "page table stride %d too small for cap_c %d", c->zone_c_page_stride, c->cap_c);
   RDKV_REQUIRE(c->sizes.n_heads == c->shape.batch * c->shape.h_kv, RDKV_ERR_INVALID_ARG,
                "cache sizes do not belong to this shape (call rdkv_plan_sizes)");
   return RDKV_OK;
@@ -406,14 +410,14 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
     const unsigned grid = (unsigned)std::min<int64_t>(ceil_div64(total, 256), 4096);
     if (s.dtype == RDKV_F16) {
       window_kernel<__half><<<grid, 256, 0, cs>>>(static_cast<const __half*>(k), N, W, s.h_kv, D, cache->cap_c, s.batch,
-                                                  cache->zone_c_k);
+                                                  cache->zone_c_k, cache->zone_c_pages, cache->zone_c_page_stride);
       window_kernel<__half><<<grid, 256, 0, cs>>>(static_cast<const __half*>(v), N, W, s.h_kv, D, cache->cap_c, s.batch,
-                                                  cache->zone_c_v);
+                                                  cache->zone_c_v, cache->zone_c_pages, cache->zone_c_page_stride);
     } else {
       window_kernel<float><<<grid, 256, 0, cs>>>(static_cast<const float*>(k), N, W, s.h_kv, D, cache->cap_c, s.batch,
-                                                 cache->zone_c_k);
+                                                 cache->zone_c_k, cache->zone_c_pages, cache->zone_c_page_stride);
       window_kernel<float><<<grid, 256, 0, cs>>>(static_cast<const float*>(v), N, W, s.h_kv, D, cache->cap_c, s.batch,
-                                                 cache->zone_c_v);
+                                                 cache->zone_c_v, cache->zone_c_pages, cache->zone_c_page_stride);
     }
     RDKV_CHECK_LAUNCH("zone C window");
   }
@@ -434,11 +438,11 @@ extern "C" rdkv_status rdkv_append(rdkv_cache* cache, const void* k_new, const v
   if (s.dtype == RDKV_F16)
     append_kernel<__half><<<1, 1024, 0, cs>>>(static_cast<const __half*>(k_new), static_cast<const __half*>(v_new), n,
                                                s.head_dim, cache->cap_c, cache->len_dev, cache->zone_c_k,
-                                               cache->zone_c_v);
+                                               cache->zone_c_v, cache->zone_c_pages, cache->zone_c_page_stride);
   else
     append_kernel<float><<<1, 1024, 0, cs>>>(static_cast<const float*>(k_new), static_cast<const float*>(v_new), n,
                                               s.head_dim, cache->cap_c, cache->len_dev, cache->zone_c_k,
-                                              cache->zone_c_v);
+                                              cache->zone_c_v, cache->zone_c_pages, cache->zone_c_page_stride);
   RDKV_CHECK_LAUNCH("append");
   cache->len_c += 1;
   return RDKV_OK;

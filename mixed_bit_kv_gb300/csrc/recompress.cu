@@ -44,11 +44,12 @@ __global__ void merge_attn_kernel(int n_parts, const float* outs, const float* _
 // Rows [0, n_move) of head (b, j) -> dst [b][t][j][D] in the cache's dtype (fp16 bits, or the fp16
 // values widened to fp32); one block per (head, row).
 template <typename T>
-__global__ void take_rows_kernel(const uint16_t* __restrict__ zk, const uint16_t* __restrict__ zv, int h_kv, int cap,
-                                 int D, int n_move, T* __restrict__ k_out, T* __restrict__ v_out) {
+__global__ void take_rows_kernel(const uint16_t* __restrict__ zk, const uint16_t* __restrict__ zv,
+                                 const int32_t* __restrict__ pages, int stride, int h_kv, int cap, int D, int n_move,
+                                 T* __restrict__ k_out, T* __restrict__ v_out) {
   const int head = blockIdx.y, t = blockIdx.x;
   const int b = head / h_kv, j = head % h_kv;
-  const int64_t src = ((int64_t)head * cap + t) * D;
+  const int64_t src = zone_c_offset(pages, stride, cap, head, t, D);
   const int64_t dst = (((int64_t)b * n_move + t) * h_kv + j) * D;
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
     if constexpr (sizeof(T) == 2) {
@@ -62,10 +63,12 @@ __global__ void take_rows_kernel(const uint16_t* __restrict__ zk, const uint16_t
 }
 
 // Rows [n_move, len_c) -> [0, len_c - n_move); the two ranges do not overlap (checked on the host).
-__global__ void shift_rows_kernel(uint16_t* __restrict__ zk, uint16_t* __restrict__ zv, int cap, int D, int n_move,
+__global__ void shift_rows_kernel(uint16_t* __restrict__ zk, uint16_t* __restrict__ zv,
+                                  const int32_t* __restrict__ pages, int stride, int cap, int D, int n_move,
                                   int32_t* len_dev, int new_len) {
   const int head = blockIdx.y, t = blockIdx.x;
-  const int64_t src = ((int64_t)head * cap + n_move + t) * D, dst = ((int64_t)head * cap + t) * D;
+  const int64_t src = zone_c_offset(pages, stride, cap, head, n_move + t, D);
+  const int64_t dst = zone_c_offset(pages, stride, cap, head, t, D);
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
     zk[dst + c] = zk[src + c];
     zv[dst + c] = zv[src + c];
@@ -188,17 +191,17 @@ extern "C" rdkv_status rdkv_zone_c_take(rdkv_cache* cache, int32_t n_move, void*
   cudaStream_t cs = (cudaStream_t)stream;
   if (s.dtype == RDKV_F16)
     take_rows_kernel<uint16_t><<<dim3(n_move, n_heads), std::min(D, 256), 0, cs>>>(
-        cache->zone_c_k, cache->zone_c_v, s.h_kv, cache->cap_c, D, n_move, static_cast<uint16_t*>(k_out),
-        static_cast<uint16_t*>(v_out));
+        cache->zone_c_k, cache->zone_c_v, cache->zone_c_pages, cache->zone_c_page_stride, s.h_kv, cache->cap_c, D,
+        n_move, static_cast<uint16_t*>(k_out), static_cast<uint16_t*>(v_out));
   else
     take_rows_kernel<float><<<dim3(n_move, n_heads), std::min(D, 256), 0, cs>>>(
-        cache->zone_c_k, cache->zone_c_v, s.h_kv, cache->cap_c, D, n_move, static_cast<float*>(k_out),
-        static_cast<float*>(v_out));
+        cache->zone_c_k, cache->zone_c_v, cache->zone_c_pages, cache->zone_c_page_stride, s.h_kv, cache->cap_c, D,
+        n_move, static_cast<float*>(k_out), static_cast<float*>(v_out));
   RDKV_CHECK_LAUNCH("zone C rows out");
   if (L - n_move > 0) {
-    shift_rows_kernel<<<dim3(L - n_move, n_heads), std::min(D, 256), 0, cs>>>(cache->zone_c_k, cache->zone_c_v,
-                                                                                cache->cap_c, D, n_move,
-                                                                                cache->len_dev, L - n_move);
+    shift_rows_kernel<<<dim3(L - n_move, n_heads), std::min(D, 256), 0, cs>>>(
+        cache->zone_c_k, cache->zone_c_v, cache->zone_c_pages, cache->zone_c_page_stride, cache->cap_c, D, n_move,
+        cache->len_dev, L - n_move);
     RDKV_CHECK_LAUNCH("zone C rows to the front");
   } else {
     set_len_value_kernel<<<1, 1, 0, cs>>>(cache->len_dev, 0);

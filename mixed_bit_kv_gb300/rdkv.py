@@ -57,7 +57,9 @@ class CacheStruct(ctypes.Structure):
                 ("zone_b", ctypes.c_void_p), ("zone_c_k", ctypes.c_void_p), ("zone_c_v", ctypes.c_void_p),
                 ("index_map", ctypes.c_void_p), ("len_dev", ctypes.c_void_p), ("cap_c", ctypes.c_int32),
                 ("len_c", ctypes.c_int32),
-                ("sizes", Sizes)]
+                ("sizes", Sizes), ("zone_c_pages", ctypes.c_void_p), ("zone_c_page_stride", ctypes.c_int32)]
+
+PAGE_ROWS = 16  # RDKV_ZONE_C_PAGE_ROWS
 
 
 HEAD_PLAN_DTYPE = [("n_v", "<i4", 4), ("tiles", "<i4", 4), ("n_k", "<i4", 5), ("k_words", "<i4", 4),
@@ -234,19 +236,38 @@ def rdkv_plan_sizes(plan, stream=None):
 class Cache:
     """Device buffers of one packed TriZone cache plus the C struct that points at them."""
 
-    def __init__(self, shape, plan, sizes, cap_c, device):
+    def __init__(self, shape, plan, sizes, cap_c, device, pages=None):
+        """pages: None for a contiguous zone C, else (pool_k, pool_v, table): fp16 pools
+        [n_pages, PAGE_ROWS, D] and an int32 page table [B * H_kv, stride] (see ``page_pool``)."""
         D = shape.head_dim
         self.shape, self.plan, self.sizes = shape, plan, sizes
         self.zone_a = torch.zeros(max(sizes.zone_a_bytes, 16), dtype=torch.uint8, device=device)
         self.zone_b = torch.zeros(max(sizes.zone_b_rows, 1), D, dtype=torch.float16, device=device)
-        self.zone_c_k = torch.zeros(shape.batch, shape.h_kv, max(cap_c, 1), D, dtype=torch.float16, device=device)
-        self.zone_c_v = torch.zeros_like(self.zone_c_k)
+        if pages is None:
+            self.zone_c_k = torch.zeros(shape.batch, shape.h_kv, max(cap_c, 1), D, dtype=torch.float16, device=device)
+            self.zone_c_v = torch.zeros_like(self.zone_c_k)
+            self.pages, table_ptr, stride = None, None, 0
+        else:
+            self.zone_c_k, self.zone_c_v, self.pages = pages
+            table_ptr, stride = self.pages.data_ptr(), self.pages.shape[1]
         self.index_map = torch.zeros(max(sizes.index_slots, 1), dtype=torch.int32, device=device)
         self.len_dev = torch.zeros(1, dtype=torch.int32, device=device)
         self.c = CacheStruct(shape, plan.data_ptr(), self.zone_a.data_ptr(), self.zone_b.data_ptr(),
                              self.zone_c_k.data_ptr(), self.zone_c_v.data_ptr(), self.index_map.data_ptr(),
-                             self.len_dev.data_ptr(), cap_c, 0, sizes)
+                             self.len_dev.data_ptr(), cap_c, 0, sizes, table_ptr, stride)
         self._ws = None
+
+    def zone_c_rows(self):
+        """Zone C as logical rows: (k, v) fp16 [B, H_kv, cap_c, D], gathered through the page table."""
+        s, cap = self.shape, self.c.cap_c
+        if self.pages is None:
+            return self.zone_c_k[:, :, :cap], self.zone_c_v[:, :, :cap]
+        rows = torch.arange(cap, device=self.pages.device)
+        phys = self.pages[:, rows // PAGE_ROWS].long() * PAGE_ROWS + rows % PAGE_ROWS  # [heads, cap]
+        D = s.head_dim
+        k = self.zone_c_k.reshape(-1, D)[phys].reshape(s.batch, s.h_kv, cap, D)
+        v = self.zone_c_v.reshape(-1, D)[phys].reshape(s.batch, s.h_kv, cap, D)
+        return k, v
 
     def fits(self, sizes):
         """True when a plan with these totals can be packed into this cache's buffers."""
@@ -265,15 +286,31 @@ class Cache:
         return self._ws
 
 
-def rdkv_pack(shape, plan, k, v, bits_tok, bits_chan, cap_c, stream=None, sizes=None, into=None):
-    """Packs into a new Cache, or into the buffers of `into` when they are large enough."""
+def page_pool(shape, cap_c, device, extra_pages=0, seed=None):
+    """A zone-C page pool for one cache: fp16 pools [n_pages, PAGE_ROWS, D] and the page table
+    [B * H_kv, ceil(cap_c / PAGE_ROWS)] naming a distinct page per 16-row block (in a seeded random
+    order when seed is given, to show that nothing depends on pages being adjacent)."""
+    heads = shape.batch * shape.h_kv
+    stride = max(1, -(-cap_c // PAGE_ROWS))
+    n_pages = heads * stride + extra_pages
+    order = torch.arange(n_pages)
+    if seed is not None:
+        order = order[torch.randperm(n_pages, generator=torch.Generator().manual_seed(seed))]
+    table = order[:heads * stride].reshape(heads, stride).to(torch.int32).to(device)
+    pool_k = torch.zeros(n_pages, PAGE_ROWS, shape.head_dim, dtype=torch.float16, device=device)
+    return pool_k, torch.zeros_like(pool_k), table
+
+
+def rdkv_pack(shape, plan, k, v, bits_tok, bits_chan, cap_c, stream=None, sizes=None, into=None, pages=None):
+    """Packs into a new Cache (zone C paged when `pages` from ``page_pool`` is given), or into the
+    buffers of `into` when they are large enough."""
     sizes = sizes if sizes is not None else rdkv_plan_sizes(plan, stream)
     if into is not None and into.fits(sizes) and into.c.cap_c == cap_c:
         cache = into
         cache.plan, cache.sizes = plan, sizes
         cache.c.plan, cache.c.sizes = plan.data_ptr(), sizes
     else:
-        cache = Cache(shape, plan, sizes, cap_c, k.device)
+        cache = Cache(shape, plan, sizes, cap_c, k.device, pages=pages)
     _check(lib().rdkv_pack(ctypes.byref(cache.c), _ptr(k), _ptr(v), _ptr(bits_tok), _ptr(bits_chan),
                            _stream(stream)))
     return cache
@@ -419,8 +456,14 @@ def recompress(live, prefill_plan, w_chan, q_recent, lse_recent, n_move, per_hea
     """Moves the oldest n_move zone-C rows of `live` into a new segment (a Cache with window 0):
     weights from the recent queries and their decode lse, widths at the water levels of
     `prefill_plan` (the plan the prefill allocation wrote), the prefill's channel weights w_chan."""
-    s = live.shape
     k, v = rdkv_zone_c_take(live, n_move, stream)
+    return recompress_from_rows(live, k, v, prefill_plan, w_chan, q_recent, lse_recent, per_head, stream)
+
+
+def recompress_from_rows(live, k, v, prefill_plan, w_chan, q_recent, lse_recent, per_head=False, stream=None):
+    """The segment of rows k, v [B, n, H_kv, D] already taken out of `live` (rdkv_zone_c_take)."""
+    s = live.shape
+    n_move = k.shape[1]
     seg = Shape(s.batch, int(n_move), s.h_q, s.h_kv, s.head_dim, 0, s.dtype)
     # a prefill weight sums the attention of up to N query rows: the recent sums are scaled by N / R
     sc = rdkv_recompress_score(seg, k, v, q_recent, lse_recent, s.n_tokens / q_recent.shape[1], stream)

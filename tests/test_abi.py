@@ -184,3 +184,14 @@ def test_multi_decode_argument_checks(L):
     arr[1] = ctypes.pointer(a)
     r = L.rdkv_decode_attn_multi(ctypes.cast(arr, ctypes.c_void_p), 2, fake, fake, None, fake, 1 << 30, None)
     assert r == rdkv.RDKV_ERR_UNSUPPORTED
+
+
+def test_paged_zone_c_table_stride_is_checked(L):
+    """A page table must cover cap_c rows: stride * 16 >= cap_c, checked before any launch."""
+    s = rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16")
+    sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 0, 1)
+    fake = ctypes.c_void_p(256)
+    c = rdkv.CacheStruct(s, 256, None, None, 256, 256, None, 256, 40, 8, sizes, 256, 2)  # 2 pages: 32 rows < 40
+    r = L.rdkv_append(ctypes.byref(c), fake, fake, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG and b"page table" in L.rdkv_last_error_string()
+    assert c.len_c == 8

@@ -331,6 +331,9 @@ def run_ours(args, ws, rank, local):
     if not args.no_comparator:
         comparator = run_fp16_comparator(w, L, pre, dq, dev)
         comparator["trizone_speedup"] = round(comparator["us_per_layer_step"] / (dec_ms_step * 1e3 / (S * L)), 2)
+    paged = None
+    if not args.no_recompress and rank == 0:
+        paged = run_paged(w, shape, pre[L - 1], alloc_out[L - 1], cap_c, dq, dk, dv, dev)
     recompress = None
     if not args.no_recompress and rank == 0:
         recompress = run_recompress(w, caches[L - 1], alloc_out[L - 1]["plan"], score_out[L - 1]["w_chan"], dq, dev)
@@ -363,6 +366,8 @@ def run_ours(args, ws, rank, local):
         line["comparator"] = comparator
     if recompress is not None:
         line["recompress"] = recompress
+    if paged is not None:
+        line["paged_zone_c"] = paged
     return line
 
 
@@ -476,6 +481,42 @@ def run_recompress(w, cache, prefill_plan, w_chan, dq, dev, recent=32, reps=20):
             "note": "take rows + weights from recent queries + widths at the prefill's levels + plan "
                     "(sizes read back) + pack, CUDA events; decodes per call from CUDA graphs: one launch for the "
                     "cache; segment and cache as two launches and a merge, or as one launch over both"}
+
+
+def run_paged(w, shape, layer_inputs, al, cap_c, dq, dk, dv, dev):
+    """Paged zone C, measured beside the path: the last layer packed twice, with a contiguous zone C
+    and with its zone C in 16-row pages of a shuffled pool; per-call time of the benchmark's fused
+    decode steps (CUDA graph of every step) on each."""
+    from mixed_bit_kv_gb300 import rdkv
+    _, k, v = layer_inputs
+    S, layer = dq.shape[0], dq.shape[1] - 1
+    sizes = rdkv.rdkv_plan_sizes(al["plan"])
+    out = torch.empty(w.batch, w.h_q, w.head_dim, dtype=torch.float32, device=dev)
+    res = {}
+    for name, pages in (("contiguous", None), ("paged", rdkv.page_pool(shape, cap_c, dev, seed=7))):
+        cache = rdkv.rdkv_pack(shape, al["plan"], k, v, al["bits_tok"], al["bits_chan"], cap_c, sizes=sizes,
+                               pages=pages)
+        cache.decode_workspace()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for s in range(S):
+                rdkv.rdkv_decode_step(cache, dq[s, layer], dk[s, layer], dv[s, layer], out=out)
+        times = []
+        for _ in range(3):
+            rdkv.rdkv_pack(shape, al["plan"], k, v, al["bits_tok"], al["bits_chan"], cap_c, sizes=sizes, into=cache)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) * 1e3 / S)
+        if rdkv.rdkv_decode_status(cache) != 0:
+            raise RuntimeError("paged decode status")
+        res[name + "_us_per_step"] = round(min(times), 3)
+    res["note"] = ("one layer, every decode step of the workload (fused append + attend) from a CUDA graph, "
+                   "best of 3; zone C in 16-row pages of a shuffled pool vs contiguous")
+    return res
 
 
 def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev):
@@ -604,7 +645,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-comparator", action="store_true", help="skip the fp16 full-cache SDPA context number")
-    ap.add_argument("--no-recompress", action="store_true", help="skip the zone-C re-compression measurement")
+    ap.add_argument("--no-recompress", action="store_true", help="skip the zone-C re-compression and paged zone-C measurements")
     args = ap.parse_args()
     ws, rank, local = dist_env()
 

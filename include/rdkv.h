@@ -236,12 +236,23 @@ rdkv_status rdkv_allocate_mode(const rdkv_shape* shape, int mode, float param, c
  * plan's device status (RDKV_ERR_INVALID_ARG if a gain was invalid). */
 rdkv_status rdkv_plan_sizes(const void* plan, rdkv_sizes* out, void* stream);
 
+/* Upper bounds of the plan totals rdkv_allocate (pooled or per-head levels)
+ * can produce for this shape and these budgets, from the budgets alone: no
+ * device access, no synchronisation.  Zones sized from them let the whole
+ * compression (rdkv_score, rdkv_allocate, rdkv_pack with cache->sizes = the
+ * bounds) run as one stream-ordered sequence, capturable in a CUDA graph;
+ * rdkv_plan_sizes afterwards gives the exact totals (and the head costs) for
+ * the decode.  Not a bound for the eviction baselines of rdkv_allocate_mode
+ * (top-k, threshold), nor for the levels of rdkv_allocate_at_levels. */
+rdkv_status rdkv_zone_bounds(const rdkv_shape* shape, float avg_bits_v, float avg_bits_k, rdkv_sizes* out);
+
 /* ---------------------------------------------------------------- TriZone pack
  * RDKV section 2.3.  Writes zone A (sizes.zone_a_bytes), zone B
  * (sizes.zone_b_rows x D fp16), the index map (sizes.index_slots int32) and
  * the window rows [0, W) of zone C from the prefill k, v [B][N][H_kv][D];
  * sets cache->len_c = W.  cache->plan must be the plan bits_tok/bits_chan came
- * with; cap_c >= W.  Bytes are bit-exact with the layout rules:
+ * with; cap_c >= W; cache->sizes the plan's totals or upper bounds of them
+ * (rdkv_zone_bounds).  Bytes are bit-exact with the layout rules:
  * asymmetric min-max codes (aistudio.id "Solusi 3") with fp16 scale/zero. */
 rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v,
                       const uint8_t* bits_tok, const uint8_t* bits_chan, void* stream);

@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   const rdkv_plan_header* hdr = plan_header(plan);
   const rdkv_head_plan* heads = plan_heads(plan);
   const int64_t slot0 = (int64_t)blockIdx.x * kTile;
+  // a grid sized from upper bounds (rdkv_zone_bounds) has blocks past the plan's last tile
+  if (slot0 >= hdr->index_slots) return;
   // head whose slot range holds this tile
   int lo = 0, hi = hdr->n_heads - 1;
   while (lo < hi) {
@@ -424,6 +426,40 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
   set_len_kernel<<<1, 1, 0, cs>>>(cache->len_dev, W);
   RDKV_CHECK_LAUNCH("zone C length");
   cache->len_c = W;
+  return RDKV_OK;
+}
+
+// Upper bounds of the plan totals (per sequence, then times the batch).  Every kept token costs at
+// least 2 of the sequence's B_V bits and a 16-bit one 16; each (head, class) segment is padded to
+// whole tiles; a K row holds sum_c b_c bits plus at most one padding word per width segment, and the
+// K widths of a sequence sum to at most B_K; a tile carries at most D + kSlotPad metadata slots.
+extern "C" rdkv_status rdkv_zone_bounds(const rdkv_shape* s, float avg_bits_v, float avg_bits_k, rdkv_sizes* out) {
+  rdkv_status st = check_shape(s);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  RDKV_REQUIRE(std::isfinite(avg_bits_v) && avg_bits_v >= 0 && std::isfinite(avg_bits_k) && avg_bits_k >= 0,
+               RDKV_ERR_INVALID_ARG, "budgets must be finite and >= 0");
+  const int64_t Np = s->n_tokens - s->window, H = s->h_kv, D = s->head_dim;
+  const int64_t UV = H * Np;
+  const int64_t BV = (int64_t)std::floor((double)avg_bits_v * (double)UV);
+  const int64_t BK = std::min<int64_t>((int64_t)std::floor((double)avg_bits_k * (double)(H * D)), 16 * H * D);
+  const int64_t kept = std::min<int64_t>(UV, BV / 2), n16 = std::min<int64_t>(UV, BV / 16);
+  const int64_t tiles = ceil_div64(kept, kTile) + 4 * H;                 // sum over (head, class) of ceil(n / 32)
+  const int64_t t_head = ceil_div64(std::min<int64_t>(Np, kept), kTile) + 4;  // tiles of one head
+  const int64_t rw_sum = ceil_div64(BK, 32) + 4 * H;                      // row words of all heads
+  const int64_t k_bytes = t_head * 4 * kTile * rw_sum + tiles * 4 * (D + kSlotPad);
+  const int64_t v_bytes = D * (std::min<int64_t>(BV, 8 * UV) / 8) + H * 4 * (kTile - 1) * D + tiles * 4 * D;
+  const int64_t b = s->batch;
+  out->zone_a_bytes = b * (k_bytes + v_bytes);
+  out->zone_b_rows = b * kTile * (ceil_div64(n16, kTile) + H);
+  out->index_slots = b * kTile * tiles;
+  out->kept_tokens = b * kept;
+  const int rw_max = (int)(D / 2 + 4), meta_max = (int)(D + kSlotPad);
+  out->max_tile_bytes = tile_bytes_of(rw_max, meta_max, (int)D, 8);
+  out->max_stage_bytes = std::max<int64_t>(out->max_tile_bytes, tile_bytes_of(rw_max, meta_max, (int)D, 16) + kTile * D * 2);
+  out->status = RDKV_OK;
+  out->n_heads = (int32_t)(b * H);
+  for (int i = 0; i < RDKV_COST_HEADS; ++i) out->head_cost[i] = 0;
   return RDKV_OK;
 }
 

@@ -29,7 +29,7 @@ EXPORTED = (
     "rdkv_decode_attn_noalloc",
     "rdkv_decode_attn_lse", "rdkv_decode_step_lse", "rdkv_merge_attn", "rdkv_zone_c_take", "rdkv_recompress_score",
     "rdkv_allocate_at_levels", "rdkv_decode_multi_workspace_bytes", "rdkv_decode_attn_multi",
-    "rdkv_decode_multi_status",
+    "rdkv_decode_multi_status", "rdkv_zone_bounds",
 )
 
 
@@ -112,6 +112,7 @@ def lib():
             "rdkv_zone_c_take": (ctypes.c_int, [cp, ctypes.c_int32, _P, _P, _P]),
             "rdkv_recompress_score": (ctypes.c_int, [sp, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32,
                                                      ctypes.c_float, _P, _P, _P, _P]),
+            "rdkv_zone_bounds": (ctypes.c_int, [sp, ctypes.c_float, ctypes.c_float, szp]),
             "rdkv_decode_multi_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32]),
             "rdkv_decode_attn_multi": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_multi_status": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P]),
@@ -514,3 +515,58 @@ class MultiDecode:
     def status(self, stream=None):
         return lib().rdkv_decode_multi_status(ctypes.cast(self._arr, _P), len(self.parts), _ptr(self.workspace()),
                                               _stream(stream))
+
+
+# ---------------------------------------------------------------- compression without synchronisation
+def rdkv_zone_bounds(shape, avg_bits_v, avg_bits_k):
+    """Upper bounds of the plan totals (host arithmetic only)."""
+    sz = Sizes()
+    _check(lib().rdkv_zone_bounds(ctypes.byref(shape), ctypes.c_float(avg_bits_v), ctypes.c_float(avg_bits_k),
+                                  ctypes.byref(sz)))
+    return sz
+
+
+class Compressor:
+    """Weights, allocation and pack of one prefill shape as one stream-ordered sequence with every
+    buffer allocated up front (zones sized by rdkv_zone_bounds): run() neither allocates nor waits
+    for the device, so it can be captured in a CUDA graph; finish() reads the exact plan totals
+    (synchronising) so that the decode sizes its work from them."""
+
+    def __init__(self, shape, avg_bits_v, avg_bits_k, cap_c, device, pages=None):
+        self.shape, self.avg = shape, (float(avg_bits_v), float(avg_bits_k))
+        self.bounds = rdkv_zone_bounds(shape, avg_bits_v, avg_bits_k)
+        L = lib()
+        B, Hkv, D, N = shape.batch, shape.h_kv, shape.head_dim, shape.n_tokens
+        Np = N - shape.window
+        f32 = dict(dtype=torch.float32, device=device)
+        self.score_out = dict(w_tok=torch.empty(B, Hkv, N, **f32), w_chan=torch.empty(B, Hkv, D, **f32),
+                              sigma_tok=torch.empty(B, Hkv, N, **f32), g_tok=torch.empty(B, Hkv, max(Np, 0), **f32))
+        self.score_ws = _ws(L.rdkv_score_workspace_bytes(ctypes.byref(shape)), device)
+        self.alloc_out = dict(bits_tok=torch.empty(B, Hkv, max(Np, 0), dtype=torch.uint8, device=device),
+                              sigma_chan=torch.empty(B, Hkv, D, **f32), g_chan=torch.empty(B, Hkv, D, **f32),
+                              bits_chan=torch.empty(B, Hkv, D, dtype=torch.uint8, device=device),
+                              plan=torch.zeros(L.rdkv_plan_bytes(ctypes.byref(shape)), dtype=torch.uint8,
+                                               device=device))
+        self.alloc_ws = _ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), device)
+        self.cache = Cache(shape, self.alloc_out["plan"], self.bounds, cap_c, device, pages=pages)
+
+    def run(self, q, k, v, stream=None):
+        s, L = self.shape, lib()
+        so, ao = self.score_out, self.alloc_out
+        _check(L.rdkv_score(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(so["w_tok"]), _ptr(so["w_chan"]),
+                            _ptr(so["sigma_tok"]), _ptr(so["g_tok"]), _ptr(self.score_ws), self.score_ws.numel(),
+                            _stream(stream)))
+        _check(L.rdkv_allocate(ctypes.byref(s), _ptr(so["g_tok"]), _ptr(so["w_chan"]), _ptr(k),
+                               ctypes.c_float(self.avg[0]), ctypes.c_float(self.avg[1]), _ptr(ao["bits_tok"]),
+                               _ptr(ao["sigma_chan"]), _ptr(ao["g_chan"]), _ptr(ao["bits_chan"]), _ptr(ao["plan"]),
+                               _ptr(self.alloc_ws), self.alloc_ws.numel(), _stream(stream)))
+        self.cache.c.sizes = self.bounds
+        _check(L.rdkv_pack(ctypes.byref(self.cache.c), _ptr(k), _ptr(v), _ptr(ao["bits_tok"]), _ptr(ao["bits_chan"]),
+                           _stream(stream)))
+        return self.cache
+
+    def finish(self, stream=None):
+        sizes = rdkv_plan_sizes(self.alloc_out["plan"], stream)
+        self.cache.sizes = sizes
+        self.cache.c.sizes = sizes
+        return self.cache

@@ -113,7 +113,8 @@ typedef struct rdkv_sizes {
 /* A packed TriZone cache.  All pointers are caller-owned device memory.
  * zone_c_k / zone_c_v are fp16 [batch][h_kv][cap_c][D], or, when
  * zone_c_pages is not NULL, pools of pages [n_pages][RDKV_ZONE_C_PAGE_ROWS][D]
- * (PagedAttention-style block table): row r of head h = b * h_kv + j is row
+ * (the PagedAttention block table of "Matematika KV Cache Compression",
+ * "Solusi 1"): row r of head h = b * h_kv + j is row
  * r % 16 of page zone_c_pages[h * zone_c_page_stride + r / 16].  The table
  * (int32, device) must name a distinct page for every 16-row block a head may
  * use (up to cap_c rows, so zone_c_page_stride >= ceil(cap_c / 16)); the

@@ -253,7 +253,7 @@ rdkv_status rdkv_zone_bounds(const rdkv_shape* shape, float avg_bits_v, float av
  * the window rows [0, W) of zone C from the prefill k, v [B][N][H_kv][D];
  * sets cache->len_c = W.  cache->plan must be the plan bits_tok/bits_chan came
  * with; cap_c >= W; cache->sizes the plan's totals or upper bounds of them
- * (rdkv_zone_bounds).  Bytes are bit-exact with the layout rules:
+ * (rdkv_zone_bounds); k and v 16-byte aligned (else RDKV_ERR_INVALID_ARG).  Bytes are bit-exact with the layout rules:
  * asymmetric min-max codes (aistudio.id "Solusi 3") with fp16 scale/zero. */
 rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v,
                       const uint8_t* bits_tok, const uint8_t* bits_chan, void* stream);

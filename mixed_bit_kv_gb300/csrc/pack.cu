@@ -119,6 +119,16 @@ __global__ void __launch_bounds__(1024) index_kernel(const uint8_t* __restrict__
 // quantiser statistics of every K slot and V group, then the codes (one element per thread step,
 // lanes along slots/channels, warps along tokens), then the words.
 constexpr int kPackThreads = 256;
+// Four consecutive elements as floats (8-byte load for fp16, 16-byte for fp32; the address is a
+// multiple of four elements).
+__device__ __forceinline__ float4 load4(const __half* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
 template <typename T>
 __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __restrict__ k, const T* __restrict__ v,
                                                                   const void* __restrict__ plan,
@@ -138,7 +148,12 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
     if (heads[mid].slot_off <= slot0) lo = mid; else hi = mid - 1;
   }
   const int head = lo;
-  const rdkv_head_plan hp = heads[head];
+  // the head record in shared memory: its arrays are read with run-time indices below
+  __shared__ __align__(16) rdkv_head_plan hps;
+  if (threadIdx.x < sizeof(rdkv_head_plan) / 4)
+    reinterpret_cast<int32_t*>(&hps)[threadIdx.x] = reinterpret_cast<const int32_t*>(heads + head)[threadIdx.x];
+  __syncthreads();
+  const rdkv_head_plan& hp = hps;
   const int b = head / h_kv, j = head % h_kv;
   int ti = (int)((slot0 - hp.slot_off) / kTile), cls = 0;
   int64_t tile_off = hp.a_off;
@@ -168,12 +183,18 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   if (tid < kTile) tok[tid] = index_map[slot0 + tid];
   for (int s = tid; s < KS; s += blockDim.x) sch[s] = slot_ch[s];
   __syncthreads();
-  for (int i = tid; i < kTile * D; i += blockDim.x) {
-    const int r = i / D, c = i % D;
+  // the tile's K and V rows, four elements per load (rows are D contiguous elements, D % 4 == 0)
+  for (int i = tid; i < kTile * D / 4; i += blockDim.x) {
+    const int r = i / (D / 4), c = 4 * (i % (D / 4));
     const int t = tok[r];
-    const int64_t src = (((int64_t)b * N + t) * h_kv + j) * D + c;
-    Kf[i] = t >= 0 ? to_float(k[src]) : 0.0f;
-    Vf[i] = t >= 0 ? to_float(v[src]) : 0.0f;
+    float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
+    if (t >= 0) {
+      const int64_t src = (((int64_t)b * N + t) * h_kv + j) * D + c;
+      kx = load4(k + src);
+      vx = load4(v + src);
+    }
+    reinterpret_cast<float4*>(Kf)[i] = kx;
+    reinterpret_cast<float4*>(Vf)[i] = vx;
   }
   __syncthreads();
 
@@ -383,6 +404,8 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
   const rdkv_shape& s = cache->shape;
   const int N = s.n_tokens, D = s.head_dim, W = s.window, Np = N - W;
   RDKV_REQUIRE(k && v && (Np == 0 || bits_tok) && bits_chan, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  RDKV_REQUIRE(reinterpret_cast<uintptr_t>(k) % 16 == 0 && reinterpret_cast<uintptr_t>(v) % 16 == 0,
+               RDKV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
   (void)bits_chan;  // the channel widths reach the pack through the plan's slot table
   cudaStream_t cs = (cudaStream_t)stream;
   const int n_heads = s.batch * s.h_kv;

@@ -203,3 +203,64 @@ def test_qwen72b_layer_sampled_head():
         assert np.abs(out[:, j * G:(j + 1) * G] - exp).max() <= 2e-3
 
     _decode_steps(w, cache, steps, check)
+
+
+def test_llama3b_layer_recompression_full_size():
+    """Llama-3.2-3B-shaped layer at N = 32768, as the benchmark's re-compression measurement runs it:
+    W + 8 fused decode steps with lse, the rows beyond the window moved into a segment from the last
+    32 queries, then one decode launch over segment and cache.  Checked for a sampled KV head against
+    the oracle: the rows, the widths at the prefill's levels (given the library's gains), the
+    segment's bytes and the merged attention of the head's query heads."""
+    w = synth.WORKLOADS["llama3b"]
+    steps = w.window + 8
+    (q, k, v), shape, sc, al, sizes, cache = _compress(w, w.budgets[0], steps)
+    G, j = w.group, 3
+    qs, ls = [], []
+    for step in range(steps):
+        qn, kn, vn = synth.decode_step(w, step)
+        _, lse = rdkv.rdkv_decode_step_lse(cache, qn.to(DEV), kn.to(DEV), vn.to(DEV))
+        qs.append(qn.to(DEV))
+        ls.append(lse.clone())
+    assert rdkv.rdkv_decode_status(cache) == 0
+    R = 32
+    q_rec, lse_rec = torch.stack(qs[-R:], 1).contiguous(), torch.stack(ls[-R:], 1).contiguous()
+    n_move = cache.len_c - w.window
+    zk_before, zv_before = (t.cpu().numpy().copy() for t in cache.zone_c_rows())
+    seg = rdkv.recompress(cache, al["plan"], sc["w_chan"], q_rec, lse_rec, n_move)
+    sc_seg, al_seg = seg._keep
+    rk = zk_before[0, :, :n_move].transpose(1, 0, 2)  # [n, H_kv, D]
+    rv = zv_before[0, :, :n_move].transpose(1, 0, 2)
+    # weights of head j from the oracle on the same recent queries and lse
+    eg = O.recompress_gains(rk, rv, q_rec[0].cpu().numpy(), lse_rec[0].cpu().numpy(), w.n_tokens / R)
+    assert _rel(sc_seg["w_tok"][0, j].cpu().numpy(), eg["w_tok"][j]).max() <= 1e-3
+    lam = rdkv.plan_levels(al["plan"]).cpu().numpy()
+    g_tok = sc_seg["g_tok"][0].cpu().numpy()
+    bits_tok = al_seg["bits_tok"][0].cpu().numpy()
+    assert np.array_equal(bits_tok.ravel(), O.widths_at(O.breakpoints(g_tok), lam[0]))
+    g_chan = al_seg["g_chan"][0].cpu().numpy()
+    bits_chan = al_seg["bits_chan"][0].cpu().numpy()
+    assert np.array_equal(bits_chan.ravel(), O.widths_at(O.breakpoints(g_chan), lam[1]))
+    # the segment's bytes of head j
+    ref_seg = O.pack(rk[None, :, j:j + 1], rv[None, :, j:j + 1], bits_tok[None, j:j + 1], bits_chan[None, j:j + 1], 0,
+                     cap_c=0)
+    _, heads_seg, _, _ = rdkv.read_plan(al_seg["plan"])
+    hp = heads_seg[j]
+    za = seg.zone_a.cpu().numpy()[int(hp["a_off"]):int(hp["a_off"]) + int(hp["a_bytes"])]
+    assert np.array_equal(za, ref_seg["zone_a"])
+    # one launch over segment and cache, head j's query heads against the oracle
+    bits_pre = al["bits_tok"].cpu().numpy()[:, j:j + 1]
+    chan_pre = al["bits_chan"].cpu().numpy()[:, j:j + 1]
+    ref = O.pack(k[:, :, j:j + 1].float().cpu().numpy(), v[:, :, j:j + 1].float().cpu().numpy(), bits_pre, chan_pre,
+                 w.window, cap_c=w.window)
+    zk, zv = (t.cpu().numpy() for t in cache.zone_c_rows())
+    ref["zone_c_k"][:, :, :w.window] = zk[:, j:j + 1, :w.window]
+    ref["zone_c_v"][:, :, :w.window] = zv[:, j:j + 1, :w.window]
+    ref["len_c"] = w.window
+    qn = synth.decode_step(w, steps)[0]
+    out, lse = rdkv.MultiDecode([seg, cache]).attn(qn.to(DEV))
+    qh = qn.numpy()[:, j * G:(j + 1) * G]
+    o1, l1 = O.decode_lse(ref_seg, qh)
+    o2, l2 = O.decode_lse(ref, qh)
+    exp, exp_lse = O.merge_attention(np.stack([o1, o2]), np.stack([l1, l2]))
+    assert np.abs(out.cpu().numpy()[:, j * G:(j + 1) * G] - exp).max() <= 2e-3
+    assert np.abs(lse.cpu().numpy()[:, j * G:(j + 1) * G] - exp_lse).max() <= 2e-3

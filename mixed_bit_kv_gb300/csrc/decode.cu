@@ -6,14 +6,18 @@
 // pass.
 //
 // Work: one block of 16 warps per SM, dealt to the (sequence, KV head) pairs
-// in proportion to their estimated cost.  A head's work items are its zone-A
-// tiles (32 tokens, in class order) followed by zone-C blocks of 16 rows;
-// split s of n takes items s, s + n, s + 2n, ... and its warps take them in
-// order of need.  Every warp streams its items through its own ring of shared
-// memory, filled by bulk asynchronous copies that complete on per-slot
-// mbarriers (all waits are bounded and report RDKV_ERR_TIMEOUT).  The last
-// block of a head to finish (an atomic ticket) merges the splits' partial
-// softmax states into the output.
+// in proportion to their estimated cost (on the host when the plan's costs are
+// there, else by the kernel).  A head's work items are its zone-A tiles (32
+// tokens, in class order) followed by zone-C blocks of 16 rows; split s of n
+// takes items s, s + n, s + 2n, ... and its warps take them in order of need.
+// Every warp streams its items through its own ring of shared memory, filled
+// by bulk asynchronous copies that complete on per-slot mbarriers (all waits
+// are bounded and report RDKV_ERR_TIMEOUT).  The last block of a head to
+// finish (an atomic ticket) merges the splits' partial softmax states into
+// the output (and, when asked, the log-sum-exp).  One launch may attend
+// several caches sharing the query (segments moved out of zone C and the live
+// cache): each block reads one cache, the blocks of a head over all caches
+// share its merge.  Zone C may be paged (16-row pages through a table).
 //
 // Products: mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens on M:
 //   S^T[16 tok x 8 heads]  += K^[16 tok x 16 slots] * Q^T[16 slots x 8 heads]
@@ -21,9 +25,9 @@
 // A 32-bit A-fragment register holds two consecutive elements along the
 // contraction axis (two K slots of one token; two tokens of one V channel);
 // the word rule of the layout puts both codes of such a pair in the two
-// half-words of one 32-bit word, so one shift and one mask place them, an
-// OR with the fp16 pattern of 1024 and a subtraction give the exact codes,
-// and one half2 FMA applies scale and zero.  The softmax runs in fp32 on the
+// half-words of one 32-bit word, so one shift and one mask (one byte permute
+// for 8-bit codes) place them as fp16 subnormals, code * 2^-24 exactly; the
+// scales enter through the other operand.  The softmax runs in fp32 on the
 // S^T accumulators (base-2 exponent); P^T is moved into B-fragment order by
 // movmatrix.  The G query heads of a group share every loaded tile.
 #include "common.cuh"

@@ -210,3 +210,25 @@ def test_recompress_helper_and_a_second_segment():
     out, lse = rdkv.MultiDecode(segs + [cache]).attn(qn.to(DEV))  # three caches, one launch
     assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3
     assert np.abs(lse.cpu().numpy() - exp_lse).max() <= 2e-3
+
+
+def test_recompress_edges_all_rows_and_an_empty_segment():
+    """Edges: every zone-C row moved (none stay), and a segment that keeps no token (a prefill with a
+    zero budget has water levels that drop every unit); the one-launch decode over the empty
+    segment and the cache still matches the oracle."""
+    w = CASES["small_f16"].scaled(window=8)
+    steps = 8
+    (q, k, v), sc, al, cache, ref = _compress(w, 0.0, steps)
+    q_rec, lse_rec = _run_steps(w, cache, ref, steps)
+    n_move = cache.len_c  # all 16 rows: none stay
+    k_seg, v_seg = rdkv.rdkv_zone_c_take(cache, n_move)
+    rk, rv = O.take_zone_c(ref, n_move)
+    assert cache.len_c == 0 and int(cache.len_dev.item()) == 0
+    assert np.array_equal(k_seg.float().cpu().numpy(), rk.astype(np.float32))
+    seg = rdkv.recompress_from_rows(cache, k_seg, v_seg, al["plan"], sc["w_chan"], q_rec, lse_rec)
+    assert seg.c.sizes.kept_tokens == 0  # the prefill kept nothing: its levels keep nothing
+    qn = synth.decode_step(w, steps)[0]
+    out, lse = rdkv.MultiDecode([seg, cache]).attn(qn.to(DEV))
+    exp, exp_lse = O.decode_lse(ref, qn.numpy())  # segment empty, cache: zones A/B empty, zone C empty
+    assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3
+    assert np.all(np.isneginf(exp_lse)) == bool(np.all(np.isneginf(lse.cpu().numpy())))

@@ -213,12 +213,12 @@ def test_recompress_helper_and_a_second_segment():
 
 
 def test_recompress_edges_all_rows_and_an_empty_segment():
-    """Edges: every zone-C row moved (none stay), and a segment that keeps no token (a prefill with a
-    zero budget has water levels that drop every unit); the one-launch decode over the empty
-    segment and the cache still matches the oracle."""
+    """Edges: every zone-C row moved (none stay); a segment that keeps no token (levels +inf); the
+    one-launch decode over an empty segment, the moved rows' segment and the cache matches the
+    oracle."""
     w = CASES["small_f16"].scaled(window=8)
     steps = 8
-    (q, k, v), sc, al, cache, ref = _compress(w, 0.0, steps)
+    (q, k, v), sc, al, cache, ref = _compress(w, w.budgets[0], steps)
     q_rec, lse_rec = _run_steps(w, cache, ref, steps)
     n_move = cache.len_c  # all 16 rows: none stay
     k_seg, v_seg = rdkv.rdkv_zone_c_take(cache, n_move)
@@ -226,9 +226,19 @@ def test_recompress_edges_all_rows_and_an_empty_segment():
     assert cache.len_c == 0 and int(cache.len_dev.item()) == 0
     assert np.array_equal(k_seg.float().cpu().numpy(), rk.astype(np.float32))
     seg = rdkv.recompress_from_rows(cache, k_seg, v_seg, al["plan"], sc["w_chan"], q_rec, lse_rec)
-    assert seg.c.sizes.kept_tokens == 0  # the prefill kept nothing: its levels keep nothing
+    al_seg = seg._keep[1]
+    seg_ref = O.pack(rk, rv, al_seg["bits_tok"].cpu().numpy(), al_seg["bits_chan"].cpu().numpy(), 0, cap_c=0)
+    # a segment at infinite levels keeps nothing
+    s_seg = rdkv.Shape(w.batch, n_move, w.h_q, w.h_kv, w.head_dim, 0, cache.shape.dtype)
+    inf_levels = torch.full((2 * w.batch,), float("inf"), device=DEV)
+    gs = rdkv.rdkv_recompress_score(s_seg, k_seg, v_seg, q_rec, lse_rec)
+    al_empty = rdkv.rdkv_allocate_at_levels(s_seg, inf_levels, gs["g_tok"], sc["w_chan"], k_seg)
+    empty = rdkv.rdkv_pack(s_seg, al_empty["plan"], k_seg, v_seg, al_empty["bits_tok"], al_empty["bits_chan"], 0)
+    assert empty.sizes.kept_tokens == 0 and int(al_empty["bits_tok"].sum().item()) == 0
     qn = synth.decode_step(w, steps)[0]
-    out, lse = rdkv.MultiDecode([seg, cache]).attn(qn.to(DEV))
-    exp, exp_lse = O.decode_lse(ref, qn.numpy())  # segment empty, cache: zones A/B empty, zone C empty
+    out, lse = rdkv.MultiDecode([empty, seg, cache]).attn(qn.to(DEV))
+    o1, l1 = O.decode_lse(seg_ref, qn.numpy())
+    o2, l2 = O.decode_lse(ref, qn.numpy())  # zones A and B of the prefill; zone C now empty
+    exp, exp_lse = O.merge_attention(np.stack([o1, o2]), np.stack([l1, l2]))
     assert np.abs(out.cpu().numpy() - exp).max() <= 2e-3
-    assert np.all(np.isneginf(exp_lse)) == bool(np.all(np.isneginf(lse.cpu().numpy())))
+    assert np.abs(lse.cpu().numpy() - exp_lse).max() <= 2e-3

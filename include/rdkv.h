@@ -307,6 +307,20 @@ rdkv_status rdkv_decode_step(rdkv_cache* cache, const void* q, const void* k_new
  * step found zone C full and did not store its token. */
 rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* ws, void* stream);
 
+/* Failure-detection self-test of the decode (no counterpart in the paper).
+ * Runs the rdkv_decode_attn kernel on `cache`, `q`, `out` and `ws` (same
+ * layouts and workspace contract) with every stage's barrier armed for 16
+ * bytes that no copy delivers, and no copy issued: each warp's bounded wait
+ * runs out after `wait_cycles` SM clock cycles (clamped to [1e5, 4e9]; 2e6
+ * is about 1 ms), the kernel records RDKV_ERR_TIMEOUT in the status word and
+ * returns, as it would if a tile copy never completed.  Nothing faults or
+ * hangs and the context stays usable; `out` holds no attention result.
+ * rdkv_decode_status then returns RDKV_ERR_TIMEOUT and clears the word.
+ * Returns RDKV_ERR_INVALID_ARG for wait_cycles <= 0, else as rdkv_decode_attn
+ * for the launch itself.  Asynchronous on `stream`. */
+rdkv_status rdkv_decode_timeout_selftest(const rdkv_cache* cache, const void* q, float* out, void* ws,
+                                         size_t ws_bytes, int64_t wait_cycles, void* stream);
+
 /* ---------------------------------------------------------------- decode without a workspace
  * No counterpart in the paper: a deployment variant of rdkv_decode_attn.
  * Some callers cannot allocate device memory themselves: a plugin hosted by

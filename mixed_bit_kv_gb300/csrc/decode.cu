@@ -36,13 +36,14 @@ namespace rdkv {
 
 constexpr int kDecWarps = 16;  // one block per SM
 constexpr int kMaxInflight = 4;
-constexpr int kPrologueItems = 2;
+constexpr int kPrologueItems = 2;     // copies a warp issues before the wait for the previous kernel
 constexpr int kMaxDealtBlocks = 256;  // grids up to this size may be dealt to heads on the host
 constexpr uint8_t kNoHead = 0xff;
-constexpr int kMaxParts = 8;          // caches one launch may attend  // copies a warp issues before the wait for the previous kernel
+constexpr int kMaxParts = 8;          // caches one launch may attend
 constexpr int kCRows = 16;        // zone-C rows per work item
 constexpr int kMaxKB = 16;        // k-blocks of a K row (D = 128: at most 13)
-constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at GB300 clocks
+constexpr long long kWaitCycles = 4000000000ll;  // limit of every wait on a tile copy: ~2 s at GB300 clocks
+constexpr long long kMinWaitCycles = 100000;     // shortest limit the timeout self-test may ask for
 
 // One k-block of a head's K rows (16 slots inside one width segment).  The same for every lane:
 // each lane adds its own constant offsets.
@@ -103,6 +104,8 @@ struct DecodeParams {
   const int16_t* slots;         // the plan's slot tables, slot_stride entries per head
   int dtype, h_q, h_kv, cap_c, ring_bytes, ring_warps, ctas, n_heads, slot_stride;
   int dealt;                    // 1: blocks dealt to heads on the host (below); 0: by the kernel
+  long long wait_cycles;        // limit of each wait on a stage's barrier (clock64 cycles)
+  int arm_only;                 // timeout self-test: stages are armed for bytes that no copy delivers
   uint8_t block_head[kMaxDealtBlocks];       // head of each block, kNoHead for a block without work
   int16_t head_first[RDKV_COST_HEADS + 1];   // first block of each head; [n_heads] = end
   // host dealing over several caches: each block reads one cache (block_part) and takes items
@@ -130,11 +133,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait; false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait; false when the limit (clock64 cycles) ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }
@@ -810,7 +813,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       witem[slot] = ((cls + 1) << 24) | (cls >= 0 ? it - (int)cstart(cls) : it - zc_start);
       unsigned char* dst = wring + phys;
       uint64_t* bar = &wbar[slot];
-      if (cls >= 0) {
+      if (P.arm_only) {
+        // timeout self-test: the stage waits for 16 bytes and no copy is issued, so its wait runs out
+        mbar_arrive_expect_tx(bar, 16u);
+      } else if (cls >= 0) {
         const int ti = it - (int)cstart(cls);
         const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
         mbar_arrive_expect_tx(bar, a_bytes + zb);
@@ -919,7 +925,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     __syncwarp();
     if (__shfl_sync(0xffffffffu, issued, 0) == done) break;  // nothing in flight and nothing left
     const int slot = done % kMaxInflight;
-    const bool arrived = mbar_wait(&wbar[slot], (uint32_t)(done / kMaxInflight) & 1u);
+    const bool arrived = mbar_wait(&wbar[slot], (uint32_t)(done / kMaxInflight) & 1u, P.wait_cycles);
     if (__any_sync(0xffffffffu, !arrived)) {
       ok = false;
       break;
@@ -1016,7 +1022,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       atomicExch(P.error, (int)RDKV_ERR_TIMEOUT);
       // wait (bounded) for this warp's copies still in flight before the ring is reused
       for (int k = done; k < issued; ++k)
-        if (!mbar_wait(&wbar[k % kMaxInflight], (uint32_t)(k / kMaxInflight) & 1u)) break;
+        if (!mbar_wait(&wbar[k % kMaxInflight], (uint32_t)(k / kMaxInflight) & 1u, P.wait_cycles)) break;
     }
     __syncwarp();
   }
@@ -1248,6 +1254,8 @@ static DecodeParams decode_params(const rdkv_cache* const* parts, int n, const D
   P.ring_bytes = geo.ring_bytes;
   P.ring_warps = geo.ring_warps;
   P.ctas = geo.ctas;
+  P.wait_cycles = kWaitCycles;
+  P.arm_only = 0;
   for (int p = 0; p < kMaxParts; ++p) {
     const rdkv_cache* c = parts[p < n ? p : 0];
     DecodePart& d = P.parts[p];
@@ -1356,8 +1364,10 @@ extern "C" size_t rdkv_decode_workspace_bytes(const rdkv_cache* cache) {
   return decode_ws_bytes(decode_geom(cache), cache->shape.batch * cache->shape.h_kv);
 }
 
+// selftest_wait > 0: the timeout self-test (stages armed for bytes that no copy delivers, each wait
+// limited to that many cycles)
 static rdkv_status decode_attn_impl(const rdkv_cache* cache, const void* q, float* out, float* lse, void* ws,
-                                    size_t ws_bytes, void* stream) {
+                                    size_t ws_bytes, void* stream, long long selftest_wait = 0) {
   rdkv_status st = check_cache_public(cache);
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(q && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
@@ -1369,8 +1379,12 @@ static rdkv_status decode_attn_impl(const rdkv_cache* cache, const void* q, floa
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
   // the tickets are zero here: the workspace starts zero-filled and every call leaves them at zero
-  return launch_decode(decode_params(cache, geo, q, out, ws, nullptr, nullptr, lse), geo, s, (cudaStream_t)stream,
-                       true);
+  DecodeParams P = decode_params(cache, geo, q, out, ws, nullptr, nullptr, lse);
+  if (selftest_wait > 0) {
+    P.arm_only = 1;
+    P.wait_cycles = std::min(kWaitCycles, std::max(kMinWaitCycles, selftest_wait));
+  }
+  return launch_decode(P, geo, s, (cudaStream_t)stream, selftest_wait == 0);
 }
 
 static rdkv_status decode_step_impl(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new, float* out,
@@ -1400,6 +1414,12 @@ extern "C" rdkv_status rdkv_decode_attn_lse(const rdkv_cache* cache, const void*
                                             size_t ws_bytes, void* stream) {
   RDKV_REQUIRE(lse, RDKV_ERR_INVALID_ARG, "NULL lse");
   return decode_attn_impl(cache, q, out, lse, ws, ws_bytes, stream);
+}
+
+extern "C" rdkv_status rdkv_decode_timeout_selftest(const rdkv_cache* cache, const void* q, float* out, void* ws,
+                                                    size_t ws_bytes, int64_t wait_cycles, void* stream) {
+  RDKV_REQUIRE(wait_cycles > 0, RDKV_ERR_INVALID_ARG, "wait_cycles %lld must be positive", (long long)wait_cycles);
+  return decode_attn_impl(cache, q, out, nullptr, ws, ws_bytes, stream, wait_cycles);
 }
 
 extern "C" rdkv_status rdkv_decode_step(rdkv_cache* cache, const void* q, const void* k_new, const void* v_new,

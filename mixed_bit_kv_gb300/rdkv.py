@@ -29,7 +29,7 @@ EXPORTED = (
     "rdkv_decode_attn_noalloc",
     "rdkv_decode_attn_lse", "rdkv_decode_step_lse", "rdkv_merge_attn", "rdkv_zone_c_take", "rdkv_recompress_score",
     "rdkv_allocate_at_levels", "rdkv_decode_multi_workspace_bytes", "rdkv_decode_attn_multi",
-    "rdkv_decode_multi_status", "rdkv_zone_bounds",
+    "rdkv_decode_multi_status", "rdkv_zone_bounds", "rdkv_decode_timeout_selftest",
 )
 
 
@@ -105,6 +105,7 @@ def lib():
             "rdkv_decode_attn": (ctypes.c_int, [cp, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_step": (ctypes.c_int, [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_status": (ctypes.c_int, [cp, _P, _P]),
+            "rdkv_decode_timeout_selftest": (ctypes.c_int, [cp, _P, _P, _P, ctypes.c_size_t, ctypes.c_int64, _P]),
             "rdkv_decode_attn_noalloc": (ctypes.c_int, [cp, _P, _P, _P]),
             "rdkv_decode_attn_lse": (ctypes.c_int, [cp, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_step_lse": (ctypes.c_int, [cp, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -349,6 +350,18 @@ def rdkv_decode_attn_noalloc(cache, q, out, stream=None):
 def rdkv_decode_status(cache, stream=None):
     ws = cache.decode_workspace()
     return lib().rdkv_decode_status(ctypes.byref(cache.c), _ptr(ws), _stream(stream))
+
+
+def rdkv_decode_timeout_selftest(cache, q, wait_cycles=2_000_000, stream=None):
+    """The decode kernel with every stage armed for bytes no copy delivers: each bounded wait runs out
+    after wait_cycles SM cycles and the status word reports RDKV_ERR_TIMEOUT (read it with
+    rdkv_decode_status).  Returns the (meaningless) output tensor."""
+    B, Hq, D = q.shape
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device=q.device)
+    ws = cache.decode_workspace()
+    _check(lib().rdkv_decode_timeout_selftest(ctypes.byref(cache.c), _ptr(q), _ptr(out), _ptr(ws), ws.numel(),
+                                              int(wait_cycles), _stream(stream)))
+    return out
 
 
 # ---------------------------------------------------------------- plan inspection (tests)

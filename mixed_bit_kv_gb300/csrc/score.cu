@@ -100,29 +100,42 @@ __global__ void colsq_kernel(const void* __restrict__ x, int dtype, int N, int c
   part[((int64_t)b * gridDim.y + chunk) * cols + col] = acc;
 }
 
-__global__ void channel_weight_kernel(const float* __restrict__ qpart, const float* __restrict__ kpart, int nchunk,
-                                      int h_q, int h_kv, int D, float* __restrict__ w_chan) {
-  // thread (r, c) sums the chunks r, r + R, ... of channel c; the R sums combine in a fixed order
-  __shared__ double sq[1024], sk[1024];
+// w_c = sqrt(sum q^2) sqrt(sum k^2) / sqrt(D) per (b, KV head j, channel c) from partial sums of squares:
+// qpart[b][nq][H_q][D] (the group's G query heads are added), kpart[b][nk][H_kv][D].  Block: 32 channels
+// x 32 partial rows; thread (r, c) adds the partials r, r + 32, ... in fp64, the 32 sums combine in a
+// fixed order (deterministic).
+__global__ void __launch_bounds__(1024) channel_weight_kernel(const float* __restrict__ qpart, int nq,
+                                                              const float* __restrict__ kpart, int nk, int h_q,
+                                                              int h_kv, int D, float* __restrict__ w_chan) {
+  __shared__ double sq[32][33], sk[32][33];
   const int head = blockIdx.x;  // b * h_kv + j
   const int b = head / h_kv, j = head % h_kv;
-  const int c = threadIdx.x % D, r = threadIdx.x / D, R = blockDim.x / D;
+  const int cc = threadIdx.x & 31, r = threadIdx.x >> 5;
+  const int c = blockIdx.y * 32 + cc;
   const int G = h_q / h_kv;
   double qs = 0.0, ks = 0.0;
-  for (int i = r; i < nchunk; i += R) {
-    const float* qp = qpart + ((int64_t)b * nchunk + i) * h_q * D;
+  for (int i = r; i < nq; i += 32) {
+    const float* qp = qpart + ((int64_t)b * nq + i) * h_q * D;
     for (int h = j * G; h < (j + 1) * G; ++h) qs += (double)qp[h * D + c];
-    ks += (double)kpart[((int64_t)b * nchunk + i) * h_kv * D + j * D + c];
   }
-  sq[threadIdx.x] = qs;
-  sk[threadIdx.x] = ks;
+  for (int i = r; i < nk; i += 32) ks += (double)kpart[((int64_t)b * nk + i) * h_kv * D + j * D + c];
+  sq[r][cc] = qs;
+  sk[r][cc] = ks;
   __syncthreads();
   if (r != 0) return;
-  for (int rr = 1; rr < R; ++rr) {
-    qs += sq[rr * D + c];
-    ks += sk[rr * D + c];
+  for (int rr = 1; rr < 32; ++rr) {
+    qs += sq[rr][cc];
+    ks += sk[rr][cc];
   }
   w_chan[head * D + c] = (float)(sqrt(qs) * sqrt(ks) / sqrt((double)D));
+}
+
+rdkv_status launch_channel_weights(const rdkv_shape* s, const float* qpart, int nq, const float* kpart, int nk,
+                                   float* w_chan, cudaStream_t st) {
+  channel_weight_kernel<<<dim3(s->batch * s->h_kv, s->head_dim / 32), 1024, 0, st>>>(qpart, nq, kpart, nk, s->h_q,
+                                                                                      s->h_kv, s->head_dim, w_chan);
+  RDKV_CHECK_LAUNCH("channel weights");
+  return RDKV_OK;
 }
 
 // ---------------------------------------------------------------- CUDA-core pass 1: row log-sum-exp (base 2)
@@ -242,14 +255,20 @@ __global__ void __launch_bounds__(128) colsum_simt_kernel(const void* __restrict
 
 // The fp16 tensor-core passes live in score_tc.cu.
 rdkv_status launch_score_tc(const rdkv_shape* s, const void* q, const void* k, const float* sigma, float* lse2,
-                            float* w_tok, float* g_tok, cudaStream_t st);
+                            float* w_tok, float* g_tok, float* qsq, float* ksq, float* w_chan, cudaStream_t st);
 int score_tc_lse_stride(int n_tokens);
+int score_tc_q_chunks(int n_tokens);
+int score_tc_k_chunks(int n_tokens);
 
+// Workspace: row log-sum-exps, then the partial sums of squares of the channel weights (chunks of
+// kColChunk rows on the CUDA-core path; 128-row blocks for q and 256-key tiles for k on the
+// tensor-core path, which takes them in scorer pass 1).
 static size_t score_ws_parts(const rdkv_shape* s, size_t* lse, size_t* qp, size_t* kp) {
   const int nchunk = ceil_div(s->n_tokens, kColChunk);
+  const int nq = std::max(nchunk, score_tc_q_chunks(s->n_tokens)), nk = std::max(nchunk, score_tc_k_chunks(s->n_tokens));
   *lse = align_up((int64_t)s->batch * s->h_q * score_tc_lse_stride(s->n_tokens) * 4, 256);
-  *qp = align_up((int64_t)s->batch * nchunk * s->h_q * s->head_dim * 4, 256);
-  *kp = align_up((int64_t)s->batch * nchunk * s->h_kv * s->head_dim * 4, 256);
+  *qp = align_up((int64_t)s->batch * nq * s->h_q * s->head_dim * 4, 256);
+  *kp = align_up((int64_t)s->batch * nk * s->h_kv * s->head_dim * 4, 256);
   return *lse + *qp + *kp;
 }
 
@@ -295,18 +314,18 @@ extern "C" rdkv_status rdkv_score(const rdkv_shape* s, const void* q, const void
     }
   }
   RDKV_CHECK_LAUNCH("value spread");
-  // channel weights
+  // fp16: token weights on the tensor cores, whose first pass also takes the channel weights' sums of
+  // squares from the tiles it loads; the channel weights follow it
+  if (s->dtype == RDKV_F16) return launch_score_tc(s, q, k, sigma_tok, lse2, w_tok, g_tok, qpart, kpart, w_chan, cs);
+  // fp32: channel weights from their own column passes, then the token weights on the CUDA cores
   const int nchunk = ceil_div(N, kColChunk);
   colsq_kernel<<<dim3(ceil_div(s->h_q * D, 256), nchunk, s->batch), 256, 0, cs>>>(q, s->dtype, N, s->h_q * D, qpart);
   RDKV_CHECK_LAUNCH("query column norms");
   colsq_kernel<<<dim3(ceil_div(s->h_kv * D, 256), nchunk, s->batch), 256, 0, cs>>>(k, s->dtype, N, s->h_kv * D,
                                                                                    kpart);
   RDKV_CHECK_LAUNCH("key column norms");
-  channel_weight_kernel<<<s->batch * s->h_kv, std::min(1024, 8 * D), 0, cs>>>(qpart, kpart, nchunk, s->h_q, s->h_kv,
-                                                                                D, w_chan);
-  RDKV_CHECK_LAUNCH("channel weights");
-  // token weights
-  if (s->dtype == RDKV_F16) return launch_score_tc(s, q, k, sigma_tok, lse2, w_tok, g_tok, cs);
+  st = launch_channel_weights(s, qpart, nchunk, kpart, nchunk, w_chan, cs);
+  if (st != RDKV_OK) return st;
   const size_t smem = (size_t)(kSTile * (D + 1) + D * (kSTile + 4) + kSTile) * 4;
   lse_simt_kernel<<<dim3(ceil_div(N, kSTile), s->h_q, s->batch), 128, smem, cs>>>(q, k, s->dtype, N, s->h_q, s->h_kv,
                                                                                     D, lse2);

@@ -11,6 +11,11 @@
 //   pass 2  A = 128 keys of KV head j, B = query tiles tau >= t of the G heads
 //           of the group.  The epilogue adds 2^(s*c - lse2[tau]) per key:
 //           the column sums of the attention, i.e. w_t; then g_t = w_t * sigma_t.
+// Pass 1 also takes the channel weights' sums of squares (section 2.1:
+// w_c = ||Q_:,c|| ||K_:,c|| / sqrt(D)) from the tiles it already holds: once the
+// producer warp has issued its last load, it sums q^2 per channel over the
+// block's 128 query rows, and in one block per (KV head, 256-key tile) k^2 over
+// that tile (the block's last), each into its own partial (no atomics).
 // Roles (576 threads): warp 0 loads tiles with TMA into a 2-stage ring of 64 KB
 // stages; warp 1 issues tcgen05.mma (one thread) into two 256-column TMEM
 // accumulators; warps 2..17 read the accumulators back (four warps per TMEM
@@ -23,6 +28,9 @@
 #include "common.cuh"
 
 namespace rdkv {
+
+rdkv_status launch_channel_weights(const rdkv_shape* s, const float* qpart, int nq, const float* kpart, int nk,
+                                   float* w_chan, cudaStream_t st);
 
 namespace tc {
 
@@ -131,7 +139,39 @@ struct Params {
   const float* sigma;  // [B][H_kv][N]
   float* w_tok;        // [B][H_kv][N]
   float* g_tok;        // [B][H_kv][Np]
+  float* qsq;          // pass 1: [B][n_blk][H_q][D] sums of q^2 over each 128-row block, or NULL
+  float* ksq;          // pass 1: [B][n_kt][H_kv][D] sums of k^2 over each 256-key tile
+  int n_kt;            // 256-key tiles: ceil(N / kCols)
 };
+
+// Sums of x^2 per channel over `rows` rows of a K-major fp16 tile written by TMA with the 128-byte
+// swizzle (64-column halves `rows` x 128 bytes apart; in a half, row r's 16-byte chunk c sits at
+// chunk c ^ (r & 7)).  Lane l takes channels D/32 * l ..; rows in order.
+template <int D>
+__device__ __forceinline__ void channel_squares(const uint8_t* tile, int rows, int lane, float (&acc)[D / 32]) {
+  constexpr int CPL = D / 32;
+  const int c0 = lane * CPL;
+  const uint8_t* half = tile + (c0 / 64) * rows * 128;
+  const int chunk = (c0 % 64) / 8, within = (c0 % 8) * 2;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
+  for (int r = 0; r < rows; ++r) {
+    const uint8_t* p = half + r * 128 + ((chunk ^ (r & 7)) << 4) + within;
+    if (CPL == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(p);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+      const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+      acc[0] = fmaf(a.x, a.x, acc[0]);
+      acc[1 % CPL] = fmaf(a.y, a.y, acc[1 % CPL]);
+      acc[2 % CPL] = fmaf(c.x, c.x, acc[2 % CPL]);
+      acc[3 % CPL] = fmaf(c.y, c.y, acc[3 % CPL]);
+    } else {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
+      acc[0] = fmaf(a.x, a.x, acc[0]);
+      acc[1 % CPL] = fmaf(a.y, a.y, acc[1 % CPL]);
+    }
+  }
+}
 
 template <int D, int PASS>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -193,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
+    int last_ok = 0;  // lane 0: every load up to the last one was issued
     if (lane == 0) {
       const int a_head = blockIdx.y;
       mbar_expect(&bar_a, kTileBytes);
@@ -211,6 +252,27 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           mbar_expect(&lfull[t], kCols * 4);
           bulk_g2s(lse_s + t * kCols, P.lse2 + ((int64_t)b * P.h_q + head) * P.lse_stride + t0, kCols * 4, &lfull[t]);
         }
+        if (i == n_tiles - 1) last_ok = 1;
+      }
+    }
+    if (PASS == 1 && P.qsq != nullptr) {
+      // channel sums of squares from the tiles this block holds (the A tile stays until the end,
+      // and the last B tile is never overwritten): the whole warp, once every load is issued
+      last_ok = __shfl_sync(0xffffffffu, last_ok, 0);
+      float acc[D / 32];
+      const bool a_ok = last_ok && mbar_wait(&bar_a, 0);
+      if (a_ok) channel_squares<D>(As, kRows, lane, acc);
+      float* qo = P.qsq + (((int64_t)b * P.n_blk + blk) * P.h_q + blockIdx.y) * D + lane * (D / 32);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) qo[i] = a_ok ? acc[i] : __int_as_float(0x7fc00000);
+      // keys: the block whose rows start the 256-key tile (its last tile), first query head of the group
+      if (blockIdx.y % P.G == 0 && (blk & 1) == 0) {
+        const int i = n_tiles - 1, s = i % kStages;
+        const bool b_ok = last_ok && mbar_wait(&full[s], (i / kStages) & 1);
+        if (b_ok) channel_squares<D>(Bs + s * kBTileBytes, kCols, lane, acc);
+        float* ko = P.ksq + (((int64_t)b * P.n_kt + blk / 2) * P.h_kv + blockIdx.y / P.G) * D + lane * (D / 32);
+#pragma unroll
+        for (int i2 = 0; i2 < D / 32; ++i2) ko[i2] = b_ok ? acc[i2] : __int_as_float(0x7fc00000);
       }
     }
   } else if (warp == 1) {
@@ -415,7 +477,8 @@ static size_t smem_bytes() {
 
 template <int D>
 static rdkv_status launch(const rdkv_shape* s, const void* q, const void* k, const float* sigma, float* lse2,
-                          int lse_stride, float* w_tok, float* g_tok, cudaStream_t st) {
+                          int lse_stride, float* w_tok, float* g_tok, float* qsq, float* ksq, float* w_chan,
+                          cudaStream_t st) {
   CUtensorMap mqa, mqb, mka, mkb;  // 128-row boxes (stationary A) and 256-row boxes (streamed B)
   rdkv_status e = make_map(&mqa, q, s->batch, s->n_tokens, s->h_q, D, kRows);
   if (e == RDKV_OK) e = make_map(&mqb, q, s->batch, s->n_tokens, s->h_q, D, kCols);
@@ -435,6 +498,9 @@ static rdkv_status launch(const rdkv_shape* s, const void* q, const void* k, con
   P.sigma = sigma;
   P.w_tok = w_tok;
   P.g_tok = g_tok;
+  P.qsq = qsq;
+  P.ksq = ksq;
+  P.n_kt = ceil_div(s->n_tokens, kCols);
   const size_t smem = smem_bytes<D>();
   static bool attr_set[2] = {false, false};
   if (!attr_set[0]) {
@@ -446,6 +512,8 @@ static rdkv_status launch(const rdkv_shape* s, const void* q, const void* k, con
   }
   score_kernel<D, 1><<<dim3(P.n_blk, s->h_q, s->batch), kThreads, smem, st>>>(mqa, mkb, P);
   RDKV_CHECK_LAUNCH("row log-sum-exp (tensor cores)");
+  const rdkv_status cw = launch_channel_weights(s, qsq, P.n_blk, ksq, P.n_kt, w_chan, st);
+  if (cw != RDKV_OK) return cw;
   score_kernel<D, 2><<<dim3(P.n_blk, s->h_kv, s->batch), kThreads, smem, st>>>(mka, mqb, P);
   RDKV_CHECK_LAUNCH("attention column sums (tensor cores)");
   return RDKV_OK;
@@ -458,12 +526,16 @@ static rdkv_status launch(const rdkv_shape* s, const void* q, const void* k, con
 int score_tc_lse_stride(int n_tokens) { return ceil_div(n_tokens, tc::kRows) * tc::kRows + (tc::kCols - tc::kRows); }
 
 rdkv_status launch_score_tc(const rdkv_shape* s, const void* q, const void* k, const float* sigma, float* lse2,
-                            float* w_tok, float* g_tok, cudaStream_t st) {
+                            float* w_tok, float* g_tok, float* qsq, float* ksq, float* w_chan, cudaStream_t st) {
   RDKV_REQUIRE(((uintptr_t)q % 16) == 0 && ((uintptr_t)k % 16) == 0, RDKV_ERR_INVALID_ARG,
                "q and k must be 16-byte aligned for the tensor-core scorer");
   const int ls = score_tc_lse_stride(s->n_tokens);
-  if (s->head_dim == 128) return tc::launch<128>(s, q, k, sigma, lse2, ls, w_tok, g_tok, st);
-  return tc::launch<64>(s, q, k, sigma, lse2, ls, w_tok, g_tok, st);
+  if (s->head_dim == 128) return tc::launch<128>(s, q, k, sigma, lse2, ls, w_tok, g_tok, qsq, ksq, w_chan, st);
+  return tc::launch<64>(s, q, k, sigma, lse2, ls, w_tok, g_tok, qsq, ksq, w_chan, st);
 }
+
+// Partial sizes of the tensor-core path's channel sums: q over 128-row blocks, k over 256-key tiles.
+int score_tc_q_chunks(int n_tokens) { return ceil_div(n_tokens, tc::kRows); }
+int score_tc_k_chunks(int n_tokens) { return ceil_div(n_tokens, tc::kCols); }
 
 }  // namespace rdkv

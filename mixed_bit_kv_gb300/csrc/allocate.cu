@@ -288,25 +288,41 @@ __global__ void plan_heads_kernel(const uint8_t* __restrict__ bits_tok, const ui
   const int head = blockIdx.x;
   __shared__ int nv[4], nk[5];
   __shared__ int seg_base[4];
+  __shared__ uint8_t bcs[256];  // this head's channel widths (D <= 256)
   if (threadIdx.x < 4) nv[threadIdx.x] = 0;
   if (threadIdx.x < 5) nk[threadIdx.x] = 0;
   int16_t* slots = reinterpret_cast<int16_t*>(plan + slots_off) + (int64_t)head * slot_stride;
   for (int i = threadIdx.x; i < slot_stride; i += blockDim.x) slots[i] = -1;
+  const uint8_t* bc = bits_chan + (int64_t)head * D;
+  for (int c = threadIdx.x; c < D; c += blockDim.x) bcs[c] = bc[c];
   __syncthreads();
   int cnt[4] = {0, 0, 0, 0};
-  const uint8_t* bt = bits_tok + (int64_t)head * Np;
-  for (int t = threadIdx.x; t < Np; t += blockDim.x) {
-    const int b = bt[t];
+  auto count = [&](uint32_t b) {
     cnt[0] += b == 2;
     cnt[1] += b == 4;
     cnt[2] += b == 8;
     cnt[3] += b == 16;
+  };
+  const uint8_t* bt = bits_tok + (int64_t)head * Np;
+  // widths of the head's tokens, sixteen per load once the row is 16-byte aligned (independent loads,
+  // all in flight together); the counts do not depend on the order
+  const int lead = min(Np, (int)((16 - ((uintptr_t)bt & 15)) & 15));
+  for (int t = threadIdx.x; t < lead; t += blockDim.x) count(bt[t]);
+  const int n16 = (Np - lead) / 16;
+  const uint4* bt16 = reinterpret_cast<const uint4*>(bt + lead);
+  for (int i = threadIdx.x; i < n16; i += blockDim.x) {
+    const uint4 w = bt16[i];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) count((ws[q] >> (8 * e)) & 255u);
   }
+  for (int t = lead + 16 * n16 + threadIdx.x; t < Np; t += blockDim.x) count(bt[t]);
 #pragma unroll
   for (int i = 0; i < 4; ++i) atomicAdd(&nv[i], cnt[i]);
-  const uint8_t* bc = bits_chan + (int64_t)head * D;
   auto kclass = [](int b) { return b == 16 ? 0 : b == 8 ? 1 : b == 4 ? 2 : b == 2 ? 3 : 4; };
-  for (int c = threadIdx.x; c < D; c += blockDim.x) atomicAdd(&nk[kclass(bc[c])], 1);
+  for (int c = threadIdx.x; c < D; c += blockDim.x) atomicAdd(&nk[kclass(bcs[c])], 1);
   __syncthreads();
   if (threadIdx.x == 0) {
     rdkv_head_plan hp;
@@ -336,10 +352,10 @@ __global__ void plan_heads_kernel(const uint8_t* __restrict__ bits_tok, const ui
   }
   __syncthreads();
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    const int cls = kclass(bc[c]);
+    const int cls = kclass(bcs[c]);
     if (cls == 4) continue;
     int rank = 0;
-    for (int c2 = 0; c2 < c; ++c2) rank += kclass(bc[c2]) == cls;
+    for (int c2 = 0; c2 < c; ++c2) rank += kclass(bcs[c2]) == cls;
     slots[seg_base[cls] + rank] = (int16_t)c;
   }
 }

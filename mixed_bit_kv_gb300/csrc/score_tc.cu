@@ -357,7 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
             m = mn;
           }
         } else {
-          const float4* ls4 = reinterpret_cast<const float4*>(lse_s + t * kCols + colh * kSliceCols + ch * 32);
+          // the staged -lse2 of the chunk's 32 queries, read with explicit shared-memory loads (the
+          // aligned dynamic shared-memory base is computed through an integer, so a plain dereference
+          // would be a generic load)
+          const uint32_t ls_a = su32(lse_s + t * kCols + colh * kSliceCols + ch * 32);
+          auto ls4_at = [&](int e4) {
+            float4 r;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(ls_a + 16 * e4));
+            return r;
+          };
           float a0 = 0.f, a1 = 0.f;
           if (t0 != row0 && t0 + kCols <= P.N) {  // no causal edge and no tail in this tile
             // the staged values are -lse2: 2^(v c - lse2) = 2^(fma(v, c, -lse2)), paired
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
             float2 p0 = make_float2(0.f, 0.f), p1 = p0;
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 L = ls4[e4];
+              const float4 L = ls4_at(e4);
               const float2 x0 = ffma2(make_float2(v[4 * e4 + 0], v[4 * e4 + 1]), cc, make_float2(L.x, L.y));
               const float2 x1 = ffma2(make_float2(v[4 * e4 + 2], v[4 * e4 + 3]), cc, make_float2(L.z, L.w));
               p0 = fadd2(p0, make_float2(ex2(x0.x), ex2(x0.y)));
@@ -377,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           } else {
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 L = ls4[e4];
+              const float4 L = ls4_at(e4);
               const float lv[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
               for (int u = 0; u < 4; ++u) {

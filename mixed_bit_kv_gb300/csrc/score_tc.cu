@@ -42,6 +42,8 @@ constexpr int kEpiWarps = 16;                 // epilogue warps: 4 per TMEM lane
 constexpr int kSlices = kEpiWarps / 4;        // column slices of the accumulator
 constexpr int kSliceCols = kCols / kSlices;   // columns per epilogue warp (multiple of 32)
 constexpr int kThreads = 64 + 32 * kEpiWarps; // producer, MMA, epilogue warps
+constexpr int kBlocksPerSM = 1;
+static_assert(kCols % kRows == 0, "a key tile spans whole row blocks");
 constexpr long long kWait = 4000000000ll;
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -174,7 +176,7 @@ __device__ __forceinline__ void channel_squares(const uint8_t* tile, int rows, i
 }
 
 template <int D, int PASS>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ CUtensorMap tmA,
+__global__ void __launch_bounds__(kThreads, kBlocksPerSM) score_kernel(const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB, Params P) {
   constexpr int kHalves = D / 64;                 // 64-element (128-byte) column halves of a row
   constexpr uint32_t kTileBytes = kRows * D * 2;   // the A block (128 rows)
@@ -265,12 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
       float* qo = P.qsq + (((int64_t)b * P.n_blk + blk) * P.h_q + blockIdx.y) * D + lane * (D / 32);
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) qo[i] = a_ok ? acc[i] : __int_as_float(0x7fc00000);
-      // keys: the block whose rows start the 256-key tile (its last tile), first query head of the group
-      if (blockIdx.y % P.G == 0 && (blk & 1) == 0) {
+      // keys: the block whose rows start the key tile (its last tile), first query head of the group
+      if (blockIdx.y % P.G == 0 && blk % (kCols / kRows) == 0) {
         const int i = n_tiles - 1, s = i % kStages;
         const bool b_ok = last_ok && mbar_wait(&full[s], (i / kStages) & 1);
         if (b_ok) channel_squares<D>(Bs + s * kBTileBytes, kCols, lane, acc);
-        float* ko = P.ksq + (((int64_t)b * P.n_kt + blk / 2) * P.h_kv + blockIdx.y / P.G) * D + lane * (D / 32);
+        float* ko = P.ksq + (((int64_t)b * P.n_kt + blk / (kCols / kRows)) * P.h_kv + blockIdx.y / P.G) * D + lane * (D / 32);
 #pragma unroll
         for (int i2 = 0; i2 < D / 32; ++i2) ko[i2] = b_ok ? acc[i2] : __int_as_float(0x7fc00000);
       }

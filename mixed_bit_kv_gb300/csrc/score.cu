@@ -12,7 +12,8 @@
 // a probability with that row's normaliser and sums the columns.  This file
 // holds the CUDA-core passes (exact fp32 logits, used for fp32 inputs) and
 // the row/column reductions; the fp16 passes run on the tensor cores
-// (score_tc.cu).
+// (score_tc.cu), whose first pass also takes the sums of squares behind w_c
+// from the tiles it loads (the column passes here serve fp32 inputs).
 #include <cmath>
 
 #include "common.cuh"

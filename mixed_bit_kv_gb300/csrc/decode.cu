@@ -141,11 +141,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   }
   return true;
 }
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
+// L2 policy of the staged zone data: evicted first, so that the small data every call re-reads
+// (plan records, slot tables, queries, the split partials) stays in L2 across the layers.  Zone C
+// too: keeping its rows (a few hundred KB per layer) resident measured no better.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_copy_once(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // atomic add of 1 with acquire-release semantics at GPU scope; returns the old value
@@ -820,8 +830,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         const int ti = it - (int)cstart(cls);
         const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
         mbar_arrive_expect_tx(bar, a_bytes + zb);
-        bulk_copy(dst, PP.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar);
-        if (zb) bulk_copy(dst + a_bytes, PP.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar);
+        const uint64_t pol = evict_first_policy();
+        bulk_copy_once(dst, PP.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar, pol);
+        if (zb) bulk_copy_once(dst + a_bytes, PP.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar, pol);
       } else {
         // rows of zone C (the fused step's new row, past them, is written by the consumer)
         const int rows = max(0, min(kCRows, len_c - c_row));
@@ -830,8 +841,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         const int64_t src = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, head, c_row, D);
         mbar_arrive_expect_tx(bar, 2 * bytes);
         if (bytes) {
-          bulk_copy(dst, PP.zone_c_k + src, bytes, bar);
-          bulk_copy(dst + kCRows * D * 2, PP.zone_c_v + src, bytes, bar);
+          const uint64_t pol = evict_first_policy();
+          bulk_copy_once(dst, PP.zone_c_k + src, bytes, bar, pol);
+          bulk_copy_once(dst + kCRows * D * 2, PP.zone_c_v + src, bytes, bar, pol);
         }
       }
       ++issued;

@@ -116,8 +116,11 @@ __global__ void __launch_bounds__(1024) index_kernel(const uint8_t* __restrict__
 
 // ---------------------------------------------------------------- tile pack
 // One block (256 threads) per zone-A tile: stage the tile's K and V rows as floats, then the
-// quantiser statistics of every K slot and V group, then the codes (one element per thread step,
-// lanes along slots/channels, warps along tokens), then the words.
+// quantiser statistics of every K slot and V group, then the K words and the V codes, then the V
+// words.  A K word is built by the lane of its token from the codes of the word's slots (warps
+// along words, lanes along tokens; K rows are padded to D + 1 floats so that the 32 lanes read 32
+// banks, and the 32 lanes store 32 adjacent words of the word-major layout).  V codes go through
+// shared memory as bytes; a V word is assembled from a pair's two code rows.
 constexpr int kPackThreads = 256;
 // Four consecutive elements as floats (8-byte load for fp16, 16-byte for fp32; the address is a
 // multiple of four elements).
@@ -129,12 +132,27 @@ __device__ __forceinline__ float4 load4(const __half* p) {
 }
 __device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-template <typename T>
+// `n` (2, 4 or 8) consecutive code bytes of a V code row, as one little-endian integer.
+__device__ __forceinline__ uint64_t code_bytes(const uint8_t* p, int n) {
+  if (n == 8) return *reinterpret_cast<const uint64_t*>(p);
+  if (n == 4) return *reinterpret_cast<const uint32_t*>(p);
+  return *reinterpret_cast<const uint16_t*>(p);
+}
+
+template <int D>
+__host__ __device__ constexpr size_t pack_smem_bytes_of() {
+  return (size_t)kTile * (D + 1) * 4 + (size_t)kTile * D * 4 + (size_t)kTile * D + (size_t)(D + kSlotPad) * 12 +
+         (size_t)kTile * (D / kVGroup) * 12 + (size_t)(D + kSlotPad) * 2 + 16;
+}
+
+template <typename T, int D>
 __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __restrict__ k, const T* __restrict__ v,
                                                                   const void* __restrict__ plan,
                                                                   const int32_t* __restrict__ index_map,
                                                                   uint8_t* __restrict__ zone_a,
-                                                                  uint16_t* __restrict__ zone_b, int N, int h_kv, int D) {
+                                                                  uint16_t* __restrict__ zone_b, int N, int h_kv) {
+  constexpr int NG = D / kVGroup;  // V groups of a token
+  constexpr int KP = D + 1;        // floats of a staged K row
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const rdkv_plan_header* hdr = plan_header(plan);
   const rdkv_head_plan* heads = plan_heads(plan);
@@ -169,22 +187,25 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   const int n_real = min(kTile, hp.n_v[cls] - ti * kTile);
   const int RW = hp.row_words, KS = hp.k_slots;
   const int16_t* slot_ch = plan_slots(plan) + (int64_t)head * hdr->slot_stride;
-  const int ngrp = D / kVGroup;
+  // width segments of the slots (16, 8, 4, 2 bits) and of the words
+  const int s16 = 2 * hp.k_words[0];          // first 8-bit slot (the raw 16-bit slots come first)
+  const int sb4 = s16 + 4 * hp.k_words[1];    // first 4-bit slot
+  const int sb2 = sb4 + 8 * hp.k_words[2];    // first 2-bit slot
+  const int w8 = hp.k_words[0], w4 = w8 + hp.k_words[1], w2 = w4 + hp.k_words[2];  // first word of each
 
-  float* Kf = reinterpret_cast<float*>(smem_raw);            // [32][D]
-  float* Vf = Kf + kTile * D;                                // [32][D]
-  uint16_t* kc = reinterpret_cast<uint16_t*>(Vf + kTile * D);  // [32][KS]
-  uint8_t* vc = reinterpret_cast<uint8_t*>(kc + kTile * KS);   // [32][D]
-  float* kq = reinterpret_cast<float*>(vc + kTile * D);        // [KS][3] zero, scale, 1/scale
-  float* vq = kq + 3 * KS;                                     // [32][ngrp][3]
-  int16_t* sch = reinterpret_cast<int16_t*>(vq + 3 * kTile * ngrp);  // [KS] slot channels
+  float* Kf = reinterpret_cast<float*>(smem_raw);               // [32][KP]
+  float* Vf = Kf + kTile * KP;                                  // [32][D] (16-byte aligned)
+  uint8_t* vc = reinterpret_cast<uint8_t*>(Vf + kTile * D);     // [32][D]
+  float* kq = reinterpret_cast<float*>(vc + kTile * D);         // [KS][3] zero, scale, 1/scale
+  float* vq = kq + 3 * KS;                                      // [32][NG][3]
+  int16_t* sch = reinterpret_cast<int16_t*>(vq + 3 * kTile * NG);  // [KS] slot channels
   __shared__ int tok[kTile];
   const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
   if (tid < kTile) tok[tid] = index_map[slot0 + tid];
-  for (int s = tid; s < KS; s += blockDim.x) sch[s] = slot_ch[s];
+  for (int s = tid; s < KS; s += kPackThreads) sch[s] = slot_ch[s];
   __syncthreads();
   // the tile's K and V rows, four elements per load (rows are D contiguous elements, D % 4 == 0)
-  for (int i = tid; i < kTile * D / 4; i += blockDim.x) {
+  for (int i = tid; i < kTile * D / 4; i += kPackThreads) {
     const int r = i / (D / 4), c = 4 * (i % (D / 4));
     const int t = tok[r];
     float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
@@ -193,7 +214,11 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
       kx = load4(k + src);
       vx = load4(v + src);
     }
-    reinterpret_cast<float4*>(Kf)[i] = kx;
+    float* kd = Kf + r * KP + c;
+    kd[0] = kx.x;
+    kd[1] = kx.y;
+    kd[2] = kx.z;
+    kd[3] = kx.w;
     reinterpret_cast<float4*>(Vf)[i] = vx;
   }
   __syncthreads();
@@ -202,18 +227,12 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   uint16_t* kmeta = reinterpret_cast<uint16_t*>(tile + 4 * kTile * RW);
   uint8_t* vcode = tile + 4 * kTile * RW + 4 * hp.meta_slots;
   uint16_t* vmeta = reinterpret_cast<uint16_t*>(vcode + kTile * D * vbits / 8);
-  const int s16 = 2 * hp.k_words[0];  // raw 16-bit slots come first
   // statistics: K slot s (quantised slots only), then V group (r, g)
-  for (int i = tid; i < KS + (vbits < 16 ? kTile * ngrp : 0); i += blockDim.x) {
+  for (int i = tid; i < KS + (vbits < 16 ? kTile * NG : 0); i += kPackThreads) {
     if (i < KS) {
       const int s = i;
       if (s < s16) continue;
-      int seg = 1, sbase = s16;
-      while (seg < 3 && s >= sbase + hp.k_words[seg] * (32 >> (4 - seg))) {
-        sbase += hp.k_words[seg] * (32 >> (4 - seg));
-        ++seg;
-      }
-      const int kb = 16 >> seg;
+      const int kb = s < sb4 ? 8 : s < sb2 ? 4 : 2;
       const int c = sch[s];
       const int m = s - s16;  // index among the quantised slots
       uint16_t sc_h = 0, ze_h = 0;
@@ -221,8 +240,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
       if (c >= 0 && n_real > 0) {
         float mn = Kf[c], mx = Kf[c];
         for (int r = 1; r < n_real; ++r) {
-          mn = fminf(mn, Kf[r * D + c]);
-          mx = fmaxf(mx, Kf[r * D + c]);
+          mn = fminf(mn, Kf[r * KP + c]);
+          mx = fmaxf(mx, Kf[r * KP + c]);
         }
         const QParams p = qparams(mn, mx, kb);
         sc_h = p.scale_h;
@@ -237,7 +256,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
       kmeta[4 * (m >> 1) + (m & 1)] = sc_h;
       kmeta[4 * (m >> 1) + 2 + (m & 1)] = ze_h;
     } else {
-      const int vi = i - KS, r = vi / ngrp, g = vi % ngrp;
+      const int vi = i - KS, r = vi / NG, g = vi % NG;
       const float* x = Vf + r * D + g * kVGroup;
       uint16_t sc_h = 0, ze_h = 0;
       float z = 0.f, sc = 0.f, rs = 0.f;
@@ -258,72 +277,72 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
       vq[3 * vi + 1] = sc;
       vq[3 * vi + 2] = rs;
       const int pp = r >> 1, mm = r & 1;
-      vmeta[(pp * ngrp + g) * 4 + mm] = sc_h;
-      vmeta[(pp * ngrp + g) * 4 + 2 + mm] = ze_h;
+      vmeta[(pp * NG + g) * 4 + mm] = sc_h;
+      vmeta[(pp * NG + g) * 4 + 2 + mm] = ze_h;
     }
   }
   if (vbits == 16) {
-    for (int i = tid; i < kTile * D; i += blockDim.x) {
+    for (int i = tid; i < kTile * D; i += kPackThreads) {
       const int r = i / D;
       zone_b[brow * D + i] = r < n_real ? half_bits(Vf[i]) : (uint16_t)0;
     }
   }
   __syncthreads();
-  // codes: lanes along slots (K) or channels (V), warps along tokens
-  for (int r = ty; r < kTile; r += blockDim.x >> 5) {
-    for (int s = tx; s < KS; s += 32) {
-      const int c = sch[s];
-      uint16_t code = 0;
-      if (c >= 0 && r < n_real) {
-        if (s < s16) {
-          code = half_bits(Kf[r * D + c]);
-        } else {
-          const int kb = s < s16 + hp.k_words[1] * 4 ? 8 : s < s16 + hp.k_words[1] * 4 + hp.k_words[2] * 8 ? 4 : 2;
-          code = (uint16_t)qcode_rcp(Kf[r * D + c], kq[3 * s], kq[3 * s + 1], kq[3 * s + 2], (float)((1 << kb) - 1));
-        }
+  // K words: word w of token r at 32 w + 4 (r mod 8) + r / 8 (word-major; tokens r, r+8, r+16, r+24
+  // of one word index side by side, so one 16-byte load gives a decode lane its four token rows).
+  // The lane of token r builds the word from the codes of its slots (0 for pad slots and pad tokens).
+  {
+    const int r = tx;
+    const bool real = r < n_real;
+    const float* kr = Kf + r * KP;
+    uint32_t* kw = reinterpret_cast<uint32_t*>(tile);
+    for (int w = ty; w < RW; w += kPackThreads / 32) {
+      int kb, s0;
+      if (w < w8) { kb = 16; s0 = 2 * w; }
+      else if (w < w4) { kb = 8; s0 = s16 + 4 * (w - w8); }
+      else if (w < w2) { kb = 4; s0 = sb4 + 8 * (w - w4); }
+      else { kb = 2; s0 = sb2 + 16 * (w - w2); }
+      const int per = 32 / kb;
+      const float hmax = (float)((1 << kb) - 1);
+      uint32_t word = 0;
+      for (int e = 0; e < per; ++e) {
+        const int s = s0 + e;
+        const int c = sch[s];
+        if (c < 0 || !real) continue;
+        const float x = kr[c];
+        const uint32_t code = kb == 16 ? (uint32_t)half_bits(x) : qcode_rcp(x, kq[3 * s], kq[3 * s + 1], kq[3 * s + 2], hmax);
+        word |= code << bit_off(e, kb);
       }
-      kc[r * KS + s] = code;
+      kw[32 * w + 4 * (r % 8) + r / 8] = word;
     }
-    if (vbits < 16) {
+  }
+  // V codes: lanes along channels, warps along tokens
+  if (vbits < 16) {
+    const float hmax = (float)((1 << vbits) - 1);
+    for (int r = ty; r < kTile; r += kPackThreads / 32) {
       for (int c = tx; c < D; c += 32) {
-        const int vi = r * ngrp + c / kVGroup;
-        vc[r * D + c] = r < n_real ? (uint8_t)qcode_rcp(Vf[r * D + c], vq[3 * vi], vq[3 * vi + 1], vq[3 * vi + 2],
-                                                          (float)((1 << vbits) - 1))
+        const int vi = r * NG + c / kVGroup;
+        vc[r * D + c] = r < n_real ? (uint8_t)qcode_rcp(Vf[r * D + c], vq[3 * vi], vq[3 * vi + 1], vq[3 * vi + 2], hmax)
                                    : (uint8_t)0;
       }
     }
   }
   __syncthreads();
-  // K words: word w of token r at 32 w + 4 (r mod 8) + r / 8 (word-major; tokens r, r+8, r+16, r+24
-  // of one word index side by side, so one 16-byte load gives a decode lane its four token rows)
-  uint32_t* kw = reinterpret_cast<uint32_t*>(tile);
-  for (int i = tid; i < kTile * RW; i += blockDim.x) {
-    const int r = i / RW, w = i % RW;
-    int seg = 0, wbase = 0, sbase = 0;
-    while (seg < 3 && w >= wbase + hp.k_words[seg]) {
-      wbase += hp.k_words[seg];
-      sbase += hp.k_words[seg] * (32 >> (4 - seg));
-      ++seg;
-    }
-    const int kb = 16 >> seg, per = 32 / kb;
-    const int s0 = sbase + (w - wbase) * per;
-    uint32_t word = 0;
-    for (int e = 0; e < per; ++e) word |= (uint32_t)kc[r * KS + s0 + e] << bit_off(e, kb);
-    kw[32 * w + 4 * (r % 8) + r / 8] = word;
-  }
   // V words: pair p, word w holds channels [w*16/b, (w+1)*16/b) of tokens 2p (low half) and 2p+1 (high
   // half); inside a pair, word w sits at (w mod R) wpp/R + w/R with R = b/2, so the words a decode lane
   // needs (channels congruent to its own mod 8) are adjacent
   if (vbits < 16) {
     uint32_t* vw = reinterpret_cast<uint32_t*>(vcode);
     const int wpp = D * vbits / 16, per = 16 / vbits, R = vbits / 2;
-    for (int i = tid; i < (kTile / 2) * wpp; i += blockDim.x) {
-      const int p = i / wpp, w = i % wpp;
+    const int lw = __ffs(wpp) - 1;  // wpp is a power of two
+    for (int i = tid; i < (kTile / 2) * wpp; i += kPackThreads) {
+      const int p = i >> lw, w = i & (wpp - 1);
+      const uint64_t lo_b = code_bytes(vc + (2 * p) * D + w * per, per);
+      const uint64_t hi_b = code_bytes(vc + (2 * p + 1) * D + w * per, per);
       uint32_t word = 0;
       for (int e = 0; e < per; ++e) {
-        const int c = w * per + e;
-        word |= (uint32_t)vc[(2 * p) * D + c] << (vbits * e);
-        word |= (uint32_t)vc[(2 * p + 1) * D + c] << (16 + vbits * e);
+        word |= (uint32_t)((lo_b >> (8 * e)) & 255u) << (vbits * e);
+        word |= (uint32_t)((hi_b >> (8 * e)) & 255u) << (16 + vbits * e);
       }
       vw[p * wpp + (w % R) * (wpp / R) + w / R] = word;
     }
@@ -366,10 +385,17 @@ __global__ void __launch_bounds__(1024) append_kernel(const T* __restrict__ kn, 
 
 __global__ void set_len_kernel(int32_t* len_dev, int value) { *len_dev = value; }
 
-static size_t pack_smem_bytes(int D) {
-  const int max_slots = D + kSlotPad;
-  return (size_t)2 * kTile * D * 4 + (size_t)kTile * max_slots * 2 + (size_t)kTile * D + (size_t)max_slots * 12 +
-         (size_t)kTile * (D / kVGroup) * 12 + (size_t)max_slots * 2 + 16;
+template <typename T, int D>
+static rdkv_status launch_pack_tiles(const void* k, const void* v, const rdkv_cache* cache, int64_t n_tiles,
+                                     cudaStream_t cs) {
+  const size_t smem = pack_smem_bytes_of<D>();
+  RDKV_TRY_CUDA(cudaFuncSetAttribute(pack_tile_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                "pack smem");
+  pack_tile_kernel<T, D><<<(unsigned)n_tiles, kPackThreads, smem, cs>>>(
+      static_cast<const T*>(k), static_cast<const T*>(v), cache->plan, cache->index_map, cache->zone_a, cache->zone_b,
+      cache->shape.n_tokens, cache->shape.h_kv);
+  RDKV_CHECK_LAUNCH("tile pack");
+  return RDKV_OK;
 }
 
 static rdkv_status check_cache(const rdkv_cache* c) {
@@ -413,22 +439,15 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
     index_kernel<<<n_heads, 1024, 0, cs>>>(bits_tok, Np, cache->plan, cache->index_map);
     RDKV_CHECK_LAUNCH("index map");
     const int64_t n_tiles = cache->sizes.index_slots / kTile;
-    const size_t smem = pack_smem_bytes(D);
     RDKV_REQUIRE(n_tiles <= 0x7fffffff, RDKV_ERR_UNSUPPORTED, "too many tiles");
-    if (s.dtype == RDKV_F16) {
-      RDKV_TRY_CUDA(cudaFuncSetAttribute(pack_tile_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                    "pack smem");
-      pack_tile_kernel<__half><<<(unsigned)n_tiles, kPackThreads, smem, cs>>>(
-          static_cast<const __half*>(k), static_cast<const __half*>(v), cache->plan, cache->index_map, cache->zone_a,
-          cache->zone_b, N, s.h_kv, D);
-    } else {
-      RDKV_TRY_CUDA(cudaFuncSetAttribute(pack_tile_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                    "pack smem");
-      pack_tile_kernel<float><<<(unsigned)n_tiles, kPackThreads, smem, cs>>>(
-          static_cast<const float*>(k), static_cast<const float*>(v), cache->plan, cache->index_map, cache->zone_a,
-          cache->zone_b, N, s.h_kv, D);
-    }
-    RDKV_CHECK_LAUNCH("tile pack");
+    rdkv_status pst;
+    if (s.dtype == RDKV_F16)
+      pst = D == 128 ? launch_pack_tiles<__half, 128>(k, v, cache, n_tiles, cs)
+                     : launch_pack_tiles<__half, 64>(k, v, cache, n_tiles, cs);
+    else
+      pst = D == 128 ? launch_pack_tiles<float, 128>(k, v, cache, n_tiles, cs)
+                     : launch_pack_tiles<float, 64>(k, v, cache, n_tiles, cs);
+    if (pst != RDKV_OK) return pst;
   }
   if (W > 0) {
     const int64_t total = (int64_t)s.batch * s.h_kv * W * D;

@@ -261,10 +261,13 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
       uint16_t sc_h = 0, ze_h = 0;
       float z = 0.f, sc = 0.f, rs = 0.f;
       if (r < n_real) {
-        float mn = x[0], mx = x[0];
+        // lanes start at different elements of their groups (groups are 32 floats apart, so in step
+        // they would all hit one bank); the minimum and maximum do not depend on the order
+        float mn = x[tx], mx = mn;
         for (int e = 1; e < kVGroup; ++e) {
-          mn = fminf(mn, x[e]);
-          mx = fmaxf(mx, x[e]);
+          const float y = x[(tx + e) & (kVGroup - 1)];
+          mn = fminf(mn, y);
+          mx = fmaxf(mx, y);
         }
         const QParams p = qparams(mn, mx, vbits);
         sc_h = p.scale_h;

@@ -189,7 +189,8 @@ rdkv_status rdkv_waterfill(int32_t n_inst, int64_t n_units, const float* g, floa
  *      water-filling per sequence with avg_bits_k -> bits_chan [B][H_kv][D];
  *   plan: counts, orders and zone offsets (layout above) in `plan`
  *      (rdkv_plan_bytes(shape) bytes of device memory).
- * k is the prefill K [B][N][H_kv][D]. */
+ * k is the prefill K [B][N][H_kv][D], 16-byte aligned (RDKV_ERR_INVALID_ARG
+ * otherwise; the same holds for rdkv_allocate_mode and rdkv_allocate_at_levels). */
 size_t rdkv_plan_bytes(const rdkv_shape* shape);
 size_t rdkv_allocate_workspace_bytes(const rdkv_shape* shape);
 rdkv_status rdkv_allocate(const rdkv_shape* shape, const float* g_tok, const float* w_chan,

@@ -208,47 +208,81 @@ __global__ void fill_u8_kernel(uint8_t* __restrict__ p, int64_t n, uint8_t v) {
 // in fp32, combined in fp64 in a fixed order; then sums of squared deviations.
 constexpr int kChanChunk = 256;
 
-__global__ void chan_pass(const void* __restrict__ k, const uint8_t* __restrict__ bits_tok, int dtype, int N, int h_kv,
-                          int D, int Np, const float* __restrict__ mean, float* __restrict__ part,
-                          int* __restrict__ part_cnt) {
+// Elements [c0, c0 + n) (n = 2 or 4, c0 a multiple of n) of one row as floats, one vector load.
+__device__ __forceinline__ void load_run(const void* p, int64_t i, int dtype, int n, float (&x)[4]) {
+  if (dtype == RDKV_F16) {
+    const __half* h = static_cast<const __half*>(p) + i;
+    if (n == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(h);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+      x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+    } else {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(h));
+      x[0] = a.x; x[1] = a.y; x[2] = x[3] = 0.f;
+    }
+  } else {
+    const float* f = static_cast<const float*>(p) + i;
+    if (n == 4) {
+      const float4 a = *reinterpret_cast<const float4*>(f);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    } else {
+      const float2 a = *reinterpret_cast<const float2*>(f);
+      x[0] = a.x; x[1] = a.y; x[2] = x[3] = 0.f;
+    }
+  }
+}
+
+// Block (chunk, head), 256 threads: lane l takes channels [l D/32, (l+1) D/32) of every token (one
+// vector load; a warp reads whole rows), warp w the chunk's tokens t0 + w, t0 + w + 8, ... in order;
+// the eight warps' sums are added in warp order (deterministic).
+constexpr int kChanWarps = 8;
+__global__ void __launch_bounds__(32 * kChanWarps) chan_pass(const void* __restrict__ k,
+                                                             const uint8_t* __restrict__ bits_tok, int dtype, int N,
+                                                             int h_kv, int D, int Np, const float* __restrict__ mean,
+                                                             float* __restrict__ part, int* __restrict__ part_cnt) {
+  __shared__ float wsum[kChanWarps][128];
+  __shared__ int wcnt[kChanWarps];
   const int head = blockIdx.y;  // b * h_kv + j
   const int b = head / h_kv, j = head % h_kv;
   const int chunk = blockIdx.x, nchunk = gridDim.x;
-  const int c = threadIdx.x;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int cpl = D / 32, c0 = lane * cpl;
   const int t0 = chunk * kChanChunk, t1 = min(Np, t0 + kChanChunk);
   const uint8_t* bt = bits_tok + (int64_t)head * Np;
-  const float m = mean ? mean[head * D + c] : 0.0f;
-  float acc = 0.0f;
+  float m[4] = {0.f, 0.f, 0.f, 0.f};
+  if (mean)
+    for (int i = 0; i < cpl; ++i) m[i] = mean[head * D + c0 + i];
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   int cnt = 0;
-  // branch-free, eight tokens per step so that their loads are in flight together; the tokens are
-  // taken in order, so the sum is the same as one token at a time
   const int64_t row = (int64_t)h_kv * D;
-  const int64_t base = (((int64_t)b * N) * h_kv + j) * D + c;
-  int t = t0;
-  for (; t + 8 <= t1; t += 8) {
-    float x[8];
-    bool keep[8];
+  const int64_t base = (((int64_t)b * N) * h_kv + j) * D + c0;
+#pragma unroll 4
+  for (int t = t0 + w; t < t1; t += kChanWarps) {
+    const bool keep = bt[t] != 0;
+    float x[4];
+    load_run(k, base + (int64_t)t * row, dtype, cpl, x);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      keep[u] = bt[t + u] != 0;
-      x[u] = load_as_float(k, base + (int64_t)(t + u) * row, dtype);
+    for (int i = 0; i < 4; ++i) {
+      const float d = x[i] - m[i];
+      acc[i] += keep ? (mean ? d * d : x[i]) : 0.0f;
     }
+    cnt += keep ? 1 : 0;
+  }
+  for (int i = 0; i < cpl; ++i) wsum[w][c0 + i] = acc[i];
+  if (lane == 0) wcnt[w] = cnt;
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float s = 0.0f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float d = x[u] - m;
-      acc += keep[u] ? (mean ? d * d : x[u]) : 0.0f;
-      cnt += keep[u] ? 1 : 0;
-    }
+    for (int q = 0; q < kChanWarps; ++q) s += wsum[q][c];
+    part[((int64_t)head * nchunk + chunk) * D + c] = s;
   }
-  for (; t < t1; ++t) {
-    if (bt[t] == 0) continue;
-    const float x = load_as_float(k, base + (int64_t)t * row, dtype);
-    const float d = x - m;
-    acc += mean ? d * d : x;
-    ++cnt;
+  if (threadIdx.x == 0 && part_cnt) {
+    int n = 0;
+    for (int q = 0; q < kChanWarps; ++q) n += wcnt[q];
+    part_cnt[head * nchunk + chunk] = n;
   }
-  part[((int64_t)head * nchunk + chunk) * D + c] = acc;
-  if (c == 0 && part_cnt) part_cnt[head * nchunk + chunk] = cnt;
 }
 
 __global__ void chan_finish(const float* __restrict__ part, const int* __restrict__ part_cnt, int nchunk, int D,
@@ -489,6 +523,7 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
   RDKV_REQUIRE(w_chan && k && bits_chan && sigma_chan && g_chan && plan && (Np == 0 || bits_tok) &&
                    (Np == 0 || (by_weight ? w_tok != nullptr : g_tok != nullptr)),
                RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  RDKV_REQUIRE(reinterpret_cast<uintptr_t>(k) % 16 == 0, RDKV_ERR_INVALID_ARG, "k must be 16-byte aligned");
   size_t wf_b, part_b, cnt_b, mean_b;
   const size_t need = alloc_ws_parts(s, &wf_b, &part_b, &cnt_b, &mean_b);
   RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "allocate workspace too small (%zu < %zu)", ws_bytes, need);
@@ -535,13 +570,13 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
   // step 3: K channel spread over the kept tokens, gains, widths
   const int nchunk = std::max(1, ceil_div(Np, kChanChunk));
   if (Np > 0) {
-    chan_pass<<<dim3(nchunk, n_heads), D, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np, nullptr, part,
-                                                   pcnt);
+    chan_pass<<<dim3(nchunk, n_heads), 32 * kChanWarps, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np,
+                                                                 nullptr, part, pcnt);
     RDKV_CHECK_LAUNCH("channel sums");
     chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, mean, nullptr, nullptr, nullptr);
     RDKV_CHECK_LAUNCH("channel means");
-    chan_pass<<<dim3(nchunk, n_heads), D, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np, mean, part,
-                                                   nullptr);
+    chan_pass<<<dim3(nchunk, n_heads), 32 * kChanWarps, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np,
+                                                                 mean, part, nullptr);
     RDKV_CHECK_LAUNCH("channel deviations");
     chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, nullptr, w_chan, sigma_chan, g_chan);
     RDKV_CHECK_LAUNCH("channel spread");

@@ -65,12 +65,29 @@ __global__ void __launch_bounds__(1024) index_kernel(const uint8_t* __restrict__
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
   const int chunk = ceil_div(Np, blockDim.x);
   const int t0 = min(Np, tid * chunk), t1 = min(Np, t0 + chunk);
-  auto cls = [](int b) { return b == 2 ? 0 : b == 4 ? 1 : b == 8 ? 2 : b == 16 ? 3 : -1; };
+  // the widths of this thread's tokens in position order: sixteen per load where the range is
+  // 16-byte aligned, the rest one at a time
+  auto visit = [&](auto&& f) {
+    int t = t0;
+    if (((uintptr_t)(bt + t) & 15) == 0) {
+      for (; t + 16 <= t1; t += 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(bt + t);
+        const uint32_t vs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) f(t + 4 * q + e, (int)((vs[q] >> (8 * e)) & 255u));
+      }
+    }
+    for (; t < t1; ++t) f(t, (int)bt[t]);
+  };
   int cnt[4] = {0, 0, 0, 0};
-  for (int t = t0; t < t1; ++t) {
-    const int c = cls(bt[t]);
-    if (c >= 0) ++cnt[c];
-  }
+  visit([&](int, int b) {  // constant indices only: the counters stay in registers
+    cnt[0] += b == 2;
+    cnt[1] += b == 4;
+    cnt[2] += b == 8;
+    cnt[3] += b == 16;
+  });
   int base[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -105,10 +122,15 @@ __global__ void __launch_bounds__(1024) index_kernel(const uint8_t* __restrict__
     acc += kTile * hp.tiles[c];
   }
   int32_t* out = index_map + hp.slot_off;
-  for (int t = t0; t < t1; ++t) {
-    const int c = cls(bt[t]);
-    if (c >= 0) out[start[c] + base[c]++] = t;
-  }
+  int next[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) next[c] = start[c] + base[c];
+  visit([&](int t, int b) {
+    if (b == 2) out[next[0]++] = t;
+    else if (b == 4) out[next[1]++] = t;
+    else if (b == 8) out[next[2]++] = t;
+    else if (b == 16) out[next[3]++] = t;
+  });
 #pragma unroll
   for (int c = 0; c < 4; ++c)
     for (int r = hp.n_v[c] + tid; r < kTile * hp.tiles[c]; r += blockDim.x) out[start[c] + r] = -1;

@@ -195,3 +195,14 @@ def test_paged_zone_c_table_stride_is_checked(L):
     r = L.rdkv_append(ctypes.byref(c), fake, fake, None)
     assert r == rdkv.RDKV_ERR_INVALID_ARG and b"page table" in L.rdkv_last_error_string()
     assert c.len_c == 8
+
+
+def test_allocate_requires_aligned_keys(L):
+    # the channel passes read whole K rows with vector loads: a misaligned k is refused on the host
+    s = rdkv.make_shape(1, 1024, 4, 1, 64, 32, "f16")
+    fake = ctypes.c_void_p(256)
+    ws = L.rdkv_allocate_workspace_bytes(ctypes.byref(s))
+    r = L.rdkv_allocate(ctypes.byref(s), fake, fake, ctypes.c_void_p(258), ctypes.c_float(2.0), ctypes.c_float(2.0),
+                        fake, fake, fake, fake, fake, fake, ws, None)
+    assert r == rdkv.RDKV_ERR_INVALID_ARG
+    assert b"aligned" in L.rdkv_last_error_string()

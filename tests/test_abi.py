@@ -206,3 +206,14 @@ def test_allocate_requires_aligned_keys(L):
                         fake, fake, fake, fake, fake, fake, ws, None)
     assert r == rdkv.RDKV_ERR_INVALID_ARG
     assert b"aligned" in L.rdkv_last_error_string()
+
+
+def test_timeout_selftest_rejects_a_non_positive_limit(L):
+    s = rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16")
+    sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 0, 1)
+    fake = ctypes.c_void_p(256)
+    c = rdkv.CacheStruct(s, 256, None, None, 256, 256, None, 256, 8, 8, sizes)
+    for limit in (0, -5):
+        r = L.rdkv_decode_timeout_selftest(ctypes.byref(c), fake, fake, fake, 1 << 20, limit, None)
+        assert r == rdkv.RDKV_ERR_INVALID_ARG
+        assert b"wait_cycles" in L.rdkv_last_error_string()

@@ -445,3 +445,19 @@ def test_allocate_per_head_reduces_to_pooled_for_one_head_and_keeps_budgets():
         lower = np.nextafter(r["lam_v"][j], np.float32(-1))
         if r["lam_v"][j] > 0:
             assert int(O.widths_at(O.breakpoints(g[j]), lower).astype(np.int64).sum()) > int(np.floor(np.float32(2.5) * 300))
+
+
+def test_bench_decode_bytes_agree_with_the_oracle():
+    """bench.py counts the decode's algorithmic bytes with its own copy of the formula (the product
+    path does not import the oracle): both must give the same number on the same plans."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(os.path.dirname(__file__), "..", "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    for avg in (0.5, 2.0, 3.0, 7.0, 16.0):
+        w, q, k, v, al, cache = _tiny_cache(avg, avg)
+        heads = cache["plan"]["heads"]
+        for len_c in (0, w.window, w.window + 3):
+            ours = O.decode_bytes(cache["plan"], w.head_dim, w.h_q, w.h_kv, len_c=len_c, batch=1)
+            theirs = bench.decode_bytes_per_call(heads, w.head_dim, w.h_q, 1, len_c)
+            assert theirs == pytest.approx(ours, rel=0, abs=1e-6), (avg, len_c)

@@ -148,6 +148,21 @@ int32_t rdkv_version(void);
  * being captured) in this process, over all threads. */
 uint64_t rdkv_launch_count(void);
 
+/* ---------------------------------------------------------------- workspace sizes
+ * One workspace query for the calls that take a shape (no counterpart in the
+ * paper).  which_call:
+ *   RDKV_CALL_SCORE     the same value as rdkv_score_workspace_bytes(shape);
+ *   RDKV_CALL_ALLOCATE  the same value as rdkv_allocate_workspace_bytes(shape)
+ *                       (also enough for rdkv_allocate_mode and
+ *                       rdkv_allocate_at_levels on that shape);
+ *   RDKV_CALL_DECODE    an upper bound of rdkv_decode_workspace_bytes(cache)
+ *                       for every single cache of this shape on the current
+ *                       device (the exact value depends on the cache's plan:
+ *                       query it once the plan's sizes are known).
+ * Returns 0 for an invalid shape or an unknown call.  Host only. */
+enum { RDKV_CALL_SCORE = 0, RDKV_CALL_ALLOCATE = 1, RDKV_CALL_DECODE = 2 };
+size_t rdkv_workspace_bytes(const rdkv_shape* shape, int32_t which_call);
+
 /* ---------------------------------------------------------------- step 1: weights
  * RDKV section 2.1 (and section 2.2 step 1: computed once after prefill on the
  * full cache).  For each sequence b and KV head j (query heads h of group j):

@@ -29,8 +29,9 @@ EXPORTED = (
     "rdkv_decode_attn_noalloc",
     "rdkv_decode_attn_lse", "rdkv_decode_step_lse", "rdkv_merge_attn", "rdkv_zone_c_take", "rdkv_recompress_score",
     "rdkv_allocate_at_levels", "rdkv_decode_multi_workspace_bytes", "rdkv_decode_attn_multi",
-    "rdkv_decode_multi_status", "rdkv_zone_bounds", "rdkv_decode_timeout_selftest",
+    "rdkv_decode_multi_status", "rdkv_zone_bounds", "rdkv_decode_timeout_selftest", "rdkv_workspace_bytes",
 )
+RDKV_CALL_SCORE, RDKV_CALL_ALLOCATE, RDKV_CALL_DECODE = 0, 1, 2
 
 
 class RDKVError(RuntimeError):
@@ -105,6 +106,7 @@ def lib():
             "rdkv_decode_attn": (ctypes.c_int, [cp, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_step": (ctypes.c_int, [cp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_status": (ctypes.c_int, [cp, _P, _P]),
+            "rdkv_workspace_bytes": (ctypes.c_size_t, [sp, ctypes.c_int32]),
             "rdkv_decode_timeout_selftest": (ctypes.c_int, [cp, _P, _P, _P, ctypes.c_size_t, ctypes.c_int64, _P]),
             "rdkv_decode_attn_noalloc": (ctypes.c_int, [cp, _P, _P, _P]),
             "rdkv_decode_attn_lse": (ctypes.c_int, [cp, _P, _P, _P, _P, ctypes.c_size_t, _P]),

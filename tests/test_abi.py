@@ -217,3 +217,21 @@ def test_timeout_selftest_rejects_a_non_positive_limit(L):
         r = L.rdkv_decode_timeout_selftest(ctypes.byref(c), fake, fake, fake, 1 << 20, limit, None)
         assert r == rdkv.RDKV_ERR_INVALID_ARG
         assert b"wait_cycles" in L.rdkv_last_error_string()
+
+
+def test_shape_workspace_query(L):
+    s = rdkv.make_shape(1, 32768, 24, 8, 128, 128, "f16")
+    assert L.rdkv_workspace_bytes(ctypes.byref(s), rdkv.RDKV_CALL_SCORE) == L.rdkv_score_workspace_bytes(ctypes.byref(s))
+    assert L.rdkv_workspace_bytes(ctypes.byref(s), rdkv.RDKV_CALL_ALLOCATE) == \
+        L.rdkv_allocate_workspace_bytes(ctypes.byref(s))
+    assert L.rdkv_workspace_bytes(ctypes.byref(s), 99) == 0
+    bad = rdkv.make_shape(1, 32768, 24, 8, 96, 128, "f16")
+    assert L.rdkv_workspace_bytes(ctypes.byref(bad), rdkv.RDKV_CALL_SCORE) == 0
+    # the decode bound covers the cache-exact query
+    for shape in (rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16"), rdkv.make_shape(2, 4096, 32, 8, 128, 128, "f16")):
+        n_heads = shape.batch * shape.h_kv
+        sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 0, n_heads)
+        c = rdkv.CacheStruct(shape, 256, None, None, 256, 256, None, 256, shape.window + 8, shape.window, sizes)
+        exact = L.rdkv_decode_workspace_bytes(ctypes.byref(c))
+        assert exact > 0
+        assert L.rdkv_workspace_bytes(ctypes.byref(shape), rdkv.RDKV_CALL_DECODE) >= exact

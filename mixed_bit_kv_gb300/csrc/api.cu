@@ -43,3 +43,25 @@ extern "C" const char* rdkv_last_error_string(void) { return rdkv::g_err; }
 extern "C" int32_t rdkv_version(void) { return 1; }
 
 extern "C" uint64_t rdkv_launch_count(void) { return rdkv::g_launches.load(std::memory_order_relaxed); }
+
+// One workspace query for the calls that take a shape.  The decode's value is a bound over every
+// single cache of the shape: its grid holds at most one dealt block per SM plus one spare block per
+// head, each with a partial of G (D + 2) floats (rounded up to four), then the per-head tickets, the
+// status word and the fused step's head counter (the layout of the decode's own workspace query).
+extern "C" size_t rdkv_workspace_bytes(const rdkv_shape* shape, int32_t which_call) {
+  using namespace rdkv;
+  if (check_shape(shape) != RDKV_OK) return 0;
+  switch (which_call) {
+    case RDKV_CALL_SCORE:
+      return rdkv_score_workspace_bytes(shape);
+    case RDKV_CALL_ALLOCATE:
+      return rdkv_allocate_workspace_bytes(shape);
+    case RDKV_CALL_DECODE: {
+      const int64_t n_heads = (int64_t)shape->batch * shape->h_kv, G = shape->h_q / shape->h_kv;
+      const int64_t partial = (G * (shape->head_dim + 2) + 3) / 4 * 4;
+      return (size_t)(align_up((num_sms() + n_heads) * partial * 4, 256) + align_up((n_heads + 2) * 4, 256));
+    }
+    default:
+      return 0;
+  }
+}

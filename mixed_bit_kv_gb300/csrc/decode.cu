@@ -1417,28 +1417,6 @@ static rdkv_status decode_step_impl(rdkv_cache* cache, const void* q, const void
   return st;
 }
 
-extern "C" size_t rdkv_workspace_bytes(const rdkv_shape* shape, int32_t which_call) {
-  if (check_shape(shape) != RDKV_OK) return 0;
-  switch (which_call) {
-    case RDKV_CALL_SCORE:
-      return rdkv_score_workspace_bytes(shape);
-    case RDKV_CALL_ALLOCATE:
-      return rdkv_allocate_workspace_bytes(shape);
-    case RDKV_CALL_DECODE: {
-      // a single cache's grid has at most one dealt block per SM plus one spare block per head
-      const int n_heads = shape->batch * shape->h_kv;
-      DecodeGeom g{};
-      g.partial_bytes = (size_t)align_up((int64_t)(num_sms() + n_heads) *
-                                             partial_stride(shape->h_q / shape->h_kv, shape->head_dim) * 4,
-                                         256);
-      g.ticket_off = g.partial_bytes;
-      return decode_ws_bytes(g, n_heads);
-    }
-    default:
-      return 0;
-  }
-}
-
 extern "C" rdkv_status rdkv_decode_attn(const rdkv_cache* cache, const void* q, float* out, void* ws, size_t ws_bytes,
                                         void* stream) {
   return decode_attn_impl(cache, q, out, nullptr, ws, ws_bytes, stream);

@@ -2,12 +2,13 @@
 """Benchmark of the RDKV hot path (score -> allocate -> TriZone pack -> append + decode) on GB300.
 
 One step = compress every layer of a stack of independently generated layers
-of the chosen workload (default: the Llama-3.2-3B-shaped layer, N = 32768,
-28 layers like the model), then run the workload's decode steps over all
-layers (append the new token, attend).  Inputs are resident in HBM when the
-timed region starts; the decode phase is replayed from a captured CUDA graph.
-The working set (prefill inputs ~9 GB, packed caches ~0.7 GB) is larger than
-L2, and each decode call reads a cache last touched 27 calls earlier.
+of the chosen workload (default: the Qwen2.5-72B-shaped layer, N = 262144,
+H_q = 64, H_kv = 8, 2 bits, window 128; 4 layers of the 80-layer stack, so the
+packed zones the decode rotates through, about 0.6 GB, exceed the 129 MB L2
+several times), then run the workload's decode steps over all layers (append
+the new token, attend).  Inputs are resident in HBM when the timed region
+starts; the decode phase is replayed from a captured CUDA graph.  Per-step
+times are medians over the timed steps.
 
 Rank 0 prints one JSON line.  `--impl reference` times the CPU oracle instead.
 """
@@ -18,19 +19,26 @@ import json
 import math
 import os
 import resource
+import statistics
 import subprocess
 import sys
 import threading
 import time
 
 import numpy as np
-import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "TriZone decode attn HBM GB/s (scoring TFLOP/s, decode us/step alongside)"
+METRIC = "TriZone decode attn HBM GB/s (decode us/step and scoring TFLOP/s alongside)"
 UNIT = "GB/s"
+
+# layers of each workload's stack in one benchmark step: enough independently packed layers that
+# the zones one decode step reads exceed the L2 several times
+DEFAULT_LAYERS = {"qwen72b": 4, "llama3b": 28, "batched": 4, "llama8b": 4, "tiny": 8}
+# decode-only measurements of other workloads added to the line: (layers, decode steps)
+EXTRA_DECODE = {"batched": (3, 64), "llama3b": (16, 64)}
+L2_BYTES = 129 * 1024 * 1024
 
 
 # ---------------------------------------------------------------- environment
@@ -51,6 +59,7 @@ def max_over_ranks(values, ws, device):
     """Element-wise maximum over ranks of per-rank totals: the slowest rank sets the step time."""
     if ws <= 1:
         return list(values)
+    import torch
     t = torch.tensor(list(values), dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return t.tolist()
@@ -121,15 +130,15 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def captured_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu record, or None when the kernel's
-    source has changed since the capture."""
+def captured_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu record, or None when
+    there is no record for that workload or the kernel's source has changed since the capture."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        rec = json.load(open(p))[kernel]
+        rec = json.load(open(p))[kernel][workload]
         src = open(os.path.join(ROOT, rec["source"]), "rb").read()
-    except (OSError, KeyError, ValueError):
+    except (OSError, KeyError, ValueError, TypeError):
         return None
     if hashlib.sha256(src).hexdigest()[:16] != rec["source_sha256_16"]:
         return None
@@ -169,13 +178,30 @@ def scorer_flops(w):
     return 2 * 2 * w.head_dim * w.h_q * w.batch * w.n_tokens * (w.n_tokens + 1) / 2
 
 
+def median(xs):
+    return float(statistics.median(xs))
+
+
+def decode_roofline(dec_bytes_per_launch, value_per_gpu, peaks, workload, time_share=None):
+    roof = {"bound": "hbm", "achieved": round(value_per_gpu, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(value_per_gpu / peaks["hbm_gbs"], 4),
+            "traffic": captured_traffic("decode_kernel", workload),
+            "algorithmic_bytes_per_launch": int(dec_bytes_per_launch),
+            "kernel": "rdkv::decode_kernel (fused append + attend, one launch per layer step)",
+            "peak_source": f"{peaks['source']} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"}
+    if time_share is not None:
+        roof["time_share"] = round(time_share, 3)
+    return roof
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, ws, rank, local):
+    import torch
     from mixed_bit_kv_gb300 import rdkv, synth
 
     dev = torch.device("cuda", local)
     w = synth.WORKLOADS[args.workload]
-    L = args.layers
+    L = args.layers if args.layers is not None else DEFAULT_LAYERS.get(w.name, 4)
     S = args.decode_steps if args.decode_steps is not None else w.decode_steps
     avg = w.budgets[0] if args.budget is None else args.budget
     first_seq, _ = rank_sequences(rank, w.batch)
@@ -194,7 +220,6 @@ def run_ours(args, ws, rank, local):
     alloc_out = [None] * L
     caches = [None] * L
     lib = rdkv.lib()
-    stream = torch.cuda.current_stream()
 
     def compress(timing):
         for layer in range(L):
@@ -251,6 +276,8 @@ def run_ours(args, ws, rank, local):
     dec_bytes = sum(decode_bytes_per_call(h, w.head_dim, w.h_q, w.batch, w.window + s + 1)
                     for h in heads_per_layer for s in range(S))
     kept = sum(int(np.sum(h["n_v"])) for h in heads_per_layer) / (L * w.batch * w.h_kv * w.n_prefix)
+    zone_bytes_layer = sum(int(c.c.sizes.zone_a_bytes) + int(c.c.sizes.zone_b_rows) * w.head_dim * 2
+                           for c in caches) / L
 
     # timed region
     if ws > 1:
@@ -270,49 +297,48 @@ def run_ours(args, ws, rank, local):
             b = torch.cuda.Event(enable_timing=True)
             c = torch.cuda.Event(enable_timing=True)
             a.record()
-            compress(score_ev)
+            step_ev = []
+            compress(step_ev)
             b.record()
             g.replay()
             c.record()
             ev.append((a, b, c))
+            score_ev.append(step_ev)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     if ws > 1:
         torch.distributed.barrier()
     compress_launches = lib.rdkv_launch_count() - launches0
     gpu_launches = int(compress_launches + args.steps * decode_launches)
+    # per-step times; the line reports the median step
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     dec_ms = [b.elapsed_time(c) for a, b, c in ev]
-    score_ms = sum(e[0].elapsed_time(e[1]) for e in score_ev) / args.steps
-    alloc_ms = sum(e[1].elapsed_time(e[2]) for e in score_ev) / args.steps  # incl. the sizes read-back
-    pack_ms = sum(e[2].elapsed_time(e[3]) for e in score_ev) / args.steps
-    tot_ms, tot_dec, tot_score = sum(step_ms), sum(dec_ms), score_ms * args.steps
-    tot_ms, tot_dec, tot_score = max_over_ranks([tot_ms, tot_dec, tot_score], ws, dev)
-    score_ms = tot_score / args.steps
+    score_ms = [sum(e[0].elapsed_time(e[1]) for e in se) for se in score_ev]
+    alloc_ms = [sum(e[1].elapsed_time(e[2]) for e in se) for se in score_ev]  # incl. the sizes read-back
+    pack_ms = [sum(e[2].elapsed_time(e[3]) for e in se) for se in score_ev]
+    med = max_over_ranks([median(step_ms), median(dec_ms), median(score_ms), median(alloc_ms), median(pack_ms)],
+                         ws, dev)
+    ms_per_step, dec_ms_step, score_ms_step, alloc_ms_step, pack_ms_step = med
 
-    ms_per_step = tot_ms / args.steps
-    dec_ms_step = tot_dec / args.steps
     value = whole_job_rate(ws, dec_bytes, dec_ms_step * 1e-3) / 1e9
     flops = scorer_flops(w) * L
-    score_tflops = whole_job_rate(ws, flops, score_ms * 1e-3) / 1e12
+    score_tflops = whole_job_rate(ws, flops, score_ms_step * 1e-3) / 1e12
     peaks = measured_peaks()
     clocks = clk.summary()
 
-    # roofline of the dominant kernel by time share in the step
-    dec_frac_time, score_frac_time = dec_ms_step / ms_per_step, score_ms / ms_per_step
-    decode_roof = {"bound": "hbm", "achieved": round(value / ws, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                   "frac": round(value / ws / peaks["hbm_gbs"], 4), "traffic": captured_traffic("decode_kernel"),
-                   "algorithmic_bytes_per_launch": int(dec_bytes / (S * L)),
-                   "peak_source": peaks["source"], "time_share": round(dec_frac_time, 3)}
+    dec_frac_time, score_frac_time = dec_ms_step / ms_per_step, score_ms_step / ms_per_step
+    decode_roof = decode_roofline(dec_bytes / (S * L), value / ws, peaks, w.name, dec_frac_time)
     # fp16 scorer on the tensor cores: measured dense bf16 peak (fp16 has the same nominal dense rate);
     # the sustained figure, since the scorer runs back to back over every layer inside the step.
     # fp32 inputs run on CUDA cores: roofline against the FP32 FMA peak instead.
     if w.dtype == "f16":
-        t1, t2 = captured_traffic("score_kernel_pass1"), captured_traffic("score_kernel_pass2")
+        t1 = captured_traffic("score_kernel_pass1", w.name)
+        t2 = captured_traffic("score_kernel_pass2", w.name)
         score_roof = {"bound": "tensor", "achieved": round(score_tflops / ws, 2),
                       "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                       "frac": round(score_tflops / ws / peaks["bf16_tflops_sustained"], 4),
                       "traffic": (t1 + t2) if (t1 and t2) else None, "flops_per_launch_pair": scorer_flops(w),
+                      "kernel": "rdkv::tc::score_kernel (passes 1 and 2)",
                       "peak_source": f"{peaks['source']} bf16 dense sustained (fp16 nominal rate equal)",
                       "time_share": round(score_frac_time, 3)}
     else:
@@ -322,7 +348,6 @@ def run_ours(args, ws, rank, local):
                       "unit": "TFLOP/s", "frac": round(score_tflops / ws / alu_peak, 4), "traffic": None,
                       "peak_source": "SMs x 128 FP32 lanes x 2 flops x max SM clock",
                       "time_share": round(score_frac_time, 3)}
-    dominant = score_roof if score_frac_time >= dec_frac_time else decode_roof
 
     e2e = None
     if not args.no_e2e:
@@ -349,20 +374,32 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": w.name, "description": w.description, "layers": L, "decode_steps": S,
                    "avg_bits": avg, "batch_per_gpu": w.batch, "kept_fraction": round(kept, 4),
                    "parallelism": f"replicas x{ws} (independent sequences per rank)",
-                   "l2": "inputs larger than L2: 9 GB prefill, ~0.7 GB of packed caches rotated across layers"},
+                   "timing": "median over the timed steps (CUDA events on the launching stream)",
+                   "l2": (f"inputs larger than L2: {sum(t.numel() * t.element_size() for p in pre for t in p) / 1e9:.1f}"
+                          f" GB of prefill inputs; the decode rotates through {L} independently packed layers of "
+                          f"{zone_bytes_layer / 1e6:.0f} MB each ({L * zone_bytes_layer / L2_BYTES:.1f}x L2)")},
         "decode_us_per_layer_step": round(dec_ms_step * 1e3 / (S * L), 3),
         "decode_ms_per_model_step": round(dec_ms_step / S, 4),
         "decode_bytes_per_step": int(dec_bytes),
-        "scorer_tflops": round(score_tflops, 2), "scorer_ms_per_layer": round(score_ms / L, 3),
+        "scorer_tflops": round(score_tflops, 2), "scorer_ms_per_layer": round(score_ms_step / L, 3),
         "compress_ms_per_layer": round((ms_per_step - dec_ms_step) / L, 3),
         "compress_breakdown_ms_per_layer": {
-            "score (weights: tensor-core passes, channel norms, V spreads)": round(score_ms / L, 3),
-            "allocate (water-filling V and K, channel spreads, plan; sizes read back)": round(alloc_ms / L, 3),
-            "pack (index map, tiles, zone B, window)": round(pack_ms / L, 3)},
-        "pack_gbs": round(sum(pack_bytes_per_layer(w, c.c.sizes) for c in caches) / (pack_ms * 1e-3) / 1e9, 1),
-        "roofline": dominant, "rooflines": {"decode": decode_roof, "scorer": score_roof},
+            "score (weights: tensor-core passes, channel norms, V spreads)": round(score_ms_step / L, 3),
+            "allocate (water-filling V and K, channel spreads, plan; sizes read back)": round(alloc_ms_step / L, 3),
+            "pack (index map, tiles, zone B, window)": round(pack_ms_step / L, 3)},
+        "pack_gbs": round(sum(pack_bytes_per_layer(w, c.c.sizes) for c in caches) / (pack_ms_step * 1e-3) / 1e9, 1),
+        "zone_bytes_per_layer": int(zone_bytes_layer),
+        "roofline": decode_roof, "rooflines": {"decode": decode_roof, "scorer": score_roof},
         "gpu_launches": gpu_launches, "clocks": clocks, "wall_s": round(wall, 3),
     }
+    if w.n_layers > 1:
+        fp16_model = 2 * w.n_layers * w.h_kv * w.head_dim * 2 * w.n_tokens * w.batch
+        line["hbm_accounting"] = {
+            "model_layers": w.n_layers, "fp16_kv_bytes": fp16_model,
+            "trizone_bytes_est": int(zone_bytes_layer * w.n_layers
+                                     + 2 * w.n_layers * w.batch * w.h_kv * cap_c * w.head_dim * 2),
+            "note": "fp16 K+V of the whole stack by the KV-size formula 2*L*H_kv*D*P*N vs the measured zones "
+                    "A and B per layer times the layers plus zone C at capacity"}
     if e2e is not None:
         line["e2e"] = e2e
     if comparator is not None:
@@ -373,14 +410,78 @@ def run_ours(args, ws, rank, local):
         line["paged_zone_c"] = paged
     if graph_compress is not None:
         line["compress_in_one_graph"] = graph_compress
+    # free this workload's buffers before the other workloads' decode measurements
+    del pre, dq, dk, dv, outs, score_out, alloc_out, caches, g
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if not args.no_extras and rank == 0:
+        line["decode_other_workloads"] = {name: run_decode_only(name, nl, ns, peaks, dev)
+                                          for name, (nl, ns) in EXTRA_DECODE.items() if name != w.name}
     return line
 
+
+def run_decode_only(name, L, S, peaks, dev):
+    """Decode of another workload, measured beside the headline: L independently packed layers
+    (compressed once, untimed), then S fused decode steps over all layers from a CUDA graph, 3
+    timed replays (median).  The layers' zones exceed the L2 several times."""
+    import torch
+    from mixed_bit_kv_gb300 import rdkv, synth
+    w = synth.WORKLOADS[name]
+    avg = w.budgets[0]
+    shape = rdkv.make_shape(w.batch, w.n_tokens, w.h_q, w.h_kv, w.head_dim, w.window, w.dtype)
+    cap_c = w.window + S
+    caches, heads = [], []
+    for layer in range(L):
+        q, k, v = synth.prefill_batch(w, layer, device=dev)
+        sc = rdkv.rdkv_score(shape, q, k, v)
+        al = rdkv.rdkv_allocate(shape, sc["g_tok"], sc["w_chan"], k, avg, avg)
+        caches.append(rdkv.rdkv_pack(shape, al["plan"], k, v, al["bits_tok"], al["bits_chan"], cap_c))
+        heads.append(rdkv.read_plan(al["plan"])[1])
+        del q, k, v, sc
+    dq, dk, dv = synth.decode_stream(w, S, L, 0, device=dev)
+    out = torch.empty(w.batch, w.h_q, w.head_dim, dtype=torch.float32, device=dev)
+    for c in caches:
+        c.decode_workspace()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for s in range(S):
+            for layer in range(L):
+                rdkv.rdkv_decode_step(caches[layer], dq[s, layer], dk[s, layer], dv[s, layer], out=out)
+    times = []
+    for _ in range(3):
+        for c in caches:  # back to the window: every replay attends over the same rows
+            c.len_dev.fill_(w.window)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    for c in caches:
+        if rdkv.rdkv_decode_status(c) != 0:
+            raise RuntimeError(f"{name}: decode status")
+    dec_bytes = sum(decode_bytes_per_call(h, w.head_dim, w.h_q, w.batch, w.window + s + 1)
+                    for h in heads for s in range(S))
+    ms = median(times)
+    gbs = dec_bytes / (ms * 1e-3) / 1e9
+    zone = sum(int(c.c.sizes.zone_a_bytes) + int(c.c.sizes.zone_b_rows) * w.head_dim * 2 for c in caches) / L
+    res = {"description": w.description, "layers": L, "decode_steps": S, "avg_bits": avg,
+           "us_per_layer_step": round(ms * 1e3 / (S * L), 3), "gbs": round(gbs, 1),
+           "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+           "algorithmic_bytes_per_launch": int(dec_bytes / (S * L)), "zone_bytes_per_layer": int(zone),
+           "traffic": captured_traffic("decode_kernel", name)}
+    del caches, dq, dk, dv, g
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
 def run_fp16_comparator(w, L, pre, dq, dev, steps=16):
     """Context number: decode over the full fp16 cache of the same layers (all N prompt tokens, no
     compression) with torch's scaled_dot_product_attention (a library call), per layer step, replayed
     from a CUDA graph like the TriZone decode.  The caches of all layers are rotated (inputs larger
     than L2)."""
+    import torch
     steps = min(steps, dq.shape[0])
     caches = [tuple(t.permute(0, 2, 1, 3).contiguous() for t in (pre[layer][1], pre[layer][2])) for layer in range(L)]
     qs = dq[:steps]  # [steps, L, B, H_q, D]
@@ -424,6 +525,7 @@ def run_recompress(w, cache, prefill_plan, w_chan, dq, dev, recent=32, reps=20):
     segment (weights from the last `recent` decode queries and their log-sum-exps); reported with
     the decode of the cache before (one launch) and after (segment and live cache: two launches and
     a merge)."""
+    import torch
     from mixed_bit_kv_gb300 import rdkv
     S, layer = dq.shape[0], dq.shape[1] - 1
     R = min(recent, S)
@@ -492,6 +594,7 @@ def run_paged(w, shape, layer_inputs, al, cap_c, dq, dk, dv, dev):
     """Paged zone C, measured beside the path: the last layer packed twice, with a contiguous zone C
     and with its zone C in 16-row pages of a shuffled pool; per-call time of the benchmark's fused
     decode steps (CUDA graph of every step) on each."""
+    import torch
     from mixed_bit_kv_gb300 import rdkv
     _, k, v = layer_inputs
     S, layer = dq.shape[0], dq.shape[1] - 1
@@ -529,6 +632,7 @@ def run_graph_compress(w, shape, layer_inputs, avg, cap_c, dev, reps=3):
     pack of one layer with zones sized from rdkv_zone_bounds, captured once in a CUDA graph and
     replayed (the benchmark's own compression reads the plan sizes back between allocation and
     pack)."""
+    import torch
     from mixed_bit_kv_gb300 import rdkv
     q, k, v = layer_inputs
     comp = rdkv.Compressor(shape, avg, avg, cap_c, dev)
@@ -552,8 +656,12 @@ def run_graph_compress(w, shape, layer_inputs, avg, cap_c, dev, reps=3):
 
 
 def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev):
-    """Same metric through the public API with pinned host inputs: every step copies the
-    prefill inputs and every decode step's inputs host->device and reads each output back."""
+    """The whole step end to end through the public API with pinned host buffers: every layer's
+    prefill inputs copied host->device, scored, allocated, its plan sizes read back, packed; then
+    every decode step's q, k, v copied host->device, the fused append + attend of every layer, and
+    the step's outputs copied device->host.  Wall time per step (median); the value is the same
+    metric as the line's (decode algorithmic bytes per second), over the whole step's time."""
+    import torch
     from mixed_bit_kv_gb300 import rdkv
 
     h_pre = [tuple(t.cpu().pin_memory() for t in trip) for trip in pre]
@@ -596,71 +704,193 @@ def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, de
     step_compress()
     g.replay()
     torch.cuda.synchronize()
-    steps = max(1, min(args.steps, 2))
-    t_dec = 0.0
+    steps = max(1, min(args.steps, 3))
+    times, t_dec = [], []
     for _ in range(steps):
-        step_compress()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
+        step_compress()
+        t1 = time.perf_counter()
         g.replay()
         torch.cuda.synchronize()
-        t_dec += time.perf_counter() - t0
+        t2 = time.perf_counter()
+        times.append(t2 - t0)
+        t_dec.append(t2 - t1)   # the decode phase, from its launch (the compress phase may still run on the GPU)
     h2d = sum(t.numel() * t.element_size() for trip in h_pre for t in trip) + \
         sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv))
-    d2h = h_out.numel() * 4 + L * 96
-    return {"value": round(ws * dec_bytes / (t_dec / steps) / 1e9, 2), "unit": UNIT,
+    d2h = h_out.numel() * 4 + L * 96   # outputs, plus the plan totals each rdkv_plan_sizes reads back
+    step_s = median(times)
+    del h_pre, d_pre, caches, score_out, alloc_out, g
+    return {"value": round(ws * dec_bytes / step_s / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "note": "decode phase wall time incl. per-decode-step H2D of q/k/v and D2H of outputs; "
-                    "the prefill H2D copies run in the compress phase of the same step"}
+            "step_ms": round(step_s * 1e3, 2),
+            "note": "whole step, median wall time: per layer the prefill inputs' H2D, score, allocate, plan sizes "
+                    "(read back), pack; then per decode step the H2D of q/k/v, every layer's fused append + "
+                    "attend and the D2H of the outputs; value = decode algorithmic bytes / step time"}
 
 
 # ---------------------------------------------------------------- CPU oracle (baseline and reference arm)
-def oracle_sample(w, avg, n_tokens, layers_sample=1, decode_calls=2):
-    """Times the CPU oracle's decode (unpack + float64 attention) on a reduced-length
-    sample of the workload; returns (GB/s of algorithmic decode bytes, cores used, description)."""
+ORACLE_SAMPLE_TOKENS = {"tiny": 512, "llama3b": 2048, "llama8b": 2048, "qwen72b": 2048, "batched": 2048}
+
+
+def _oracle_job(job):
+    """One oracle call in a worker process (one thread): returns its seconds."""
+    import oracle as O
+    kind, a = job
+    t0 = time.perf_counter()
+    if kind == "score":
+        O.score(a["q"], a["k"], a["v"], a["window"])
+    elif kind == "allocate":
+        O.allocate(a["g_tok"], a["w_chan"], a["k"], a["avg"], a["avg"])
+    elif kind == "pack":
+        O.pack(a["k"], a["v"], a["bits_tok"], a["bits_chan"], a["window"], cap_c=a["cap_c"])
+    elif kind == "decode":
+        O.decode(a["cache"], a["q"])
+    return time.perf_counter() - t0
+
+
+def _oracle_setup(name, n_tokens):
+    """A bounded sample of a workload for the oracle: one sequence, one layer, N = n_tokens; its
+    weights, allocation and pack by the oracle (untimed), and the jobs of each step with their
+    units of work."""
     import oracle as O
     from mixed_bit_kv_gb300 import synth
-    ws_ = w.scaled(n_tokens=n_tokens, batch=1)
-    q, k, v = (t.numpy() for t in synth.prefill(ws_, 0, 0))
-    sc = O.score(q, k, v, ws_.window)
+    w = synth.WORKLOADS[name].scaled(n_tokens=n_tokens, batch=1)
+    avg = w.budgets[0]
+    q, k, v = (t.numpy() for t in synth.prefill(w, 0, 0))
+    sc = O.score(q, k, v, w.window)
     al = O.allocate(sc["g_tok"], sc["w_chan"], k, avg, avg)
-    cache = O.pack(k[None], v[None], al["bits_tok"][None], al["bits_chan"][None], ws_.window,
-                   cap_c=ws_.window + decode_calls)
-    qn, kn, vn = (t.numpy() for t in synth.decode_step(ws_, 0))
+    cache = O.pack(k[None], v[None], al["bits_tok"][None], al["bits_chan"][None], w.window, cap_c=w.window + 1)
+    qn, kn, vn = (t.numpy() for t in synth.decode_step(w, 0))
     O.append(cache, kn, vn)
-    r0 = resource.getrusage(resource.RUSAGE_SELF)
-    t0 = time.perf_counter()
-    nbytes = 0.0
-    for _ in range(decode_calls):
-        O.decode(cache, qn)
-        nbytes += O.decode_bytes(cache["plan"], ws_.head_dim, ws_.h_q, ws_.h_kv, cache["len_c"], 1)
-    dt = time.perf_counter() - t0
-    r1 = resource.getrusage(resource.RUSAGE_SELF)
-    cpu = (r1.ru_utime - r0.ru_utime) + (r1.ru_stime - r0.ru_stime)
-    cores = max(1, int(round(cpu / dt)))
-    desc = (f"oracle decode (unpack + float64 attention) of one {w.name}-shaped layer at N={n_tokens} "
-            f"(full workload N={w.n_tokens}), {decode_calls} calls, {dt:.1f} s")
-    return nbytes / dt / 1e9, cores, desc
+    P = 2 if w.dtype == "f16" else 4
+    plan = cache["plan"]
+    pack_bytes = (2 * plan["kept_tokens"] * w.head_dim * P + 2 * w.h_kv * w.window * w.head_dim * (P + 2)
+                  + plan["zone_a_bytes"] + plan["zone_b_rows"] * w.head_dim * 2 + plan["index_slots"] * 4)
+    jobs = {
+        "score": (("score", dict(q=q, k=k, v=v, window=w.window)), scorer_flops(w), "flop"),
+        "allocate": (("allocate", dict(g_tok=sc["g_tok"], w_chan=sc["w_chan"], k=k, avg=avg)), 1, "call"),
+        "pack": (("pack", dict(k=k[None], v=v[None], bits_tok=al["bits_tok"][None], bits_chan=al["bits_chan"][None],
+                               window=w.window, cap_c=w.window + 1)), pack_bytes, "byte"),
+        "decode": (("decode", dict(cache=cache, q=qn)),
+                   O.decode_bytes(plan, w.head_dim, w.h_q, w.h_kv, cache["len_c"], 1), "byte"),
+    }
+    return w, jobs
+
+
+def _spawn_pool(n):
+    """A pool of n single-threaded worker processes, started with spawn (safe after CUDA use)."""
+    import multiprocessing as mp
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        pool = mp.get_context("spawn").Pool(n)
+        pool.map(math.sqrt, range(n))   # workers up before anything is timed
+    finally:
+        for k, val in saved.items():
+            if val is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = val
+    return pool
+
+
+def oracle_baseline(headline):
+    """The oracle as it stands, timed on this host's cores: each step on one core (one worker, one
+    thread) and on all cores (one single-threaded worker per core, each running the same call),
+    on bounded samples of the workloads (one sequence, one layer, reduced N).  Steps: decode,
+    allocate and pack on the 3B-shaped layer and the headline workload, the scorer on the tiny,
+    3B- and 8B-shaped layers.  Returns the cpu_baseline object (value: headline decode GB/s on all
+    cores)."""
+    nproc = os.cpu_count() or 1
+    t_all0 = time.perf_counter()
+    plan = [("decode", "llama3b"), ("allocate", "llama3b"), ("pack", "llama3b"),
+            ("score", "tiny"), ("score", "llama3b"), ("score", "llama8b")]
+    if headline not in ("llama3b",):
+        plan = [("decode", headline), ("allocate", headline), ("pack", headline)] + plan
+    setups = {}
+    for _, name in plan:
+        if name not in setups:
+            setups[name] = _oracle_setup(name, ORACLE_SAMPLE_TOKENS.get(name, 2048))
+    steps = {}
+    one = _spawn_pool(1)
+    try:
+        for kind, name in plan:
+            job, units, unit = setups[name][1][kind]
+            steps.setdefault(kind, {})[name] = {"one_core_s": one.map(_oracle_job, [job])[0]}
+    finally:
+        one.close()
+        one.join()
+    allp = _spawn_pool(nproc)
+    try:
+        for kind, name in plan:
+            job, units, unit = setups[name][1][kind]
+            t0 = time.perf_counter()
+            allp.map(_oracle_job, [job] * nproc, chunksize=1)
+            steps[kind][name]["all_cores_s"] = time.perf_counter() - t0
+    finally:
+        allp.close()
+        allp.join()
+    for kind, name in plan:
+        w, jobs = setups[name]
+        _, units, unit = jobs[kind]
+        r = steps[kind][name]
+        r["sample"] = f"one sequence, one layer, N={w.n_tokens} (workload N={ORACLE_FULL_N[name]})"
+        if unit == "byte":
+            r["one_core_gbs"] = units / r["one_core_s"] / 1e9
+            r["all_cores_gbs"] = nproc * units / r["all_cores_s"] / 1e9
+        elif unit == "flop":
+            r["one_core_gflops"] = units / r["one_core_s"] / 1e9
+            r["all_cores_gflops"] = nproc * units / r["all_cores_s"] / 1e9
+        else:
+            r["one_core_us_per_call"] = r["one_core_s"] * 1e6
+            r["all_cores_calls_per_s"] = nproc / r["all_cores_s"]
+    head = steps["decode"][headline]
+    return {"value": head["all_cores_gbs"], "unit": UNIT, "cores": nproc, "kind": "oracle",
+            "one_core_value": head["one_core_gbs"],
+            "sample": (f"oracle decode (unpack + float64 attention) of one {headline}-shaped layer at "
+                       f"N={setups[headline][0].n_tokens}; value on all {nproc} cores ({nproc} single-threaded "
+                       f"workers, each one call), one_core_value on one; steps below: one core and all cores"),
+            "steps": steps, "wall_s": round(time.perf_counter() - t_all0, 1)}
+
+
+ORACLE_FULL_N = {"tiny": 512, "llama3b": 32768, "llama8b": 131072, "qwen72b": 262144, "batched": 32768}
 
 
 def run_reference(args):
-    from mixed_bit_kv_gb300 import synth
-    w = synth.WORKLOADS[args.workload]
-    avg = w.budgets[0] if args.budget is None else args.budget
-    n = min(w.n_tokens, args.oracle_tokens)
-    vals, t_all = [], time.perf_counter()
-    for _ in range(args.warmup + args.steps):
-        gbs, cores, desc = oracle_sample(w, avg, n, decode_calls=1)
-        vals.append(gbs)
-    value = float(np.mean(vals[args.warmup:]))
+    """The reference arm: the CPU oracle's decode on a bounded sample of the workload (one
+    sequence, one layer, reduced N), on all host cores (one single-threaded worker per core, each
+    one decode call per step)."""
+    name = args.workload
+    nproc = os.cpu_count() or 1
+    t_all = time.perf_counter()
+    w, jobs = _oracle_setup(name, ORACLE_SAMPLE_TOKENS.get(name, 2048))
+    job, units, _ = jobs["decode"]
+    pool = _spawn_pool(nproc)
+    vals, secs = [], []
+    try:
+        for _ in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            pool.map(_oracle_job, [job] * nproc, chunksize=1)
+            dt = time.perf_counter() - t0
+            secs.append(dt)
+            vals.append(nproc * units / dt / 1e9)
+    finally:
+        pool.close()
+        pool.join()
+    value = median(vals[args.warmup:])
+    desc = (f"oracle decode (unpack + float64 attention) of one {name}-shaped layer at N={w.n_tokens} "
+            f"(workload N={ORACLE_FULL_N[name]}); {nproc} single-threaded workers, one call each per step")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round((time.perf_counter() - t_all) * 1e3 / (args.warmup + args.steps), 1),
+            "ms_per_step": round(median(secs[args.warmup:]) * 1e3, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded generator)", "config": {"workload": w.name, "avg_bits": avg,
-                                                               "oracle_tokens": n},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "data": "synthetic (seeded generator)",
+            "config": {"workload": name, "avg_bits": w.budgets[0], "oracle_tokens": w.n_tokens},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nproc, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.perf_counter() - t_all, 1)}
 
 
 def main():
@@ -669,15 +899,15 @@ def main():
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama3b")
-    ap.add_argument("--layers", type=int, default=28)
+    ap.add_argument("--workload", default="qwen72b")
+    ap.add_argument("--layers", type=int, default=None, help="layers of the stack (default: per workload)")
     ap.add_argument("--decode-steps", type=int, default=None)
     ap.add_argument("--budget", type=float, default=None)
-    ap.add_argument("--oracle-tokens", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-comparator", action="store_true", help="skip the fp16 full-cache SDPA context number")
     ap.add_argument("--no-recompress", action="store_true", help="skip the zone-C re-compression and paged zone-C measurements")
+    ap.add_argument("--no-extras", action="store_true", help="skip the decode measurements of the other workloads")
     args = ap.parse_args()
     ws, rank, local = dist_env()
 
@@ -686,6 +916,7 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
 
+    import torch
     if ws > 1:
         torch.distributed.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -697,11 +928,7 @@ def main():
     line = run_ours(args, ws, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
-            from mixed_bit_kv_gb300 import synth
-            w = synth.WORKLOADS[args.workload]
-            avg = w.budgets[0] if args.budget is None else args.budget
-            gbs, cores, desc = oracle_sample(w, avg, min(w.n_tokens, args.oracle_tokens))
-            line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+            line["cpu_baseline"] = oracle_baseline(args.workload)
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()

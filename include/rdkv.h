@@ -350,12 +350,17 @@ rdkv_status rdkv_decode_timeout_selftest(const rdkv_cache* cache, const void* q,
  *     than 4 MiB of scratch (rdkv_decode_workspace_bytes tells how much).
  *   - The first call on a device looks up the array's device address (and
  *     raises the kernel's shared-memory limit); make that first call before
- *     any stream capture.
+ *     any stream capture.  The lookup is cached per device for the CUDA
+ *     runtime's primary context of that device (the context every call of
+ *     this library runs in); host threads may make their first calls at the
+ *     same time.
  *   - All calls share the one array and each clears the counters it needs, so
  *     calls that overlap on the GPU (other streams, other threads) race and
  *     must be serialised by the caller.
- *   - The status word of a call lives in that shared array and is not exposed;
- *     callers that need the timeout report use rdkv_decode_attn. */
+ *   - The status word of a call lives in that shared array and is not exposed:
+ *     if a bounded wait for a tile copy runs out inside this call, nothing
+ *     reports it, the call still returns RDKV_OK and its output is undefined.
+ *     Callers that need the timeout report use rdkv_decode_attn. */
 rdkv_status rdkv_decode_attn_noalloc(const rdkv_cache* cache, const void* q, float* out, void* stream);
 
 /* ---------------------------------------------------------------- zone-C re-compression

@@ -30,6 +30,8 @@
 // scales enter through the other operand.  The softmax runs in fp32 on the
 // S^T accumulators (base-2 exponent); P^T is moved into B-fragment order by
 // movmatrix.  The G query heads of a group share every loaded tile.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace rdkv {
@@ -1332,8 +1334,9 @@ static DecodeParams decode_params(const rdkv_cache* cache, const DecodeGeom& geo
 // it reads the query, the new token or zone C.
 static rdkv_status launch_decode(const DecodeParams& P, const DecodeGeom& geo, const rdkv_shape& s, cudaStream_t cs,
                                  bool pdl) {
-  // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is captured)
-  static size_t smem_set[6][64] = {};
+  // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is
+  // captured); threads that get here together may both raise it, to the same value
+  static std::atomic<size_t> smem_set[6][64];
   int dev = 0;
   RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
   const bool qlo = s.dtype == RDKV_F32;
@@ -1346,11 +1349,11 @@ static rdkv_status launch_decode(const DecodeParams& P, const DecodeGeom& geo, c
                                  : ki == 1 ? decode_kernel<64, true, false>
                                  : ki == 2 ? decode_kernel<64, false, true>
                                            : decode_kernel<64, false, false>;
-  if (dev < 64 && geo.smem > smem_set[ki][dev]) {
+  if (dev < 64 && geo.smem > smem_set[ki][dev].load(std::memory_order_acquire)) {
     RDKV_TRY_CUDA(cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kDecodeSmemLimit),
                   "decode smem");
-    smem_set[ki][dev] = (size_t)kDecodeSmemLimit;
+    smem_set[ki][dev].store((size_t)kDecodeSmemLimit, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(geo.splits);
@@ -1527,18 +1530,22 @@ constexpr size_t kNoAllocScratchBytes = 4u << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch array for the current device, looked up once per
-// device.  The array's name is only a host-side stand-in in host code.
+// device (in the CUDA runtime's primary context of that device, the one every
+// entry point of this library runs in).  The array's name is only a host-side
+// stand-in in host code.  Threads making their first call at the same time may
+// each look the address up; they store the same value into an atomic slot, so
+// the cache itself never races.
 static rdkv_status noalloc_scratch(void** out) {
-  static void* addr[64] = {};
+  static std::atomic<void*> addr[64];
   int dev = 0;
   RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
   RDKV_REQUIRE(dev >= 0 && dev < 64, RDKV_ERR_UNSUPPORTED, "device index %d", dev);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
+  void* p = addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
     RDKV_TRY_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch), "scratch address");
-    addr[dev] = p;
+    addr[dev].store(p, std::memory_order_release);
   }
-  *out = addr[dev];
+  *out = p;
   return RDKV_OK;
 }
 }  // namespace rdkv

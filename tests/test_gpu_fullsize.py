@@ -57,6 +57,18 @@ def _check_weights(w, q, k, v, sc, b, tail_rows):
     assert _rel(sc["sigma_tok"][b].cpu().numpy(), O.value_spread(vb)).max() <= 1e-3
 
 
+def _check_interior_columns(w, q, k, sc, b, j, t0, width):
+    """w_t of KV head j for the interior columns [t0, t0 + width), element by element: those
+    columns receive attention only from rows tau >= t0, so the oracle over those rows of the
+    group's G query heads (each row normalised over all its keys) is exact for them."""
+    G = w.group
+    qb = q[b, :, j * G:(j + 1) * G].float().cpu().numpy()
+    kb = k[b, :, j:j + 1].float().cpu().numpy()
+    ref = O.token_weights(qb, kb, first_row=t0)[0, t0:t0 + width]
+    got = sc["w_tok"][b, j, t0:t0 + width].cpu().numpy()
+    assert _rel(got, ref).max() <= 1e-3, (j, t0, _rel(got, ref).max())
+
+
 def _check_alloc_and_plan(w, k, sc, al, avg, seqs):
     g_tok = sc["g_tok"].cpu().numpy()
     bits_tok = al["bits_tok"].cpu().numpy()
@@ -110,6 +122,9 @@ def test_llama3b_layer_full_size():
     steps = 3
     (q, k, v), shape, sc, al, sizes, cache = _compress(w, w.budgets[0], steps)
     _check_weights(w, q, k, v, sc, 0, tail_rows=16)
+    # a block of 64 interior columns of one KV head at N/2: 64 key tiles of 256 precede it and 128
+    # query blocks of 128 rows contribute to it
+    _check_interior_columns(w, q, k, sc, 0, 5, w.n_tokens // 2, 64)
     bits_tok, bits_chan, heads = _check_alloc_and_plan(w, k, sc, al, w.budgets[0], seqs=[0])
     ref, a0, a1 = _oracle_cache(w, k, v, bits_tok, bits_chan, 0, heads[: w.h_kv], w.window + steps)
     un = _check_pack_and_decode(w, cache, ref, a0, a1, 0, steps)
@@ -264,3 +279,15 @@ def test_llama3b_layer_recompression_full_size():
     exp, exp_lse = O.merge_attention(np.stack([o1, o2]), np.stack([l1, l2]))
     assert np.abs(out.cpu().numpy()[:, j * G:(j + 1) * G] - exp).max() <= 2e-3
     assert np.abs(lse.cpu().numpy()[:, j * G:(j + 1) * G] - exp_lse).max() <= 2e-3
+
+
+def test_early_columns_token_weights():
+    """w_t of the early columns [256, 320) of one KV head on a 3B-shaped layer of N = 8192, element
+    by element against the oracle over the rows tau >= 256 (exact for those columns): the 62
+    query blocks of 128 rows from row 256 on contribute to every one of its columns."""
+    w = synth.WORKLOADS["llama3b"].scaled(n_tokens=8192)
+    q, k, v = synth.prefill_batch(w, device=DEV)
+    shape = rdkv.shape_of(q, k, w.window)
+    sc = rdkv.rdkv_score(shape, q, k, v)
+    torch.cuda.synchronize()
+    _check_interior_columns(w, q, k, sc, 0, 2, 256, 64)

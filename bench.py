@@ -158,15 +158,15 @@ def pack_bytes_per_layer(w, sizes):
 
 
 def decode_bytes_per_call(heads, D, h_q, batch, len_c):
-    """Bytes one decode call must move: zone-A payload and metadata of real tokens
-    and channels, zone-B rows of real tokens, len_c zone-C rows per head, q in and
-    out.  Padding excluded."""
+    """Bytes one decode call must move: zone-A payload of real tokens and channels with the K
+    metadata of each head's quantised channels (once per head) and the V metadata of each token,
+    zone-B rows of real tokens, len_c zone-C rows per head, q in and out.  Padding excluded."""
     total = 0.0
     for hp in heads:
         n16k, n8k, n4k, n2k, _ = (int(x) for x in hp["n_k"])
         ntok = int(np.sum(hp["n_v"]))
         kq = n8k + n4k + n2k
-        total += ntok * (2 * n16k + (8 * n8k + 4 * n4k + 2 * n2k) / 8) + 4 * kq * ntok / 32
+        total += ntok * (2 * n16k + (8 * n8k + 4 * n4k + 2 * n2k) / 8) + (4 * kq if ntok else 0)
         for n, b in zip(hp["n_v"], (2, 4, 8, 16)):
             total += int(n) * (D * b / 8 + (4 * D / 32 if b < 16 else 0))
         total += len_c * 4 * D

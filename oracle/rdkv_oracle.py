@@ -37,7 +37,8 @@ Readings where the pages are silent (each is a project decision):
     B = floor(avg_bits * units); slack left unused.
  R5 At a breakpoint the cheaper width wins (strict >); g = 0 gives 0 bits.
  R6 Quantiser groups: 32 consecutive channels of a V row; for K, one channel
-    over the real tokens of a 32-token tile.  fp16 scale and zero.
+    over every kept prefix token of its (sequence, KV head): the per-channel K
+    groups the quantiser statement names.  fp16 scale and zero.
  R7 16-bit K channels are stored raw in fp16 inside zone A; 0-bit K channels
     are dropped and contribute nothing to the logits.
  R8 Byte layout of the zones: see ``pack``.
@@ -283,33 +284,70 @@ def threshold_keep(w, tau):
 # ---------------------------------------------------------------------------
 # TriZone plan and pack (RDKV section 2.3; layout R8)
 # ---------------------------------------------------------------------------
+KB = 16                                                  # K slots of one k-block
+
+
 def _ceil_div(a, b):
     return -(-a // b)
 
 
+def k_slot_in_block(b, i, e):
+    """Slot, inside its 16-slot k-block, of element e of the block's word i at K width b
+    (project layout; the page fixes no order).  The slots of a block are read in four
+    lanes q = 0..3, lane q taking slots 2q, 2q+1 and 2q+8, 2q+9:
+      b = 16: word i (of 8) holds slots 2i, 2i+1;
+      b = 8:  word i (of 4) holds lane i's slots: 2i, 2i+1 (elements 0, 1) and 2i+8, 2i+9 (2, 3);
+      b = 4:  word i (of 2) holds lane 2i's slots (elements 0-3) then lane 2i+1's (4-7),
+              each lane's in the order 2q, 2q+1, 2q+8, 2q+9;
+      b = 2:  the block's one word holds slots 0..15 in element order."""
+    if b == 16:
+        return 2 * i + e
+    if b == 8:
+        return 2 * i + (e % 2) + 8 * (e // 2)
+    if b == 4:
+        q = 2 * i + e // 4
+        return 2 * q + (e % 2) + 8 * ((e // 2) % 2)
+    return e
+
+
 def head_plan(bits_tok_j, bits_chan_j, head_dim):
-    """Counts, sizes and orders of one (sequence, KV head)."""
+    """Counts, sizes and orders of one (sequence, KV head).
+
+    K segments (widths 16, 8, 4, 2) hold the channels of their width in ascending
+    order, packed into k_words[i] = ceil(n * b / 32) words per token; a segment's
+    slot range is whole 16-slot k-blocks (k_blocks[i] of them), the channel of rank
+    r going to element r mod (32/b) of word r div (32/b), whose slot follows
+    ``k_slot_in_block``; every other slot of the range is a pad (-1).  The K
+    quantiser parameters of the 8/4/2-bit slots (meta_slots of them) sit once per
+    head in front of its tiles (meta_bytes); a tile holds K codes and, for V width
+    b < 16, V codes and V metadata."""
     D = head_dim
     n_v = [int((bits_tok_j == b).sum()) for b in V_CLASSES]
     tiles = [_ceil_div(n, TILE) for n in n_v]
     n_k = [int((bits_chan_j == b).sum()) for b in K_CLASSES]
     k_words = [_ceil_div(n * b, 32) for n, b in zip(n_k, K_CLASSES)]
+    k_blocks = [_ceil_div(w * (32 // b), KB) for w, b in zip(k_words, K_CLASSES)]
     row_words = sum(k_words)
-    k_slots = sum(w * (32 // b) for w, b in zip(k_words, K_CLASSES))
-    meta_slots = sum(w * (32 // b) for w, b in zip(k_words, K_CLASSES) if b < 16)
-    tile_bytes = [4 * TILE * row_words + 4 * meta_slots + ((TILE * D * b) // 8 + 4 * D if b < 16 else 0)
-                  for b in V_CLASSES]
+    k_slots = KB * sum(k_blocks)
+    meta_slots = KB * sum(nb for nb, b in zip(k_blocks, K_CLASSES) if b < 16)
+    meta_bytes = 16 * _ceil_div(4 * meta_slots, 16)
+    tile_bytes = [4 * TILE * row_words + ((TILE * D * b) // 8 + 4 * D if b < 16 else 0) for b in V_CLASSES]
     slots = []
-    for (b, w) in zip(K_CLASSES, k_words):
-        ch = np.nonzero(bits_chan_j == b)[0].tolist()
-        slots += ch + [-1] * (w * (32 // b) - len(ch))
+    for b, nb in zip(K_CLASSES, k_blocks):
+        seg = [-1] * (KB * nb)
+        per, wpk = 32 // b, b // 2                       # elements per word, words per k-block
+        for r, ch in enumerate(np.nonzero(bits_chan_j == b)[0].tolist()):
+            wg, e = divmod(r, per)
+            seg[KB * (wg // wpk) + k_slot_in_block(b, wg % wpk, e)] = ch
+        slots += seg
     tokens = []
     for b, nt in zip(V_CLASSES, tiles):
         t = np.nonzero(bits_tok_j == b)[0].tolist()
         tokens.append(np.array(t + [-1] * (nt * TILE - len(t)), dtype=np.int64))
-    return dict(n_v=n_v, tiles=tiles, n_k=n_k + [D - sum(n_k)], k_words=k_words, row_words=row_words,
-                k_slots=k_slots, meta_slots=meta_slots, tile_bytes=tile_bytes,
-                a_bytes=sum(nt * tb for nt, tb in zip(tiles, tile_bytes)),
+    return dict(n_v=n_v, tiles=tiles, n_k=n_k + [D - sum(n_k)], k_words=k_words, k_blocks=k_blocks,
+                row_words=row_words, k_slots=k_slots, meta_slots=meta_slots, meta_bytes=meta_bytes,
+                tile_bytes=tile_bytes,
+                a_bytes=meta_bytes + sum(nt * tb for nt, tb in zip(tiles, tile_bytes)),
                 slots=np.array(slots, dtype=np.int64), tokens=tokens)
 
 
@@ -367,15 +405,36 @@ def k_word_position(t, w):
     return 32 * w + 4 * (t % 8) + t // 8
 
 
-def v_word_position(w, b, head_dim):
-    """Index, among the D*b/16 V words of one token pair, of the word that holds
-    channels [w*16/b, (w+1)*16/b): with R = b/2 the words are grouped by w mod R
-    (group r first holds words r, r+R, r+2R, ...), so the words whose channels
-    are congruent mod 8 to one value are adjacent.  R = 1 (b = 2) keeps the
-    natural order.  (Project layout.)"""
-    wpp = head_dim * b // 16
-    R = b // 2
-    return (w % R) * (wpp // R) + w // R
+def v_code_position(p, c, b, head_dim):
+    """(word index among a tile's D*b V code words, bit offset) of channel c of token pair p
+    (tokens 2p and 2p+1; the odd token's code sits 16 bits above the even one's).  Project
+    layout, made for the decode's fragments:
+      * pair p = 8 tb + q + 4 h (tb = 16-token block, q = lane of the pair, h = which of the
+        lane's two pairs); channel c = 16 cm + 8 s + g (g = lane row, s = which of its two
+        row sets); the lane's channel list is k = s * D/16 + cm;
+      * lane (g, q) of block tb owns 2 * nw consecutive words (nw = D*b/128), pair h's nw words
+        after pair 0's, at ((tb*8 + g)*4 + q) * 2nw + h nw;
+      * channel k sits in word k div (16/b) of its pair, at bit b * (k mod (16/b))."""
+    D = head_dim
+    CM, nw, per = D // 16, D * b // 128, 16 // b
+    tb, r = divmod(p, 8)
+    q, h = r % 4, r // 4
+    cm, rr = divmod(c, 16)
+    s, g = divmod(rr, 8)
+    k = s * CM + cm
+    wk, e = divmod(k, per)
+    return ((tb * 8 + g) * 4 + q) * 2 * nw + h * nw + wk, b * e
+
+
+def v_meta_position(p, grp, head_dim):
+    """(index of the 32-bit scale pair, index of the 32-bit zero pair) of token pair p and
+    32-channel group grp among a tile's 32*D/32 metadata words; each pair holds the even
+    token's fp16 in its low half.  Scales first, ordered (tb, q, h, group), so a lane reads
+    every group's scales of its two pairs at once; then zeros, ordered (tb, group, q, h)."""
+    NG = head_dim // GROUP
+    tb, r = divmod(p, 8)
+    q, h = r % 4, r // 4
+    return ((tb * 4 + q) * 2 + h) * NG + grp, 16 * NG + ((tb * NG + grp) * 4 + q) * 2 + h
 
 
 def _k_positions(row_words):
@@ -384,96 +443,130 @@ def _k_positions(row_words):
     return k_word_position(t, w)                   # [32, row_words]
 
 
-def _v_positions(b, head_dim):
-    return np.array([v_word_position(w, b, head_dim) for w in range(head_dim * b // 16)], dtype=np.int64)
-
-
 def _halves_bits(a):
     return np.asarray(a, dtype=np.float16).view(np.uint16).astype(np.uint32)
 
 
-def _pack_words(codes, b, per_word, first_off_fn):
-    """Sum codes (uint64 [..., n]) shifted to their bit offsets into words [..., n // per_word]."""
-    n = codes.shape[-1]
-    shifts = np.array([first_off_fn(e) for e in range(n)], dtype=np.uint64)
-    return (codes.astype(np.uint64) << shifts).reshape(*codes.shape[:-1], n // per_word, per_word).sum(axis=-1)
-
-
 def _k_segments(hp):
-    """(width, first word, words, first meta slot, slot list) of each K segment, in row order."""
+    """(width, first word, words, first slot, slot list) of each K segment, in row order."""
     seg = []
-    w0 = m0 = s0 = 0
-    for b, nw in zip(K_CLASSES, hp["k_words"]):
-        ns = nw * (32 // b)
-        seg.append((b, w0, nw, m0, hp["slots"][s0:s0 + ns]))
+    w0 = s0 = 0
+    for b, nw, nb in zip(K_CLASSES, hp["k_words"], hp["k_blocks"]):
+        ns = KB * nb
+        seg.append((b, w0, nw, s0, hp["slots"][s0:s0 + ns]))
         w0 += nw
         s0 += ns
-        if b < 16:
-            m0 += ns
     return seg
+
+
+def _k_word_slots(b, nw):
+    """[nw, 32 // b]: the segment slot that element e of the segment's word w holds."""
+    per, wpk = 32 // b, b // 2
+    return np.array([[KB * (w // wpk) + k_slot_in_block(b, w % wpk, e) for e in range(per)] for w in range(nw)],
+                    dtype=np.int64).reshape(nw, per)
+
+
+def _v_tables(b, head_dim):
+    """Word index and bit offset of every (pair, channel) of a V tile: [16, D] each."""
+    pos = [[v_code_position(p, c, b, head_dim) for c in range(head_dim)] for p in range(TILE // 2)]
+    return (np.array([[x[0] for x in row] for row in pos], dtype=np.int64),
+            np.array([[x[1] for x in row] for row in pos], dtype=np.uint64))
+
+
+def _v_meta_tables(head_dim):
+    NG = head_dim // GROUP
+    sidx = np.array([[v_meta_position(p, g, head_dim)[0] for g in range(NG)] for p in range(TILE // 2)])
+    zidx = np.array([[v_meta_position(p, g, head_dim)[1] for g in range(NG)] for p in range(TILE // 2)])
+    return sidx, zidx
+
+
+def k_head_quantizer(k_j, hp):
+    """Per quantised slot of the head (slot order, pads 0): fp16 scale and zero of its channel over
+    every kept prefix token of the head (R6: one K group per channel of the head)."""
+    kept = np.sort(np.concatenate([t[t >= 0] for t in hp["tokens"]])) if hp["tokens"] else np.zeros(0, np.int64)
+    QS = hp["meta_slots"]
+    s_q0 = hp["k_slots"] - QS                      # first slot of the 8-bit segment
+    ksc = np.zeros(QS, np.float16)
+    kze = np.zeros(QS, np.float16)
+    for b, _, _, s0, slots in _k_segments(hp):
+        if b == 16:
+            continue
+        for s in np.nonzero(slots >= 0)[0]:
+            m = s0 + s - s_q0
+            if kept.size:
+                _, sc, ze = quantize_groups(k_j[kept, slots[s]], b)
+                ksc[m], kze[m] = sc, ze
+    return ksc, kze
 
 
 def pack_head(k_j, v_j, hp, head_dim):
     """Zone-A bytes and zone-B rows of one (sequence, KV head).
 
-    k_j, v_j: [N, D] float32 values of that head.  Tile layout (little-endian):
-      K codes   32 rows x row_words uint32 (segments 16, 8, 4, 2 bits, each
-                padded to whole words; a 16-bit slot holds the raw fp16 value),
-                word (t, w) stored at k_word_position(t, w)
-      K meta    per slot pair of the 8/4/2-bit segments: scale(2i), scale(2i+1),
-                zero(2i), zero(2i+1) as fp16
-      V codes   (width b < 16 only) 16 token pairs x D*b/16 uint32; word w of
-                pair p holds channels [w*16/b, (w+1)*16/b): token 2p in the low
-                half, token 2p+1 in the high half, LSB-first; stored pair by pair,
-                word w of a pair at v_word_position(w, b, D)
-      V meta    (b < 16 only) per token pair and 32-channel group: scale(2p),
-                scale(2p+1), zero(2p), zero(2p+1) as fp16
+    k_j, v_j: [N, D] float32 values of that head.  Layout (little-endian):
+      head meta  per quantised K slot (slot order from the first 8-bit slot, pads 0):
+                 fp16 scale, fp16 zero of the channel over all kept prefix tokens of the
+                 head; padded to meta_bytes (whole 16 bytes)
+    then the tiles of each V width in class order:
+      K codes    32 rows x row_words uint32 (segments 16, 8, 4, 2 bits, each padded to whole
+                 words; element e of a word at bit_offset(e, b) holds the slot given by
+                 k_slot_in_block; a 16-bit slot holds the raw fp16 value), word (t, w) stored
+                 at k_word_position(t, w)
+      V codes    (width b < 16 only) D*b words, channel c of token pair p at v_code_position
+      V meta     (b < 16 only) fp16 scale and zero per token and 32-channel group, in pairs of
+                 tokens at v_meta_position
     Pad tokens and pad slots hold code 0, scale 0 and zero 0.
     """
     D = head_dim
     out, zone_b = [], []
     seg = _k_segments(hp)
     RW, QS = hp["row_words"], hp["meta_slots"]
+    s_q0 = hp["k_slots"] - QS
+    ksc, kze = k_head_quantizer(k_j, hp)
+    meta = np.zeros(hp["meta_bytes"] // 2, np.float16)
+    meta[0:2 * QS:2], meta[1:2 * QS:2] = ksc, kze
+    out.append(meta.tobytes())
+    NG = D // GROUP
     for ci, bv in enumerate(V_CLASSES):
         toks = hp["tokens"][ci]
+        if bv < 16 and hp["tiles"][ci]:
+            vword, vbit = _v_tables(bv, D)
+            sidx, zidx = _v_meta_tables(D)
         for ti in range(hp["tiles"][ci]):
             tt = toks[ti * TILE:(ti + 1) * TILE]
             real = tt >= 0
             rows = tt[real]
             kw = np.zeros((TILE, RW), dtype=np.uint64)
-            ksc = np.zeros(QS, dtype=np.float16)
-            kze = np.zeros(QS, dtype=np.float16)
-            for b, wbase, nw, mbase, slots in seg:
+            for b, wbase, nw, s0, slots in seg:
                 if nw == 0:
                     continue
-                per_word = 32 // b
-                sidx = np.nonzero(slots >= 0)[0]
-                X = k_j[np.ix_(rows, slots[sidx])]                     # [real tokens, channels]
-                codes = np.zeros((rows.size, slots.size), dtype=np.uint32)
-                if b == 16:
-                    codes[:, sidx] = _halves_bits(X)
-                else:
-                    c, sc, ze = quantize_groups(X.T, b)                 # one group per channel
-                    codes[:, sidx] = c.T
-                    ksc[mbase + sidx], kze[mbase + sidx] = sc, ze
-                kw[real, wbase:wbase + nw] = _pack_words(codes, b, per_word, lambda e: bit_offset(e % per_word, b))
-            kmeta = np.stack([ksc[0::2], ksc[1::2], kze[0::2], kze[1::2]], axis=1)
+                wslots = _k_word_slots(b, nw)                           # [nw, per]
+                codes = np.zeros((rows.size, slots.size), dtype=np.uint64)
+                for s in np.nonzero(slots >= 0)[0]:
+                    x = k_j[rows, slots[s]]
+                    if b == 16:
+                        codes[:, s] = _halves_bits(x)
+                    else:
+                        m = s0 + s - s_q0
+                        c, _, _ = quantize_groups_with(x, b, ksc[m], kze[m])
+                        codes[:, s] = c
+                shifts = np.array([bit_offset(e, b) for e in range(32 // b)], dtype=np.uint64)
+                words = (codes[:, wslots] << shifts[None, None, :]).sum(axis=2)    # [real, nw]
+                kw[real, wbase:wbase + nw] = words
             kflat = np.zeros(TILE * RW, dtype=np.uint32)
             kflat[_k_positions(RW)] = kw.astype(np.uint32)
-            parts = [kflat.tobytes(), kmeta.astype(np.float16).tobytes()]
+            parts = [kflat.tobytes()]
             if bv < 16:
                 vals = np.zeros((TILE, D), dtype=np.float32)
                 vals[real] = v_j[rows]
-                codes, sc, ze = quantize_groups(vals.reshape(TILE, D // GROUP, GROUP), bv)
-                codes = codes.reshape(TILE, D)
+                codes, sc, ze = quantize_groups(vals.reshape(TILE, NG, GROUP), bv)
+                codes = codes.reshape(TILE, D).astype(np.uint64)
                 codes[~real], sc[~real], ze[~real] = 0, 0, 0
-                per_word = 16 // bv                                    # channels per word
-                words = _pack_words(codes, bv, per_word, lambda c: bv * (c % per_word))
-                vw = words[0::2] + (words[1::2] << np.uint64(16))      # even token low, odd token high
-                vstore = np.zeros(vw.shape, dtype=np.uint32)
-                vstore[:, _v_positions(bv, D)] = vw.astype(np.uint32)
-                vmeta = np.stack([sc[0::2], sc[1::2], ze[0::2], ze[1::2]], axis=2)   # [16, D/32, 4]
-                parts += [vstore.tobytes(), vmeta.astype(np.float16).tobytes()]
+                vw = np.zeros(D * bv, dtype=np.uint64)
+                np.add.at(vw, vword, (codes[0::2] << vbit) + (codes[1::2] << (vbit + np.uint64(16))))
+                vm = np.zeros(2 * 32 * NG, dtype=np.float16)        # 32 * NG 32-bit words as fp16 halves
+                vm[2 * sidx], vm[2 * sidx + 1] = sc[0::2], sc[1::2]
+                vm[2 * zidx], vm[2 * zidx + 1] = ze[0::2], ze[1::2]
+                parts += [vw.astype(np.uint32).tobytes(), vm.tobytes()]
             else:
                 rows16 = np.zeros((TILE, D), dtype=np.float16)
                 rows16[real] = v_j[rows].astype(np.float16)
@@ -483,6 +576,17 @@ def pack_head(k_j, v_j, hp, head_dim):
             out.append(tile)
     zb = np.concatenate(zone_b) if zone_b else np.zeros((0, D), np.float16)
     return b"".join(out), zb
+
+
+def quantize_groups_with(x, b, scale, zero):
+    """Codes of x under given fp16 scale and zero (the quantiser's code rule of
+    ``quantize_groups``: IEEE float32 division, round half to even, clamp; scale 0 -> 0)."""
+    x = np.asarray(x, dtype=np.float32)
+    s32, z32 = np.float32(np.float16(scale)), np.float32(np.float16(zero))
+    if s32 == 0:
+        return np.zeros(x.shape, np.uint32), scale, zero
+    t = (x - z32) / s32
+    return np.clip(np.rint(t), 0, (1 << b) - 1).astype(np.uint32), scale, zero
 
 
 def pack(k, v, bits_tok, bits_chan, window, cap_c=None):
@@ -527,49 +631,60 @@ def append(cache, k_new, v_new):
 # Unpack and decode (RDKV section 2.3: attention over zones A, B and C)
 # ---------------------------------------------------------------------------
 def _field(words, off, b):
-    return (words >> np.uint32(off)) & np.uint32((1 << b) - 1)
+    return (words >> np.uint64(off)) & np.uint64((1 << b) - 1)
 
 
 def unpack_head(zone_a, zone_b, hp, head_dim):
     """Read one head's tiles back: (original positions, K-hat [n, D], V-hat [n, D]) in float64.
     Dequantised value = zero + scale * code; dropped channels read as 0."""
     D = head_dim
+    NG = D // GROUP
     RW, QS = hp["row_words"], hp["meta_slots"]
+    s_q0 = hp["k_slots"] - QS
     seg = _k_segments(hp)
     toks_all, K_all, V_all = [], [], []
     off = hp["a_off"]
+    km = np.frombuffer(zone_a, np.float16, 2 * QS, off).astype(np.float64)
+    ksc, kze = km[0::2], km[1::2]
+    off += hp["meta_bytes"]
     brow = hp["b_row"]
-    r = np.arange(TILE)[:, None]
-    c = np.arange(D)[None, :]
     for ci, bv in enumerate(V_CLASSES):
+        if bv < 16 and hp["tiles"][ci]:
+            vword, vbit = _v_tables(bv, D)
+            sidx, zidx = _v_meta_tables(D)
         for ti in range(hp["tiles"][ci]):
             tt = hp["tokens"][ci][ti * TILE:(ti + 1) * TILE]
             real = tt >= 0
-            kw = np.frombuffer(zone_a, np.uint32, TILE * RW, off)[_k_positions(RW)]   # [32, RW]
+            kw = np.frombuffer(zone_a, np.uint32, TILE * RW, off)[_k_positions(RW)].astype(np.uint64)   # [32, RW]
             p = off + 4 * TILE * RW
-            km = np.frombuffer(zone_a, np.float16, 2 * QS, p).reshape(QS // 2, 4).astype(np.float64)
-            ksc, kze = np.empty(QS), np.empty(QS)
-            ksc[0::2], ksc[1::2], kze[0::2], kze[1::2] = km[:, 0], km[:, 1], km[:, 2], km[:, 3]
-            p += 4 * QS
             Kt = np.zeros((TILE, D))
-            for b, wbase, nw, mbase, slots in seg:
-                per_word = 32 // b
-                for s in np.nonzero(slots >= 0)[0]:
-                    code = _field(kw[:, wbase + s // per_word], bit_offset(s % per_word, b), b)
-                    if b == 16:
-                        Kt[:, slots[s]] = code.astype(np.uint16).view(np.float16).astype(np.float64)
-                    else:
-                        Kt[:, slots[s]] = kze[mbase + s] + ksc[mbase + s] * code.astype(np.float64)
+            for b, wbase, nw, s0, slots in seg:
+                if nw == 0:
+                    continue
+                wslots = _k_word_slots(b, nw)
+                for w in range(nw):
+                    for e in range(32 // b):
+                        s = wslots[w, e]
+                        ch = slots[s]
+                        if ch < 0:
+                            continue
+                        code = _field(kw[:, wbase + w], bit_offset(e, b), b)
+                        if b == 16:
+                            Kt[:, ch] = code.astype(np.uint16).view(np.float16).astype(np.float64)
+                        else:
+                            m = s0 + s - s_q0
+                            Kt[:, ch] = kze[m] + ksc[m] * code.astype(np.float64)
             if bv < 16:
-                per_word = 16 // bv
-                vw = np.frombuffer(zone_a, np.uint32, (TILE // 2) * (D // per_word), p).reshape(TILE // 2, D // per_word)
+                vw = np.frombuffer(zone_a, np.uint32, D * bv, p).astype(np.uint64)
                 p += 4 * vw.size
-                vw = vw[:, _v_positions(bv, D)]
-                vm = np.frombuffer(zone_a, np.float16, (TILE // 2) * (D // GROUP) * 4, p)
-                vm = vm.reshape(TILE // 2, D // GROUP, 4).astype(np.float64)
+                vm = np.frombuffer(zone_a, np.float16, 2 * 32 * NG, p).astype(np.float64)
                 p += 2 * vm.size
-                code = _field(vw[r // 2, c // per_word], 16 * (r % 2) + bv * (c % per_word), bv).astype(np.float64)
-                Vt = vm[r // 2, c // GROUP, 2 + r % 2] + vm[r // 2, c // GROUP, r % 2] * code
+                Vt = np.zeros((TILE, D))
+                for par in range(2):            # even, odd token of each pair
+                    code = _field(vw[vword], vbit + np.uint64(16 * par), bv).astype(np.float64)   # [16, D]
+                    sc = vm[2 * sidx + par]                                                      # [16, NG]
+                    ze = vm[2 * zidx + par]
+                    Vt[par::2] = np.repeat(ze, GROUP, axis=1) + np.repeat(sc, GROUP, axis=1) * code
             else:
                 Vt = zone_b[brow:brow + TILE].astype(np.float64)
                 brow += TILE
@@ -622,8 +737,9 @@ def decode(cache, q, unpacked=None):
 
 def decode_bytes(plan, head_dim, h_q, h_kv, len_c, batch):
     """Algorithmic bytes one decode step must read and write: zone-A payload and
-    metadata of real tokens and real channels, zone-B rows of real tokens,
-    zone-C rows, q (fp16) and out (fp32).  Padding is excluded."""
+    metadata of real tokens and real channels (the K metadata once per head),
+    zone-B rows of real tokens, zone-C rows, q (fp16) and out (fp32).  Padding is
+    excluded."""
     D = head_dim
     total = 0
     for hp in plan["heads"]:
@@ -631,7 +747,7 @@ def decode_bytes(plan, head_dim, h_q, h_kv, len_c, batch):
         kq = n8k + n4k + n2k
         ntok = sum(hp["n_v"])
         k_payload = ntok * (2 * n16k + (8 * n8k + 4 * n4k + 2 * n2k) / 8)
-        k_meta = 4 * kq * ntok / TILE
+        k_meta = 4 * kq if ntok else 0                  # scale and zero per quantised channel, once per head
         v_payload = sum(n * (D * b / 8 + (4 * D / GROUP if b < 16 else 0)) for n, b in zip(hp["n_v"], V_CLASSES))
         total += k_payload + k_meta + v_payload + len_c * 4 * D
     total += batch * h_q * D * (2 + 4)

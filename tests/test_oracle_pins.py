@@ -242,46 +242,100 @@ def test_tile_layout_golden():
     g = json.load(open(os.path.join(GOLDEN, "tile_layout.json")))
     for c in g["k_positions"]:
         assert O.k_word_position(c["t"], c["w"]) == c["pos"], c
-    for c in g["v_positions"]:
-        assert O.v_word_position(c["w"], c["b"], c["D"]) == c["pos"], c
-    # both rules are permutations of the words they place
+    for c in g["k_slots_in_block"]:
+        assert O.k_slot_in_block(c["b"], c["i"], c["e"]) == c["slot"], c
+    for c in g["v_code_positions"]:
+        assert O.v_code_position(c["p"], c["c"], c["b"], c["D"]) == (c["word"], c["bit"]), c
+    for c in g["v_meta_positions"]:
+        assert O.v_meta_position(c["p"], c["grp"], c["D"]) == (c["scale"], c["zero"]), c
+    # every rule is a permutation of what it places
     for rw in (1, 3, 11):
         pos = sorted(O.k_word_position(t, w) for t in range(32) for w in range(rw))
         assert pos == list(range(32 * rw))
+    for b in (16, 8, 4, 2):
+        per = 32 // b
+        assert sorted(O.k_slot_in_block(b, i, e) for i in range(b // 2) for e in range(per)) == list(range(16))
     for b in (2, 4, 8):
         for D in (64, 128):
-            assert sorted(O.v_word_position(w, b, D) for w in range(D * b // 16)) == list(range(D * b // 16))
+            bits = sorted(32 * w + bit for p in range(16) for c in range(D)
+                          for (w, bit) in [O.v_code_position(p, c, b, D)])
+            # each (pair, channel) takes b bits of the low half; together with the odd token's high
+            # half they fill all D*b words exactly once
+            assert len(set(bits)) == 16 * D and max(w for w, _ in (O.v_code_position(p, c, b, D)
+                                                               for p in range(16) for c in range(D))) == D * b - 1
+            assert all(bit % 32 + b <= 16 for bit in bits)
+    for D in (64, 128):
+        NG = D // 32
+        idx = sorted(x for p in range(16) for g in range(NG) for x in O.v_meta_position(p, g, D))
+        assert idx == list(range(32 * NG))
+
+
+def test_plan_sizes_golden():
+    """Hand-worked plans: every size and order field, the slot tables, the offsets of a second head,
+    the batch totals and the decode's byte count."""
+    for case in json.load(open(os.path.join(GOLDEN, "plan_sizes.json")))["cases"]:
+        D, Np = case["head_dim"], case["n_prefix"]
+        H = len(case["bits_chan"])
+        bits_tok = np.zeros((1, H, Np), np.uint8)
+        for j, runs in enumerate(case["bits_tok_runs"]):
+            for a, b_, w in runs:
+                bits_tok[0, j, a:b_] = w
+        bits_chan = np.array(case["bits_chan"], np.uint8)[None]
+        plan = O.make_plan(bits_tok, bits_chan, D)
+        for j, exp in enumerate(case["heads"]):
+            hp = plan["heads"][j]
+            for key, val in exp.items():
+                got = hp[key].tolist() if key == "slots" else hp[key]
+                assert got == val, (case["name"], j, key, got, val)
+        for key, val in case["totals"].items():
+            assert plan[key] == val, (case["name"], key)
+        nb = O.decode_bytes(plan, D, case["h_q"], H, case["len_c"], 1)
+        assert nb == case["decode_bytes"], (case["name"], nb)
 
 
 def test_packed_words_sit_where_the_layout_puts_them():
-    """A word of the packed tile, rebuilt from the quantiser's codes, is found at its layout position."""
+    """A K word and a V word of the packed tile, rebuilt from the quantiser's codes with the layout
+    rules, are found at their positions; the head's K metadata leads its zone-A bytes."""
     w, q, k, v, al, cache = _tiny_cache(3.0, 3.0)
     hp = cache["plan"]["heads"][0]
     za = cache["zone_a"].view(np.uint32)
-    # first tile of the first non-empty 2/4/8-bit class: its first quantised K segment, word 0 of token 9
+    kept = np.sort(np.concatenate([t[t >= 0] for t in hp["tokens"]]))
+    # first tile of the first non-empty 2/4/8-bit class
     ci = next(i for i in range(3) if hp["tiles"][i] > 0)
-    off_words = hp["a_off"] // 4 + sum(hp["tiles"][i] * hp["tile_bytes"][i] for i in range(ci)) // 4
+    off_words = (hp["a_off"] + hp["meta_bytes"] + sum(hp["tiles"][i] * hp["tile_bytes"][i] for i in range(ci))) // 4
     tt = hp["tokens"][ci][:32]
-    # K segments in row order: widths 16, 8, 4, 2, each k_words[i] words of 32 / width slots
+    t = 9 if tt[9] >= 0 else 0
+    # the first word of every quantised K segment of token t: element e holds slot slot_in_block(b, 0, e)
     wbase = sbase = 0
+    s_q0 = hp["k_slots"] - hp["meta_slots"]
+    meta = cache["zone_a"][hp["a_off"]:hp["a_off"] + 4 * hp["meta_slots"]].view(np.float16)
     for b, nw in zip((16, 8, 4, 2), hp["k_words"]):
         if b < 16 and nw > 0:
-            break
+            word = 0
+            for e in range(32 // b):
+                s = sbase + O.k_slot_in_block(b, 0, e)
+                ch = hp["slots"][s]
+                if ch < 0:
+                    continue
+                codes, sc, ze = O.quantize_groups(k[kept, 0, ch].astype(np.float32)[None], b)
+                assert meta[2 * (s - s_q0)] == sc[0] and meta[2 * (s - s_q0) + 1] == ze[0]
+                word |= int(codes[0][np.nonzero(kept == tt[t])[0][0]]) << O.bit_offset(e, b)
+            assert int(za[off_words + O.k_word_position(t, wbase)]) == word, b
         wbase += nw
-        sbase += nw * (32 // b)
-    per = 32 // b
-    slots = hp["slots"][sbase:sbase + per]
-    t = 9 if tt[9] >= 0 else 0
-    rows = tt[tt >= 0]
-    word = 0
-    for e in range(per):
-        ch = slots[e]
-        if ch < 0:
-            continue
-        codes, _, _ = O.quantize_groups(k[rows, 0, ch].astype(np.float32)[None], b)
-        code = int(codes[0][np.nonzero(rows == tt[t])[0][0]])
-        word |= code << O.bit_offset(e, b)
-    assert int(za[off_words + O.k_word_position(t, wbase)]) == word
+        sbase += 16 * hp["k_blocks"][(16, 8, 4, 2).index(b)]
+    # a V word: pair p of the tile, the words of lane (g, q) hold its channels
+    b = (2, 4, 8)[ci]
+    D = w.head_dim
+    vbase = off_words + 32 * hp["row_words"]
+    p = 5
+    codes_even = O.quantize_groups(v[tt[2 * p], 0].reshape(-1, 32), b)[0].ravel()
+    codes_odd = O.quantize_groups(v[tt[2 * p + 1], 0].reshape(-1, 32), b)[0].ravel() if tt[2 * p + 1] >= 0 else None
+    c = 37
+    widx, bit = O.v_code_position(p, c, b, D)
+    word = int(za[vbase + widx])
+    assert (word >> bit) & ((1 << b) - 1) == codes_even[c]
+    if codes_odd is not None:
+        assert (word >> (bit + 16)) & ((1 << b) - 1) == codes_odd[c]
 
 
 def _tiny_cache(avg_v, avg_k, cap_extra=4, seed_w="tiny"):
@@ -307,30 +361,26 @@ def test_pack_unpack_round_trip_matches_quantiser():
         else:
             c, s, z = O.quantize_groups(v[t, 0].reshape(-1, 32), bv)
             np.testing.assert_array_equal(Vh[i], (z.astype(np.float64)[:, None] + s.astype(np.float64)[:, None] * c).ravel())
-    # K: channel c of a tile is quantised over that tile's real tokens
-    for ci, bv in enumerate(O.V_CLASSES):
-        toks = hp["tokens"][ci]
-        for ti in range(hp["tiles"][ci]):
-            tt = toks[ti * 32:(ti + 1) * 32]
-            tt = tt[tt >= 0]
-            rows = np.searchsorted(pos, tt) if np.all(np.diff(pos) > 0) else np.array([np.nonzero(pos == t)[0][0] for t in tt])
-            for c in range(w.head_dim):
-                bk = int(al["bits_chan"][0, c])
-                got = Kh[rows, c]
-                if bk == 0:
-                    assert np.all(got == 0)
-                elif bk == 16:
-                    np.testing.assert_array_equal(got, k[tt, 0, c].astype(np.float16).astype(np.float64))
-                else:
-                    cc, s, z = O.quantize_groups(k[tt, 0, c], bk)
-                    np.testing.assert_array_equal(got, float(z) + float(s) * cc.astype(np.float64))
+    # K: channel c is quantised over every kept prefix token of the head
+    for c in range(w.head_dim):
+        bk = int(al["bits_chan"][0, c])
+        got = Kh[:, c]
+        if bk == 0:
+            assert np.all(got == 0)
+        elif bk == 16:
+            np.testing.assert_array_equal(got, k[pos, 0, c].astype(np.float16).astype(np.float64))
+        else:
+            kept = np.sort(pos)
+            cc, s, z = O.quantize_groups(k[kept, 0, c], bk)
+            exp = float(z) + float(s) * cc.astype(np.float64)
+            np.testing.assert_array_equal(got, exp[np.searchsorted(kept, pos)])
 
 
 def test_pack_sizes_and_index():
     w, q, k, v, al, cache = _tiny_cache(3.0, 3.0)
     hp = cache["plan"]["heads"][0]
-    assert cache["zone_a"].size == sum(n * b for n, b in zip(hp["tiles"], hp["tile_bytes"]))
-    assert all(tb % 16 == 0 for tb in hp["tile_bytes"])
+    assert cache["zone_a"].size == hp["meta_bytes"] + sum(n * b for n, b in zip(hp["tiles"], hp["tile_bytes"]))
+    assert all(tb % 16 == 0 for tb in hp["tile_bytes"]) and hp["meta_bytes"] % 16 == 0
     idx = cache["index"]
     assert sorted(idx[idx >= 0].tolist()) == np.nonzero(al["bits_tok"][0])[0].tolist()
 

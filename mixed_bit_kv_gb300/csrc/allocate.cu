@@ -235,13 +235,17 @@ __device__ __forceinline__ void load_run(const void* p, int64_t i, int dtype, in
 
 // Block (chunk, head), 256 threads: lane l takes channels [l D/32, (l+1) D/32) of every token (one
 // vector load; a warp reads whole rows), warp w the chunk's tokens t0 + w, t0 + w + 8, ... in order;
-// the eight warps' sums are added in warp order (deterministic).
+// the eight warps' sums are added in warp order (deterministic).  The first pass (no mean) also
+// takes each channel's minimum and maximum over the kept tokens (pmin, pmax): the K quantiser's
+// group of a channel is its head's kept tokens.
 constexpr int kChanWarps = 8;
 __global__ void __launch_bounds__(32 * kChanWarps) chan_pass(const void* __restrict__ k,
                                                              const uint8_t* __restrict__ bits_tok, int dtype, int N,
                                                              int h_kv, int D, int Np, const float* __restrict__ mean,
-                                                             float* __restrict__ part, int* __restrict__ part_cnt) {
+                                                             float* __restrict__ part, int* __restrict__ part_cnt,
+                                                             float* __restrict__ pmin, float* __restrict__ pmax) {
   __shared__ float wsum[kChanWarps][128];
+  __shared__ float wmin[kChanWarps][128], wmax[kChanWarps][128];
   __shared__ int wcnt[kChanWarps];
   const int head = blockIdx.y;  // b * h_kv + j
   const int b = head / h_kv, j = head % h_kv;
@@ -254,6 +258,7 @@ __global__ void __launch_bounds__(32 * kChanWarps) chan_pass(const void* __restr
   if (mean)
     for (int i = 0; i < cpl; ++i) m[i] = mean[head * D + c0 + i];
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   int cnt = 0;
   const int64_t row = (int64_t)h_kv * D;
   const int64_t base = (((int64_t)b * N) * h_kv + j) * D + c0;
@@ -266,17 +271,31 @@ __global__ void __launch_bounds__(32 * kChanWarps) chan_pass(const void* __restr
     for (int i = 0; i < 4; ++i) {
       const float d = x[i] - m[i];
       acc[i] += keep ? (mean ? d * d : x[i]) : 0.0f;
+      mn[i] = keep ? fminf(mn[i], x[i]) : mn[i];
+      mx[i] = keep ? fmaxf(mx[i], x[i]) : mx[i];
     }
     cnt += keep ? 1 : 0;
   }
-  for (int i = 0; i < cpl; ++i) wsum[w][c0 + i] = acc[i];
+  for (int i = 0; i < cpl; ++i) {
+    wsum[w][c0 + i] = acc[i];
+    wmin[w][c0 + i] = mn[i];
+    wmax[w][c0 + i] = mx[i];
+  }
   if (lane == 0) wcnt[w] = cnt;
   __syncthreads();
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float s = 0.0f;
+    float s = 0.0f, lo = INFINITY, hi = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < kChanWarps; ++q) s += wsum[q][c];
+    for (int q = 0; q < kChanWarps; ++q) {
+      s += wsum[q][c];
+      lo = fminf(lo, wmin[q][c]);
+      hi = fmaxf(hi, wmax[q][c]);
+    }
     part[((int64_t)head * nchunk + chunk) * D + c] = s;
+    if (pmin) {
+      pmin[((int64_t)head * nchunk + chunk) * D + c] = lo;
+      pmax[((int64_t)head * nchunk + chunk) * D + c] = hi;
+    }
   }
   if (threadIdx.x == 0 && part_cnt) {
     int n = 0;
@@ -285,28 +304,42 @@ __global__ void __launch_bounds__(32 * kChanWarps) chan_pass(const void* __restr
   }
 }
 
+// The first call (mean_out set) also combines the chunks' minima and maxima into the head's K
+// channel statistics kstat [head][c] = {min, max} over the kept tokens ({0, 0} when none is kept).
 __global__ void chan_finish(const float* __restrict__ part, const int* __restrict__ part_cnt, int nchunk, int D,
                             float* __restrict__ mean_out, const float* __restrict__ w_chan,
-                            float* __restrict__ sigma_out, float* __restrict__ g_out) {
+                            float* __restrict__ sigma_out, float* __restrict__ g_out, const float* __restrict__ pmin,
+                            const float* __restrict__ pmax, float2* __restrict__ kstat) {
   // thread (r, c) sums the chunks r, r + R, r + 2R, ... of channel c; the R sums are combined in a
   // fixed order (deterministic)
   __shared__ double ssum[1024];
   __shared__ long long scnt[1024];
+  __shared__ float smin[1024], smax[1024];
   const int head = blockIdx.x, c = threadIdx.x % D, r = threadIdx.x / D, R = blockDim.x / D;
   double s = 0.0;
   long long n = 0;
+  float lo = INFINITY, hi = -INFINITY;
   for (int i = r; i < nchunk; i += R) {
     s += (double)part[((int64_t)head * nchunk + i) * D + c];
     n += part_cnt[head * nchunk + i];
+    if (kstat) {
+      lo = fminf(lo, pmin[((int64_t)head * nchunk + i) * D + c]);
+      hi = fmaxf(hi, pmax[((int64_t)head * nchunk + i) * D + c]);
+    }
   }
   ssum[threadIdx.x] = s;
   scnt[threadIdx.x] = n;
+  smin[threadIdx.x] = lo;
+  smax[threadIdx.x] = hi;
   __syncthreads();
   if (r != 0) return;
   for (int rr = 1; rr < R; ++rr) {
     s += ssum[rr * D + c];
     n += scnt[rr * D + c];
+    lo = fminf(lo, smin[rr * D + c]);
+    hi = fmaxf(hi, smax[rr * D + c]);
   }
+  if (kstat) kstat[head * D + c] = n ? make_float2(lo, hi) : make_float2(0.f, 0.f);
   if (mean_out) {
     mean_out[head * D + c] = n ? (float)(s / (double)n) : 0.0f;
   } else {
@@ -359,25 +392,27 @@ __global__ void plan_heads_kernel(const uint8_t* __restrict__ bits_tok, const ui
   for (int c = threadIdx.x; c < D; c += blockDim.x) atomicAdd(&nk[kclass(bcs[c])], 1);
   __syncthreads();
   if (threadIdx.x == 0) {
+    // K segments of widths 16, 8, 4, 2: whole words per token, slot ranges of whole k-blocks
     rdkv_head_plan hp;
     int words_total = 0, slots_total = 0, meta = 0;
     for (int i = 0; i < 4; ++i) {
-      const int b = 16 >> i;  // K segment widths 16, 8, 4, 2
+      const int b = 16 >> i;
       hp.k_words[i] = ceil_div(nk[i] * b, 32);
+      const int blocks = ceil_div(hp.k_words[i] * (32 / b), kKB);
       seg_base[i] = slots_total;
       words_total += hp.k_words[i];
-      slots_total += hp.k_words[i] * (32 / b);
-      if (b < 16) meta += hp.k_words[i] * (32 / b);
+      slots_total += kKB * blocks;
+      if (b < 16) meta += kKB * blocks;
     }
     for (int i = 0; i < 5; ++i) hp.n_k[i] = nk[i];
     hp.row_words = words_total;
     hp.k_slots = slots_total;
     hp.meta_slots = meta;
-    int64_t a = 0;
+    int64_t a = head_meta_bytes(meta);
     for (int i = 0; i < 4; ++i) {
       hp.n_v[i] = nv[i];
       hp.tiles[i] = ceil_div(nv[i], kTile);
-      hp.tile_bytes[i] = tile_bytes_of(words_total, meta, D, 2 << i);  // V widths 2, 4, 8, 16
+      hp.tile_bytes[i] = tile_bytes_of(words_total, D, 2 << i);  // V widths 2, 4, 8, 16
       a += (int64_t)hp.tiles[i] * hp.tile_bytes[i];
     }
     hp.a_bytes = a;
@@ -385,12 +420,16 @@ __global__ void plan_heads_kernel(const uint8_t* __restrict__ bits_tok, const ui
     reinterpret_cast<rdkv_head_plan*>(plan + heads_off)[head] = hp;
   }
   __syncthreads();
+  // the channel of rank r in its segment: element r mod (32/b) of word r div (32/b), in the k-block
+  // of that word at the slot k_slot_in_block gives
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
     const int cls = kclass(bcs[c]);
     if (cls == 4) continue;
     int rank = 0;
     for (int c2 = 0; c2 < c; ++c2) rank += kclass(bcs[c2]) == cls;
-    slots[seg_base[cls] + rank] = (int16_t)c;
+    const int b = 16 >> cls, per = 32 / b, wpk = b / 2;
+    const int wg = rank / per, e = rank % per;
+    slots[seg_base[cls] + kKB * (wg / wpk) + k_slot_in_block(b, wg % wpk, e)] = (int16_t)c;
   }
 }
 
@@ -486,6 +525,8 @@ extern "C" size_t rdkv_plan_bytes(const rdkv_shape* s) {
   return (size_t)plan_layout(s->batch, s->h_kv, s->head_dim).total;
 }
 
+// Workspace of the allocation: water-filling state, channel partial sums (and, from the same chunks,
+// partial minima and maxima), counts, channel means, status words.
 static size_t alloc_ws_parts(const rdkv_shape* s, size_t* wf, size_t* part, size_t* cnt, size_t* mean) {
   const int64_t n_heads = (int64_t)s->batch * s->h_kv;
   const int Np = s->n_tokens - s->window;
@@ -494,7 +535,7 @@ static size_t alloc_ws_parts(const rdkv_shape* s, size_t* wf, size_t* part, size
   *part = align_up(n_heads * nchunk * s->head_dim * 4, 256);
   *cnt = align_up(n_heads * nchunk * 4, 256);
   *mean = align_up(n_heads * s->head_dim * 4, 256);
-  return *wf + *part + *cnt + *mean + 256;
+  return *wf + 3 * *part + *cnt + *mean + 256;
 }
 
 extern "C" size_t rdkv_allocate_workspace_bytes(const rdkv_shape* s) {
@@ -531,12 +572,15 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
   char* w = static_cast<char*>(ws);
   char* wf = w;
   float* part = reinterpret_cast<float*>(w + wf_b);
-  int* pcnt = reinterpret_cast<int*>(w + wf_b + part_b);
-  float* mean = reinterpret_cast<float*>(w + wf_b + part_b + cnt_b);
-  int32_t* status = reinterpret_cast<int32_t*>(w + wf_b + part_b + cnt_b + mean_b);  // [2]
+  float* pmin = reinterpret_cast<float*>(w + wf_b + part_b);
+  float* pmax = reinterpret_cast<float*>(w + wf_b + 2 * part_b);
+  int* pcnt = reinterpret_cast<int*>(w + wf_b + 3 * part_b);
+  float* mean = reinterpret_cast<float*>(w + wf_b + 3 * part_b + cnt_b);
+  int32_t* status = reinterpret_cast<int32_t*>(w + wf_b + 3 * part_b + cnt_b + mean_b);  // [2]
   const PlanLayout L = plan_layout(s->batch, s->h_kv, s->head_dim);
   char* pl = static_cast<char*>(plan);
   float* lam = reinterpret_cast<float*>(pl + L.lambda_off);
+  float2* kstat = reinterpret_cast<float2*>(pl + L.kstat_off);
   const int D = s->head_dim;
   const int n_heads = s->batch * s->h_kv;
   // levels: pooled: V [batch] then K [batch]; the other modes: V [n_heads] then K [n_heads]
@@ -571,18 +615,21 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
   const int nchunk = std::max(1, ceil_div(Np, kChanChunk));
   if (Np > 0) {
     chan_pass<<<dim3(nchunk, n_heads), 32 * kChanWarps, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np,
-                                                                 nullptr, part, pcnt);
+                                                                 nullptr, part, pcnt, pmin, pmax);
     RDKV_CHECK_LAUNCH("channel sums");
-    chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, mean, nullptr, nullptr, nullptr);
+    chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, mean, nullptr, nullptr, nullptr,
+                                                           pmin, pmax, kstat);
     RDKV_CHECK_LAUNCH("channel means");
     chan_pass<<<dim3(nchunk, n_heads), 32 * kChanWarps, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np,
-                                                                 mean, part, nullptr);
+                                                                 mean, part, nullptr, nullptr, nullptr);
     RDKV_CHECK_LAUNCH("channel deviations");
-    chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, nullptr, w_chan, sigma_chan, g_chan);
+    chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, nullptr, w_chan, sigma_chan, g_chan,
+                                                           nullptr, nullptr, nullptr);
     RDKV_CHECK_LAUNCH("channel spread");
   } else {
     RDKV_TRY_CUDA(cudaMemsetAsync(sigma_chan, 0, 4 * (size_t)n_heads * D, cs), "sigma reset");
     RDKV_TRY_CUDA(cudaMemsetAsync(g_chan, 0, 4 * (size_t)n_heads * D, cs), "gain reset");
+    RDKV_TRY_CUDA(cudaMemsetAsync(kstat, 0, 8 * (size_t)n_heads * D, cs), "channel statistics reset");
   }
   if (mode == RDKV_ALLOC_POOLED) {
     st = launch_waterfill(s->batch, (int64_t)s->h_kv * D, g_chan, avg_bits_k, bits_chan, lam + n_lev, status + 1,

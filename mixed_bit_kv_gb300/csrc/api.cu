@@ -57,9 +57,9 @@ extern "C" size_t rdkv_workspace_bytes(const rdkv_shape* shape, int32_t which_ca
     case RDKV_CALL_ALLOCATE:
       return rdkv_allocate_workspace_bytes(shape);
     case RDKV_CALL_DECODE: {
-      const int64_t n_heads = (int64_t)shape->batch * shape->h_kv, G = shape->h_q / shape->h_kv;
-      const int64_t partial = (G * (shape->head_dim + 2) + 3) / 4 * 4;
-      return (size_t)(align_up((num_sms() + n_heads) * partial * 4, 256) + align_up((n_heads + 2) * 4, 256));
+      const int64_t n_heads = (int64_t)shape->batch * shape->h_kv;
+      const int64_t partial = decode_partial_stride(shape->h_q / shape->h_kv, shape->head_dim);
+      return (size_t)(align_up((num_sms() + n_heads) * partial * 4, 256) + decode_ticket_bytes(n_heads));
     }
     default:
       return 0;

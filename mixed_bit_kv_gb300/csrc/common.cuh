@@ -16,7 +16,8 @@ namespace rdkv {
 
 constexpr int kTile = 32;          // tokens per zone-A tile
 constexpr int kVGroup = 32;        // channels per V quantiser group
-constexpr int kSlotPad = 32;       // extra K slots a head may need for word padding
+constexpr int kKB = 16;            // K slots of one k-block
+constexpr int kSlotPad = 64;       // extra K slots a head may need: each width segment spans whole k-blocks
 
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -24,10 +25,13 @@ __host__ __device__ inline int64_t align_up(int64_t a, int64_t b) { return ceil_
 
 // ---------------------------------------------------------------- plan buffer
 struct PlanLayout {
-  int64_t heads_off, slots_off, lambda_off, total;
+  int64_t heads_off, slots_off, lambda_off, kstat_off, total;
   int slot_stride;
 };
 
+// The plan buffer: header, head records, slot tables, water levels (one per (sequence, KV head) at
+// most), then the K channel statistics of each head: {min, max} over its kept prefix tokens, fp32
+// [n_heads][D][2] (written by the allocation, read by the pack).
 __host__ __device__ inline PlanLayout plan_layout(int batch, int h_kv, int head_dim) {
   PlanLayout L;
   const int64_t n_heads = (int64_t)batch * h_kv;
@@ -35,23 +39,36 @@ __host__ __device__ inline PlanLayout plan_layout(int batch, int h_kv, int head_
   L.heads_off = align_up(sizeof(rdkv_plan_header), 128);
   L.slots_off = align_up(L.heads_off + n_heads * (int64_t)sizeof(rdkv_head_plan), 128);
   L.lambda_off = align_up(L.slots_off + n_heads * L.slot_stride * 2, 128);
-  L.total = align_up(L.lambda_off + 2 * n_heads * 4, 256);  // room for one level per (sequence, KV head)
+  L.kstat_off = align_up(L.lambda_off + 2 * n_heads * 4, 256);
+  L.total = align_up(L.kstat_off + n_heads * head_dim * 8, 256);
   return L;
 }
+
+// Slot, inside its k-block, of element e of the block's word i at K width b (the layout rule of the
+// K rows: lane q of a decode fragment reads slots 2q, 2q+1, 2q+8, 2q+9 of a block from one word).
+__host__ __device__ inline int k_slot_in_block(int b, int i, int e) {
+  if (b == 16) return 2 * i + e;
+  if (b == 8) return 2 * i + (e & 1) + 8 * (e >> 1);
+  if (b == 4) return 2 * (2 * i + (e >> 2)) + (e & 1) + 8 * ((e >> 1) & 1);
+  return e;
+}
+
+// K metadata of a head (fp16 scale and zero per quantised slot) in front of its tiles, whole 16 bytes.
+__host__ __device__ inline int64_t head_meta_bytes(int meta_slots) { return align_up(4 * (int64_t)meta_slots, 16); }
 
 // Estimated zone-A decode cost of a head (instruction units per warp) from its plan record: every
 // tile pays a base (softmax, staging) plus its K k-blocks (quantised blocks cost about twice a raw
 // 16-bit one) plus its V class.  Only the ratios between heads matter: they decide how many
 // blocks each head gets.
 __host__ __device__ inline int64_t head_cost_a(const rdkv_head_plan& hp) {
-  const int nkb16 = ceil_div(hp.k_words[0] * 2, 16);
-  const int nkbq = ceil_div(hp.k_words[1] * 4, 16) + ceil_div(hp.k_words[2] * 8, 16) + ceil_div(hp.k_words[3] * 16, 16);
-  const int64_t per_tile = 250 + 20 * nkb16 + 40 * nkbq;
-  return (int64_t)hp.tiles[0] * (per_tile + 200) + (int64_t)hp.tiles[1] * (per_tile + 215) +
-         (int64_t)hp.tiles[2] * (per_tile + 250) + (int64_t)hp.tiles[3] * (per_tile + 60);
+  const int nkb16 = ceil_div(hp.k_words[0] * 2, kKB);
+  const int nkbq = ceil_div(hp.k_words[1] * 4, kKB) + ceil_div(hp.k_words[2] * 8, kKB) + ceil_div(hp.k_words[3] * 16, kKB);
+  const int64_t per_tile = 80 + 12 * nkb16 + 16 * nkbq;
+  return (int64_t)hp.tiles[0] * (per_tile + 115) + (int64_t)hp.tiles[1] * (per_tile + 130) +
+         (int64_t)hp.tiles[2] * (per_tile + 140) + (int64_t)hp.tiles[3] * (per_tile + 50);
 }
 // ... and of one zone-C block of 16 rows
-constexpr int kZoneCBlockCost = 300;
+constexpr int kZoneCBlockCost = 120;
 
 __device__ __forceinline__ const rdkv_plan_header* plan_header(const void* plan) {
   return reinterpret_cast<const rdkv_plan_header*>(plan);
@@ -63,12 +80,18 @@ __device__ __forceinline__ const int16_t* plan_slots(const void* plan) {
   return reinterpret_cast<const int16_t*>(static_cast<const char*>(plan) + plan_header(plan)->slots_off);
 }
 
-// Tile byte size of width class c for a head (same rule as the plan kernel).
-__host__ __device__ inline int tile_bytes_of(int row_words, int meta_slots, int head_dim, int vbits) {
-  int b = 4 * kTile * row_words + 4 * meta_slots;
+// Tile byte size of V width vbits for a head (same rule as the plan kernel): K codes, then for
+// vbits < 16 the V codes and the V metadata.
+__host__ __device__ inline int tile_bytes_of(int row_words, int head_dim, int vbits) {
+  int b = 4 * kTile * row_words;
   if (vbits < 16) b += (kTile * head_dim * vbits) / 8 + 4 * head_dim;
   return b;
 }
+
+// Decode workspace: one partial result (m, l, o of the G query heads) per block, G (D + 2) floats
+// rounded up to four, then the per-head tickets, the status word and the fused step's head counter.
+__host__ __device__ constexpr int decode_partial_stride(int G, int D) { return (G * (D + 2) + 3) / 4 * 4; }
+__host__ __device__ inline int64_t decode_ticket_bytes(int64_t n_heads) { return align_up((n_heads + 2) * 4, 256); }
 
 // Element offset of row `row` of head `head` in zone C: contiguous [heads][cap][D], or, with a page
 // table, row row % 16 of page pages[head * stride + row / 16] of a pool [pages][16][D].

@@ -5,30 +5,34 @@
 // tokens) and C (fp16 K and V rows of the window and of decoded tokens) in one
 // pass.
 //
-// Work: one block of 16 warps per SM, dealt to the (sequence, KV head) pairs
-// in proportion to their estimated cost (on the host when the plan's costs are
-// there, else by the kernel).  A head's work items are its zone-A tiles (32
-// tokens, in class order) followed by zone-C blocks of 16 rows; split s of n
-// takes items s, s + n, s + 2n, ... and its warps take them in order of need.
-// Every warp streams its items through its own ring of shared memory, filled
-// by bulk asynchronous copies that complete on per-slot mbarriers (all waits
-// are bounded and report RDKV_ERR_TIMEOUT).  The last block of a head to
-// finish (an atomic ticket) merges the splits' partial softmax states into
-// the output (and, when asked, the log-sum-exp).  One launch may attend
-// several caches sharing the query (segments moved out of zone C and the live
-// cache): each block reads one cache, the blocks of a head over all caches
+// Work: one block per SM, dealt to the (sequence, KV head) pairs in proportion
+// to their estimated cost (on the host when the plan's costs are there, else by
+// the kernel).  A head's work items are its zone-A tiles (32 tokens, in class
+// order) followed by zone-C blocks of 16 rows; split s of n takes items s,
+// s + n, s + 2n, ...  One producer warp streams the items into a shared-memory
+// ring per consumer warp with bulk asynchronous copies (its lane w serves
+// consumer warp w, taking the block's next item whenever that ring has room);
+// every stage has a full and an empty mbarrier, and every wait is bounded
+// (RDKV_ERR_TIMEOUT).  The sixteen consumer warps only compute.  The last block
+// of a head to finish (an atomic ticket) merges the splits' partial softmax
+// states into the output (and, when asked, the log-sum-exp).  One launch may
+// attend several caches sharing the query (segments moved out of zone C and the
+// live cache): each block reads one cache, the blocks of a head over all caches
 // share its merge.  Zone C may be paged (16-row pages through a table).
 //
 // Products: mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens on M:
-//   S^T[16 tok x 8 heads]  += K^[16 tok x 16 slots] * Q^T[16 slots x 8 heads]
+//   S^T[16 tok x 8 heads]  += K^[16 tok x 16 slots] * B[16 slots x 8 heads]
 //   O^T[16 ch  x 8 heads]  += V^T[16 ch x 16 tok]   * P^T[16 tok x 8 heads]
-// A 32-bit A-fragment register holds two consecutive elements along the
-// contraction axis (two K slots of one token; two tokens of one V channel);
-// the word rule of the layout puts both codes of such a pair in the two
-// half-words of one 32-bit word, so one shift and one mask (one byte permute
-// for 8-bit codes) place them as fp16 subnormals, code * 2^-24 exactly; the
-// scales enter through the other operand.  The softmax runs in fp32 on the
-// S^T accumulators (base-2 exponent); P^T is moved into B-fragment order by
+// K is quantised per (channel, head): k^ = zero_c + scale_c * code, so the
+// logit of head h is sum_c q_hc zero_c (a per-head constant, added once) plus
+// sum_c code * (q_hc scale_c).  The B operand q_hc * scale_c is built once per
+// block, as an fp16 high part and remainder (~22 bits).  A 32-bit A-fragment
+// register holds two codes of one token (K) or of one channel (V); the layout
+// puts them in the two half-words of one 32-bit word, at a bit position below
+// 10, so ONE mask (a shift first for the upper positions) turns them into fp16
+// subnormals code * 2^(pos - 24) exactly; the 2^pos goes into B (K) or into a
+// per-channel power of two undone once (V).  The softmax runs in fp32 on the S^T
+// accumulators (base-2 exponent); P^T is moved into B-fragment order by
 // movmatrix.  The G query heads of a group share every loaded tile.
 #include <atomic>
 
@@ -36,39 +40,32 @@
 
 namespace rdkv {
 
-constexpr int kDecWarps = 16;  // one block per SM
-constexpr int kMaxInflight = 4;
-constexpr int kPrologueItems = 2;     // copies a warp issues before the wait for the previous kernel
-constexpr int kMaxDealtBlocks = 256;  // grids up to this size may be dealt to heads on the host
+constexpr int kConsumers = 15;             // consumer warps of a block (one block per SM; with the producer, four warps per scheduler)
+constexpr int kDecWarps = kConsumers + 1;  // and the producer warp
+constexpr int kStages = 4;                 // stages in flight per consumer warp
+constexpr int kPrologueItems = 2;          // stages per consumer issued before the wait for the previous kernel
+constexpr int kMaxDealtBlocks = 256;       // grids up to this size may be dealt to heads on the host
 constexpr uint8_t kNoHead = 0xff;
-constexpr int kMaxParts = 8;          // caches one launch may attend
-constexpr int kCRows = 16;        // zone-C rows per work item
-constexpr int kMaxKB = 16;        // k-blocks of a K row (D = 128: at most 13)
+constexpr int kMaxParts = 8;               // caches one launch may attend
+constexpr int kCRows = 16;                 // zone-C rows per work item
+constexpr int kMaxKB = 16;                 // k-blocks of a K row (D = 128: at most 12)
+constexpr int kItemEnd = -1;               // stage record: no more items for this consumer
 constexpr long long kWaitCycles = 4000000000ll;  // limit of every wait on a tile copy: ~2 s at GB300 clocks
 constexpr long long kMinWaitCycles = 100000;     // shortest limit the timeout self-test may ask for
 
-// One k-block of a head's K rows (16 slots inside one width segment).  The same for every lane:
-// each lane adds its own constant offsets.
-struct KBDesc {
-  int32_t wbyte;    // byte offset in a tile of the block's first word: 128 * word (word-major layout)
-  int32_t mbyte;    // byte offset of the block's first slot pair in the K metadata: 8 * pair
-  int32_t nrem;     // slots of the segment from the block start (>= 1)
-  int32_t slot0;    // first slot of the block (for the query fragments)
-};
-
-// Bytes of the fixed part of the decode kernel's shared memory (before the rings): k-block
-// descriptors, query fragments (float4 per lane for fp32 queries, two fp16 pairs otherwise),
-// zone-C query fragments, slot table, ring bookkeeping, the fused step's new row.
-__host__ __device__ constexpr int64_t decode_fixed_smem(int D, bool qlo) {
-  return ((256 + (int64_t)kMaxKB * 32 * (qlo ? 16 : 8) + (int64_t)(D / 16) * 32 * 16 +
-           (int64_t)(D + kSlotPad) * 2 + kDecWarps * kMaxInflight * 20 + (int64_t)2 * D * 2) + 127) /
+// Bytes of the fixed part of the decode kernel's shared memory (before the rings): the K B-fragments
+// (16 bytes per k-block and lane), zone-C query fragments, slot table, k-block offsets, stage
+// barriers and records, the fused step's new row.
+__host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
+  return ((int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + (int64_t)(D + kSlotPad) * 2 + kMaxKB * 8 +
+          (int64_t)kConsumers * kStages * 24 + (int64_t)2 * D * 2 + 127) /
          128 * 128;
 }
 // Floats of one block's partial result (m, l, o for G heads), rounded up to a multiple of 4.
-__host__ __device__ constexpr int partial_stride(int G, int D) { return (G * (D + 2) + 3) / 4 * 4; }
+__host__ __device__ constexpr int partial_stride(int G, int D) { return decode_partial_stride(G, D); }
 
-// The warps' partial results are combined in the ring area once every ring is drained.
-__host__ __device__ constexpr int64_t decode_reduce_bytes(int D) { return (int64_t)kDecWarps * 8 * (D + 2) * 4; }
+// The consumer warps' partial results are combined in the ring area once every ring is drained.
+__host__ __device__ constexpr int64_t decode_reduce_bytes(int D) { return (int64_t)kConsumers * 8 * (D + 2) * 4; }
 
 // One cache attended by a launch: its zones, its zone-C length and capacity and its plan's head
 // records and slot tables.  A launch attends one cache, or several sharing the query (segments
@@ -126,10 +123,23 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking probe of a phase (the producer polls its consumers' empty barriers with it).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
@@ -144,8 +154,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   return true;
 }
 // L2 policy of the staged zone data: evicted first, so that the small data every call re-reads
-// (plan records, slot tables, queries, the split partials) stays in L2 across the layers.  Zone C
-// too: keeping its rows (a few hundred KB per layer) resident measured no better.
+// (plan records, slot tables, queries, the split partials) stays in L2 across the layers.
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -160,6 +169,8 @@ __device__ __forceinline__ void bulk_copy_once(void* dst, const void* src, uint3
       : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// the consumer warps alone (named barrier 1)
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory"); }
 // atomic add of 1 with acquire-release semantics at GPU scope; returns the old value
 __device__ __forceinline__ int ticket_acq_rel(int32_t* p) {
   int old;
@@ -192,9 +203,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 // Shared-memory loads through typed pointers into the block's shared window, so
 // the compiler folds constant offsets into the address ([reg + imm]).
-__device__ __forceinline__ uint32_t lds32(const unsigned char* base, uint32_t off) {
-  return *reinterpret_cast<const uint32_t*>(base + off);
-}
 __device__ __forceinline__ uint2 lds64(const unsigned char* base, uint32_t off) {
   return *reinterpret_cast<const uint2*>(base + off);
 }
@@ -202,28 +210,8 @@ __device__ __forceinline__ uint4 lds128(const unsigned char* base, uint32_t off)
   return *reinterpret_cast<const uint4*>(base + off);
 }
 __device__ __forceinline__ uint32_t pick4(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
-
-// Byte-permute selector that moves bytes (0, 2) (odd = 0) or (1, 3) (odd = 1) of a word to the
-// low bytes of its two half-words and zeroes the high bytes: the two 8-bit codes of a pair at
-// bit 0 and bit 16, the same as a shift by 0 or 8 and a mask, in one instruction.
-__device__ __forceinline__ uint32_t byte_pair_sel(int odd) { return odd ? 0x4341u : 0x4240u; }
-
-// Two codes of a pair (already shifted to bit 0 and bit 16) -> exact fp16 codes
-// -> scale * code + zero, one rounding.
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t w, int shift, uint32_t mask2, uint32_t scale2,
-                                                 uint32_t zero2) {
-  const uint32_t x = ((w >> shift) & mask2) | 0x64006400u;
-  const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&x), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-  const __half2 r = __hfma2(c, *reinterpret_cast<const __half2*>(&scale2), *reinterpret_cast<const __half2*>(&zero2));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-// Two codes of a pair -> the same codes as exact fp16 values (no scale, no zero).
-__device__ __forceinline__ uint32_t exact_codes(uint32_t w, int shift, uint32_t mask2) {
-  const uint32_t x = ((w >> shift) & mask2) | 0x64006400u;
-  const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&x), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-  return *reinterpret_cast<const uint32_t*>(&c);
-}
+// (x >> 8) & 0x00ff00ff in one byte permute: bytes 1 and 3 to bytes 0 and 2, zeros above
+__device__ __forceinline__ uint32_t high_bytes(uint32_t x) { return __byte_perm(x, 0u, 0x4341u); }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -314,278 +302,199 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
   acc.l[1] += ps1;
 }
 
-// K logits of one width segment of a zone-A tile, k-blocks [kb0, kb1).
-// A quantised K element is zero_c + scale_c * code, so per head g
-//   q_g . k^ = sum_c q_gc zero_c + sum_c code * (q_gc scale_c).
-// The codes are exact in fp16 and form the A operand; q_gc * scale_c (exact in
-// fp32) is split into an fp16 high part and an fp16 remainder, two B operands,
-// so the products keep ~22 bits; the zero term is summed in fp32.  Raw 16-bit
-// channels use the stored fp16 value against q (split the same way when q
-// carries more than fp16 precision).
-template <int W, bool QLO>
-__device__ __forceinline__ void k_segment(const unsigned char* kw, const unsigned char* kmeta, int kb0, int kb1,
-                                          const KBDesc* kbd, const float4* qv, int lane, float (&s)[2][4],
-                                          float& bias) {
-  const int g = lane >> 2, q = lane & 3;
-  // word offsets (inside the block's first word) and shifts of this lane's two slot pairs
-  constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
-  const int o0 = W == 16 ? q : W == 8 ? (q >> 1) : 0;
-  const int o1 = W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0;
-  const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
-  const int sh1 = W == 2 ? 2 * q + 8 : sh0;
-  for (int kb = kb0; kb < kb1; ++kb) {
-    const KBDesc d = kbd[kb];
-    const float4 qq = qv[kb * 32 + lane];  // q_g at slots 2q, 2q+1, 2q+8, 2q+9 (0 for pads and missing slots)
-    uint32_t bh0, bh1, bl0 = 0, bl1 = 0;
-    if (W == 16) {
-      if (QLO) {
-        const uint4 t = split_hi_lo(qq.x, qq.y, qq.z, qq.w);
-        bh0 = t.x; bh1 = t.y; bl0 = t.z; bl1 = t.w;
-      } else {
-        bh0 = pack_half2(qq.x, qq.y);
-        bh1 = pack_half2(qq.z, qq.w);
-      }
-    } else {
-      // a pair past the segment end reads the block's first (valid) pair: its q entries are 0
-      const uint32_t p0 = d.mbyte + (2 * q < d.nrem ? 8 * q : 0), p1 = d.mbyte + (2 * q + 8 < d.nrem ? 8 * (q + 4) : 0);
-      const uint2 m0 = lds64(kmeta, p0), m1 = lds64(kmeta, p1);
-      const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&m0.x));
-      const float2 z0 = __half22float2(*reinterpret_cast<const __half2*>(&m0.y));
-      const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&m1.x));
-      const float2 z1 = __half22float2(*reinterpret_cast<const __half2*>(&m1.y));
-      bias = fmaf(qq.x, z0.x, fmaf(qq.y, z0.y, fmaf(qq.z, z1.x, fmaf(qq.w, z1.y, bias))));
-      const uint4 t = split_hi_lo(qq.x * s0.x, qq.y * s0.y, qq.z * s1.x, qq.w * s1.y);
-      bh0 = t.x; bh1 = t.y; bl0 = t.z; bl1 = t.w;
-    }
-    // tokens g, g+8, g+16, g+24 of the lane's two words
-    const uint4 x0 = lds128(kw, (uint32_t)d.wbyte + 128u * o0 + 16u * g);
-    const uint4 x1 = W == 2 ? x0 : lds128(kw, (uint32_t)d.wbyte + 128u * o1 + 16u * g);
-#pragma unroll
-    for (int tb = 0; tb < 2; ++tb) {
-      uint32_t a0, a1, a2, a3;
-      if (W == 16) {
-        // raw fp16 words past the segment end may hold anything: zero them
-        const bool v0 = 2 * q < d.nrem, v1 = 2 * q + 8 < d.nrem;
-        a0 = v0 ? pick4(x0, 2 * tb) : 0u; a1 = v0 ? pick4(x0, 2 * tb + 1) : 0u;
-        a2 = v1 ? pick4(x1, 2 * tb) : 0u; a3 = v1 ? pick4(x1, 2 * tb + 1) : 0u;
-      } else {
-        // codes past the segment end are small integers met by zero query entries
-        a0 = exact_codes(pick4(x0, 2 * tb), sh0, mask2);
-        a1 = exact_codes(pick4(x0, 2 * tb + 1), sh0, mask2);
-        a2 = exact_codes(pick4(x1, 2 * tb), sh1, mask2);
-        a3 = exact_codes(pick4(x1, 2 * tb + 1), sh1, mask2);
-      }
-      mma16816(s[tb], a0, a1, a2, a3, bh0, bh1);
-      if (W != 16 || QLO) mma16816(s[tb], a0, a1, a2, a3, bl0, bl1);
-    }
-  }
-}
-
-// The same for fp16 queries (q exact in fp16).  hi = fp16(q * scale) by one
-// half2 multiply (the exact product rounded once) and lo = q * scale - hi by
-// one half2 FMA, which is exact because that remainder fits fp16.  The codes
-// enter the tensor core as fp16 subnormals: the bit pattern of a code c placed
-// at bit 0 of a half-word is the value c * 2^-24 exactly, so one shift and one
-// mask make the A operand and the products land at 2^-24: the hi products in
-// shi, the lo products in slo (two accumulators, two independent chains).  Raw
-// 16-bit channels use the stored fp16 value against q, at scale 1, into shi.
-// The zero-point term sum_c q_c zero_c runs as an MMA whose A rows g + 8 hold
-// the zeros, so zacc[2], zacc[3] carry it for heads (2q, 2q+1).  A segment's
-// k-blocks are consecutive: 64 W bytes of words and 64 bytes of metadata
-// apart, and only the last one may be partial.
-// PK (at most 4 heads): the hi and lo operands share one MMA.  B columns 0-3
-// take hi of heads 0-3 and columns 4-7 lo of the same heads (lanes g >= 4 of
-// the query fragments hold head g - 4), so one product gives both and shi
-// holds hi in its columns (2q, 2q+1) for q < 2 and lo for q >= 2; slo is unused.
+// K logits of one width segment W of a zone-A tile, k-blocks [kb0, kb1) (the segment's blocks are
+// consecutive: 64 W bytes of words apart, the first at wb0).  Lane (g, q) reads tokens g, g+8,
+// g+16, g+24 of its word of each block (one 16-byte load) and makes its two A registers per
+// token with one mask each (W = 2: bits 2q and, after a shift by 8, 2q + 8; W = 4: bits 0 and 4
+// after a shift by 8 (q & 1); W = 8: bytes 0, 2 and 1, 3); B (built once per block) carries
+// the 2^-pos of those positions.  PK: hi and lo share one MMA (B columns 0-3 hi, 4-7 lo); else
+// hi products go to shi and lo products to slo.
 template <int W, bool PK>
-__device__ __forceinline__ void k_segment_h(const unsigned char* kw, const unsigned char* kmeta, int kb0, int kb1,
-                                            const KBDesc* kbd, const uint2* qh, int lane, float (&shi)[2][4],
-                                            float (&slo)[2][4], float (&zacc)[4]) {
+__device__ __forceinline__ void k_segment(const unsigned char* kw, uint32_t wb0, int kb0, int kb1, const uint4* bfr,
+                                          int lane, float (&shi)[2][4], float (&slo)[2][4], int nrem16) {
   if (kb0 >= kb1) return;
   const int g = lane >> 2, q = lane & 3;
-  // PK: lo lanes take q * scale - fp16(q * scale), hi lanes fp16(q * scale); raw channels only hi
-  const bool lo_lane = PK && g >= 4;
-  const __half2 lo_sel = lo_lane ? __half2(__float2half(-1.f), __float2half(-1.f)) : __half2(__float2half(0.f), __float2half(0.f));
-  constexpr uint32_t mask2 = W == 8 ? 0x00ff00ffu : W == 4 ? 0x000f000fu : 0x00030003u;
-  const int sh0 = W == 8 ? 8 * (q & 1) : W == 4 ? 4 * q : W == 2 ? 2 * q : 0;
-  const int sh1 = W == 2 ? 2 * q + 8 : sh0;
-  const uint32_t bsel = byte_pair_sel(q & 1);  // 8-bit codes: bytes (0, 2) or (1, 3) of a word
-  // this lane's offsets from a block's first word: words o0, o1 of its two slot pairs, tokens g ..
-  const uint32_t c0 = 128u * (W == 16 ? q : W == 8 ? (q >> 1) : 0) + 16u * g;
-  const uint32_t c1 = 128u * (W == 16 ? q + 4 : W == 8 ? (q >> 1) + 2 : W == 4 ? 1 : 0) + 16u * g;
-  const KBDesc d0 = kbd[kb0];
-  const int last_nrem = kbd[kb1 - 1].nrem;
-  uint32_t wb = (uint32_t)d0.wbyte, mb = (uint32_t)d0.mbyte;
-  const uint2* qp = qh + kb0 * 32 + lane;
+  // this lane's byte offset from a block's first word: its word index times 128, its tokens 16 g
+  const uint32_t c0 = 128u * (W == 16 ? q : W == 8 ? q : W == 4 ? (q >> 1) : 0) + 16u * g;
+  // (a partial 8- or 4-bit block's lanes past its last word read the next words of the tile: codes
+  // of other slots or V bytes, always in the staged item, met by B = 0)
+  const uint32_t c1 = 128u * (q + 4) + 16u * g;  // W = 16: the word of slots 2q + 8, 2q + 9
+  const uint32_t m2 = 0x00030003u << (2 * q);
+  const int sh4 = 8 * (q & 1);
+  uint32_t wb = wb0;
+  const uint4* bp = bfr + kb0 * 32 + lane;
 #pragma unroll 1
-  for (int kb = kb0; kb < kb1; ++kb, wb += 64u * W, mb += 64u, qp += 32) {
-    const int nrem = kb == kb1 - 1 ? last_nrem : 16;
-    const uint2 qq = *qp;  // q_g (fp16 pairs) at slots (2q, 2q+1), (2q+8, 2q+9); 0 for pads
-    const bool v0 = 2 * q < nrem, v1 = 2 * q + 8 < nrem;
-    // tokens g, g+8, g+16, g+24 of the lane's two words (one word for 2-bit codes)
+  for (int kb = kb0; kb < kb1; ++kb, wb += 64u * W, bp += 32) {
+    const uint4 bq = *bp;
     const uint4 y0 = lds128(kw, wb + c0);
-    const uint4 y1 = W == 2 ? y0 : lds128(kw, wb + c1);
-    uint32_t bh0 = lo_lane ? 0u : qq.x, bh1 = lo_lane ? 0u : qq.y, bl0 = 0, bl1 = 0;
-    if (W != 16 && PK) {
-      const uint2 m0 = lds64(kmeta, mb + (v0 ? 8u * q : 0u));
-      const uint2 m1 = lds64(kmeta, mb + (v1 ? 8u * (q + 4) : 0u));
-      const __half2 q0 = *reinterpret_cast<const __half2*>(&qq.x), q1 = *reinterpret_cast<const __half2*>(&qq.y);
-      const __half2 s0 = *reinterpret_cast<const __half2*>(&m0.x), s1 = *reinterpret_cast<const __half2*>(&m1.x);
-      // hi: q * scale + 0 rounded once; lo: q * scale - hi, exact
-      const __half2 h0 = __hmul2(q0, s0), h1 = __hmul2(q1, s1);
-      const __half2 b0 = __hfma2(q0, s0, __hmul2(h0, lo_sel)), b1 = __hfma2(q1, s1, __hmul2(h1, lo_sel));
-      bh0 = *reinterpret_cast<const uint32_t*>(&b0);
-      bh1 = *reinterpret_cast<const uint32_t*>(&b1);
-      mma16816(zacc, m0.x, m0.y, m1.x, m1.y, qq.x, qq.y);
-    } else if (W != 16) {
-      // a pair past the segment end reads the block's first pair (its q entries are 0)
-      const uint2 m0 = lds64(kmeta, mb + (v0 ? 8u * q : 0u));
-      const uint2 m1 = lds64(kmeta, mb + (v1 ? 8u * (q + 4) : 0u));
-      const __half2 q0 = *reinterpret_cast<const __half2*>(&qq.x), q1 = *reinterpret_cast<const __half2*>(&qq.y);
-      const __half2 s0 = *reinterpret_cast<const __half2*>(&m0.x), s1 = *reinterpret_cast<const __half2*>(&m1.x);
-      const __half2 h0 = __hmul2(q0, s0), h1 = __hmul2(q1, s1);
-      const __half2 l0 = __hfma2(q0, s0, __hneg2(h0)), l1 = __hfma2(q1, s1, __hneg2(h1));
-      bh0 = *reinterpret_cast<const uint32_t*>(&h0);
-      bh1 = *reinterpret_cast<const uint32_t*>(&h1);
-      bl0 = *reinterpret_cast<const uint32_t*>(&l0);
-      bl1 = *reinterpret_cast<const uint32_t*>(&l1);
-      // A = the metadata as loaded, {scales, zeros} of the two pairs: rows g get sum scale * q
-      // (unused) and rows g + 8 the zero-point term sum zero * q, with no register shuffling
-      mma16816(zacc, m0.x, m0.y, m1.x, m1.y, qq.x, qq.y);
+    uint4 y1 = y0;
+    uint32_t k0 = ~0u, k1 = ~0u;
+    if (W == 16) {
+      // raw fp16 words past the segment's last real word (the next segment's, or past the staged
+      // tile) are not read: such a lane reads its first word again and masks both to zero
+      const int nrem = kb == kb1 - 1 ? nrem16 : kKB;
+      k0 = 2 * q < nrem ? ~0u : 0u;
+      k1 = 2 * q + 8 < nrem ? ~0u : 0u;
+      y1 = lds128(kw, wb + (k1 ? c1 : c0));
     }
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
-      const uint32_t x0 = pick4(y0, 2 * tb), x1 = pick4(y0, 2 * tb + 1);
-      const uint32_t x2 = pick4(y1, 2 * tb), x3 = pick4(y1, 2 * tb + 1);
-      if (W == 16) {  // raw fp16 words past the segment end may hold anything: zero them
-        const uint32_t k0 = v0 ? ~0u : 0u, k1 = v1 ? ~0u : 0u;
-        mma16816(shi[tb], x0 & k0, x1 & k0, x2 & k1, x3 & k1, bh0, bh1);
+      const uint32_t x0 = pick4(y0, 2 * tb), x1 = pick4(y0, 2 * tb + 1);  // tokens g + 16 tb, g + 8 + 16 tb
+      uint32_t a0, a1, a2, a3;
+      if (W == 16) {
+        a0 = x0 & k0;
+        a1 = x1 & k0;
+        a2 = pick4(y1, 2 * tb) & k1;
+        a3 = pick4(y1, 2 * tb + 1) & k1;
+      } else if (W == 8) {
+        a0 = x0 & 0x00ff00ffu;
+        a1 = x1 & 0x00ff00ffu;
+        a2 = high_bytes(x0);
+        a3 = high_bytes(x1);
+      } else if (W == 4) {
+        const uint32_t t0 = x0 >> sh4, t1 = x1 >> sh4;
+        a0 = t0 & 0x000f000fu;
+        a1 = t1 & 0x000f000fu;
+        a2 = t0 & 0x00f000f0u;
+        a3 = t1 & 0x00f000f0u;
       } else {
-        const uint32_t a0 = W == 8 ? __byte_perm(x0, 0u, bsel) : (x0 >> sh0) & mask2;
-        const uint32_t a1 = W == 8 ? __byte_perm(x1, 0u, bsel) : (x1 >> sh0) & mask2;
-        const uint32_t a2 = W == 8 ? __byte_perm(x2, 0u, bsel) : (x2 >> sh1) & mask2;
-        const uint32_t a3 = W == 8 ? __byte_perm(x3, 0u, bsel) : (x3 >> sh1) & mask2;
-        mma16816(shi[tb], a0, a1, a2, a3, bh0, bh1);
-        if (!PK) mma16816(slo[tb], a0, a1, a2, a3, bl0, bl1);
+        a0 = x0 & m2;
+        a1 = x1 & m2;
+        a2 = (x0 >> 8) & m2;
+        a3 = (x1 >> 8) & m2;
       }
+      mma16816(shi[tb], a0, a1, a2, a3, bq.x, bq.y);
+      if (!PK) mma16816(slo[tb], a0, a1, a2, a3, bq.z, bq.w);
     }
   }
 }
 
-template <int D, bool QLO, bool PK>
-__device__ __forceinline__ void tile_logits(const unsigned char* kw, const unsigned char* kmeta, const int (&seg_kb)[5],
-                                            const KBDesc* kbd, const float4* qv, int lane,
+// Logits (base 2, with the per-head zero-point term) of the 32 tokens of a zone-A tile:
+// raw 16-bit channels first at scale 1, then the accumulators move to 2^-24 and take the
+// quantised segments' products (codes as fp16 subnormals), then back, times log2(e)/sqrt(D).
+template <bool PK>
+__device__ __forceinline__ void tile_logits(const unsigned char* kw, const int (&seg_kb)[5], const uint32_t (&seg_wb)[4],
+                                            int nrem16, const uint4* bfr, int lane, float c24, float b0, float b1,
                                             float (&s)[2][4]) {
-  float bias = 0.f;  // sum over this lane's slots of q_g * zero (head g)
+  float slo[2][4];
 #pragma unroll
-  for (int tb = 0; tb < 2; ++tb) s[tb][0] = s[tb][1] = s[tb][2] = s[tb][3] = 0.f;
-  const int q = lane & 3;
-  float be, bo;
-  if (QLO) {
-    k_segment<16, QLO>(kw, kmeta, seg_kb[0], seg_kb[1], kbd, qv, lane, s, bias);
-    k_segment<8, QLO>(kw, kmeta, seg_kb[1], seg_kb[2], kbd, qv, lane, s, bias);
-    k_segment<4, QLO>(kw, kmeta, seg_kb[2], seg_kb[3], kbd, qv, lane, s, bias);
-    k_segment<2, QLO>(kw, kmeta, seg_kb[3], seg_kb[4], kbd, qv, lane, s, bias);
-    // zero-point term: lanes (g, 0..3) hold parts of head g; S^T lane (g', q') needs heads 2q', 2q'+1
-    bias += __shfl_xor_sync(0xffffffffu, bias, 1);
-    bias += __shfl_xor_sync(0xffffffffu, bias, 2);
-    be = __shfl_sync(0xffffffffu, bias, 8 * q);
-    bo = __shfl_sync(0xffffffffu, bias, 8 * q + 4);
-  } else {
-    const uint2* qh = reinterpret_cast<const uint2*>(qv);
-    float zacc[4] = {0.f, 0.f, 0.f, 0.f};  // [2], [3]: zero-point term of heads 2q, 2q+1
-    // raw 16-bit channels first, at scale 1 in s; then s moves to 2^-24 and takes the hi products
-    float slo[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    k_segment_h<16, PK>(kw, kmeta, seg_kb[0], seg_kb[1], kbd, qh, lane, s, slo, zacc);
+  for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[tb][e] = slo[tb][e] = 0.f;
+  if (seg_kb[1] > seg_kb[0]) {
+    k_segment<16, PK>(kw, seg_wb[0], seg_kb[0], seg_kb[1], bfr, lane, s, slo, nrem16);
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[tb][e] *= 5.9604644775390625e-8f;
-    k_segment_h<8, PK>(kw, kmeta, seg_kb[1], seg_kb[2], kbd, qh, lane, s, slo, zacc);
-    k_segment_h<4, PK>(kw, kmeta, seg_kb[2], seg_kb[3], kbd, qh, lane, s, slo, zacc);
-    k_segment_h<2, PK>(kw, kmeta, seg_kb[3], seg_kb[4], kbd, qh, lane, s, slo, zacc);
-    // back to scale 1; PK: the lo columns (2q + 4, 2q + 5) are held by lane q ^ 2
-#pragma unroll
-    for (int tb = 0; tb < 2; ++tb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        s[tb][e] = (s[tb][e] + (PK ? __shfl_xor_sync(0xffffffffu, s[tb][e], 2) : slo[tb][e])) * 16777216.f;
-    be = zacc[2];
-    bo = zacc[3];
+      for (int e = 0; e < 4; ++e) {
+        s[tb][e] *= 5.9604644775390625e-8f;
+        slo[tb][e] *= 5.9604644775390625e-8f;
+      }
   }
+  k_segment<8, PK>(kw, seg_wb[1], seg_kb[1], seg_kb[2], bfr, lane, s, slo, kKB);
+  k_segment<4, PK>(kw, seg_wb[2], seg_kb[2], seg_kb[3], bfr, lane, s, slo, kKB);
+  k_segment<2, PK>(kw, seg_wb[3], seg_kb[3], seg_kb[4], bfr, lane, s, slo, kKB);
+  // PK: the lo columns (2q + 4, 2q + 5) are held by lane q ^ 2
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
-    s[tb][0] += be;
-    s[tb][1] += bo;
-    s[tb][2] += be;
-    s[tb][3] += bo;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float t = s[tb][e] + (PK ? __shfl_xor_sync(0xffffffffu, s[tb][e], 2) : slo[tb][e]);
+      s[tb][e] = fmaf(t, c24, (e & 1) ? b1 : b0);
+    }
   }
+}
+
+// Exponent of the power of two the products of V class `vb` (2, 4, 8; 16 = fp16 rows) carry in
+// the accumulators of channel block cm: 2^-24 for the subnormal codes times 2^pos of the code's
+// bit position inside its half-word (below 8 after the optional shift by 8).
+__device__ __forceinline__ int v_scale_exp(int vb, int cm) {
+  if (vb == 16) return 0;
+  const int per = 16 / vb;
+  return -24 + ((vb * (cm % per)) & 7);
+}
+
+// Moves the O^T accumulators from the scale of V class `from` to that of class `to` (powers of
+// two per channel block: exact).
+template <int D>
+__device__ __forceinline__ void rescale_o(WarpAcc<D>& acc, int from, int to) {
+#pragma unroll
+  for (int cm = 0; cm < D / 16; ++cm) {
+    const float f = __int_as_float((127 + v_scale_exp(to, cm) - v_scale_exp(from, cm)) << 23);
+    acc.o[cm][0] *= f;
+    acc.o[cm][1] *= f;
+    acc.o[cm][2] *= f;
+    acc.o[cm][3] *= f;
+  }
+}
+
+// One code field of a V word: element e of the word (bit VB e of each half), as an fp16 subnormal
+// pair at bit position (VB e) mod 8 -- positions 8 and up are shifted down by 8 first.
+template <int VB>
+__device__ __forceinline__ uint32_t v_field(uint32_t x, int e) {
+  constexpr uint32_t m = VB == 8 ? 0x00ff00ffu : VB == 4 ? 0x000f000fu : 0x00030003u;
+  const int pos = VB * e;
+  if (VB == 8) return pos == 0 ? (x & m) : high_bytes(x);
+  return pos < 8 ? (x & (m << pos)) : ((x >> 8) & (m << (pos - 8)));
 }
 
 // PV of a zone-A tile with packed V of width VB.  A dequantised V element is
 // zero + scale * code per (token, 32-channel group), so per head h and channel c
 //   O[h][c] += sum_t (p_ht scale_t) code_tc + sum_t p_ht zero_t.
-// The codes enter the tensor core as fp16 subnormals (code * 2^-24, one shift
-// and one mask) against B = p * scale of the group (one half2 multiply per
-// fragment), so the products land in acc.o scaled by 2^-24 (the caller keeps
-// track of that scale); the zero-point sums go to acc.z through one MMA per
-// 16 tokens whose A row g holds the zeros of channel group g.
+// Lane (g, q) of 16-token block tb owns 2 nw consecutive code words (its two token pairs): entry k
+// of its channel list (channel 16 (k mod D/16) + 8 (k div D/16) + g) sits in word k / per at
+// element k mod per.  B = p * scale of the channel group (one half2 multiply per fragment); the
+// zero-point sums go to acc.z through one MMA per 16 tokens whose A row g holds the zeros of
+// channel group g.
 template <int D, int VB>
-__device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned char* vcodes, const unsigned char* vmeta, int lane,
-                                               const uint32_t (&pb)[2][2]) {
+__device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned char* vcodes, const unsigned char* vmeta,
+                                               int lane, const uint32_t (&pb)[2][2]) {
   const int g = lane >> 2, q = lane & 3;
-  constexpr int wpp = D * VB / 16;  // words per token pair
-  constexpr int per = 16 / VB;      // channels per half-word
-  constexpr int NG = D / 32;        // channel groups
-  constexpr uint32_t mask2 = VB == 8 ? 0x00ff00ffu : VB == 4 ? 0x000f000fu : 0x00030003u;
-  constexpr int R = VB / 2;         // word groups inside a pair (words w = r mod R together)
-  const int sh0 = VB * (g % per), sh1 = VB * ((g + 8) % per);
-  const uint32_t bsel = byte_pair_sel(g & 1);  // 8-bit codes: bytes (0, 2) or (1, 3) of a word
+  constexpr int CM = D / 16, NG = D / 32, NW = D * VB / 128, PER = 16 / VB;
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
-    const int p0 = 8 * tb + q, p1 = p0 + 4;
-    // this lane's channels c = g + 8 i (i = 0 .. D/8-1) live in the words w = 2 i / ... of group
-    // g / per, stored adjacently in order of i: word i of the group holds channel g + 8 i
-    const unsigned char* base0 = vcodes + 4 * (p0 * wpp + (g / per) * (wpp / R));
-    const unsigned char* base1 = vcodes + 4 * (p1 * wpp + (g / per) * (wpp / R));
-    uint32_t za0 = 0u, za2 = 0u;
-    if (g < NG) {
-      za0 = lds32(vmeta, 8 * (p0 * NG + g) + 4);
-      za2 = lds32(vmeta, 8 * (p1 * NG + g) + 4);
+    // scales of the lane's two pairs for every group (h = 0, then h = 1), 2 NG words
+    uint32_t sc[2 * NG];
+    const unsigned char* sp = vmeta + 4 * ((tb * 4 + q) * 2 * NG);
+#pragma unroll
+    for (int i = 0; i < 2 * NG; i += 4) {
+      const uint4 t = lds128(sp, 4 * i);
+      sc[i] = t.x; sc[i + 1] = t.y; sc[i + 2] = t.z; sc[i + 3] = t.w;
     }
-    mma16816(acc.z, za0, 0u, za2, 0u, pb[tb][0], pb[tb][1]);
+    uint2 za = make_uint2(0u, 0u);
+    if (g < NG) za = lds64(vmeta, 4 * (16 * NG + ((tb * NG + g) * 4 + q) * 2));
+    mma16816(acc.z, za.x, 0u, za.y, 0u, pb[tb][0], pb[tb][1]);
+    uint32_t bb[2][NG];
 #pragma unroll
     for (int grp = 0; grp < NG; ++grp) {
-      const uint32_t s0 = lds32(vmeta, 8 * (p0 * NG + grp)), s1 = lds32(vmeta, 8 * (p1 * NG + grp));
-      const __half2 b0h = __hmul2(*reinterpret_cast<const __half2*>(&pb[tb][0]), *reinterpret_cast<const __half2*>(&s0));
-      const __half2 b1h = __hmul2(*reinterpret_cast<const __half2*>(&pb[tb][1]), *reinterpret_cast<const __half2*>(&s1));
-      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&b0h), b1 = *reinterpret_cast<const uint32_t*>(&b1h);
-      // words i = 4 grp .. 4 grp + 3 of the lane's group: channels of (cm, c0), (cm, c1) for
-      // cm = 2 grp, 2 grp + 1
-      const uint4 v0 = lds128(base0, 16 * grp), v1 = lds128(base1, 16 * grp);
-      const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+      const __half2 h0 = __hmul2(*reinterpret_cast<const __half2*>(&pb[tb][0]), *reinterpret_cast<const __half2*>(&sc[grp]));
+      const __half2 h1 = __hmul2(*reinterpret_cast<const __half2*>(&pb[tb][1]), *reinterpret_cast<const __half2*>(&sc[NG + grp]));
+      bb[0][grp] = *reinterpret_cast<const uint32_t*>(&h0);
+      bb[1][grp] = *reinterpret_cast<const uint32_t*>(&h1);
+    }
+    // the lane's code words: pair h = 0 then h = 1, NW words each
+    uint32_t wd[2 * NW];
+    const unsigned char* cp = vcodes + 4 * (((tb * 8 + g) * 4 + q) * 2 * NW);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int cm = 2 * grp + half;
-        const uint32_t a0 = VB == 8 ? __byte_perm(w0[2 * half], 0u, bsel) : (w0[2 * half] >> sh0) & mask2;
-        const uint32_t a1 = VB == 8 ? __byte_perm(w0[2 * half + 1], 0u, bsel) : (w0[2 * half + 1] >> sh1) & mask2;
-        const uint32_t a2 = VB == 8 ? __byte_perm(w1[2 * half], 0u, bsel) : (w1[2 * half] >> sh0) & mask2;
-        const uint32_t a3 = VB == 8 ? __byte_perm(w1[2 * half + 1], 0u, bsel) : (w1[2 * half + 1] >> sh1) & mask2;
-        mma16816(acc.o[cm], a0, a1, a2, a3, b0, b1);
+    for (int i = 0; i < 2 * NW; i += 4) {
+      if (2 * NW >= 4) {
+        const uint4 t = lds128(cp, 4 * i);
+        wd[i] = t.x; wd[i + 1] = t.y; wd[i + 2] = t.z; wd[i + 3] = t.w;
       }
     }
-  }
-}
-
-// Multiplies the O^T accumulators by f (a power of two: exact).
-template <int D>
-__device__ __forceinline__ void scale_o(WarpAcc<D>& acc, float f) {
+    if (2 * NW == 2) {
+      const uint2 t = lds64(cp, 0);
+      wd[0] = t.x; wd[1] = t.y;
+    }
 #pragma unroll
-  for (int cm = 0; cm < D / 16; ++cm) {
-    acc.o[cm][0] *= f;
-    acc.o[cm][1] *= f;
-    acc.o[cm][2] *= f;
-    acc.o[cm][3] *= f;
+    for (int cm = 0; cm < CM; ++cm) {
+      const int k0 = cm, k1 = CM + cm;  // the lane's entries for rows g and g + 8
+      const uint32_t a0 = v_field<VB>(wd[k0 / PER], k0 % PER);
+      const uint32_t a1 = v_field<VB>(wd[k1 / PER], k1 % PER);
+      const uint32_t a2 = v_field<VB>(wd[NW + k0 / PER], k0 % PER);
+      const uint32_t a3 = v_field<VB>(wd[NW + k1 / PER], k1 % PER);
+      mma16816(acc.o[cm], a0, a1, a2, a3, bb[0][cm / 2], bb[1][cm / 2]);
+    }
   }
 }
 
@@ -617,7 +526,7 @@ struct ClassVals {
   __device__ __forceinline__ int64_t operator()(int c) const { return c == 0 ? v[0] : c == 1 ? v[1] : c == 2 ? v[2] : v[3]; }
 };
 
-template <int D, bool QLO, bool PK>
+template <int D, bool PK>
 __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeParams P) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -626,6 +535,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int asg[3];  // head, first block of the head, blocks of the head
   __shared__ __align__(16) rdkv_head_plan hp_s;  // this block's head record
+  __shared__ float bias_s[8];                    // zero-point term of each query head (base 2)
+  __shared__ int next_k;                         // the block's next item (producer warp)
+  __shared__ int abort_s;                        // a bounded wait ran out somewhere in the block
+  __shared__ int is_last;
   int16_t slot_pre = -1;  // dealt on the host: this thread's slot-table entry, loaded with the record
   // the cache this block reads (part 0 unless the host dealt blocks over several caches)
   const DecodePart& PP = P.parts[P.dealt ? P.block_part[blockIdx.x] : 0];
@@ -645,10 +558,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   } else if (warp == 0) {
     // Blocks are dealt to heads in proportion to their estimated cost, at least one per head, over a
     // nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the blocks past the last head's
-    // range leave at once.  Warp 0: one lane per head, one round trip for the plan records and the
-    // zone-C length, then a scan.
-    // static inputs only (plan and capacity): the dealing is the same in every launch, also before
-    // the previous kernel on the stream has finished
+    // range leave at once.  Warp 0: one lane per head, one round trip for the plan records, then a
+    // scan.  Static inputs only (plan and capacity): the dealing is the same in every launch, also
+    // before the previous kernel on the stream has finished.
     const int zc = ceil_div(P.cap_c, kCRows);
     int64_t total = 0;
     for (int h = lane; h < P.n_heads; h += 32) total += head_cost(P.heads[h], zc);
@@ -689,35 +601,31 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   const int b = head / P.h_kv, j = head % P.h_kv;
   const rdkv_head_plan* hpp = &hp_s;
   const bool fused = P.k_new != nullptr;
-
-  // the slot table goes into registers now (static data)
   const int qbase = b * P.h_q + j * G;
   const int16_t* slot_ch = PP.slots + (int64_t)head * P.slot_stride;
   const int k_slots = hpp->k_slots;  // <= D + kSlotPad <= the block's threads
   const int16_t sr = tid < k_slots ? (P.dealt ? slot_pre : slot_ch[tid]) : (int16_t)-1;
 
   // shared memory map
-  KBDesc* kbd = reinterpret_cast<KBDesc*>(smem);                                   // [kMaxKB]
-  float4* qv = reinterpret_cast<float4*>(smem + 256);                              // [kMaxKB][32] (uint2 if !QLO)
-  uint4* qfragc = reinterpret_cast<uint4*>(smem + 256 + kMaxKB * 32 * (QLO ? 16 : 8));  // [D/16][32] hi, lo
-  int16_t* slot_s = reinterpret_cast<int16_t*>(qfragc + (D / 16) * 32);            // [D + kSlotPad] slot table
-  uint64_t* bars = reinterpret_cast<uint64_t*>(slot_s + D + kSlotPad);             // [warps][kMaxInflight]
-  int* ring_pos = reinterpret_cast<int*>(bars + kDecWarps * kMaxInflight);         // [warps][kMaxInflight]
-  int* ring_item = ring_pos + kDecWarps * kMaxInflight;                            // [warps][kMaxInflight]
-  uint32_t* ring_need = reinterpret_cast<uint32_t*>(ring_item + kDecWarps * kMaxInflight);  // [warps][kMaxInflight]
-  uint16_t* newrow = reinterpret_cast<uint16_t*>(ring_need + kDecWarps * kMaxInflight);     // [2][D] fused step: k, v
-  unsigned char* ring = smem + decode_fixed_smem(D, QLO);
-  float* red = reinterpret_cast<float*>(ring);                                     // [warps][8][D + 2], after the loop
-  __shared__ int seg_kb_s[5];
-  __shared__ int is_last;
-  __shared__ int next_k;
+  uint4* bfr = reinterpret_cast<uint4*>(smem);                                     // [kMaxKB][32]
+  uint4* qfragc = bfr + kMaxKB * 32;                                               // [D/16][32] hi, lo
+  int16_t* slot_s = reinterpret_cast<int16_t*>(qfragc + (D / 16) * 32);            // [D + kSlotPad]
+  uint32_t* kb_wb = reinterpret_cast<uint32_t*>(slot_s + D + kSlotPad);            // [kMaxKB] (unused entries 0)
+  int* seg_kb_s = reinterpret_cast<int*>(kb_wb + kMaxKB);                          // [kMaxKB]: [0..4] block ranges
+  uint64_t* full = reinterpret_cast<uint64_t*>(seg_kb_s + kMaxKB);                 // [consumers][stages]
+  uint64_t* empty = full + kConsumers * kStages;                                   // [consumers][stages]
+  int* st_pos = reinterpret_cast<int*>(empty + kConsumers * kStages);              // [consumers][stages]
+  int* st_item = st_pos + kConsumers * kStages;                                    // [consumers][stages]
+  uint16_t* newrow = reinterpret_cast<uint16_t*>(st_item + kConsumers * kStages);  // [2][D] fused step: k, v
+  unsigned char* ring = smem + decode_fixed_smem(D);
+  float* red = reinterpret_cast<float*>(ring);                                     // [consumers][8][D + 2], after the loop
 
   // items of this head: its tiles in class order, then its zone-C blocks
   ClassVals cstart, coff, ctb, cnv;  // first item, first byte in zone A, tile bytes, kept tokens per class
   int zc_start;
   {
     int t = 0;
-    int64_t off = hpp->a_off;
+    int64_t off = hpp->a_off + head_meta_bytes(hpp->meta_slots);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       cstart.v[c] = t;
@@ -730,353 +638,418 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     zc_start = t;
   }
   const int64_t b_row = hpp->b_row;
-  const int RW = hpp->row_words, meta_slots = hpp->meta_slots;
-  // split s of n takes items s, s + n, s + 2n, ...: every split gets its share of each class.  The
-  // zone-C length is known only after the wait for the previous kernel: until then only zone-A
-  // items are issued (an item past them stays pending)
-  int n_items = zc_start, len_c = 0, n_rows = 0;
-  bool items_final = false;
-  if (tid == 0) next_k = 0;
-
-  // k-block descriptors of this head's K rows (each block inside one width segment), one per thread
+  const int RW = hpp->row_words;
+  if (tid == 0) {
+    next_k = 0;
+    abort_s = 0;
+  }
+  // k-block ranges of the width segments (16, 8, 4, 2 bits) and each block's first K word (bytes)
   if (warp == 1 && lane < kMaxKB) {
-    int nb[4], wb[4], sb[4], mb[4], ns[4];
-    int nkb = 0, wsum = 0, ssum = 0, msum = 0;
+    int nb[4], wfirst[4];
+    int nkb = 0, wsum = 0;
 #pragma unroll
     for (int seg = 0; seg < 4; ++seg) {
-      const int w = 16 >> seg, per = 32 / w;
-      const int nslot = hpp->k_words[seg] * per;
-      ns[seg] = nslot;
+      const int w = 16 >> seg;
       nb[seg] = nkb;
-      wb[seg] = wsum;
-      sb[seg] = ssum;
-      mb[seg] = msum;
-      nkb += ceil_div(nslot, 16);
+      wfirst[seg] = wsum;
+      nkb += ceil_div(hpp->k_words[seg] * (32 / w), kKB);
       wsum += hpp->k_words[seg];
-      ssum += nslot;
-      if (w < 16) msum += nslot;
     }
     auto pick = [](const int (&a)[4], int i) { return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : a[3]; };
     if (lane < 4) seg_kb_s[lane] = pick(nb, lane);
     if (lane == 4) seg_kb_s[4] = nkb;
+    uint32_t wb = 0;
     if (lane < nkb) {
       const int seg = (lane >= nb[1]) + (lane >= nb[2]) + (lane >= nb[3]);
-      const int w = 16 >> seg, per = 32 / w;
-      const int nslot = pick(ns, seg);
-      const int s0 = 16 * (lane - pick(nb, seg));
-      KBDesc d;
-      d.wbyte = 128 * (pick(wb, seg) + s0 / per);
-      d.mbyte = 8 * ((w < 16 ? pick(mb, seg) + s0 : 0) / 2);
-      d.nrem = min(16, nslot - s0);
-      d.slot0 = pick(sb, seg) + s0;
-      kbd[lane] = d;
+      const int w = 16 >> seg;
+      wb = 128u * (uint32_t)(pick(wfirst, seg) + (lane - pick(nb, seg)) * (w / 2));
     }
+    kb_wb[lane] = wb;
   }
+  if (tid < kConsumers * kStages) {
+    mbar_init(&full[tid], 1);
+    mbar_init(&empty[tid], 1);
+  }
+  if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (tid < k_slots) slot_s[tid] = sr;
+  __syncthreads();  // next_k, the barriers, the k-block ranges and the slot table are set
 
   auto item_cls = [&](int it) {
     return it < (int)cstart.v[1] ? 0 : it < (int)cstart.v[2] ? 1 : it < (int)cstart.v[3] ? 2 : it < zc_start ? 3 : -1;
   };
-
-  // per-warp ring of shared memory filled by bulk copies (lane 0 issues)
-  unsigned char* wring = ring + (int64_t)warp * P.ring_bytes;
-  uint64_t* wbar = bars + warp * kMaxInflight;
-  int* wpos = ring_pos + warp * kMaxInflight;
-  uint32_t head_p = 0, used = 0;       // lane 0: next write offset; bytes held, wrap waste included
-  int* witem = ring_item + warp * kMaxInflight;  // per slot: (class + 1) << 24 | index within the class
-  uint32_t* wneed = ring_need + warp * kMaxInflight;  // bytes each slot holds, wrap waste included
-  int issued = 0, done = 0;
-  bool drained = warp >= P.ring_warps;  // lane 0: no item left for this warp (warps without a ring take none)
-  int pending = -1;                    // lane 0: item taken but not yet issued (ring full)
-  int cap = kPrologueItems;  // items in flight per warp: fewer before the loop starts
-  auto issue = [&]() {
-    if (issued == done) head_p = used = 0;  // empty ring: start at its beginning
-    while (!drained && issued - done < cap) {
-      int it = pending;
-      if (it < 0) it = isplit + in_split * atomicAdd(&next_k, 1);  // taken in order of need: no warp idles early
-      if (it >= n_items) {
-        if (items_final) drained = true;
-        else pending = it;
-        break;
-      }
-      const int cls = item_cls(it);
-      uint32_t sz, a_bytes = 0;
-      int c_row = 0;
-      if (cls >= 0) {
-        a_bytes = (uint32_t)ctb(cls);
-        sz = (uint32_t)align_up(a_bytes + (cls == 3 ? kTile * D * 2 : 0), 128);
-      } else {
-        c_row = (it - zc_start) * kCRows;
-        sz = 2u * kCRows * D * 2;
-      }
-      // the held bytes end at head_p (circularly); a copy that does not fit before the end of the
-      // ring starts at its beginning and also holds the skipped tail until it is released
-      uint32_t phys = head_p, need = sz;
-      if (phys + sz > (uint32_t)P.ring_bytes) { need += (uint32_t)P.ring_bytes - phys; phys = 0; }
-      if (used + need > (uint32_t)P.ring_bytes) {
-        pending = it;
-        break;
-      }
-      pending = -1;
-      head_p = phys + sz;
-      used += need;
-      const int slot = issued % kMaxInflight;
-      wneed[slot] = need;
-      wpos[slot] = (int)phys;
-      witem[slot] = ((cls + 1) << 24) | (cls >= 0 ? it - (int)cstart(cls) : it - zc_start);
-      unsigned char* dst = wring + phys;
-      uint64_t* bar = &wbar[slot];
-      if (P.arm_only) {
-        // timeout self-test: the stage waits for 16 bytes and no copy is issued, so its wait runs out
-        mbar_arrive_expect_tx(bar, 16u);
-      } else if (cls >= 0) {
-        const int ti = it - (int)cstart(cls);
-        const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
-        mbar_arrive_expect_tx(bar, a_bytes + zb);
-        const uint64_t pol = evict_first_policy();
-        bulk_copy_once(dst, PP.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar, pol);
-        if (zb) bulk_copy_once(dst + a_bytes, PP.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar, pol);
-      } else {
-        // rows of zone C (the fused step's new row, past them, is written by the consumer)
-        const int rows = max(0, min(kCRows, len_c - c_row));
-        const uint32_t bytes = (uint32_t)rows * D * 2;
-        // a zone-C item is 16 rows: one page when zone C is paged
-        const int64_t src = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, head, c_row, D);
-        mbar_arrive_expect_tx(bar, 2 * bytes);
-        if (bytes) {
-          const uint64_t pol = evict_first_policy();
-          bulk_copy_once(dst, PP.zone_c_k + src, bytes, bar, pol);
-          bulk_copy_once(dst + kCRows * D * 2, PP.zone_c_v + src, bytes, bar, pol);
-        }
-      }
-      ++issued;
-    }
-  };
-  if (lane == 0) {
-    for (int k = 0; k < kMaxInflight; ++k) mbar_init(&wbar[k], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (tid < k_slots) slot_s[tid] = sr;
-  __syncthreads();  // next_k, the barriers, the k-block descriptors and the slot table are set
-  if (lane == 0) issue();  // the first zone-A copies fly while the query fragments are built
-  const int nkb = seg_kb_s[4];
-  int seg_kb[5];
-#pragma unroll
-  for (int i = 0; i < 5; ++i) seg_kb[i] = seg_kb_s[i];
-  // Query fragments: B[k = slot pair][n = head g] in slot order (zone A) and channel order (zone C),
-  // at most two per thread.  Which query element each entry takes is static: look it up now.
-  static_assert((kMaxKB + 128 / 16) * 32 <= 2 * kDecWarps * 32, "two query fragments per thread");
-  const int n_frag = (nkb + D / 16) * 32;
-  int fq[2][4];  // element of the group's query rows [G][D] per fragment entry, or -1
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int i = tid + r * kDecWarps * 32;
-    const int kb = i >> 5, ln = i & 31, qq = ln & 3;
-    // the head of column g: zone-A fragments with PK hold heads 0-3 twice (hi and lo columns)
-    const int g = (PK && kb < nkb) ? (ln >> 2) & 3 : ln >> 2;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int off = 2 * qq + (e & 1) + 8 * (e >> 1);
-      int ch = -1;
-      if (i < n_frag && g < G) {
-        if (kb < nkb) {
-          const KBDesc d = kbd[kb];
-          ch = off < d.nrem ? slot_s[d.slot0 + off] : -1;
-        } else {
-          ch = 16 * (kb - nkb) + off;
-        }
-      }
-      fq[r][e] = ch >= 0 ? g * D + ch : -1;
-    }
-  }
-  // Everything so far read only the plan and zone A, which the kernel launched just before this one
-  // on the stream does not write.  The query, the new token and the zone-C length may come from
-  // it: wait for it here (a no-op without programmatic dependent launch).
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  len_c = min(*PP.len_dev, PP.cap_c);
-  n_rows = len_c + (fused ? 1 : 0);
-  n_items = zc_start + ceil_div(n_rows, kCRows);
-  items_final = true;
-  float qf[2][4];
-#pragma unroll
-  for (int r = 0; r < 2; ++r)
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      qf[r][e] = fq[r][e] >= 0 ? load_as_float(P.q, (int64_t)qbase * D + fq[r][e], P.dtype) : 0.f;
-  if (fused && tid < 2 * D) {
-    const int64_t src = (int64_t)head * D + (tid % D);
-    newrow[tid] = half_bits(load_as_float(tid < D ? P.k_new : P.v_new, src, P.dtype));
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int i = tid + r * kDecWarps * 32;
-    if (i < n_frag) {
-      const int kb = i >> 5, ln = i & 31;
-      const float* v = qf[r];
-      if (kb >= nkb) qfragc[(kb - nkb) * 32 + ln] = split_hi_lo(v[0], v[1], v[2], v[3]);
-      else if (QLO) qv[kb * 32 + ln] = make_float4(v[0], v[1], v[2], v[3]);
-      else reinterpret_cast<uint2*>(qv)[kb * 32 + ln] = make_uint2(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]));
-    }
-  }
-  __syncthreads();
-
-  cap = kMaxInflight;
+  // a consumer warp's softmax state and output accumulators (unused in the producer warp)
   WarpAcc<D> acc;
 #pragma unroll
   for (int cm = 0; cm < D / 16; ++cm) acc.o[cm][0] = acc.o[cm][1] = acc.o[cm][2] = acc.o[cm][3] = 0.f;
   acc.z[0] = acc.z[1] = acc.z[2] = acc.z[3] = 0.f;
-  // acc.o holds packed-V products at 2^-24 while this is set; a warp meets the classes in
-  // increasing order (items ascend), so it switches at most once, at its first 16-bit tile or
-  // zone-C block
-  bool o_sub = true;
   acc.m[0] = acc.m[1] = -INFINITY;
   acc.l[0] = acc.l[1] = 0.f;
-  const float sl2 = 1.4426950408889634f / sqrtf((float)D);
-  const int g = lane >> 2, q = lane & 3;
-  bool ok = true;
 
-  while (true) {
-    if (lane == 0) issue();
-    __syncwarp();
-    if (__shfl_sync(0xffffffffu, issued, 0) == done) break;  // nothing in flight and nothing left
-    const int slot = done % kMaxInflight;
-    const bool arrived = mbar_wait(&wbar[slot], (uint32_t)(done / kMaxInflight) & 1u, P.wait_cycles);
-    if (__any_sync(0xffffffffu, !arrived)) {
-      ok = false;
-      break;
-    }
-    const uint32_t st = smem_u32(wring + wpos[slot]);
-    const int rec = witem[slot];
-    const int cls = (rec >> 24) - 1, ti = rec & 0xffffff;  // ti: tile of the class, or zone-C block
-    if (cls >= 0) {
-      const int n_real = min(kTile, (int)cnv(cls) - kTile * ti);
-      const unsigned char* stp = wring + wpos[slot];
-      const unsigned char* kmeta = stp + 4 * kTile * RW;
-      float s[2][4];
-      tile_logits<D, QLO, PK>(stp, kmeta, seg_kb, kbd, qv, lane, s);
-#pragma unroll
-      for (int tb = 0; tb < 2; ++tb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[tb][e] *= sl2;
-      if (n_real < kTile) {  // the last tile of a class: tokens past the kept ones
-#pragma unroll
-        for (int tb = 0; tb < 2; ++tb) {
-          const bool va = 16 * tb + g < n_real, vb = 16 * tb + g + 8 < n_real;
-          s[tb][0] = va ? s[tb][0] : -INFINITY;
-          s[tb][1] = va ? s[tb][1] : -INFINITY;
-          s[tb][2] = vb ? s[tb][2] : -INFINITY;
-          s[tb][3] = vb ? s[tb][3] : -INFINITY;
+  if (warp == kConsumers) {
+    // ------------------------------------------------------------ producer warp
+    // lane w serves consumer warp w: its ring [ring_bytes] holds up to kStages items; an item is
+    // taken from the block's counter when the ring has room for it, copied in with bulk copies that
+    // complete on the stage's full barrier, and its bytes come back when the consumer arrives on the
+    // stage's empty barrier.  After the last item, a stage with the record kItemEnd ends the consumer.
+    const bool serve = lane < kConsumers;
+    const bool has_ring = lane < P.ring_warps;
+    unsigned char* wring = ring + (int64_t)lane * P.ring_bytes;
+    int issued = 0, released = 0, pending = -1;
+    uint32_t head_p = 0, used = 0, need[kStages] = {0u, 0u, 0u, 0u};
+    bool drained = !has_ring, ended = !serve, items_final = false;
+    int n_items = zc_start, len_c = 0;
+    int cap = kPrologueItems;
+    long long idle0 = clock64();
+    bool timed_out = false;
+    auto step = [&]() -> bool {  // one round of this lane's work; true if anything moved
+      bool moved = false;
+      if (ended) return false;
+      // stages the consumer has released
+      while (issued > released && mbar_test(&empty[lane * kStages + released % kStages], (uint32_t)(released / kStages) & 1u)) {
+        used -= need[released % kStages];
+        ++released;
+        moved = true;
+      }
+      if (issued == released) head_p = used = 0;  // empty ring: start at its beginning
+      while (!drained && issued - released < min(cap, kStages)) {
+        int it = pending;
+        if (it < 0) it = isplit + in_split * atomicAdd(&next_k, 1);
+        if (it >= n_items) {
+          if (items_final) drained = true;
+          else pending = it;
+          break;
         }
-      }
-      uint32_t pb[2][2];
-      softmax_update<D, 2>(acc, s, pb);
-      const unsigned char* vcodes = kmeta + 4 * meta_slots;
-      if (cls < 3 && !o_sub) {
-        scale_o(acc, 5.9604644775390625e-8f);
-        o_sub = true;
-      } else if (cls == 3 && o_sub) {
-        scale_o(acc, 16777216.f);
-        o_sub = false;
-      }
-      if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + kTile * D * 2 / 8, lane, pb);
-      else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + kTile * D * 4 / 8, lane, pb);
-      else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + kTile * D * 8 / 8, lane, pb);
-      else pv_fp16<D, 2>(acc, st + (uint32_t)ctb.v[3], lane, pb);
-    } else {
-      if (o_sub) {
-        scale_o(acc, 16777216.f);
-        o_sub = false;
-      }
-      const int c_row = ti * kCRows;
-      const int rows = min(kCRows, n_rows - c_row);  // rows attended (the fused step's new row last)
-      const int copied = max(0, min(kCRows, len_c - c_row));
-      if (rows < kCRows || copied < rows) {
-        uint32_t* kz = reinterpret_cast<uint32_t*>(wring + wpos[slot]);
-        // clear the rows past the attended ones (they meet p = 0 in the products)
-        for (int i = rows * D / 2 + lane; i < kCRows * D / 2; i += 32) {
-          kz[i] = 0u;
-          kz[kCRows * D / 2 + i] = 0u;
+        const int cls = item_cls(it);
+        uint32_t sz, a_bytes = 0;
+        int c_row = 0;
+        if (cls >= 0) {
+          a_bytes = (uint32_t)ctb(cls);
+          sz = (uint32_t)align_up(a_bytes + (cls == 3 ? kTile * D * 2 : 0), 128);
+        } else {
+          c_row = (it - zc_start) * kCRows;
+          sz = 2u * kCRows * D * 2;
         }
-        if (copied < rows) {  // the new row, from the staged copy of the caller's k_new, v_new
-          const uint32_t* nr = reinterpret_cast<const uint32_t*>(newrow);
-          for (int i = lane; i < D / 2; i += 32) {
-            kz[copied * D / 2 + i] = nr[i];
-            kz[kCRows * D / 2 + copied * D / 2 + i] = nr[D / 2 + i];
+        // the held bytes end at head_p (circularly); a copy that does not fit before the end of the
+        // ring starts at its beginning and also holds the skipped tail until it is released
+        uint32_t phys = head_p, nd = sz;
+        if (phys + sz > (uint32_t)P.ring_bytes) { nd += (uint32_t)P.ring_bytes - phys; phys = 0; }
+        if (used + nd > (uint32_t)P.ring_bytes) {
+          pending = it;
+          break;
+        }
+        pending = -1;
+        head_p = phys + sz;
+        used += nd;
+        const int slot = issued % kStages;
+        need[slot] = nd;
+        const int sidx = lane * kStages + slot;
+        st_pos[sidx] = (int)phys;
+        st_item[sidx] = ((cls + 1) << 24) | (cls >= 0 ? it - (int)cstart(cls) : it - zc_start);
+        unsigned char* dst = wring + phys;
+        uint64_t* bar = &full[sidx];
+        if (P.arm_only) {
+          // timeout self-test: the stage waits for 16 bytes and no copy is issued, so its wait runs out
+          mbar_arrive_expect_tx(bar, 16u);
+        } else if (cls >= 0) {
+          const int ti = it - (int)cstart(cls);
+          const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
+          mbar_arrive_expect_tx(bar, a_bytes + zb);
+          const uint64_t pol = evict_first_policy();
+          bulk_copy_once(dst, PP.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar, pol);
+          if (zb) bulk_copy_once(dst + a_bytes, PP.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar, pol);
+        } else {
+          // rows of zone C (the fused step's new row, past them, is written by the consumer)
+          const int rows = max(0, min(kCRows, len_c - c_row));
+          const uint32_t bytes = (uint32_t)rows * D * 2;
+          // a zone-C item is 16 rows: one page when zone C is paged
+          const int64_t src = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, head, c_row, D);
+          mbar_arrive_expect_tx(bar, 2 * bytes);
+          if (bytes) {
+            const uint64_t pol = evict_first_policy();
+            bulk_copy_once(dst, PP.zone_c_k + src, bytes, bar, pol);
+            bulk_copy_once(dst + kCRows * D * 2, PP.zone_c_v + src, bytes, bar, pol);
           }
         }
-        __syncwarp();
+        ++issued;
+        moved = true;
       }
-      float s[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-      const int mi = lane >> 3, r = lane & 7;
-#pragma unroll
-      for (int kb = 0; kb < D / 16; ++kb) {
-        uint32_t a0, a1, a2, a3;
-        const int row = (mi & 1) * 8 + r, col = 16 * kb + (mi >> 1) * 8;
-        ldsm_x4(st + 2u * (row * D + col), a0, a1, a2, a3);
-        const uint4 qf = qfragc[kb * 32 + lane];
-        mma16816(s[0], a0, a1, a2, a3, qf.x, qf.y);
-        if (QLO) mma16816(s[0], a0, a1, a2, a3, qf.z, qf.w);
+      if (drained && issued - released < kStages) {
+        const int sidx = lane * kStages + issued % kStages;
+        st_item[sidx] = kItemEnd;
+        mbar_arrive(&full[sidx]);
+        ended = true;
+        moved = true;
       }
-      const bool va = g < rows, vb = g + 8 < rows;
-      s[0][0] = va ? s[0][0] * sl2 : -INFINITY;
-      s[0][1] = va ? s[0][1] * sl2 : -INFINITY;
-      s[0][2] = vb ? s[0][2] * sl2 : -INFINITY;
-      s[0][3] = vb ? s[0][3] * sl2 : -INFINITY;
-      uint32_t pb[1][2];
-      softmax_update<D, 1>(acc, s, pb);
-      pv_fp16<D, 1>(acc, st + kCRows * D * 2, lane, pb);
+      return moved;
+    };
+    // zone-A items of the prologue: static data only, before the wait for the previous kernel
+    if (serve) step();
+    // The query, the new token and the zone-C length may come from the kernel launched just before
+    // this one on the stream: wait for it here (a no-op without programmatic dependent launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    len_c = min(*PP.len_dev, PP.cap_c);
+    n_items = zc_start + ceil_div(len_c + (fused ? 1 : 0), kCRows);
+    items_final = true;
+    cap = kStages;
+    idle0 = clock64();
+    while (true) {
+      const bool moved = serve && step();
+      if (__all_sync(0xffffffffu, ended)) break;
+      if (__any_sync(0xffffffffu, moved)) {
+        idle0 = clock64();
+      } else {
+        if (clock64() - idle0 > P.wait_cycles || *(volatile int*)&abort_s) {
+          timed_out = true;
+          break;
+        }
+        __nanosleep(64);
+      }
     }
-    // release the stage: order this warp's reads before later bulk writes into it
-    fence_proxy_async();
-    __syncwarp();
-    if (lane == 0) used -= wneed[slot];
-    ++done;
-  }
-  if (!ok) {
-    if (lane == 0) {
-      atomicExch(P.error, (int)RDKV_ERR_TIMEOUT);
-      // wait (bounded) for this warp's copies still in flight before the ring is reused
-      for (int k = done; k < issued; ++k)
-        if (!mbar_wait(&wbar[k % kMaxInflight], (uint32_t)(k / kMaxInflight) & 1u, P.wait_cycles)) break;
+    if (timed_out) {
+      if (lane == 0) {
+        atomicExch(&abort_s, 1);
+        atomicExch(P.error, (int)RDKV_ERR_TIMEOUT);
+      }
     }
     __syncwarp();
-  }
-  __syncthreads();  // every ring drained: the ring area now holds the warps' results
-  if (o_sub) scale_o(acc, 16777216.f);
-  // zero-point sums of packed V: channel 16 cm + g (+8) is in group cm / 2, held by lane (cm / 2, q)
+    // before the ring area is reused: every issued stage's copies have landed (bounded, as a whole)
+    if (serve && *(volatile int*)&abort_s) {
+      const long long t0 = clock64();
+      for (int k = released; k < issued; ++k) {
+        const uint64_t* bar = &full[lane * kStages + k % kStages];
+        while (!mbar_try_wait(const_cast<uint64_t*>(bar), (uint32_t)(k / kStages) & 1u))
+          if (clock64() - t0 > P.wait_cycles) break;
+        if (clock64() - t0 > P.wait_cycles) break;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    // Everything above read only the plan and zone A, which the kernel launched just before this one
+    // on the stream does not write.  The query, the new token and the zone-C length may come from
+    // it: wait for it here (a no-op without programmatic dependent launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int len_c = min(*PP.len_dev, PP.cap_c);
+    const int n_rows = len_c + (fused ? 1 : 0);
+    const int nkb = seg_kb_s[4];
+    const float sl2 = 1.4426950408889634f / sqrtf((float)D);
+    // K B-fragments, built once: entry (k-block kb, lane (g, q)) holds B[slot][column g] for slots
+    // 2q, 2q+1 (.x) and 2q+8, 2q+9 (.y) of the block (and the remainders in .z, .w without PK);
+    // column g is query head g, or with PK head g & 3, hi for g < 4 and lo for g >= 4.  A quantised
+    // slot's value is q * scale * 2^-pos (pos: the bit position its lane's mask leaves the code at).
+    const int s_q0 = k_slots - hpp->meta_slots;   // first quantised slot
+    const uint32_t* kmeta = reinterpret_cast<const uint32_t*>(PP.zone_a + hpp->a_off);  // {scale, zero} per slot
+    for (int i = tid; i < nkb * 32; i += kConsumers * 32) {
+      const int kb = i >> 5, ln = i & 31, qq = ln & 3, gg = ln >> 2;
+      const int seg = (kb >= seg_kb_s[1]) + (kb >= seg_kb_s[2]) + (kb >= seg_kb_s[3]);
+      const int w = 16 >> seg;
+      const int hd = PK ? (gg & 3) : gg;
+      const bool lo_col = PK && gg >= 4;
+      float x[4];
 #pragma unroll
-  for (int cm = 0; cm < D / 16; ++cm) {
-    const float z0 = __shfl_sync(0xffffffffu, acc.z[0], (cm / 2) * 4 + q);
-    const float z1 = __shfl_sync(0xffffffffu, acc.z[1], (cm / 2) * 4 + q);
-    acc.o[cm][0] += z0;
-    acc.o[cm][1] += z1;
-    acc.o[cm][2] += z0;
-    acc.o[cm][3] += z1;
-  }
+      for (int e = 0; e < 4; ++e) {
+        const int off = 2 * qq + (e & 1) + 8 * (e >> 1);
+        const int slot = kKB * kb + off;
+        const int ch = slot_s[slot];
+        float v = 0.f;
+        if (ch >= 0 && hd < G) {
+          v = load_as_float(P.q, (int64_t)(qbase + hd) * D + ch, P.dtype);
+          if (w < 16) {
+            const uint32_t m = __ldg(kmeta + (slot - s_q0));
+            const int pos = w == 2 ? 2 * qq : (w == 4 && (e >> 1)) ? 4 : 0;
+            v *= __half2float(__ushort_as_half((uint16_t)(m & 0xffffu))) * __int_as_float((127 - pos) << 23);
+          }
+        }
+        x[e] = v;
+      }
+      const uint4 t = split_hi_lo(x[0], x[1], x[2], x[3]);
+      bfr[i] = PK ? make_uint4(lo_col ? t.z : t.x, lo_col ? t.w : t.y, 0u, 0u) : t;
+    }
+    // zone-C query fragments: B[k = channel pair][n = head g] in channel order, hi and lo
+    for (int i = tid; i < (D / 16) * 32; i += kConsumers * 32) {
+      const int kb = i >> 5, ln = i & 31, qq = ln & 3, gg = ln >> 2;
+      float x[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int ch = 16 * kb + 2 * qq + (e & 1) + 8 * (e >> 1);
+        x[e] = gg < G ? load_as_float(P.q, (int64_t)(qbase + gg) * D + ch, P.dtype) : 0.f;
+      }
+      qfragc[i] = split_hi_lo(x[0], x[1], x[2], x[3]);
+    }
+    // zero-point term of the quantised K channels per query head (warp h): sum_c q_hc zero_c, base 2
+    if (warp < G) {
+      float acc0 = 0.f;
+      for (int m = lane; m < hpp->meta_slots; m += 32) {
+        const int ch = slot_s[s_q0 + m];
+        if (ch >= 0) {
+          const uint32_t mw = __ldg(kmeta + m);
+          acc0 = fmaf(load_as_float(P.q, (int64_t)(qbase + warp) * D + ch, P.dtype),
+                      __half2float(__ushort_as_half((uint16_t)(mw >> 16))), acc0);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc0 += __shfl_xor_sync(0xffffffffu, acc0, o);
+      if (lane == 0) bias_s[warp] = acc0 * sl2;
+    } else if (warp < 8 && lane == 0) {
+      bias_s[warp] = 0.f;
+    }
+    if (fused && tid < 2 * D) {
+      const int64_t src = (int64_t)head * D + (tid % D);
+      newrow[tid] = half_bits(load_as_float(tid < D ? P.k_new : P.v_new, src, P.dtype));
+    }
+    consumers_sync();
 
-  // warp result -> shared memory: m, l per head; O per head and channel
-  float l0 = acc.l[0], l1 = acc.l[1];
+    // the V class whose scale acc.o carries (2, 4, 8; 16 for fp16 rows); a warp meets the classes
+    // in increasing order (items ascend), so it switches at most four times
+    int o_mode = 2;
+    const int g = lane >> 2, q = lane & 3;
+    const float c24 = 16777216.f * sl2;
+    const bool qlo = P.dtype == RDKV_F32;
+    const float bias0 = bias_s[(2 * q) & 7], bias1 = bias_s[(2 * q + 1) & 7];
+    int seg_kb[5];
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-  }
-  float* rw = red + (int64_t)warp * 8 * (D + 2);
+    for (int i = 0; i < 5; ++i) seg_kb[i] = seg_kb_s[i];
+    uint32_t seg_wb[4];
 #pragma unroll
-  for (int cm = 0; cm < D / 16; ++cm) {
-    rw[(2 * q) * (D + 2) + 16 * cm + g] = acc.o[cm][0];
-    rw[(2 * q + 1) * (D + 2) + 16 * cm + g] = acc.o[cm][1];
-    rw[(2 * q) * (D + 2) + 16 * cm + g + 8] = acc.o[cm][2];
-    rw[(2 * q + 1) * (D + 2) + 16 * cm + g + 8] = acc.o[cm][3];
+    for (int i = 0; i < 4; ++i) seg_wb[i] = kb_wb[min(seg_kb[i], kMaxKB - 1)];
+    const int nrem16 = 2 * hpp->k_words[0] - kKB * (seg_kb[1] - 1);  // real slots of the last raw block
+    unsigned char* wring = ring + (int64_t)warp * P.ring_bytes;
+    bool ok = true;
+    for (int k = 0;; ++k) {
+      const int sidx = warp * kStages + k % kStages;
+      if (!mbar_wait(&full[sidx], (uint32_t)(k / kStages) & 1u, P.wait_cycles)) {
+        ok = false;
+        break;
+      }
+      const int rec = st_item[sidx];
+      if (rec == kItemEnd) break;
+      if (*(volatile int*)&abort_s) {
+        ok = false;
+        break;
+      }
+      const unsigned char* stp = wring + st_pos[sidx];
+      const int cls = (rec >> 24) - 1, ti = rec & 0xffffff;  // ti: tile of the class, or zone-C block
+      if (cls >= 0) {
+        const int n_real = min(kTile, (int)cnv(cls) - kTile * ti);
+        float s[2][4];
+        tile_logits<PK>(stp, seg_kb, seg_wb, nrem16, bfr, lane, c24, bias0, bias1, s);
+        if (n_real < kTile) {  // the last tile of a class: tokens past the kept ones
+#pragma unroll
+          for (int tb = 0; tb < 2; ++tb) {
+            const bool va = 16 * tb + g < n_real, vb = 16 * tb + g + 8 < n_real;
+            s[tb][0] = va ? s[tb][0] : -INFINITY;
+            s[tb][1] = va ? s[tb][1] : -INFINITY;
+            s[tb][2] = vb ? s[tb][2] : -INFINITY;
+            s[tb][3] = vb ? s[tb][3] : -INFINITY;
+          }
+        }
+        uint32_t pb[2][2];
+        softmax_update<D, 2>(acc, s, pb);
+        const int vb_cls = 2 << cls;
+        if (vb_cls != o_mode) {
+          rescale_o<D>(acc, o_mode, vb_cls);
+          o_mode = vb_cls;
+        }
+        const unsigned char* vcodes = stp + 4 * kTile * RW;
+        if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + kTile * D * 2 / 8, lane, pb);
+        else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + kTile * D * 4 / 8, lane, pb);
+        else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + kTile * D * 8 / 8, lane, pb);
+        else pv_fp16<D, 2>(acc, smem_u32(stp) + (uint32_t)ctb.v[3], lane, pb);
+      } else {
+        if (o_mode != 16) {
+          rescale_o<D>(acc, o_mode, 16);
+          o_mode = 16;
+        }
+        const uint32_t st = smem_u32(stp);
+        const int c_row = ti * kCRows;
+        const int rows = min(kCRows, n_rows - c_row);  // rows attended (the fused step's new row last)
+        const int copied = max(0, min(kCRows, len_c - c_row));
+        if (rows < kCRows || copied < rows) {
+          uint32_t* kz = reinterpret_cast<uint32_t*>(const_cast<unsigned char*>(stp));
+          // clear the rows past the attended ones (they meet p = 0 in the products)
+          for (int i = rows * D / 2 + lane; i < kCRows * D / 2; i += 32) {
+            kz[i] = 0u;
+            kz[kCRows * D / 2 + i] = 0u;
+          }
+          if (copied < rows) {  // the new row, from the staged copy of the caller's k_new, v_new
+            const uint32_t* nr = reinterpret_cast<const uint32_t*>(newrow);
+            for (int i = lane; i < D / 2; i += 32) {
+              kz[copied * D / 2 + i] = nr[i];
+              kz[kCRows * D / 2 + copied * D / 2 + i] = nr[D / 2 + i];
+            }
+          }
+          __syncwarp();
+        }
+        float s[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+        const int mi = lane >> 3, r = lane & 7;
+#pragma unroll
+        for (int kb = 0; kb < D / 16; ++kb) {
+          uint32_t a0, a1, a2, a3;
+          const int row = (mi & 1) * 8 + r, col = 16 * kb + (mi >> 1) * 8;
+          ldsm_x4(st + 2u * (row * D + col), a0, a1, a2, a3);
+          const uint4 qf = qfragc[kb * 32 + lane];
+          mma16816(s[0], a0, a1, a2, a3, qf.x, qf.y);
+          if (qlo) mma16816(s[0], a0, a1, a2, a3, qf.z, qf.w);  // fp16 queries have no remainder
+        }
+        const bool va = g < rows, vb = g + 8 < rows;
+        s[0][0] = va ? s[0][0] * sl2 : -INFINITY;
+        s[0][1] = va ? s[0][1] * sl2 : -INFINITY;
+        s[0][2] = vb ? s[0][2] * sl2 : -INFINITY;
+        s[0][3] = vb ? s[0][3] * sl2 : -INFINITY;
+        uint32_t pb[1][2];
+        softmax_update<D, 1>(acc, s, pb);
+        pv_fp16<D, 1>(acc, st + kCRows * D * 2, lane, pb);
+      }
+      // release the stage: order this warp's reads before later bulk writes into it
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sidx]);
+    }
+    if (!ok && lane == 0) {
+      atomicExch(&abort_s, 1);
+      atomicExch(P.error, (int)RDKV_ERR_TIMEOUT);
+    }
+    if (o_mode != 16) rescale_o<D>(acc, o_mode, 16);
+    // zero-point sums of packed V: channel 16 cm + g (+8) is in group cm / 2, held by lane (cm / 2, q)
+#pragma unroll
+    for (int cm = 0; cm < D / 16; ++cm) {
+      const float z0 = __shfl_sync(0xffffffffu, acc.z[0], (cm / 2) * 4 + q);
+      const float z1 = __shfl_sync(0xffffffffu, acc.z[1], (cm / 2) * 4 + q);
+      acc.o[cm][0] += z0;
+      acc.o[cm][1] += z1;
+      acc.o[cm][2] += z0;
+      acc.o[cm][3] += z1;
+    }
+    // the warp's row sums, kept in registers until the rings are free (block barrier below)
+    float l0 = acc.l[0], l1 = acc.l[1];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    acc.l[0] = l0;
+    acc.l[1] = l1;
   }
-  if (g == 0) {
-    rw[(2 * q) * (D + 2) + D] = acc.m[0];
-    rw[(2 * q + 1) * (D + 2) + D] = acc.m[1];
-    rw[(2 * q) * (D + 2) + D + 1] = l0;
-    rw[(2 * q + 1) * (D + 2) + D + 1] = l1;
+  __syncthreads();  // every ring drained: the ring area now holds the consumer warps' results
+  if (warp < kConsumers) {
+    const int g = lane >> 2, q = lane & 3;
+    float* rw = red + (int64_t)warp * 8 * (D + 2);
+#pragma unroll
+    for (int cm = 0; cm < D / 16; ++cm) {
+      rw[(2 * q) * (D + 2) + 16 * cm + g] = acc.o[cm][0];
+      rw[(2 * q + 1) * (D + 2) + 16 * cm + g] = acc.o[cm][1];
+      rw[(2 * q) * (D + 2) + 16 * cm + g + 8] = acc.o[cm][2];
+      rw[(2 * q + 1) * (D + 2) + 16 * cm + g + 8] = acc.o[cm][3];
+    }
+    if (g == 0) {
+      rw[(2 * q) * (D + 2) + D] = acc.m[0];
+      rw[(2 * q + 1) * (D + 2) + D] = acc.m[1];
+      rw[(2 * q) * (D + 2) + D + 1] = acc.l[0];
+      rw[(2 * q + 1) * (D + 2) + D + 1] = acc.l[1];
+    }
   }
   __syncthreads();
-  // combine the warps; write this block's partial result (m, l, unnormalised o) for the G heads;
-  // one block's partial takes pstride floats
+  // combine the consumer warps; write this block's partial result (m, l, unnormalised o) for the G
+  // heads; one block's partial takes pstride floats
   const int pstride = partial_stride(G, D);
   float* part = P.partial + (int64_t)first_block * pstride;
   float* mine = part + (int64_t)split * pstride;
@@ -1084,10 +1057,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   // weighted by 2^(m_w - M) (the m (c = D) entry holds M)
   for (int i = tid; i < G * (D + 2); i += blockDim.x) {
     const int h = i / (D + 2), c = i % (D + 2);
-    float mw[kDecWarps];
+    float mw[kConsumers];
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
+    for (int w = 0; w < kConsumers; ++w) {
       mw[w] = red[((int64_t)w * 8 + h) * (D + 2) + D];
       M = fmaxf(M, mw[w]);
     }
@@ -1096,7 +1069,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       val = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) val = fmaf(ex2(mw[w] - M), red[((int64_t)w * 8 + h) * (D + 2) + c], val);
+        for (int w = 0; w < kConsumers; ++w) val = fmaf(ex2(mw[w] - M), red[((int64_t)w * 8 + h) * (D + 2) + c], val);
       }
     }
     mine[i] = val;
@@ -1113,6 +1086,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   if (fused) {
     // every block of this head has read zone C: store the new row of this head; the last head to
     // get here advances the length (every block of every head has read it by then)
+    const int len_c = min(*PP.len_dev, PP.cap_c);
     if (len_c < P.cap_c) {
       const int64_t dst = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, head, len_c, D);
       for (int i = tid; i < D; i += blockDim.x) {
@@ -1189,18 +1163,18 @@ static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n) {
   const int D = s.head_dim, G = s.h_q / s.h_kv;
   const int n_heads = s.batch * s.h_kv;
   const int sms = num_sms();
-  const int64_t fixed = decode_fixed_smem(D, s.dtype == RDKV_F32);
+  const int64_t fixed = decode_fixed_smem(D);
   int64_t max_item = 2 * kCRows * D * 2, items = 0;
   for (int p = 0; p < n; ++p) {
     max_item = std::max<int64_t>(max_item, align_up(parts[p]->sizes.max_stage_bytes, 128));
     items += ceil_div64(parts[p]->sizes.index_slots, kTile) + (int64_t)n_heads * ceil_div(parts[p]->cap_c, kCRows);
   }
   g.max_item = max_item;
-  // one block of kDecWarps warps per SM; the warps with a ring share what is left equally: all of
-  // them, or half (a quarter) with twice (four times) the ring when the largest staged tile needs it
-  int ring_warps = kDecWarps;
+  // one block per SM; the consumer warps with a ring share what is left equally: all of them, or
+  // half (a quarter) with twice (four times) the ring when the largest staged tile needs it
+  int ring_warps = kConsumers;
   int64_t ring = ((kDecodeSmemLimit - fixed) / ring_warps) / 128 * 128;
-  while (ring < max_item && ring_warps > kDecWarps / 4) {
+  while (ring < max_item && ring_warps > kConsumers / 4) {
     ring_warps /= 2;
     ring = ((kDecodeSmemLimit - fixed) / ring_warps) / 128 * 128;
   }
@@ -1210,13 +1184,13 @@ static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n) {
   g.ring_warps = ring_warps;
   g.smem = (size_t)(fixed + (int64_t)ring_warps * ring);
   // blocks dealt to heads in proportion to their work: a nominal count that fills every SM once,
-  // fewer when there is little work (at least kDecWarps items per block on average).
+  // fewer when there is little work (at least kConsumers items per block on average).
   // With few heads, leave one SM per head free: the last block of each head merges after the
   // others have left, and on those SMs the next call's blocks would otherwise start only after
   // the merge, with their whole set-up still ahead of them.
   const int free_sms = n_heads <= sms / 16 ? n_heads : 0;
   g.ctas = (int)std::max<int64_t>(
-      1, std::min<int64_t>((int64_t)blocks_per_sm * (sms - free_sms), ceil_div64(items, kDecWarps)));
+      1, std::min<int64_t>((int64_t)blocks_per_sm * (sms - free_sms), ceil_div64(items, kConsumers)));
   g.splits = g.ctas + n_heads * n;  // grid size: room for at least one block per (cache, head)
   g.partial_bytes = (size_t)align_up((int64_t)g.splits * partial_stride(G, D) * 4, 256);
   g.ticket_off = g.partial_bytes;
@@ -1225,9 +1199,7 @@ static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n) {
 static DecodeGeom decode_geom(const rdkv_cache* c) { return decode_geom(&c, 1); }
 
 // ws: partials, then per-head tickets, the status word and the fused step's head counter
-static size_t decode_ws_bytes(const DecodeGeom& g, int n_heads) {
-  return g.ticket_off + (size_t)align_up(((int64_t)n_heads + 2) * 4, 256);
-}
+static size_t decode_ws_bytes(const DecodeGeom& g, int n_heads) { return g.ticket_off + (size_t)decode_ticket_bytes(n_heads); }
 
 rdkv_status check_cache_public(const rdkv_cache* c);
 
@@ -1336,19 +1308,16 @@ static rdkv_status launch_decode(const DecodeParams& P, const DecodeGeom& geo, c
                                  bool pdl) {
   // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is
   // captured); threads that get here together may both raise it, to the same value
-  static std::atomic<size_t> smem_set[6][64];
+  static std::atomic<size_t> smem_set[4][64];
   int dev = 0;
   RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
-  const bool qlo = s.dtype == RDKV_F32;
-  // fp16 queries and at most 4 heads per KV head: hi and lo share one MMA per K block
-  const bool pk = !qlo && s.h_q / s.h_kv <= 4;
-  const int ki = (s.head_dim == 128 ? 3 : 0) + (qlo ? 1 : pk ? 2 : 0);
-  void (*const fn)(DecodeParams) = ki == 4 ? decode_kernel<128, true, false>
-                                 : ki == 5 ? decode_kernel<128, false, true>
-                                 : ki == 3 ? decode_kernel<128, false, false>
-                                 : ki == 1 ? decode_kernel<64, true, false>
-                                 : ki == 2 ? decode_kernel<64, false, true>
-                                           : decode_kernel<64, false, false>;
+  // at most 4 query heads per KV head: the hi and lo parts of the K operand share one MMA per block
+  const bool pk = s.h_q / s.h_kv <= 4;
+  const int ki = (s.head_dim == 128 ? 2 : 0) + (pk ? 1 : 0);
+  void (*const fn)(DecodeParams) = ki == 3 ? decode_kernel<128, true>
+                                 : ki == 2 ? decode_kernel<128, false>
+                                 : ki == 1 ? decode_kernel<64, true>
+                                           : decode_kernel<64, false>;
   if (dev < 64 && geo.smem > smem_set[ki][dev].load(std::memory_order_acquire)) {
     RDKV_TRY_CUDA(cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kDecodeSmemLimit),

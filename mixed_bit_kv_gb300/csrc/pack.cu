@@ -8,7 +8,8 @@
 //   zero = fp16(min), scale = fp16(fl32(max - min) / (2^b - 1)),
 //   code = clamp(rint((x - zero) / scale), 0, 2^b - 1)   (IEEE fp32, ties to even)
 // V groups are 32 consecutive channels of a token; K groups are one channel
-// over the real tokens of a 32-token tile.  Layout rules: include/rdkv.h.
+// over every kept prefix token of its (sequence, KV head), whose scale and zero
+// are stored once in front of the head's tiles.  Layout rules: include/rdkv.h.
 #include "common.cuh"
 
 namespace rdkv {
@@ -136,13 +137,43 @@ __global__ void __launch_bounds__(1024) index_kernel(const uint8_t* __restrict__
     for (int r = hp.n_v[c] + tid; r < kTile * hp.tiles[c]; r += blockDim.x) out[start[c] + r] = -1;
 }
 
+// ---------------------------------------------------------------- head K metadata
+// One block per (sequence, KV head): fp16 scale and zero of every quantised K slot from the channel's
+// minimum and maximum over the head's kept tokens (the allocation's channel statistics in the plan),
+// in slot order from the first 8-bit slot; pads and the tail up to 16 bytes are zero.
+__global__ void head_meta_kernel(const void* __restrict__ plan, const float2* __restrict__ kstat, int D,
+                                 uint8_t* __restrict__ zone_a) {
+  const int head = blockIdx.x;
+  const rdkv_plan_header* hdr = plan_header(plan);
+  const rdkv_head_plan& hp = plan_heads(plan)[head];
+  const int16_t* slot_ch = plan_slots(plan) + (int64_t)head * hdr->slot_stride;
+  const int QS = hp.meta_slots, s_q0 = hp.k_slots - QS;
+  const int sb4 = s_q0 + kKB * ceil_div(4 * hp.k_words[1], kKB);   // first 4-bit slot
+  const int sb2 = sb4 + kKB * ceil_div(8 * hp.k_words[2], kKB);    // first 2-bit slot
+  uint32_t* out = reinterpret_cast<uint32_t*>(zone_a + hp.a_off);
+  const int n_words = (int)(head_meta_bytes(QS) / 4);
+  for (int m = threadIdx.x; m < n_words; m += blockDim.x) {
+    uint32_t v = 0;
+    const int s = s_q0 + m;
+    const int c = m < QS ? slot_ch[s] : -1;
+    if (c >= 0) {
+      const int b = s < sb4 ? 8 : s < sb2 ? 4 : 2;
+      const float2 st = kstat[(int64_t)head * D + c];
+      const QParams p = qparams(st.x, st.y, b);
+      v = (uint32_t)p.scale_h | ((uint32_t)p.zero_h << 16);
+    }
+    out[m] = v;
+  }
+}
+
 // ---------------------------------------------------------------- tile pack
 // One block (256 threads) per zone-A tile: stage the tile's K and V rows as floats, then the
-// quantiser statistics of every K slot and V group, then the K words and the V codes, then the V
-// words.  A K word is built by the lane of its token from the codes of the word's slots (warps
-// along words, lanes along tokens; K rows are padded to D + 1 floats so that the 32 lanes read 32
-// banks, and the 32 lanes store 32 adjacent words of the word-major layout).  V codes go through
-// shared memory as bytes; a V word is assembled from a pair's two code rows.
+// quantiser parameters of every K slot (from the head's channel statistics) and V group, then the K
+// words and the V codes, then the V words.  A K word is built by the lane of its token from the
+// codes of the word's slots (warps along words, lanes along tokens; K rows are padded to D + 1
+// floats so that the 32 lanes read 32 banks, and the 32 lanes store 32 adjacent words of the
+// word-major layout).  V codes go through shared memory as bytes; a V word is assembled from a
+// pair's two code rows.
 constexpr int kPackThreads = 256;
 // Four consecutive elements as floats (8-byte load for fp16, 16-byte for fp32; the address is a
 // multiple of four elements).
@@ -154,13 +185,6 @@ __device__ __forceinline__ float4 load4(const __half* p) {
 }
 __device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-// `n` (2, 4 or 8) consecutive code bytes of a V code row, as one little-endian integer.
-__device__ __forceinline__ uint64_t code_bytes(const uint8_t* p, int n) {
-  if (n == 8) return *reinterpret_cast<const uint64_t*>(p);
-  if (n == 4) return *reinterpret_cast<const uint32_t*>(p);
-  return *reinterpret_cast<const uint16_t*>(p);
-}
-
 template <int D>
 __host__ __device__ constexpr size_t pack_smem_bytes_of() {
   return (size_t)kTile * (D + 1) * 4 + (size_t)kTile * D * 4 + (size_t)kTile * D + (size_t)(D + kSlotPad) * 12 +
@@ -170,6 +194,7 @@ __host__ __device__ constexpr size_t pack_smem_bytes_of() {
 template <typename T, int D>
 __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __restrict__ k, const T* __restrict__ v,
                                                                   const void* __restrict__ plan,
+                                                                  const float2* __restrict__ kstat,
                                                                   const int32_t* __restrict__ index_map,
                                                                   uint8_t* __restrict__ zone_a,
                                                                   uint16_t* __restrict__ zone_b, int N, int h_kv) {
@@ -196,7 +221,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   const rdkv_head_plan& hp = hps;
   const int b = head / h_kv, j = head % h_kv;
   int ti = (int)((slot0 - hp.slot_off) / kTile), cls = 0;
-  int64_t tile_off = hp.a_off;
+  int64_t tile_off = hp.a_off + head_meta_bytes(hp.meta_slots);
   int64_t brow = hp.b_row;
   while (ti >= hp.tiles[cls]) {
     ti -= hp.tiles[cls];
@@ -209,10 +234,10 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   const int n_real = min(kTile, hp.n_v[cls] - ti * kTile);
   const int RW = hp.row_words, KS = hp.k_slots;
   const int16_t* slot_ch = plan_slots(plan) + (int64_t)head * hdr->slot_stride;
-  // width segments of the slots (16, 8, 4, 2 bits) and of the words
-  const int s16 = 2 * hp.k_words[0];          // first 8-bit slot (the raw 16-bit slots come first)
-  const int sb4 = s16 + 4 * hp.k_words[1];    // first 4-bit slot
-  const int sb2 = sb4 + 8 * hp.k_words[2];    // first 2-bit slot
+  // width segments of the slots (16, 8, 4, 2 bits; each spans whole k-blocks) and of the words
+  const int s16 = kKB * ceil_div(2 * hp.k_words[0], kKB);    // first 8-bit slot (the raw 16-bit slots come first)
+  const int sb4 = s16 + kKB * ceil_div(4 * hp.k_words[1], kKB);  // first 4-bit slot
+  const int sb2 = sb4 + kKB * ceil_div(8 * hp.k_words[2], kKB);  // first 2-bit slot
   const int w8 = hp.k_words[0], w4 = w8 + hp.k_words[1], w2 = w4 + hp.k_words[2];  // first word of each
 
   float* Kf = reinterpret_cast<float*>(smem_raw);               // [32][KP]
@@ -246,28 +271,20 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   __syncthreads();
 
   uint8_t* tile = zone_a + tile_off;
-  uint16_t* kmeta = reinterpret_cast<uint16_t*>(tile + 4 * kTile * RW);
-  uint8_t* vcode = tile + 4 * kTile * RW + 4 * hp.meta_slots;
+  uint8_t* vcode = tile + 4 * kTile * RW;
   uint16_t* vmeta = reinterpret_cast<uint16_t*>(vcode + kTile * D * vbits / 8);
-  // statistics: K slot s (quantised slots only), then V group (r, g)
+  // quantiser parameters: K slot s (quantised slots only: the head's channel statistics), then V
+  // group (r, g) of the tile
   for (int i = tid; i < KS + (vbits < 16 ? kTile * NG : 0); i += kPackThreads) {
     if (i < KS) {
       const int s = i;
       if (s < s16) continue;
       const int kb = s < sb4 ? 8 : s < sb2 ? 4 : 2;
       const int c = sch[s];
-      const int m = s - s16;  // index among the quantised slots
-      uint16_t sc_h = 0, ze_h = 0;
       float z = 0.f, sc = 0.f, rs = 0.f;
-      if (c >= 0 && n_real > 0) {
-        float mn = Kf[c], mx = Kf[c];
-        for (int r = 1; r < n_real; ++r) {
-          mn = fminf(mn, Kf[r * KP + c]);
-          mx = fmaxf(mx, Kf[r * KP + c]);
-        }
-        const QParams p = qparams(mn, mx, kb);
-        sc_h = p.scale_h;
-        ze_h = p.zero_h;
+      if (c >= 0) {
+        const float2 st = kstat[(int64_t)head * D + c];
+        const QParams p = qparams(st.x, st.y, kb);
         z = p.zero;
         sc = p.scale;
         rs = sc != 0.f ? __frcp_rn(sc) : 0.f;
@@ -275,8 +292,6 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
       kq[3 * s] = z;
       kq[3 * s + 1] = sc;
       kq[3 * s + 2] = rs;
-      kmeta[4 * (m >> 1) + (m & 1)] = sc_h;
-      kmeta[4 * (m >> 1) + 2 + (m & 1)] = ze_h;
     } else {
       const int vi = i - KS, r = vi / NG, g = vi % NG;
       const float* x = Vf + r * D + g * kVGroup;
@@ -301,9 +316,11 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
       vq[3 * vi] = z;
       vq[3 * vi + 1] = sc;
       vq[3 * vi + 2] = rs;
-      const int pp = r >> 1, mm = r & 1;
-      vmeta[(pp * NG + g) * 4 + mm] = sc_h;
-      vmeta[(pp * NG + g) * 4 + 2 + mm] = ze_h;
+      // token pair p = 8 tb + q + 4 h: scales ordered (tb, q, h, group), zeros (tb, group, q, h), each
+      // 32-bit word the pair's even token (low half) and odd token (high half)
+      const int pp = r >> 1, tb = pp >> 3, q = pp & 3, h = (pp >> 2) & 1;
+      vmeta[2 * (((tb * 4 + q) * 2 + h) * NG + g) + (r & 1)] = sc_h;
+      vmeta[2 * (16 * NG + ((tb * NG + g) * 4 + q) * 2 + h) + (r & 1)] = ze_h;
     }
   }
   if (vbits == 16) {
@@ -322,16 +339,18 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
     const float* kr = Kf + r * KP;
     uint32_t* kw = reinterpret_cast<uint32_t*>(tile);
     for (int w = ty; w < RW; w += kPackThreads / 32) {
-      int kb, s0;
-      if (w < w8) { kb = 16; s0 = 2 * w; }
-      else if (w < w4) { kb = 8; s0 = s16 + 4 * (w - w8); }
-      else if (w < w2) { kb = 4; s0 = sb4 + 8 * (w - w4); }
-      else { kb = 2; s0 = sb2 + 16 * (w - w2); }
-      const int per = 32 / kb;
+      // segment width, first slot of the word's k-block and the word's index inside that block
+      int kb, sbase, wg;
+      if (w < w8) { kb = 16; sbase = 0; wg = w; }
+      else if (w < w4) { kb = 8; sbase = s16; wg = w - w8; }
+      else if (w < w2) { kb = 4; sbase = sb4; wg = w - w4; }
+      else { kb = 2; sbase = sb2; wg = w - w2; }
+      const int per = 32 / kb, wpk = kb / 2;
+      const int s0 = sbase + kKB * (wg / wpk), wi = wg % wpk;
       const float hmax = (float)((1 << kb) - 1);
       uint32_t word = 0;
       for (int e = 0; e < per; ++e) {
-        const int s = s0 + e;
+        const int s = s0 + k_slot_in_block(kb, wi, e);
         const int c = sch[s];
         if (c < 0 || !real) continue;
         const float x = kr[c];
@@ -353,23 +372,26 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
     }
   }
   __syncthreads();
-  // V words: pair p, word w holds channels [w*16/b, (w+1)*16/b) of tokens 2p (low half) and 2p+1 (high
-  // half); inside a pair, word w sits at (w mod R) wpp/R + w/R with R = b/2, so the words a decode lane
-  // needs (channels congruent to its own mod 8) are adjacent
+  // V words: word i of the tile is word wk of pair h of lane (g, q) of 16-token block tb,
+  // i = ((tb * 8 + g) * 4 + q) * 2 nw + h nw + wk (nw = D b / 128); it holds entries k = wk per + e
+  // (per = 16 / b) of the lane's channel list, channel 16 (k mod D/16) + 8 (k div D/16) + g, at bit
+  // b e for token 2p (low half) and 16 + b e for token 2p + 1, p = 8 tb + q + 4 h
   if (vbits < 16) {
     uint32_t* vw = reinterpret_cast<uint32_t*>(vcode);
-    const int wpp = D * vbits / 16, per = 16 / vbits, R = vbits / 2;
-    const int lw = __ffs(wpp) - 1;  // wpp is a power of two
-    for (int i = tid; i < (kTile / 2) * wpp; i += kPackThreads) {
-      const int p = i >> lw, w = i & (wpp - 1);
-      const uint64_t lo_b = code_bytes(vc + (2 * p) * D + w * per, per);
-      const uint64_t hi_b = code_bytes(vc + (2 * p + 1) * D + w * per, per);
+    constexpr int CM = D / 16;
+    const int nw = D * vbits / 128, per = 16 / vbits;
+    for (int i = tid; i < D * vbits; i += kPackThreads) {
+      const int wk = i % nw, rest = i / nw;
+      const int h = rest & 1, q = (rest >> 1) & 3, g = (rest >> 3) & 7, tb = rest >> 6;
+      const int p = 8 * tb + q + 4 * h;
       uint32_t word = 0;
       for (int e = 0; e < per; ++e) {
-        word |= (uint32_t)((lo_b >> (8 * e)) & 255u) << (vbits * e);
-        word |= (uint32_t)((hi_b >> (8 * e)) & 255u) << (16 + vbits * e);
+        const int kk = wk * per + e;
+        const int c = 16 * (kk % CM) + 8 * (kk / CM) + g;
+        word |= (uint32_t)vc[(2 * p) * D + c] << (vbits * e);
+        word |= (uint32_t)vc[(2 * p + 1) * D + c] << (16 + vbits * e);
       }
-      vw[p * wpp + (w % R) * (wpp / R) + w / R] = word;
+      vw[i] = word;
     }
   }
 }
@@ -416,9 +438,11 @@ static rdkv_status launch_pack_tiles(const void* k, const void* v, const rdkv_ca
   const size_t smem = pack_smem_bytes_of<D>();
   RDKV_TRY_CUDA(cudaFuncSetAttribute(pack_tile_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
                 "pack smem");
+  const PlanLayout L = plan_layout(cache->shape.batch, cache->shape.h_kv, D);
+  const float2* kstat = reinterpret_cast<const float2*>(static_cast<const char*>(cache->plan) + L.kstat_off);
   pack_tile_kernel<T, D><<<(unsigned)n_tiles, kPackThreads, smem, cs>>>(
-      static_cast<const T*>(k), static_cast<const T*>(v), cache->plan, cache->index_map, cache->zone_a, cache->zone_b,
-      cache->shape.n_tokens, cache->shape.h_kv);
+      static_cast<const T*>(k), static_cast<const T*>(v), cache->plan, kstat, cache->index_map, cache->zone_a,
+      cache->zone_b, cache->shape.n_tokens, cache->shape.h_kv);
   RDKV_CHECK_LAUNCH("tile pack");
   return RDKV_OK;
 }
@@ -460,6 +484,13 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
   (void)bits_chan;  // the channel widths reach the pack through the plan's slot table
   cudaStream_t cs = (cudaStream_t)stream;
   const int n_heads = s.batch * s.h_kv;
+  if (Np > 0 && cache->sizes.zone_a_bytes > 0) {
+    const PlanLayout L = plan_layout(s.batch, s.h_kv, D);
+    head_meta_kernel<<<n_heads, 128, 0, cs>>>(
+        cache->plan, reinterpret_cast<const float2*>(static_cast<const char*>(cache->plan) + L.kstat_off), D,
+        cache->zone_a);
+    RDKV_CHECK_LAUNCH("head K metadata");
+  }
   if (Np > 0 && cache->sizes.index_slots > 0) {
     index_kernel<<<n_heads, 1024, 0, cs>>>(bits_tok, Np, cache->plan, cache->index_map);
     RDKV_CHECK_LAUNCH("index map");
@@ -499,7 +530,7 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
 // Upper bounds of the plan totals (per sequence, then times the batch).  Every kept token costs at
 // least 2 of the sequence's B_V bits and a 16-bit one 16; each (head, class) segment is padded to
 // whole tiles; a K row holds sum_c b_c bits plus at most one padding word per width segment, and the
-// K widths of a sequence sum to at most B_K; a tile carries at most D + kSlotPad metadata slots.
+// K widths of a sequence sum to at most B_K; a head's K metadata covers at most D + kSlotPad slots.
 extern "C" rdkv_status rdkv_zone_bounds(const rdkv_shape* s, float avg_bits_v, float avg_bits_k, rdkv_sizes* out) {
   rdkv_status st = check_shape(s);
   if (st != RDKV_OK) return st;
@@ -514,16 +545,16 @@ extern "C" rdkv_status rdkv_zone_bounds(const rdkv_shape* s, float avg_bits_v, f
   const int64_t tiles = ceil_div64(kept, kTile) + 4 * H;                 // sum over (head, class) of ceil(n / 32)
   const int64_t t_head = ceil_div64(std::min<int64_t>(Np, kept), kTile) + 4;  // tiles of one head
   const int64_t rw_sum = ceil_div64(BK, 32) + 4 * H;                      // row words of all heads
-  const int64_t k_bytes = t_head * 4 * kTile * rw_sum + tiles * 4 * (D + kSlotPad);
+  const int64_t k_bytes = t_head * 4 * kTile * rw_sum + H * head_meta_bytes((int)(D + kSlotPad));
   const int64_t v_bytes = D * (std::min<int64_t>(BV, 8 * UV) / 8) + H * 4 * (kTile - 1) * D + tiles * 4 * D;
   const int64_t b = s->batch;
   out->zone_a_bytes = b * (k_bytes + v_bytes);
   out->zone_b_rows = b * kTile * (ceil_div64(n16, kTile) + H);
   out->index_slots = b * kTile * tiles;
   out->kept_tokens = b * kept;
-  const int rw_max = (int)(D / 2 + 4), meta_max = (int)(D + kSlotPad);
-  out->max_tile_bytes = tile_bytes_of(rw_max, meta_max, (int)D, 8);
-  out->max_stage_bytes = std::max<int64_t>(out->max_tile_bytes, tile_bytes_of(rw_max, meta_max, (int)D, 16) + kTile * D * 2);
+  const int rw_max = (int)(D / 2 + 4);
+  out->max_tile_bytes = tile_bytes_of(rw_max, (int)D, 8);
+  out->max_stage_bytes = std::max<int64_t>(out->max_tile_bytes, tile_bytes_of(rw_max, (int)D, 16) + kTile * D * 2);
   out->status = RDKV_OK;
   out->n_heads = (int32_t)(b * H);
   for (int i = 0; i < RDKV_COST_HEADS; ++i) out->head_cost[i] = 0;

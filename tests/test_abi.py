@@ -227,11 +227,17 @@ def test_shape_workspace_query(L):
     assert L.rdkv_workspace_bytes(ctypes.byref(s), 99) == 0
     bad = rdkv.make_shape(1, 32768, 24, 8, 96, 128, "f16")
     assert L.rdkv_workspace_bytes(ctypes.byref(bad), rdkv.RDKV_CALL_SCORE) == 0
-    # the decode bound covers the cache-exact query
-    for shape in (rdkv.make_shape(1, 64, 4, 1, 64, 8, "f16"), rdkv.make_shape(2, 4096, 32, 8, 128, 128, "f16")):
-        n_heads = shape.batch * shape.h_kv
-        sizes = rdkv.Sizes(0, 0, 0, 0, 0, 0, 0, n_heads)
-        c = rdkv.CacheStruct(shape, 256, None, None, 256, 256, None, 256, shape.window + 8, shape.window, sizes)
-        exact = L.rdkv_decode_workspace_bytes(ctypes.byref(c))
-        assert exact > 0
-        assert L.rdkv_workspace_bytes(ctypes.byref(shape), rdkv.RDKV_CALL_DECODE) >= exact
+    # the decode bound covers the cache-exact query: group sizes 1, 3, 4, 8, both head sizes, batches up
+    # to 8, plans with few and with many tiles (index slots) and zone-C capacities from 0 to 4096 rows
+    for G in (1, 3, 4, 8):
+        for D in (64, 128):
+            for batch, h_kv in ((1, 1), (2, 4), (8, 8)):
+                for slots, extra in ((0, 0), (32 * 7, 8), (32 * 5000, 300), (32 * 200000, 4096)):
+                    shape = rdkv.make_shape(batch, 4096, G * h_kv, h_kv, D, 128, "f16")
+                    n_heads = batch * h_kv
+                    sizes = rdkv.Sizes(1 << 20, 64, slots, slots, 4096, 4096, 0, n_heads)
+                    c = rdkv.CacheStruct(shape, 256, 256, 256, 256, 256, 256, 256, 128 + extra, 128, sizes)
+                    exact = L.rdkv_decode_workspace_bytes(ctypes.byref(c))
+                    assert exact > 0, (G, D, batch, slots)
+                    assert L.rdkv_workspace_bytes(ctypes.byref(shape), rdkv.RDKV_CALL_DECODE) >= exact, \
+                        (G, D, batch, h_kv, slots, extra)

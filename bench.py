@@ -276,6 +276,7 @@ def run_ours(args, ws, rank, local):
     dec_bytes = sum(decode_bytes_per_call(h, w.head_dim, w.h_q, w.batch, w.window + s + 1)
                     for h in heads_per_layer for s in range(S))
     kept = sum(int(np.sum(h["n_v"])) for h in heads_per_layer) / (L * w.batch * w.h_kv * w.n_prefix)
+    tiles_per_launch = sum(int(np.sum(h["tiles"])) for h in heads_per_layer) / L
     zone_bytes_layer = sum(int(c.c.sizes.zone_a_bytes) + int(c.c.sizes.zone_b_rows) * w.head_dim * 2
                            for c in caches) / L
 
@@ -381,6 +382,7 @@ def run_ours(args, ws, rank, local):
         "decode_us_per_layer_step": round(dec_ms_step * 1e3 / (S * L), 3),
         "decode_ms_per_model_step": round(dec_ms_step / S, 4),
         "decode_bytes_per_step": int(dec_bytes),
+        "decode_tiles_per_launch": int(round(tiles_per_launch)),
         "scorer_tflops": round(score_tflops, 2), "scorer_ms_per_layer": round(score_ms_step / L, 3),
         "compress_ms_per_layer": round((ms_per_step - dec_ms_step) / L, 3),
         "compress_breakdown_ms_per_layer": {

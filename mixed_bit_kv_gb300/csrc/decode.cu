@@ -55,10 +55,11 @@ constexpr long long kMinWaitCycles = 100000;     // shortest limit the timeout s
 
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings): the K B-fragments
 // (16 bytes per k-block and lane), zone-C query fragments, slot table, k-block offsets, stage
-// barriers and records, the fused step's new row.
+// barriers and records, the fused step's new row, the head's K metadata and the group's query rows.
 __host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
   return ((int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + (int64_t)(D + kSlotPad) * 2 + kMaxKB * 8 +
-          (int64_t)kConsumers * kStages * 24 + (int64_t)2 * D * 2 + 127) /
+          (int64_t)kConsumers * kStages * 24 + (int64_t)2 * D * 2 + (int64_t)(D + kSlotPad) * 4 +
+          (int64_t)8 * D * 4 + 127) /
          128 * 128;
 }
 // Floats of one block's partial result (m, l, o for G heads), rounded up to a multiple of 4.
@@ -145,8 +146,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait; false when the limit (clock64 cycles) ran out.
+// Bounded wait; false when the limit (clock64 cycles) ran out.  The clock is read only when the
+// first probe finds the phase still open.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > limit) return false;
@@ -303,27 +306,27 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
 }
 
 // K logits of one width segment W of a zone-A tile, k-blocks [kb0, kb1) (the segment's blocks are
-// consecutive: 64 W bytes of words apart, the first at wb0).  Lane (g, q) reads tokens g, g+8,
-// g+16, g+24 of its word of each block (one 16-byte load) and makes its two A registers per
-// token with one mask each (W = 2: bits 2q and, after a shift by 8, 2q + 8; W = 4: bits 0 and 4
-// after a shift by 8 (q & 1); W = 8: bytes 0, 2 and 1, 3); B (built once per block) carries
-// the 2^-pos of those positions.  PK: hi and lo share one MMA (B columns 0-3 hi, 4-7 lo); else
-// hi products go to shi and lo products to slo.
+// consecutive: 64 W bytes of words apart, the first at wb0).  Lane (g, q) reads tokens g, g+8, g+16,
+// g+24 of its word of each block (one 16-byte load) and makes its two A registers per token with
+// one mask each (W = 2: bits 2q and, after a shift by 8, 2q + 8; W = 4: bits 0 and 4 after a shift
+// by 8 (q & 1); W = 8: bytes 0, 2 and 1, 3); B (built once per block) carries the 2^-pos of those
+// positions.  PK: hi and lo share one MMA (B columns 0-3 hi, 4-7 lo); else hi products go to shi and
+// lo products to slo.
 template <int W, bool PK>
 __device__ __forceinline__ void k_segment(const unsigned char* kw, uint32_t wb0, int kb0, int kb1, const uint4* bfr,
                                           int lane, float (&shi)[2][4], float (&slo)[2][4], int nrem16) {
   if (kb0 >= kb1) return;
   const int g = lane >> 2, q = lane & 3;
   // this lane's byte offset from a block's first word: its word index times 128, its tokens 16 g
-  const uint32_t c0 = 128u * (W == 16 ? q : W == 8 ? q : W == 4 ? (q >> 1) : 0) + 16u * g;
   // (a partial 8- or 4-bit block's lanes past its last word read the next words of the tile: codes
   // of other slots or V bytes, always in the staged item, met by B = 0)
+  const uint32_t c0 = 128u * (W == 16 ? q : W == 8 ? q : W == 4 ? (q >> 1) : 0) + 16u * g;
   const uint32_t c1 = 128u * (q + 4) + 16u * g;  // W = 16: the word of slots 2q + 8, 2q + 9
   const uint32_t m2 = 0x00030003u << (2 * q);
   const int sh4 = 8 * (q & 1);
   uint32_t wb = wb0;
   const uint4* bp = bfr + kb0 * 32 + lane;
-#pragma unroll 1
+#pragma unroll 2
   for (int kb = kb0; kb < kb1; ++kb, wb += 64u * W, bp += 32) {
     const uint4 bq = *bp;
     const uint4 y0 = lds128(kw, wb + c0);
@@ -409,9 +412,7 @@ __device__ __forceinline__ void tile_logits(const unsigned char* kw, const int (
 // the accumulators of channel block cm: 2^-24 for the subnormal codes times 2^pos of the code's
 // bit position inside its half-word (below 8 after the optional shift by 8).
 __device__ __forceinline__ int v_scale_exp(int vb, int cm) {
-  if (vb == 16) return 0;
-  const int per = 16 / vb;
-  return -24 + ((vb * (cm % per)) & 7);
+  return vb == 16 ? 0 : vb == 2 ? -24 + 2 * (cm & 3) : vb == 4 ? -24 + 4 * (cm & 1) : -24;
 }
 
 // Moves the O^T accumulators from the scale of V class `from` to that of class `to` (powers of
@@ -448,7 +449,7 @@ __device__ __forceinline__ uint32_t v_field(uint32_t x, int e) {
 // channel group g.
 template <int D, int VB>
 __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned char* vcodes, const unsigned char* vmeta,
-                                               int lane, const uint32_t (&pb)[2][2]) {
+                                               int lane, const uint32_t (*pb)[2]) {
   const int g = lane >> 2, q = lane & 3;
   constexpr int CM = D / 16, NG = D / 32, NW = D * VB / 128, PER = 16 / VB;
 #pragma unroll
@@ -513,6 +514,41 @@ __device__ __forceinline__ void pv_fp16(WarpAcc<D>& acc, uint32_t vrows, int lan
       mma16816(acc.o[cm], a0, a1, a2, a3, pb[tb][0], pb[tb][1]);
     }
   }
+}
+
+// One zone-A tile of class cls (class 3: its zone-B rows follow the tile's tb bytes): logits, the
+// tokens past the kept ones masked (the last tile of a class), the softmax update, the accumulators
+// moved to the class's scale, PV.
+template <int D, bool PK>
+__device__ __forceinline__ void consume_tile(WarpAcc<D>& acc, int& o_mode, const unsigned char* stp, uint32_t tb_bytes,
+                                             int cls, int n_real, int RW, const int (&seg_kb)[5],
+                                             const uint32_t (&seg_wb)[4], int nrem16, const uint4* bfr, int lane,
+                                             float c24, float bias0, float bias1) {
+  const int g = lane >> 2;
+  float s[2][4];
+  tile_logits<PK>(stp, seg_kb, seg_wb, nrem16, bfr, lane, c24, bias0, bias1, s);
+  if (n_real < kTile) {
+#pragma unroll
+    for (int tb = 0; tb < 2; ++tb) {
+      const bool va = 16 * tb + g < n_real, vb = 16 * tb + g + 8 < n_real;
+      s[tb][0] = va ? s[tb][0] : -INFINITY;
+      s[tb][1] = va ? s[tb][1] : -INFINITY;
+      s[tb][2] = vb ? s[tb][2] : -INFINITY;
+      s[tb][3] = vb ? s[tb][3] : -INFINITY;
+    }
+  }
+  uint32_t pb[2][2];
+  softmax_update<D, 2>(acc, s, pb);
+  const int vb_cls = 2 << cls;
+  if (vb_cls != o_mode) {
+    rescale_o<D>(acc, o_mode, vb_cls);
+    o_mode = vb_cls;
+  }
+  const unsigned char* vcodes = stp + 4 * kTile * RW;
+  if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + kTile * D * 2 / 8, lane, pb);
+  else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + kTile * D * 4 / 8, lane, pb);
+  else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + kTile * D * 8 / 8, lane, pb);
+  else pv_fp16<D, 2>(acc, smem_u32(stp) + tb_bytes, lane, pb);
 }
 
 // Estimated decode cost of a head: its zone-A tiles and its zone-C blocks.
@@ -617,6 +653,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   int* st_pos = reinterpret_cast<int*>(empty + kConsumers * kStages);              // [consumers][stages]
   int* st_item = st_pos + kConsumers * kStages;                                    // [consumers][stages]
   uint16_t* newrow = reinterpret_cast<uint16_t*>(st_item + kConsumers * kStages);  // [2][D] fused step: k, v
+  uint32_t* kmeta_s = reinterpret_cast<uint32_t*>(newrow + 2 * D);                 // [D + kSlotPad] {scale, zero}
+  float* q_s = reinterpret_cast<float*>(kmeta_s + D + kSlotPad);                   // [8][D] the group's queries
   unsigned char* ring = smem + decode_fixed_smem(D);
   float* red = reinterpret_cast<float*>(ring);                                     // [consumers][8][D + 2], after the loop
 
@@ -672,7 +710,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   }
   if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   if (tid < k_slots) slot_s[tid] = sr;
-  __syncthreads();  // next_k, the barriers, the k-block ranges and the slot table are set
+  // the head's K metadata (zone A: static, may be read before the wait for the previous kernel)
+  if (tid < hpp->meta_slots)
+    kmeta_s[tid] = __ldg(reinterpret_cast<const uint32_t*>(PP.zone_a + hpp->a_off) + tid);
+  __syncthreads();  // next_k, the barriers, the k-block ranges, the slot table and K metadata are set
 
   auto item_cls = [&](int it) {
     return it < (int)cstart.v[1] ? 0 : it < (int)cstart.v[2] ? 1 : it < (int)cstart.v[3] ? 2 : it < zc_start ? 3 : -1;
@@ -697,7 +738,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     int issued = 0, released = 0, pending = -1;
     uint32_t head_p = 0, used = 0, need[kStages] = {0u, 0u, 0u, 0u};
     bool drained = !has_ring, ended = !serve, items_final = false;
-    int n_items = zc_start, len_c = 0;
+    int n_items = zc_start, len_c = 0, n_block_items = 0;
     int cap = kPrologueItems;
     long long idle0 = clock64();
     bool timed_out = false;
@@ -711,7 +752,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         moved = true;
       }
       if (issued == released) head_p = used = 0;  // empty ring: start at its beginning
-      while (!drained && issued - released < min(cap, kStages)) {
+      // near the end of the block's items a consumer holds at most two (the one it works on and the
+      // next), so that the warps run out of work together
+      const int left = items_final ? n_block_items - *(volatile int*)&next_k : kStages * kConsumers;
+      const int depth = left < 2 * kConsumers ? 2 : kStages;
+      while (!drained && issued - released < min(cap, depth)) {
         int it = pending;
         if (it < 0) it = isplit + in_split * atomicAdd(&next_k, 1);
         if (it >= n_items) {
@@ -789,20 +834,26 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     asm volatile("griddepcontrol.wait;" ::: "memory");
     len_c = min(*PP.len_dev, PP.cap_c);
     n_items = zc_start + ceil_div(len_c + (fused ? 1 : 0), kCRows);
+    n_block_items = n_items > isplit ? ceil_div(n_items - isplit, in_split) : 0;
     items_final = true;
     cap = kStages;
     idle0 = clock64();
+    // a consumer takes microseconds per tile and holds up to kStages of them: the producer polls its
+    // empty barriers at a growing interval while nothing moves (reset by every move)
+    unsigned nap = 32;
     while (true) {
       const bool moved = serve && step();
       if (__all_sync(0xffffffffu, ended)) break;
       if (__any_sync(0xffffffffu, moved)) {
         idle0 = clock64();
+        nap = 32;
       } else {
         if (clock64() - idle0 > P.wait_cycles || *(volatile int*)&abort_s) {
           timed_out = true;
           break;
         }
-        __nanosleep(64);
+        __nanosleep(nap);
+        nap = min(nap * 2, 512u);
       }
     }
     if (timed_out) {
@@ -837,7 +888,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     // column g is query head g, or with PK head g & 3, hi for g < 4 and lo for g >= 4.  A quantised
     // slot's value is q * scale * 2^-pos (pos: the bit position its lane's mask leaves the code at).
     const int s_q0 = k_slots - hpp->meta_slots;   // first quantised slot
-    const uint32_t* kmeta = reinterpret_cast<const uint32_t*>(PP.zone_a + hpp->a_off);  // {scale, zero} per slot
+    // the group's query rows, widened to fp32 (one load per element, all in flight together)
+    for (int i = tid; i < G * D; i += kConsumers * 32) q_s[i] = load_as_float(P.q, (int64_t)qbase * D + i, P.dtype);
+    consumers_sync();
     for (int i = tid; i < nkb * 32; i += kConsumers * 32) {
       const int kb = i >> 5, ln = i & 31, qq = ln & 3, gg = ln >> 2;
       const int seg = (kb >= seg_kb_s[1]) + (kb >= seg_kb_s[2]) + (kb >= seg_kb_s[3]);
@@ -852,9 +905,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         const int ch = slot_s[slot];
         float v = 0.f;
         if (ch >= 0 && hd < G) {
-          v = load_as_float(P.q, (int64_t)(qbase + hd) * D + ch, P.dtype);
+          v = q_s[hd * D + ch];
           if (w < 16) {
-            const uint32_t m = __ldg(kmeta + (slot - s_q0));
+            const uint32_t m = kmeta_s[slot - s_q0];
             const int pos = w == 2 ? 2 * qq : (w == 4 && (e >> 1)) ? 4 : 0;
             v *= __half2float(__ushort_as_half((uint16_t)(m & 0xffffu))) * __int_as_float((127 - pos) << 23);
           }
@@ -871,7 +924,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int ch = 16 * kb + 2 * qq + (e & 1) + 8 * (e >> 1);
-        x[e] = gg < G ? load_as_float(P.q, (int64_t)(qbase + gg) * D + ch, P.dtype) : 0.f;
+        x[e] = gg < G ? q_s[gg * D + ch] : 0.f;
       }
       qfragc[i] = split_hi_lo(x[0], x[1], x[2], x[3]);
     }
@@ -880,11 +933,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       float acc0 = 0.f;
       for (int m = lane; m < hpp->meta_slots; m += 32) {
         const int ch = slot_s[s_q0 + m];
-        if (ch >= 0) {
-          const uint32_t mw = __ldg(kmeta + m);
-          acc0 = fmaf(load_as_float(P.q, (int64_t)(qbase + warp) * D + ch, P.dtype),
-                      __half2float(__ushort_as_half((uint16_t)(mw >> 16))), acc0);
-        }
+        if (ch >= 0) acc0 = fmaf(q_s[warp * D + ch], __half2float(__ushort_as_half((uint16_t)(kmeta_s[m] >> 16))), acc0);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc0 += __shfl_xor_sync(0xffffffffu, acc0, o);
@@ -929,31 +978,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       const unsigned char* stp = wring + st_pos[sidx];
       const int cls = (rec >> 24) - 1, ti = rec & 0xffffff;  // ti: tile of the class, or zone-C block
       if (cls >= 0) {
-        const int n_real = min(kTile, (int)cnv(cls) - kTile * ti);
-        float s[2][4];
-        tile_logits<PK>(stp, seg_kb, seg_wb, nrem16, bfr, lane, c24, bias0, bias1, s);
-        if (n_real < kTile) {  // the last tile of a class: tokens past the kept ones
-#pragma unroll
-          for (int tb = 0; tb < 2; ++tb) {
-            const bool va = 16 * tb + g < n_real, vb = 16 * tb + g + 8 < n_real;
-            s[tb][0] = va ? s[tb][0] : -INFINITY;
-            s[tb][1] = va ? s[tb][1] : -INFINITY;
-            s[tb][2] = vb ? s[tb][2] : -INFINITY;
-            s[tb][3] = vb ? s[tb][3] : -INFINITY;
-          }
-        }
-        uint32_t pb[2][2];
-        softmax_update<D, 2>(acc, s, pb);
-        const int vb_cls = 2 << cls;
-        if (vb_cls != o_mode) {
-          rescale_o<D>(acc, o_mode, vb_cls);
-          o_mode = vb_cls;
-        }
-        const unsigned char* vcodes = stp + 4 * kTile * RW;
-        if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + kTile * D * 2 / 8, lane, pb);
-        else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + kTile * D * 4 / 8, lane, pb);
-        else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + kTile * D * 8 / 8, lane, pb);
-        else pv_fp16<D, 2>(acc, smem_u32(stp) + (uint32_t)ctb.v[3], lane, pb);
+        consume_tile<D, PK>(acc, o_mode, stp, (uint32_t)ctb(cls), cls, min(kTile, (int)cnv(cls) - kTile * ti), RW,
+                            seg_kb, seg_wb, nrem16, bfr, lane, c24, bias0, bias1);
       } else {
         if (o_mode != 16) {
           rescale_o<D>(acc, o_mode, 16);
@@ -1184,13 +1210,10 @@ static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n) {
   g.ring_warps = ring_warps;
   g.smem = (size_t)(fixed + (int64_t)ring_warps * ring);
   // blocks dealt to heads in proportion to their work: a nominal count that fills every SM once,
-  // fewer when there is little work (at least kConsumers items per block on average).
-  // With few heads, leave one SM per head free: the last block of each head merges after the
-  // others have left, and on those SMs the next call's blocks would otherwise start only after
-  // the merge, with their whole set-up still ahead of them.
-  const int free_sms = n_heads <= sms / 16 ? n_heads : 0;
-  g.ctas = (int)std::max<int64_t>(
-      1, std::min<int64_t>((int64_t)blocks_per_sm * (sms - free_sms), ceil_div64(items, kConsumers)));
+  // fewer when there is little work (at least kConsumers items per block on average).  Every SM
+  // takes work: leaving one per head free for the merges measured slower (the next call's blocks
+  // wait for this call to finish before they read the query anyway).
+  g.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)blocks_per_sm * sms, ceil_div64(items, kConsumers)));
   g.splits = g.ctas + n_heads * n;  // grid size: room for at least one block per (cache, head)
   g.partial_bytes = (size_t)align_up((int64_t)g.splits * partial_stride(G, D) * 4, 256);
   g.ticket_off = g.partial_bytes;

@@ -43,7 +43,7 @@ namespace rdkv {
 constexpr int kConsumers = 15;             // consumer warps of a block (one block per SM; with the producer, four warps per scheduler)
 constexpr int kDecWarps = kConsumers + 1;  // and the producer warp
 constexpr int kStages = 4;                 // stages in flight per consumer warp
-constexpr int kPrologueItems = 2;          // stages per consumer issued before the wait for the previous kernel
+constexpr int kPrologueItems = 4;          // stages per consumer issued before the wait for the previous kernel (all of them)
 constexpr int kMaxDealtBlocks = 256;       // grids up to this size may be dealt to heads on the host
 constexpr uint8_t kNoHead = 0xff;
 constexpr int kMaxParts = 8;               // caches one launch may attend
@@ -1079,24 +1079,27 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   const int pstride = partial_stride(G, D);
   float* part = P.partial + (int64_t)first_block * pstride;
   float* mine = part + (int64_t)split * pstride;
-  // each element: the block's running max M of its head over the warps, then the warps' results
-  // weighted by 2^(m_w - M) (the m (c = D) entry holds M)
-  for (int i = tid; i < G * (D + 2); i += blockDim.x) {
-    const int h = i / (D + 2), c = i % (D + 2);
-    float mw[kConsumers];
+  // per head: the block's running max M over the warps and each warp's weight 2^(m_w - M) (0 for
+  // a warp that saw no token), computed once; then each element sums the warps' results with those
+  // weights (the m (c = D) entry holds M)
+  __shared__ float wgt_s[8][kConsumers + 1];
+  if (tid < G * kConsumers) {
+    const int h = tid / kConsumers, w = tid % kConsumers;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumers; ++w) {
-      mw[w] = red[((int64_t)w * 8 + h) * (D + 2) + D];
-      M = fmaxf(M, mw[w]);
-    }
-    float val = M;
+    for (int u = 0; u < kConsumers; ++u) M = fmaxf(M, red[((int64_t)u * 8 + h) * (D + 2) + D]);
+    const float mw = red[((int64_t)w * 8 + h) * (D + 2) + D];
+    wgt_s[h][w] = M == -INFINITY ? 0.f : ex2(mw - M);
+    if (w == 0) wgt_s[h][kConsumers] = M;
+  }
+  __syncthreads();
+  for (int i = tid; i < G * (D + 2); i += blockDim.x) {
+    const int h = i / (D + 2), c = i % (D + 2);
+    float val = wgt_s[h][kConsumers];
     if (c != D) {
       val = 0.f;
-      if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kConsumers; ++w) val = fmaf(ex2(mw[w] - M), red[((int64_t)w * 8 + h) * (D + 2) + c], val);
-      }
+      for (int w = 0; w < kConsumers; ++w) val = fmaf(wgt_s[h][w], red[((int64_t)w * 8 + h) * (D + 2) + c], val);
     }
     mine[i] = val;
   }
@@ -1127,42 +1130,45 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       if (len_c < P.cap_c) *P.len_dev = len_c + 1;
     }
   }
-  // Merge: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per query head and channel.  One
-  // thread per output element loads what it needs straight from the splits' partials (L2; the
-  // acquire above made them visible), kMergeBatch splits at a time with every load of a batch in
-  // flight together, and folds each batch into its running (M, L, O).
+  // Merge: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per query head and channel.  Each
+  // thread takes two adjacent channels of one head and loads, for every split, that head's (m, l) and
+  // the two o values (8-byte loads from L2; the acquire above made them visible), all in flight
+  // together (kMergeBatch splits at a time), then folds each batch into its running (M, L, O).
   constexpr int kMergeBatch = 24;
-  for (int i = tid; i < G * D; i += blockDim.x) {
-    const int h = i / D, c = i % D;
+  for (int i = tid; i < G * D / 2; i += blockDim.x) {
+    const int h = (2 * i) / D, c = (2 * i) % D;
     const float* ph = part + h * (D + 2);
-    float M = -INFINITY, L = 0.f, O = 0.f;
+    float M = -INFINITY, L = 0.f, O0 = 0.f, O1 = 0.f;
     for (int s0 = 0; s0 < n_split; s0 += kMergeBatch) {
-      float mv[kMergeBatch], lv[kMergeBatch], ov[kMergeBatch];
+      float2 ml[kMergeBatch], ov[kMergeBatch];
 #pragma unroll
       for (int k = 0; k < kMergeBatch; ++k) {
         const bool in = s0 + k < n_split;
         const float* ps = ph + (int64_t)(s0 + k) * pstride;
-        mv[k] = in ? __ldcg(ps + D) : -INFINITY;
-        lv[k] = in ? __ldcg(ps + D + 1) : 0.f;
-        ov[k] = in ? __ldcg(ps + c) : 0.f;
+        ml[k] = in ? __ldcg(reinterpret_cast<const float2*>(ps + D)) : make_float2(-INFINITY, 0.f);
+        ov[k] = in ? __ldcg(reinterpret_cast<const float2*>(ps + c)) : make_float2(0.f, 0.f);
       }
       float Mn = M;
 #pragma unroll
-      for (int k = 0; k < kMergeBatch; ++k) Mn = fmaxf(Mn, mv[k]);
+      for (int k = 0; k < kMergeBatch; ++k) Mn = fmaxf(Mn, ml[k].x);
       if (Mn == -INFINITY) continue;  // no token seen so far
       const float so = M == -INFINITY ? 0.f : ex2(M - Mn);
-      float l1 = 0.f, o1 = 0.f;
+      float l1 = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
       for (int k = 0; k < kMergeBatch; ++k) {
-        const float w = ex2(mv[k] - Mn);  // 0 for a split without tokens (m = -inf)
-        l1 = fmaf(w, lv[k], l1);
-        o1 = fmaf(w, ov[k], o1);
+        const float w = ex2(ml[k].x - Mn);  // 0 for a split without tokens (m = -inf)
+        l1 = fmaf(w, ml[k].y, l1);
+        o0 = fmaf(w, ov[k].x, o0);
+        o1 = fmaf(w, ov[k].y, o1);
       }
       L = fmaf(L, so, l1);
-      O = fmaf(O, so, o1);
+      O0 = fmaf(O0, so, o0);
+      O1 = fmaf(O1, so, o1);
       M = Mn;
     }
-    P.out[((int64_t)b * P.h_q + j * G + h) * D + c] = L > 0.f ? O / L : 0.f;
+    float* op = P.out + ((int64_t)b * P.h_q + j * G + h) * D + c;  // (the caller's out needs 4-byte alignment only)
+    op[0] = L > 0.f ? O0 / L : 0.f;
+    op[1] = L > 0.f ? O1 / L : 0.f;
     // ln of the denominator: the running sums are of 2^(s log2(e) / sqrt(D) - M)
     if (P.lse != nullptr && c == 0)
       P.lse[(int64_t)b * P.h_q + j * G + h] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;

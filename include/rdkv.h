@@ -109,6 +109,10 @@ typedef struct rdkv_sizes {
 
 /* Rows of one zone-C page when zone C is paged (see rdkv_cache). */
 #define RDKV_ZONE_C_PAGE_ROWS 16
+/* Bytes of one zone-A page and rows of one zone-B page when zones A and B are
+ * paged (see rdkv_cache). */
+#define RDKV_ZONE_A_PAGE_BYTES 65536
+#define RDKV_ZONE_B_PAGE_ROWS 16
 
 /* A packed TriZone cache.  All pointers are caller-owned device memory.
  * zone_c_k / zone_c_v are fp16 [batch][h_kv][cap_c][D], or, when
@@ -124,7 +128,20 @@ typedef struct rdkv_sizes {
  * append + decode calls stays correct when replayed; len_c is the host mirror
  * the host-side capacity check uses.  rdkv_pack sets both to the window W;
  * rdkv_append advances both.  Replaying captured appends advances only
- * len_dev; a device-side append past cap_c writes nothing. */
+ * len_dev; a device-side append past cap_c writes nothing.
+ *
+ * Zones A and B may live in pages of pools shared by several caches (the same
+ * block table idea, applied to the zones the pack writes): when zone_a_pages is
+ * not NULL, byte o of the cache's zone A (the plan's offsets, a_off and up) is
+ * byte o % RDKV_ZONE_A_PAGE_BYTES of page zone_a_pages[o / RDKV_ZONE_A_PAGE_BYTES]
+ * of the pool at zone_a (pages of RDKV_ZONE_A_PAGE_BYTES bytes); when
+ * zone_b_pages is not NULL, zone-B row r is row r % 16 of page
+ * zone_b_pages[r / 16] of the pool at zone_b ([n_pages][16][D] fp16).  The
+ * tables (int32, device) name a distinct page for every page the cache's sizes
+ * need (ceil(zone_a_bytes / RDKV_ZONE_A_PAGE_BYTES), ceil(zone_b_rows / 16));
+ * rdkv_pack writes through them and the decode calls read through them.
+ * Caches of sequences with different prompt lengths can so share one pool and
+ * be attended in one launch (rdkv_decode_ragged). */
 typedef struct rdkv_cache {
   rdkv_shape shape;
   const void* plan;
@@ -139,6 +156,8 @@ typedef struct rdkv_cache {
   rdkv_sizes sizes;
   const int32_t* zone_c_pages;  /* NULL: contiguous zone C; else its page table */
   int32_t zone_c_page_stride;   /* table entries per head */
+  const int32_t* zone_a_pages;  /* NULL: contiguous zone A; else its page table */
+  const int32_t* zone_b_pages;  /* NULL: contiguous zone B; else its page table */
 } rdkv_cache;
 
 /* ---------------------------------------------------------------- misc */
@@ -407,6 +426,27 @@ size_t rdkv_decode_multi_workspace_bytes(const rdkv_cache* const* parts, int32_t
 rdkv_status rdkv_decode_attn_multi(const rdkv_cache* const* parts, int32_t n_parts, const void* q, float* out,
                                    float* lse, void* ws, size_t ws_bytes, void* stream);
 rdkv_status rdkv_decode_multi_status(const rdkv_cache* const* parts, int32_t n_parts, const void* ws, void* stream);
+
+/* ---------------------------------------------------------------- ragged batch
+ * RDKV section 2.3 for a batch of independent sequences with different prompt
+ * lengths (the batching of "Matematika KV Cache Compression", "Solusi 1"): each
+ * sequence is its own cache (batch 1, its own n_tokens, plan and zones, often
+ * in pages of shared pools), and ONE launch attends all of them:
+ *   out[s][h] = sum_t softmax_t(q[s][h] . k^_t / sqrt(D)) v^_t over the keys of
+ *   sequence s only (zones A and B and the *len_dev rows of its zone C).
+ * seqs[0 .. n_seq) (1 <= n_seq <= 8) must share h_q, h_kv, head_dim and dtype,
+ * have batch 1, carry their plan costs (rdkv_plan_sizes), and n_seq * h_kv
+ * must be at most RDKV_COST_HEADS, else RDKV_ERR_INVALID_ARG or
+ * RDKV_ERR_UNSUPPORTED.  q [n_seq][H_q][D] in the caches' dtype, out
+ * [n_seq][H_q][D] fp32, lse [n_seq][H_q] fp32 or NULL; the workspace sized by
+ * rdkv_decode_ragged_workspace_bytes for the same list (0 if it is invalid),
+ * with the zero-filled contract of rdkv_decode_attn.  rdkv_decode_ragged_status
+ * reads and clears the status word as rdkv_decode_status does.  (Append the new
+ * tokens with rdkv_append before the call.) */
+size_t rdkv_decode_ragged_workspace_bytes(const rdkv_cache* const* seqs, int32_t n_seq);
+rdkv_status rdkv_decode_ragged(const rdkv_cache* const* seqs, int32_t n_seq, const void* q, float* out, float* lse,
+                               void* ws, size_t ws_bytes, void* stream);
+rdkv_status rdkv_decode_ragged_status(const rdkv_cache* const* seqs, int32_t n_seq, const void* ws, void* stream);
 
 /* Takes rows [0, n_move) of every head's zone C out of the cache: copies them
  * to k_out, v_out [B][n_move][H_kv][D] in the cache's dtype (the fp16 values

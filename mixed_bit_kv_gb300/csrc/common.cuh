@@ -101,6 +101,22 @@ __host__ __device__ inline int64_t zone_c_offset(const int32_t* pages, int strid
                : ((int64_t)head * cap + row) * D;
 }
 
+// Byte offset in the zone-A pool of byte o of a cache's zone A: o itself (contiguous), or through the
+// cache's page table (pages of RDKV_ZONE_A_PAGE_BYTES).  A staged copy that crosses a page boundary
+// is split there (zone_a_run gives the bytes left in o's page).
+constexpr int64_t kZoneAPageBytes = RDKV_ZONE_A_PAGE_BYTES;
+__host__ __device__ inline int64_t zone_a_offset(const int32_t* pages, int64_t o) {
+  return pages ? (int64_t)pages[o / kZoneAPageBytes] * kZoneAPageBytes + o % kZoneAPageBytes : o;
+}
+__host__ __device__ inline int64_t zone_a_run(const int32_t* pages, int64_t o) {
+  return pages ? kZoneAPageBytes - o % kZoneAPageBytes : INT64_MAX;
+}
+// Element offset (of D fp16) of zone-B row r: r * D, or through the page table (16-row pages).
+constexpr int kZoneBPageRows = RDKV_ZONE_B_PAGE_ROWS;
+__host__ __device__ inline int64_t zone_b_offset(const int32_t* pages, int64_t r, int D) {
+  return (pages ? (int64_t)pages[r / kZoneBPageRows] * kZoneBPageRows + r % kZoneBPageRows : r) * D;
+}
+
 // ---------------------------------------------------------------- numerics
 __device__ __forceinline__ float load_as_float(const void* p, int64_t i, int dtype) {
   return dtype == RDKV_F16 ? __half2float(static_cast<const __half*>(p)[i]) : static_cast<const float*>(p)[i];

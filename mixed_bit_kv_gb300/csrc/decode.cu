@@ -82,6 +82,8 @@ struct DecodePart {
   const int32_t* zc_pages;  // zone-C page table, or NULL (contiguous)
   int zc_page_stride;
   int cap_c;
+  const int32_t* a_pages;   // zone-A page table, or NULL (contiguous)
+  const int32_t* b_pages;   // zone-B page table, or NULL (contiguous)
 };
 
 struct DecodeParams {
@@ -104,6 +106,8 @@ struct DecodeParams {
   const int16_t* slots;         // the plan's slot tables, slot_stride entries per head
   int dtype, h_q, h_kv, cap_c, ring_bytes, ring_warps, ctas, n_heads, slot_stride;
   int dealt;                    // 1: blocks dealt to heads on the host (below); 0: by the kernel
+  int ragged;                   // 1: part p is sequence p of a ragged batch (batch 1 each); the dealt head
+                                //    index h means sequence h / h_kv, head h % h_kv of that cache
   long long wait_cycles;        // limit of each wait on a stage's barrier (clock64 cycles)
   int arm_only;                 // timeout self-test: stages are armed for bytes that no copy delivers
   uint8_t block_head[kMaxDealtBlocks];       // head of each block, kNoHead for a block without work
@@ -581,7 +585,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   if (P.dealt) {
     // dealt on the host: this block's head and split range are kernel arguments
     const int hb = P.block_head[blockIdx.x];
-    if (hb != kNoHead && tid < P.slot_stride) slot_pre = PP.slots[(int64_t)hb * P.slot_stride + tid];
+    const int hbc = P.ragged ? hb % P.h_kv : hb;  // the head within its cache
+    if (hb != kNoHead && tid < P.slot_stride) slot_pre = PP.slots[(int64_t)hbc * P.slot_stride + tid];
     if (warp == 0) {
       if (lane == 0) {
         asg[0] = hb == kNoHead ? -1 : hb;
@@ -589,7 +594,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         asg[2] = hb == kNoHead ? 0 : P.head_first[hb + 1] - P.head_first[hb];
       }
       if (hb != kNoHead)  // the head record into shared memory, one word per lane
-        reinterpret_cast<int32_t*>(&hp_s)[lane] = reinterpret_cast<const int32_t*>(PP.heads + hb)[lane];
+        reinterpret_cast<int32_t*>(&hp_s)[lane] = reinterpret_cast<const int32_t*>(PP.heads + hbc)[lane];
     }
   } else if (warp == 0) {
     // Blocks are dealt to heads in proportion to their estimated cost, at least one per head, over a
@@ -634,11 +639,12 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   // items of this block's cache: isplit, isplit + in_split, ...
   const int isplit = P.dealt ? (int)P.block_split[blockIdx.x] : split;
   const int in_split = P.dealt ? (int)P.block_nsplit[blockIdx.x] : n_split;
-  const int b = head / P.h_kv, j = head % P.h_kv;
+  const int b = head / P.h_kv, j = head % P.h_kv;     // sequence (the part, when ragged) and KV head
+  const int hc = P.ragged ? j : head;                 // the head within its cache: record, slots, zone C
   const rdkv_head_plan* hpp = &hp_s;
   const bool fused = P.k_new != nullptr;
   const int qbase = b * P.h_q + j * G;
-  const int16_t* slot_ch = PP.slots + (int64_t)head * P.slot_stride;
+  const int16_t* slot_ch = PP.slots + (int64_t)hc * P.slot_stride;
   const int k_slots = hpp->k_slots;  // <= D + kSlotPad <= the block's threads
   const int16_t sr = tid < k_slots ? (P.dealt ? slot_pre : slot_ch[tid]) : (int16_t)-1;
 
@@ -712,7 +718,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   if (tid < k_slots) slot_s[tid] = sr;
   // the head's K metadata (zone A: static, may be read before the wait for the previous kernel)
   if (tid < hpp->meta_slots)
-    kmeta_s[tid] = __ldg(reinterpret_cast<const uint32_t*>(PP.zone_a + hpp->a_off) + tid);
+    kmeta_s[tid] = __ldg(reinterpret_cast<const uint32_t*>(PP.zone_a + zone_a_offset(PP.a_pages, hpp->a_off + 4 * tid)));
   __syncthreads();  // next_k, the barriers, the k-block ranges, the slot table and K metadata are set
 
   auto item_cls = [&](int it) {
@@ -800,14 +806,27 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
           const uint32_t zb = cls == 3 ? (uint32_t)kTile * D * 2 : 0u;
           mbar_arrive_expect_tx(bar, a_bytes + zb);
           const uint64_t pol = evict_first_policy();
-          bulk_copy_once(dst, PP.zone_a + coff(cls) + (int64_t)ti * a_bytes, a_bytes, bar, pol);
-          if (zb) bulk_copy_once(dst + a_bytes, PP.zone_b + (b_row + (int64_t)kTile * ti) * D, zb, bar, pol);
+          // zone A through its page table: a tile that crosses a page boundary comes in two copies
+          const int64_t la = coff(cls) + (int64_t)ti * a_bytes;
+          const uint32_t run = (uint32_t)min((int64_t)a_bytes, zone_a_run(PP.a_pages, la));
+          bulk_copy_once(dst, PP.zone_a + zone_a_offset(PP.a_pages, la), run, bar, pol);
+          if (run < a_bytes) bulk_copy_once(dst + run, PP.zone_a + zone_a_offset(PP.a_pages, la + run), a_bytes - run, bar, pol);
+          if (zb) {  // 32 zone-B rows: two pages of 16 rows when zone B is paged (b_row is a multiple of 32)
+            const int64_t r0 = b_row + (int64_t)kTile * ti;
+            if (PP.b_pages) {
+              bulk_copy_once(dst + a_bytes, PP.zone_b + zone_b_offset(PP.b_pages, r0, D), zb / 2, bar, pol);
+              bulk_copy_once(dst + a_bytes + zb / 2, PP.zone_b + zone_b_offset(PP.b_pages, r0 + kZoneBPageRows, D), zb / 2,
+                             bar, pol);
+            } else {
+              bulk_copy_once(dst + a_bytes, PP.zone_b + r0 * D, zb, bar, pol);
+            }
+          }
         } else {
           // rows of zone C (the fused step's new row, past them, is written by the consumer)
           const int rows = max(0, min(kCRows, len_c - c_row));
           const uint32_t bytes = (uint32_t)rows * D * 2;
           // a zone-C item is 16 rows: one page when zone C is paged
-          const int64_t src = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, head, c_row, D);
+          const int64_t src = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, hc, c_row, D);
           mbar_arrive_expect_tx(bar, 2 * bytes);
           if (bytes) {
             const uint64_t pol = evict_first_policy();
@@ -1117,7 +1136,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     // get here advances the length (every block of every head has read it by then)
     const int len_c = min(*PP.len_dev, PP.cap_c);
     if (len_c < P.cap_c) {
-      const int64_t dst = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, head, len_c, D);
+      const int64_t dst = zone_c_offset(PP.zc_pages, PP.zc_page_stride, PP.cap_c, hc, len_c, D);
       for (int i = tid; i < D; i += blockDim.x) {
         const_cast<uint16_t*>(PP.zone_c_k)[dst + i] = newrow[i];
         const_cast<uint16_t*>(PP.zone_c_v)[dst + i] = newrow[D + i];
@@ -1186,10 +1205,12 @@ struct DecodeGeom {
   size_t smem;
   size_t partial_bytes;
   size_t ticket_off;   // tickets then the status word
+  int n_heads;         // heads with their own ticket and merge: batch * h_kv, or n * h_kv for a ragged batch
 };
 
-// Geometry of a launch over the caches parts[0 .. n) (one, or segments and the live cache).
-static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n) {
+// Geometry of a launch over the caches parts[0 .. n): one, segments and the live cache of the same
+// sequences, or (ragged) the independent sequences of a ragged batch.
+static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n, bool ragged = false) {
   DecodeGeom g;
   const rdkv_shape& s = parts[0]->shape;
   const int D = s.head_dim, G = s.h_q / s.h_kv;
@@ -1223,12 +1244,13 @@ static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n) {
   g.splits = g.ctas + n_heads * n;  // grid size: room for at least one block per (cache, head)
   g.partial_bytes = (size_t)align_up((int64_t)g.splits * partial_stride(G, D) * 4, 256);
   g.ticket_off = g.partial_bytes;
+  g.n_heads = ragged ? n * s.h_kv : n_heads;
   return g;
 }
 static DecodeGeom decode_geom(const rdkv_cache* c) { return decode_geom(&c, 1); }
 
 // ws: partials, then per-head tickets, the status word and the fused step's head counter
-static size_t decode_ws_bytes(const DecodeGeom& g, int n_heads) { return g.ticket_off + (size_t)decode_ticket_bytes(n_heads); }
+static size_t decode_ws_bytes(const DecodeGeom& g) { return g.ticket_off + (size_t)decode_ticket_bytes(g.n_heads); }
 
 rdkv_status check_cache_public(const rdkv_cache* c);
 
@@ -1237,10 +1259,11 @@ rdkv_status check_cache_public(const rdkv_cache* c);
 // (rdkv_plan_sizes), else (one cache only) by the kernel.
 static DecodeParams decode_params(const rdkv_cache* const* parts, int n, const DecodeGeom& geo, const void* q,
                                   float* out, void* ws, const void* k_new = nullptr, const void* v_new = nullptr,
-                                  float* lse = nullptr) {
+                                  float* lse = nullptr, bool ragged = false) {
   const rdkv_cache* cache = parts[0];
   const rdkv_shape& s = cache->shape;
-  const int n_heads = s.batch * s.h_kv;
+  const int n_heads = geo.n_heads;                    // heads with their own ticket and merge
+  const int cache_heads = s.batch * s.h_kv;           // heads of one cache
   const PlanLayout L = plan_layout(s.batch, s.h_kv, s.head_dim);
   DecodeParams P;
   P.plan = cache->plan;
@@ -1271,6 +1294,7 @@ static DecodeParams decode_params(const rdkv_cache* const* parts, int n, const D
   P.ctas = geo.ctas;
   P.wait_cycles = kWaitCycles;
   P.arm_only = 0;
+  P.ragged = ragged ? 1 : 0;
   for (int p = 0; p < kMaxParts; ++p) {
     const rdkv_cache* c = parts[p < n ? p : 0];
     DecodePart& d = P.parts[p];
@@ -1284,28 +1308,35 @@ static DecodeParams decode_params(const rdkv_cache* const* parts, int n, const D
     d.zc_pages = c->zone_c_pages;
     d.zc_page_stride = c->zone_c_page_stride;
     d.cap_c = c->cap_c;
+    d.a_pages = c->zone_a_pages;
+    d.b_pages = c->zone_b_pages;
   }
   // Deal the blocks to the heads here when the plans' cost estimates reached the host: the kernel
   // then knows its head at once instead of reading every head record first.  The rule is the
-  // kernel's own (at least one block per head and cache, the rest in proportion to the cost).
+  // kernel's own (at least one block per head and cache, the rest in proportion to the cost).  A
+  // ragged batch: head h is head h % h_kv of cache h / h_kv alone.
   P.dealt = 0;
   bool known = n_heads <= RDKV_COST_HEADS && geo.splits <= kMaxDealtBlocks;
   for (int p = 0; known && p < n; ++p) {
-    known = parts[p]->sizes.n_heads == n_heads;
-    for (int h = 0; known && h < n_heads; ++h) known = parts[p]->sizes.head_cost[h] > 0;
+    known = parts[p]->sizes.n_heads == cache_heads;
+    for (int h = 0; known && h < cache_heads; ++h) known = parts[p]->sizes.head_cost[h] > 0;
   }
   if (known) {
     auto cost = [&](int p, int h) {
       return parts[p]->sizes.head_cost[h] + (int64_t)ceil_div(parts[p]->cap_c, kCRows) * kZoneCBlockCost;
     };
+    auto part_of = [&](int h, int p) { return ragged ? h / s.h_kv : p; };       // the cache of (head, part p)
+    auto head_in = [&](int h) { return ragged ? h % s.h_kv : h; };             // the head within that cache
+    const int parts_per_head = ragged ? 1 : n;
     int64_t total = 0;
-    for (int p = 0; p < n; ++p)
-      for (int h = 0; h < n_heads; ++h) total += cost(p, h);
+    for (int h = 0; h < n_heads; ++h)
+      for (int p = 0; p < parts_per_head; ++p) total += cost(part_of(h, p), head_in(h));
     int start = 0;
     for (int h = 0; h < n_heads; ++h) {
       P.head_first[h] = (int16_t)start;
-      for (int p = 0; p < n; ++p) {
-        const int c = std::max(1, (int)(cost(p, h) * geo.ctas / total));
+      for (int pi = 0; pi < parts_per_head; ++pi) {
+        const int p = part_of(h, pi);
+        const int c = std::max(1, (int)(cost(p, head_in(h)) * geo.ctas / total));
         for (int k = 0; k < c; ++k) {
           P.block_head[start + k] = (uint8_t)h;
           P.block_part[start + k] = (uint8_t)p;
@@ -1374,7 +1405,7 @@ using namespace rdkv;
 
 extern "C" size_t rdkv_decode_workspace_bytes(const rdkv_cache* cache) {
   if (check_cache_public(cache) != RDKV_OK) return 0;
-  return decode_ws_bytes(decode_geom(cache), cache->shape.batch * cache->shape.h_kv);
+  return decode_ws_bytes(decode_geom(cache));
 }
 
 // selftest_wait > 0: the timeout self-test (stages armed for bytes that no copy delivers, each wait
@@ -1385,9 +1416,8 @@ static rdkv_status decode_attn_impl(const rdkv_cache* cache, const void* q, floa
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(q && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
   const rdkv_shape& s = cache->shape;
-  const int n_heads = s.batch * s.h_kv;
   const DecodeGeom geo = decode_geom(cache);
-  const size_t need = decode_ws_bytes(geo, n_heads);
+  const size_t need = decode_ws_bytes(geo);
   RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
@@ -1407,9 +1437,8 @@ static rdkv_status decode_step_impl(rdkv_cache* cache, const void* q, const void
   RDKV_REQUIRE(q && out && k_new && v_new, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
   RDKV_REQUIRE(cache->len_c < cache->cap_c, RDKV_ERR_CAPACITY, "zone C is full (%d rows)", cache->cap_c);
   const rdkv_shape& s = cache->shape;
-  const int n_heads = s.batch * s.h_kv;
   const DecodeGeom geo = decode_geom(cache);
-  const size_t need = decode_ws_bytes(geo, n_heads);
+  const size_t need = decode_ws_bytes(geo);
   RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
@@ -1468,8 +1497,7 @@ extern "C" rdkv_status rdkv_decode_status(const rdkv_cache* cache, const void* w
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(ws, RDKV_ERR_INVALID_ARG, "NULL workspace");
   const DecodeGeom geo = decode_geom(cache);
-  const int n_heads = cache->shape.batch * cache->shape.h_kv;
-  return decode_status_at(ws, geo.ticket_off + 4 * (size_t)n_heads, stream);
+  return decode_status_at(ws, geo.ticket_off + 4 * (size_t)geo.n_heads, stream);
 }
 
 // ---------------------------------------------------------------- one launch over several caches
@@ -1489,7 +1517,7 @@ static rdkv_status check_parts(const rdkv_cache* const* parts, int32_t n_parts) 
 
 extern "C" size_t rdkv_decode_multi_workspace_bytes(const rdkv_cache* const* parts, int32_t n_parts) {
   if (check_parts(parts, n_parts) != RDKV_OK) return 0;
-  return decode_ws_bytes(decode_geom(parts, n_parts), parts[0]->shape.batch * parts[0]->shape.h_kv);
+  return decode_ws_bytes(decode_geom(parts, n_parts));
 }
 
 extern "C" rdkv_status rdkv_decode_attn_multi(const rdkv_cache* const* parts, int32_t n_parts, const void* q,
@@ -1498,9 +1526,8 @@ extern "C" rdkv_status rdkv_decode_attn_multi(const rdkv_cache* const* parts, in
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(q && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
   const rdkv_shape& s = parts[0]->shape;
-  const int n_heads = s.batch * s.h_kv;
   const DecodeGeom geo = decode_geom(parts, n_parts);
-  const size_t need = decode_ws_bytes(geo, n_heads);
+  const size_t need = decode_ws_bytes(geo);
   RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
   RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
                (long long)geo.max_item);
@@ -1517,7 +1544,55 @@ extern "C" rdkv_status rdkv_decode_multi_status(const rdkv_cache* const* parts, 
   if (st != RDKV_OK) return st;
   RDKV_REQUIRE(ws, RDKV_ERR_INVALID_ARG, "NULL workspace");
   const DecodeGeom geo = decode_geom(parts, n_parts);
-  return decode_status_at(ws, geo.ticket_off + 4 * (size_t)(parts[0]->shape.batch * parts[0]->shape.h_kv), stream);
+  return decode_status_at(ws, geo.ticket_off + 4 * (size_t)geo.n_heads, stream);
+}
+
+// ---------------------------------------------------------------- one launch over a ragged batch
+static rdkv_status check_ragged(const rdkv_cache* const* seqs, int32_t n_seq) {
+  RDKV_REQUIRE(seqs && n_seq >= 1 && n_seq <= kMaxParts, RDKV_ERR_INVALID_ARG, "n_seq %d outside [1, %d]", n_seq,
+               kMaxParts);
+  for (int p = 0; p < n_seq; ++p) {
+    rdkv_status st = check_cache_public(seqs[p]);
+    if (st != RDKV_OK) return st;
+    const rdkv_shape &a = seqs[0]->shape, &b = seqs[p]->shape;
+    RDKV_REQUIRE(b.batch == 1, RDKV_ERR_INVALID_ARG, "sequence %d: a ragged batch takes caches of batch 1", p);
+    RDKV_REQUIRE(a.h_q == b.h_q && a.h_kv == b.h_kv && a.head_dim == b.head_dim && a.dtype == b.dtype,
+                 RDKV_ERR_INVALID_ARG, "sequence %d does not share the heads, D and dtype of sequence 0", p);
+  }
+  RDKV_REQUIRE((int64_t)n_seq * seqs[0]->shape.h_kv <= RDKV_COST_HEADS, RDKV_ERR_UNSUPPORTED,
+               "a ragged batch holds at most %d (sequence, KV head) pairs", RDKV_COST_HEADS);
+  return RDKV_OK;
+}
+
+extern "C" size_t rdkv_decode_ragged_workspace_bytes(const rdkv_cache* const* seqs, int32_t n_seq) {
+  if (check_ragged(seqs, n_seq) != RDKV_OK) return 0;
+  return decode_ws_bytes(decode_geom(seqs, n_seq, true));
+}
+
+extern "C" rdkv_status rdkv_decode_ragged(const rdkv_cache* const* seqs, int32_t n_seq, const void* q, float* out,
+                                          float* lse, void* ws, size_t ws_bytes, void* stream) {
+  rdkv_status st = check_ragged(seqs, n_seq);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(q && out, RDKV_ERR_INVALID_ARG, "NULL pointer argument");
+  const DecodeGeom geo = decode_geom(seqs, n_seq, true);
+  const size_t need = decode_ws_bytes(geo);
+  RDKV_REQUIRE(ws && ws_bytes >= need, RDKV_ERR_WORKSPACE, "decode workspace too small (%zu < %zu)", ws_bytes, need);
+  RDKV_REQUIRE(geo.ring_bytes >= geo.max_item, RDKV_ERR_UNSUPPORTED, "tiles too large for the decode ring (%lld B)",
+               (long long)geo.max_item);
+  const DecodeParams P = decode_params(seqs, n_seq, geo, q, out, ws, nullptr, nullptr, lse, true);
+  RDKV_REQUIRE(P.dealt, RDKV_ERR_UNSUPPORTED,
+               "a ragged batch needs every cache's plan costs on the host (rdkv_plan_sizes) and at most %d blocks",
+               kMaxDealtBlocks);
+  return launch_decode(P, geo, seqs[0]->shape, (cudaStream_t)stream, true);
+}
+
+extern "C" rdkv_status rdkv_decode_ragged_status(const rdkv_cache* const* seqs, int32_t n_seq, const void* ws,
+                                                 void* stream) {
+  rdkv_status st = check_ragged(seqs, n_seq);
+  if (st != RDKV_OK) return st;
+  RDKV_REQUIRE(ws, RDKV_ERR_INVALID_ARG, "NULL workspace");
+  const DecodeGeom geo = decode_geom(seqs, n_seq, true);
+  return decode_status_at(ws, geo.ticket_off + 4 * (size_t)geo.n_heads, stream);
 }
 
 // ---------------------------------------------------------------- decode without a caller workspace
@@ -1555,7 +1630,7 @@ extern "C" rdkv_status rdkv_decode_attn_noalloc(const rdkv_cache* cache, const v
   const rdkv_shape& s = cache->shape;
   const int n_heads = s.batch * s.h_kv;
   const DecodeGeom geo = decode_geom(cache);
-  const size_t need = decode_ws_bytes(geo, n_heads);
+  const size_t need = decode_ws_bytes(geo);
   RDKV_REQUIRE(need <= kNoAllocScratchBytes, RDKV_ERR_WORKSPACE,
                "this cache needs %zu bytes of decode scratch; the built-in scratch holds %zu "
                "(use rdkv_decode_attn with a workspace)",

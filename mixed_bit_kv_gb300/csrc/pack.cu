@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(1024) index_kernel(const uint8_t* __restrict__
 // minimum and maximum over the head's kept tokens (the allocation's channel statistics in the plan),
 // in slot order from the first 8-bit slot; pads and the tail up to 16 bytes are zero.
 __global__ void head_meta_kernel(const void* __restrict__ plan, const float2* __restrict__ kstat, int D,
-                                 uint8_t* __restrict__ zone_a) {
+                                 uint8_t* __restrict__ zone_a, const int32_t* __restrict__ a_pages) {
   const int head = blockIdx.x;
   const rdkv_plan_header* hdr = plan_header(plan);
   const rdkv_head_plan& hp = plan_heads(plan)[head];
@@ -150,7 +150,6 @@ __global__ void head_meta_kernel(const void* __restrict__ plan, const float2* __
   const int QS = hp.meta_slots, s_q0 = hp.k_slots - QS;
   const int sb4 = s_q0 + kKB * ceil_div(4 * hp.k_words[1], kKB);   // first 4-bit slot
   const int sb2 = sb4 + kKB * ceil_div(8 * hp.k_words[2], kKB);    // first 2-bit slot
-  uint32_t* out = reinterpret_cast<uint32_t*>(zone_a + hp.a_off);
   const int n_words = (int)(head_meta_bytes(QS) / 4);
   for (int m = threadIdx.x; m < n_words; m += blockDim.x) {
     uint32_t v = 0;
@@ -162,7 +161,7 @@ __global__ void head_meta_kernel(const void* __restrict__ plan, const float2* __
       const QParams p = qparams(st.x, st.y, b);
       v = (uint32_t)p.scale_h | ((uint32_t)p.zero_h << 16);
     }
-    out[m] = v;
+    *reinterpret_cast<uint32_t*>(zone_a + zone_a_offset(a_pages, hp.a_off + 4 * (int64_t)m)) = v;
   }
 }
 
@@ -197,7 +196,9 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
                                                                   const float2* __restrict__ kstat,
                                                                   const int32_t* __restrict__ index_map,
                                                                   uint8_t* __restrict__ zone_a,
-                                                                  uint16_t* __restrict__ zone_b, int N, int h_kv) {
+                                                                  uint16_t* __restrict__ zone_b, int N, int h_kv,
+                                                                  const int32_t* __restrict__ a_pages,
+                                                                  const int32_t* __restrict__ b_pages) {
   constexpr int NG = D / kVGroup;  // V groups of a token
   constexpr int KP = D + 1;        // floats of a staged K row
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -270,9 +271,11 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   }
   __syncthreads();
 
-  uint8_t* tile = zone_a + tile_off;
-  uint8_t* vcode = tile + 4 * kTile * RW;
-  uint16_t* vmeta = reinterpret_cast<uint16_t*>(vcode + kTile * D * vbits / 8);
+  // the tile's bytes in the zone-A pool (through the page table when zone A is paged; a tile may
+  // cross a page boundary, so every store translates its own offset)
+  auto at = [&](int64_t byte) { return zone_a + zone_a_offset(a_pages, tile_off + byte); };
+  const int64_t vcode_b = 4 * kTile * RW;                      // V codes, then V metadata
+  const int64_t vmeta_b = vcode_b + kTile * D * vbits / 8;
   // quantiser parameters: K slot s (quantised slots only: the head's channel statistics), then V
   // group (r, g) of the tile
   for (int i = tid; i < KS + (vbits < 16 ? kTile * NG : 0); i += kPackThreads) {
@@ -319,14 +322,14 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
       // token pair p = 8 tb + q + 4 h: scales ordered (tb, q, h, group), zeros (tb, group, q, h), each
       // 32-bit word the pair's even token (low half) and odd token (high half)
       const int pp = r >> 1, tb = pp >> 3, q = pp & 3, h = (pp >> 2) & 1;
-      vmeta[2 * (((tb * 4 + q) * 2 + h) * NG + g) + (r & 1)] = sc_h;
-      vmeta[2 * (16 * NG + ((tb * NG + g) * 4 + q) * 2 + h) + (r & 1)] = ze_h;
+      *reinterpret_cast<uint16_t*>(at(vmeta_b + 2 * (2 * (((tb * 4 + q) * 2 + h) * NG + g) + (r & 1)))) = sc_h;
+      *reinterpret_cast<uint16_t*>(at(vmeta_b + 2 * (2 * (16 * NG + ((tb * NG + g) * 4 + q) * 2 + h) + (r & 1)))) = ze_h;
     }
   }
   if (vbits == 16) {
     for (int i = tid; i < kTile * D; i += kPackThreads) {
       const int r = i / D;
-      zone_b[brow * D + i] = r < n_real ? half_bits(Vf[i]) : (uint16_t)0;
+      zone_b[zone_b_offset(b_pages, brow + r, D) + i % D] = r < n_real ? half_bits(Vf[i]) : (uint16_t)0;
     }
   }
   __syncthreads();
@@ -337,7 +340,6 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
     const int r = tx;
     const bool real = r < n_real;
     const float* kr = Kf + r * KP;
-    uint32_t* kw = reinterpret_cast<uint32_t*>(tile);
     for (int w = ty; w < RW; w += kPackThreads / 32) {
       // segment width, first slot of the word's k-block and the word's index inside that block
       int kb, sbase, wg;
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
         const uint32_t code = kb == 16 ? (uint32_t)half_bits(x) : qcode_rcp(x, kq[3 * s], kq[3 * s + 1], kq[3 * s + 2], hmax);
         word |= code << bit_off(e, kb);
       }
-      kw[32 * w + 4 * (r % 8) + r / 8] = word;
+      *reinterpret_cast<uint32_t*>(at(4 * (32 * w + 4 * (r % 8) + r / 8))) = word;
     }
   }
   // V codes: lanes along channels, warps along tokens
@@ -377,7 +379,6 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   // (per = 16 / b) of the lane's channel list, channel 16 (k mod D/16) + 8 (k div D/16) + g, at bit
   // b e for token 2p (low half) and 16 + b e for token 2p + 1, p = 8 tb + q + 4 h
   if (vbits < 16) {
-    uint32_t* vw = reinterpret_cast<uint32_t*>(vcode);
     constexpr int CM = D / 16;
     const int nw = D * vbits / 128, per = 16 / vbits;
     for (int i = tid; i < D * vbits; i += kPackThreads) {
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
         word |= (uint32_t)vc[(2 * p) * D + c] << (vbits * e);
         word |= (uint32_t)vc[(2 * p + 1) * D + c] << (16 + vbits * e);
       }
-      vw[i] = word;
+      *reinterpret_cast<uint32_t*>(at(vcode_b + 4 * (int64_t)i)) = word;
     }
   }
 }
@@ -442,7 +443,7 @@ static rdkv_status launch_pack_tiles(const void* k, const void* v, const rdkv_ca
   const float2* kstat = reinterpret_cast<const float2*>(static_cast<const char*>(cache->plan) + L.kstat_off);
   pack_tile_kernel<T, D><<<(unsigned)n_tiles, kPackThreads, smem, cs>>>(
       static_cast<const T*>(k), static_cast<const T*>(v), cache->plan, kstat, cache->index_map, cache->zone_a,
-      cache->zone_b, cache->shape.n_tokens, cache->shape.h_kv);
+      cache->zone_b, cache->shape.n_tokens, cache->shape.h_kv, cache->zone_a_pages, cache->zone_b_pages);
   RDKV_CHECK_LAUNCH("tile pack");
   return RDKV_OK;
 }
@@ -488,7 +489,7 @@ extern "C" rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v
     const PlanLayout L = plan_layout(s.batch, s.h_kv, D);
     head_meta_kernel<<<n_heads, 128, 0, cs>>>(
         cache->plan, reinterpret_cast<const float2*>(static_cast<const char*>(cache->plan) + L.kstat_off), D,
-        cache->zone_a);
+        cache->zone_a, cache->zone_a_pages);
     RDKV_CHECK_LAUNCH("head K metadata");
   }
   if (Np > 0 && cache->sizes.index_slots > 0) {

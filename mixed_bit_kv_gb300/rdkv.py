@@ -30,6 +30,7 @@ EXPORTED = (
     "rdkv_decode_attn_lse", "rdkv_decode_step_lse", "rdkv_merge_attn", "rdkv_zone_c_take", "rdkv_recompress_score",
     "rdkv_allocate_at_levels", "rdkv_decode_multi_workspace_bytes", "rdkv_decode_attn_multi",
     "rdkv_decode_multi_status", "rdkv_zone_bounds", "rdkv_decode_timeout_selftest", "rdkv_workspace_bytes",
+    "rdkv_decode_ragged_workspace_bytes", "rdkv_decode_ragged", "rdkv_decode_ragged_status",
 )
 RDKV_CALL_SCORE, RDKV_CALL_ALLOCATE, RDKV_CALL_DECODE = 0, 1, 2
 
@@ -58,9 +59,12 @@ class CacheStruct(ctypes.Structure):
                 ("zone_b", ctypes.c_void_p), ("zone_c_k", ctypes.c_void_p), ("zone_c_v", ctypes.c_void_p),
                 ("index_map", ctypes.c_void_p), ("len_dev", ctypes.c_void_p), ("cap_c", ctypes.c_int32),
                 ("len_c", ctypes.c_int32),
-                ("sizes", Sizes), ("zone_c_pages", ctypes.c_void_p), ("zone_c_page_stride", ctypes.c_int32)]
+                ("sizes", Sizes), ("zone_c_pages", ctypes.c_void_p), ("zone_c_page_stride", ctypes.c_int32),
+                ("zone_a_pages", ctypes.c_void_p), ("zone_b_pages", ctypes.c_void_p)]
 
 PAGE_ROWS = 16  # RDKV_ZONE_C_PAGE_ROWS
+A_PAGE_BYTES = 65536  # RDKV_ZONE_A_PAGE_BYTES
+B_PAGE_ROWS = 16  # RDKV_ZONE_B_PAGE_ROWS
 
 
 HEAD_PLAN_DTYPE = [("n_v", "<i4", 4), ("tiles", "<i4", 4), ("n_k", "<i4", 5), ("k_words", "<i4", 4),
@@ -121,6 +125,9 @@ def lib():
             "rdkv_decode_multi_status": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P]),
             "rdkv_allocate_at_levels": (ctypes.c_int, [sp, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                        ctypes.c_size_t, _P]),
+            "rdkv_decode_ragged_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32]),
+            "rdkv_decode_ragged": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+            "rdkv_decode_ragged_status": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -240,13 +247,19 @@ def rdkv_plan_sizes(plan, stream=None):
 class Cache:
     """Device buffers of one packed TriZone cache plus the C struct that points at them."""
 
-    def __init__(self, shape, plan, sizes, cap_c, device, pages=None):
+    def __init__(self, shape, plan, sizes, cap_c, device, pages=None, ab_pool=None):
         """pages: None for a contiguous zone C, else (pool_k, pool_v, table): fp16 pools
-        [n_pages, PAGE_ROWS, D] and an int32 page table [B * H_kv, stride] (see ``page_pool``)."""
+        [n_pages, PAGE_ROWS, D] and an int32 page table [B * H_kv, stride] (see ``page_pool``).
+        ab_pool: None for contiguous zones A and B, else a ``ZonePool`` whose pages hold them."""
         D = shape.head_dim
         self.shape, self.plan, self.sizes = shape, plan, sizes
-        self.zone_a = torch.zeros(max(sizes.zone_a_bytes, 16), dtype=torch.uint8, device=device)
-        self.zone_b = torch.zeros(max(sizes.zone_b_rows, 1), D, dtype=torch.float16, device=device)
+        self.ab_pool, self.a_table, self.b_table = ab_pool, None, None
+        if ab_pool is None:
+            self.zone_a = torch.zeros(max(sizes.zone_a_bytes, 16), dtype=torch.uint8, device=device)
+            self.zone_b = torch.zeros(max(sizes.zone_b_rows, 1), D, dtype=torch.float16, device=device)
+        else:
+            self.zone_a, self.zone_b = ab_pool.zone_a, ab_pool.zone_b
+            self.a_table, self.b_table = ab_pool.take(sizes)
         if pages is None:
             self.zone_c_k = torch.zeros(shape.batch, shape.h_kv, max(cap_c, 1), D, dtype=torch.float16, device=device)
             self.zone_c_v = torch.zeros_like(self.zone_c_k)
@@ -258,8 +271,33 @@ class Cache:
         self.len_dev = torch.zeros(1, dtype=torch.int32, device=device)
         self.c = CacheStruct(shape, plan.data_ptr(), self.zone_a.data_ptr(), self.zone_b.data_ptr(),
                              self.zone_c_k.data_ptr(), self.zone_c_v.data_ptr(), self.index_map.data_ptr(),
-                             self.len_dev.data_ptr(), cap_c, 0, sizes, table_ptr, stride)
+                             self.len_dev.data_ptr(), cap_c, 0, sizes, table_ptr, stride,
+                             None if self.a_table is None else self.a_table.data_ptr(),
+                             None if self.b_table is None else self.b_table.data_ptr())
         self._ws = None
+
+    def zone_a_bytes(self):
+        """The cache's zone A as its logical bytes (gathered through the page table when paged)."""
+        n = int(self.sizes.zone_a_bytes)
+        if self.a_table is None:
+            return self.zone_a[:n]
+        o = torch.arange(n, device=self.zone_a.device)
+        return self.zone_a[self.a_table[o // A_PAGE_BYTES].long() * A_PAGE_BYTES + o % A_PAGE_BYTES]
+
+    def zone_b_rows(self):
+        """The cache's zone-B rows [rows, D] (gathered through the page table when paged)."""
+        n = int(self.sizes.zone_b_rows)
+        if self.b_table is None:
+            return self.zone_b[:n]
+        r = torch.arange(n, device=self.zone_b.device)
+        return self.zone_b.reshape(-1, self.shape.head_dim)[self.b_table[r // B_PAGE_ROWS].long() * B_PAGE_ROWS
+                                                             + r % B_PAGE_ROWS]
+
+    def release(self):
+        """Returns the cache's zone-A and zone-B pages to its pool (the cache must not be used after)."""
+        if self.ab_pool is not None and self.a_table is not None:
+            self.ab_pool.give_back(self.a_table, self.b_table)
+            self.a_table = self.b_table = None
 
     def zone_c_rows(self):
         """Zone C as logical rows: (k, v) fp16 [B, H_kv, cap_c, D], gathered through the page table."""
@@ -275,6 +313,8 @@ class Cache:
 
     def fits(self, sizes):
         """True when a plan with these totals can be packed into this cache's buffers."""
+        if self.ab_pool is not None:
+            return False
         return (sizes.zone_a_bytes <= self.zone_a.numel() and sizes.zone_b_rows <= self.zone_b.shape[0]
                 and sizes.index_slots <= self.index_map.numel())
 
@@ -305,16 +345,52 @@ def page_pool(shape, cap_c, device, extra_pages=0, seed=None):
     return pool_k, torch.zeros_like(pool_k), table
 
 
-def rdkv_pack(shape, plan, k, v, bits_tok, bits_chan, cap_c, stream=None, sizes=None, into=None, pages=None):
-    """Packs into a new Cache (zone C paged when `pages` from ``page_pool`` is given), or into the
-    buffers of `into` when they are large enough."""
+class ZonePool:
+    """Shared pools of zone-A pages (A_PAGE_BYTES each) and zone-B pages (B_PAGE_ROWS fp16 rows of D)
+    for the caches of several sequences, with a host-side free list: ``take`` hands a cache the page
+    tables its sizes need (distinct pages, in a seeded random order when seed is given, to show that
+    nothing depends on pages being adjacent), ``give_back`` returns them."""
+
+    def __init__(self, head_dim, a_pages, b_pages, device, seed=None):
+        self.D = head_dim
+        self.zone_a = torch.zeros(max(a_pages, 1) * A_PAGE_BYTES, dtype=torch.uint8, device=device)
+        self.zone_b = torch.zeros(max(b_pages, 1) * B_PAGE_ROWS, head_dim, dtype=torch.float16, device=device)
+        order_a, order_b = torch.arange(max(a_pages, 1)), torch.arange(max(b_pages, 1))
+        if seed is not None:
+            g = torch.Generator().manual_seed(seed)
+            order_a, order_b = order_a[torch.randperm(order_a.numel(), generator=g)], order_b[
+                torch.randperm(order_b.numel(), generator=g)]
+        self.free_a, self.free_b = order_a.tolist(), order_b.tolist()
+        self.device = device
+
+    def take(self, sizes):
+        na = max(1, -(-int(sizes.zone_a_bytes) // A_PAGE_BYTES))
+        nb = max(1, -(-int(sizes.zone_b_rows) // B_PAGE_ROWS))
+        if na > len(self.free_a) or nb > len(self.free_b):
+            raise RDKVError(RDKV_ERR_CAPACITY, f"zone pool exhausted: {na} A pages, {nb} B pages wanted, "
+                                               f"{len(self.free_a)}, {len(self.free_b)} free")
+        ta, self.free_a = self.free_a[:na], self.free_a[na:]
+        tb, self.free_b = self.free_b[:nb], self.free_b[nb:]
+        return (torch.tensor(ta, dtype=torch.int32, device=self.device),
+                torch.tensor(tb, dtype=torch.int32, device=self.device))
+
+    def give_back(self, a_table, b_table):
+        self.free_a += a_table.tolist()
+        self.free_b += b_table.tolist()
+
+
+def rdkv_pack(shape, plan, k, v, bits_tok, bits_chan, cap_c, stream=None, sizes=None, into=None, pages=None,
+              ab_pool=None):
+    """Packs into a new Cache (zone C paged when `pages` from ``page_pool`` is given; zones A and B in
+    pages of `ab_pool`, a ``ZonePool``, when given), or into the buffers of `into` when they are large
+    enough."""
     sizes = sizes if sizes is not None else rdkv_plan_sizes(plan, stream)
     if into is not None and into.fits(sizes) and into.c.cap_c == cap_c:
         cache = into
         cache.plan, cache.sizes = plan, sizes
         cache.c.plan, cache.c.sizes = plan.data_ptr(), sizes
     else:
-        cache = Cache(shape, plan, sizes, cap_c, k.device, pages=pages)
+        cache = Cache(shape, plan, sizes, cap_c, k.device, pages=pages, ab_pool=ab_pool)
     _check(lib().rdkv_pack(ctypes.byref(cache.c), _ptr(k), _ptr(v), _ptr(bits_tok), _ptr(bits_chan),
                            _stream(stream)))
     return cache
@@ -533,6 +609,36 @@ class MultiDecode:
 
 
 # ---------------------------------------------------------------- compression without synchronisation
+class RaggedDecode:
+    """One decode launch over the sequences of a ragged batch (rdkv_decode_ragged): caches of batch 1
+    with their own prompt lengths (zones often in one ZonePool), queries q [n_seq, H_q, D]."""
+
+    def __init__(self, seqs):
+        self.seqs = list(seqs)
+        self._arr = (ctypes.POINTER(CacheStruct) * len(self.seqs))(*[ctypes.pointer(c.c) for c in self.seqs])
+        self._ws = None
+
+    def workspace(self):
+        nb = lib().rdkv_decode_ragged_workspace_bytes(ctypes.cast(self._arr, _P), len(self.seqs))
+        if nb == 0:
+            raise RDKVError(RDKV_ERR_INVALID_ARG, lib().rdkv_last_error_string().decode())
+        if self._ws is None or self._ws.numel() < nb:
+            self._ws = torch.zeros(int(nb), dtype=torch.uint8, device=self.seqs[0].zone_a.device)
+        return self._ws
+
+    def attn(self, q, out=None, lse=None, stream=None):
+        n, Hq, D = q.shape
+        out = out if out is not None else torch.empty(n, Hq, D, dtype=torch.float32, device=q.device)
+        ws = self.workspace()
+        _check(lib().rdkv_decode_ragged(ctypes.cast(self._arr, _P), len(self.seqs), _ptr(q), _ptr(out), _ptr(lse),
+                                        _ptr(ws), ws.numel(), _stream(stream)))
+        return out
+
+    def status(self, stream=None):
+        return lib().rdkv_decode_ragged_status(ctypes.cast(self._arr, _P), len(self.seqs), _ptr(self.workspace()),
+                                               _stream(stream))
+
+
 def rdkv_zone_bounds(shape, avg_bits_v, avg_bits_k):
     """Upper bounds of the plan totals (host arithmetic only)."""
     sz = Sizes()

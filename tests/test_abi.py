@@ -241,3 +241,30 @@ def test_shape_workspace_query(L):
                     assert exact > 0, (G, D, batch, slots)
                     assert L.rdkv_workspace_bytes(ctypes.byref(shape), rdkv.RDKV_CALL_DECODE) >= exact, \
                         (G, D, batch, h_kv, slots, extra)
+
+
+def test_ragged_decode_argument_checks(L):
+    """The ragged launch refuses, before any launch, lists it cannot serve: no sequence or more than
+    eight, a cache of batch > 1, sequences with other heads, more than RDKV_COST_HEADS heads."""
+    fake = ctypes.c_void_p(256)
+
+    def cache(batch=1, h_q=8, h_kv=2, n=1000):
+        s = rdkv.make_shape(batch, n, h_q, h_kv, 128, 32, "f16")
+        sizes = rdkv.Sizes(4096, 0, 64, 64, 1024, 1024, 0, batch * h_kv)
+        return rdkv.CacheStruct(s, 256, 256, 256, 256, 256, 256, 256, 40, 32, sizes)
+
+    def arr(cs):
+        a = (ctypes.POINTER(rdkv.CacheStruct) * len(cs))(*[ctypes.pointer(c) for c in cs])
+        return ctypes.cast(a, ctypes.c_void_p)
+
+    good = [cache(n=1000), cache(n=3000)]
+    assert L.rdkv_decode_ragged_workspace_bytes(arr(good), 2) > 0
+    for cs, n, code in (([], 0, rdkv.RDKV_ERR_INVALID_ARG),
+                        ([cache()] * 9, 9, rdkv.RDKV_ERR_INVALID_ARG),
+                        ([cache(), cache(batch=2)], 2, rdkv.RDKV_ERR_INVALID_ARG),
+                        ([cache(), cache(h_q=16)], 2, rdkv.RDKV_ERR_INVALID_ARG),
+                        ([cache(h_q=64, h_kv=16)] * 5, 5, rdkv.RDKV_ERR_UNSUPPORTED)):
+        ptr = arr(cs) if cs else ctypes.c_void_p(0)
+        assert L.rdkv_decode_ragged_workspace_bytes(ptr, n) == 0
+        r = L.rdkv_decode_ragged(ptr, n, fake, fake, None, fake, 1 << 30, None)
+        assert r == code, (n, r)

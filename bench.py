@@ -201,6 +201,9 @@ def run_ours(args, ws, rank, local):
 
     dev = torch.device("cuda", local)
     w = synth.WORKLOADS[args.workload]
+    if args.tokens is not None:  # reduced prompt length (profiling captures); the description says so
+        w = w.scaled(n_tokens=args.tokens,
+                     description=w.description + f" (prompt reduced to N={args.tokens})")
     L = args.layers if args.layers is not None else DEFAULT_LAYERS.get(w.name, 4)
     S = args.decode_steps if args.decode_steps is not None else w.decode_steps
     avg = w.budgets[0] if args.budget is None else args.budget
@@ -986,6 +989,8 @@ def main():
     ap.add_argument("--layers", type=int, default=None, help="layers of the stack (default: per workload)")
     ap.add_argument("--decode-steps", type=int, default=None)
     ap.add_argument("--budget", type=float, default=None)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="prompt length N (default: the workload's; shorter for profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-comparator", action="store_true", help="skip the fp16 full-cache SDPA context number")

@@ -13,12 +13,13 @@
 // ring per consumer warp with bulk asynchronous copies (its lane w serves
 // consumer warp w, taking the block's next item whenever that ring has room);
 // every stage has a full and an empty mbarrier, and every wait is bounded
-// (RDKV_ERR_TIMEOUT).  The sixteen consumer warps only compute.  The last block
+// (RDKV_ERR_TIMEOUT).  The fifteen consumer warps only compute.  The last block
 // of a head to finish (an atomic ticket) merges the splits' partial softmax
 // states into the output (and, when asked, the log-sum-exp).  One launch may
 // attend several caches sharing the query (segments moved out of zone C and the
 // live cache): each block reads one cache, the blocks of a head over all caches
-// share its merge.  Zone C may be paged (16-row pages through a table).
+// share its merge; a ragged launch attends several sequences, each head with its own merge.  The
+// zones may be paged: zone A in 64 KB pages, zones B and C in 16-row pages, through tables.
 //
 // Products: mma.sync m16n8k16 (fp16 in, fp32 accumulate), tokens on M:
 //   S^T[16 tok x 8 heads]  += K^[16 tok x 16 slots] * B[16 slots x 8 heads]
@@ -597,21 +598,33 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         reinterpret_cast<int32_t*>(&hp_s)[lane] = reinterpret_cast<const int32_t*>(PP.heads + hbc)[lane];
     }
   } else if (warp == 0) {
-    // Blocks are dealt to heads in proportion to their estimated cost, at least one per head, over a
-    // nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the blocks past the last head's
-    // range leave at once.  Warp 0: one lane per head, one round trip for the plan records, then a
-    // scan.  Static inputs only (plan and capacity): the dealing is the same in every launch, also
-    // before the previous kernel on the stream has finished.
+    // Blocks are dealt to heads in proportion to their estimated cost (cumulative rounding), at least
+    // one per head, over a nominal P.ctas blocks; the grid has P.ctas + n_heads blocks and the blocks
+    // past the last head's range leave at once.  Warp 0: one lane per head, one round trip for the
+    // plan records, then a scan.  Static inputs only (plan and capacity): the dealing is the same in
+    // every launch, also before the previous kernel on the stream has finished.
     const int zc = ceil_div(P.cap_c, kCRows);
     int64_t total = 0;
     for (int h = lane; h < P.n_heads; h += 32) total += head_cost(P.heads[h], zc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
     int start = 0, found = -1;
+    int64_t wbase = 0;  // cost of the heads before this round of 32
     for (int h0 = 0; h0 < P.n_heads; h0 += 32) {
       const int h = h0 + lane;
       const int64_t w = h < P.n_heads ? head_cost(P.heads[h], zc) : 0;
-      const int c = h < P.n_heads ? max(1, (int)(total > 0 ? w * P.ctas / total : 0)) : 0;
+      // the head's share of the nominal blocks by cumulative rounding (the shares add up to P.ctas),
+      // at least one
+      int64_t wincl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o) wincl += v;
+      }
+      const int64_t lo = total > 0 ? (wbase + wincl - w) * P.ctas / total : 0;
+      const int64_t hi = total > 0 ? (wbase + wincl) * P.ctas / total : 0;
+      wbase += __shfl_sync(0xffffffffu, wincl, 31);
+      const int c = h < P.n_heads ? max(1, (int)(hi - lo)) : 0;
       int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1312,9 +1325,10 @@ static DecodeParams decode_params(const rdkv_cache* const* parts, int n, const D
     d.b_pages = c->zone_b_pages;
   }
   // Deal the blocks to the heads here when the plans' cost estimates reached the host: the kernel
-  // then knows its head at once instead of reading every head record first.  The rule is the
-  // kernel's own (at least one block per head and cache, the rest in proportion to the cost).  A
-  // ragged batch: head h is head h % h_kv of cache h / h_kv alone.
+  // then knows its head at once instead of reading every head record first.  At least one block per
+  // head and cache; every other block of the nominal count goes, one at a time, to the (head, cache)
+  // whose cost per block is then the largest, so the slowest block is as fast as it can be and every
+  // SM takes work.  A ragged batch: head h is head h % h_kv of cache h / h_kv alone.
   P.dealt = 0;
   bool known = n_heads <= RDKV_COST_HEADS && geo.splits <= kMaxDealtBlocks;
   for (int p = 0; known && p < n; ++p) {
@@ -1328,15 +1342,32 @@ static DecodeParams decode_params(const rdkv_cache* const* parts, int n, const D
     auto part_of = [&](int h, int p) { return ragged ? h / s.h_kv : p; };       // the cache of (head, part p)
     auto head_in = [&](int h) { return ragged ? h % s.h_kv : h; };             // the head within that cache
     const int parts_per_head = ragged ? 1 : n;
+    const int n_units = n_heads * parts_per_head;  // unit u: head u / parts_per_head, part u % parts_per_head
+    int64_t ucost[RDKV_COST_HEADS * kMaxParts];
+    int ublocks[RDKV_COST_HEADS * kMaxParts];
     int64_t total = 0;
-    for (int h = 0; h < n_heads; ++h)
-      for (int p = 0; p < parts_per_head; ++p) total += cost(part_of(h, p), head_in(h));
+    for (int u = 0; u < n_units; ++u) {
+      ucost[u] = std::max<int64_t>(1, cost(part_of(u / parts_per_head, u % parts_per_head), head_in(u / parts_per_head)));
+      total += ucost[u];
+    }
+    // in proportion, rounded down (at least one), then the rest one at a time
+    int dealt = 0;
+    for (int u = 0; u < n_units; ++u) {
+      ublocks[u] = std::max(1, (int)(ucost[u] * geo.ctas / total));
+      dealt += ublocks[u];
+    }
+    for (int extra = geo.ctas - dealt; extra > 0; --extra) {
+      int best = 0;  // the unit with the largest cost per block (cross-multiplied: exact)
+      for (int u = 1; u < n_units; ++u)
+        if (ucost[u] * ublocks[best] > ucost[best] * ublocks[u]) best = u;
+      ++ublocks[best];
+    }
     int start = 0;
     for (int h = 0; h < n_heads; ++h) {
       P.head_first[h] = (int16_t)start;
       for (int pi = 0; pi < parts_per_head; ++pi) {
         const int p = part_of(h, pi);
-        const int c = std::max(1, (int)(cost(p, head_in(h)) * geo.ctas / total));
+        const int c = ublocks[h * parts_per_head + pi];
         for (int k = 0; k < c; ++k) {
           P.block_head[start + k] = (uint8_t)h;
           P.block_part[start + k] = (uint8_t)p;

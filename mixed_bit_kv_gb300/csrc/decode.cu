@@ -211,11 +211,17 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 // Shared-memory loads through typed pointers into the block's shared window, so
 // the compiler folds constant offsets into the address ([reg + imm]).
-__device__ __forceinline__ uint2 lds64(const unsigned char* base, uint32_t off) {
-  return *reinterpret_cast<const uint2*>(base + off);
+// Loads from a 32-bit shared-memory address (no generic-address arithmetic per access).  Volatile:
+// they keep their place among the mbarrier waits and arrivals that guard the staged data.
+__device__ __forceinline__ uint4 lds128_s(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
-__device__ __forceinline__ uint4 lds128(const unsigned char* base, uint32_t off) {
-  return *reinterpret_cast<const uint4*>(base + off);
+__device__ __forceinline__ uint2 lds64_s(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 __device__ __forceinline__ uint32_t pick4(const uint4& v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
 // (x >> 8) & 0x00ff00ff in one byte permute: bytes 1 and 3 to bytes 0 and 2, zeros above
@@ -318,8 +324,8 @@ __device__ __forceinline__ void softmax_update(WarpAcc<D>& acc, float (&s)[NTB][
 // positions.  PK: hi and lo share one MMA (B columns 0-3 hi, 4-7 lo); else hi products go to shi and
 // lo products to slo.
 template <int W, bool PK>
-__device__ __forceinline__ void k_segment(const unsigned char* kw, uint32_t wb0, int kb0, int kb1, const uint4* bfr,
-                                          int lane, float (&shi)[2][4], float (&slo)[2][4], int nrem16) {
+__device__ __forceinline__ void k_segment(uint32_t kw, uint32_t wb0, int kb0, int kb1, uint32_t bfr, int lane,
+                                          float (&shi)[2][4], float (&slo)[2][4], int nrem16) {
   if (kb0 >= kb1) return;
   const int g = lane >> 2, q = lane & 3;
   // this lane's byte offset from a block's first word: its word index times 128, its tokens 16 g
@@ -329,12 +335,12 @@ __device__ __forceinline__ void k_segment(const unsigned char* kw, uint32_t wb0,
   const uint32_t c1 = 128u * (q + 4) + 16u * g;  // W = 16: the word of slots 2q + 8, 2q + 9
   const uint32_t m2 = 0x00030003u << (2 * q);
   const int sh4 = 8 * (q & 1);
-  uint32_t wb = wb0;
-  const uint4* bp = bfr + kb0 * 32 + lane;
+  uint32_t wb = kw + wb0;                            // shared address of the block's first word
+  uint32_t bp = bfr + 16u * (uint32_t)(kb0 * 32 + lane);  // this lane's B entry of the block
 #pragma unroll 2
-  for (int kb = kb0; kb < kb1; ++kb, wb += 64u * W, bp += 32) {
-    const uint4 bq = *bp;
-    const uint4 y0 = lds128(kw, wb + c0);
+  for (int kb = kb0; kb < kb1; ++kb, wb += 64u * W, bp += 512u) {
+    const uint4 bq = lds128_s(bp);
+    const uint4 y0 = lds128_s(wb + c0);
     uint4 y1 = y0;
     uint32_t k0 = ~0u, k1 = ~0u;
     if (W == 16) {
@@ -343,7 +349,7 @@ __device__ __forceinline__ void k_segment(const unsigned char* kw, uint32_t wb0,
       const int nrem = kb == kb1 - 1 ? nrem16 : kKB;
       k0 = 2 * q < nrem ? ~0u : 0u;
       k1 = 2 * q + 8 < nrem ? ~0u : 0u;
-      y1 = lds128(kw, wb + (k1 ? c1 : c0));
+      y1 = lds128_s(wb + (k1 ? c1 : c0));
     }
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
@@ -381,8 +387,8 @@ __device__ __forceinline__ void k_segment(const unsigned char* kw, uint32_t wb0,
 // raw 16-bit channels first at scale 1, then the accumulators move to 2^-24 and take the
 // quantised segments' products (codes as fp16 subnormals), then back, times log2(e)/sqrt(D).
 template <bool PK>
-__device__ __forceinline__ void tile_logits(const unsigned char* kw, const int (&seg_kb)[5], const uint32_t (&seg_wb)[4],
-                                            int nrem16, const uint4* bfr, int lane, float c24, float b0, float b1,
+__device__ __forceinline__ void tile_logits(uint32_t kw, const int (&seg_kb)[5], const uint32_t (&seg_wb)[4],
+                                            int nrem16, uint32_t bfr, int lane, float c24, float b0, float b1,
                                             float (&s)[2][4]) {
   float slo[2][4];
 #pragma unroll
@@ -453,22 +459,22 @@ __device__ __forceinline__ uint32_t v_field(uint32_t x, int e) {
 // zero-point sums go to acc.z through one MMA per 16 tokens whose A row g holds the zeros of
 // channel group g.
 template <int D, int VB>
-__device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned char* vcodes, const unsigned char* vmeta,
-                                               int lane, const uint32_t (*pb)[2]) {
+__device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, uint32_t vcodes, uint32_t vmeta, int lane,
+                                               const uint32_t (*pb)[2]) {
   const int g = lane >> 2, q = lane & 3;
   constexpr int CM = D / 16, NG = D / 32, NW = D * VB / 128, PER = 16 / VB;
 #pragma unroll
   for (int tb = 0; tb < 2; ++tb) {
     // scales of the lane's two pairs for every group (h = 0, then h = 1), 2 NG words
     uint32_t sc[2 * NG];
-    const unsigned char* sp = vmeta + 4 * ((tb * 4 + q) * 2 * NG);
+    const uint32_t sp = vmeta + 4u * ((tb * 4 + q) * 2 * NG);
 #pragma unroll
     for (int i = 0; i < 2 * NG; i += 4) {
-      const uint4 t = lds128(sp, 4 * i);
+      const uint4 t = lds128_s(sp + 4u * i);
       sc[i] = t.x; sc[i + 1] = t.y; sc[i + 2] = t.z; sc[i + 3] = t.w;
     }
     uint2 za = make_uint2(0u, 0u);
-    if (g < NG) za = lds64(vmeta, 4 * (16 * NG + ((tb * NG + g) * 4 + q) * 2));
+    if (g < NG) za = lds64_s(vmeta + 4u * (16 * NG + ((tb * NG + g) * 4 + q) * 2));
     mma16816(acc.z, za.x, 0u, za.y, 0u, pb[tb][0], pb[tb][1]);
     uint32_t bb[2][NG];
 #pragma unroll
@@ -480,16 +486,16 @@ __device__ __forceinline__ void tile_pv_packed(WarpAcc<D>& acc, const unsigned c
     }
     // the lane's code words: pair h = 0 then h = 1, NW words each
     uint32_t wd[2 * NW];
-    const unsigned char* cp = vcodes + 4 * (((tb * 8 + g) * 4 + q) * 2 * NW);
+    const uint32_t cp = vcodes + 4u * (((tb * 8 + g) * 4 + q) * 2 * NW);
 #pragma unroll
     for (int i = 0; i < 2 * NW; i += 4) {
       if (2 * NW >= 4) {
-        const uint4 t = lds128(cp, 4 * i);
+        const uint4 t = lds128_s(cp + 4u * i);
         wd[i] = t.x; wd[i + 1] = t.y; wd[i + 2] = t.z; wd[i + 3] = t.w;
       }
     }
     if (2 * NW == 2) {
-      const uint2 t = lds64(cp, 0);
+      const uint2 t = lds64_s(cp);
       wd[0] = t.x; wd[1] = t.y;
     }
 #pragma unroll
@@ -525,9 +531,9 @@ __device__ __forceinline__ void pv_fp16(WarpAcc<D>& acc, uint32_t vrows, int lan
 // tokens past the kept ones masked (the last tile of a class), the softmax update, the accumulators
 // moved to the class's scale, PV.
 template <int D, bool PK>
-__device__ __forceinline__ void consume_tile(WarpAcc<D>& acc, int& o_mode, const unsigned char* stp, uint32_t tb_bytes,
+__device__ __forceinline__ void consume_tile(WarpAcc<D>& acc, int& o_mode, uint32_t stp, uint32_t tb_bytes,
                                              int cls, int n_real, int RW, const int (&seg_kb)[5],
-                                             const uint32_t (&seg_wb)[4], int nrem16, const uint4* bfr, int lane,
+                                             const uint32_t (&seg_wb)[4], int nrem16, uint32_t bfr, int lane,
                                              float c24, float bias0, float bias1) {
   const int g = lane >> 2;
   float s[2][4];
@@ -549,11 +555,11 @@ __device__ __forceinline__ void consume_tile(WarpAcc<D>& acc, int& o_mode, const
     rescale_o<D>(acc, o_mode, vb_cls);
     o_mode = vb_cls;
   }
-  const unsigned char* vcodes = stp + 4 * kTile * RW;
+  const uint32_t vcodes = stp + 4u * kTile * RW;
   if (cls == 0) tile_pv_packed<D, 2>(acc, vcodes, vcodes + kTile * D * 2 / 8, lane, pb);
   else if (cls == 1) tile_pv_packed<D, 4>(acc, vcodes, vcodes + kTile * D * 4 / 8, lane, pb);
   else if (cls == 2) tile_pv_packed<D, 8>(acc, vcodes, vcodes + kTile * D * 8 / 8, lane, pb);
-  else pv_fp16<D, 2>(acc, smem_u32(stp) + tb_bytes, lane, pb);
+  else pv_fp16<D, 2>(acc, stp + tb_bytes, lane, pb);
 }
 
 // Estimated decode cost of a head: its zone-A tiles and its zone-C blocks.
@@ -1010,8 +1016,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       const unsigned char* stp = wring + st_pos[sidx];
       const int cls = (rec >> 24) - 1, ti = rec & 0xffffff;  // ti: tile of the class, or zone-C block
       if (cls >= 0) {
-        consume_tile<D, PK>(acc, o_mode, stp, (uint32_t)ctb(cls), cls, min(kTile, (int)cnv(cls) - kTile * ti), RW,
-                            seg_kb, seg_wb, nrem16, bfr, lane, c24, bias0, bias1);
+        consume_tile<D, PK>(acc, o_mode, smem_u32(stp), (uint32_t)ctb(cls), cls, min(kTile, (int)cnv(cls) - kTile * ti),
+                            RW, seg_kb, seg_wb, nrem16, smem_u32(bfr), lane, c24, bias0, bias1);
       } else {
         if (o_mode != 16) {
           rescale_o<D>(acc, o_mode, 16);

@@ -184,10 +184,60 @@ __device__ __forceinline__ float4 load4(const __half* p) {
 }
 __device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
+// One 32-bit K word of token row kr: word wg of the width-KB segment whose first slot is sbase.
+// prm[s] = {zero, scale, 1/scale, channel (as int bits, -1 for a pad)} of slot s; codes of pad slots
+// and of pad tokens (real false) are 0.
+template <int KB>
+__device__ __forceinline__ uint32_t k_word(int wg, int sbase, const float* kr, bool real, const float4* prm) {
+  constexpr int per = 32 / KB, wpk = KB / 2;
+  constexpr float hmax = (float)((1 << (KB < 16 ? KB : 1)) - 1);
+  const int s0 = sbase + kKB * (wg / wpk), wi = wg % wpk;
+  uint32_t word = 0;
+#pragma unroll
+  for (int e = 0; e < per; ++e) {
+    const float4 pr = prm[s0 + k_slot_in_block(KB, wi, e)];
+    const int c = __float_as_int(pr.w);
+    if (c >= 0 && real) {
+      const float x = kr[c];
+      const uint32_t code = KB == 16 ? (uint32_t)half_bits(x) : qcode_rcp(x, pr.x, pr.y, pr.z, hmax);
+      word |= code << bit_off(e, KB);
+    }
+  }
+  return word;
+}
+
+// The V words of a tile of width VB < 16, straight from the staged rows Vf [32][D + 1]: word i is
+// word wk of pair h of lane (g, q) of 16-token block tb, i = ((tb * 8 + g) * 4 + q) * 2 nw + h nw + wk
+// (nw = D VB / 128); it holds entries kk = wk per + e (per = 16 / VB) of the lane's channel list,
+// channel 16 (kk mod D/16) + 8 (kk div D/16) + g, at bit VB e for token 2p (low half) and 16 + VB e
+// for token 2p + 1, p = 8 tb + q + 4 h.  vq [32][D/32] holds {zero, scale, 1/scale} per token and
+// group; pad tokens (n_real and up) get code 0.
+template <int VB, int D, typename At>
+__device__ __forceinline__ void v_words(const float* Vf, const float4* vq, int n_real, int64_t vcode_b, At at) {
+  constexpr int VP = D + 1, CM = D / 16, NG = D / kVGroup, NW = D * VB / 128, PER = 16 / VB;
+  constexpr float hmax = (float)((1 << VB) - 1);
+  for (int i = threadIdx.x; i < D * VB; i += kPackThreads) {
+    const int wk = i % NW, rest = i / NW;
+    const int h = rest & 1, q = (rest >> 1) & 3, g = (rest >> 3) & 7, tb = rest >> 6;
+    const int r0 = 2 * (8 * tb + q + 4 * h), r1 = r0 + 1;
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int kk = wk * PER + e;
+      const int c = 16 * (kk % CM) + 8 * (kk / CM) + g;
+      const float4 p0 = vq[r0 * NG + c / kVGroup], p1 = vq[r1 * NG + c / kVGroup];
+      const uint32_t c0 = r0 < n_real ? qcode_rcp(Vf[r0 * VP + c], p0.x, p0.y, p0.z, hmax) : 0u;
+      const uint32_t c1 = r1 < n_real ? qcode_rcp(Vf[r1 * VP + c], p1.x, p1.y, p1.z, hmax) : 0u;
+      word |= (c0 << (VB * e)) | (c1 << (16 + VB * e));
+    }
+    *reinterpret_cast<uint32_t*>(at(vcode_b + 4 * (int64_t)i)) = word;
+  }
+}
+
 template <int D>
 __host__ __device__ constexpr size_t pack_smem_bytes_of() {
-  return (size_t)kTile * (D + 1) * 4 + (size_t)kTile * D * 4 + (size_t)kTile * D + (size_t)(D + kSlotPad) * 12 +
-         (size_t)kTile * (D / kVGroup) * 12 + (size_t)(D + kSlotPad) * 2 + 16;
+  return (size_t)2 * kTile * (D + 1) * 4 + (size_t)(D + kSlotPad) * 16 + (size_t)kTile * (D / kVGroup) * 16 +
+         (size_t)(D + kSlotPad) * 2 + 16;
 }
 
 template <typename T, int D>
@@ -242,11 +292,10 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   const int w8 = hp.k_words[0], w4 = w8 + hp.k_words[1], w2 = w4 + hp.k_words[2];  // first word of each
 
   float* Kf = reinterpret_cast<float*>(smem_raw);               // [32][KP]
-  float* Vf = Kf + kTile * KP;                                  // [32][D] (16-byte aligned)
-  uint8_t* vc = reinterpret_cast<uint8_t*>(Vf + kTile * D);     // [32][D]
-  float* kq = reinterpret_cast<float*>(vc + kTile * D);         // [KS][3] zero, scale, 1/scale
-  float* vq = kq + 3 * KS;                                      // [32][NG][3]
-  int16_t* sch = reinterpret_cast<int16_t*>(vq + 3 * kTile * NG);  // [KS] slot channels
+  float* Vf = Kf + kTile * KP;                                  // [32][KP]
+  float4* kq = reinterpret_cast<float4*>(Vf + kTile * KP);      // [KS] zero, scale, 1/scale, channel
+  float4* vq = kq + KS;                                         // [32][NG] zero, scale, 1/scale
+  int16_t* sch = reinterpret_cast<int16_t*>(vq + kTile * NG);   // [KS] slot channels
   __shared__ int tok[kTile];
   const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
   if (tid < kTile) tok[tid] = index_map[slot0 + tid];
@@ -267,7 +316,11 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
     kd[1] = kx.y;
     kd[2] = kx.z;
     kd[3] = kx.w;
-    reinterpret_cast<float4*>(Vf)[i] = vx;
+    float* vd = Vf + r * KP + c;
+    vd[0] = vx.x;
+    vd[1] = vx.y;
+    vd[2] = vx.z;
+    vd[3] = vx.w;
   }
   __syncthreads();
 
@@ -281,23 +334,20 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   for (int i = tid; i < KS + (vbits < 16 ? kTile * NG : 0); i += kPackThreads) {
     if (i < KS) {
       const int s = i;
-      if (s < s16) continue;
-      const int kb = s < sb4 ? 8 : s < sb2 ? 4 : 2;
       const int c = sch[s];
       float z = 0.f, sc = 0.f, rs = 0.f;
-      if (c >= 0) {
+      if (c >= 0 && s >= s16) {
+        const int kb = s < sb4 ? 8 : s < sb2 ? 4 : 2;
         const float2 st = kstat[(int64_t)head * D + c];
         const QParams p = qparams(st.x, st.y, kb);
         z = p.zero;
         sc = p.scale;
         rs = sc != 0.f ? __frcp_rn(sc) : 0.f;
       }
-      kq[3 * s] = z;
-      kq[3 * s + 1] = sc;
-      kq[3 * s + 2] = rs;
+      kq[s] = make_float4(z, sc, rs, __int_as_float(c));
     } else {
       const int vi = i - KS, r = vi / NG, g = vi % NG;
-      const float* x = Vf + r * D + g * kVGroup;
+      const float* x = Vf + r * KP + g * kVGroup;
       uint16_t sc_h = 0, ze_h = 0;
       float z = 0.f, sc = 0.f, rs = 0.f;
       if (r < n_real) {
@@ -316,9 +366,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
         sc = p.scale;
         rs = sc != 0.f ? __frcp_rn(sc) : 0.f;
       }
-      vq[3 * vi] = z;
-      vq[3 * vi + 1] = sc;
-      vq[3 * vi + 2] = rs;
+      vq[vi] = make_float4(z, sc, rs, 0.f);
       // token pair p = 8 tb + q + 4 h: scales ordered (tb, q, h, group), zeros (tb, group, q, h), each
       // 32-bit word the pair's even token (low half) and odd token (high half)
       const int pp = r >> 1, tb = pp >> 3, q = pp & 3, h = (pp >> 2) & 1;
@@ -329,7 +377,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
   if (vbits == 16) {
     for (int i = tid; i < kTile * D; i += kPackThreads) {
       const int r = i / D;
-      zone_b[zone_b_offset(b_pages, brow + r, D) + i % D] = r < n_real ? half_bits(Vf[i]) : (uint16_t)0;
+      zone_b[zone_b_offset(b_pages, brow + r, D) + i % D] = r < n_real ? half_bits(Vf[r * KP + i % D]) : (uint16_t)0;
     }
   }
   __syncthreads();
@@ -341,60 +389,18 @@ __global__ void __launch_bounds__(kPackThreads) pack_tile_kernel(const T* __rest
     const bool real = r < n_real;
     const float* kr = Kf + r * KP;
     for (int w = ty; w < RW; w += kPackThreads / 32) {
-      // segment width, first slot of the word's k-block and the word's index inside that block
-      int kb, sbase, wg;
-      if (w < w8) { kb = 16; sbase = 0; wg = w; }
-      else if (w < w4) { kb = 8; sbase = s16; wg = w - w8; }
-      else if (w < w2) { kb = 4; sbase = sb4; wg = w - w4; }
-      else { kb = 2; sbase = sb2; wg = w - w2; }
-      const int per = 32 / kb, wpk = kb / 2;
-      const int s0 = sbase + kKB * (wg / wpk), wi = wg % wpk;
-      const float hmax = (float)((1 << kb) - 1);
-      uint32_t word = 0;
-      for (int e = 0; e < per; ++e) {
-        const int s = s0 + k_slot_in_block(kb, wi, e);
-        const int c = sch[s];
-        if (c < 0 || !real) continue;
-        const float x = kr[c];
-        const uint32_t code = kb == 16 ? (uint32_t)half_bits(x) : qcode_rcp(x, kq[3 * s], kq[3 * s + 1], kq[3 * s + 2], hmax);
-        word |= code << bit_off(e, kb);
-      }
+      // the word's segment (a warp-uniform branch), then its codes with the width known
+      const uint32_t word = w < w8   ? k_word<16>(w, 0, kr, real, kq)
+                            : w < w4 ? k_word<8>(w - w8, s16, kr, real, kq)
+                            : w < w2 ? k_word<4>(w - w4, sb4, kr, real, kq)
+                                     : k_word<2>(w - w2, sb2, kr, real, kq);
       *reinterpret_cast<uint32_t*>(at(4 * (32 * w + 4 * (r % 8) + r / 8))) = word;
     }
   }
-  // V codes: lanes along channels, warps along tokens
-  if (vbits < 16) {
-    const float hmax = (float)((1 << vbits) - 1);
-    for (int r = ty; r < kTile; r += kPackThreads / 32) {
-      for (int c = tx; c < D; c += 32) {
-        const int vi = r * NG + c / kVGroup;
-        vc[r * D + c] = r < n_real ? (uint8_t)qcode_rcp(Vf[r * D + c], vq[3 * vi], vq[3 * vi + 1], vq[3 * vi + 2], hmax)
-                                   : (uint8_t)0;
-      }
-    }
-  }
-  __syncthreads();
-  // V words: word i of the tile is word wk of pair h of lane (g, q) of 16-token block tb,
-  // i = ((tb * 8 + g) * 4 + q) * 2 nw + h nw + wk (nw = D b / 128); it holds entries k = wk per + e
-  // (per = 16 / b) of the lane's channel list, channel 16 (k mod D/16) + 8 (k div D/16) + g, at bit
-  // b e for token 2p (low half) and 16 + b e for token 2p + 1, p = 8 tb + q + 4 h
-  if (vbits < 16) {
-    constexpr int CM = D / 16;
-    const int nw = D * vbits / 128, per = 16 / vbits;
-    for (int i = tid; i < D * vbits; i += kPackThreads) {
-      const int wk = i % nw, rest = i / nw;
-      const int h = rest & 1, q = (rest >> 1) & 3, g = (rest >> 3) & 7, tb = rest >> 6;
-      const int p = 8 * tb + q + 4 * h;
-      uint32_t word = 0;
-      for (int e = 0; e < per; ++e) {
-        const int kk = wk * per + e;
-        const int c = 16 * (kk % CM) + 8 * (kk / CM) + g;
-        word |= (uint32_t)vc[(2 * p) * D + c] << (vbits * e);
-        word |= (uint32_t)vc[(2 * p + 1) * D + c] << (16 + vbits * e);
-      }
-      *reinterpret_cast<uint32_t*>(at(vcode_b + 4 * (int64_t)i)) = word;
-    }
-  }
+  // V words (codes taken straight from the staged rows), the width known at compile time
+  if (vbits == 2) v_words<2, D>(Vf, vq, n_real, vcode_b, at);
+  else if (vbits == 4) v_words<4, D>(Vf, vq, n_real, vcode_b, at);
+  else if (vbits == 8) v_words<8, D>(Vf, vq, n_real, vcode_b, at);
 }
 
 template <typename T>

@@ -291,3 +291,45 @@ def test_early_columns_token_weights():
     sc = rdkv.rdkv_score(shape, q, k, v)
     torch.cuda.synchronize()
     _check_interior_columns(w, q, k, sc, 0, 2, 256, 64)
+
+
+def test_ragged_batch_full_size_sampled_sequences():
+    """The benchmark's ragged batch: eight Llama-3.2-3B-shaped sequences of 32768 down to 4096 prompt
+    tokens, each compressed on its own at 2.5 bits, zones A and B in one shuffled page pool, one
+    rdkv_decode_ragged launch.  Sequences 0, 4 and 7 (32768, 16384 and 4096 tokens): their zones
+    gathered back through the page tables equal the oracle's pack byte for byte, and their outputs
+    and log-sum-exps match the oracle's decode of each sequence alone."""
+    base = synth.WORKLOADS["llama3b"]
+    lengths = (32768, 28672, 24576, 20480, 16384, 12288, 8192, 4096)
+    avg, D = base.budgets[0], base.head_dim
+    packs = []
+    for i, n in enumerate(lengths):
+        w = base.scaled(n_tokens=n)
+        q, k, v = (t[None].to(DEV) for t in synth.prefill(w, i, 0))
+        shape = rdkv.shape_of(q, k, w.window)
+        sc = rdkv.rdkv_score(shape, q, k, v)
+        al = rdkv.rdkv_allocate(shape, sc["g_tok"], sc["w_chan"], k, avg, avg)
+        packs.append((shape, al, k, v, rdkv.rdkv_plan_sizes(al["plan"])))
+        del q, sc
+    a_pages = sum(-(-int(p[4].zone_a_bytes) // rdkv.A_PAGE_BYTES) for p in packs)
+    b_pages = sum(max(1, -(-int(p[4].zone_b_rows) // rdkv.B_PAGE_ROWS)) for p in packs)
+    pool = rdkv.ZonePool(D, a_pages, b_pages, DEV, seed=3)
+    caches = [rdkv.rdkv_pack(shape, al["plan"], k, v, al["bits_tok"], al["bits_chan"], base.window, sizes=sizes,
+                             ab_pool=pool) for shape, al, k, v, sizes in packs]
+    qs = [synth.decode_step(base.scaled(n_tokens=n), 0, 0)[0][0] for n in lengths]
+    lse = torch.empty(len(lengths), base.h_q, dtype=torch.float32, device=DEV)
+    rd = rdkv.RaggedDecode(caches)
+    out = rd.attn(torch.stack(qs).to(DEV), lse=lse).cpu().numpy()
+    assert rd.status() == rdkv.RDKV_OK
+    lse = lse.cpu().numpy()
+    for i in (0, 4, 7):
+        shape, al, k, v, sizes = packs[i]
+        ref = O.pack(k.float().cpu().numpy(), v.float().cpu().numpy(), al["bits_tok"].cpu().numpy(),
+                     al["bits_chan"].cpu().numpy(), base.window, cap_c=base.window)
+        za = caches[i].zone_a_bytes().cpu().numpy()
+        assert za.size == ref["zone_a"].size and np.array_equal(za, ref["zone_a"]), i
+        zb = caches[i].zone_b_rows().cpu().numpy()
+        assert np.array_equal(zb.view(np.uint16)[: ref["zone_b"].shape[0]], ref["zone_b"].view(np.uint16)), i
+        exp, exp_lse = O.decode_lse(ref, qs[i][None].numpy())
+        assert np.abs(out[i] - exp[0]).max() <= 2e-3, i
+        assert np.abs(lse[i] - exp_lse[0]).max() <= 2e-3, i

@@ -43,8 +43,8 @@ namespace rdkv {
 
 constexpr int kConsumers = 15;             // consumer warps of a block (one block per SM; with the producer, four warps per scheduler)
 constexpr int kDecWarps = kConsumers + 1;  // and the producer warp
-constexpr int kStages = 4;                 // stages in flight per consumer warp
-constexpr int kPrologueItems = 4;          // stages per consumer issued before the wait for the previous kernel (all of them)
+constexpr int kStages = 8;                 // stages in flight per consumer warp (the ring's bytes permitting)
+constexpr int kPrologueItems = 4;          // stages per consumer issued before the wait for the previous kernel
 constexpr int kMaxDealtBlocks = 256;       // grids up to this size may be dealt to heads on the host
 constexpr uint8_t kNoHead = 0xff;
 constexpr int kMaxParts = 8;               // caches one launch may attend
@@ -761,9 +761,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     const bool has_ring = lane < P.ring_warps;
     unsigned char* wring = ring + (int64_t)lane * P.ring_bytes;
     int issued = 0, released = 0, pending = -1;
-    uint32_t head_p = 0, used = 0, need[kStages] = {0u, 0u, 0u, 0u};
+    uint32_t head_p = 0, used = 0, need[kStages] = {};
     bool drained = !has_ring, ended = !serve, items_final = false;
-    int n_items = zc_start, len_c = 0, n_block_items = 0;
+    int n_items = zc_start, len_c = 0;
     int cap = kPrologueItems;
     long long idle0 = clock64();
     bool timed_out = false;
@@ -777,11 +777,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
         moved = true;
       }
       if (issued == released) head_p = used = 0;  // empty ring: start at its beginning
-      // near the end of the block's items a consumer holds at most two (the one it works on and the
-      // next), so that the warps run out of work together
-      const int left = items_final ? n_block_items - *(volatile int*)&next_k : kStages * kConsumers;
-      const int depth = left < 2 * kConsumers ? 2 : kStages;
-      while (!drained && issued - released < min(cap, depth)) {
+      while (!drained && issued - released < cap) {
         int it = pending;
         if (it < 0) it = isplit + in_split * atomicAdd(&next_k, 1);
         if (it >= n_items) {
@@ -872,7 +868,6 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     asm volatile("griddepcontrol.wait;" ::: "memory");
     len_c = min(*PP.len_dev, PP.cap_c);
     n_items = zc_start + ceil_div(len_c + (fused ? 1 : 0), kCRows);
-    n_block_items = n_items > isplit ? ceil_div(n_items - isplit, in_split) : 0;
     items_final = true;
     cap = kStages;
     idle0 = clock64();

@@ -56,19 +56,24 @@ __host__ __device__ inline int k_slot_in_block(int b, int i, int e) {
 // K metadata of a head (fp16 scale and zero per quantised slot) in front of its tiles, whole 16 bytes.
 __host__ __device__ inline int64_t head_meta_bytes(int meta_slots) { return align_up(4 * (int64_t)meta_slots, 16); }
 
-// Estimated zone-A decode cost of a head (instruction units per warp) from its plan record: every
-// tile pays a base (softmax, staging) plus its K k-blocks (quantised blocks cost about twice a raw
-// 16-bit one) plus its V class.  Only the ratios between heads matter: they decide how many
-// blocks each head gets.
+// Estimated zone-A decode cost of a head (units of about a third of a nanosecond of one block's
+// loop) from its plan record: every tile pays its V class (with the staging, softmax and
+// bookkeeping every tile has) plus its K k-blocks.  The constants are a least-squares fit of the
+// measured per-block loop times of 112 (head, workload, budget) cases on GB300; raw 16-bit K
+// blocks, absent from those cases, are costed at three quarters of a 2-bit one, as their
+// instruction count suggests.  Only the ratios between heads matter: they decide how many blocks
+// each head gets.
 __host__ __device__ inline int64_t head_cost_a(const rdkv_head_plan& hp) {
-  const int nkb16 = ceil_div(hp.k_words[0] * 2, kKB);
-  const int nkbq = ceil_div(hp.k_words[1] * 4, kKB) + ceil_div(hp.k_words[2] * 8, kKB) + ceil_div(hp.k_words[3] * 16, kKB);
-  const int64_t per_tile = 80 + 12 * nkb16 + 16 * nkbq;
-  return (int64_t)hp.tiles[0] * (per_tile + 115) + (int64_t)hp.tiles[1] * (per_tile + 130) +
-         (int64_t)hp.tiles[2] * (per_tile + 140) + (int64_t)hp.tiles[3] * (per_tile + 50);
+  const int64_t nkb16 = ceil_div(hp.k_words[0] * 2, kKB);
+  const int64_t nkb8 = ceil_div(hp.k_words[1] * 4, kKB), nkb4 = ceil_div(hp.k_words[2] * 8, kKB);
+  const int64_t nkb2 = ceil_div(hp.k_words[3] * 16, kKB);
+  const int64_t per_tile_k = 12 * nkb16 + 20 * nkb8 + 21 * nkb4 + 16 * nkb2;
+  const int64_t tiles = (int64_t)hp.tiles[0] + hp.tiles[1] + hp.tiles[2] + hp.tiles[3];
+  return (int64_t)hp.tiles[0] * 238 + (int64_t)hp.tiles[1] * 277 + (int64_t)hp.tiles[2] * 534 +
+         (int64_t)hp.tiles[3] * 1557 + tiles * per_tile_k;
 }
-// ... and of one zone-C block of 16 rows
-constexpr int kZoneCBlockCost = 120;
+// ... and of one zone-C block of 16 rows (fp16 K and V: about half a class-16 tile)
+constexpr int kZoneCBlockCost = 800;
 
 __device__ __forceinline__ const rdkv_plan_header* plan_header(const void* plan) {
   return reinterpret_cast<const rdkv_plan_header*>(plan);

@@ -17,7 +17,7 @@ namespace rdkv {
 __device__ __forceinline__ float to_float(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_float(float x) { return x; }
 
-// Quantiser parameters of one group; returns false when scale is 0 (all codes 0).
+// Quantiser parameters of one group (scale 0: every code of the group is 0).
 struct QParams {
   float zero, scale;
   uint16_t zero_h, scale_h;
@@ -32,16 +32,10 @@ __device__ __forceinline__ QParams qparams(float mn, float mx, int bits) {
   p.scale = __half2float(sh);
   return p;
 }
-__device__ __forceinline__ uint32_t qcode(float x, const QParams& p, int bits) {
-  if (p.scale == 0.0f) return 0u;
-  const float t = rintf(__fdiv_rn(x - p.zero, p.scale));
-  const float hi = (float)((1 << bits) - 1);
-  return (uint32_t)fminf(fmaxf(t, 0.0f), hi);
-}
-
-// The same code with the division replaced by a multiply with r = fp32(1/scale): |d r - d/scale|
-// stays below 2^-15 for the |d/scale| < 256 of a group's own values, so rint agrees with the IEEE
-// quotient's unless d r is within 2^-12 of a half-integer; there the quotient is computed exactly.
+// The code clamp(rint((x - zero) / scale), 0, hi) (IEEE fp32 quotient, ties to even), with the
+// division replaced by a multiply with r = fp32(1/scale): |d r - d/scale| stays below 2^-15 for the
+// |d/scale| < 256 of a group's own values, so rint agrees with the IEEE quotient's unless d r is
+// within 2^-12 of a half-integer; there the quotient is computed exactly.
 __device__ __forceinline__ uint32_t qcode_rcp(float x, float zero, float scale, float rscale, float hi) {
   if (scale == 0.0f) return 0u;
   const float d = x - zero;

@@ -24,6 +24,12 @@ CASES = {
                                                    decode_steps=6),
     "d64_f16": synth.WORKLOADS["tiny"].scaled(dtype="f16", n_tokens=777, h_q=8, h_kv=2, window=17, batch=1),
     "zipf_f16": synth.WORKLOADS["llama8b"].scaled(n_tokens=1500, h_q=8, h_kv=2, window=128, batch=1),
+    # one query head per KV head; two (fp32, D = 64); eight (fp32, D = 128: the K operand's high part
+    # and remainder as two products, the zone-C queries' remainder too)
+    "mha_f16": synth.WORKLOADS["llama3b"].scaled(n_tokens=900, h_q=4, h_kv=4, window=32, batch=1, decode_steps=4),
+    "g2_f32": synth.WORKLOADS["tiny"].scaled(n_tokens=700, h_q=4, h_kv=2, window=20),
+    "g8_f32": synth.WORKLOADS["llama3b"].scaled(dtype="f32", n_tokens=600, h_q=16, h_kv=2, window=24, batch=1,
+                                                 decode_steps=4),
 }
 
 

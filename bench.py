@@ -851,7 +851,7 @@ def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, de
     h2d = sum(t.numel() * t.element_size() for trip in h_pre for t in trip) + \
         sum(t.numel() * t.element_size() for t in (h_dq, h_dk, h_dv))
     d2h = h_out.numel() * 4 + L * 96   # outputs, plus the plan totals each rdkv_plan_sizes reads back
-    step_s = median(times)
+    step_s = max_over_ranks([median(times)], ws, dev)[0]  # the slowest rank sets the whole job's step
     del h_pre, d_pre, caches, score_out, alloc_out, g
     return {"value": round(ws * dec_bytes / step_s / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

@@ -59,7 +59,8 @@ extern "C" size_t rdkv_workspace_bytes(const rdkv_shape* shape, int32_t which_ca
     case RDKV_CALL_DECODE: {
       const int64_t n_heads = (int64_t)shape->batch * shape->h_kv;
       const int64_t partial = decode_partial_stride(shape->h_q / shape->h_kv, shape->head_dim);
-      return (size_t)(align_up((num_sms() + n_heads) * partial * 4, 256) + decode_ticket_bytes(n_heads));
+      // up to two blocks per SM plus one spare block per head (launches over many heads)
+      return (size_t)(align_up((2 * num_sms() + n_heads) * partial * 4, 256) + decode_ticket_bytes(n_heads));
     }
     default:
       return 0;

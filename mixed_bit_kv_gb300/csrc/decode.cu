@@ -41,11 +41,15 @@
 
 namespace rdkv {
 
-constexpr int kConsumers = 15;             // consumer warps of a block (one block per SM; with the producer, four warps per scheduler)
-constexpr int kDecWarps = kConsumers + 1;  // and the producer warp
+// Consumer warps of a block: 15 with one block per SM (with the producer, four warps per
+// scheduler), or 7 with two blocks per SM for launches over many (head, cache) units, whose blocks
+// then share their SM as they finish.
+constexpr int kConsumersWide = 15;
+constexpr int kConsumersNarrow = 7;
+constexpr int kManyUnits = 32;  // launches over this many units or more take the two-block layout
 constexpr int kStages = 8;                 // stages in flight per consumer warp (the ring's bytes permitting)
 constexpr int kPrologueItems = 4;          // stages per consumer issued before the wait for the previous kernel
-constexpr int kMaxDealtBlocks = 256;       // grids up to this size may be dealt to heads on the host
+constexpr int kMaxDealtBlocks = 512;       // grids up to this size may be dealt to heads on the host
 constexpr uint8_t kNoHead = 0xff;
 constexpr int kMaxParts = 8;               // caches one launch may attend
 constexpr int kCRows = 16;                 // zone-C rows per work item
@@ -57,9 +61,9 @@ constexpr long long kMinWaitCycles = 100000;     // shortest limit the timeout s
 // Bytes of the fixed part of the decode kernel's shared memory (before the rings): the K B-fragments
 // (16 bytes per k-block and lane), zone-C query fragments, slot table, k-block offsets, stage
 // barriers and records, the fused step's new row, the head's K metadata and the group's query rows.
-__host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
+__host__ __device__ constexpr int64_t decode_fixed_smem(int D, int NC) {
   return ((int64_t)kMaxKB * 32 * 16 + (int64_t)(D / 16) * 32 * 16 + (int64_t)(D + kSlotPad) * 2 + kMaxKB * 8 +
-          (int64_t)kConsumers * kStages * 24 + (int64_t)2 * D * 2 + (int64_t)(D + kSlotPad) * 4 +
+          (int64_t)NC * kStages * 24 + (int64_t)2 * D * 2 + (int64_t)(D + kSlotPad) * 4 +
           (int64_t)8 * D * 4 + 127) /
          128 * 128;
 }
@@ -67,7 +71,7 @@ __host__ __device__ constexpr int64_t decode_fixed_smem(int D) {
 __host__ __device__ constexpr int partial_stride(int G, int D) { return decode_partial_stride(G, D); }
 
 // The consumer warps' partial results are combined in the ring area once every ring is drained.
-__host__ __device__ constexpr int64_t decode_reduce_bytes(int D) { return (int64_t)kConsumers * 8 * (D + 2) * 4; }
+__host__ __device__ constexpr int64_t decode_reduce_bytes(int D, int NC) { return (int64_t)NC * 8 * (D + 2) * 4; }
 
 // One cache attended by a launch: its zones, its zone-C length and capacity and its plan's head
 // records and slot tables.  A launch attends one cache, or several sharing the query (segments
@@ -178,7 +182,8 @@ __device__ __forceinline__ void bulk_copy_once(void* dst, const void* src, uint3
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // the consumer warps alone (named barrier 1)
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory"); }
+template <int NC>
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NC * 32) : "memory"); }
 // atomic add of 1 with acquire-release semantics at GPU scope; returns the old value
 __device__ __forceinline__ int ticket_acq_rel(int32_t* p) {
   int old;
@@ -573,8 +578,10 @@ struct ClassVals {
   __device__ __forceinline__ int64_t operator()(int c) const { return c == 0 ? v[0] : c == 1 ? v[1] : c == 2 ? v[2] : v[3]; }
 };
 
-template <int D, bool PK>
-__global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_constant__ DecodeParams P) {
+template <int D, bool PK, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32, NC == kConsumersWide ? 1 : 2)
+    decode_kernel(const __grid_constant__ DecodeParams P) {
+  constexpr int kConsumers = NC;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = P.h_q / P.h_kv;
@@ -680,7 +687,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
   uint16_t* newrow = reinterpret_cast<uint16_t*>(st_item + kConsumers * kStages);  // [2][D] fused step: k, v
   uint32_t* kmeta_s = reinterpret_cast<uint32_t*>(newrow + 2 * D);                 // [D + kSlotPad] {scale, zero}
   float* q_s = reinterpret_cast<float*>(kmeta_s + D + kSlotPad);                   // [8][D] the group's queries
-  unsigned char* ring = smem + decode_fixed_smem(D);
+  unsigned char* ring = smem + decode_fixed_smem(D, NC);
   float* red = reinterpret_cast<float*>(ring);                                     // [consumers][8][D + 2], after the loop
 
   // items of this head: its tiles in class order, then its zone-C blocks
@@ -923,7 +930,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
     const int s_q0 = k_slots - hpp->meta_slots;   // first quantised slot
     // the group's query rows, widened to fp32 (one load per element, all in flight together)
     for (int i = tid; i < G * D; i += kConsumers * 32) q_s[i] = load_as_float(P.q, (int64_t)qbase * D + i, P.dtype);
-    consumers_sync();
+    consumers_sync<NC>();
     for (int i = tid; i < nkb * 32; i += kConsumers * 32) {
       const int kb = i >> 5, ln = i & 31, qq = ln & 3, gg = ln >> 2;
       const int seg = (kb >= seg_kb_s[1]) + (kb >= seg_kb_s[2]) + (kb >= seg_kb_s[3]);
@@ -962,23 +969,23 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
       qfragc[i] = split_hi_lo(x[0], x[1], x[2], x[3]);
     }
     // zero-point term of the quantised K channels per query head (warp h): sum_c q_hc zero_c, base 2
-    if (warp < G) {
+    for (int hq = warp; hq < 8; hq += kConsumers) {  // query head hq (0 past the group)
       float acc0 = 0.f;
-      for (int m = lane; m < hpp->meta_slots; m += 32) {
-        const int ch = slot_s[s_q0 + m];
-        if (ch >= 0) acc0 = fmaf(q_s[warp * D + ch], __half2float(__ushort_as_half((uint16_t)(kmeta_s[m] >> 16))), acc0);
-      }
+      if (hq < G)
+        for (int m = lane; m < hpp->meta_slots; m += 32) {
+          const int ch = slot_s[s_q0 + m];
+          if (ch >= 0) acc0 = fmaf(q_s[hq * D + ch], __half2float(__ushort_as_half((uint16_t)(kmeta_s[m] >> 16))), acc0);
+        }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc0 += __shfl_xor_sync(0xffffffffu, acc0, o);
-      if (lane == 0) bias_s[warp] = acc0 * sl2;
-    } else if (warp < 8 && lane == 0) {
-      bias_s[warp] = 0.f;
+      if (lane == 0) bias_s[hq] = acc0 * sl2;
     }
-    if (fused && tid < 2 * D) {
-      const int64_t src = (int64_t)head * D + (tid % D);
-      newrow[tid] = half_bits(load_as_float(tid < D ? P.k_new : P.v_new, src, P.dtype));
-    }
-    consumers_sync();
+    if (fused)
+      for (int i = tid; i < 2 * D; i += kConsumers * 32) {
+        const int64_t src = (int64_t)head * D + (i % D);
+        newrow[i] = half_bits(load_as_float(i < D ? P.k_new : P.v_new, src, P.dtype));
+      }
+    consumers_sync<NC>();
 
     // the V class whose scale acc.o carries (2, 4, 8; 16 for fp16 rows); a warp meets the classes
     // in increasing order (items ascend), so it switches at most four times
@@ -1209,8 +1216,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const __grid_
 }
 
 constexpr int64_t kDecodeSmemLimit = 227 * 1024 - 1024;  // per-block limit less room for static shared memory
+constexpr int64_t kDecodeSmemLimitNarrow = 112 * 1024;    // two blocks per SM (228 KB) with their static parts
 
 struct DecodeGeom {
+  int nc;       // consumer warps of a block (kConsumersWide, one block per SM, or kConsumersNarrow, two)
   int64_t max_item;
   int ctas;     // nominal number of blocks dealt to heads
   int splits;   // grid size: ctas + one spare block per head
@@ -1230,31 +1239,35 @@ static DecodeGeom decode_geom(const rdkv_cache* const* parts, int n, bool ragged
   const int D = s.head_dim, G = s.h_q / s.h_kv;
   const int n_heads = s.batch * s.h_kv;
   const int sms = num_sms();
-  const int64_t fixed = decode_fixed_smem(D);
+  // (head, cache) units of the launch: many of them take two narrower blocks per SM
+  const int nc = (int64_t)n_heads * n >= kManyUnits ? kConsumersNarrow : kConsumersWide;
+  const int blocks_per_sm = nc == kConsumersWide ? 1 : 2;
+  const int64_t smem_limit = nc == kConsumersWide ? kDecodeSmemLimit : kDecodeSmemLimitNarrow;
+  const int64_t fixed = decode_fixed_smem(D, nc);
+  g.nc = nc;
   int64_t max_item = 2 * kCRows * D * 2, items = 0;
   for (int p = 0; p < n; ++p) {
     max_item = std::max<int64_t>(max_item, align_up(parts[p]->sizes.max_stage_bytes, 128));
     items += ceil_div64(parts[p]->sizes.index_slots, kTile) + (int64_t)n_heads * ceil_div(parts[p]->cap_c, kCRows);
   }
   g.max_item = max_item;
-  // one block per SM; the consumer warps with a ring share what is left equally: all of them, or
-  // half (a quarter) with twice (four times) the ring when the largest staged tile needs it
-  int ring_warps = kConsumers;
-  int64_t ring = ((kDecodeSmemLimit - fixed) / ring_warps) / 128 * 128;
-  while (ring < max_item && ring_warps > kConsumers / 4) {
+  // the consumer warps with a ring share what is left equally: all of them, or half (a quarter)
+  // with twice (four times) the ring when the largest staged tile needs it
+  int ring_warps = nc;
+  int64_t ring = ((smem_limit - fixed) / ring_warps) / 128 * 128;
+  while (ring < max_item && ring_warps > std::max(1, nc / 4)) {
     ring_warps /= 2;
-    ring = ((kDecodeSmemLimit - fixed) / ring_warps) / 128 * 128;
+    ring = ((smem_limit - fixed) / ring_warps) / 128 * 128;
   }
-  const int blocks_per_sm = 1;
-  if ((int64_t)ring_warps * ring < decode_reduce_bytes(D)) ring = 0;  // the warps' results reuse the rings
+  if ((int64_t)ring_warps * ring < decode_reduce_bytes(D, nc)) ring = 0;  // the warps' results reuse the rings
   g.ring_bytes = (int)ring;
   g.ring_warps = ring_warps;
   g.smem = (size_t)(fixed + (int64_t)ring_warps * ring);
   // blocks dealt to heads in proportion to their work: a nominal count that fills every SM once,
-  // fewer when there is little work (at least kConsumers items per block on average).  Every SM
+  // fewer when there is little work (at least one item per consumer warp on average).  Every SM
   // takes work: leaving one per head free for the merges measured slower (the next call's blocks
   // wait for this call to finish before they read the query anyway).
-  g.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)blocks_per_sm * sms, ceil_div64(items, kConsumers)));
+  g.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)blocks_per_sm * sms, ceil_div64(items, nc)));
   g.splits = g.ctas + n_heads * n;  // grid size: room for at least one block per (cache, head)
   g.partial_bytes = (size_t)align_up((int64_t)g.splits * partial_stride(G, D) * 4, 256);
   g.ticket_off = g.partial_bytes;
@@ -1400,25 +1413,30 @@ static rdkv_status launch_decode(const DecodeParams& P, const DecodeGeom& geo, c
                                  bool pdl) {
   // the dynamic shared-memory limit is raised once per device and kernel (not while a graph is
   // captured); threads that get here together may both raise it, to the same value
-  static std::atomic<size_t> smem_set[4][64];
+  static std::atomic<size_t> smem_set[8][64];
   int dev = 0;
   RDKV_TRY_CUDA(cudaGetDevice(&dev), "device");
   // at most 4 query heads per KV head: the hi and lo parts of the K operand share one MMA per block
   const bool pk = s.h_q / s.h_kv <= 4;
-  const int ki = (s.head_dim == 128 ? 2 : 0) + (pk ? 1 : 0);
-  void (*const fn)(DecodeParams) = ki == 3 ? decode_kernel<128, true>
-                                 : ki == 2 ? decode_kernel<128, false>
-                                 : ki == 1 ? decode_kernel<64, true>
-                                           : decode_kernel<64, false>;
+  const bool wide = geo.nc == kConsumersWide;
+  const int ki = (s.head_dim == 128 ? 2 : 0) + (pk ? 1 : 0) + (wide ? 4 : 0);
+  void (*const fn)(DecodeParams) = ki == 7 ? decode_kernel<128, true, kConsumersWide>
+                                 : ki == 6 ? decode_kernel<128, false, kConsumersWide>
+                                 : ki == 5 ? decode_kernel<64, true, kConsumersWide>
+                                 : ki == 4 ? decode_kernel<64, false, kConsumersWide>
+                                 : ki == 3 ? decode_kernel<128, true, kConsumersNarrow>
+                                 : ki == 2 ? decode_kernel<128, false, kConsumersNarrow>
+                                 : ki == 1 ? decode_kernel<64, true, kConsumersNarrow>
+                                           : decode_kernel<64, false, kConsumersNarrow>;
+  const int64_t limit = wide ? kDecodeSmemLimit : kDecodeSmemLimitNarrow;
   if (dev < 64 && geo.smem > smem_set[ki][dev].load(std::memory_order_acquire)) {
-    RDKV_TRY_CUDA(cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kDecodeSmemLimit),
+    RDKV_TRY_CUDA(cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit),
                   "decode smem");
-    smem_set[ki][dev].store((size_t)kDecodeSmemLimit, std::memory_order_release);
+    smem_set[ki][dev].store((size_t)limit, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(geo.splits);
-  cfg.blockDim = dim3(kDecWarps * 32);
+  cfg.blockDim = dim3((geo.nc + 1) * 32);
   cfg.dynamicSmemBytes = geo.smem;
   cfg.stream = cs;
   cudaLaunchAttribute attr[1];

@@ -30,6 +30,11 @@ CASES = {
     "g2_f32": synth.WORKLOADS["tiny"].scaled(n_tokens=700, h_q=4, h_kv=2, window=20),
     "g8_f32": synth.WORKLOADS["llama3b"].scaled(dtype="f32", n_tokens=600, h_q=16, h_kv=2, window=24, batch=1,
                                                  decode_steps=4),
+    # 32 (sequence, KV head) pairs: the decode's two-blocks-per-SM layout
+    "many_g8_d128": synth.WORKLOADS["llama3b"].scaled(n_tokens=400, h_q=32, h_kv=4, window=16, batch=8,
+                                                      decode_steps=3),
+    "many_g4_d64_f32": synth.WORKLOADS["tiny"].scaled(n_tokens=300, h_q=16, h_kv=4, window=16, batch=8),
+    "many_g8_d64": synth.WORKLOADS["tiny"].scaled(dtype="f16", n_tokens=350, h_q=32, h_kv=4, window=16, batch=8),
 }
 
 

@@ -768,9 +768,69 @@ def run_graph_compress(w, shape, layer_inputs, avg, cap_c, dev, reps=3):
     b.record()
     torch.cuda.synchronize()
     exact = comp.finish()
-    return {"ms_per_layer": round(a.elapsed_time(b) / reps, 3),
-            "zone_a_bytes_bound": int(comp.bounds.zone_a_bytes), "zone_a_bytes": int(exact.sizes.zone_a_bytes),
-            "note": "score + allocate + pack from one CUDA graph, zones sized by rdkv_zone_bounds"}
+    res = {"ms_per_layer": round(a.elapsed_time(b) / reps, 3),
+           "zone_a_bytes_bound": int(comp.bounds.zone_a_bytes), "zone_a_bytes": int(exact.sizes.zone_a_bytes),
+           "note": "score + allocate + pack from one CUDA graph, zones sized by rdkv_zone_bounds"}
+    res["allocate_pack"] = run_allocate_pack_compare(shape, comp, q, k, v, avg, cap_c, dev)
+    return res
+
+
+def run_allocate_pack_compare(shape, comp, q, k, v, avg, cap_c, dev, reps=5):
+    """Allocation and pack of one layer (the scorer's outputs already in place), each way captured in
+    a CUDA graph and replayed: the allocation's and the pack's own kernels (rdkv_allocate, rdkv_pack
+    into zones sized by rdkv_zone_bounds) against the one persistent launch (rdkv_allocate_pack).
+    Both ways leave byte-identical zones (checked here on zone A)."""
+    import ctypes
+    import torch
+    from mixed_bit_kv_gb300 import rdkv
+    L = rdkv.lib()
+    so = comp.score_out
+    step_out = {key: torch.empty_like(t) for key, t in comp.alloc_out.items()}
+    step_ws = rdkv._ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), dev)
+    step_cache = rdkv.Cache(shape, step_out["plan"], comp.bounds, cap_c, dev)
+    one_out = {key: torch.empty_like(t) for key, t in comp.alloc_out.items()}
+    one_ws = rdkv._ws(L.rdkv_allocate_pack_workspace_bytes(ctypes.byref(shape), 0), dev)
+    one_cache = rdkv.Cache(shape, one_out["plan"], comp.bounds, cap_c, dev)
+
+    def step_by_step():
+        rdkv.rdkv_allocate(shape, so["g_tok"], so["w_chan"], k, avg, avg, out=step_out, ws=step_ws)
+        step_cache.c.sizes = comp.bounds
+        rdkv._check(L.rdkv_pack(ctypes.byref(step_cache.c), rdkv._ptr(k), rdkv._ptr(v), rdkv._ptr(step_out["bits_tok"]),
+                                rdkv._ptr(step_out["bits_chan"]), rdkv._stream()))
+
+    def one_launch():
+        rdkv.rdkv_allocate_pack(shape, so["g_tok"], so["w_chan"], k, v, avg, avg, cap_c, out=one_out, ws=one_ws,
+                                cache=one_cache)
+
+    def graph_ms(fn):
+        n0 = L.rdkv_launch_count()
+        fn()
+        torch.cuda.synchronize()
+        launches = int(L.rdkv_launch_count() - n0)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        return median(times), launches
+
+    step_ms, step_n = graph_ms(step_by_step)
+    one_ms, one_n = graph_ms(one_launch)
+    n = int(rdkv.rdkv_plan_sizes(one_out["plan"]).zone_a_bytes)
+    same = bool(torch.equal(step_cache.zone_a[:n], one_cache.zone_a[:n])
+                and torch.equal(step_out["plan"], one_out["plan"]))
+    return {"step_by_step_ms": round(step_ms, 4), "step_by_step_launches": step_n,
+            "one_launch_ms": round(one_ms, 4), "one_launch_launches": one_n, "identical_zone_a_and_plan": same,
+            "note": "allocation + pack of one layer from CUDA graphs (median of 5 replays): the stage kernels "
+                    "against one cooperative persistent kernel"}
 
 
 def run_e2e(args, w, shape, L, S, avg, cap_c, pre, dq, dk, dv, dec_bytes, ws, dev):

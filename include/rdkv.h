@@ -293,6 +293,44 @@ rdkv_status rdkv_zone_bounds(const rdkv_shape* shape, float avg_bits_v, float av
 rdkv_status rdkv_pack(rdkv_cache* cache, const void* k, const void* v,
                       const uint8_t* bits_tok, const uint8_t* bits_chan, void* stream);
 
+/* ---------------------------------------------------------------- allocation and pack in one launch
+ * RDKV section 2.2 steps 2 and 3, then section 2.3, as ONE persistent
+ * (cooperative) kernel whose phases are separated by grid-wide barriers: the
+ * V water level and widths, the K channel spreads over the kept tokens, the K
+ * water level and widths, the plan, the index map, the head K metadata, the
+ * zone-A tiles and zone-B rows, the zone-C window and *len_dev = W.  Every
+ * output (bits_tok, sigma_chan, g_chan, bits_chan, the plan with its levels
+ * and channel statistics, zones A and B, the index map, zone C rows [0, W))
+ * is byte-identical to rdkv_allocate (per_head = 0; rdkv_allocate_mode with
+ * RDKV_ALLOC_PER_HEAD for per_head = 1) followed by rdkv_pack.
+ *
+ * cache: as for rdkv_pack, except that cache->plan is the plan buffer this
+ *   call WRITES (rdkv_plan_bytes(shape) bytes) and cache->sizes holds the
+ *   zones' capacities (zone_a_bytes, zone_b_rows, index_slots; normally
+ *   rdkv_zone_bounds for these budgets).  The exact totals (and the head
+ *   costs the decode deals its blocks by) come afterwards from
+ *   rdkv_plan_sizes; the call itself does not synchronise, so it can be
+ *   captured in a CUDA graph.  Sets cache->len_c = W.
+ * g_tok, w_chan: rdkv_score's outputs; k, v: the prefill [B][N][H_kv][D],
+ *   16-byte aligned.  Outputs as for rdkv_allocate.
+ * ws: rdkv_allocate_pack_workspace_bytes(shape, per_head) bytes of device
+ *   memory (the call clears the part it needs cleared, asynchronously on
+ *   `stream`).
+ * Errors: the host checks of rdkv_allocate and rdkv_pack (nothing launched);
+ *   RDKV_ERR_UNSUPPORTED when fewer blocks stay resident than there are
+ *   water-filling instances.  Device-side outcomes land in the plan status
+ *   (read by rdkv_plan_sizes): RDKV_ERR_INVALID_ARG for an invalid gain (the
+ *   pack still runs, as rdkv_pack would), RDKV_ERR_CAPACITY when the plan
+ *   needs more than a capacity (then nothing is packed), RDKV_ERR_TIMEOUT when
+ *   a grid barrier waited past its bound (about two seconds; the outputs are
+ *   then not valid). */
+size_t rdkv_allocate_pack_workspace_bytes(const rdkv_shape* shape, int32_t per_head);
+rdkv_status rdkv_allocate_pack(rdkv_cache* cache, int32_t per_head, const float* g_tok,
+                               const float* w_chan, const void* k, const void* v,
+                               float avg_bits_v, float avg_bits_k, uint8_t* bits_tok,
+                               float* sigma_chan, float* g_chan, uint8_t* bits_chan,
+                               void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- append
  * RDKV section 2.3 zone C: writes the new token's k_new, v_new [B][H_kv][D]
  * (shape->dtype) as fp16 rows at row *len_dev of zone C and advances *len_dev

@@ -18,22 +18,9 @@
 #include <algorithm>
 #include <cmath>
 
-#include "common.cuh"
+#include "stages.cuh"
 
 namespace rdkv {
-
-// Distortion drop per bit of each upgrade 0->2, 2->4, 4->8, 8->16, exact in fp32.
-constexpr float kRdkvSlopes[4] = {0.375f, 0.09375f, 0.0146484375f, 255.0f / 524288.0f};
-// All four breakpoints at the gain itself: a unit goes from 0 straight to 16 bits once its gain
-// passes the level (the keep-or-drop selection of the eviction baselines).
-constexpr float kKeepSlopes[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-
-struct Slopes {
-  float s[4];
-};
-static Slopes slopes_of(const float (&a)[4]) { return Slopes{{a[0], a[1], a[2], a[3]}}; }
-__constant__ uint32_t kStepBits[4] = {2, 2, 4, 8};
-__constant__ uint8_t kWidth[5] = {0, 2, 4, 8, 16};
 
 struct WfState {
   unsigned long long above;  // bits bought strictly above the fixed prefix range
@@ -51,61 +38,26 @@ __global__ void wf_init(WfState* st, unsigned long long* hist, int n_inst, int32
   if (blockIdx.x == 0 && threadIdx.x == 0 && status) *status = RDKV_OK;
 }
 
-__device__ __forceinline__ bool gain_valid(float g) { return g >= 0.0f && g <= 3.402823466e38f; }
-
 // g of instance i starts at g + i * in_stride (units contiguous).
 __global__ void wf_hist(const float* __restrict__ g, int64_t n_units, int64_t in_stride, Slopes sl, int level,
                         const WfState* __restrict__ st, unsigned long long* __restrict__ hist, int32_t* status) {
   __shared__ uint32_t h[256];
   const int inst = blockIdx.y;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
-  __syncthreads();
-  const uint32_t prefix = st[inst].prefix;
-  const int shift = 24 - 8 * level;
-  const float* gi = g + (int64_t)inst * in_stride;
-  bool bad = false;
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)gridDim.x * blockDim.x) {
-    const float gv = gi[u];
-    if (!gain_valid(gv)) {
-      bad = true;
-      continue;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t p = level_bits(gv * sl.s[k]);
-      if (level == 0 || (p >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&h[(p >> shift) & 255u], kStepBits[k]);
-    }
-  }
-  if (bad && level == 0 && status) atomicExch(status, (int32_t)RDKV_ERR_INVALID_ARG);
-  __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x)
-    if (h[i]) atomicAdd(&hist[inst * 256 + i], (unsigned long long)h[i]);
+  wf_hist_part(g + (int64_t)inst * in_stride, n_units, sl, level, st[inst].prefix, blockIdx.x, gridDim.x, h,
+               hist + inst * 256, status);
 }
 
 // One block of 256 threads per instance: digit d is kept if the bits bought
 // above x_d = prefix | d << shift | (lower bits all ones) fit the budget.
 __global__ void wf_select(int level, long long budget, WfState* st, unsigned long long* hist) {
-  __shared__ unsigned long long s[256];
+  __shared__ unsigned long long s[257];
   __shared__ int best;
   const int inst = blockIdx.x, t = threadIdx.x;
-  const unsigned long long v = hist[inst * 256 + t];
-  s[255 - t] = v;  // reversed so that an inclusive scan gives sums over d' >= t
-  if (t == 0) best = 255;
-  __syncthreads();
-  for (int off = 1; off < 256; off <<= 1) {
-    unsigned long long x = (255 - t >= off) ? s[255 - t - off] : 0ull;
-    __syncthreads();
-    s[255 - t] += x;
-    __syncthreads();
-  }
-  const unsigned long long tail = s[255 - t] - v;  // sum over d' > t
-  const unsigned long long above = st[inst].above;
-  if (above + tail <= (unsigned long long)budget) atomicMin(&best, t);
-  __syncthreads();
-  const int d = best;
-  if (t == d) {
-    st[inst].prefix |= (uint32_t)d << (24 - 8 * level);
-    st[inst].above = above + tail;
+  const WfPick cur{st[inst].prefix, st[inst].above};
+  const WfPick nxt = wf_pick(hist[inst * 256 + t], level, budget, cur, s, &best);
+  if (t == 0) {
+    st[inst].prefix = nxt.prefix;
+    st[inst].above = nxt.above;
   }
   hist[inst * 256 + t] = 0;
 }
@@ -115,17 +67,7 @@ __global__ void wf_assign(const float* __restrict__ g, int64_t n_units, int64_t 
   const int inst = blockIdx.y;
   const uint32_t lam = st[inst].prefix;
   if (lambda_out && blockIdx.x == 0 && threadIdx.x == 0) lambda_out[inst] = __uint_as_float(lam);
-  const float* gi = g + (int64_t)inst * in_stride;
-  uint8_t* bi = bits + (int64_t)inst * n_units;
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)gridDim.x * blockDim.x) {
-    const float gv = gi[u];
-    int m = 0;
-    if (gain_valid(gv)) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) m += level_bits(gv * sl.s[k]) > lam ? 1 : 0;
-    }
-    bi[u] = kWidth[m];
-  }
+  wf_assign_part(g + (int64_t)inst * in_stride, n_units, sl, lam, blockIdx.x, gridDim.x, bits + (int64_t)inst * n_units);
 }
 
 // One level per instance; instance i's n_units gains start at g + i * in_stride (in_stride = n_units
@@ -190,7 +132,7 @@ __global__ void assign_at_level_kernel(const float* __restrict__ g, int64_t n_un
     } else {
       bad = true;
     }
-    bi[u] = kWidth[m];
+    bi[u] = width_after(m);
   }
   if (bad && status) atomicExch(status, (int32_t)RDKV_ERR_INVALID_ARG);
 }
@@ -204,152 +146,36 @@ __global__ void fill_u8_kernel(uint8_t* __restrict__ p, int64_t n, uint8_t v) {
 }
 
 // ---------------------------------------------------------------- K channel spread over kept tokens
-// sigma_c (population std of K[kept tokens, j, c]) in two passes: chunk sums
-// in fp32, combined in fp64 in a fixed order; then sums of squared deviations.
-constexpr int kChanChunk = 256;
-
-// Elements [c0, c0 + n) (n = 2 or 4, c0 a multiple of n) of one row as floats, one vector load.
-__device__ __forceinline__ void load_run(const void* p, int64_t i, int dtype, int n, float (&x)[4]) {
-  if (dtype == RDKV_F16) {
-    const __half* h = static_cast<const __half*>(p) + i;
-    if (n == 4) {
-      const uint2 u = *reinterpret_cast<const uint2*>(h);
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-      x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-    } else {
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(h));
-      x[0] = a.x; x[1] = a.y; x[2] = x[3] = 0.f;
-    }
-  } else {
-    const float* f = static_cast<const float*>(p) + i;
-    if (n == 4) {
-      const float4 a = *reinterpret_cast<const float4*>(f);
-      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    } else {
-      const float2 a = *reinterpret_cast<const float2*>(f);
-      x[0] = a.x; x[1] = a.y; x[2] = x[3] = 0.f;
-    }
-  }
-}
-
-// Block (chunk, head), 256 threads: lane l takes channels [l D/32, (l+1) D/32) of every token (one
-// vector load; a warp reads whole rows), warp w the chunk's tokens t0 + w, t0 + w + 8, ... in order;
-// the eight warps' sums are added in warp order (deterministic).  The first pass (no mean) also
-// takes each channel's minimum and maximum over the kept tokens (pmin, pmax): the K quantiser's
-// group of a channel is its head's kept tokens.
-constexpr int kChanWarps = 8;
+// Block (chunk, head): one chunk item of a channel pass (stages.cuh).
 __global__ void __launch_bounds__(32 * kChanWarps) chan_pass(const void* __restrict__ k,
                                                              const uint8_t* __restrict__ bits_tok, int dtype, int N,
                                                              int h_kv, int D, int Np, const float* __restrict__ mean,
                                                              float* __restrict__ part, int* __restrict__ part_cnt,
                                                              float* __restrict__ pmin, float* __restrict__ pmax) {
-  __shared__ float wsum[kChanWarps][128];
-  __shared__ float wmin[kChanWarps][128], wmax[kChanWarps][128];
-  __shared__ int wcnt[kChanWarps];
-  const int head = blockIdx.y;  // b * h_kv + j
-  const int b = head / h_kv, j = head % h_kv;
-  const int chunk = blockIdx.x, nchunk = gridDim.x;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int cpl = D / 32, c0 = lane * cpl;
-  const int t0 = chunk * kChanChunk, t1 = min(Np, t0 + kChanChunk);
-  const uint8_t* bt = bits_tok + (int64_t)head * Np;
-  float m[4] = {0.f, 0.f, 0.f, 0.f};
-  if (mean)
-    for (int i = 0; i < cpl; ++i) m[i] = mean[head * D + c0 + i];
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float mn[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  int cnt = 0;
-  const int64_t row = (int64_t)h_kv * D;
-  const int64_t base = (((int64_t)b * N) * h_kv + j) * D + c0;
-#pragma unroll 4
-  for (int t = t0 + w; t < t1; t += kChanWarps) {
-    const bool keep = bt[t] != 0;
-    float x[4];
-    load_run(k, base + (int64_t)t * row, dtype, cpl, x);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float d = x[i] - m[i];
-      acc[i] += keep ? (mean ? d * d : x[i]) : 0.0f;
-      mn[i] = keep ? fminf(mn[i], x[i]) : mn[i];
-      mx[i] = keep ? fmaxf(mx[i], x[i]) : mx[i];
-    }
-    cnt += keep ? 1 : 0;
-  }
-  for (int i = 0; i < cpl; ++i) {
-    wsum[w][c0 + i] = acc[i];
-    wmin[w][c0 + i] = mn[i];
-    wmax[w][c0 + i] = mx[i];
-  }
-  if (lane == 0) wcnt[w] = cnt;
-  __syncthreads();
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float s = 0.0f, lo = INFINITY, hi = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < kChanWarps; ++q) {
-      s += wsum[q][c];
-      lo = fminf(lo, wmin[q][c]);
-      hi = fmaxf(hi, wmax[q][c]);
-    }
-    part[((int64_t)head * nchunk + chunk) * D + c] = s;
-    if (pmin) {
-      pmin[((int64_t)head * nchunk + chunk) * D + c] = lo;
-      pmax[((int64_t)head * nchunk + chunk) * D + c] = hi;
-    }
-  }
-  if (threadIdx.x == 0 && part_cnt) {
-    int n = 0;
-    for (int q = 0; q < kChanWarps; ++q) n += wcnt[q];
-    part_cnt[head * nchunk + chunk] = n;
-  }
+  __shared__ ChanSmem sm;
+  chan_pass_item(blockIdx.x, gridDim.x, blockIdx.y, k, bits_tok, dtype, N, h_kv, D, Np, mean, part, part_cnt, pmin,
+                 pmax, sm);
 }
 
-// The first call (mean_out set) also combines the chunks' minima and maxima into the head's K
-// channel statistics kstat [head][c] = {min, max} over the kept tokens ({0, 0} when none is kept).
-__global__ void chan_finish(const float* __restrict__ part, const int* __restrict__ part_cnt, int nchunk, int D,
-                            float* __restrict__ mean_out, const float* __restrict__ w_chan,
-                            float* __restrict__ sigma_out, float* __restrict__ g_out, const float* __restrict__ pmin,
-                            const float* __restrict__ pmax, float2* __restrict__ kstat) {
-  // thread (r, c) sums the chunks r, r + R, r + 2R, ... of channel c; the R sums are combined in a
-  // fixed order (deterministic)
-  __shared__ double ssum[1024];
-  __shared__ long long scnt[1024];
-  __shared__ float smin[1024], smax[1024];
-  const int head = blockIdx.x, c = threadIdx.x % D, r = threadIdx.x / D, R = blockDim.x / D;
-  double s = 0.0;
-  long long n = 0;
-  float lo = INFINITY, hi = -INFINITY;
-  for (int i = r; i < nchunk; i += R) {
-    s += (double)part[((int64_t)head * nchunk + i) * D + c];
-    n += part_cnt[head * nchunk + i];
-    if (kstat) {
-      lo = fminf(lo, pmin[((int64_t)head * nchunk + i) * D + c]);
-      hi = fmaxf(hi, pmax[((int64_t)head * nchunk + i) * D + c]);
-    }
-  }
-  ssum[threadIdx.x] = s;
-  scnt[threadIdx.x] = n;
-  smin[threadIdx.x] = lo;
-  smax[threadIdx.x] = hi;
-  __syncthreads();
-  if (r != 0) return;
-  for (int rr = 1; rr < R; ++rr) {
-    s += ssum[rr * D + c];
-    n += scnt[rr * D + c];
-    lo = fminf(lo, smin[rr * D + c]);
-    hi = fmaxf(hi, smax[rr * D + c]);
-  }
-  if (kstat) kstat[head * D + c] = n ? make_float2(lo, hi) : make_float2(0.f, 0.f);
-  if (mean_out) {
-    mean_out[head * D + c] = n ? (float)(s / (double)n) : 0.0f;
-  } else {
-    const float sig = n ? (float)sqrt(s / (double)n) : 0.0f;
-    sigma_out[head * D + c] = sig;
-    g_out[head * D + c] = w_chan[head * D + c] * sig;
-  }
+// Block (head, 32-channel slice), 256 threads: the chunk combine (stages.cuh).  The first call
+// (mean_out set) also writes the head's K channel statistics kstat.
+__global__ void __launch_bounds__(32 * kChanRows) chan_finish(const float* __restrict__ part,
+                                                              const int* __restrict__ part_cnt, int nchunk, int D,
+                                                              float* __restrict__ mean_out,
+                                                              const float* __restrict__ w_chan,
+                                                              float* __restrict__ sigma_out, float* __restrict__ g_out,
+                                                              const float* __restrict__ pmin,
+                                                              const float* __restrict__ pmax,
+                                                              float2* __restrict__ kstat) {
+  __shared__ ChanFinishSmem sm;
+  const int slices = D / 32;
+  chan_finish_item(blockIdx.x / slices, blockIdx.x % slices, part, part_cnt, nchunk, D, mean_out, w_chan, sigma_out,
+                   g_out, pmin, pmax, kstat, sm);
 }
 
 // ---------------------------------------------------------------- plan
+// One block (256 threads) per head: V class counts of its tokens and K class counts of its
+// channels, the head record, then the slot table.
 __global__ void plan_heads_kernel(const uint8_t* __restrict__ bits_tok, const uint8_t* __restrict__ bits_chan, int Np,
                                   int D, char* plan, int64_t heads_off, int64_t slots_off, int slot_stride) {
   const int head = blockIdx.x;
@@ -364,118 +190,24 @@ __global__ void plan_heads_kernel(const uint8_t* __restrict__ bits_tok, const ui
   for (int c = threadIdx.x; c < D; c += blockDim.x) bcs[c] = bc[c];
   __syncthreads();
   int cnt[4] = {0, 0, 0, 0};
-  auto count = [&](uint32_t b) {
-    cnt[0] += b == 2;
-    cnt[1] += b == 4;
-    cnt[2] += b == 8;
-    cnt[3] += b == 16;
-  };
-  const uint8_t* bt = bits_tok + (int64_t)head * Np;
-  // widths of the head's tokens, sixteen per load once the row is 16-byte aligned (independent loads,
-  // all in flight together); the counts do not depend on the order
-  const int lead = min(Np, (int)((16 - ((uintptr_t)bt & 15)) & 15));
-  for (int t = threadIdx.x; t < lead; t += blockDim.x) count(bt[t]);
-  const int n16 = (Np - lead) / 16;
-  const uint4* bt16 = reinterpret_cast<const uint4*>(bt + lead);
-  for (int i = threadIdx.x; i < n16; i += blockDim.x) {
-    const uint4 w = bt16[i];
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) count((ws[q] >> (8 * e)) & 255u);
-  }
-  for (int t = lead + 16 * n16 + threadIdx.x; t < Np; t += blockDim.x) count(bt[t]);
+  count_classes(bits_tok + (int64_t)head * Np, 0, Np, blockDim.x, threadIdx.x, cnt);
 #pragma unroll
   for (int i = 0; i < 4; ++i) atomicAdd(&nv[i], cnt[i]);
-  auto kclass = [](int b) { return b == 16 ? 0 : b == 8 ? 1 : b == 4 ? 2 : b == 2 ? 3 : 4; };
-  for (int c = threadIdx.x; c < D; c += blockDim.x) atomicAdd(&nk[kclass(bcs[c])], 1);
+  plan_count_k(bcs, D, nk);
   __syncthreads();
   if (threadIdx.x == 0) {
-    // K segments of widths 16, 8, 4, 2: whole words per token, slot ranges of whole k-blocks
-    rdkv_head_plan hp;
-    int words_total = 0, slots_total = 0, meta = 0;
-    for (int i = 0; i < 4; ++i) {
-      const int b = 16 >> i;
-      hp.k_words[i] = ceil_div(nk[i] * b, 32);
-      const int blocks = ceil_div(hp.k_words[i] * (32 / b), kKB);
-      seg_base[i] = slots_total;
-      words_total += hp.k_words[i];
-      slots_total += kKB * blocks;
-      if (b < 16) meta += kKB * blocks;
-    }
-    for (int i = 0; i < 5; ++i) hp.n_k[i] = nk[i];
-    hp.row_words = words_total;
-    hp.k_slots = slots_total;
-    hp.meta_slots = meta;
-    int64_t a = head_meta_bytes(meta);
-    for (int i = 0; i < 4; ++i) {
-      hp.n_v[i] = nv[i];
-      hp.tiles[i] = ceil_div(nv[i], kTile);
-      hp.tile_bytes[i] = tile_bytes_of(words_total, D, 2 << i);  // V widths 2, 4, 8, 16
-      a += (int64_t)hp.tiles[i] * hp.tile_bytes[i];
-    }
-    hp.a_bytes = a;
-    hp.a_off = hp.b_row = hp.slot_off = 0;
-    reinterpret_cast<rdkv_head_plan*>(plan + heads_off)[head] = hp;
+    const int v4[4] = {nv[0], nv[1], nv[2], nv[3]}, k5[5] = {nk[0], nk[1], nk[2], nk[3], nk[4]};
+    reinterpret_cast<rdkv_head_plan*>(plan + heads_off)[head] = make_head_record(v4, k5, D, seg_base);
   }
   __syncthreads();
-  // the channel of rank r in its segment: element r mod (32/b) of word r div (32/b), in the k-block
-  // of that word at the slot k_slot_in_block gives
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    const int cls = kclass(bcs[c]);
-    if (cls == 4) continue;
-    int rank = 0;
-    for (int c2 = 0; c2 < c; ++c2) rank += kclass(bcs[c2]) == cls;
-    const int b = 16 >> cls, per = 32 / b, wpk = b / 2;
-    const int wg = rank / per, e = rank % per;
-    slots[seg_base[cls] + kKB * (wg / wpk) + k_slot_in_block(b, wg % wpk, e)] = (int16_t)c;
-  }
+  plan_slot_table(bcs, D, seg_base, slots);
 }
 
 __global__ void plan_offsets_kernel(char* plan, int batch, int h_kv, int D, int slot_stride, int64_t heads_off,
                                     int64_t slots_off, int64_t lambda_off, const int32_t* status_v,
                                     const int32_t* status_k) {
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  auto* hdr = reinterpret_cast<rdkv_plan_header*>(plan);
-  auto* heads = reinterpret_cast<rdkv_head_plan*>(plan + heads_off);
-  const int n_heads = batch * h_kv;
-  int64_t a = 0, brow = 0, slot = 0, kept = 0, maxt = 0, maxs = 0;
-  for (int i = 0; i < n_heads; ++i) {
-    rdkv_head_plan& hp = heads[i];
-    hp.a_off = a;
-    hp.b_row = brow;
-    hp.slot_off = slot;
-    a += hp.a_bytes;
-    brow += (int64_t)kTile * hp.tiles[3];
-    int nt = 0;
-    for (int c = 0; c < 4; ++c) {
-      nt += hp.tiles[c];
-      kept += hp.n_v[c];
-      if (hp.tiles[c] && hp.tile_bytes[c] > maxt) maxt = hp.tile_bytes[c];
-      const int64_t stage = hp.tile_bytes[c] + (c == 3 ? (int64_t)kTile * D * 2 : 0);
-      if (hp.tiles[c] && stage > maxs) maxs = stage;
-    }
-    slot += (int64_t)kTile * nt;
-  }
-  int32_t s = RDKV_OK;
-  if (*status_v != RDKV_OK) s = *status_v;
-  if (*status_k != RDKV_OK) s = *status_k;
-  hdr->status = s;
-  hdr->n_heads = n_heads;
-  hdr->batch = batch;
-  hdr->h_kv = h_kv;
-  hdr->head_dim = D;
-  hdr->slot_stride = slot_stride;
-  hdr->heads_off = heads_off;
-  hdr->slots_off = slots_off;
-  hdr->lambda_off = lambda_off;
-  hdr->zone_a_bytes = a;
-  hdr->zone_b_rows = brow;
-  hdr->index_slots = slot;
-  hdr->kept_tokens = kept;
-  hdr->max_tile_bytes = maxt;
-  hdr->max_stage_bytes = maxs;
+  plan_offsets_body(plan, batch, h_kv, D, slot_stride, heads_off, slots_off, lambda_off, *status_v, *status_k);
 }
 
 // ---------------------------------------------------------------- shape checks shared with the other calls
@@ -617,14 +349,14 @@ static rdkv_status allocate_impl(const rdkv_shape* s, int mode, float param, con
     chan_pass<<<dim3(nchunk, n_heads), 32 * kChanWarps, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np,
                                                                  nullptr, part, pcnt, pmin, pmax);
     RDKV_CHECK_LAUNCH("channel sums");
-    chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, mean, nullptr, nullptr, nullptr,
-                                                           pmin, pmax, kstat);
+    chan_finish<<<n_heads * (D / 32), 32 * kChanRows, 0, cs>>>(part, pcnt, nchunk, D, mean, nullptr, nullptr,
+                                                               nullptr, pmin, pmax, kstat);
     RDKV_CHECK_LAUNCH("channel means");
     chan_pass<<<dim3(nchunk, n_heads), 32 * kChanWarps, 0, cs>>>(k, bits_tok, s->dtype, s->n_tokens, s->h_kv, D, Np,
                                                                  mean, part, nullptr, nullptr, nullptr);
     RDKV_CHECK_LAUNCH("channel deviations");
-    chan_finish<<<n_heads, std::min(1024, 8 * D), 0, cs>>>(part, pcnt, nchunk, D, nullptr, w_chan, sigma_chan, g_chan,
-                                                           nullptr, nullptr, nullptr);
+    chan_finish<<<n_heads * (D / 32), 32 * kChanRows, 0, cs>>>(part, pcnt, nchunk, D, nullptr, w_chan, sigma_chan,
+                                                               g_chan, nullptr, nullptr, nullptr);
     RDKV_CHECK_LAUNCH("channel spread");
   } else {
     RDKV_TRY_CUDA(cudaMemsetAsync(sigma_chan, 0, 4 * (size_t)n_heads * D, cs), "sigma reset");

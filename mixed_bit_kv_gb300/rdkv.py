@@ -31,6 +31,7 @@ EXPORTED = (
     "rdkv_allocate_at_levels", "rdkv_decode_multi_workspace_bytes", "rdkv_decode_attn_multi",
     "rdkv_decode_multi_status", "rdkv_zone_bounds", "rdkv_decode_timeout_selftest", "rdkv_workspace_bytes",
     "rdkv_decode_ragged_workspace_bytes", "rdkv_decode_ragged", "rdkv_decode_ragged_status",
+    "rdkv_allocate_pack_workspace_bytes", "rdkv_allocate_pack",
 )
 RDKV_CALL_SCORE, RDKV_CALL_ALLOCATE, RDKV_CALL_DECODE = 0, 1, 2
 
@@ -128,6 +129,9 @@ def lib():
             "rdkv_decode_ragged_workspace_bytes": (ctypes.c_size_t, [_P, ctypes.c_int32]),
             "rdkv_decode_ragged": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "rdkv_decode_ragged_status": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P]),
+            "rdkv_allocate_pack_workspace_bytes": (ctypes.c_size_t, [sp, ctypes.c_int32]),
+            "rdkv_allocate_pack": (ctypes.c_int, [cp, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_float, ctypes.c_float,
+                                                  _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -396,6 +400,40 @@ def rdkv_pack(shape, plan, k, v, bits_tok, bits_chan, cap_c, stream=None, sizes=
     return cache
 
 
+def rdkv_allocate_pack(shape, g_tok, w_chan, k, v, avg_bits_v, avg_bits_k, cap_c, per_head=False, stream=None,
+                       out=None, ws=None, cache=None, pages=None):
+    """Allocation and pack in one launch.  The zones are sized from rdkv_zone_bounds (a new Cache unless
+    `cache`, built on those bounds, is given); the plan buffer is out["plan"].  Returns (out, cache):
+    call ``finish_sizes`` (synchronising) before the decode so that the cache carries the exact
+    totals."""
+    dev = k.device
+    B, Hkv, D = shape.batch, shape.h_kv, shape.head_dim
+    Np = shape.n_tokens - shape.window
+    L = lib()
+    if out is None:
+        out = dict(bits_tok=torch.empty(B, Hkv, max(Np, 0), dtype=torch.uint8, device=dev),
+                   sigma_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+                   g_chan=torch.empty(B, Hkv, D, dtype=torch.float32, device=dev),
+                   bits_chan=torch.empty(B, Hkv, D, dtype=torch.uint8, device=dev),
+                   plan=torch.zeros(L.rdkv_plan_bytes(ctypes.byref(shape)), dtype=torch.uint8, device=dev))
+    if ws is None:
+        ws = _ws(L.rdkv_allocate_pack_workspace_bytes(ctypes.byref(shape), int(per_head)), dev)
+    if cache is None:
+        cache = Cache(shape, out["plan"], rdkv_zone_bounds(shape, avg_bits_v, avg_bits_k), cap_c, dev, pages=pages)
+    _check(L.rdkv_allocate_pack(ctypes.byref(cache.c), int(per_head), _ptr(g_tok), _ptr(w_chan), _ptr(k), _ptr(v),
+                                float(avg_bits_v), float(avg_bits_k), _ptr(out["bits_tok"]), _ptr(out["sigma_chan"]),
+                                _ptr(out["g_chan"]), _ptr(out["bits_chan"]), _ptr(ws), ws.numel(), _stream(stream)))
+    return out, cache
+
+
+def finish_sizes(cache, stream=None):
+    """Reads the plan's exact totals (synchronising) into the cache, for the decode."""
+    sizes = rdkv_plan_sizes(cache.plan, stream)
+    cache.sizes = sizes
+    cache.c.sizes = sizes
+    return cache
+
+
 def rdkv_append(cache, k_new, v_new, stream=None):
     _check(lib().rdkv_append(ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new), _stream(stream)))
 
@@ -653,8 +691,10 @@ class Compressor:
     for the device, so it can be captured in a CUDA graph; finish() reads the exact plan totals
     (synchronising) so that the decode sizes its work from them."""
 
-    def __init__(self, shape, avg_bits_v, avg_bits_k, cap_c, device, pages=None):
-        self.shape, self.avg = shape, (float(avg_bits_v), float(avg_bits_k))
+    def __init__(self, shape, avg_bits_v, avg_bits_k, cap_c, device, pages=None, fused=False):
+        """fused: allocation and pack as one persistent launch (rdkv_allocate_pack) instead of the
+        allocation's and the pack's own kernels."""
+        self.shape, self.avg, self.fused = shape, (float(avg_bits_v), float(avg_bits_k)), fused
         self.bounds = rdkv_zone_bounds(shape, avg_bits_v, avg_bits_k)
         L = lib()
         B, Hkv, D, N = shape.batch, shape.h_kv, shape.head_dim, shape.n_tokens
@@ -668,7 +708,8 @@ class Compressor:
                               bits_chan=torch.empty(B, Hkv, D, dtype=torch.uint8, device=device),
                               plan=torch.zeros(L.rdkv_plan_bytes(ctypes.byref(shape)), dtype=torch.uint8,
                                                device=device))
-        self.alloc_ws = _ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), device)
+        self.alloc_ws = _ws(L.rdkv_allocate_pack_workspace_bytes(ctypes.byref(shape), 0) if fused
+                            else L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), device)
         self.cache = Cache(shape, self.alloc_out["plan"], self.bounds, cap_c, device, pages=pages)
 
     def run(self, q, k, v, stream=None):
@@ -677,11 +718,15 @@ class Compressor:
         _check(L.rdkv_score(ctypes.byref(s), _ptr(q), _ptr(k), _ptr(v), _ptr(so["w_tok"]), _ptr(so["w_chan"]),
                             _ptr(so["sigma_tok"]), _ptr(so["g_tok"]), _ptr(self.score_ws), self.score_ws.numel(),
                             _stream(stream)))
+        self.cache.c.sizes = self.bounds
+        if self.fused:
+            rdkv_allocate_pack(s, so["g_tok"], so["w_chan"], k, v, self.avg[0], self.avg[1], self.cache.c.cap_c,
+                               stream=stream, out=ao, ws=self.alloc_ws, cache=self.cache)
+            return self.cache
         _check(L.rdkv_allocate(ctypes.byref(s), _ptr(so["g_tok"]), _ptr(so["w_chan"]), _ptr(k),
                                ctypes.c_float(self.avg[0]), ctypes.c_float(self.avg[1]), _ptr(ao["bits_tok"]),
                                _ptr(ao["sigma_chan"]), _ptr(ao["g_chan"]), _ptr(ao["bits_chan"]), _ptr(ao["plan"]),
                                _ptr(self.alloc_ws), self.alloc_ws.numel(), _stream(stream)))
-        self.cache.c.sizes = self.bounds
         _check(L.rdkv_pack(ctypes.byref(self.cache.c), _ptr(k), _ptr(v), _ptr(ao["bits_tok"]), _ptr(ao["bits_chan"]),
                            _stream(stream)))
         return self.cache

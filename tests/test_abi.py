@@ -268,3 +268,26 @@ def test_ragged_decode_argument_checks(L):
         assert L.rdkv_decode_ragged_workspace_bytes(ptr, n) == 0
         r = L.rdkv_decode_ragged(ptr, n, fake, fake, None, fake, 1 << 30, None)
         assert r == code, (n, r)
+
+
+def test_allocate_pack_argument_checks(L):
+    """The one-launch allocation and pack rejects bad arguments on the host, before any CUDA call."""
+    s = rdkv.make_shape(1, 1024, 4, 1, 64, 32, "f16")
+    need = L.rdkv_allocate_pack_workspace_bytes(ctypes.byref(s), 0)
+    assert need > 0 and L.rdkv_allocate_pack_workspace_bytes(ctypes.byref(s), 1) >= need
+    assert L.rdkv_allocate_pack_workspace_bytes(ctypes.byref(s), 2) == 0
+    sizes = rdkv.Sizes(4096, 64, 1024, 900, 2048, 2048, 0, 1)
+    fake = ctypes.c_void_p(256)
+    c = rdkv.CacheStruct(s, 256, 256, 256, 256, 256, 256, 256, 64, 0, sizes)
+    f = ctypes.c_float
+
+    def call(per_head=0, k=fake, bv=2.0, ws_bytes=need):
+        return L.rdkv_allocate_pack(ctypes.byref(c), per_head, fake, fake, k, fake, f(bv), f(2.0), fake, fake, fake,
+                                    fake, fake, ws_bytes, None)
+
+    assert call(per_head=2) == rdkv.RDKV_ERR_INVALID_ARG
+    assert call(bv=float("nan")) == rdkv.RDKV_ERR_INVALID_ARG
+    assert call(k=None) == rdkv.RDKV_ERR_INVALID_ARG
+    assert call(k=ctypes.c_void_p(264)) == rdkv.RDKV_ERR_INVALID_ARG  # not 16-byte aligned
+    assert call(ws_bytes=need - 1) == rdkv.RDKV_ERR_WORKSPACE
+    assert c.len_c == 0

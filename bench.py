@@ -785,10 +785,10 @@ def run_allocate_pack_compare(shape, comp, q, k, v, avg, cap_c, dev, reps=5):
     from mixed_bit_kv_gb300 import rdkv
     L = rdkv.lib()
     so = comp.score_out
-    step_out = {key: torch.empty_like(t) for key, t in comp.alloc_out.items()}
+    step_out = {key: torch.zeros_like(t) for key, t in comp.alloc_out.items()}
     step_ws = rdkv._ws(L.rdkv_allocate_workspace_bytes(ctypes.byref(shape)), dev)
     step_cache = rdkv.Cache(shape, step_out["plan"], comp.bounds, cap_c, dev)
-    one_out = {key: torch.empty_like(t) for key, t in comp.alloc_out.items()}
+    one_out = {key: torch.zeros_like(t) for key, t in comp.alloc_out.items()}
     one_ws = rdkv._ws(L.rdkv_allocate_pack_workspace_bytes(ctypes.byref(shape), 0), dev)
     one_cache = rdkv.Cache(shape, one_out["plan"], comp.bounds, cap_c, dev)
 

@@ -50,7 +50,7 @@ __global__ void wf_hist(const float* __restrict__ g, int64_t n_units, int64_t in
 // One block of 256 threads per instance: digit d is kept if the bits bought
 // above x_d = prefix | d << shift | (lower bits all ones) fit the budget.
 __global__ void wf_select(int level, long long budget, WfState* st, unsigned long long* hist) {
-  __shared__ unsigned long long s[257];
+  __shared__ unsigned long long s[9];
   __shared__ int best;
   const int inst = blockIdx.x, t = threadIdx.x;
   const WfPick cur{st[inst].prefix, st[inst].above};

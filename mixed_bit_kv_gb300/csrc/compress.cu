@@ -9,19 +9,22 @@
 // byte-identical to rdkv_allocate (or the per-head levels of
 // rdkv_allocate_mode) followed by rdkv_pack.
 //
-// Work inside a phase is dealt to blocks as items:
-//   water-filling  instance i gets per blocks (the same ones at every level,
-//                  so each block keeps its instance's bisection state; every
-//                  block holding an instance computes the level's digit itself
-//                  from the level's histogram, so one barrier per level);
-//   channel passes (chunk of 256 tokens, head), then (head, 32 channels);
-//   plan           one item per head (K classes, slot table) and one per
-//                  (head, chunk of 8192 tokens) counting its V classes; block 0
-//                  then builds the head records and the zone offsets while the
-//                  others copy the zone-C window;
-//   index map      (head, chunk of 8192 tokens): the chunk's tokens placed at
-//                  their class's slots after the counts of the chunks before
-//                  it; head metadata one item per head;
+// Phases (grid barriers between them, 8 on a prompt with kept tokens) and how their work is dealt:
+//   V water level  instance i gets `per` blocks (the same ones at every level, so each keeps its
+//                  instance's bisection state; every block holding an instance computes the
+//                  level's digit itself from the level's histogram, and those blocks alone wait for
+//                  one another between levels); then the V widths;
+//   channel pass 1 items (chunk of 256 tokens, head), beside the plan's V class counts, items
+//                  (head, chunk of 8192 tokens); then the chunk combine, items (head, 32
+//                  channels); pass 2 and its combine the same way;
+//   K stage        one item per head: the block runs its instance's K water-filling by itself
+//                  (histograms in shared memory), writes the head's widths, its K class counts
+//                  and its slot table;
+//   plan records   block 0 builds the head records and the zone offsets while the other blocks
+//                  copy the zone-C window;
+//   index map      items (head, chunk of 8192 tokens): the chunk's tokens placed at their class's
+//                  slots after the counts of the chunks before it; head K metadata, one item per
+//                  head;
 //   pack           one item per 32-token tile.
 #include "stages.cuh"
 
@@ -31,13 +34,23 @@ constexpr int kFusedThreads = 256;
 constexpr int kFusedBlocksPerSm = 5;   // by the tile items' shared memory (about 40 KB a block)
 constexpr int kIdxChunk = 8192;        // tokens of a counting / index item: 32 per thread
 
-// Grid barrier state (workspace, cleared before every launch).
-struct GridSync {
-  unsigned int count;  // blocks arrived at the current barrier
-  unsigned int gen;    // barriers completed
-  int abort;           // a block gave up waiting: nobody waits any more
-  unsigned int done;   // blocks finished (the last one records a timeout in the plan status)
+// Grid barrier state (workspace, cleared before every launch).  Each word has a 128-byte line of its
+// own.  A grid barrier is two-level: block b arrives on the counter of its group (b mod 32); the
+// last block of a group arrives on the top counter; the last group releases every group's flag,
+// which only that group's blocks poll (so no line holds more than a group's arrivals and polls).
+constexpr int kSyncGroups = 32;
+struct alignas(128) SyncWord {
+  unsigned int v;
 };
+struct GridSync {
+  SyncWord grp[kSyncGroups];  // arrivals of each group so far (all barriers)
+  SyncWord rel[kSyncGroups];  // barriers released, per group
+  SyncWord top;               // groups complete so far
+  SyncWord group;             // arrivals of the V water-filling's blocks (their own barriers)
+  SyncWord abort;             // nonzero: a block gave up waiting, nobody waits any more
+  SyncWord done;              // blocks finished (the last one records a timeout in the plan status)
+};
+static_assert(sizeof(GridSync) == (2 * kSyncGroups + 4) * 128, "one line per word");
 
 struct FusedArgs {
   // inputs (never written by the launch)
@@ -47,11 +60,11 @@ struct FusedArgs {
   const void* v;
   int batch, N, h_kv, W, Np;
   Slopes sl;
-  // water-filling: instances, units per instance, budgets, blocks per instance
+  // water-filling: instances, units per instance, budgets, blocks per V instance
   int n_inst_v, n_inst_k;
   int64_t units_v, units_k;
   long long budget_v, budget_k;
-  int per_v, per_k;
+  int per_v;
   // allocation outputs
   uint8_t* bits_tok;
   float* sigma_chan;
@@ -65,7 +78,6 @@ struct FusedArgs {
   GridSync* sync;
   int32_t* status;  // [2]: V and K water-filling status
   unsigned long long* hist_v;  // [4][n_inst_v][256]
-  unsigned long long* hist_k;  // [4][n_inst_k][256]
   float *part1, *part2, *pmin, *pmax, *mean;
   int* pcnt;
   int nchunk;   // 256-token chunks of the channel passes
@@ -84,35 +96,33 @@ struct FusedArgs {
   long long wait_cycles;                       // bound of one barrier wait
 };
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+// Polls are relaxed loads (an acquire load on every poll would also discard the polling SM's L1,
+// which the blocks still working on that SM use); the fence after the last poll makes the acquire.
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
   unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
-// Every thread of every block calls it.  The block's writes so far become visible to every block
-// that returns from the same barrier.  The wait is bounded: a block that waits longer than `limit`
-// cycles sets the abort flag, and from then on no block waits; the return value is false once the
-// flag is set.
-__device__ __forceinline__ bool grid_barrier(GridSync* gs, long long limit, int* flag_s) {
+// Barrier of a set of blocks on a counter that only grows (every thread of each of them calls it;
+// thread 0's `target` is the count at which every block of the set has arrived at this barrier).
+// The block's writes so far become visible to every block that returns from the same barrier: one
+// arrival (after a fence), then a poll.  The wait is bounded: a block that waits longer than
+// `limit` cycles sets the abort flag, and from then on no block waits; the return value is false
+// once the flag is set.
+__device__ __forceinline__ bool counter_barrier(GridSync* gs, unsigned* ctr, unsigned target, long long limit,
+                                                int* flag_s) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const unsigned g0 = ld_acquire_gpu(&gs->gen);  // moves only once this block has arrived too
     __threadfence();
-    if (atomicAdd(&gs->count, 1u) == gridDim.x - 1) {
-      atomicExch(&gs->count, 0u);
-      __threadfence();
-      st_release_gpu(&gs->gen, g0 + 1);
-    } else {
+    atomicAdd(ctr, 1u);
+    if (ld_relaxed_gpu(ctr) < target) {
       const long long t0 = clock64();
       unsigned nap = 32;
-      while (ld_acquire_gpu(&gs->gen) == g0) {
-        if (*(volatile int*)&gs->abort || clock64() - t0 > limit) {
-          atomicExch(&gs->abort, 1);
+      while (ld_relaxed_gpu(ctr) < target) {
+        if (*(volatile unsigned*)&gs->abort.v || clock64() - t0 > limit) {
+          atomicExch(&gs->abort.v, 1u);
           ok = 0;
           break;
         }
@@ -121,7 +131,44 @@ __device__ __forceinline__ bool grid_barrier(GridSync* gs, long long limit, int*
       }
     }
     __threadfence();
-    if (*(volatile int*)&gs->abort) ok = 0;
+    if (*(volatile unsigned*)&gs->abort.v) ok = 0;
+    *flag_s = ok;
+  }
+  __syncthreads();
+  return *flag_s != 0;
+}
+// All blocks; bar_k (shared, thread 0's) counts the block's grid barriers so far.  Same visibility
+// and bound as counter_barrier; the arrival goes through the block's group (see GridSync).
+__device__ __forceinline__ bool grid_barrier(GridSync* gs, long long limit, int* flag_s, unsigned* bar_k) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const unsigned k = ++*bar_k, nb = gridDim.x;
+    const unsigned ng = min(nb, (unsigned)kSyncGroups), g = blockIdx.x % ng;
+    const unsigned gsize = nb / ng + (g < nb % ng ? 1u : 0u);
+    __threadfence();
+    if (atomicAdd(&gs->grp[g].v, 1u) == k * gsize - 1) {  // the group's last block
+      __threadfence();
+      if (atomicAdd(&gs->top.v, 1u) == k * ng - 1) {        // the last group: release them all
+        __threadfence();
+        for (unsigned q = 0; q < ng; ++q) atomicMax(&gs->rel[q].v, k);
+      }
+    }
+    if (ld_relaxed_gpu(&gs->rel[g].v) < k) {
+      const long long t0 = clock64();
+      unsigned nap = 32;
+      while (ld_relaxed_gpu(&gs->rel[g].v) < k) {
+        if (*(volatile unsigned*)&gs->abort.v || clock64() - t0 > limit) {
+          atomicExch(&gs->abort.v, 1u);
+          ok = 0;
+          break;
+        }
+        __nanosleep(nap);
+        if (nap < 256) nap *= 2;
+      }
+    }
+    __threadfence();
+    if (*(volatile unsigned*)&gs->abort.v) ok = 0;
     *flag_s = ok;
   }
   __syncthreads();
@@ -130,9 +177,10 @@ __device__ __forceinline__ bool grid_barrier(GridSync* gs, long long limit, int*
 
 // Small shared scratch of the non-pack phases (placed after the tile items' area).
 struct FusedSmall {
-  unsigned long long s[257];
+  unsigned long long s[9];
   uint32_t h[256];
   int best, flag;
+  unsigned bar_k;
   int nk[5], seg_base[4], cnt[4];
   int wtot[4][kFusedThreads / 32];
   int base[4];
@@ -148,24 +196,84 @@ __host__ __device__ constexpr size_t fused_smem_bytes() {
   return fused_small_off<D>() + sizeof(FusedSmall);
 }
 
-// Water-filling of one stage: 4 levels (one barrier each), then the widths.  Instance `inst` of this
-// block (or -1), its part x of `per`; g: the instances' gains; lam: the levels' output.
+// V water-filling: 4 levels, then the widths.  Blocks [0, n_part) hold the instances' shares
+// (instance `inst` of this block, its part x of `per`; inst = -1 elsewhere): after each level they
+// wait for one another only (a block barrier when one block does it all); the caller ends the stage
+// with a grid barrier.  g: the instances' gains; lam: the levels' output.
 __device__ __forceinline__ bool fused_waterfill(const FusedArgs& a, bool ok, int inst, int x, int per, int n_inst,
                                                 const float* g, int64_t units, long long budget,
                                                 unsigned long long* hist, int32_t* status, uint8_t* bits,
                                                 float* lam, FusedSmall& sm) {
+  const unsigned n_part = (unsigned)(n_inst * per);
+  if (inst >= 0) {
+    WfPick st{0u, 0ull};
+#pragma unroll 1
+    for (int level = 0; level < 4; ++level) {
+      unsigned long long* hl = hist + ((int64_t)level * n_inst + inst) * 256;
+      if (ok) wf_hist_part(g + (int64_t)inst * units, units, a.sl, level, st.prefix, x, per, sm.h, hl, status);
+      if (n_part == 1) __syncthreads();
+      else ok = counter_barrier(a.sync, &a.sync->group.v, n_part * (level + 1), a.wait_cycles, &sm.flag) && ok;
+      if (ok) st = wf_pick(__ldcg(hl + threadIdx.x), level, budget, st, sm.s, &sm.best);
+    }
+    if (ok) {
+      if (x == 0 && threadIdx.x == 0) lam[inst] = __uint_as_float(st.prefix);
+      wf_assign_part(g + (int64_t)inst * units, units, a.sl, st.prefix, x, per, bits + (int64_t)inst * units);
+    }
+  }
+  return ok;
+}
+
+// Plan item of a head's K channels: class counts (kept for the records) and the slot table.
+__device__ __forceinline__ void k_part_item(const FusedArgs& a, int head, int D, FusedSmall& sm) {
+  const int tid = threadIdx.x;
+  int16_t* slots = reinterpret_cast<int16_t*>(a.plan + a.slots_off) + (int64_t)head * a.slot_stride;
+  for (int i = tid; i < a.slot_stride; i += blockDim.x) slots[i] = -1;
+  for (int c = tid; c < D; c += blockDim.x) sm.bcs[c] = a.bits_chan[(int64_t)head * D + c];
+  if (tid < 5) sm.nk[tid] = 0;
+  __syncthreads();
+  plan_count_k(sm.bcs, D, sm.nk);
+  __syncthreads();
+  if (tid == 0) {
+    const int v0[4] = {0, 0, 0, 0}, k5[5] = {sm.nk[0], sm.nk[1], sm.nk[2], sm.nk[3], sm.nk[4]};
+    (void)make_head_record(v0, k5, D, sm.seg_base);
+    for (int i = 0; i < 5; ++i) a.nk[head * 8 + i] = k5[i];
+  }
+  __syncthreads();
+  plan_slot_table(sm.bcs, D, sm.seg_base, slots);
+  __syncthreads();
+}
+
+// K stage item of a head (see the kernel).
+__device__ __forceinline__ void k_head_item(const FusedArgs& a, int head, int D, float* lam_k, FusedSmall& sm) {
+  const int hpi = a.batch * a.h_kv / a.n_inst_k;  // heads of an instance
+  const int inst = head / hpi, j = head % hpi;
+  const float* g = a.g_chan + (int64_t)inst * a.units_k;
   WfPick st{0u, 0ull};
+#pragma unroll 1
   for (int level = 0; level < 4; ++level) {
-    unsigned long long* hl = hist + ((int64_t)level * n_inst + (inst < 0 ? 0 : inst)) * 256;
-    if (ok && inst >= 0) wf_hist_part(g + (int64_t)inst * units, units, a.sl, level, st.prefix, x, per, sm.h, hl, status);
-    ok = grid_barrier(a.sync, a.wait_cycles, &sm.flag) && ok;
-    if (ok && inst >= 0) st = wf_pick(__ldcg(hl + threadIdx.x), level, budget, st, sm.s, &sm.best);
+    wf_hist_part(g, a.units_k, a.sl, level, st.prefix, 0, 1, sm.h, nullptr, a.status + 1);
+    st = wf_pick(sm.h[threadIdx.x], level, a.budget_k, st, sm.s, &sm.best);
   }
-  if (ok && inst >= 0) {
-    if (x == 0 && threadIdx.x == 0) lam[inst] = __uint_as_float(st.prefix);
-    wf_assign_part(g + (int64_t)inst * units, units, a.sl, st.prefix, x, per, bits + (int64_t)inst * units);
-  }
-  return grid_barrier(a.sync, a.wait_cycles, &sm.flag) && ok;
+  if (j == 0 && threadIdx.x == 0) lam_k[inst] = __uint_as_float(st.prefix);
+  // this head's D channels are units [j D, (j + 1) D) of its instance
+  wf_assign_part(g + (int64_t)j * D, D, a.sl, st.prefix, 0, 1, a.bits_chan + (int64_t)head * D);
+  __syncthreads();
+  k_part_item(a, head, D, sm);
+}
+
+// Plan item (head, chunk c of 8192 tokens): the chunk's V class counts.
+__device__ __forceinline__ void count_item(const FusedArgs& a, int head, int c, FusedSmall& sm) {
+  const int tid = threadIdx.x;
+  if (tid < 4) sm.cnt[tid] = 0;
+  __syncthreads();
+  int cnt[4] = {0, 0, 0, 0};
+  const int t0 = c * kIdxChunk, t1 = min(a.Np, t0 + kIdxChunk);
+  count_classes(a.bits_tok + (int64_t)head * a.Np, t0, t1, blockDim.x, tid, cnt);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) atomicAdd(&sm.cnt[q], cnt[q]);
+  __syncthreads();
+  if (tid < 4) a.ccnt[((int64_t)head * a.nidx + c) * 4 + tid] = sm.cnt[tid];
+  __syncthreads();
 }
 
 // Index item (head, chunk c): the chunk's kept tokens at their class's slots, in position order,
@@ -206,10 +314,28 @@ __device__ __forceinline__ void index_item(const FusedArgs& a, int head, int c, 
   int cnt[4] = {0, 0, 0, 0};
   uint32_t cls_bits[2] = {0u, 0u};  // 2-bit class code of each token (class 0..3; width 0 marked apart)
   uint32_t kept = 0;                // bit e: token t0 + e is kept
+  // the 32 widths: two 16-byte loads when the run is whole and aligned, else one byte at a time
+  uint32_t wv[8];
+  if (t0 + 32 <= a.Np && ((uintptr_t)(bt + t0) & 15) == 0) {
+    const uint4 x0 = __ldcg(reinterpret_cast<const uint4*>(bt + t0));
+    const uint4 x1 = __ldcg(reinterpret_cast<const uint4*>(bt + t0) + 1);
+    wv[0] = x0.x; wv[1] = x0.y; wv[2] = x0.z; wv[3] = x0.w;
+    wv[4] = x1.x; wv[5] = x1.y; wv[6] = x1.z; wv[7] = x1.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        const int t = t0 + 4 * i + f;
+        x |= (t < a.Np ? (uint32_t)bt[t] : 0u) << (8 * f);
+      }
+      wv[i] = x;
+    }
+  }
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
-    const int t = t0 + e;
-    const int b = t < a.Np ? bt[t] : 0;
+    const int b = (int)((wv[e >> 2] >> (8 * (e & 3))) & 255u);
     const int cl = b == 2 ? 0 : b == 4 ? 1 : b == 8 ? 2 : b == 16 ? 3 : -1;
     if (cl >= 0) {
       kept |= 1u << e;
@@ -247,13 +373,17 @@ __device__ __forceinline__ void index_item(const FusedArgs& a, int head, int c, 
     }
   }
   int32_t* out = a.index_map + hp->slot_off;
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    if (kept >> e & 1u) {
-      const int cl = (int)((cls_bits[e >> 4] >> (2 * (e & 15))) & 3u);
-      const int pos = cl == 0 ? excl[0]++ : cl == 1 ? excl[1]++ : cl == 2 ? excl[2]++ : excl[3]++;
-      out[start[cl] + pos] = t0 + e;
-    }
+  // each class's next slot, kept in four scalars (no indexed local array); the kept tokens in
+  // position order, one loop trip each
+  int n0 = start[0] + excl[0], n1 = start[1] + excl[1], n2 = start[2] + excl[2], n3 = start[3] + excl[3];
+#pragma unroll 1
+  while (kept) {
+    const int e = __ffs(kept) - 1;
+    kept &= kept - 1u;
+    const uint32_t cb = e < 16 ? cls_bits[0] : cls_bits[1];
+    const int cl = (int)((cb >> (2 * (e & 15))) & 3u);
+    const int pos = cl == 0 ? n0++ : cl == 1 ? n1++ : cl == 2 ? n2++ : n3++;
+    out[pos] = t0 + e;
   }
   if (c == 0) {
 #pragma unroll
@@ -274,6 +404,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSm) compress_ker
   float* lam = reinterpret_cast<float*>(a.plan + a.lambda_off);
   float2* kstat = reinterpret_cast<float2*>(a.plan + a.kstat_off);
   const long long lim = a.wait_cycles;
+  if (tid == 0) sm.bar_k = 0;
   bool ok = true;
 
   // ---------------------------------------------------------------- step 2: V tokens
@@ -281,25 +412,31 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSm) compress_ker
     const bool mine = bid < a.n_inst_v * a.per_v;
     ok = fused_waterfill(a, ok, mine ? bid / a.per_v : -1, mine ? bid % a.per_v : 0, a.per_v, a.n_inst_v, a.g_tok,
                          a.units_v, a.budget_v, a.hist_v, a.status, a.bits_tok, lam, sm);
+    ok = grid_barrier(a.sync, lim, &sm.flag, &sm.bar_k) && ok;
   }
   // ---------------------------------------------------------------- step 3: K channel spreads, gains
   if (a.Np > 0) {
     const int dt = sizeof(T) == 2 ? RDKV_F16 : RDKV_F32;
+    // the first channel pass and the plan's V class counts (both need only the V widths)
     if (ok)
-      for (int it = bid; it < a.nchunk * n_heads; it += nb)
-        chan_pass_item(it % a.nchunk, a.nchunk, it / a.nchunk, a.k, a.bits_tok, dt, a.N, a.h_kv, D, a.Np, nullptr,
-                       a.part1, a.pcnt, a.pmin, a.pmax, csm);
-    ok = grid_barrier(a.sync, lim, &sm.flag) && ok;
+      for (int it = bid; it < a.nchunk * n_heads + n_heads * a.nidx; it += nb) {
+        if (it < a.nchunk * n_heads)
+          chan_pass_item(it % a.nchunk, a.nchunk, it / a.nchunk, a.k, a.bits_tok, dt, a.N, a.h_kv, D, a.Np, nullptr,
+                         a.part1, a.pcnt, a.pmin, a.pmax, csm);
+        else
+          count_item(a, (it - a.nchunk * n_heads) / a.nidx, (it - a.nchunk * n_heads) % a.nidx, sm);
+      }
+    ok = grid_barrier(a.sync, lim, &sm.flag, &sm.bar_k) && ok;
     if (ok)
       for (int it = bid; it < n_heads * (D / 32); it += nb)
         chan_finish_item(it / (D / 32), it % (D / 32), a.part1, a.pcnt, a.nchunk, D, a.mean, nullptr, nullptr,
                          nullptr, a.pmin, a.pmax, kstat, fsm);
-    ok = grid_barrier(a.sync, lim, &sm.flag) && ok;
+    ok = grid_barrier(a.sync, lim, &sm.flag, &sm.bar_k) && ok;
     if (ok)
       for (int it = bid; it < a.nchunk * n_heads; it += nb)
         chan_pass_item(it % a.nchunk, a.nchunk, it / a.nchunk, a.k, a.bits_tok, dt, a.N, a.h_kv, D, a.Np, a.mean,
                        a.part2, nullptr, nullptr, nullptr, csm);
-    ok = grid_barrier(a.sync, lim, &sm.flag) && ok;
+    ok = grid_barrier(a.sync, lim, &sm.flag, &sm.bar_k) && ok;
     if (ok)
       for (int it = bid; it < n_heads * (D / 32); it += nb)
         chan_finish_item(it / (D / 32), it % (D / 32), a.part2, a.pcnt, a.nchunk, D, nullptr, a.w_chan, a.sigma_chan,
@@ -311,47 +448,14 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSm) compress_ker
       kstat[i] = make_float2(0.f, 0.f);
     }
   }
-  ok = grid_barrier(a.sync, lim, &sm.flag) && ok;
-  {
-    const bool mine = bid < a.n_inst_k * a.per_k;
-    ok = fused_waterfill(a, ok, mine ? bid / a.per_k : -1, mine ? bid % a.per_k : 0, a.per_k, a.n_inst_k, a.g_chan,
-                         a.units_k, a.budget_k, a.hist_k, a.status + 1, a.bits_chan, lam + a.n_inst_v, sm);
-  }
-  // ---------------------------------------------------------------- plan: K classes and slot tables, V class counts
-  if (ok) {
-    for (int it = bid; it < n_heads + n_heads * a.nidx; it += nb) {
-      if (it < n_heads) {
-        const int head = it;
-        int16_t* slots = reinterpret_cast<int16_t*>(a.plan + a.slots_off) + (int64_t)head * a.slot_stride;
-        for (int i = tid; i < a.slot_stride; i += blockDim.x) slots[i] = -1;
-        for (int c = tid; c < D; c += blockDim.x) sm.bcs[c] = a.bits_chan[(int64_t)head * D + c];
-        if (tid < 5) sm.nk[tid] = 0;
-        __syncthreads();
-        plan_count_k(sm.bcs, D, sm.nk);
-        __syncthreads();
-        if (tid == 0) {
-          const int v0[4] = {0, 0, 0, 0}, k5[5] = {sm.nk[0], sm.nk[1], sm.nk[2], sm.nk[3], sm.nk[4]};
-          (void)make_head_record(v0, k5, D, sm.seg_base);
-          for (int i = 0; i < 5; ++i) a.nk[head * 8 + i] = k5[i];
-        }
-        __syncthreads();
-        plan_slot_table(sm.bcs, D, sm.seg_base, slots);
-      } else {
-        const int head = (it - n_heads) / a.nidx, c = (it - n_heads) % a.nidx;
-        if (tid < 4) sm.cnt[tid] = 0;
-        __syncthreads();
-        int cnt[4] = {0, 0, 0, 0};
-        const int t0 = c * kIdxChunk, t1 = min(a.Np, t0 + kIdxChunk);
-        count_classes(a.bits_tok + (int64_t)head * a.Np, t0, t1, blockDim.x, tid, cnt);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) atomicAdd(&sm.cnt[q], cnt[q]);
-        __syncthreads();
-        if (tid < 4) a.ccnt[((int64_t)head * a.nidx + c) * 4 + tid] = sm.cnt[tid];
-      }
-      __syncthreads();
-    }
-  }
-  ok = grid_barrier(a.sync, lim, &sm.flag) && ok;
+  ok = grid_barrier(a.sync, lim, &sm.flag, &sm.bar_k) && ok;
+  // K water level, widths and plan items, one item per head: the item's block runs the water-filling
+  // of the head's instance (at most h_kv D units) by itself, from histograms in shared memory (every
+  // block of an instance finds the same level: the digits are exact integer sums), then writes its
+  // head's widths (and, for the instance's first head, the level) and the head's K plan items
+  if (ok)
+    for (int it = bid; it < n_heads; it += nb) k_head_item(a, it, D, lam + a.n_inst_v, sm);
+  ok = grid_barrier(a.sync, lim, &sm.flag, &sm.bar_k) && ok;
   // ---------------------------------------------------------------- plan: records and offsets (block 0); window
   if (ok) {
     if (bid == 0) {
@@ -385,7 +489,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSm) compress_ker
                   i0, step);
     }
   }
-  ok = grid_barrier(a.sync, lim, &sm.flag) && ok;
+  ok = grid_barrier(a.sync, lim, &sm.flag, &sm.bar_k) && ok;
   const rdkv_plan_header* hdr = plan_header(a.plan);
   const bool fits = ok && __ldcg(&hdr->status) != RDKV_ERR_CAPACITY;
   // ---------------------------------------------------------------- index map, head K metadata
@@ -395,7 +499,7 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSm) compress_ker
       else head_meta_body(it - n_heads * a.nidx, a.plan, kstat, D, a.zone_a, a.a_pages);
     }
   }
-  ok = grid_barrier(a.sync, lim, &sm.flag) && ok;
+  ok = grid_barrier(a.sync, lim, &sm.flag, &sm.bar_k) && ok;
   // ---------------------------------------------------------------- tiles
   if (fits && ok && a.Np > 0) {
     const int64_t n_tiles = __ldcg(reinterpret_cast<const long long*>(&hdr->index_slots)) / kTile;
@@ -408,17 +512,17 @@ __global__ void __launch_bounds__(kFusedThreads, kFusedBlocksPerSm) compress_ker
   if (tid == 0) {
     if (bid == 0 && ok) *a.len_dev = a.W;
     __threadfence();
-    if (atomicAdd(&a.sync->done, 1u) == (unsigned)nb - 1) {
+    if (atomicAdd(&a.sync->done.v, 1u) == (unsigned)nb - 1) {
       __threadfence();
-      if (*(volatile int*)&a.sync->abort) reinterpret_cast<rdkv_plan_header*>(a.plan)->status = RDKV_ERR_TIMEOUT;
+      if (*(volatile unsigned*)&a.sync->abort.v) reinterpret_cast<rdkv_plan_header*>(a.plan)->status = RDKV_ERR_TIMEOUT;
     }
   }
 }
 
-// Workspace: barrier state and status words, the histograms (these are cleared per call), then the
+// Workspace: barrier state and status words, the V histograms (these are cleared per call), then the
 // channel partials, counts and means, the index chunks' counts and the K class counts.
 struct FusedWs {
-  size_t sync, hist_v, hist_k, part, cnt, mean, ccnt, nk, total, clear;
+  size_t sync, hist_v, part, cnt, mean, ccnt, nk, total, clear;
   int nchunk, nidx, n_inst_v, n_inst_k;
 };
 static FusedWs fused_ws(const rdkv_shape* s, int per_head) {
@@ -431,11 +535,9 @@ static FusedWs fused_ws(const rdkv_shape* s, int per_head) {
   w.nidx = ceil_div(Np, kIdxChunk);
   size_t o = 0;
   w.sync = o;
-  o += 256;
+  o += sizeof(GridSync) + 256;  // then the status words, on a line of their own
   w.hist_v = o;
   o += align_up(4 * (int64_t)w.n_inst_v * 256 * 8, 256);
-  w.hist_k = o;
-  o += align_up(4 * (int64_t)w.n_inst_k * 256 * 8, 256);
   w.clear = o;
   w.part = o;
   o += 4 * align_up(n_heads * w.nchunk * D * 4, 256);  // part1, part2, pmin, pmax
@@ -539,8 +641,8 @@ extern "C" rdkv_status rdkv_allocate_pack(rdkv_cache* cache, int32_t per_head, c
   a.units_k = per_head ? (int64_t)D : (int64_t)s->h_kv * D;
   a.budget_v = (long long)std::floor((double)avg_bits_v * (double)a.units_v);
   a.budget_k = (long long)std::floor((double)avg_bits_k * (double)a.units_k);
-  a.per_v = nb / a.n_inst_v;
-  a.per_k = nb / a.n_inst_k;
+  // blocks per V instance: about 16 units a thread, as the stage kernels take them
+  a.per_v = (int)std::min<int64_t>(std::max<int64_t>(ceil_div64(a.units_v, 256 * 16), 1), nb / a.n_inst_v);
   a.bits_tok = bits_tok;
   a.sigma_chan = sigma_chan;
   a.g_chan = g_chan;
@@ -552,9 +654,8 @@ extern "C" rdkv_status rdkv_allocate_pack(rdkv_cache* cache, int32_t per_head, c
   a.kstat_off = L.kstat_off;
   a.slot_stride = L.slot_stride;
   a.sync = reinterpret_cast<GridSync*>(wsb + w.sync);
-  a.status = reinterpret_cast<int32_t*>(wsb + w.sync + 64);
+  a.status = reinterpret_cast<int32_t*>(wsb + w.sync + sizeof(GridSync));
   a.hist_v = reinterpret_cast<unsigned long long*>(wsb + w.hist_v);
-  a.hist_k = reinterpret_cast<unsigned long long*>(wsb + w.hist_k);
   const size_t pb = align_up(n_heads * w.nchunk * D * 4, 256);
   a.part1 = reinterpret_cast<float*>(wsb + w.part);
   a.part2 = reinterpret_cast<float*>(wsb + w.part + pb);

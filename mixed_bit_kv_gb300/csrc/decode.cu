@@ -1011,10 +1011,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC == kConsumersWide ? 1 : 2)
       }
       const int rec = st_item[sidx];
       if (rec == kItemEnd) break;
-      if (*(volatile int*)&abort_s) {
-        ok = false;
-        break;
-      }
       const unsigned char* stp = wring + st_pos[sidx];
       const int cls = (rec >> 24) - 1, ti = rec & 0xffffff;  // ti: tile of the class, or zone-C block
       if (cls >= 0) {

@@ -47,8 +47,9 @@ struct WfPick {
 // Level `level` histogram of one block's share of an instance: units u = x 256 + t, stepping by
 // nx 256 (t the thread, 256 threads), of the gains g[0, n_units).  Every breakpoint fl32(g s_k)
 // whose bits above this level's byte match `prefix` adds its upgrade's bits to bin (pattern >> shift)
-// & 255; the block's bins go to hist[256] with one atomic each.  h: 256 words of shared memory.
-// Invalid gains (NaN, infinite, negative) set *status at level 0 and buy nothing.
+// & 255 of h (256 words of shared memory); then, unless hist is null (a block that covers the whole
+// instance keeps its bins in h), the block's bins go to hist[256] with one atomic each.  Invalid
+// gains (NaN, infinite, negative) set *status at level 0 and buy nothing.
 __device__ __forceinline__ void wf_hist_part(const float* g, int64_t n_units, Slopes sl, int level, uint32_t prefix,
                                              int x, int nx, uint32_t* h, unsigned long long* hist,
                                              int32_t* status) {
@@ -56,49 +57,56 @@ __device__ __forceinline__ void wf_hist_part(const float* g, int64_t n_units, Sl
   __syncthreads();
   const int shift = 24 - 8 * level;
   bool bad = false;
+  // lanes that hit the same bin add once, their count times the upgrade's bits (most gains of an
+  // instance share a few bins at the first levels)
   for (int64_t u = (int64_t)x * blockDim.x + threadIdx.x; u < n_units; u += (int64_t)nx * blockDim.x) {
     const float gv = g[u];
-    if (!gain_valid(gv)) {
-      bad = true;
-      continue;
-    }
+    const bool valid = gain_valid(gv);
+    bad |= !valid;
+    const unsigned active = __activemask();
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t p = level_bits(gv * sl.s[k]);
-      if (level == 0 || (p >> (shift + 8)) == (prefix >> (shift + 8))) atomicAdd(&h[(p >> shift) & 255u], step_bits(k));
+      const bool in = valid && (level == 0 || (p >> (shift + 8)) == (prefix >> (shift + 8)));
+      const uint32_t bin = in ? (p >> shift) & 255u : 256u;
+      const unsigned same = __match_any_sync(active, bin);
+      if (in && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&h[bin], step_bits(k) * __popc(same));
     }
   }
   if (bad && level == 0 && status) atomicExch(status, (int32_t)RDKV_ERR_INVALID_ARG);
   __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x)
-    if (h[i]) atomicAdd(&hist[i], (unsigned long long)h[i]);
+  if (hist)
+    for (int i = threadIdx.x; i < 256; i += blockDim.x)
+      if (h[i]) atomicAdd(&hist[i], (unsigned long long)h[i]);
 }
 
 // The digit of level `level` (256 threads, thread t holding v = the level's bin t): the smallest d
 // whose upper tail (bins > d) still fits the budget with the bits already above, i.e. the level is
-// prefix | d << shift | (lower bits all ones).  Every thread returns the new state.  s: 257 64-bit
-// words of shared memory, best: one int.
+// prefix | d << shift | (lower bits all ones).  Every thread returns the new state.  The tails are
+// integer sums (exact in any order): suffix sums inside each warp by shuffles, then the totals of
+// the warps above.  s: 9 64-bit words of shared memory, best: one int.
 __device__ __forceinline__ WfPick wf_pick(unsigned long long v, int level, long long budget, WfPick cur,
                                           unsigned long long* s, int* best) {
-  const int t = threadIdx.x;
-  s[255 - t] = v;  // reversed so that an inclusive scan gives sums over d' >= t
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  unsigned long long x = v;  // sum over this warp's bins d' >= t
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  if (lane == 0) s[w] = x;
   if (t == 0) *best = 255;
   __syncthreads();
-  for (int off = 1; off < 256; off <<= 1) {
-    const unsigned long long x = (255 - t >= off) ? s[255 - t - off] : 0ull;
-    __syncthreads();
-    s[255 - t] += x;
-    __syncthreads();
-  }
-  const unsigned long long tail = s[255 - t] - v;  // sum over d' > t
+  for (int w2 = w + 1; w2 < 8; ++w2) x += s[w2];
+  const unsigned long long tail = x - v;  // sum over d' > t
   if (cur.above + tail <= (unsigned long long)budget) atomicMin(best, t);
   __syncthreads();
   const int d = *best;
-  if (t == d) s[256] = tail;
+  if (t == d) s[8] = tail;
   __syncthreads();
   WfPick nxt;
   nxt.prefix = cur.prefix | ((uint32_t)d << (24 - 8 * level));
-  nxt.above = cur.above + s[256];
+  nxt.above = cur.above + s[8];
   __syncthreads();  // s is free again
   return nxt;
 }
@@ -180,7 +188,7 @@ __device__ __forceinline__ void chan_pass_item(int chunk, int nchunk, int head, 
   int cnt = 0;
   const int64_t row = (int64_t)h_kv * D;
   const int64_t base = (((int64_t)b * N) * h_kv + j) * D + c0;
-#pragma unroll 4
+#pragma unroll 8
   for (int t = t0 + w; t < t1; t += kChanWarps) {
     const bool keep = __ldcg(bt + t) != 0;
     float x[4];
@@ -229,40 +237,59 @@ struct ChanFinishSmem {
   float smin[kChanRows][32], smax[kChanRows][32];
 };
 
-// Item (head, 32-channel slice) of the chunk combine, 256 threads: thread (r, l) sums the chunks
-// r, r + 8, r + 16, ... of channel 32 slice + l in fp64, in order (loads eight chunks at a time,
-// all in flight together); row 0 then adds rows 1..7 in order.  The first call (mean_out set) also
-// combines the chunks' minima and maximum into the head's K channel statistics kstat[head][c] =
-// {min, max} over the kept tokens ({0, 0} when none is kept); the second writes sigma and the gain
-// fl32(w_chan * sigma).
+// Item (head, 32-channel slice) of the chunk combine, 256 threads: thread (r, l) takes the chunks
+// r, r + 8, r + 16, ... of channel 32 slice + l, eight at a time (all loads in flight together): the
+// e-th of each eight goes to fp64 accumulator e mod 4 (four independent chains), and the four
+// accumulators are added in order at the end; row 0 then adds rows 1..7 in order.  The first call
+// (mean_out set) also combines the chunks' minima and maxima into the head's K channel statistics
+// kstat[head][c] = {min, max} over the kept tokens ({0, 0} when none is kept); the second writes
+// sigma and the gain fl32(w_chan * sigma).
 __device__ __forceinline__ void chan_finish_item(int head, int slice, const float* part, const int* part_cnt,
                                                  int nchunk, int D, float* mean_out, const float* w_chan,
                                                  float* sigma_out, float* g_out, const float* pmin, const float* pmax,
                                                  float2* kstat, ChanFinishSmem& sm) {
   const int l = threadIdx.x & 31, r = threadIdx.x >> 5, c = 32 * slice + l;
   constexpr int kBatch = 8;
-  double s = 0.0;
+  constexpr int kAcc = 4;
+  double acc[kAcc];
+#pragma unroll
+  for (int e = 0; e < kAcc; ++e) acc[e] = 0.0;
   long long n = 0;
   float lo = INFINITY, hi = -INFINITY;
   const int64_t hb = (int64_t)head * nchunk;
   for (int i0 = r; i0 < nchunk; i0 += kChanRows * kBatch) {
-    float ps[kBatch], pl[kBatch], ph[kBatch];
+    float ps[kBatch];
     int pc[kBatch];
 #pragma unroll
     for (int e = 0; e < kBatch; ++e) {
       const int i = i0 + kChanRows * e;
-      const bool in = i < nchunk;
-      ps[e] = in ? __ldcg(part + (hb + i) * D + c) : 0.f;
-      pc[e] = in ? __ldcg(part_cnt + hb + i) : 0;
-      pl[e] = in && kstat ? __ldcg(pmin + (hb + i) * D + c) : INFINITY;
-      ph[e] = in && kstat ? __ldcg(pmax + (hb + i) * D + c) : -INFINITY;
+      ps[e] = i < nchunk ? __ldcg(part + (hb + i) * D + c) : 0.f;
+      pc[e] = i < nchunk ? __ldcg(part_cnt + hb + i) : 0;
     }
 #pragma unroll
     for (int e = 0; e < kBatch; ++e) {
-      if (i0 + kChanRows * e < nchunk) s += (double)ps[e];
+      if (i0 + kChanRows * e < nchunk) acc[e % kAcc] += (double)ps[e];
       n += pc[e];
-      lo = fminf(lo, pl[e]);
-      hi = fmaxf(hi, ph[e]);
+    }
+  }
+  double s = acc[0];
+#pragma unroll
+  for (int e = 1; e < kAcc; ++e) s += acc[e];
+  if (kstat) {
+    constexpr int kMB = 8;
+    for (int i0 = r; i0 < nchunk; i0 += kChanRows * kMB) {
+      float pl[kMB], ph[kMB];
+#pragma unroll
+      for (int e = 0; e < kMB; ++e) {
+        const int i = i0 + kChanRows * e;
+        pl[e] = i < nchunk ? __ldcg(pmin + (hb + i) * D + c) : INFINITY;
+        ph[e] = i < nchunk ? __ldcg(pmax + (hb + i) * D + c) : -INFINITY;
+      }
+#pragma unroll
+      for (int e = 0; e < kMB; ++e) {
+        lo = fminf(lo, pl[e]);
+        hi = fmaxf(hi, ph[e]);
+      }
     }
   }
   sm.ssum[r][l] = s;

@@ -31,7 +31,7 @@
 namespace rdkv {
 
 constexpr int kFusedThreads = 256;
-constexpr int kFusedBlocksPerSm = 5;   // by the tile items' shared memory (about 40 KB a block)
+constexpr int kFusedBlocksPerSm = 5;   // by the tile items' shared memory (about 42 KB a block)
 constexpr int kIdxChunk = 8192;        // tokens of a counting / index item: 32 per thread
 
 // Grid barrier state (workspace, cleared before every launch).  Each word has a 128-byte line of its
@@ -96,8 +96,8 @@ struct FusedArgs {
   long long wait_cycles;                       // bound of one barrier wait
 };
 
-// Polls are relaxed loads (an acquire load on every poll would also discard the polling SM's L1,
-// which the blocks still working on that SM use); the fence after the last poll makes the acquire.
+// Polls are relaxed loads; the fence after the last poll makes the acquire (one per barrier, not
+// one per poll).
 __device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

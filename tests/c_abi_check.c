@@ -30,6 +30,11 @@ int main(void) {
          (long long)b.index_slots, (int)b.n_heads);
   expect(b.zone_a_bytes > 0 && b.index_slots > 0 && b.n_heads == 8, "bound values");
 
+  const size_t ws_ap = rdkv_allocate_pack_workspace_bytes(&s, 0);
+  printf("ws_allocate_pack %zu\n", ws_ap);
+  expect(ws_ap > 0 && rdkv_allocate_pack_workspace_bytes(&s, 1) >= ws_ap, "allocate+pack workspace query");
+  expect(rdkv_allocate_pack_workspace_bytes(&s, 2) == 0, "allocate+pack scope checked");
+
   rdkv_shape bad = s;
   bad.head_dim = 96;
   const rdkv_status st = rdkv_zone_bounds(&bad, 2.5f, 2.5f, &b);

@@ -34,3 +34,4 @@ def test_c_program_links_and_calls_the_library(tmp_path):
     assert L.rdkv_zone_bounds(ctypes.byref(s), ctypes.c_float(2.5), ctypes.c_float(2.5), ctypes.byref(b)) == 0
     assert int(got["bound_zone_a"]) == b.zone_a_bytes
     assert int(got["bad_head_dim_status"]) == rdkv.RDKV_ERR_UNSUPPORTED
+    assert int(got["ws_allocate_pack"]) == L.rdkv_allocate_pack_workspace_bytes(ctypes.byref(s), 0)

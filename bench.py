@@ -178,6 +178,11 @@ def scorer_flops(w):
     return 2 * 2 * w.head_dim * w.h_q * w.batch * w.n_tokens * (w.n_tokens + 1) / 2
 
 
+def scorer_exps(w):
+    """The scorer's second ceiling: one base-2 exponential per causal pair in each of the two passes."""
+    return 2 * w.h_q * w.batch * w.n_tokens * (w.n_tokens + 1) / 2
+
+
 def median(xs):
     return float(statistics.median(xs))
 
@@ -352,6 +357,10 @@ def run_ours(args, ws, rank, local):
                       "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                       "frac": round(score_tflops / ws / peaks["bf16_tflops_sustained"], 4),
                       "traffic": (t1 + t2) if (t1 and t2) else None, "flops_per_launch_pair": scorer_flops(w),
+                      "exp2_per_launch_pair": scorer_exps(w),
+                      "exp2_per_s": round(score_tflops / ws * 1e12 * scorer_exps(w) / scorer_flops(w), 1),
+                      "exp2_note": "the SFU's share of its peak is an ncu counter (XU pipe active 57-61 %, "
+                                   "profiles/score_kernel_llama3b_layer.md)",
                       "kernel": "rdkv::tc::score_kernel (passes 1 and 2)",
                       "peak_source": f"{peaks['source']} bf16 dense sustained (fp16 nominal rate equal)",
                       "time_share": round(score_frac_time, 3)}
